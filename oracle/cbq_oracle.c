@@ -1,0 +1,284 @@
+/*
+ * cbq_oracle.c -- plain, slow CPU oracle for the codebook-4bit matvec.
+ *
+ * TEST INFRASTRUCTURE ONLY (see cbq_oracle.h): loaded by the tests, the
+ * smoke check and the benchmark's CPU-baseline leg, never by the product.
+ *
+ * Compiled with -ffp-contract=off and without fast-math so that every fp32
+ * and fp64 operation below is one correctly rounded IEEE operation, on x86-64
+ * and on aarch64 alike.  Loops follow the definitions in the header, one
+ * element at a time; nothing is blocked, fused or reordered.
+ */
+#include "cbq_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* The 16 int8 levels of the 4-bit codebook, in index order. */
+const int8_t oracle_codebook[16] = {
+    -127, -104, -83, -65, -49, -35, -22, -10,
+       1,   13,  25,  38,  53,  69,  89, 113,
+};
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * exponent 0 -> subnormal: fraction * 2^-24; exponent 31 -> inf/NaN;
+ * otherwise (1024 + fraction) * 2^(exponent - 25). */
+float oracle_half_to_float(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int expo = (h >> 10) & 0x1f;
+    const int frac = h & 0x3ff;
+    double mag;
+    if (expo == 0) {
+        mag = ldexp((double)frac, -24);
+    } else if (expo == 31) {
+        mag = frac ? NAN : INFINITY;
+    } else {
+        mag = ldexp((double)(1024 + frac), expo - 25);
+    }
+    return (float)(sign ? -mag : mag);
+}
+
+static uint16_t block_scale_bits(const uint8_t *blk)
+{
+    return (uint16_t)(blk[0] | (blk[1] << 8));
+}
+
+int oracle_block_index(const uint8_t *blk, int i)
+{
+    const uint8_t *qs = blk + 2;
+    if (i < 16) return qs[i] & 0x0f;
+    return qs[i - 16] >> 4;
+}
+
+void oracle_dequantize_block(const uint8_t *blk, double out[32])
+{
+    const double dw = (double)oracle_half_to_float(block_scale_bits(blk));
+    for (int i = 0; i < ORACLE_QK; ++i)
+        out[i] = dw * (double)oracle_codebook[oracle_block_index(blk, i)];
+}
+
+void oracle_quantize_act(const float *x, int64_t K, int n, int8_t *qx, float *dx)
+{
+    const int64_t nb = K / ORACLE_QK;
+    for (int c = 0; c < n; ++c) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float *xb = x + (int64_t)c * K + b * ORACLE_QK;
+            int8_t *qb = qx + (int64_t)c * K + b * ORACLE_QK;
+            float amax = 0.0f;
+            for (int i = 0; i < ORACLE_QK; ++i) {
+                const float ax = fabsf(xb[i]);
+                if (ax > amax) amax = ax;
+            }
+            const float d = amax / 127.0f;
+            dx[(int64_t)c * nb + b] = d;
+            for (int i = 0; i < ORACLE_QK; ++i) {
+                if (d == 0.0f) {
+                    qb[i] = 0;
+                    continue;
+                }
+                float q = rintf(xb[i] / d);
+                if (q > 127.0f) q = 127.0f;
+                if (q < -127.0f) q = -127.0f;
+                qb[i] = (int8_t)q;
+            }
+        }
+    }
+}
+
+static int32_t block_dot(const uint8_t *blk, const int8_t *qxb)
+{
+    int32_t s = 0;
+    for (int i = 0; i < ORACLE_QK; ++i)
+        s += (int32_t)oracle_codebook[oracle_block_index(blk, i)] * (int32_t)qxb[i];
+    return s;
+}
+
+void oracle_block_dots(const uint8_t *W, int64_t M, int64_t K,
+                       const int8_t *qx, int n, int32_t *s)
+{
+    const int64_t nb = K / ORACLE_QK;
+    for (int c = 0; c < n; ++c)
+        for (int64_t r = 0; r < M; ++r)
+            for (int64_t b = 0; b < nb; ++b)
+                s[((int64_t)c * M + r) * nb + b] =
+                    block_dot(W + (r * nb + b) * ORACLE_BLOCK_BYTES,
+                              qx + (int64_t)c * K + b * ORACLE_QK);
+}
+
+/* One output: sum over blocks of dw * dx * s, fp64. */
+static double row_dot(const uint8_t *Wrow, int64_t nb, const int8_t *qxc, const float *dxc)
+{
+    double acc = 0.0;
+    for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t *blk = Wrow + b * ORACLE_BLOCK_BYTES;
+        const double dw = (double)oracle_half_to_float(block_scale_bits(blk));
+        const double s = (double)block_dot(blk, qxc + b * ORACLE_QK);
+        acc += dw * (double)dxc[b] * s;
+    }
+    return acc;
+}
+
+/* One tolerance base: sum_i |w_i * xhat_i|. */
+static double row_bound(const uint8_t *Wrow, int64_t nb, const int8_t *qxc, const float *dxc)
+{
+    double acc = 0.0;
+    double w[ORACLE_QK];
+    for (int64_t b = 0; b < nb; ++b) {
+        oracle_dequantize_block(Wrow + b * ORACLE_BLOCK_BYTES, w);
+        for (int i = 0; i < ORACLE_QK; ++i)
+            acc += fabs(w[i] * ((double)qxc[b * ORACLE_QK + i] * (double)dxc[b]));
+    }
+    return acc;
+}
+
+void oracle_matvec_q(const uint8_t *W, int64_t M, int64_t K,
+                     const int8_t *qx, const float *dx, int n, double *y)
+{
+    const int64_t nb = K / ORACLE_QK;
+    for (int c = 0; c < n; ++c)
+        for (int64_t r = 0; r < M; ++r)
+            y[(int64_t)c * M + r] = row_dot(W + r * nb * ORACLE_BLOCK_BYTES, nb,
+                                            qx + (int64_t)c * K, dx + (int64_t)c * nb);
+}
+
+void oracle_matvec_q_rows(const uint8_t *W, int64_t M, int64_t K,
+                          const int8_t *qx, const float *dx, int n,
+                          const int64_t *rows, int64_t nrows, double *y)
+{
+    const int64_t nb = K / ORACLE_QK;
+    (void)M;
+    for (int c = 0; c < n; ++c)
+        for (int64_t i = 0; i < nrows; ++i)
+            y[(int64_t)c * nrows + i] = row_dot(W + rows[i] * nb * ORACLE_BLOCK_BYTES, nb,
+                                                qx + (int64_t)c * K, dx + (int64_t)c * nb);
+}
+
+void oracle_matvec(const uint8_t *W, int64_t M, int64_t K,
+                   const float *x, int n, double *y)
+{
+    const int64_t nb = K / ORACLE_QK;
+    int8_t *qx = (int8_t *)malloc((size_t)(n * K));
+    float *dx = (float *)malloc((size_t)(n * nb) * sizeof(float));
+    oracle_quantize_act(x, K, n, qx, dx);
+    oracle_matvec_q(W, M, K, qx, dx, n, y);
+    free(qx);
+    free(dx);
+}
+
+void oracle_matvec_bound(const uint8_t *W, int64_t M, int64_t K,
+                         const int8_t *qx, const float *dx, int n, double *bound)
+{
+    const int64_t nb = K / ORACLE_QK;
+    for (int c = 0; c < n; ++c)
+        for (int64_t r = 0; r < M; ++r)
+            bound[(int64_t)c * M + r] = row_bound(W + r * nb * ORACLE_BLOCK_BYTES, nb,
+                                                  qx + (int64_t)c * K, dx + (int64_t)c * nb);
+}
+
+void oracle_matvec_bound_rows(const uint8_t *W, int64_t M, int64_t K,
+                              const int8_t *qx, const float *dx, int n,
+                              const int64_t *rows, int64_t nrows, double *bound)
+{
+    const int64_t nb = K / ORACLE_QK;
+    (void)M;
+    for (int c = 0; c < n; ++c)
+        for (int64_t i = 0; i < nrows; ++i)
+            bound[(int64_t)c * nrows + i] = row_bound(W + rows[i] * nb * ORACLE_BLOCK_BYTES, nb,
+                                                      qx + (int64_t)c * K, dx + (int64_t)c * nb);
+}
+
+double oracle_silu(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+int oracle_moe(const uint8_t *gate_up, const uint8_t *down, int E, int64_t H, int64_t F,
+               const float *h, int n_tok, const int32_t *ids, const float *wts, int k,
+               int swiglu, double *y, float *a_out, int8_t *qa_out, float *da_out)
+{
+    const int64_t nbH = H / ORACLE_QK;
+    const int64_t nbF = F / ORACLE_QK;
+    const size_t gu_bytes = (size_t)(2 * F * nbH * ORACLE_BLOCK_BYTES);
+    const size_t dn_bytes = (size_t)(H * nbF * ORACLE_BLOCK_BYTES);
+    int8_t *qh = (int8_t *)malloc((size_t)H);
+    float *dh = (float *)malloc((size_t)nbH * sizeof(float));
+    float *a = (float *)malloc((size_t)F * sizeof(float));
+    int8_t *qa = (int8_t *)malloc((size_t)F);
+    float *da = (float *)malloc((size_t)nbF * sizeof(float));
+    int bad = 0;
+
+    for (int t = 0; t < n_tok; ++t) {
+        double *yt = y + (int64_t)t * H;
+        for (int64_t r = 0; r < H; ++r) yt[r] = 0.0;
+        oracle_quantize_act(h + (int64_t)t * H, H, 1, qh, dh);
+        for (int j = 0; j < k; ++j) {
+            const int p = t * k + j;
+            const int32_t e = ids[p];
+            if (e < 0 || e >= E) {
+                ++bad;
+                if (a_out) memset(a_out + (int64_t)p * F, 0, (size_t)F * sizeof(float));
+                if (qa_out) memset(qa_out + (int64_t)p * F, 0, (size_t)F);
+                if (da_out) memset(da_out + (int64_t)p * nbF, 0, (size_t)nbF * sizeof(float));
+                continue;
+            }
+            const uint8_t *gu = gate_up + (size_t)e * gu_bytes;
+            const uint8_t *dn = down + (size_t)e * dn_bytes;
+            for (int64_t r = 0; r < F; ++r) {
+                const double g = row_dot(gu + r * nbH * ORACLE_BLOCK_BYTES, nbH, qh, dh);
+                const double u = row_dot(gu + (F + r) * nbH * ORACLE_BLOCK_BYTES, nbH, qh, dh);
+                a[r] = (float)(swiglu ? oracle_silu(g) * u : g * u);
+            }
+            oracle_quantize_act(a, F, 1, qa, da);
+            if (a_out) memcpy(a_out + (int64_t)p * F, a, (size_t)F * sizeof(float));
+            if (qa_out) memcpy(qa_out + (int64_t)p * F, qa, (size_t)F);
+            if (da_out) memcpy(da_out + (int64_t)p * nbF, da, (size_t)nbF * sizeof(float));
+            const double wj = (double)wts[p];
+            for (int64_t r = 0; r < H; ++r)
+                yt[r] += wj * row_dot(dn + r * nbF * ORACLE_BLOCK_BYTES, nbF, qa, da);
+        }
+    }
+    free(qh);
+    free(dh);
+    free(a);
+    free(qa);
+    free(da);
+    return bad;
+}
+
+int oracle_moe_down_combine(const uint8_t *down, int E, int64_t H, int64_t F,
+                            int n_tok, const int32_t *ids, const float *wts, int k,
+                            const int8_t *qa, const float *da,
+                            double *y, double *ybound)
+{
+    const int64_t nbF = F / ORACLE_QK;
+    const size_t dn_bytes = (size_t)(H * nbF * ORACLE_BLOCK_BYTES);
+    int bad = 0;
+    for (int t = 0; t < n_tok; ++t) {
+        double *yt = y + (int64_t)t * H;
+        double *bt = ybound + (int64_t)t * H;
+        for (int64_t r = 0; r < H; ++r) {
+            yt[r] = 0.0;
+            bt[r] = 0.0;
+        }
+        for (int j = 0; j < k; ++j) {
+            const int p = t * k + j;
+            const int32_t e = ids[p];
+            if (e < 0 || e >= E) {
+                ++bad;
+                continue;
+            }
+            const uint8_t *dn = down + (size_t)e * dn_bytes;
+            const int8_t *qap = qa + (int64_t)p * F;
+            const float *dap = da + (int64_t)p * nbF;
+            const double wj = (double)wts[p];
+            for (int64_t r = 0; r < H; ++r) {
+                const uint8_t *row = dn + r * nbF * ORACLE_BLOCK_BYTES;
+                yt[r] += wj * row_dot(row, nbF, qap, dap);
+                bt[r] += fabs(wj) * row_bound(row, nbF, qap, dap);
+            }
+        }
+    }
+    return bad;
+}

@@ -1,0 +1,424 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself.
+
+Every test here runs on the CPU.  The pins are hand-worked fixtures
+(tests/golden), exact-rational properties, numpy library routines (fp16
+decoding, fp64 matmul) and invariants of the mathematics (linearity, sign
+symmetry, zero scales, closed forms, the silu odd-part identity, the k=1
+reduction of the routed-expert FFN).  Each one is chosen so that a plausible
+slip in the oracle (a dropped factor, a swapped nibble, a wrong tie rule, a
+gate/up swap, a misindexed router weight) fails at least one of them.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from verify_matvec_gb300 import synth
+
+QK = 32
+
+
+# ---------------------------------------------------------------- fixtures --
+
+def _read_codebook(golden_dir):
+    with open(os.path.join(golden_dir, "codebook.txt")) as f:
+        vals = [ln for ln in f if ln.strip() and not ln.startswith("#")]
+    return np.array([int(v) for v in vals[0].split()], dtype=np.int8)
+
+
+def _read_quant_cases(golden_dir):
+    cases, cur = [], {}
+    with open(os.path.join(golden_dir, "quantize_blocks.txt")) as f:
+        for ln in f:
+            if ln.startswith("#") or not ln.strip():
+                continue
+            key, val = ln.split(":", 1)
+            cur[key] = val.split()
+            if key == "q":
+                cases.append(cur)
+                cur = {}
+    return cases
+
+
+def _read_block_cases(golden_dir):
+    blocks = []
+    with open(os.path.join(golden_dir, "block_dots.txt")) as f:
+        for ln in f:
+            if ln.startswith("#") or not ln.strip():
+                continue
+            parts = ln.split()
+            if parts[0] == "block":
+                bits = int(parts[2], 16)
+                qs = [int(b, 16) for b in parts[3:]]
+                assert len(qs) == 16
+                blk = np.array([bits & 0xFF, bits >> 8] + qs, dtype=np.uint8)
+                blocks.append({"name": parts[1], "blk": blk, "dots": []})
+            elif parts[0] == "w":
+                blocks[-1]["w"] = np.array([float(v) for v in parts[1:]])
+            elif parts[0] == "dot":
+                eq = parts.index("=")
+                qx = np.array([int(v) for v in parts[1:eq]], dtype=np.int8)
+                blocks[-1]["dots"].append((qx, int(parts[eq + 1])))
+    return blocks
+
+
+def _np_dequant(W, M, K):
+    """Independent fp64 dequantization with numpy bit operations."""
+    cb = O.CODEBOOK.astype(np.float64)
+    Wb = np.asarray(W, dtype=np.uint8).reshape(M, K // QK, 18)
+    scale = Wb[:, :, 0:2].copy().view(np.float16)[:, :, 0].astype(np.float64)
+    qs = Wb[:, :, 2:]
+    idx = np.concatenate([qs & 0x0F, qs >> 4], axis=2)
+    return (scale[:, :, None] * cb[idx]).reshape(M, K)
+
+
+# ------------------------------------------------------------- codebook ----
+
+def test_codebook_matches_fixture(golden_dir):
+    cb = _read_codebook(golden_dir)
+    assert cb.tolist() == O.CODEBOOK.tolist()
+    assert int(cb.astype(np.int64).sum()) == -94
+    for i in range(16):
+        blk = np.zeros(18, dtype=np.uint8)
+        blk[0:2] = [0x00, 0x3C]  # scale 1.0
+        blk[2:] = i | (i << 4)
+        np.testing.assert_array_equal(O.dequantize_block(blk), np.full(32, float(cb[i])))
+
+
+def test_half_to_float_every_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([O.half_to_float(int(b)) for b in bits], dtype=np.float32)
+    nan = np.isnan(ref)
+    np.testing.assert_array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+# --------------------------------------------------------- quantization ----
+
+def test_quantize_golden_blocks(golden_dir):
+    for case in _read_quant_cases(golden_dir):
+        x = np.array([float(v) for v in case["x"]], dtype=np.float32)
+        q, d = O.quantize_act(x)
+        assert q.tolist() == [int(v) for v in case["q"]]
+        if case["d"][0] != "None":
+            assert float(d[0]) == float(case["d"][0])
+
+
+def test_quantize_golden_blocks_as_columns_and_rows(golden_dir):
+    cases = _read_quant_cases(golden_dir)
+    X = np.array([[float(v) for v in c["x"]] for c in cases], dtype=np.float32)
+    Q = np.array([[int(v) for v in c["q"]] for c in cases], dtype=np.int8)
+    q_cols, _ = O.quantize_act(X)                   # n columns of one block
+    np.testing.assert_array_equal(q_cols, Q)
+    q_row, d_row = O.quantize_act(X.reshape(1, -1))  # one column of n blocks
+    np.testing.assert_array_equal(q_row.reshape(Q.shape), Q)
+    assert d_row.shape == (1, len(cases))
+
+
+def _exact_checks(x, q, d):
+    """q is the nearest integer to x/d up to the fp32 rounding of the quotient,
+    d is fl32(amax/127), and exact half-integer quotients round to even."""
+    amax = Fraction(float(np.max(np.abs(x))))
+    d_exact = amax / 127
+    df = Fraction(float(d))
+    if amax == 0:
+        assert df == 0 and not np.any(q)
+        return
+    ulp = Fraction(float(np.spacing(np.float32(d))))
+    assert abs(df - d_exact) <= ulp / 2
+    for xi, qi in zip(x.tolist(), q.tolist()):
+        r = Fraction(xi) / df
+        assert abs(r - qi) <= Fraction(1, 2) + abs(r) * Fraction(1, 2 ** 23)
+        if r.denominator == 2:
+            assert qi % 2 == 0
+        assert -127 <= qi <= 127
+
+
+def test_quantize_exact_rational_properties():
+    g = np.random.default_rng(7)
+    for trial in range(200):
+        x = g.standard_normal(32).astype(np.float32) * np.float32(10.0 ** g.integers(-3, 4))
+        if trial % 3 == 0:  # force exact ties: amax = 127 * 2^e so d = 2^e
+            e = int(g.integers(-6, 6))
+            x = (g.integers(-254, 255, 32) / 2.0 * 2.0 ** e).astype(np.float32)
+            x[g.integers(0, 32)] = np.float32(127 * 2.0 ** e)
+        q, d = O.quantize_act(x)
+        _exact_checks(x, q, d[0])
+
+
+def test_quantize_sign_symmetry_and_power_of_two_scaling():
+    x = synth.activations(3, 256, stream=77, outliers=True)
+    q, d = O.quantize_act(x)
+    qn, dn = O.quantize_act(-x)
+    np.testing.assert_array_equal(qn, -q)
+    np.testing.assert_array_equal(dn, d)
+    q4, d4 = O.quantize_act(x * np.float32(4.0))
+    np.testing.assert_array_equal(q4, q)
+    np.testing.assert_array_equal(d4, d * np.float32(4.0))
+
+
+def test_quantize_extreme_element_maps_to_127():
+    x = synth.activations(4, 512, stream=78)
+    q, _ = O.quantize_act(x)
+    xb = x.reshape(4, 16, 32)
+    qb = q.reshape(4, 16, 32)
+    am = np.argmax(np.abs(xb), axis=2)
+    top = np.take_along_axis(qb, am[:, :, None], axis=2)[:, :, 0]
+    sign = np.sign(np.take_along_axis(xb, am[:, :, None], axis=2)[:, :, 0])
+    np.testing.assert_array_equal(top, (127 * sign).astype(np.int8))
+
+
+# ---------------------------------------------------- block format / dots --
+
+def test_nibble_layout_one_hot():
+    for p in range(32):
+        for i in (1, 7, 8, 15):
+            blk = np.zeros(18, dtype=np.uint8)
+            blk[0:2] = [0x00, 0x3C]
+            if p < 16:
+                blk[2 + p] = i
+            else:
+                blk[2 + p - 16] = i << 4
+            got = [O.block_index(blk, j) for j in range(32)]
+            want = [i if j == p else 0 for j in range(32)]
+            assert got == want
+            qx = np.zeros(32, dtype=np.int8)
+            qx[p] = 3
+            s = O.block_dots(blk, 1, 32, qx)
+            # every other element has index 0 but meets qx == 0
+            assert int(s[0, 0, 0]) == 3 * int(O.CODEBOOK[i])
+
+
+def test_block_dots_golden(golden_dir):
+    for case in _read_block_cases(golden_dir):
+        np.testing.assert_array_equal(O.dequantize_block(case["blk"]), case["w"])
+        for qx, s in case["dots"]:
+            assert int(O.block_dots(case["blk"], 1, 32, qx)[0, 0, 0]) == s, case["name"]
+
+
+def test_codebook_table_dots():
+    for i in range(16):
+        blk = np.zeros(18, dtype=np.uint8)
+        blk[2:] = i | (i << 4)
+        s = O.block_dots(blk, 1, 32, np.ones(32, dtype=np.int8))
+        assert int(s[0, 0, 0]) == 32 * int(O.CODEBOOK[i])
+
+
+def test_block_dots_brute_force_small():
+    M, K = 3, 96
+    W = synth.weight_blocks(M, K, stream=90)
+    qx = np.random.default_rng(3).integers(-127, 128, size=(2, K)).astype(np.int8)
+    s = O.block_dots(W, M, K, qx)
+    Wd = _np_dequant(W, M, K)
+    scale = W[:, :, 0:2].copy().view(np.float16)[:, :, 0].astype(np.float64)
+    for c in range(2):
+        for r in range(M):
+            for b in range(K // QK):
+                ints = Wd[r, 32 * b:32 * b + 32] / scale[r, b]
+                assert np.all(ints == np.round(ints))
+                assert int(s[c, r, b]) == int(np.dot(ints.astype(np.int64), qx[c, 32 * b:32 * b + 32]))
+
+
+# --------------------------------------------------------------- matvec ----
+
+@pytest.mark.parametrize("M,K,n", [(7, 64, 1), (33, 320, 3), (64, 1024, 5)])
+def test_matvec_equals_dequantize_then_dot(M, K, n):
+    W = synth.weight_blocks(M, K, stream=11)
+    x = synth.activations(n, K, stream=12, outliers=True)
+    qx, dx = O.quantize_act(x)
+    xhat = qx.astype(np.float64) * np.repeat(dx.astype(np.float64), QK, axis=1)
+    ref = xhat @ _np_dequant(W, M, K).T
+    y = O.matvec(W, M, K, x)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-15)
+    np.testing.assert_array_equal(O.matvec_q(W, M, K, qx, dx), y)
+
+
+def test_matvec_scale_linearity_exact():
+    M, K = 40, 256
+    W = synth.weight_blocks(M, K, stream=13)
+    x = synth.activations(2, K, stream=14)
+    y = O.matvec(W, M, K, x)
+    W2 = W.copy()
+    bits = W2[:, :, 0:2].copy().view(np.uint16)
+    W2[:, :, 0:2] = (bits + np.uint16(0x0400)).view(np.uint8)  # exponent + 1: dw * 2
+    np.testing.assert_array_equal(O.matvec(W2, M, K, x), 2.0 * y)
+
+
+def test_matvec_sign_symmetry_exact():
+    M, K = 40, 256
+    W = synth.weight_blocks(M, K, stream=15)
+    x = synth.activations(3, K, stream=16)
+    np.testing.assert_array_equal(O.matvec(W, M, K, -x), -O.matvec(W, M, K, x))
+
+
+def test_matvec_zero_scale_rows():
+    M, K = 16, 128
+    W = synth.weight_blocks(M, K, stream=17)
+    W[5, :, 0:2] = 0        # +0 scale
+    W[9, :, 0:2] = [0, 0x80]  # -0 scale
+    y = O.matvec(W, M, K, synth.activations(2, K, stream=18))
+    assert np.all(y[:, 5] == 0) and np.all(y[:, 9] == 0)
+    assert np.all(y[:, [0, 1, 2, 3]] != 0)
+
+
+def test_matvec_constant_index_closed_form():
+    M, K, i = 4, 192, 13
+    W = synth.weight_blocks(M, K, stream=19)
+    W[:, :, 2:] = i | (i << 4)
+    x = synth.activations(1, K, stream=20)
+    qx, dx = O.quantize_act(x)
+    dw = W[:, :, 0:2].copy().view(np.float16)[:, :, 0].astype(np.float64)
+    qsum = qx.reshape(K // QK, QK).astype(np.int64).sum(axis=1).astype(np.float64)
+    want = float(O.CODEBOOK[i]) * (dw * dx[0].astype(np.float64) * qsum).sum(axis=1)
+    np.testing.assert_allclose(O.matvec(W, M, K, x)[0], want, rtol=1e-13)
+
+
+def test_matvec_rows_subset_and_bound():
+    M, K = 50, 256
+    W = synth.weight_blocks(M, K, stream=21)
+    x = synth.activations(2, K, stream=22, outliers=True)
+    qx, dx = O.quantize_act(x)
+    y = O.matvec_q(W, M, K, qx, dx)
+    rows = np.array([49, 0, 17, 17, 3])
+    np.testing.assert_array_equal(O.matvec_q(W, M, K, qx, dx, rows=rows), y[:, rows])
+    b = O.matvec_bound(W, M, K, qx, dx)
+    assert np.all(b >= np.abs(y))
+    xhat = qx.astype(np.float64) * np.repeat(dx.astype(np.float64), QK, axis=1)
+    np.testing.assert_allclose(b, np.abs(xhat) @ np.abs(_np_dequant(W, M, K)).T, rtol=1e-12)
+    np.testing.assert_array_equal(O.matvec_bound(W, M, K, qx, dx, rows=rows), b[:, rows])
+
+
+# ------------------------------------------------------------------ silu ---
+
+def test_silu_identities():
+    assert O.silu(0.0) == 0.0
+    for z in (0.1, 0.5, 1.0, 3.0, 7.5, 20.0):
+        assert abs((O.silu(z) - O.silu(-z)) - z) <= 1e-15 * max(1.0, z)
+    assert abs(O.silu(40.0) - 40.0) <= 40.0 * 1e-15
+    assert abs(O.silu(-40.0)) <= 1e-15
+    assert abs(O.silu(1.0) - 1.0 / (1.0 + np.exp(-1.0))) <= 1e-16
+
+
+# ------------------------------------------------------------------- MoE ---
+
+E_, H_, F_ = 6, 64, 32
+
+
+@pytest.fixture(scope="module")
+def tiny_layer():
+    gu = synth.expert_blocks(E_, 2 * F_, H_, stream=31)
+    dn = synth.expert_blocks(E_, H_, F_, stream=32)
+    return gu, dn
+
+
+def _expert_slot(gu, dn, e, h, swiglu):
+    """One (token, slot) through the pinned matvec pieces, gate rows first."""
+    qh, dh = O.quantize_act(h)
+    g_rows = gu[e].reshape(2 * F_, -1)
+    g = O.matvec_q(g_rows[:F_].ravel(), F_, H_, qh, dh)[0]
+    u = O.matvec_q(g_rows[F_:].ravel(), F_, H_, qh, dh)[0]
+    if swiglu:
+        a = np.array([O.silu(v) * w for v, w in zip(g, u)]).astype(np.float32)
+    else:
+        a = (g * u).astype(np.float32)
+    qa, da = O.quantize_act(a)
+    return O.matvec_q(dn[e].ravel(), H_, F_, qa, da)[0], a
+
+
+@pytest.mark.parametrize("swiglu", [1, 0])
+def test_moe_k1_reduces_to_matvecs(tiny_layer, swiglu):
+    gu, dn = tiny_layer
+    h = synth.activations(1, H_, stream=33)
+    for e in range(E_):
+        y, a, qa, da, nbad = O.moe(gu, dn, E_, H_, F_, h, np.array([[e]]), np.array([[1.0]]),
+                                   swiglu=swiglu, want_intermediate=True)
+        want, a_want = _expert_slot(gu, dn, e, h[0], swiglu)
+        assert nbad == 0
+        np.testing.assert_array_equal(a[0], a_want)
+        np.testing.assert_array_equal(y[0], want)
+
+
+def test_moe_gate_and_up_are_not_interchangeable(tiny_layer):
+    gu, dn = tiny_layer
+    h = synth.activations(1, H_, stream=34)
+    ids, wts = np.array([[2]]), np.array([[1.0]])
+    y = O.moe(gu, dn, E_, H_, F_, h, ids, wts)
+    sw = gu.copy()
+    rows = sw[2].reshape(2 * F_, -1).copy()
+    sw[2] = np.concatenate([rows[F_:], rows[:F_]]).reshape(sw[2].shape)
+    assert not np.allclose(O.moe(sw, dn, E_, H_, F_, h, ids, wts), y)
+    z = gu.copy()
+    zr = z[2].reshape(2 * F_, H_ // QK, 18)
+    zr[F_:, :, 0:2] = 0  # up half scaled to zero -> a == 0 -> y == 0
+    z[2] = zr.reshape(z[2].shape)
+    assert np.all(O.moe(z, dn, E_, H_, F_, h, ids, wts) == 0)
+
+
+def test_moe_router_weights_and_slots(tiny_layer):
+    gu, dn = tiny_layer
+    h = synth.activations(1, H_, stream=35)
+    ids = np.array([[4, 1]])
+    wts = np.array([[0.75, 0.25]], dtype=np.float32)
+    y = O.moe(gu, dn, E_, H_, F_, h, ids, wts)
+    y4 = O.moe(gu, dn, E_, H_, F_, h, np.array([[4]]), np.array([[1.0]]))
+    y1 = O.moe(gu, dn, E_, H_, F_, h, np.array([[1]]), np.array([[1.0]]))
+    np.testing.assert_allclose(y, 0.75 * y4 + 0.25 * y1, rtol=1e-12, atol=1e-14)
+    # doubling every router weight doubles y exactly
+    np.testing.assert_array_equal(O.moe(gu, dn, E_, H_, F_, h, ids, 2 * wts), 2 * y)
+    # slot order only changes the fp64 summation order
+    np.testing.assert_allclose(O.moe(gu, dn, E_, H_, F_, h, ids[:, ::-1], wts[:, ::-1]), y,
+                               rtol=1e-12, atol=1e-14)
+
+
+def test_moe_tokens_are_independent(tiny_layer):
+    gu, dn = tiny_layer
+    h = synth.activations(5, H_, stream=36)
+    ids, wts = synth.router(5, 3, E_, stream=37)
+    y = O.moe(gu, dn, E_, H_, F_, h, ids, wts)
+    for t in range(5):
+        np.testing.assert_array_equal(O.moe(gu, dn, E_, H_, F_, h[t:t + 1], ids[t:t + 1], wts[t:t + 1])[0], y[t])
+
+
+def test_moe_bad_ids_and_duplicates(tiny_layer):
+    gu, dn = tiny_layer
+    h = synth.activations(1, H_, stream=38)
+    y_ok = O.moe(gu, dn, E_, H_, F_, h, np.array([[3]]), np.array([[0.5]]))
+    y, _, _, _, nbad = O.moe(gu, dn, E_, H_, F_, h, np.array([[3, E_, -1]]),
+                             np.array([[0.5, 0.3, 0.2]]), want_intermediate=True)
+    assert nbad == 2
+    np.testing.assert_array_equal(y, y_ok)
+    y_dup = O.moe(gu, dn, E_, H_, F_, h, np.array([[3, 3]]), np.array([[0.25, 0.25]]))
+    np.testing.assert_allclose(y_dup, y_ok, rtol=1e-12, atol=1e-14)
+
+
+def test_moe_down_combine_matches_full(tiny_layer):
+    gu, dn = tiny_layer
+    h = synth.activations(4, H_, stream=39)
+    ids, wts = synth.router(4, 2, E_, stream=40)
+    y, a, qa, da, _ = O.moe(gu, dn, E_, H_, F_, h, ids, wts, want_intermediate=True)
+    y2, yb, nbad = O.moe_down_combine(dn, E_, H_, F_, ids, wts, qa, da)
+    assert nbad == 0
+    np.testing.assert_array_equal(y2, y)
+    assert np.all(yb >= np.abs(y))
+    qa2, da2 = O.quantize_act(a)
+    np.testing.assert_array_equal(qa2, qa)
+    np.testing.assert_array_equal(da2, da)
+
+
+def test_moe_large_gate_makes_silu_identity(tiny_layer):
+    """Gate rows pushed far positive: silu(g) = g to fp32, so a = g*u."""
+    gu, dn = tiny_layer
+    big = gu.copy()
+    r = big[0].reshape(2 * F_, H_ // QK, 18)
+    r[:F_, :, 2:] = 0xFF                       # every gate index -> codebook max 113
+    r[:F_, :, 0:2] = np.frombuffer(np.float16(0.5).tobytes(), dtype=np.uint8)
+    big[0] = r.reshape(big[0].shape)
+    h = np.abs(synth.activations(1, H_, stream=41))  # positive input -> g >> 0
+    _, a1, _, _, _ = O.moe(big, dn, E_, H_, F_, h, np.array([[0]]), np.array([[1.0]]),
+                           swiglu=1, want_intermediate=True)
+    _, a0, _, _, _ = O.moe(big, dn, E_, H_, F_, h, np.array([[0]]), np.array([[1.0]]),
+                           swiglu=0, want_intermediate=True)
+    np.testing.assert_allclose(a1, a0, rtol=1e-6)
