@@ -1,0 +1,408 @@
+"""Benchmark of the codebook-4bit MoE verify layer on GB300.
+
+One step = the whole hot path over one batch: the routed-expert layer at
+batch 5 with top-8 of 256 experts (H=4096, F=2048; activation quantization,
+gate_up + SwiGLU + requantization, down + weighted combine) plus the
+129280 x 4096 output-head matvec at n = 5.  Weights are resident in HBM;
+every step takes the next of 16 seeded routing tables and inputs.  The
+metric is weight GB/s: the distinct experts' bytes plus the head's bytes,
+read once per step, over the device time of the step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Prints one JSON line (rank 0).  For N > 1 (torchrun) every rank runs an
+independent replica; the value is the bytes of all ranks over the slowest
+rank's time.  `--impl reference` times the CPU oracle on a bounded sample of
+the same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from verify_matvec_gb300 import synth  # noqa: E402
+
+E, H, F = 256, 4096, 2048
+N_TOK, TOPK = 5, 8
+HEAD_M, HEAD_K, HEAD_N = 129280, 4096, 5
+N_SETS = 16
+QK, BB = 32, 18
+EXPERT_BYTES = (2 * F * (H // QK) + H * (F // QK)) * BB        # 14,155,776
+GATE_UP_BYTES = 2 * F * (H // QK) * BB                          # 9,437,184
+DOWN_BYTES = H * (F // QK) * BB                                 # 4,718,592
+HEAD_BYTES = HEAD_M * (HEAD_K // QK) * BB                       # 297,861,120
+METRIC = "4-bit MoE matvec weight GB/s vs GB300 HBM peak; us/layer at batch 1 and 5"
+WORKLOAD = ("MoE verify layer: 5 tokens x top-8 of 256 codebook-4bit experts (gate_up 4096x4096, "
+            "down 4096 rows x 2048) with fused SwiGLU and weighted combine, plus the 129280x4096 "
+            "output head at n=5")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        v = d.get("hbm_gbs")
+        if v:
+            return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def routing_sets(seed_base=synth.S_IDS + 100):
+    sets = []
+    for i in range(N_SETS):
+        ids, wts = synth.router(N_TOK, TOPK, E, stream=seed_base + i)
+        h = synth.activations(N_TOK, H, stream=synth.S_H + 100 + i)
+        x = synth.activations(HEAD_N, HEAD_K, stream=synth.S_HEAD_X + 100 + i)
+        sets.append((ids, wts, h, x))
+    return sets
+
+
+# -------------------------------------------------------------- oracle -----
+
+def oracle_sample(sets, n_steps, per_step_seconds_hint=None):
+    """Time the CPU oracle on a bounded sample of the workload: token 0 of the
+    MoE layer (its 8 slots) plus 1/16 of the head rows at n = 5, per step."""
+    from oracle import oracle as O
+    ids, wts, h, x = sets[0]
+    used = synth.distinct_experts(ids[:1], E)
+    gu = np.zeros((E, 2 * F, H // QK, BB), dtype=np.uint8)
+    dn = np.zeros((E, H, F // QK, BB), dtype=np.uint8)
+    for e in used:
+        gu[e] = synth.weight_blocks(2 * F, H, stream=synth.S_GATE_UP * 1000 + int(e))
+        dn[e] = synth.weight_blocks(H, F, stream=synth.S_DOWN * 1000 + int(e))
+    rows = HEAD_M // 16
+    head = synth.weight_blocks(rows, HEAD_K, stream=synth.S_HEAD)
+    step_bytes = len(used) * EXPERT_BYTES + rows * (HEAD_K // QK) * BB
+    times = []
+    for _ in range(n_steps):
+        t0 = time.perf_counter()
+        O.moe(gu, dn, E, H, F, h[:1], ids[:1], wts[:1], swiglu=1)
+        O.matvec(head, rows, HEAD_K, x)
+        times.append(time.perf_counter() - t0)
+    sample = (f"per step: token 0 of the batch-5 MoE layer ({len(used)} experts, "
+              f"{len(used) * EXPERT_BYTES} B) + {rows} of {HEAD_M} head rows at n=5; single-threaded oracle")
+    return step_bytes, times, sample
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    sets = routing_sets()
+    step_bytes, times, sample = oracle_sample(sets, args.warmup + args.steps)
+    timed = times[args.warmup:]
+    total = sum(timed)
+    value = step_bytes * len(timed) / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(timed),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8xi4-codebook/f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU ------
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self, ident):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(ident), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                p = [v.strip() for v in ln.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_ident(torch, local):
+    """nvidia-smi's name for this rank's GPU: its UUID when torch exposes it."""
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        parts = [p for p in vis.split(",") if p.strip()]
+        return parts[local] if local < len(parts) else local
+
+
+def build_layer(torch, cbq):
+    """All 256 experts drawn from their seeded streams, repacked on device."""
+    gu = np.empty((E, 2 * F, H // QK, BB), dtype=np.uint8)
+    dn = np.empty((E, H, F // QK, BB), dtype=np.uint8)
+    synth.expert_blocks(E, 2 * F, H, stream=synth.S_GATE_UP, out=gu)
+    synth.expert_blocks(E, H, F, stream=synth.S_DOWN, out=dn)
+    L = cbq.Moe(gu, dn, E, H, F)
+    del gu, dn
+    head = cbq.Weights(synth.weight_blocks(HEAD_M, HEAD_K, stream=synth.S_HEAD), HEAD_M, HEAD_K)
+    return L, head
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from verify_matvec_gb300 import build, cbq
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    build.build()  # no-op once built; each rank loads the same in-tree library
+    cbq.load()
+
+    L, head = build_layer(torch, cbq)
+    sets = routing_sets()
+    d_sets = []
+    for ids, wts, h, x in sets:
+        d_sets.append(tuple(torch.from_numpy(a).to(dev) for a in (ids, wts, h, x)))
+    distinct = [len(synth.distinct_experts(s[0], E)) for s in sets]
+    y = torch.empty((N_TOK, H), dtype=torch.float32, device=dev)
+    yh = torch.empty((HEAD_N, HEAD_M), dtype=torch.float32, device=dev)
+    qx = torch.empty((HEAD_N, HEAD_K), dtype=torch.int8, device=dev)
+    dx = torch.empty((HEAD_N, HEAD_K // QK), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    total = args.warmup + args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(total)]
+
+    def step(i, events):
+        ids, wts, h, x = d_sets[i % N_SETS]
+        if events is not None:
+            cbq.cbq_moe_set_stage_events(L, events[0:4])
+        cbq.cbq_moe_matvec(L, h, ids, wts, swiglu=1, y=y)
+        if events is not None:
+            events[4].record(stream)
+        cbq.cbq_quantize_act(x, qx, dx)
+        if events is not None:
+            events[5].record(stream)
+        cbq.cbq_matvec_q(head, qx, dx, y=yh)
+        if events is not None:
+            events[6].record(stream)
+
+    # untimed warm-up
+    for i in range(args.warmup):
+        step(i, ev[i])
+    torch.cuda.synchronize()
+    clocks = Clocks()
+    clocks.start(gpu_ident(torch, local))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.warmup, total):
+        step(i, ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    cbq.cbq_moe_set_stage_events(L, None)
+    ms = t0.elapsed_time(t1)
+
+    timed = range(args.warmup, total)
+    wbytes = [distinct[i % N_SETS] * EXPERT_BYTES + HEAD_BYTES for i in timed]
+    k_gate = [ev[i][1].elapsed_time(ev[i][2]) for i in timed]
+    k_down = [ev[i][2].elapsed_time(ev[i][3]) for i in timed]
+    k_head = [ev[i][5].elapsed_time(ev[i][6]) for i in timed]
+    k_quant = [ev[i][0].elapsed_time(ev[i][1]) + ev[i][4].elapsed_time(ev[i][5]) for i in timed]
+    err = cbq.cbq_get_device_error()
+
+    # per-launch algorithmic bytes: weights + activations read + outputs written
+    act_h = N_TOK * H * (1 + 4 / QK)
+    slots = N_TOK * TOPK
+    gate_alg = [distinct[i % N_SETS] * GATE_UP_BYTES + act_h + slots * F * (1 + 4 / QK) for i in timed]
+    head_alg = HEAD_BYTES + HEAD_N * HEAD_K * (1 + 4 / QK) + 4 * HEAD_N * HEAD_M
+    kern = {"k_moe_gate_up": (sum(k_gate), sum(gate_alg) / len(k_gate)),
+            "k_matvec<5> (head)": (sum(k_head), head_alg)}
+    dom = max(kern, key=lambda k: kern[k][0])
+    dom_ms, dom_bytes = kern[dom][0] / len(timed), kern[dom][1]
+    peak, peak_kind = peaks()
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+
+    # end to end through the host-buffer entry points (pinned host memory)
+    h_sets = []
+    for ids, wts, h, x in sets:
+        h_sets.append(tuple(torch.from_numpy(a).pin_memory().numpy() for a in (ids, wts, h, x)))
+    y_host = torch.empty((N_TOK, H), dtype=torch.float32).pin_memory().numpy()
+    yh_host = torch.empty((HEAD_N, HEAD_M), dtype=torch.float32).pin_memory().numpy()
+
+    def e2e_step(i):
+        ids, wts, h, x = h_sets[i % N_SETS]
+        cbq.cbq_moe_matvec_host(L, h, ids, wts, swiglu=1, y=y_host)
+        cbq.cbq_matvec_host(head, x, y=yh_host)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.warmup, total):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    # microseconds per layer at batch 1 (top-4) and batch 5 (top-8)
+    def layer_us(n_tok, k, reps=50):
+        tabs = []
+        for i in range(N_SETS):
+            ids_i, wts_i = synth.router(n_tok, k, E, stream=synth.S_IDS + 300 + 17 * n_tok + i)
+            tabs.append((torch.from_numpy(ids_i).to(dev), torch.from_numpy(wts_i).to(dev),
+                         torch.from_numpy(synth.activations(n_tok, H, stream=synth.S_H + 300 + i)).to(dev),
+                         len(synth.distinct_experts(ids_i, E))))
+        yl = torch.empty((n_tok, H), dtype=torch.float32, device=dev)
+        for i in range(5):
+            t = tabs[i % N_SETS]
+            cbq.cbq_moe_matvec(L, t[2], t[0], t[1], y=yl)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        nbytes = 0
+        for i in range(reps):
+            t = tabs[i % N_SETS]
+            cbq.cbq_moe_matvec(L, t[2], t[0], t[1], y=yl)
+            nbytes += t[3] * EXPERT_BYTES
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * a.elapsed_time(b) / reps
+        return us, nbytes / reps / (us * 1e-6) / 1e9
+
+    b1_us, b1_gbs = layer_us(1, 4)
+    b5_us, b5_gbs = layer_us(5, 8)
+
+    # slowest rank decides; bytes add up over ranks
+    my = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(my, op=dist.ReduceOp.MAX)
+    ms_max, e2e_max = float(my[0]), float(my[1])
+    total_bytes = sum(wbytes) * world
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+    e2e_value = total_bytes / (e2e_max * 1e-3) / 1e9
+    h2d = N_TOK * H * 4 + 2 * slots * 4 + HEAD_N * HEAD_K * 4
+    d2h = N_TOK * H * 4 + HEAD_N * HEAD_M * 4
+
+    cpu = None
+    if rank == 0 and world == 1:
+        n_cpu = 1
+        _, t1s = oracle_sample(sets, 1)[0:2]
+        n_cpu = max(1, min(20, int(10.0 / max(t1s[0], 1e-3))))
+        step_bytes, times, sample = oracle_sample(sets, n_cpu)
+        cpu = {"value": step_bytes * len(times) / sum(times) / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": f"{n_cpu} repetitions; " + sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "i8xi4-codebook/f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n_tok": N_TOK, "topk": TOPK, "experts": E, "hidden": H,
+                       "ffn": F, "head": [HEAD_M, HEAD_K], "head_cols": HEAD_N,
+                       "distinct_experts_per_step": [distinct[i % N_SETS] for i in timed][:N_SETS],
+                       "weight_bytes_per_step_mean": sum(wbytes) / len(wbytes),
+                       "l2": "inputs larger than L2 (~0.8 GB of weights per step, 16 rotating routing tables)",
+                       "parallelism": f"replicas x{world}"},
+            "us_per_layer": {"batch1_top4": b1_us, "batch5_top8": b5_us,
+                             "batch1_weight_gbs": b1_gbs, "batch5_weight_gbs": b5_gbs},
+            "kernels_ms_per_step": {"quantize(x2)": sum(k_quant) / len(timed),
+                                    "k_moe_gate_up": sum(k_gate) / len(timed),
+                                    "k_moe_down": sum(k_down) / len(timed),
+                                    "k_matvec<5> (head)": sum(k_head) / len(timed)},
+            "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 5 * args.steps,
+            "clocks": clk,
+            "device_error": err,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

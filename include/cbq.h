@@ -1,0 +1,196 @@
+/*
+ * cbq.h -- C ABI of the codebook-4bit quantized matvec library (libcbq.so).
+ *
+ * The library computes the low-bit quantized matrix-vector product that
+ * streams 4-bit codebook weights for single-token decode and for small-batch
+ * speculative verification (n = 1..5 activation columns), over dense
+ * projections and over top-k routed MoE experts with the SwiGLU split and the
+ * router-weighted combine fused in.  Every step runs in CUDA kernels built for
+ * sm_103a; there is no CPU fallback.
+ *
+ * Sources of each operation (pages: the lucebox pull requests about the
+ * DeepSeek-V4-Flash "DS4" server):
+ *   - quant type + CPU reference conversion: "feat(ds4): add DSpark speculative
+ *     runtime + optimizations" #496, summary bullet "ROCmFP4/ROCmFPX quant types
+ *     + CPU reference conversions";
+ *   - MMVQ vecdot / MMVQ kernel over ne1 columns, MMVQ_MAX_MOE_BATCH_SIZE: same
+ *     summary ("CUDA/HIP dequant, copy, getrows, MMVQ vecdot, MMVF ...");
+ *   - codebook-16 expander: "fix(ggml): make ROCmFP4 codebook self-contained on
+ *     CUDA" (commit on "fix(ds4): correct layer-split HC handoff and per-device
+ *     state" #507);
+ *   - SwiGLU split for the fused FFN matvec paths: #496 summary, "DS4 SwiGLU
+ *     split op plumbing";
+ *   - routed-expert top-k and the fused expert-FFN combine: "fix(ds4): keep
+ *     ROCmFPX generation byte-safe" #494 (DFLASH_DS4_FFN_FUSED_COMBINE) and
+ *     "feat(ds4): add DSpark speculative decoding" (configured routed-expert
+ *     top-k, fused batched verification).
+ *
+ * Weight format ("canonical blocks"): a matrix of M rows x K columns
+ * (K % 32 == 0) is M x (K/32) blocks, row-major, 18 bytes per block:
+ *   bytes 0-1  fp16 scale dw, little-endian;
+ *   bytes 2-17 index bytes qs: byte j holds the codebook index of element j
+ *              in its low nibble and of element j+16 in its high nibble;
+ *   weight_i = dw * codebook[index_i], codebook = {-127,-104,-83,-65,-49,-35,
+ *              -22,-10,1,13,25,38,53,69,89,113}.
+ *
+ * Activation quantization (per 32 consecutive values of one column):
+ *   d = max|x| / 127 (fp32), q = round-half-to-even(x / d) clamped to
+ *   [-127,127], q = 0 when d == 0.  Inputs are assumed finite.
+ *
+ * Conventions for every entry point:
+ *   - returns CBQ_OK (0) or a negative cbq_status; argument errors are
+ *     reported before anything is launched;
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream); work is enqueued on it and the call returns without waiting,
+ *     except where a function says it synchronizes;
+ *   - pointers named *_dev are device pointers owned by the caller; the
+ *     library only reads inputs and writes outputs within the stated sizes;
+ *   - a handle owns its device memory (repacked weights and a workspace) and
+ *     remembers its device; calls switch to that device and restore the
+ *     caller's current device before returning;
+ *   - the workspace of a handle is shared by its calls: two calls on one
+ *     handle that overlap on the GPU (different streams without ordering)
+ *     race.  Calls on one stream are ordered and safe;
+ *   - no call allocates or frees memory except *_create / *_destroy.
+ */
+#ifndef CBQ_H
+#define CBQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CBQ_QK 32            /* weights per block */
+#define CBQ_BLOCK_BYTES 18   /* bytes per canonical block */
+#define CBQ_MAX_COLS 5       /* activation columns per matvec (decode + verify q<=4) */
+#define CBQ_MAX_TOKENS 5     /* tokens per MoE call */
+#define CBQ_MAX_TOPK 16      /* routed experts per token */
+
+typedef enum {
+    CBQ_OK = 0,
+    CBQ_EINVAL = -1,   /* bad argument (null pointer, size, count) */
+    CBQ_ECUDA = -2,    /* a CUDA runtime call or a launch failed */
+    CBQ_ENOMEM = -3,   /* device allocation failed in a *_create */
+    CBQ_EDEVICE = -4   /* no usable sm_103 device */
+} cbq_status;
+
+/* Bits of the device error word (cbq_get_device_error). */
+#define CBQ_DEVERR_BAD_EXPERT_ID 0x1u /* an id outside [0,E): that slot was skipped */
+
+typedef struct cbq_weights cbq_weights; /* one dense M x K matrix, repacked on device */
+typedef struct cbq_moe cbq_moe;         /* E experts: gate_up (2F x H) and down (H x F) */
+
+/* Human-readable name of a cbq_status. */
+const char *cbq_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread ("" if none). */
+const char *cbq_last_cuda_error(void);
+
+/* Create a dense weight handle on the current device from canonical blocks
+ * `blocks` (M*(K/32)*18 bytes; host memory if on_device == 0, else device
+ * memory).  The blocks are repacked into the device layout (16-byte index
+ * stream interleaved by 32-row groups plus a separate fp16 scale stream); the
+ * source is not retained.  Synchronizes `stream`.
+ * Errors: EINVAL (null, M < 1, K < 32, K % 32 != 0), ENOMEM, ECUDA, EDEVICE. */
+int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device,
+                       void *stream, cbq_weights **out);
+int cbq_weights_destroy(cbq_weights *W);
+
+/* Shape of a handle and the device bytes it holds (any pointer may be NULL). */
+int cbq_weights_info(const cbq_weights *W, int64_t *M, int64_t *K, int64_t *device_bytes);
+
+/* Activation quantization (pages: activation side of the MMVQ vecdot).
+ * x_dev: n x K fp32, row-major (column c at x_dev + c*K); K % 32 == 0; n >= 1.
+ * qx_dev: n x K int8 out; dx_dev: n x (K/32) fp32 out.
+ * Bit-exact with the rule in the header comment. */
+int cbq_quantize_act(const float *x_dev, int64_t K, int n, int8_t *qx_dev, float *dx_dev,
+                     void *stream);
+
+/* Quantized matvec from already-quantized activations (MMVQ with ne1 = n).
+ * qx_dev: n x K int8, dx_dev: n x (K/32) fp32 (layout of cbq_quantize_act);
+ * y_dev: n x M fp32 out, y[c][r] = sum_b dw(r,b) * dx[c][b] * s(r,b,c) where
+ * s is the exact int32 block dot.  1 <= n <= CBQ_MAX_COLS.  All n columns are
+ * computed in one pass over the weights. */
+int cbq_matvec_q(const cbq_weights *W, const int8_t *qx_dev, const float *dx_dev, int n,
+                 float *y_dev, void *stream);
+
+/* The whole dense path: quantize x_dev (n x K fp32) into the handle's
+ * workspace, then cbq_matvec_q into y_dev (n x M fp32). */
+int cbq_matvec(const cbq_weights *W, const float *x_dev, int n, float *y_dev, void *stream);
+
+/* Same with HOST buffers: copies x (n x K fp32) to the device, runs
+ * cbq_matvec and copies y (n x M fp32) back, then synchronizes `stream`.
+ * Pinned host memory makes the copies asynchronous to the host. */
+int cbq_matvec_host(const cbq_weights *W, const float *x_host, int n, float *y_host,
+                    void *stream);
+
+/* Create an MoE layer handle from canonical blocks of E experts, contiguous
+ * per expert: gate_up = E x (2F rows x H cols), rows 0..F-1 the gate
+ * projection and rows F..2F-1 the up projection; down = E x (H rows x F cols).
+ * H % 32 == 0, F % 32 == 0, E >= 1.  Host memory if on_device == 0.
+ * Synchronizes `stream`.  Errors as cbq_weights_create. */
+int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int64_t F,
+                   int on_device, void *stream, cbq_moe **out);
+int cbq_moe_destroy(cbq_moe *L);
+int cbq_moe_info(const cbq_moe *L, int *E, int64_t *H, int64_t *F, int64_t *device_bytes);
+
+/* Routed-expert FFN (mul_mat_id with the SwiGLU split and the weighted
+ * combine fused).  h_dev: n_tok x H fp32; ids_dev: n_tok x topk int32 expert
+ * ids; wts_dev: n_tok x topk fp32 router weights; y_dev: n_tok x H fp32 out.
+ * For every token t and slot j (slot order), expert e = ids[t][j]:
+ *   g,u = gate/up rows of e applied to quantize(h_t);
+ *   a = swiglu ? silu(g)*u : g*u (fp32), silu(z) = z/(1+exp(-z));
+ *   o = down_e applied to quantize(a);  y_t = sum_j wts[t][j] * o.
+ * Tokens are grouped by expert on the device: each distinct expert's bytes
+ * are read once per call for all of its tokens.  Ids should be distinct per
+ * token; a repeated id is served as an extra column and summed on its own.
+ * An id outside [0,E) skips its slot and sets CBQ_DEVERR_BAD_EXPERT_ID.
+ * 1 <= n_tok <= CBQ_MAX_TOKENS, 1 <= topk <= min(CBQ_MAX_TOPK, E). */
+int cbq_moe_matvec(const cbq_moe *L, const float *h_dev, int n_tok, const int32_t *ids_dev,
+                   const float *wts_dev, int topk, int swiglu, float *y_dev, void *stream);
+
+/* Same with HOST buffers (h, ids, wts in; y out), then synchronizes `stream`. */
+int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok,
+                        const int32_t *ids_host, const float *wts_host, int topk, int swiglu,
+                        float *y_host, void *stream);
+
+/* Stage timing: when set, cbq_moe_matvec records these CUDA events
+ * (cudaEvent_t passed as void*) on its stream before the activation
+ * quantization, before the gate_up kernel, before the down kernel and after
+ * it.  Pass NULL for all four to stop.  The events stay owned by the caller. */
+int cbq_moe_set_stage_events(cbq_moe *L, void *ev_quant, void *ev_gate_up, void *ev_down, void *ev_end);
+
+/* Reads and clears the device error word of the current device (bits
+ * CBQ_DEVERR_*).  Synchronizes the device. */
+int cbq_get_device_error(unsigned int *code);
+
+/* ---- checking entry points (used by the parity tests) ---------------- */
+
+/* Per-block int32 dots s_dev[c][r][b] (n x M x K/32) of W with plain int8
+ * activations qx_dev (n x K), through the same codebook expander and dp4a
+ * sequence as the matvec kernels.  1 <= n <= CBQ_MAX_COLS. */
+int cbq_debug_block_dots(const cbq_weights *W, const int8_t *qx_dev, int n, int32_t *s_dev,
+                         void *stream);
+
+/* Same for expert e of an MoE layer: which = 0 gate_up, 1 down. */
+int cbq_moe_debug_block_dots(const cbq_moe *L, int e, int which, const int8_t *qx_dev, int n,
+                             int32_t *s_dev, void *stream);
+
+/* Keep (1) or stop keeping (0) the fp32 intermediate a of each slot in the
+ * workspace during cbq_moe_matvec (costs 4*F bytes of writes per slot). */
+int cbq_moe_set_debug(cbq_moe *L, int keep_intermediate);
+
+/* Copy the intermediate of the last cbq_moe_matvec on this handle, for
+ * slots p = t*topk + j < nslots: a_dev[p][F] fp32 (needs debug on),
+ * qa_dev[p][F] int8, da_dev[p][F/32] fp32 (any may be NULL).  Slots whose id
+ * was out of range hold stale data. */
+int cbq_moe_debug_intermediate(const cbq_moe *L, int nslots, float *a_dev, int8_t *qa_dev,
+                               float *da_dev, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CBQ_H */

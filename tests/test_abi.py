@@ -1,0 +1,58 @@
+"""The C-ABI library on the CPU: it loads, exports every declared entry point,
+and rejects bad arguments before touching a GPU."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from verify_matvec_gb300 import build, cbq
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return cbq.load()
+
+
+def test_every_header_function_is_exported(lib):
+    names = cbq.header_functions()
+    assert len(names) >= 19
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(cbq._SIGS), "binding and header disagree"
+
+
+def test_status_strings(lib):
+    for st in (0, -1, -2, -3, -4):
+        assert lib.cbq_status_string(st).decode().startswith("CBQ_")
+    assert b"unknown" in lib.cbq_status_string(7)
+
+
+def test_argument_errors_need_no_gpu(lib):
+    P = ctypes.c_void_p
+    dummy = P(16)
+    h = ctypes.c_void_p()
+    EINVAL = cbq.CBQ_EINVAL
+    # bad shapes / null pointers are rejected before any CUDA call
+    assert lib.cbq_weights_create(None, 4, 64, 0, None, ctypes.byref(h)) == EINVAL
+    assert lib.cbq_weights_create(dummy, 4, 48, 0, None, ctypes.byref(h)) == EINVAL
+    assert lib.cbq_weights_create(dummy, 0, 64, 0, None, ctypes.byref(h)) == EINVAL
+    assert lib.cbq_weights_create(dummy, 4, 64, 0, None, None) == EINVAL
+    assert lib.cbq_quantize_act(None, 64, 1, dummy, dummy, None) == EINVAL
+    assert lib.cbq_quantize_act(dummy, 40, 1, dummy, dummy, None) == EINVAL
+    assert lib.cbq_quantize_act(dummy, 64, 0, dummy, dummy, None) == EINVAL
+    assert lib.cbq_matvec(None, dummy, 1, dummy, None) == EINVAL
+    assert lib.cbq_matvec_q(None, dummy, dummy, 1, dummy, None) == EINVAL
+    assert lib.cbq_moe_create(dummy, dummy, 0, 64, 64, 0, None, ctypes.byref(h)) == EINVAL
+    assert lib.cbq_moe_create(dummy, dummy, 4, 60, 64, 0, None, ctypes.byref(h)) == EINVAL
+    assert lib.cbq_moe_matvec(None, dummy, 1, dummy, dummy, 1, 1, dummy, None) == EINVAL
+    assert lib.cbq_weights_destroy(None) == EINVAL
+    assert lib.cbq_moe_destroy(None) == EINVAL
+    assert lib.cbq_get_device_error(None) == EINVAL
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(cbq, "_lib", None)
+    monkeypatch.setattr(cbq, "LIB_PATH", str(tmp_path / "libcbq.so"))
+    with pytest.raises(ImportError):
+        cbq.load()

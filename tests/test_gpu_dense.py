@@ -1,0 +1,157 @@
+"""Dense path on the GPU (through the C ABI) against the CPU oracle.
+
+Bit-exact: activation quantization and every per-block int32 dot.  Within
+1e-4 * sum_i |w_i * xhat_i| per output: the fp32 matvec.  Exact on the GPU
+too: doubling every scale doubles y, negating x negates y, a zero scale gives
+a zero row.
+"""
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from tests.gpu_util import assert_within_bound, cuda
+from verify_matvec_gb300 import cbq, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return cuda()
+
+
+def _dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+# --------------------------------------------------------- quantization ---
+
+@pytest.mark.parametrize("n,K,outliers", [(1, 1024, False), (1, 4096, True), (5, 4096, False),
+                                          (3, 2048, True), (2, 32, False), (5, 96, True)])
+def test_quantize_bit_exact(torch, n, K, outliers):
+    x = synth.activations(n, K, stream=101 + K + n, outliers=outliers)
+    x[0, :32] = 0.0                         # an all-zero block
+    x[-1, 32 * (K // 64):32 * (K // 64) + 32] = 3.0  # a constant block
+    qx, dx = cbq.cbq_quantize_act(_dev(torch, x))
+    qr, dr = O.quantize_act(x)
+    np.testing.assert_array_equal(qx.cpu().numpy(), qr)
+    np.testing.assert_array_equal(dx.cpu().numpy().view(np.uint32), dr.view(np.uint32))
+
+
+def test_quantize_golden_ties(torch, golden_dir):
+    from tests.test_oracle import _read_quant_cases
+    cases = _read_quant_cases(golden_dir)
+    X = np.array([[float(v) for v in c["x"]] for c in cases], dtype=np.float32)
+    qx, _ = cbq.cbq_quantize_act(_dev(torch, X))
+    np.testing.assert_array_equal(qx.cpu().numpy(), np.array([[int(v) for v in c["q"]] for c in cases]))
+
+
+# ------------------------------------------------------------ block dots ---
+
+@pytest.mark.parametrize("M,K", [(256, 1024), (70, 160), (33, 32), (1, 96), (130, 4096)])
+@pytest.mark.parametrize("n", [1, 2, 3, 5])
+def test_block_dots_bit_exact(torch, M, K, n):
+    W = synth.weight_blocks(M, K, stream=201 + M)
+    Wh = cbq.Weights(W, M, K)
+    qx = np.random.default_rng(M * 7 + n).integers(-127, 128, size=(n, K)).astype(np.int8)
+    qx[0, :32] = 127
+    s = cbq.cbq_debug_block_dots(Wh, _dev(torch, qx)).cpu().numpy()
+    np.testing.assert_array_equal(s, O.block_dots(W, M, K, qx))
+
+
+def test_block_dots_every_codebook_entry(torch):
+    M, K = 32, 512
+    W = np.zeros((M, K // 32, 18), dtype=np.uint8)
+    for r in range(M):
+        W[r, :, 2:] = (r % 16) | ((15 - r % 16) << 4)
+    Wh = cbq.Weights(W, M, K)
+    qx = np.ones((4, K), dtype=np.int8)
+    qx[1] = -1
+    qx[2, ::2] = 127
+    qx[3] = np.random.default_rng(5).integers(-127, 128, size=K)
+    s = cbq.cbq_debug_block_dots(Wh, _dev(torch, qx)).cpu().numpy()
+    np.testing.assert_array_equal(s, O.block_dots(W, M, K, qx))
+
+
+# ---------------------------------------------------------------- matvec ---
+
+def _check_matvec(torch, W, M, K, x, rows=None):
+    Wh = cbq.Weights(W, M, K)
+    y = cbq.cbq_matvec(Wh, _dev(torch, x)).cpu().numpy()
+    qx, dx = O.quantize_act(x)
+    yr = O.matvec_q(W, M, K, qx, dx, rows=rows)
+    b = O.matvec_bound(W, M, K, qx, dx, rows=rows)
+    assert_within_bound(y if rows is None else y[:, rows], yr, b)
+    return Wh, y
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_matvec_tiny_config(torch, n):
+    M, K = 256, 1024
+    W = synth.weight_blocks(M, K, stream=synth.S_W)
+    _check_matvec(torch, W, M, K, synth.activations(n, K, stream=synth.S_X))
+
+
+@pytest.mark.parametrize("M,K", [(70, 160), (33, 32), (1, 4096), (100, 2080)])
+@pytest.mark.parametrize("n", [1, 3, 5])
+def test_matvec_ragged(torch, M, K, n):
+    W = synth.weight_blocks(M, K, stream=301 + M + K)
+    _check_matvec(torch, W, M, K, synth.activations(n, K, stream=302, outliers=True))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_matvec_4096_full(torch, n):
+    M = K = 4096
+    W = synth.weight_blocks(M, K, stream=synth.S_W)
+    _check_matvec(torch, W, M, K, synth.activations(n, K, stream=synth.S_X + n, outliers=(n == 1)))
+
+
+@pytest.mark.parametrize("n", [1, 5])
+def test_matvec_16384_sampled(torch, n):
+    M, K = 16384, 4096
+    W = synth.weight_blocks(M, K, stream=synth.S_W + 50)
+    rows = np.unique(np.concatenate([np.arange(0, 40), np.arange(M - 40, M),
+                                     np.random.default_rng(1).integers(0, M, 400)]))
+    _check_matvec(torch, W, M, K, synth.activations(n, K, stream=synth.S_X + 50, outliers=True), rows=rows)
+
+
+def test_matvec_q_equals_matvec_and_host_entry(torch):
+    M, K, n = 300, 1024, 4
+    W = synth.weight_blocks(M, K, stream=401)
+    x = synth.activations(n, K, stream=402)
+    Wh = cbq.Weights(W, M, K)
+    y = cbq.cbq_matvec(Wh, _dev(torch, x)).cpu().numpy()
+    qx, dx = cbq.cbq_quantize_act(_dev(torch, x))
+    yq = cbq.cbq_matvec_q(Wh, qx, dx).cpu().numpy()
+    np.testing.assert_array_equal(yq, y)
+    yh = cbq.cbq_matvec_host(Wh, x)
+    np.testing.assert_array_equal(yh, y)
+
+
+def test_matvec_exact_invariants(torch):
+    M, K, n = 200, 2048, 5
+    W = synth.weight_blocks(M, K, stream=501)
+    W[7, :, 0:2] = 0
+    x = synth.activations(n, K, stream=502)
+    Wh = cbq.Weights(W, M, K)
+    y = cbq.cbq_matvec(Wh, _dev(torch, x)).cpu().numpy()
+    assert np.all(y[:, 7] == 0)
+    yn = cbq.cbq_matvec(Wh, _dev(torch, -x)).cpu().numpy()
+    np.testing.assert_array_equal(yn, -y)
+    W2 = W.copy()
+    bits = W2[:, :, 0:2].copy().view(np.uint16)
+    nz = bits != 0
+    bits[nz] += np.uint16(0x0400)
+    W2[:, :, 0:2] = bits.view(np.uint8)
+    y2 = cbq.cbq_matvec(cbq.Weights(W2, M, K), _dev(torch, x)).cpu().numpy()
+    np.testing.assert_array_equal(y2, 2 * y)
+
+
+def test_output_head_sampled_bench_shape(torch):
+    """The 129280 x 4096 head at n = 5, launched as the benchmark launches it."""
+    M, K, n = 129280, 4096, 5
+    W = synth.weight_blocks(M, K, stream=synth.S_HEAD)
+    x = synth.activations(n, K, stream=synth.S_HEAD_X)
+    rows = np.unique(np.concatenate([np.arange(0, 32), np.arange(M - 64, M),
+                                     np.random.default_rng(2).integers(0, M, 300)]))
+    _check_matvec(torch, W, M, K, x, rows=rows)

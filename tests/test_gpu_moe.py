@@ -1,0 +1,182 @@
+"""Routed-expert path (gate_up + SwiGLU + requant, down + combine) on the GPU
+against the CPU oracle, stage by stage and end to end.
+
+Stage 1: the fp32 intermediate a of every (token, slot) within the bound
+propagated from the gate/up tolerance.  Requantization: (qa, da) bit-exact
+with the oracle's quantization of the GPU's own a.  Stage 2: y within
+1e-4 * sum_j |r_j| * sum_i |wd_i * ahat_i| of the oracle's down+combine fed
+the GPU's own (qa, da).  End to end: y against the oracle's own a, with the
+extra term sum_j |r_j| sum_i |wd_i| |ahat_gpu - ahat_ref| for requantization
+flips near rounding ties.
+"""
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from tests.gpu_util import TOL, assert_within_bound, cuda
+from tests.test_oracle import _np_dequant
+from verify_matvec_gb300 import cbq, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return cuda()
+
+
+def _dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, swiglu, expect_bad=0):
+    n_tok, k = ids.shape
+    cbq.cbq_moe_set_debug(L, True)
+    y = cbq.cbq_moe_matvec(L, _dev(torch, h), _dev(torch, ids), _dev(torch, wts), swiglu=swiglu).cpu().numpy()
+    a_g, qa_g, da_g = (t.cpu().numpy() for t in cbq.cbq_moe_debug_intermediate(L, n_tok * k))
+    err = cbq.cbq_get_device_error()
+    assert err == (cbq.CBQ_DEVERR_BAD_EXPERT_ID if expect_bad else 0)
+    valid = ((ids >= 0) & (ids < E)).ravel()
+
+    # stage 1: a per slot against the oracle's g, u and their bounds
+    qh, dh = O.quantize_act(h)
+    for p in np.flatnonzero(valid):
+        t, e = p // k, int(ids.ravel()[p])
+        G = gu[e].reshape(2 * F, -1)
+        g = O.matvec_q(G[:F].ravel(), F, H, qh[t], dh[t])[0]
+        u = O.matvec_q(G[F:].ravel(), F, H, qh[t], dh[t])[0]
+        bg = TOL * O.matvec_bound(G[:F].ravel(), F, H, qh[t], dh[t])[0]
+        bu = TOL * O.matvec_bound(G[F:].ravel(), F, H, qh[t], dh[t])[0]
+        if swiglu:
+            sg = np.array([O.silu(v) for v in g])
+            a_ref = sg * u
+            lim = 1.1 * np.abs(u) * bg + np.abs(sg) * bu + 1.1 * bg * bu
+        else:
+            a_ref = g * u
+            lim = np.abs(u) * bg + np.abs(g) * bu + bg * bu
+        lim = lim + 4 * 2.0 ** -24 * np.abs(a_ref) + 1e-30
+        assert np.all(np.abs(a_g[p] - a_ref) <= lim), f"slot {p}: a outside bound"
+        # requantization: bit-exact on the GPU's own a
+        qa_r, da_r = O.quantize_act(a_g[p])
+        np.testing.assert_array_equal(qa_g[p], qa_r)
+        np.testing.assert_array_equal(da_g[p].view(np.uint32), da_r.view(np.uint32))
+
+    # stage 2: down + combine from the GPU's own quantized intermediate
+    qa_use = np.where(valid[:, None], qa_g, 0).astype(np.int8)
+    da_use = np.where(valid[:, None], da_g, 0).astype(np.float32)
+    y2, yb, nbad = O.moe_down_combine(dn, E, H, F, ids, wts, qa_use, da_use)
+    assert nbad == expect_bad
+    assert_within_bound(y, y2, yb, what="y (stage 2)")
+
+    # end to end against the oracle's own intermediate
+    y_ref, _, qa_r, da_r, nbad = O.moe(gu, dn, E, H, F, h, ids, wts, swiglu=swiglu, want_intermediate=True)
+    extra = np.zeros_like(y_ref)
+    for p in np.flatnonzero(valid):
+        t, e = p // k, int(ids.ravel()[p])
+        dah = np.abs(qa_use[p].astype(np.float64) * np.repeat(da_use[p].astype(np.float64), 32)
+                     - qa_r[p].astype(np.float64) * np.repeat(da_r[p].astype(np.float64), 32))
+        if np.any(dah):
+            extra[t] += abs(float(wts.ravel()[p])) * (np.abs(_np_dequant(dn[e], H, F)) @ dah)
+    assert_within_bound(y, y_ref, yb + extra / TOL, what="y (end to end)")
+    return y
+
+
+# ------------------------------------------------------------- small layer -
+
+E_S, H_S, F_S = 8, 256, 128
+
+
+@pytest.fixture(scope="module")
+def small(torch):
+    gu = synth.expert_blocks(E_S, 2 * F_S, H_S, stream=601)
+    dn = synth.expert_blocks(E_S, H_S, F_S, stream=602)
+    return gu, dn, cbq.Moe(gu, dn, E_S, H_S, F_S)
+
+
+@pytest.mark.parametrize("n_tok,k", [(1, 1), (1, 4), (3, 2), (5, 3), (5, 8), (2, 8)])
+@pytest.mark.parametrize("swiglu", [1, 0])
+def test_small_layer(torch, small, n_tok, k, swiglu):
+    gu, dn, L = small
+    h = synth.activations(n_tok, H_S, stream=603 + n_tok)
+    ids, wts = synth.router(n_tok, k, E_S, stream=604 + k)
+    _check_layer(torch, L, gu, dn, E_S, H_S, F_S, h, ids, wts, swiglu)
+
+
+def test_duplicates_and_bad_ids(torch, small):
+    gu, dn, L = small
+    h = synth.activations(5, H_S, stream=610)
+    ids = np.array([[3, 3, 1], [9, 2, -4], [2, 2, 2], [0, 7, 3], [3, 3, 3]], dtype=np.int32)
+    wts = np.random.default_rng(3).random((5, 3)).astype(np.float32)
+    _check_layer(torch, L, gu, dn, E_S, H_S, F_S, h, ids, wts, 1, expect_bad=2)
+
+
+def test_nothing_routed_gives_zero(torch, small):
+    gu, dn, L = small
+    h = synth.activations(2, H_S, stream=611)
+    ids = np.array([[-1, 8], [100, -7]], dtype=np.int32)
+    wts = np.ones((2, 2), dtype=np.float32)
+    y = cbq.cbq_moe_matvec(L, _dev(torch, h), _dev(torch, ids), _dev(torch, wts)).cpu().numpy()
+    assert np.all(y == 0)
+    assert cbq.cbq_get_device_error() == cbq.CBQ_DEVERR_BAD_EXPERT_ID
+    assert cbq.cbq_get_device_error() == 0  # read clears
+
+
+def test_host_entry_matches(torch, small):
+    gu, dn, L = small
+    h = synth.activations(4, H_S, stream=612)
+    ids, wts = synth.router(4, 3, E_S, stream=613)
+    y = cbq.cbq_moe_matvec(L, _dev(torch, h), _dev(torch, ids), _dev(torch, wts)).cpu().numpy()
+    np.testing.assert_array_equal(cbq.cbq_moe_matvec_host(L, h, ids, wts), y)
+
+
+def test_expert_block_dots(torch, small):
+    gu, dn, L = small
+    qx = np.random.default_rng(9).integers(-127, 128, size=(3, H_S)).astype(np.int8)
+    s = cbq.cbq_moe_debug_block_dots(L, 5, 0, _dev(torch, qx)).cpu().numpy()
+    np.testing.assert_array_equal(s, O.block_dots(gu[5], 2 * F_S, H_S, qx))
+    qx = np.random.default_rng(10).integers(-127, 128, size=(2, F_S)).astype(np.int8)
+    s = cbq.cbq_moe_debug_block_dots(L, 7, 1, _dev(torch, qx)).cpu().numpy()
+    np.testing.assert_array_equal(s, O.block_dots(dn[7], H_S, F_S, qx))
+
+
+def test_repeated_calls_are_deterministic(torch, small):
+    gu, dn, L = small
+    h = _dev(torch, synth.activations(5, H_S, stream=614))
+    ids, wts = synth.router(5, 8, E_S, stream=615)
+    ids, wts = _dev(torch, ids), _dev(torch, wts)
+    ys = [cbq.cbq_moe_matvec(L, h, ids, wts).cpu().numpy() for _ in range(3)]
+    np.testing.assert_array_equal(ys[0], ys[1])
+    np.testing.assert_array_equal(ys[0], ys[2])
+
+
+# --------------------------------------------------------- full-size layer -
+
+E, H, F = 256, 4096, 2048
+
+
+@pytest.fixture(scope="module")
+def full(torch):
+    """The 256-expert layer; only the experts the two routing tables use are
+    drawn, the rest stay zero (their bytes are never read)."""
+    ids1, wts1 = synth.router(1, 4, E, stream=synth.S_IDS)
+    ids5, wts5 = synth.router(5, 8, E, stream=synth.S_IDS + 1)
+    used = np.union1d(synth.distinct_experts(ids1, E), synth.distinct_experts(ids5, E))
+    gu = np.zeros((E, 2 * F, H // 32, 18), dtype=np.uint8)
+    dn = np.zeros((E, H, F // 32, 18), dtype=np.uint8)
+    for e in used:
+        gu[e] = synth.weight_blocks(2 * F, H, stream=synth.S_GATE_UP * 1000 + int(e))
+        dn[e] = synth.weight_blocks(H, F, stream=synth.S_DOWN * 1000 + int(e))
+    L = cbq.Moe(gu, dn, E, H, F)
+    return gu, dn, L, (ids1, wts1), (ids5, wts5)
+
+
+def test_full_layer_batch1_top4(torch, full):
+    gu, dn, L, (ids, wts), _ = full
+    h = synth.activations(1, H, stream=synth.S_H)
+    _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, 1)
+
+
+def test_full_layer_batch5_top8(torch, full):
+    gu, dn, L, _, (ids, wts) = full
+    h = synth.activations(5, H, stream=synth.S_H + 1)
+    _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, 1)

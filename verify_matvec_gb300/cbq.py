@@ -1,0 +1,335 @@
+"""Thin ctypes binding of libcbq.so (include/cbq.h), same names as the C ABI.
+
+Argument marshalling only: torch tensors give device pointers and the current
+stream, numpy arrays give host pointers.  Every step of the path runs in the
+library's CUDA kernels; if libcbq.so is missing this module raises instead of
+computing anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libcbq.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "cbq.h")
+
+CBQ_OK, CBQ_EINVAL, CBQ_ECUDA, CBQ_ENOMEM, CBQ_EDEVICE = 0, -1, -2, -3, -4
+CBQ_QK = 32
+CBQ_BLOCK_BYTES = 18
+CBQ_MAX_COLS = 5
+CBQ_MAX_TOKENS = 5
+CBQ_MAX_TOPK = 16
+CBQ_DEVERR_BAD_EXPERT_ID = 0x1
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SIGS = {
+    "cbq_status_string": ([_I], ctypes.c_char_p),
+    "cbq_last_cuda_error": ([], ctypes.c_char_p),
+    "cbq_weights_create": ([_P, _I64, _I64, _I, _P, ctypes.POINTER(_P)], _I),
+    "cbq_weights_destroy": ([_P], _I),
+    "cbq_weights_info": ([_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)], _I),
+    "cbq_quantize_act": ([_P, _I64, _I, _P, _P, _P], _I),
+    "cbq_matvec_q": ([_P, _P, _P, _I, _P, _P], _I),
+    "cbq_matvec": ([_P, _P, _I, _P, _P], _I),
+    "cbq_matvec_host": ([_P, _P, _I, _P, _P], _I),
+    "cbq_moe_create": ([_P, _P, _I, _I64, _I64, _I, _P, ctypes.POINTER(_P)], _I),
+    "cbq_moe_destroy": ([_P], _I),
+    "cbq_moe_info": ([_P, ctypes.POINTER(_I), ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)], _I),
+    "cbq_moe_matvec": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
+    "cbq_moe_matvec_host": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
+    "cbq_get_device_error": ([ctypes.POINTER(ctypes.c_uint)], _I),
+    "cbq_debug_block_dots": ([_P, _P, _I, _P, _P], _I),
+    "cbq_moe_debug_block_dots": ([_P, _I, _I, _P, _I, _P, _P], _I),
+    "cbq_moe_set_debug": ([_P, _I], _I),
+    "cbq_moe_set_stage_events": ([_P, _P, _P, _P, _P], _I),
+    "cbq_moe_debug_intermediate": ([_P, _I, _P, _P, _P, _P], _I),
+}
+
+_lib = None
+
+
+class CbqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = load()
+        msg = lib.cbq_status_string(status).decode()
+        cuda = lib.cbq_last_cuda_error().decode()
+        super().__init__(f"{where}: {msg}" + (f" [{cuda}]" if cuda else ""))
+        self.status = status
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/cbq.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char \*)\s*(cbq_\w+)\s*\(", text, re.M)))
+
+
+def load():
+    """Load libcbq.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m verify_matvec_gb300.build`; "
+                          "this package has no CPU path")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (args, res) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != CBQ_OK:
+        raise CbqError(status, where)
+
+
+# ----------------------------------------------------------- marshalling --
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev_ptr(t, dtype, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _host_ptr(a: np.ndarray, dtype, name):
+    if not isinstance(a, np.ndarray) or a.dtype != dtype or not a.flags["C_CONTIGUOUS"]:
+        raise TypeError(f"{name} must be a C-contiguous numpy {np.dtype(dtype).name} array")
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ----------------------------------------------------------------- handles --
+
+class Weights:
+    """cbq_weights: one dense M x K codebook-4bit matrix on the device."""
+
+    def __init__(self, blocks, M: int, K: int, stream=None):
+        torch = _torch()
+        lib = load()
+        h = ctypes.c_void_p()
+        if isinstance(blocks, torch.Tensor):
+            if blocks.numel() != M * (K // CBQ_QK) * CBQ_BLOCK_BYTES:
+                raise ValueError("blocks do not match M x K")
+            ptr, on_dev = _dev_ptr(blocks, torch.uint8, "blocks"), 1
+        else:
+            blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+            if blocks.size != M * (K // CBQ_QK) * CBQ_BLOCK_BYTES:
+                raise ValueError("blocks do not match M x K")
+            ptr, on_dev = blocks.ctypes.data_as(ctypes.c_void_p), 0
+        _check(lib.cbq_weights_create(ptr, M, K, on_dev, _stream(stream), ctypes.byref(h)), "cbq_weights_create")
+        self._h = h
+        self.M, self.K = M, K
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("destroyed handle")
+        return self._h
+
+    def device_bytes(self) -> int:
+        b = ctypes.c_int64()
+        _check(load().cbq_weights_info(self.handle, None, None, ctypes.byref(b)), "cbq_weights_info")
+        return b.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            load().cbq_weights_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Moe:
+    """cbq_moe: E experts, each a stacked gate_up (2F x H) and a down (H x F)."""
+
+    def __init__(self, gate_up, down, E: int, H: int, F: int, stream=None):
+        torch = _torch()
+        lib = load()
+        h = ctypes.c_void_p()
+        if isinstance(gate_up, torch.Tensor):
+            p1, p2, on_dev = _dev_ptr(gate_up, torch.uint8, "gate_up"), _dev_ptr(down, torch.uint8, "down"), 1
+        else:
+            gate_up = np.ascontiguousarray(gate_up, dtype=np.uint8)
+            down = np.ascontiguousarray(down, dtype=np.uint8)
+            p1, p2, on_dev = gate_up.ctypes.data_as(_P), down.ctypes.data_as(_P), 0
+        nbH, nbF = H // CBQ_QK, F // CBQ_QK
+        n_gu = gate_up.numel() if isinstance(gate_up, torch.Tensor) else gate_up.size
+        n_dn = down.numel() if isinstance(down, torch.Tensor) else down.size
+        if n_gu != E * 2 * F * nbH * CBQ_BLOCK_BYTES or n_dn != E * H * nbF * CBQ_BLOCK_BYTES:
+            raise ValueError("expert blocks do not match E, H, F")
+        _check(lib.cbq_moe_create(p1, p2, E, H, F, on_dev, _stream(stream), ctypes.byref(h)), "cbq_moe_create")
+        self._h = h
+        self.E, self.H, self.F = E, H, F
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("destroyed handle")
+        return self._h
+
+    def device_bytes(self) -> int:
+        b = ctypes.c_int64()
+        _check(load().cbq_moe_info(self.handle, None, None, None, ctypes.byref(b)), "cbq_moe_info")
+        return b.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            load().cbq_moe_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ----------------------------------------------------------- entry points --
+
+def cbq_quantize_act(x, qx=None, dx=None, stream=None):
+    """x: (n, K) float32 CUDA tensor -> (qx int8 (n, K), dx float32 (n, K/32))."""
+    torch = _torch()
+    x2 = x.reshape(-1, x.shape[-1])
+    n, K = x2.shape
+    if qx is None:
+        qx = torch.empty((n, K), dtype=torch.int8, device=x.device)
+    if dx is None:
+        dx = torch.empty((n, K // CBQ_QK), dtype=torch.float32, device=x.device)
+    _check(load().cbq_quantize_act(_dev_ptr(x2, torch.float32, "x"), K, n, _dev_ptr(qx, torch.int8, "qx"),
+                                   _dev_ptr(dx, torch.float32, "dx"), _stream(stream)), "cbq_quantize_act")
+    return qx, dx
+
+
+def _y_out(y, n, M, device):
+    torch = _torch()
+    if y is None:
+        y = torch.empty((n, M), dtype=torch.float32, device=device)
+    return y
+
+
+def cbq_matvec_q(W: Weights, qx, dx, y=None, stream=None):
+    torch = _torch()
+    n = qx.reshape(-1, W.K).shape[0]
+    y = _y_out(y, n, W.M, qx.device)
+    _check(load().cbq_matvec_q(W.handle, _dev_ptr(qx, torch.int8, "qx"), _dev_ptr(dx, torch.float32, "dx"), n,
+                               _dev_ptr(y, torch.float32, "y"), _stream(stream)), "cbq_matvec_q")
+    return y
+
+
+def cbq_matvec(W: Weights, x, y=None, stream=None):
+    torch = _torch()
+    n = x.reshape(-1, W.K).shape[0]
+    y = _y_out(y, n, W.M, x.device)
+    _check(load().cbq_matvec(W.handle, _dev_ptr(x, torch.float32, "x"), n, _dev_ptr(y, torch.float32, "y"),
+                             _stream(stream)), "cbq_matvec")
+    return y
+
+
+def cbq_matvec_host(W: Weights, x: np.ndarray, y: np.ndarray | None = None, stream=None):
+    n = x.reshape(-1, W.K).shape[0]
+    if y is None:
+        y = np.empty((n, W.M), dtype=np.float32)
+    _check(load().cbq_matvec_host(W.handle, _host_ptr(x, np.float32, "x"), n, _host_ptr(y, np.float32, "y"),
+                                  _stream(stream)), "cbq_matvec_host")
+    return y
+
+
+def cbq_moe_matvec(L: Moe, h, ids, wts, swiglu: int = 1, y=None, stream=None):
+    torch = _torch()
+    n_tok, k = ids.shape
+    if y is None:
+        y = torch.empty((n_tok, L.H), dtype=torch.float32, device=h.device)
+    _check(load().cbq_moe_matvec(L.handle, _dev_ptr(h, torch.float32, "h"), n_tok, _dev_ptr(ids, torch.int32, "ids"),
+                                 _dev_ptr(wts, torch.float32, "wts"), k, int(swiglu),
+                                 _dev_ptr(y, torch.float32, "y"), _stream(stream)), "cbq_moe_matvec")
+    return y
+
+
+def cbq_moe_matvec_host(L: Moe, h: np.ndarray, ids: np.ndarray, wts: np.ndarray, swiglu: int = 1,
+                        y: np.ndarray | None = None, stream=None):
+    n_tok, k = ids.shape
+    if y is None:
+        y = np.empty((n_tok, L.H), dtype=np.float32)
+    _check(load().cbq_moe_matvec_host(L.handle, _host_ptr(h, np.float32, "h"), n_tok,
+                                      _host_ptr(ids, np.int32, "ids"), _host_ptr(wts, np.float32, "wts"), k,
+                                      int(swiglu), _host_ptr(y, np.float32, "y"), _stream(stream)),
+           "cbq_moe_matvec_host")
+    return y
+
+
+def cbq_get_device_error() -> int:
+    code = ctypes.c_uint()
+    _check(load().cbq_get_device_error(ctypes.byref(code)), "cbq_get_device_error")
+    return code.value
+
+
+def cbq_debug_block_dots(W: Weights, qx, s=None, stream=None):
+    torch = _torch()
+    n = qx.reshape(-1, W.K).shape[0]
+    if s is None:
+        s = torch.empty((n, W.M, W.K // CBQ_QK), dtype=torch.int32, device=qx.device)
+    _check(load().cbq_debug_block_dots(W.handle, _dev_ptr(qx, torch.int8, "qx"), n, _dev_ptr(s, torch.int32, "s"),
+                                       _stream(stream)), "cbq_debug_block_dots")
+    return s
+
+
+def cbq_moe_debug_block_dots(L: Moe, e: int, which: int, qx, s=None, stream=None):
+    torch = _torch()
+    M, K = (2 * L.F, L.H) if which == 0 else (L.H, L.F)
+    n = qx.reshape(-1, K).shape[0]
+    if s is None:
+        s = torch.empty((n, M, K // CBQ_QK), dtype=torch.int32, device=qx.device)
+    _check(load().cbq_moe_debug_block_dots(L.handle, e, which, _dev_ptr(qx, torch.int8, "qx"), n,
+                                           _dev_ptr(s, torch.int32, "s"), _stream(stream)), "cbq_moe_debug_block_dots")
+    return s
+
+
+def cbq_moe_set_debug(L: Moe, keep: bool):
+    _check(load().cbq_moe_set_debug(L.handle, int(bool(keep))), "cbq_moe_set_debug")
+
+
+def cbq_moe_set_stage_events(L: Moe, events=None):
+    """events: four torch.cuda.Event(enable_timing=True) or None to stop."""
+    ptrs = [None] * 4 if events is None else [ctypes.c_void_p(ev.cuda_event) for ev in events]
+    _check(load().cbq_moe_set_stage_events(L.handle, *ptrs), "cbq_moe_set_stage_events")
+
+
+def cbq_moe_debug_intermediate(L: Moe, nslots: int, stream=None):
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    a = torch.empty((nslots, L.F), dtype=torch.float32, device=dev)
+    qa = torch.empty((nslots, L.F), dtype=torch.int8, device=dev)
+    da = torch.empty((nslots, L.F // CBQ_QK), dtype=torch.float32, device=dev)
+    _check(load().cbq_moe_debug_intermediate(L.handle, nslots, _dev_ptr(a, torch.float32, "a"),
+                                             _dev_ptr(qa, torch.int8, "qa"), _dev_ptr(da, torch.float32, "da"),
+                                             _stream(stream)), "cbq_moe_debug_intermediate")
+    return a, qa, da

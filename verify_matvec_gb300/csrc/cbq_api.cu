@@ -1,0 +1,468 @@
+// cbq_api.cu -- the C ABI declared in include/cbq.h: handles, argument
+// checks, device selection and launch sequencing.  No arithmetic of the
+// method lives here; every step of the path runs in the kernels of
+// cbq_kernels.cu.
+#include "cbq.h"
+#include "cbq_internal.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+using cbq::DevMat;
+using cbq::DevMoe;
+using cbq::MoeWork;
+
+struct cbq_weights {
+    int device;
+    DevMat mat;
+    uint4 *qs;
+    uint2 *sc;
+    int8_t *ws_qx;   // CBQ_MAX_COLS x K
+    float *ws_dx;    // CBQ_MAX_COLS x K/32
+    float *st_x;     // host-entry staging: CBQ_MAX_COLS x K fp32
+    float *st_y;     // CBQ_MAX_COLS x M fp32
+    int64_t K;
+    int64_t bytes;
+};
+
+struct cbq_moe {
+    int device;
+    DevMoe L;
+    uint4 *gu_qs, *dn_qs;
+    uint2 *gu_sc, *dn_sc;
+    MoeWork ws;
+    float *st_h;      // CBQ_MAX_TOKENS x H
+    int32_t *st_ids;  // kMaxSlots
+    float *st_wts;    // kMaxSlots
+    float *st_y;      // CBQ_MAX_TOKENS x H
+    int64_t bytes;
+};
+
+namespace {
+
+thread_local char t_last_error[256] = "";
+
+int cuda_fail(cudaError_t e, const char *where) {
+    snprintf(t_last_error, sizeof t_last_error, "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+    return CBQ_ECUDA;
+}
+
+#define CBQ_CUDA(call)                                        \
+    do {                                                      \
+        cudaError_t e_ = (call);                              \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call);   \
+    } while (0)
+
+class DeviceScope {
+  public:
+    explicit DeviceScope(int dev) {
+        status_ = cudaGetDevice(&prev_);
+        if (status_ == cudaSuccess && prev_ != dev) {
+            status_ = cudaSetDevice(dev);
+            changed_ = status_ == cudaSuccess;
+        }
+    }
+    ~DeviceScope() {
+        if (changed_) cudaSetDevice(prev_);
+    }
+    cudaError_t status() const { return status_; }
+
+  private:
+    int prev_ = 0;
+    bool changed_ = false;
+    cudaError_t status_ = cudaSuccess;
+};
+
+int check_device(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "cudaGetDevice");
+        return CBQ_EDEVICE;
+    }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess)
+        return CBQ_EDEVICE;
+    if (major != 10 || minor != 3) {
+        snprintf(t_last_error, sizeof t_last_error, "device %d is sm_%d%d; this library is built for sm_103a",
+                 *dev, major, minor);
+        return CBQ_EDEVICE;
+    }
+    return CBQ_OK;
+}
+
+template <typename T>
+int dev_alloc(T **p, size_t count, int64_t *bytes) {
+    *p = nullptr;
+    if (count == 0) return CBQ_OK;
+    if (cudaMalloc((void **)p, count * sizeof(T)) != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        snprintf(t_last_error, sizeof t_last_error, "cudaMalloc of %zu bytes failed", count * sizeof(T));
+        return CBQ_ENOMEM;
+    }
+    *bytes += (int64_t)(count * sizeof(T));
+    return CBQ_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Repack canonical blocks (host or device) of an M x K matrix into qs/sc.
+int repack_into(const void *blocks, int64_t M, int nb, int on_device, uint4 *qs, uint2 *sc, cudaStream_t s) {
+    const size_t nbytes = (size_t)M * (size_t)nb * CBQ_BLOCK_BYTES;
+    const uint8_t *src = static_cast<const uint8_t *>(blocks);
+    uint8_t *tmp = nullptr;
+    if (!on_device) {
+        if (cudaMalloc((void **)&tmp, nbytes) != cudaSuccess) {
+            cudaGetLastError();
+            return CBQ_ENOMEM;
+        }
+        cudaError_t e = cudaMemcpyAsync(tmp, blocks, nbytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) {
+            cudaFree(tmp);
+            return cuda_fail(e, "cudaMemcpyAsync(blocks)");
+        }
+        src = tmp;
+    }
+    cudaError_t e = cbq::launch_repack(src, M, nb, qs, sc, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (tmp) cudaFree(tmp);
+    if (e != cudaSuccess) return cuda_fail(e, "repack");
+    return CBQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *cbq_status_string(int status) {
+    switch (status) {
+        case CBQ_OK: return "CBQ_OK";
+        case CBQ_EINVAL: return "CBQ_EINVAL: invalid argument";
+        case CBQ_ECUDA: return "CBQ_ECUDA: CUDA error";
+        case CBQ_ENOMEM: return "CBQ_ENOMEM: device allocation failed";
+        case CBQ_EDEVICE: return "CBQ_EDEVICE: no usable sm_103 device";
+        default: return "unknown cbq status";
+    }
+}
+
+const char *cbq_last_cuda_error(void) { return t_last_error; }
+
+// ------------------------------------------------------------ dense ------
+
+int cbq_weights_destroy(cbq_weights *W) {
+    if (!W) return CBQ_EINVAL;
+    DeviceScope scope(W->device);
+    cudaFree(W->qs);
+    cudaFree(W->sc);
+    cudaFree(W->ws_qx);
+    cudaFree(W->ws_dx);
+    cudaFree(W->st_x);
+    cudaFree(W->st_y);
+    delete W;
+    return CBQ_OK;
+}
+
+int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device, void *stream, cbq_weights **out) {
+    if (!out) return CBQ_EINVAL;
+    *out = nullptr;
+    if (!blocks || M < 1 || K < CBQ_QK || K % CBQ_QK != 0 || M > (int64_t)1 << 31 || K > (int64_t)1 << 20)
+        return CBQ_EINVAL;
+    int dev = 0;
+    int rc = check_device(&dev);
+    if (rc != CBQ_OK) return rc;
+    const int nb = (int)(K / CBQ_QK);
+    const int nbp = cbq::round_up4(nb);
+    size_t smem_max = 0;
+    CBQ_CUDA(cbq::device_smem_limit(&smem_max));
+    if (cbq::matvec_smem_bytes(nbp, CBQ_MAX_COLS) > smem_max) return CBQ_EINVAL;
+
+    cbq_weights *W = new (std::nothrow) cbq_weights();
+    if (!W) return CBQ_ENOMEM;
+    W->device = dev;
+    W->K = K;
+    if ((rc = dev_alloc(&W->qs, cbq::qs_elems(M, nb), &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->sc, cbq::sc_elems(M, nb), &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->ws_qx, (size_t)CBQ_MAX_COLS * K, &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->ws_dx, (size_t)CBQ_MAX_COLS * nb, &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->st_x, (size_t)CBQ_MAX_COLS * K, &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->st_y, (size_t)CBQ_MAX_COLS * M, &W->bytes)) != CBQ_OK) {
+        cbq_weights_destroy(W);
+        return rc;
+    }
+    rc = repack_into(blocks, M, nb, on_device, W->qs, W->sc, as_stream(stream));
+    if (rc != CBQ_OK) {
+        cbq_weights_destroy(W);
+        return rc;
+    }
+    W->mat.qs = W->qs;
+    W->mat.sc = W->sc;
+    W->mat.M = M;
+    W->mat.nb = nb;
+    W->mat.nbp = nbp;
+    W->mat.G = (int)((M + 31) / 32);
+    *out = W;
+    return CBQ_OK;
+}
+
+int cbq_weights_info(const cbq_weights *W, int64_t *M, int64_t *K, int64_t *device_bytes) {
+    if (!W) return CBQ_EINVAL;
+    if (M) *M = W->mat.M;
+    if (K) *K = W->K;
+    if (device_bytes) *device_bytes = W->bytes;
+    return CBQ_OK;
+}
+
+int cbq_quantize_act(const float *x_dev, int64_t K, int n, int8_t *qx_dev, float *dx_dev, void *stream) {
+    if (!x_dev || !qx_dev || !dx_dev || n < 1 || K < CBQ_QK || K % CBQ_QK != 0) return CBQ_EINVAL;
+    CBQ_CUDA(cbq::launch_quantize(x_dev, K, n, qx_dev, dx_dev, as_stream(stream)));
+    return CBQ_OK;
+}
+
+int cbq_matvec_q(const cbq_weights *W, const int8_t *qx_dev, const float *dx_dev, int n, float *y_dev,
+                 void *stream) {
+    if (!W || !qx_dev || !dx_dev || !y_dev || n < 1 || n > CBQ_MAX_COLS || !aligned16(qx_dev)) return CBQ_EINVAL;
+    DeviceScope scope(W->device);
+    CBQ_CUDA(scope.status());
+    CBQ_CUDA(cbq::launch_matvec(W->mat, qx_dev, dx_dev, n, y_dev, as_stream(stream)));
+    return CBQ_OK;
+}
+
+int cbq_matvec(const cbq_weights *W, const float *x_dev, int n, float *y_dev, void *stream) {
+    if (!W || !x_dev || !y_dev || n < 1 || n > CBQ_MAX_COLS) return CBQ_EINVAL;
+    DeviceScope scope(W->device);
+    CBQ_CUDA(scope.status());
+    cudaStream_t s = as_stream(stream);
+    CBQ_CUDA(cbq::launch_quantize(x_dev, W->K, n, W->ws_qx, W->ws_dx, s));
+    CBQ_CUDA(cbq::launch_matvec(W->mat, W->ws_qx, W->ws_dx, n, y_dev, s));
+    return CBQ_OK;
+}
+
+int cbq_matvec_host(const cbq_weights *W, const float *x_host, int n, float *y_host, void *stream) {
+    if (!W || !x_host || !y_host || n < 1 || n > CBQ_MAX_COLS) return CBQ_EINVAL;
+    DeviceScope scope(W->device);
+    CBQ_CUDA(scope.status());
+    cudaStream_t s = as_stream(stream);
+    CBQ_CUDA(cudaMemcpyAsync(W->st_x, x_host, (size_t)n * W->K * sizeof(float), cudaMemcpyHostToDevice, s));
+    int rc = cbq_matvec(W, W->st_x, n, W->st_y, stream);
+    if (rc != CBQ_OK) return rc;
+    CBQ_CUDA(cudaMemcpyAsync(y_host, W->st_y, (size_t)n * W->mat.M * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CBQ_CUDA(cudaStreamSynchronize(s));
+    return CBQ_OK;
+}
+
+int cbq_debug_block_dots(const cbq_weights *W, const int8_t *qx_dev, int n, int32_t *s_dev, void *stream) {
+    if (!W || !qx_dev || !s_dev || n < 1 || n > CBQ_MAX_COLS || !aligned16(qx_dev)) return CBQ_EINVAL;
+    DeviceScope scope(W->device);
+    CBQ_CUDA(scope.status());
+    CBQ_CUDA(cbq::launch_block_dots(W->mat, qx_dev, n, s_dev, as_stream(stream)));
+    return CBQ_OK;
+}
+
+// --------------------------------------------------------------- MoE -----
+
+int cbq_moe_destroy(cbq_moe *L) {
+    if (!L) return CBQ_EINVAL;
+    DeviceScope scope(L->device);
+    cudaFree(L->gu_qs);
+    cudaFree(L->gu_sc);
+    cudaFree(L->dn_qs);
+    cudaFree(L->dn_sc);
+    cudaFree(L->ws.qh);
+    cudaFree(L->ws.dh);
+    cudaFree(L->ws.qa);
+    cudaFree(L->ws.da);
+    cudaFree(L->ws.a_dbg);
+    cudaFree(L->ws.obuf);
+    cudaFree(L->ws.cnt);
+    cudaFree(L->st_h);
+    cudaFree(L->st_ids);
+    cudaFree(L->st_wts);
+    cudaFree(L->st_y);
+    delete L;
+    return CBQ_OK;
+}
+
+int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int64_t F, int on_device, void *stream,
+                   cbq_moe **out) {
+    if (!out) return CBQ_EINVAL;
+    *out = nullptr;
+    if (!gate_up || !down || E < 1 || H < CBQ_QK || F < CBQ_QK || H % CBQ_QK || F % CBQ_QK || H > (1 << 20) ||
+        F > (1 << 20))
+        return CBQ_EINVAL;
+    int dev = 0;
+    int rc = check_device(&dev);
+    if (rc != CBQ_OK) return rc;
+    const int nbH = (int)(H / CBQ_QK), nbF = (int)(F / CBQ_QK);
+    size_t smem_max = 0;
+    CBQ_CUDA(cbq::device_smem_limit(&smem_max));
+    if (cbq::matvec_smem_bytes(cbq::round_up4(nbH), CBQ_MAX_TOKENS) > smem_max ||
+        cbq::matvec_smem_bytes(cbq::round_up4(nbF), CBQ_MAX_COLS) > smem_max)
+        return CBQ_EINVAL;
+
+    cbq_moe *L = new (std::nothrow) cbq_moe();
+    if (!L) return CBQ_ENOMEM;
+    L->device = dev;
+    const size_t guq = cbq::qs_elems(2 * F, nbH), gus = cbq::sc_elems(2 * F, nbH);
+    const size_t dnq = cbq::qs_elems(H, nbF), dns = cbq::sc_elems(H, nbF);
+    const size_t slots = cbq::kMaxSlots;
+    if ((rc = dev_alloc(&L->gu_qs, guq * E, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->gu_sc, gus * E, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->dn_qs, dnq * E, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->dn_sc, dns * E, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.qh, (size_t)CBQ_MAX_TOKENS * H, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.dh, (size_t)CBQ_MAX_TOKENS * nbH, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.qa, slots * F, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.da, slots * nbF, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.a_dbg, slots * F, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.obuf, slots * H, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.cnt, (size_t)(H / 32), &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->st_h, (size_t)CBQ_MAX_TOKENS * H, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->st_ids, slots, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->st_wts, slots, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->st_y, (size_t)CBQ_MAX_TOKENS * H, &L->bytes)) != CBQ_OK) {
+        cbq_moe_destroy(L);
+        return rc;
+    }
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemsetAsync(L->ws.cnt, 0, (size_t)(H / 32) * sizeof(unsigned), s) != cudaSuccess) {
+        cbq_moe_destroy(L);
+        return CBQ_ECUDA;
+    }
+    const size_t gu_bytes = (size_t)2 * F * nbH * CBQ_BLOCK_BYTES;
+    const size_t dn_bytes = (size_t)H * nbF * CBQ_BLOCK_BYTES;
+    for (int e = 0; e < E; ++e) {
+        rc = repack_into(static_cast<const uint8_t *>(gate_up) + e * gu_bytes, 2 * F, nbH, on_device,
+                         L->gu_qs + e * guq, L->gu_sc + e * gus, s);
+        if (rc == CBQ_OK)
+            rc = repack_into(static_cast<const uint8_t *>(down) + e * dn_bytes, H, nbF, on_device, L->dn_qs + e * dnq,
+                             L->dn_sc + e * dns, s);
+        if (rc != CBQ_OK) {
+            cbq_moe_destroy(L);
+            return rc;
+        }
+    }
+    L->L.gu_qs = L->gu_qs;
+    L->L.gu_sc = L->gu_sc;
+    L->L.dn_qs = L->dn_qs;
+    L->L.dn_sc = L->dn_sc;
+    L->L.E = E;
+    L->L.H = (int)H;
+    L->L.F = (int)F;
+    L->L.gu_qs_stride = guq;
+    L->L.gu_sc_stride = gus;
+    L->L.dn_qs_stride = dnq;
+    L->L.dn_sc_stride = dns;
+    *out = L;
+    return CBQ_OK;
+}
+
+int cbq_moe_info(const cbq_moe *L, int *E, int64_t *H, int64_t *F, int64_t *device_bytes) {
+    if (!L) return CBQ_EINVAL;
+    if (E) *E = L->L.E;
+    if (H) *H = L->L.H;
+    if (F) *F = L->L.F;
+    if (device_bytes) *device_bytes = L->bytes;
+    return CBQ_OK;
+}
+
+int cbq_moe_matvec(const cbq_moe *L, const float *h_dev, int n_tok, const int32_t *ids_dev, const float *wts_dev,
+                   int topk, int swiglu, float *y_dev, void *stream) {
+    if (!L || !h_dev || !ids_dev || !wts_dev || !y_dev || n_tok < 1 || n_tok > CBQ_MAX_TOKENS || topk < 1 ||
+        topk > CBQ_MAX_TOPK || topk > L->L.E || (swiglu != 0 && swiglu != 1))
+        return CBQ_EINVAL;
+    DeviceScope scope(L->device);
+    CBQ_CUDA(scope.status());
+    CBQ_CUDA(cbq::launch_moe(L->L, L->ws, h_dev, n_tok, ids_dev, wts_dev, topk, swiglu, y_dev, as_stream(stream)));
+    return CBQ_OK;
+}
+
+int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok, const int32_t *ids_host,
+                        const float *wts_host, int topk, int swiglu, float *y_host, void *stream) {
+    if (!L || !h_host || !ids_host || !wts_host || !y_host || n_tok < 1 || n_tok > CBQ_MAX_TOKENS || topk < 1 ||
+        topk > CBQ_MAX_TOPK || topk > L->L.E)
+        return CBQ_EINVAL;
+    DeviceScope scope(L->device);
+    CBQ_CUDA(scope.status());
+    cudaStream_t s = as_stream(stream);
+    const size_t H = (size_t)L->L.H, N = (size_t)n_tok * topk;
+    CBQ_CUDA(cudaMemcpyAsync(L->st_h, h_host, n_tok * H * sizeof(float), cudaMemcpyHostToDevice, s));
+    CBQ_CUDA(cudaMemcpyAsync(L->st_ids, ids_host, N * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    CBQ_CUDA(cudaMemcpyAsync(L->st_wts, wts_host, N * sizeof(float), cudaMemcpyHostToDevice, s));
+    int rc = cbq_moe_matvec(L, L->st_h, n_tok, L->st_ids, L->st_wts, topk, swiglu, L->st_y, stream);
+    if (rc != CBQ_OK) return rc;
+    CBQ_CUDA(cudaMemcpyAsync(y_host, L->st_y, n_tok * H * sizeof(float), cudaMemcpyDeviceToHost, s));
+    CBQ_CUDA(cudaStreamSynchronize(s));
+    return CBQ_OK;
+}
+
+int cbq_moe_debug_block_dots(const cbq_moe *L, int e, int which, const int8_t *qx_dev, int n, int32_t *s_dev,
+                             void *stream) {
+    if (!L || e < 0 || e >= L->L.E || (which != 0 && which != 1) || !qx_dev || !s_dev || n < 1 ||
+        n > CBQ_MAX_COLS || !aligned16(qx_dev))
+        return CBQ_EINVAL;
+    DeviceScope scope(L->device);
+    CBQ_CUDA(scope.status());
+    DevMat m;
+    if (which == 0) {
+        m.qs = L->gu_qs + e * L->L.gu_qs_stride;
+        m.sc = L->gu_sc + e * L->L.gu_sc_stride;
+        m.M = 2 * (int64_t)L->L.F;
+        m.nb = L->L.H / CBQ_QK;
+    } else {
+        m.qs = L->dn_qs + e * L->L.dn_qs_stride;
+        m.sc = L->dn_sc + e * L->L.dn_sc_stride;
+        m.M = L->L.H;
+        m.nb = L->L.F / CBQ_QK;
+    }
+    m.nbp = cbq::round_up4(m.nb);
+    m.G = (int)((m.M + 31) / 32);
+    CBQ_CUDA(cbq::launch_block_dots(m, qx_dev, n, s_dev, as_stream(stream)));
+    return CBQ_OK;
+}
+
+int cbq_moe_set_debug(cbq_moe *L, int keep_intermediate) {
+    if (!L) return CBQ_EINVAL;
+    L->ws.keep_a = keep_intermediate ? 1 : 0;
+    return CBQ_OK;
+}
+
+int cbq_moe_set_stage_events(cbq_moe *L, void *ev_quant, void *ev_gate_up, void *ev_down, void *ev_end) {
+    if (!L) return CBQ_EINVAL;
+    const bool all = ev_quant && ev_gate_up && ev_down && ev_end;
+    const bool none = !ev_quant && !ev_gate_up && !ev_down && !ev_end;
+    if (!all && !none) return CBQ_EINVAL;
+    L->ws.ev[0] = reinterpret_cast<cudaEvent_t>(ev_quant);
+    L->ws.ev[1] = reinterpret_cast<cudaEvent_t>(ev_gate_up);
+    L->ws.ev[2] = reinterpret_cast<cudaEvent_t>(ev_down);
+    L->ws.ev[3] = reinterpret_cast<cudaEvent_t>(ev_end);
+    return CBQ_OK;
+}
+
+int cbq_moe_debug_intermediate(const cbq_moe *L, int nslots, float *a_dev, int8_t *qa_dev, float *da_dev,
+                               void *stream) {
+    if (!L || nslots < 1 || nslots > cbq::kMaxSlots) return CBQ_EINVAL;
+    DeviceScope scope(L->device);
+    CBQ_CUDA(scope.status());
+    cudaStream_t s = as_stream(stream);
+    const size_t F = (size_t)L->L.F;
+    if (a_dev) CBQ_CUDA(cudaMemcpyAsync(a_dev, L->ws.a_dbg, nslots * F * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    if (qa_dev) CBQ_CUDA(cudaMemcpyAsync(qa_dev, L->ws.qa, nslots * F, cudaMemcpyDeviceToDevice, s));
+    if (da_dev)
+        CBQ_CUDA(cudaMemcpyAsync(da_dev, L->ws.da, nslots * (F / CBQ_QK) * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    return CBQ_OK;
+}
+
+int cbq_get_device_error(unsigned int *code) {
+    if (!code) return CBQ_EINVAL;
+    CBQ_CUDA(cbq::read_and_clear_device_error(code));
+    return CBQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,243 @@
+// cbq_device.cuh -- device building blocks of the codebook-4bit matvec.
+//
+// Device layout of one matrix (built by the repack kernel from canonical
+// blocks): rows are taken in groups of 32; for group g and block column b the
+// 32 rows' 16-byte index fields are contiguous (qs[(g*nbp + b)*32 + lane]), so
+// a warp whose lane l owns row 32g+l reads 512 contiguous bytes per block with
+// one 128-bit load per lane.  The fp16 scales sit in a separate stream, four
+// consecutive blocks of one row per 8-byte word (sc[(g*nbq + q)*32 + lane]).
+// nbp = K/32 rounded up to a multiple of 4; padded blocks and rows carry a
+// zero scale and zero indices.
+//
+// The hot loop per block and column: expand the 32 nibble indices through the
+// 16-level int8 codebook with byte permutes (the role of the pages'
+// codebook-16 expander, "fix(ggml): make ROCmFP4 codebook self-contained on
+// CUDA"), take the exact int32 block dot with dp4a against the int8
+// activations (MMVQ vecdot), and accumulate dw * dx * s in fp32.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace cbq {
+
+constexpr int kQK = 32;
+constexpr int kWarps = 8;           // warps per CTA of the matvec kernels
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxCols = 5;
+// 4-block quads each lane loads before computing on them: 16 blocks (256 B
+// per lane in flight) for one or two columns, 8 for three to five, whose
+// accumulators and expanded words need the registers.
+template <int NC>
+struct QuadBatch { static constexpr int value = NC <= 2 ? 4 : 2; };
+
+// Codebook bytes packed four per word, index order.
+//   {-127,-104,-83,-65} {-49,-35,-22,-10} {1,13,25,38} {53,69,89,113}
+constexpr uint32_t kCb0 = 0xBFAD9881u;
+constexpr uint32_t kCb1 = 0xF6EADDCFu;
+constexpr uint32_t kCb2 = 0x26190D01u;
+constexpr uint32_t kCb3 = 0x71594535u;
+// Upper eight levels plus one: {2,14,26,39} {54,70,90,114} (see expand_split).
+constexpr uint32_t kCbP0 = 0x271A0E02u;
+constexpr uint32_t kCbP1 = 0x725A4636u;
+
+// float(s) for |s| < 2^22 without an int->float conversion: the dp4a chain
+// starts from the bit pattern of 1.5*2^23, so the integer sum s lands in the
+// mantissa; subtracting 1.5*2^23 in fp32 is exact.
+constexpr int kMagicBits = 0x4B400000;
+constexpr float kMagic = 12582912.0f;
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    // Generic-mode prmt: selector nibble bits 0-2 pick one of the 8 bytes of
+    // {b,a}; bit 3 set replaces it by its sign replicated over the byte.
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint2 ld_stream8(const uint2 *p) {
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float half_lo(uint32_t v) {
+    return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t v) {
+    return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+}
+
+// ---------------------------------------------------------------------------
+// Codebook expansion.  One 32-bit index word w (index bytes 4m..4m+3) holds,
+// nibble by nibble, the indices of elements 4m, 4m+16, 4m+1, 4m+17, 4m+2,
+// 4m+18, 4m+3, 4m+19.  A byte permute uses the low 16 bits of its selector,
+// so w and w>>16 each select four codebook bytes in that element order; the
+// activations are staged in the matching order (stage_cols below).
+//
+// expand_select: exact codebook bytes.  Two permutes look the low three index
+// bits up in the lower and upper eight levels; a third, in sign mode, turns
+// index bit 3 into a byte mask that picks between them.  11 ALU ops per word.
+__device__ __forceinline__ void expand_select(uint32_t w, uint32_t &e0, uint32_t &e1) {
+    const uint32_t s = w & 0x77777777u;
+    const uint32_t a = w << 4;               // bit 3 of even nibbles -> byte sign bits
+    const uint32_t m0 = prmt(a, w, 0xD9C8u); // masks of nibbles 0..3
+    const uint32_t m1 = prmt(a, w, 0xFBEAu); // masks of nibbles 4..7
+    const uint32_t s1 = s >> 16;
+    const uint32_t l0 = prmt(kCb0, kCb1, s), h0 = prmt(kCb2, kCb3, s);
+    const uint32_t l1 = prmt(kCb0, kCb1, s1), h1 = prmt(kCb2, kCb3, s1);
+    e0 = (h0 & m0) | (l0 & ~m0);
+    e1 = (h1 & m1) | (l1 & ~m1);
+}
+
+// expand_split: two words whose byte-wise SUM is the codebook byte.  With the
+// raw index as selector, the lower-level table yields the level for indices
+// 0..7 and, in sign mode, -1 for 8..15 (all lower levels are negative).  With
+// bit 3 flipped, the upper table (levels + 1, all positive) yields level+1 for
+// 8..15 and 0 for 0..7.  The dot is then dp4a(lo,x) + dp4a(hi,x): 7 ALU ops
+// and two dp4a per word and column -- cheaper for one or two columns.
+__device__ __forceinline__ void expand_split(uint32_t w, uint32_t &lo0, uint32_t &hi0,
+                                             uint32_t &lo1, uint32_t &hi1) {
+    const uint32_t f = w ^ 0x88888888u;
+    lo0 = prmt(kCb0, kCb1, w);
+    hi0 = prmt(kCbP0, kCbP1, f);
+    lo1 = prmt(kCb0, kCb1, w >> 16);
+    hi1 = prmt(kCbP0, kCbP1, f >> 16);
+}
+
+template <int NC>
+struct UseSplit { static constexpr bool value = NC <= 2; };
+
+// Exact int32 block dots (offset by kMagicBits) of one index block against NC
+// permuted activation blocks act[c][0..1] (8 words each).
+template <int NC>
+__device__ __forceinline__ void block_dots(const uint4 w, const uint4 *const *act, int b, int sdot[NC]) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    if constexpr (UseSplit<NC>::value) {
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) expand_split(ws[m], lo[2 * m], hi[2 * m], lo[2 * m + 1], hi[2 * m + 1]);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const uint4 a0 = act[c][2 * b], a1 = act[c][2 * b + 1];
+            const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            int s = kMagicBits;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                s = __dp4a((int)lo[i], (int)av[i], s);
+                s = __dp4a((int)hi[i], (int)av[i], s);
+            }
+            sdot[c] = s;
+        }
+    } else {
+        uint32_t e[8];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) expand_select(ws[m], e[2 * m], e[2 * m + 1]);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const uint4 a0 = act[c][2 * b], a1 = act[c][2 * b + 1];
+            const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            int s = kMagicBits;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s = __dp4a((int)e[i], (int)av[i], s);
+            sdot[c] = s;
+        }
+    }
+}
+
+// One warp, lane = row of a 32-row group: accumulate quads [q0,q1) of the
+// group into acc[c] += dw * dx[c][b] * s(b,c).
+//   qs: group base of the index stream; sc: group base of the scale stream.
+template <int NC>
+__device__ __forceinline__ void warp_rows_dot(const uint4 *__restrict__ qs, const uint2 *__restrict__ sc,
+                                              int q0, int q1, const uint4 *const *act,
+                                              const float *const *dxs, float acc[NC], int lane) {
+    constexpr int QB = QuadBatch<NC>::value;
+    for (int qb = q0; qb < q1; qb += QB) {
+        uint4 w[QB * 4];
+        uint2 s[QB];
+#pragma unroll
+        for (int i = 0; i < QB; ++i) {
+            if (qb + i < q1) {
+                s[i] = ld_stream8(sc + (size_t)(qb + i) * 32 + lane);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) w[4 * i + j] = ld_stream16(qs + ((size_t)(qb + i) * 4 + j) * 32 + lane);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < QB; ++i) {
+            if (qb + i < q1) {
+                const float dw[4] = {half_lo(s[i].x), half_hi(s[i].x), half_lo(s[i].y), half_hi(s[i].y)};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int b = (qb + i) * 4 + j;
+                    int sd[NC];
+                    block_dots<NC>(w[4 * i + j], act, b, sd);
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        const float sf = __int_as_float(sd[c]) - kMagic;
+                        acc[c] = fmaf(dw[j] * dxs[c][b], sf, acc[c]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Stage activation columns into shared memory in the expander's element
+// order.  src[c] = plain int8 column (K bytes, 16-byte aligned; nullptr
+// stages a zero column), dsrc[c] its K/32 scales (dsrc == nullptr stages zero
+// scales).  act_s: ncols x nbp x 2
+// uint4; dx_s: ncols x nbp floats.  Blocks nb..nbp-1 are zero.  Must be
+// called by all threads of the CTA.
+__device__ __forceinline__ void stage_cols(const int8_t *const *src, const float *const *dsrc, int ncols,
+                                           int nb, int nbp, uint4 *act_s, float *dx_s) {
+    for (int idx = threadIdx.x; idx < ncols * nbp; idx += blockDim.x) {
+        const int c = idx / nbp, b = idx - c * nbp;
+        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+        float d = 0.0f;
+        if (b < nb && src[c]) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(src[c] + (size_t)b * kQK);
+            const uint4 x0 = p[0], x1 = p[1];
+            const uint32_t P[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            // word 2m   = x[4m], x[4m+16], x[4m+1], x[4m+17]
+            // word 2m+1 = x[4m+2], x[4m+18], x[4m+3], x[4m+19]
+            o0.x = prmt(P[0], P[4], 0x5140u); o0.y = prmt(P[0], P[4], 0x7362u);
+            o0.z = prmt(P[1], P[5], 0x5140u); o0.w = prmt(P[1], P[5], 0x7362u);
+            o1.x = prmt(P[2], P[6], 0x5140u); o1.y = prmt(P[2], P[6], 0x7362u);
+            o1.z = prmt(P[3], P[7], 0x5140u); o1.w = prmt(P[3], P[7], 0x7362u);
+            if (dsrc) d = dsrc[c][b];
+        }
+        act_s[(size_t)idx * 2] = o0;
+        act_s[(size_t)idx * 2 + 1] = o1;
+        dx_s[idx] = d;
+    }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// The activation quantization rule on one 32-value block held one value per
+// lane: d = max|v|/127 (IEEE fp32 division), q = rint(v/d) clamped, q = 0
+// when d == 0.
+__device__ __forceinline__ int8_t quant_lane(float v, float &d_out) {
+    const float amax = warp_max(fabsf(v));
+    const float d = amax / 127.0f;
+    d_out = d;
+    if (d == 0.0f) return 0;
+    float q = rintf(v / d);
+    q = fminf(fmaxf(q, -127.0f), 127.0f);
+    return (int8_t)q;
+}
+
+}  // namespace cbq

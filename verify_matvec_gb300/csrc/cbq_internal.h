@@ -1,0 +1,63 @@
+// cbq_internal.h -- launchers shared by the C-ABI layer (cbq_api.cu) and the
+// kernel translation unit (cbq_kernels.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cbq {
+
+// One repacked matrix on the device (layout described in cbq_device.cuh).
+struct DevMat {
+    const uint4 *qs;  // G * nbp * 32 index fields
+    const uint2 *sc;  // G * nbq * 32 words of four fp16 scales
+    int64_t M;        // rows
+    int nb;           // K / 32
+    int nbp;          // nb rounded up to a multiple of 4
+    int G;            // ceil(M / 32) row groups
+};
+
+inline int round_up4(int v) { return (v + 3) & ~3; }
+
+// Index/scale element counts of a repacked M x K matrix.
+inline size_t qs_elems(int64_t M, int nb) { return (size_t)((M + 31) / 32) * (size_t)round_up4(nb) * 32; }
+inline size_t sc_elems(int64_t M, int nb) { return (size_t)((M + 31) / 32) * (size_t)(round_up4(nb) / 4) * 32; }
+
+// A routed-expert layer: E stacked gate_up (2F x H) and down (H x F) matrices.
+struct DevMoe {
+    const uint4 *gu_qs;
+    const uint2 *gu_sc;
+    const uint4 *dn_qs;
+    const uint2 *dn_sc;
+    int E, H, F;
+    size_t gu_qs_stride, gu_sc_stride, dn_qs_stride, dn_sc_stride;  // per expert
+};
+
+// Per-call scratch of an MoE layer handle (device memory it owns).
+struct MoeWork {
+    int8_t *qh;       // CBQ_MAX_TOKENS x H
+    float *dh;        // CBQ_MAX_TOKENS x H/32
+    int8_t *qa;       // slots x F
+    float *da;        // slots x F/32
+    float *a_dbg;     // slots x F (written when keep_a)
+    float *obuf;      // slots x H, down-projection output per slot
+    unsigned *cnt;    // H/32 arrival counters (zero between calls)
+    int keep_a;
+    cudaEvent_t ev[4];  // optional stage events (quant, gate_up, down, end)
+};
+
+constexpr int kMaxSlots = 80;  // CBQ_MAX_TOKENS * CBQ_MAX_TOPK
+
+cudaError_t launch_repack(const uint8_t *src, int64_t M, int nb, uint4 *qs, uint2 *sc, cudaStream_t s);
+cudaError_t launch_quantize(const float *x, int64_t K, int n, int8_t *qx, float *dx, cudaStream_t s);
+cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, int n, float *y,
+                          cudaStream_t s);
+cudaError_t launch_block_dots(const DevMat &W, const int8_t *qx, int n, int32_t *sdot, cudaStream_t s);
+cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n_tok, const int32_t *ids,
+                       const float *wts, int k, int swiglu, float *y, cudaStream_t s);
+// Largest dynamic shared memory a matvec over K columns with n columns needs.
+size_t matvec_smem_bytes(int nbp, int n);
+cudaError_t device_smem_limit(size_t *bytes);
+cudaError_t read_and_clear_device_error(unsigned *code);
+
+}  // namespace cbq

@@ -1,0 +1,592 @@
+// cbq_kernels.cu -- sm_103a kernels of the codebook-4bit matvec and their
+// launchers.
+//
+//   k_repack          canonical 18-byte blocks -> device layout (handle creation)
+//   k_quantize        activation quantization, one warp per 32-value block
+//   k_matvec<NC>      dense MMVQ over NC <= 5 columns, one pass over the weights
+//   k_block_dots<NC>  the same integer path, exporting every per-block dot
+//   k_moe_gate_up     routed experts: gate+up rows, SwiGLU split, requantization
+//   k_moe_down        routed experts: down rows, router-weighted combine
+//
+// All matvec-type kernels are persistent: a grid of at most (SMs x resident
+// CTAs) CTAs, each taking a contiguous range of 32-row work items, so the
+// activations are staged into shared memory once per CTA.
+#include "cbq_device.cuh"
+#include "cbq_internal.h"
+
+#include <algorithm>
+
+namespace cbq {
+
+__device__ unsigned int g_device_error;  // CBQ_DEVERR_* bits
+constexpr unsigned kErrBadExpertId = 0x1u;
+
+// ------------------------------------------------------------- repack ------
+
+__global__ void k_repack(const uint8_t *__restrict__ src, int64_t M, int nb, int nbp, uint4 *__restrict__ qs,
+                         uint16_t *__restrict__ sc16) {
+    const int64_t total = ((M + 31) / 32) * (int64_t)nbp * 32;
+    const int nbq = nbp / 4;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int lane = (int)(idx & 31);
+        const int64_t gb = idx >> 5;
+        const int b = (int)(gb % nbp);
+        const int64_t g = gb / nbp;
+        const int64_t row = g * 32 + lane;
+        uint32_t w[4] = {0, 0, 0, 0};
+        uint16_t scale = 0;
+        if (row < M && b < nb) {
+            const uint8_t *p = src + ((size_t)row * nb + b) * 18;
+            scale = (uint16_t)(p[0] | (p[1] << 8));
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                w[i] = (uint32_t)p[2 + 4 * i] | ((uint32_t)p[3 + 4 * i] << 8) | ((uint32_t)p[4 + 4 * i] << 16) |
+                       ((uint32_t)p[5 + 4 * i] << 24);
+        }
+        qs[idx] = make_uint4(w[0], w[1], w[2], w[3]);
+        sc16[((g * nbq + b / 4) * 32 + lane) * 4 + (b & 3)] = scale;
+    }
+}
+
+cudaError_t launch_repack(const uint8_t *src, int64_t M, int nb, uint4 *qs, uint2 *sc, cudaStream_t s) {
+    const int nbp = round_up4(nb);
+    const int64_t total = ((M + 31) / 32) * (int64_t)nbp * 32;
+    const int grid = (int)std::min<int64_t>((total + 255) / 256, 65535);
+    k_repack<<<grid, 256, 0, s>>>(src, M, nb, nbp, qs, reinterpret_cast<uint16_t *>(sc));
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------- quantize ------
+
+__global__ void k_quantize(const float *__restrict__ x, int64_t total, int8_t *__restrict__ qx,
+                           float *__restrict__ dx) {
+    // total = n*K, a multiple of 32; one lane per value, one warp per block.
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx - (threadIdx.x & 31) < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        // every lane of a warp shares idx>>5, so the warp enters and leaves together
+        float d;
+        const int8_t q = quant_lane(x[idx], d);
+        qx[idx] = q;
+        if ((threadIdx.x & 31) == 0) dx[idx >> 5] = d;
+    }
+}
+
+cudaError_t launch_quantize(const float *x, int64_t K, int n, int8_t *qx, float *dx, cudaStream_t s) {
+    const int64_t total = (int64_t)n * K;
+    if (total == 0) return cudaSuccess;
+    const int grid = (int)std::min<int64_t>((total + 255) / 256, 4096);
+    k_quantize<<<grid, 256, 0, s>>>(x, total, qx, dx);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------- dense MMVQ -----
+
+size_t matvec_smem_bytes(int nbp, int n) {
+    return (size_t)n * nbp * (2 * sizeof(uint4) + sizeof(float)) + (size_t)kWarps * kMaxCols * 32 * sizeof(float);
+}
+
+struct SmemLayout {
+    uint4 *act;
+    float *dx;
+    float *part;
+};
+
+__device__ __forceinline__ SmemLayout carve(unsigned char *smem, int ncols, int nbp) {
+    SmemLayout L;
+    L.act = reinterpret_cast<uint4 *>(smem);
+    L.dx = reinterpret_cast<float *>(L.act + (size_t)ncols * nbp * 2);
+    L.part = L.dx + (size_t)ncols * nbp;
+    return L;
+}
+
+template <int NC>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_matvec(const uint4 *__restrict__ qs, const uint2 *__restrict__ sc, int64_t M, int G, int nb, int nbp,
+             const int8_t *__restrict__ qx, const float *__restrict__ dx, int64_t K, float *__restrict__ y,
+             int chunk) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int g0 = blockIdx.x * chunk;
+    const int g1 = min(G, g0 + chunk);
+    if (g0 >= G) return;
+    const SmemLayout S = carve(smem, NC, nbp);
+    {
+        const int8_t *src[NC];
+        const float *dsrc[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            src[c] = qx + (size_t)c * K;
+            dsrc[c] = dx + (size_t)c * nb;
+        }
+        stage_cols(src, dsrc, NC, nb, nbp, S.act, S.dx);
+    }
+    __syncthreads();
+    const uint4 *act[NC];
+    const float *dxs[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        act[c] = S.act + (size_t)c * nbp * 2;
+        dxs[c] = S.dx + (size_t)c * nbp;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbq = nbp / 4;
+    const int q0 = warp * nbq / kWarps, q1 = (warp + 1) * nbq / kWarps;
+    for (int g = g0; g < g1; ++g) {
+        float acc[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
+        warp_rows_dot<NC>(qs + (size_t)g * nbp * 32, sc + (size_t)g * nbq * 32, q0, q1, act, dxs, acc, lane);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) S.part[(warp * NC + c) * 32 + lane] = acc[c];
+        __syncthreads();
+        if (warp < NC) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) v += S.part[(w * NC + warp) * 32 + lane];
+            const int64_t row = (int64_t)g * 32 + lane;
+            if (row < M) y[(size_t)warp * M + row] = v;
+        }
+        __syncthreads();
+    }
+}
+
+template <int NC>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_block_dots(const uint4 *__restrict__ qs, const uint2 *__restrict__ sc, int64_t M, int G, int nb, int nbp,
+                 const int8_t *__restrict__ qx, int64_t K, int32_t *__restrict__ sdot, int chunk) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int g0 = blockIdx.x * chunk;
+    const int g1 = min(G, g0 + chunk);
+    if (g0 >= G) return;
+    const SmemLayout S = carve(smem, NC, nbp);
+    {
+        // the activation scales do not enter the integer dots: stage zeros
+        const int8_t *src[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) src[c] = qx + (size_t)c * K;
+        stage_cols(src, nullptr, NC, nb, nbp, S.act, S.dx);
+    }
+    __syncthreads();
+    const uint4 *act[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) act[c] = S.act + (size_t)c * nbp * 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbq = nbp / 4;
+    const int q0 = warp * nbq / kWarps, q1 = (warp + 1) * nbq / kWarps;
+    for (int g = g0; g < g1; ++g) {
+        const int64_t row = (int64_t)g * 32 + lane;
+        for (int q = q0; q < q1; ++q) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int b = 4 * q + j;
+                const uint4 w = ld_stream16(qs + ((size_t)g * nbp + b) * 32 + lane);
+                int sd[NC];
+                block_dots<NC>(w, act, b, sd);
+                if (row < M && b < nb) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) sdot[((size_t)c * M + row) * nb + b] = sd[c] - kMagicBits;
+                }
+            }
+        }
+    }
+}
+
+static int g_num_sms = 0;
+
+static cudaError_t num_sms(int *out) {
+    if (g_num_sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    *out = g_num_sms;
+    return cudaSuccess;
+}
+
+cudaError_t device_smem_limit(size_t *bytes) {
+    int dev = 0, v = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    *bytes = (size_t)v;
+    return e;
+}
+
+// Grid of a persistent kernel over `items` work items: at most resident
+// capacity, with contiguous equal chunks.
+template <typename Kernel>
+static cudaError_t persistent_grid(Kernel kern, size_t smem, int64_t items, int *grid, int *chunk) {
+    int sms = 0, per_sm = 0;
+    cudaError_t e = num_sms(&sms);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t cap = (int64_t)sms * std::max(per_sm, 1);
+    const int64_t g = std::max<int64_t>(1, std::min<int64_t>(items, cap));
+    const int64_t ch = (items + g - 1) / g;
+    *chunk = (int)std::max<int64_t>(ch, 1);
+    *grid = (int)std::max<int64_t>(1, (items + *chunk - 1) / *chunk);
+    return cudaSuccess;
+}
+
+template <int NC>
+static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const float *dx, float *y, cudaStream_t s) {
+    const size_t smem = matvec_smem_bytes(W.nbp, NC);
+    int grid = 0, chunk = 0;
+    cudaError_t e = persistent_grid(k_matvec<NC>, smem, W.G, &grid, &chunk);
+    if (e != cudaSuccess) return e;
+    k_matvec<NC><<<grid, kThreads, smem, s>>>(W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx, dx, (int64_t)W.nb * kQK, y,
+                                              chunk);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, int n, float *y, cudaStream_t s) {
+    switch (n) {
+        case 1: return launch_matvec_n<1>(W, qx, dx, y, s);
+        case 2: return launch_matvec_n<2>(W, qx, dx, y, s);
+        case 3: return launch_matvec_n<3>(W, qx, dx, y, s);
+        case 4: return launch_matvec_n<4>(W, qx, dx, y, s);
+        case 5: return launch_matvec_n<5>(W, qx, dx, y, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int NC>
+static cudaError_t launch_block_dots_n(const DevMat &W, const int8_t *qx, int32_t *sdot, cudaStream_t s) {
+    const size_t smem = matvec_smem_bytes(W.nbp, NC);
+    int grid = 0, chunk = 0;
+    cudaError_t e = persistent_grid(k_block_dots<NC>, smem, W.G, &grid, &chunk);
+    if (e != cudaSuccess) return e;
+    k_block_dots<NC><<<grid, kThreads, smem, s>>>(W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx, (int64_t)W.nb * kQK, sdot,
+                                                  chunk);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_block_dots(const DevMat &W, const int8_t *qx, int n, int32_t *sdot, cudaStream_t s) {
+    switch (n) {
+        case 1: return launch_block_dots_n<1>(W, qx, sdot, s);
+        case 2: return launch_block_dots_n<2>(W, qx, sdot, s);
+        case 3: return launch_block_dots_n<3>(W, qx, sdot, s);
+        case 4: return launch_block_dots_n<4>(W, qx, sdot, s);
+        case 5: return launch_block_dots_n<5>(W, qx, sdot, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// --------------------------------------------------------- routed experts --
+
+struct MoeArgs {
+    DevMoe L;
+    MoeWork ws;
+    const int32_t *ids;
+    const float *wts;
+    float *y;
+    int n_tok, k, swiglu;
+    int nbH, nbpH, nbF, nbpF;
+};
+
+// Distinct in-range expert ids of the routing table, ascending, computed
+// redundantly by every CTA from the <= 80 ids (no host round trip).
+struct Routing {
+    int ids[kMaxSlots];
+    int first[kMaxSlots];
+    int uniq[kMaxSlots];
+    int slots[kMaxSlots];  // slots of the current expert, ascending
+    int D;
+    int ns;
+    int last;
+};
+
+__device__ void route(const int32_t *__restrict__ ids, int N, int E, Routing &R, bool report) {
+    const int t = threadIdx.x;
+    if (t < N) R.ids[t] = ids[t];
+    __syncthreads();
+    if (t < N) {
+        const int e = R.ids[t];
+        const bool valid = e >= 0 && e < E;
+        int f = valid ? 1 : 0;
+        for (int p = 0; p < t; ++p)
+            if (R.ids[p] == e) f = 0;
+        R.first[t] = f;
+        if (!valid && report) atomicOr(&g_device_error, kErrBadExpertId);
+    }
+    __syncthreads();
+    if (t < N && R.first[t]) {
+        int rank = 0;
+        for (int p = 0; p < N; ++p)
+            if (R.first[p] && R.ids[p] < R.ids[t]) ++rank;
+        R.uniq[rank] = R.ids[t];
+    }
+    if (t == 0) {
+        int D = 0;
+        for (int p = 0; p < N; ++p) D += R.first[p];
+        R.D = D;
+    }
+    __syncthreads();
+}
+
+// Slots of expert uniq[u], ascending, into R.slots / R.ns.  All threads.
+__device__ void expert_slots(Routing &R, int u, int N) {
+    if (threadIdx.x == 0) {
+        const int e = R.uniq[u];
+        int ns = 0;
+        for (int p = 0; p < N; ++p)
+            if (R.ids[p] == e) R.slots[ns++] = p;
+        R.ns = ns;
+    }
+    __syncthreads();
+}
+
+// gate (warps 0-3) and up (warps 4-7) rows of one 32-row-pair group, then the
+// SwiGLU split and the requantization of the 32 outputs, per column.  NC is 1
+// (exact) or kMaxCols, with columns nc..NC-1 reading the zero column staged
+// after the tokens and their results dropped.
+template <int NC>
+__device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R, const SmemLayout &S, int e, int g,
+                                             int c0, int nc) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = warp >> 2;  // 0 gate, 1 up
+    const int nbq = A.nbpH / 4;
+    const int q0 = (warp & 3) * nbq / 4, q1 = ((warp & 3) + 1) * nbq / 4;
+    const int Gf = A.L.F / 32;
+    const int grp = g + half * Gf;
+    const uint4 *qs = A.L.gu_qs + (size_t)e * A.L.gu_qs_stride + (size_t)grp * A.nbpH * 32;
+    const uint2 *sc = A.L.gu_sc + (size_t)e * A.L.gu_sc_stride + (size_t)grp * nbq * 32;
+    const uint4 *act[NC];
+    const float *dxs[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const int tok = c < nc ? R.slots[c0 + c] / A.k : A.n_tok;
+        act[c] = S.act + (size_t)tok * A.nbpH * 2;
+        dxs[c] = S.dx + (size_t)tok * A.nbpH;
+    }
+    float acc[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
+    warp_rows_dot<NC>(qs, sc, q0, q1, act, dxs, acc, lane);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) S.part[(warp * NC + c) * 32 + lane] = acc[c];
+    __syncthreads();
+    if (warp < nc) {
+        const int c = warp;
+        float gs = 0.0f, us = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            gs += S.part[(w * NC + c) * 32 + lane];
+            us += S.part[((w + 4) * NC + c) * 32 + lane];
+        }
+        const float a = A.swiglu ? gs / (1.0f + expf(-gs)) * us : gs * us;
+        float d;
+        const int8_t q = quant_lane(a, d);
+        const int p = R.slots[c0 + c];
+        const size_t o = (size_t)p * A.L.F + (size_t)g * 32 + lane;
+        A.ws.qa[o] = q;
+        if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
+        if (A.ws.keep_a) A.ws.a_dbg[o] = a;
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_moe_gate_up(MoeArgs A) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ Routing R;
+    const int N = A.n_tok * A.k;
+    route(A.ids, N, A.L.E, R, blockIdx.x == 0);
+    const int Gf = A.L.F / 32;
+    const int total = R.D * Gf;
+    const int chunk = (total + gridDim.x - 1) / gridDim.x;
+    const int i0 = blockIdx.x * chunk, i1 = min(total, i0 + chunk);
+    if (i0 >= i1) return;
+    const SmemLayout S = carve(smem, A.n_tok + 1, A.nbpH);
+    {
+        const int8_t *src[kMaxCols + 1];
+        const float *dsrc[kMaxCols + 1];
+        for (int t = 0; t <= A.n_tok; ++t) {  // column n_tok stays zero
+            src[t] = t < A.n_tok ? A.ws.qh + (size_t)t * A.L.H : nullptr;
+            dsrc[t] = t < A.n_tok ? A.ws.dh + (size_t)t * A.nbH : A.ws.dh;
+        }
+        stage_cols(src, dsrc, A.n_tok + 1, A.nbH, A.nbpH, S.act, S.dx);
+    }
+    int cur_u = -1;
+    for (int it = i0; it < i1; ++it) {
+        const int u = it / Gf, g = it - u * Gf;
+        if (u != cur_u) {
+            __syncthreads();
+            expert_slots(R, u, N);
+            cur_u = u;
+        }
+        __syncthreads();
+        const int e = R.uniq[u];
+        for (int c0 = 0; c0 < R.ns; c0 += kMaxCols) {
+            const int nc = min(kMaxCols, R.ns - c0);
+            if (nc == 1)
+                gate_up_item<1>(A, R, S, e, g, c0, 1);
+            else
+                gate_up_item<kMaxCols>(A, R, S, e, g, c0, nc);
+        }
+    }
+}
+
+// down rows of one 32-row group for the columns staged in S (slots
+// R.slots[c0..c0+nc), zero columns after them), written per slot to obuf.
+template <int NC>
+__device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, const SmemLayout &S, int e, int g,
+                                          int c0, int nc) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbq = A.nbpF / 4;
+    const int q0 = warp * nbq / kWarps, q1 = (warp + 1) * nbq / kWarps;
+    const uint4 *qs = A.L.dn_qs + (size_t)e * A.L.dn_qs_stride + (size_t)g * A.nbpF * 32;
+    const uint2 *sc = A.L.dn_sc + (size_t)e * A.L.dn_sc_stride + (size_t)g * nbq * 32;
+    const uint4 *act[NC];
+    const float *dxs[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        act[c] = S.act + (size_t)c * A.nbpF * 2;
+        dxs[c] = S.dx + (size_t)c * A.nbpF;
+    }
+    float acc[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
+    warp_rows_dot<NC>(qs, sc, q0, q1, act, dxs, acc, lane);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) S.part[(warp * NC + c) * 32 + lane] = acc[c];
+    __syncthreads();
+    if (warp < nc) {
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += S.part[(w * NC + warp) * 32 + lane];
+        const int p = R.slots[c0 + warp];
+        A.ws.obuf[(size_t)p * A.L.H + (size_t)g * 32 + lane] = v;
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_moe_down(MoeArgs A) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ Routing R;
+    const int N = A.n_tok * A.k;
+    route(A.ids, N, A.L.E, R, false);
+    const int Gd = A.L.H / 32;
+    if (R.D == 0) {  // nothing routed: the output is zero
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < A.n_tok * A.L.H; i += gridDim.x * blockDim.x)
+            A.y[i] = 0.0f;
+        return;
+    }
+    const int total = R.D * Gd;
+    const int chunk = (total + gridDim.x - 1) / gridDim.x;
+    const int i0 = blockIdx.x * chunk, i1 = min(total, i0 + chunk);
+    if (i0 >= i1) return;
+    const SmemLayout S = carve(smem, kMaxCols, A.nbpF);
+    int cur_u = -1;
+    for (int it = i0; it < i1; ++it) {
+        const int u = it / Gd, g = it - u * Gd;
+        if (u != cur_u) {
+            __syncthreads();
+            expert_slots(R, u, N);
+            cur_u = u;
+        }
+        const int e = R.uniq[u];
+        for (int c0 = 0; c0 < R.ns; c0 += kMaxCols) {
+            const int nc = min(kMaxCols, R.ns - c0);
+            // (re)stage this chunk's columns when the expert or chunk changed
+            if (it == i0 || g == 0 || R.ns > kMaxCols) {
+                __syncthreads();
+                const int8_t *src[kMaxCols];
+                const float *dsrc[kMaxCols];
+                for (int c = 0; c < kMaxCols; ++c) {
+                    const int p = R.slots[c0 + min(c, nc - 1)];
+                    src[c] = c < nc ? A.ws.qa + (size_t)p * A.L.F : nullptr;
+                    dsrc[c] = A.ws.da + (size_t)p * A.nbF;
+                }
+                stage_cols(src, dsrc, nc == 1 ? 1 : kMaxCols, A.nbF, A.nbpF, S.act, S.dx);
+            }
+            __syncthreads();
+            if (nc == 1)
+                down_item<1>(A, R, S, e, g, c0, 1);
+            else
+                down_item<kMaxCols>(A, R, S, e, g, c0, nc);
+        }
+        // Arrival count of row group g; the CTA completing the last of the D
+        // experts' items combines y for these rows in slot order.
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const unsigned old = atomicAdd(&A.ws.cnt[g], 1u);
+            R.last = (old == (unsigned)R.D - 1u);
+        }
+        __syncthreads();
+        if (R.last) {
+            __threadfence();
+            for (int i = threadIdx.x; i < A.n_tok * 32; i += blockDim.x) {
+                const int t = i >> 5, lane = i & 31;
+                const size_t row = (size_t)g * 32 + lane;
+                float v = 0.0f;
+                for (int j = 0; j < A.k; ++j) {
+                    const int p = t * A.k + j;
+                    const int id = R.ids[p];
+                    if (id >= 0 && id < A.L.E) v += A.wts[p] * __ldcg(A.ws.obuf + (size_t)p * A.L.H + row);
+                }
+                A.y[(size_t)t * A.L.H + row] = v;
+            }
+            if (threadIdx.x == 0) A.ws.cnt[g] = 0u;
+        }
+    }
+}
+
+cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n_tok, const int32_t *ids,
+                       const float *wts, int k, int swiglu, float *y, cudaStream_t s) {
+    MoeArgs A;
+    A.L = L;
+    A.ws = ws;
+    A.ids = ids;
+    A.wts = wts;
+    A.y = y;
+    A.n_tok = n_tok;
+    A.k = k;
+    A.swiglu = swiglu;
+    A.nbH = L.H / kQK;
+    A.nbpH = round_up4(A.nbH);
+    A.nbF = L.F / kQK;
+    A.nbpF = round_up4(A.nbF);
+    cudaError_t e = cudaSuccess;
+    if (ws.ev[0] && (e = cudaEventRecord(ws.ev[0], s)) != cudaSuccess) return e;
+    e = launch_quantize(h, L.H, n_tok, ws.qh, ws.dh, s);
+    if (e != cudaSuccess) return e;
+    if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
+    const int64_t max_experts = std::min(n_tok * k, L.E);
+    {
+        const size_t smem = matvec_smem_bytes(A.nbpH, n_tok + 1);
+        int grid = 0, chunk = 0;
+        e = persistent_grid(k_moe_gate_up, smem, max_experts * (L.F / 32), &grid, &chunk);
+        if (e != cudaSuccess) return e;
+        k_moe_gate_up<<<grid, kThreads, smem, s>>>(A);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (ws.ev[2] && (e = cudaEventRecord(ws.ev[2], s)) != cudaSuccess) return e;
+    {
+        const size_t smem = matvec_smem_bytes(A.nbpF, kMaxCols);
+        int grid = 0, chunk = 0;
+        e = persistent_grid(k_moe_down, smem, max_experts * (L.H / 32), &grid, &chunk);
+        if (e != cudaSuccess) return e;
+        k_moe_down<<<grid, kThreads, smem, s>>>(A);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (ws.ev[3]) e = cudaEventRecord(ws.ev[3], s);
+    return e;
+}
+
+cudaError_t read_and_clear_device_error(unsigned *code) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace cbq
