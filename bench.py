@@ -52,7 +52,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     return ap.parse_args()
@@ -145,10 +145,14 @@ class Clocks:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(ident), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        t0 = time.time()  # wait for the first sample so the timed region is covered
+        while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -176,6 +180,14 @@ class Clocks:
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def timing_event(torch, stream):
+    """A timing event whose CUDA handle exists (torch creates it lazily, at
+    its first record), so the library can record it by handle."""
+    e = torch.cuda.Event(enable_timing=True)
+    e.record(stream)
+    return e
 
 
 def gpu_ident(torch, local):
@@ -232,7 +244,8 @@ def run_gpu(args):
     dx = torch.empty((HEAD_N, HEAD_K // QK), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     total = args.warmup + args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(total)]
+    ev = [[timing_event(torch, stream) for _ in range(7)] for _ in range(total)]
+    torch.cuda.synchronize()
 
     def step(i, events):
         ids, wts, h, x = d_sets[i % N_SETS]

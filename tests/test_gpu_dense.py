@@ -155,3 +155,8 @@ def test_output_head_sampled_bench_shape(torch):
     rows = np.unique(np.concatenate([np.arange(0, 32), np.arange(M - 64, M),
                                      np.random.default_rng(2).integers(0, M, 300)]))
     _check_matvec(torch, W, M, K, x, rows=rows)
+
+
+def test_no_device_error_left(torch):
+    """No kernel of this module recorded a pipeline timeout or a bad id."""
+    assert cbq.cbq_get_device_error() == 0

@@ -3,8 +3,9 @@
 // Device layout of one matrix (built by the repack kernel from canonical
 // blocks): rows are taken in groups of 32; for group g and block column b the
 // 32 rows' 16-byte index fields are contiguous (qs[(g*nbp + b)*32 + lane]), so
-// a warp whose lane l owns row 32g+l reads 512 contiguous bytes per block with
-// one 128-bit load per lane.  The fp16 scales sit in a separate stream, four
+// a warp whose lane l owns row 32g+l reads 512 contiguous bytes per block, and
+// a whole group's K range is one contiguous span (bulk-copied by the pipeline
+// of cbq_pipe.cuh).  The fp16 scales sit in a separate stream, four
 // consecutive blocks of one row per 8-byte word (sc[(g*nbq + q)*32 + lane]).
 // nbp = K/32 rounded up to a multiple of 4; padded blocks and rows carry a
 // zero scale and zero indices.
@@ -25,12 +26,6 @@ constexpr int kQK = 32;
 constexpr int kWarps = 8;           // warps per CTA of the matvec kernels
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCols = 5;
-// 4-block quads each lane loads before computing on them: 16 blocks (256 B
-// per lane in flight) for one or two columns, 8 for three to five, whose
-// accumulators and expanded words need the registers.
-template <int NC>
-struct QuadBatch { static constexpr int value = NC <= 2 ? 4 : 2; };
-
 // Codebook bytes packed four per word, index order.
 //   {-127,-104,-83,-65} {-49,-35,-22,-10} {1,13,25,38} {53,69,89,113}
 constexpr uint32_t kCb0 = 0xBFAD9881u;
@@ -152,54 +147,15 @@ __device__ __forceinline__ void block_dots(const uint4 w, const uint4 *const *ac
     }
 }
 
-// One warp, lane = row of a 32-row group: accumulate quads [q0,q1) of the
-// group into acc[c] += dw * dx[c][b] * s(b,c).
-//   qs: group base of the index stream; sc: group base of the scale stream.
-template <int NC>
-__device__ __forceinline__ void warp_rows_dot(const uint4 *__restrict__ qs, const uint2 *__restrict__ sc,
-                                              int q0, int q1, const uint4 *const *act,
-                                              const float *const *dxs, float acc[NC], int lane) {
-    constexpr int QB = QuadBatch<NC>::value;
-    for (int qb = q0; qb < q1; qb += QB) {
-        uint4 w[QB * 4];
-        uint2 s[QB];
-#pragma unroll
-        for (int i = 0; i < QB; ++i) {
-            if (qb + i < q1) {
-                s[i] = ld_stream8(sc + (size_t)(qb + i) * 32 + lane);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) w[4 * i + j] = ld_stream16(qs + ((size_t)(qb + i) * 4 + j) * 32 + lane);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < QB; ++i) {
-            if (qb + i < q1) {
-                const float dw[4] = {half_lo(s[i].x), half_hi(s[i].x), half_lo(s[i].y), half_hi(s[i].y)};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int b = (qb + i) * 4 + j;
-                    int sd[NC];
-                    block_dots<NC>(w[4 * i + j], act, b, sd);
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        const float sf = __int_as_float(sd[c]) - kMagic;
-                        acc[c] = fmaf(dw[j] * dxs[c][b], sf, acc[c]);
-                    }
-                }
-            }
-        }
-    }
-}
-
 // Stage activation columns into shared memory in the expander's element
 // order.  src[c] = plain int8 column (K bytes, 16-byte aligned; nullptr
 // stages a zero column), dsrc[c] its K/32 scales (dsrc == nullptr stages zero
 // scales).  act_s: ncols x nbp x 2
-// uint4; dx_s: ncols x nbp floats.  Blocks nb..nbp-1 are zero.  Must be
-// called by all threads of the CTA.
+// uint4; dx_s: ncols x nbp floats.  Blocks nb..nbp-1 are zero.  Threads
+// tid = 0..nthr-1 share the work.
 __device__ __forceinline__ void stage_cols(const int8_t *const *src, const float *const *dsrc, int ncols,
-                                           int nb, int nbp, uint4 *act_s, float *dx_s) {
-    for (int idx = threadIdx.x; idx < ncols * nbp; idx += blockDim.x) {
+                                           int nb, int nbp, uint4 *act_s, float *dx_s, int tid, int nthr) {
+    for (int idx = tid; idx < ncols * nbp; idx += nthr) {
         const int c = idx / nbp, b = idx - c * nbp;
         uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
         float d = 0.0f;

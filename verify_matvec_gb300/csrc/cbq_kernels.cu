@@ -17,9 +17,15 @@
 #include <algorithm>
 
 namespace cbq {
-
 __device__ unsigned int g_device_error;  // CBQ_DEVERR_* bits
+}  // namespace cbq
+
+#include "cbq_pipe.cuh"
+
+namespace cbq {
+
 constexpr unsigned kErrBadExpertId = 0x1u;
+constexpr int kStages = 4;  // pipeline depth: 4 x 18 KB per CTA, two CTAs per SM
 
 // ------------------------------------------------------------- repack ------
 
@@ -82,34 +88,34 @@ cudaError_t launch_quantize(const float *x, int64_t K, int n, int8_t *qx, float 
 
 // ---------------------------------------------------------- dense MMVQ -----
 
-size_t matvec_smem_bytes(int nbp, int n) {
-    return (size_t)n * nbp * (2 * sizeof(uint4) + sizeof(float)) + (size_t)kWarps * kMaxCols * 32 * sizeof(float);
-}
+size_t matvec_smem_bytes(int nbp, int n) { return pipe_smem_bytes(kStages, n, nbp); }
 
-struct SmemLayout {
-    uint4 *act;
-    float *dx;
-    float *part;
-};
+// Debug kernel smem: activations + scales only.
+static size_t dots_smem_bytes(int nbp, int n) { return (size_t)n * nbp * 36; }
 
-__device__ __forceinline__ SmemLayout carve(unsigned char *smem, int ncols, int nbp) {
-    SmemLayout L;
-    L.act = reinterpret_cast<uint4 *>(smem);
-    L.dx = reinterpret_cast<float *>(L.act + (size_t)ncols * nbp * 2);
-    L.part = L.dx + (size_t)ncols * nbp;
-    return L;
-}
-
+// Dense MMVQ: 32-row groups [g0, g1) of this CTA, all NC columns per pass.
 template <int NC>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kPipeThreads, 2)
     k_matvec(const uint4 *__restrict__ qs, const uint2 *__restrict__ sc, int64_t M, int G, int nb, int nbp,
              const int8_t *__restrict__ qx, const float *__restrict__ dx, int64_t K, float *__restrict__ y,
              int chunk) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     const int g0 = blockIdx.x * chunk;
     const int g1 = min(G, g0 + chunk);
     if (g0 >= G) return;
-    const SmemLayout S = carve(smem, NC, nbp);
+    const PipeSmem S = carve_pipe(smem, kStages, NC, nbp);
+    pipe_init(S.pipe);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbq = nbp / 4;
+    if (warp == kConsumerWarps) {  // producer
+        if (lane == 0) {
+            Producer pr;
+            for (int g = g0; g < g1; ++g) pr.group(S.pipe, qs + (size_t)g * nbp * 32, sc + (size_t)g * nbq * 32, nbp);
+            pr.drain(S.pipe);
+        }
+        return;
+    }
     {
         const int8_t *src[NC];
         const float *dsrc[NC];
@@ -118,9 +124,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             src[c] = qx + (size_t)c * K;
             dsrc[c] = dx + (size_t)c * nb;
         }
-        stage_cols(src, dsrc, NC, nb, nbp, S.act, S.dx);
+        stage_cols(src, dsrc, NC, nb, nbp, S.act, S.dx, threadIdx.x, kConsumers);
     }
-    __syncthreads();
+    consumer_sync();
     const uint4 *act[NC];
     const float *dxs[NC];
 #pragma unroll
@@ -128,25 +134,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         act[c] = S.act + (size_t)c * nbp * 2;
         dxs[c] = S.dx + (size_t)c * nbp;
     }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nbq = nbp / 4;
-    const int q0 = warp * nbq / kWarps, q1 = (warp + 1) * nbq / kWarps;
+    Consumer co;
     for (int g = g0; g < g1; ++g) {
         float acc[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
-        warp_rows_dot<NC>(qs + (size_t)g * nbp * 32, sc + (size_t)g * nbq * 32, q0, q1, act, dxs, acc, lane);
+        co.group<NC>(S.pipe, nbp, act, dxs, acc, warp, lane);
 #pragma unroll
         for (int c = 0; c < NC; ++c) S.part[(warp * NC + c) * 32 + lane] = acc[c];
-        __syncthreads();
+        consumer_sync();
         if (warp < NC) {
             float v = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) v += S.part[(w * NC + warp) * 32 + lane];
+            for (int w = 0; w < kConsumerWarps; ++w) v += S.part[(w * NC + warp) * 32 + lane];
             const int64_t row = (int64_t)g * 32 + lane;
             if (row < M) y[(size_t)warp * M + row] = v;
         }
-        __syncthreads();
+        consumer_sync();
     }
 }
 
@@ -154,22 +158,23 @@ template <int NC>
 __global__ void __launch_bounds__(kThreads, 2)
     k_block_dots(const uint4 *__restrict__ qs, const uint2 *__restrict__ sc, int64_t M, int G, int nb, int nbp,
                  const int8_t *__restrict__ qx, int64_t K, int32_t *__restrict__ sdot, int chunk) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     const int g0 = blockIdx.x * chunk;
     const int g1 = min(G, g0 + chunk);
     if (g0 >= G) return;
-    const SmemLayout S = carve(smem, NC, nbp);
+    uint4 *act_s = reinterpret_cast<uint4 *>(smem);
+    float *dx_s = reinterpret_cast<float *>(act_s + (size_t)NC * nbp * 2);
     {
         // the activation scales do not enter the integer dots: stage zeros
         const int8_t *src[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) src[c] = qx + (size_t)c * K;
-        stage_cols(src, nullptr, NC, nb, nbp, S.act, S.dx);
+        stage_cols(src, nullptr, NC, nb, nbp, act_s, dx_s, threadIdx.x, blockDim.x);
     }
     __syncthreads();
     const uint4 *act[NC];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) act[c] = S.act + (size_t)c * nbp * 2;
+    for (int c = 0; c < NC; ++c) act[c] = act_s + (size_t)c * nbp * 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbq = nbp / 4;
     const int q0 = warp * nbq / kWarps, q1 = (warp + 1) * nbq / kWarps;
@@ -216,13 +221,13 @@ cudaError_t device_smem_limit(size_t *bytes) {
 // Grid of a persistent kernel over `items` work items: at most resident
 // capacity, with contiguous equal chunks.
 template <typename Kernel>
-static cudaError_t persistent_grid(Kernel kern, size_t smem, int64_t items, int *grid, int *chunk) {
+static cudaError_t persistent_grid(Kernel kern, int threads, size_t smem, int64_t items, int *grid, int *chunk) {
     int sms = 0, per_sm = 0;
     cudaError_t e = num_sms(&sms);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
     if (e != cudaSuccess) return e;
     const int64_t cap = (int64_t)sms * std::max(per_sm, 1);
     const int64_t g = std::max<int64_t>(1, std::min<int64_t>(items, cap));
@@ -236,9 +241,9 @@ template <int NC>
 static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const float *dx, float *y, cudaStream_t s) {
     const size_t smem = matvec_smem_bytes(W.nbp, NC);
     int grid = 0, chunk = 0;
-    cudaError_t e = persistent_grid(k_matvec<NC>, smem, W.G, &grid, &chunk);
+    cudaError_t e = persistent_grid(k_matvec<NC>, kPipeThreads, smem, W.G, &grid, &chunk);
     if (e != cudaSuccess) return e;
-    k_matvec<NC><<<grid, kThreads, smem, s>>>(W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx, dx, (int64_t)W.nb * kQK, y,
+    k_matvec<NC><<<grid, kPipeThreads, smem, s>>>(W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx, dx, (int64_t)W.nb * kQK, y,
                                               chunk);
     return cudaGetLastError();
 }
@@ -256,9 +261,9 @@ cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, in
 
 template <int NC>
 static cudaError_t launch_block_dots_n(const DevMat &W, const int8_t *qx, int32_t *sdot, cudaStream_t s) {
-    const size_t smem = matvec_smem_bytes(W.nbp, NC);
+    const size_t smem = dots_smem_bytes(W.nbp, NC);
     int grid = 0, chunk = 0;
-    cudaError_t e = persistent_grid(k_block_dots<NC>, smem, W.G, &grid, &chunk);
+    cudaError_t e = persistent_grid(k_block_dots<NC>, kThreads, smem, W.G, &grid, &chunk);
     if (e != cudaSuccess) return e;
     k_block_dots<NC><<<grid, kThreads, smem, s>>>(W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx, (int64_t)W.nb * kQK, sdot,
                                                   chunk);
@@ -328,7 +333,7 @@ __device__ void route(const int32_t *__restrict__ ids, int N, int E, Routing &R,
     __syncthreads();
 }
 
-// Slots of expert uniq[u], ascending, into R.slots / R.ns.  All threads.
+// Slots of expert uniq[u], ascending, into R.slots / R.ns.  Consumer threads.
 __device__ void expert_slots(Routing &R, int u, int N) {
     if (threadIdx.x == 0) {
         const int e = R.uniq[u];
@@ -337,24 +342,26 @@ __device__ void expert_slots(Routing &R, int u, int N) {
             if (R.ids[p] == e) R.slots[ns++] = p;
         R.ns = ns;
     }
-    __syncthreads();
+    consumer_sync();
 }
 
-// gate (warps 0-3) and up (warps 4-7) rows of one 32-row-pair group, then the
-// SwiGLU split and the requantization of the 32 outputs, per column.  NC is 1
-// (exact) or kMaxCols, with columns nc..NC-1 reading the zero column staged
-// after the tokens and their results dropped.
+// Number of slots of expert uniq[u] (any thread, from the routing table).
+__device__ __forceinline__ int expert_ns(const Routing &R, int u, int N) {
+    const int e = R.uniq[u];
+    int ns = 0;
+    for (int p = 0; p < N; ++p) ns += R.ids[p] == e;
+    return ns;
+}
+
+__device__ __forceinline__ int col_chunks(int ns) { return (ns + kMaxCols - 1) / kMaxCols; }
+
+// Gate rows (first pass) and up rows (second pass) of one 32-row-pair group
+// over the whole K, then the SwiGLU split and the requantization of the 32
+// outputs, per column.  NC is 1 (exact) or kMaxCols, with columns nc..NC-1
+// reading the zero column staged after the tokens and their results dropped.
 template <int NC>
-__device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R, const SmemLayout &S, int e, int g,
-                                             int c0, int nc) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int half = warp >> 2;  // 0 gate, 1 up
-    const int nbq = A.nbpH / 4;
-    const int q0 = (warp & 3) * nbq / 4, q1 = ((warp & 3) + 1) * nbq / 4;
-    const int Gf = A.L.F / 32;
-    const int grp = g + half * Gf;
-    const uint4 *qs = A.L.gu_qs + (size_t)e * A.L.gu_qs_stride + (size_t)grp * A.nbpH * 32;
-    const uint2 *sc = A.L.gu_sc + (size_t)e * A.L.gu_sc_stride + (size_t)grp * nbq * 32;
+__device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
+                                             int g, int c0, int nc, int warp, int lane) {
     const uint4 *act[NC];
     const float *dxs[NC];
 #pragma unroll
@@ -363,20 +370,26 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
         act[c] = S.act + (size_t)tok * A.nbpH * 2;
         dxs[c] = S.dx + (size_t)tok * A.nbpH;
     }
-    float acc[NC];
+    float accg[NC], accu[NC];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
-    warp_rows_dot<NC>(qs, sc, q0, q1, act, dxs, acc, lane);
+    for (int c = 0; c < NC; ++c) accg[c] = accu[c] = 0.0f;
+    co.group<NC>(S.pipe, A.nbpH, act, dxs, accg, warp, lane);
+    co.group<NC>(S.pipe, A.nbpH, act, dxs, accu, warp, lane);
+    float *pg = S.part;
+    float *pu = S.part + kConsumerWarps * kMaxCols * 32;
 #pragma unroll
-    for (int c = 0; c < NC; ++c) S.part[(warp * NC + c) * 32 + lane] = acc[c];
-    __syncthreads();
+    for (int c = 0; c < NC; ++c) {
+        pg[(warp * kMaxCols + c) * 32 + lane] = accg[c];
+        pu[(warp * kMaxCols + c) * 32 + lane] = accu[c];
+    }
+    consumer_sync();
     if (warp < nc) {
         const int c = warp;
         float gs = 0.0f, us = 0.0f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            gs += S.part[(w * NC + c) * 32 + lane];
-            us += S.part[((w + 4) * NC + c) * 32 + lane];
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            gs += pg[(w * kMaxCols + c) * 32 + lane];
+            us += pu[(w * kMaxCols + c) * 32 + lane];
         }
         const float a = A.swiglu ? gs / (1.0f + expf(-gs)) * us : gs * us;
         float d;
@@ -387,11 +400,14 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
         if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
         if (A.ws.keep_a) A.ws.a_dbg[o] = a;
     }
-    __syncthreads();
+    consumer_sync();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_moe_gate_up(MoeArgs A) {
-    extern __shared__ __align__(16) unsigned char smem[];
+// Items are (expert rank u, 32-row-pair group g), u-major, one contiguous
+// range per CTA.  The producer streams, per item and column chunk, the gate
+// group g then the up group g + F/32 of expert uniq[u].
+__global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
     const int N = A.n_tok * A.k;
     route(A.ids, N, A.L.E, R, blockIdx.x == 0);
@@ -400,7 +416,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_gate_up(MoeArgs A) {
     const int chunk = (total + gridDim.x - 1) / gridDim.x;
     const int i0 = blockIdx.x * chunk, i1 = min(total, i0 + chunk);
     if (i0 >= i1) return;
-    const SmemLayout S = carve(smem, A.n_tok + 1, A.nbpH);
+    const PipeSmem S = carve_pipe(smem, kStages, A.n_tok + 1, A.nbpH);
+    pipe_init(S.pipe);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbq = A.nbpH / 4;
+    if (warp == kConsumerWarps) {  // producer
+        if (lane == 0) {
+            Producer pr;
+            for (int it = i0; it < i1; ++it) {
+                const int u = it / Gf, g = it - u * Gf;
+                const size_t e = (size_t)R.uniq[u];
+                const int nch = col_chunks(expert_ns(R, u, N));
+                for (int ch = 0; ch < nch; ++ch) {
+                    for (int half = 0; half < 2; ++half) {
+                        const size_t grp = (size_t)g + (size_t)half * Gf;
+                        pr.group(S.pipe, A.L.gu_qs + e * A.L.gu_qs_stride + grp * A.nbpH * 32,
+                                 A.L.gu_sc + e * A.L.gu_sc_stride + grp * nbq * 32, A.nbpH);
+                    }
+                }
+            }
+            pr.drain(S.pipe);
+        }
+        return;
+    }
     {
         const int8_t *src[kMaxCols + 1];
         const float *dsrc[kMaxCols + 1];
@@ -408,38 +447,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_gate_up(MoeArgs A) {
             src[t] = t < A.n_tok ? A.ws.qh + (size_t)t * A.L.H : nullptr;
             dsrc[t] = t < A.n_tok ? A.ws.dh + (size_t)t * A.nbH : A.ws.dh;
         }
-        stage_cols(src, dsrc, A.n_tok + 1, A.nbH, A.nbpH, S.act, S.dx);
+        stage_cols(src, dsrc, A.n_tok + 1, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
     }
+    Consumer co;
     int cur_u = -1;
     for (int it = i0; it < i1; ++it) {
         const int u = it / Gf, g = it - u * Gf;
         if (u != cur_u) {
-            __syncthreads();
+            consumer_sync();
             expert_slots(R, u, N);
             cur_u = u;
         }
-        __syncthreads();
-        const int e = R.uniq[u];
         for (int c0 = 0; c0 < R.ns; c0 += kMaxCols) {
             const int nc = min(kMaxCols, R.ns - c0);
             if (nc == 1)
-                gate_up_item<1>(A, R, S, e, g, c0, 1);
+                gate_up_item<1>(A, R, S, co, g, c0, 1, warp, lane);
             else
-                gate_up_item<kMaxCols>(A, R, S, e, g, c0, nc);
+                gate_up_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane);
         }
     }
 }
 
-// down rows of one 32-row group for the columns staged in S (slots
+// Down rows of one 32-row group for the columns staged in S (slots
 // R.slots[c0..c0+nc), zero columns after them), written per slot to obuf.
 template <int NC>
-__device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, const SmemLayout &S, int e, int g,
-                                          int c0, int nc) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nbq = A.nbpF / 4;
-    const int q0 = warp * nbq / kWarps, q1 = (warp + 1) * nbq / kWarps;
-    const uint4 *qs = A.L.dn_qs + (size_t)e * A.L.dn_qs_stride + (size_t)g * A.nbpF * 32;
-    const uint2 *sc = A.L.dn_sc + (size_t)e * A.L.dn_sc_stride + (size_t)g * nbq * 32;
+__device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
+                                          int g, int c0, int nc, int warp, int lane) {
     const uint4 *act[NC];
     const float *dxs[NC];
 #pragma unroll
@@ -450,22 +483,22 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, co
     float acc[NC];
 #pragma unroll
     for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
-    warp_rows_dot<NC>(qs, sc, q0, q1, act, dxs, acc, lane);
+    co.group<NC>(S.pipe, A.nbpF, act, dxs, acc, warp, lane);
 #pragma unroll
-    for (int c = 0; c < NC; ++c) S.part[(warp * NC + c) * 32 + lane] = acc[c];
-    __syncthreads();
+    for (int c = 0; c < NC; ++c) S.part[(warp * kMaxCols + c) * 32 + lane] = acc[c];
+    consumer_sync();
     if (warp < nc) {
         float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += S.part[(w * NC + warp) * 32 + lane];
+        for (int w = 0; w < kConsumerWarps; ++w) v += S.part[(w * kMaxCols + warp) * 32 + lane];
         const int p = R.slots[c0 + warp];
         A.ws.obuf[(size_t)p * A.L.H + (size_t)g * 32 + lane] = v;
     }
-    __syncthreads();
+    consumer_sync();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_moe_down(MoeArgs A) {
-    extern __shared__ __align__(16) unsigned char smem[];
+__global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
     const int N = A.n_tok * A.k;
     route(A.ids, N, A.L.E, R, false);
@@ -479,21 +512,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down(MoeArgs A) {
     const int chunk = (total + gridDim.x - 1) / gridDim.x;
     const int i0 = blockIdx.x * chunk, i1 = min(total, i0 + chunk);
     if (i0 >= i1) return;
-    const SmemLayout S = carve(smem, kMaxCols, A.nbpF);
+    const PipeSmem S = carve_pipe(smem, kStages, kMaxCols, A.nbpF);
+    pipe_init(S.pipe);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbq = A.nbpF / 4;
+    if (warp == kConsumerWarps) {  // producer
+        if (lane == 0) {
+            Producer pr;
+            for (int it = i0; it < i1; ++it) {
+                const int u = it / Gd, g = it - u * Gd;
+                const size_t e = (size_t)R.uniq[u];
+                const int nch = col_chunks(expert_ns(R, u, N));
+                for (int ch = 0; ch < nch; ++ch)
+                    pr.group(S.pipe, A.L.dn_qs + e * A.L.dn_qs_stride + (size_t)g * A.nbpF * 32,
+                             A.L.dn_sc + e * A.L.dn_sc_stride + (size_t)g * nbq * 32, A.nbpF);
+            }
+            pr.drain(S.pipe);
+        }
+        return;
+    }
+    Consumer co;
     int cur_u = -1;
     for (int it = i0; it < i1; ++it) {
         const int u = it / Gd, g = it - u * Gd;
         if (u != cur_u) {
-            __syncthreads();
+            consumer_sync();
             expert_slots(R, u, N);
             cur_u = u;
         }
-        const int e = R.uniq[u];
         for (int c0 = 0; c0 < R.ns; c0 += kMaxCols) {
             const int nc = min(kMaxCols, R.ns - c0);
-            // (re)stage this chunk's columns when the expert or chunk changed
+            // (re)stage this chunk's columns when the expert or the chunk changed
             if (it == i0 || g == 0 || R.ns > kMaxCols) {
-                __syncthreads();
+                consumer_sync();
                 const int8_t *src[kMaxCols];
                 const float *dsrc[kMaxCols];
                 for (int c = 0; c < kMaxCols; ++c) {
@@ -501,28 +553,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_down(MoeArgs A) {
                     src[c] = c < nc ? A.ws.qa + (size_t)p * A.L.F : nullptr;
                     dsrc[c] = A.ws.da + (size_t)p * A.nbF;
                 }
-                stage_cols(src, dsrc, nc == 1 ? 1 : kMaxCols, A.nbF, A.nbpF, S.act, S.dx);
+                stage_cols(src, dsrc, nc == 1 ? 1 : kMaxCols, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers);
+                consumer_sync();
             }
-            __syncthreads();
             if (nc == 1)
-                down_item<1>(A, R, S, e, g, c0, 1);
+                down_item<1>(A, R, S, co, g, c0, 1, warp, lane);
             else
-                down_item<kMaxCols>(A, R, S, e, g, c0, nc);
+                down_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane);
         }
         // Arrival count of row group g; the CTA completing the last of the D
         // experts' items combines y for these rows in slot order.
         __threadfence();
-        __syncthreads();
+        consumer_sync();
         if (threadIdx.x == 0) {
             const unsigned old = atomicAdd(&A.ws.cnt[g], 1u);
             R.last = (old == (unsigned)R.D - 1u);
         }
-        __syncthreads();
+        consumer_sync();
         if (R.last) {
             __threadfence();
-            for (int i = threadIdx.x; i < A.n_tok * 32; i += blockDim.x) {
-                const int t = i >> 5, lane = i & 31;
-                const size_t row = (size_t)g * 32 + lane;
+            for (int i = threadIdx.x; i < A.n_tok * 32; i += kConsumers) {
+                const int t = i >> 5, l = i & 31;
+                const size_t row = (size_t)g * 32 + l;
                 float v = 0.0f;
                 for (int j = 0; j < A.k; ++j) {
                     const int p = t * A.k + j;
@@ -558,21 +610,21 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
     const int64_t max_experts = std::min(n_tok * k, L.E);
     {
-        const size_t smem = matvec_smem_bytes(A.nbpH, n_tok + 1);
+        const size_t smem = pipe_smem_bytes(kStages, n_tok + 1, A.nbpH);
         int grid = 0, chunk = 0;
-        e = persistent_grid(k_moe_gate_up, smem, max_experts * (L.F / 32), &grid, &chunk);
+        e = persistent_grid(k_moe_gate_up, kPipeThreads, smem, max_experts * (L.F / 32), &grid, &chunk);
         if (e != cudaSuccess) return e;
-        k_moe_gate_up<<<grid, kThreads, smem, s>>>(A);
+        k_moe_gate_up<<<grid, kPipeThreads, smem, s>>>(A);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (ws.ev[2] && (e = cudaEventRecord(ws.ev[2], s)) != cudaSuccess) return e;
     {
-        const size_t smem = matvec_smem_bytes(A.nbpF, kMaxCols);
+        const size_t smem = pipe_smem_bytes(kStages, kMaxCols, A.nbpF);
         int grid = 0, chunk = 0;
-        e = persistent_grid(k_moe_down, smem, max_experts * (L.H / 32), &grid, &chunk);
+        e = persistent_grid(k_moe_down, kPipeThreads, smem, max_experts * (L.H / 32), &grid, &chunk);
         if (e != cudaSuccess) return e;
-        k_moe_down<<<grid, kThreads, smem, s>>>(A);
+        k_moe_down<<<grid, kPipeThreads, smem, s>>>(A);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

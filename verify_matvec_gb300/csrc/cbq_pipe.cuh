@@ -1,0 +1,213 @@
+// cbq_pipe.cuh -- the weight-stream pipeline of the matvec kernels.
+//
+// One producer warp per CTA moves the weight stream from HBM into a ring of
+// shared-memory stages with 1-D bulk copies (cp.async.bulk, the TMA's
+// non-tensor form), each stage completing on an mbarrier.  Eight consumer
+// warps wait for a stage, expand and dot it from shared memory, and release it
+// through a second mbarrier.  A stage is one chunk of a 32-row group: up to 32
+// block columns, i.e. 16 KB of index fields plus 2 KB of scales, contiguous in
+// the device layout (cbq_device.cuh), so each stage is two bulk copies.
+//
+// Every wait is bounded: after kSpinLimit polls it sets kErrPipeTimeout in the
+// device error word and a CTA-wide abort flag; the other waits of the CTA
+// then give up too, consumers keep their barrier sequence (so no named
+// barrier is left waiting), and the producer waits for its own copies in
+// flight before the CTA exits.
+#pragma once
+
+#include <stdint.h>
+
+#include "cbq_device.cuh"
+
+namespace cbq {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kPipeThreads = kConsumers + 32;   // + one producer warp
+constexpr int kChunkBlocks = 32;                 // block columns per stage
+constexpr int kStageQsBytes = kChunkBlocks * 512;
+constexpr int kStageBytes = kStageQsBytes + kChunkBlocks / 4 * 256;  // 18,432
+constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr unsigned kErrPipeTimeout = 0x100u;
+
+// The device error word, defined by the translation unit that includes this
+// header (before including it).
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` of transaction on bar.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+// Shared part of the pipeline (carved from dynamic shared memory).
+struct Pipe {
+    uint64_t *full;   // [S] stage filled (producer arrive + bulk bytes)
+    uint64_t *empty;  // [S] stage released (one arrive per consumer warp)
+    int *abort;       // CTA-wide give-up flag
+    unsigned char *ring;
+    int S;
+};
+
+// Bounded wait for phase `parity` of bar.  Returns false on timeout or when
+// the CTA already gave up (check_abort).
+__device__ __forceinline__ bool pipe_wait(const Pipe &P, uint64_t *bar, uint32_t parity, bool check_abort) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (check_abort && (i & 31u) == 31u && *(volatile int *)P.abort) return false;
+    }
+    atomicOr(&g_device_error, kErrPipeTimeout);
+    *(volatile int *)P.abort = 1;
+    return false;
+}
+
+// Producer side: a running count of issued stages.
+struct Producer {
+    uint32_t it = 0;
+    bool stopped = false;
+
+    // Issue the stages of one 32-row group pass (blocks [0, nbp)).
+    __device__ __forceinline__ void group(const Pipe &P, const uint4 *qs_g, const uint2 *sc_g, int nbp) {
+        for (int b0 = 0; b0 < nbp && !stopped; b0 += kChunkBlocks) {
+            const int nblk = min(kChunkBlocks, nbp - b0);
+            const uint32_t slot = it % P.S, use = it / P.S;
+            if (use > 0 && !pipe_wait(P, P.empty + slot, (use - 1) & 1u, true)) {
+                stopped = true;
+                break;
+            }
+            unsigned char *dst = P.ring + (size_t)slot * kStageBytes;
+            const uint32_t bq = (uint32_t)nblk * 512u, bs = (uint32_t)nblk / 4u * 256u;
+            mbar_expect_tx(P.full + slot, bq + bs);
+            bulk_g2s(dst, qs_g + (size_t)b0 * 32, bq, P.full + slot);
+            bulk_g2s(dst + kStageQsBytes, sc_g + (size_t)(b0 / 4) * 32, bs, P.full + slot);
+            ++it;
+        }
+    }
+
+    // Wait for the copies still in flight (the last S issued stages) so the
+    // CTA never exits while the TMA writes into its shared memory.
+    __device__ __forceinline__ void drain(const Pipe &P) {
+        const uint32_t first = it > (uint32_t)P.S ? it - P.S : 0u;
+        for (uint32_t k = first; k < it; ++k) pipe_wait(P, P.full + (k % P.S), (k / P.S) & 1u, false);
+    }
+};
+
+// Consumer side: the same running count, advanced in lock step.
+struct Consumer {
+    uint32_t it = 0;
+
+    // Accumulate one 32-row group pass (blocks [0, nbp)) into acc.
+    template <int NC>
+    __device__ __forceinline__ void group(const Pipe &P, int nbp, const uint4 *const *act, const float *const *dxs,
+                                          float acc[NC], int warp, int lane) {
+        for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
+            const int nq = min(kChunkBlocks, nbp - b0) / 4;
+            const uint32_t slot = it % P.S, use = it / P.S;
+            const bool ok = pipe_wait(P, P.full + slot, use & 1u, true);
+            if (ok) {
+                const unsigned char *st = P.ring + (size_t)slot * kStageBytes;
+                const uint4 *qs_s = reinterpret_cast<const uint4 *>(st);
+                const uint2 *sc_s = reinterpret_cast<const uint2 *>(st + kStageQsBytes);
+                const int q0 = warp * nq / kConsumerWarps, q1 = (warp + 1) * nq / kConsumerWarps;
+                for (int q = q0; q < q1; ++q) {
+                    const uint2 s = sc_s[q * 32 + lane];
+                    const float dw[4] = {half_lo(s.x), half_hi(s.x), half_lo(s.y), half_hi(s.y)};
+                    uint4 w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) w[j] = qs_s[(q * 4 + j) * 32 + lane];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int b = b0 + q * 4 + j;
+                        int sd[NC];
+                        block_dots<NC>(w[j], act, b, sd);
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) {
+                            const float sf = __int_as_float(sd[c]) - kMagic;
+                            acc[c] = fmaf(dw[j] * dxs[c][b], sf, acc[c]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(P.empty + slot);
+            ++it;
+        }
+    }
+};
+
+// Dynamic shared memory of a pipelined kernel:
+//   [full S][empty S][abort] | ring S x kStageBytes | act ncols x nbp x 32 | dx | part
+struct PipeSmem {
+    Pipe pipe;
+    uint4 *act;
+    float *dx;
+    float *part;  // 2 x kConsumerWarps x kMaxCols x 32 (two partial sets)
+};
+
+__host__ __device__ inline size_t pipe_header_bytes(int S) { return ((size_t)16 * S + 4 + 127) / 128 * 128; }
+
+__host__ __device__ inline size_t pipe_smem_bytes(int S, int ncols, int nbp) {
+    return pipe_header_bytes(S) + (size_t)S * kStageBytes + (size_t)ncols * nbp * 36 +
+           (size_t)2 * kConsumerWarps * kMaxCols * 32 * 4;
+}
+
+__device__ __forceinline__ PipeSmem carve_pipe(unsigned char *smem, int S, int ncols, int nbp) {
+    PipeSmem L;
+    L.pipe.full = reinterpret_cast<uint64_t *>(smem);
+    L.pipe.empty = L.pipe.full + S;
+    L.pipe.abort = reinterpret_cast<int *>(L.pipe.empty + S);
+    L.pipe.ring = smem + pipe_header_bytes(S);
+    L.pipe.S = S;
+    L.act = reinterpret_cast<uint4 *>(L.pipe.ring + (size_t)S * kStageBytes);
+    L.dx = reinterpret_cast<float *>(L.act + (size_t)ncols * nbp * 2);
+    L.part = L.dx + (size_t)ncols * nbp;
+    return L;
+}
+
+// Thread 0 initialises the barriers; all threads must then __syncthreads().
+__device__ __forceinline__ void pipe_init(const Pipe &P) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P.S; ++s) {
+            mbar_init(P.full + s, 1);
+            mbar_init(P.empty + s, kConsumerWarps);
+        }
+        *P.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+}
+
+}  // namespace cbq
