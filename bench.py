@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--profile", action="store_true",
+                    help="time the main loop only (no e2e, per-layer or oracle legs); for profiler runs")
+    ap.add_argument("--experts", type=int, default=E,
+                    help="experts in the layer (default 256); smaller layers keep profiler captures small")
     return ap.parse_args()
 
 
@@ -71,10 +75,10 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def routing_sets(seed_base=synth.S_IDS + 100):
+def routing_sets(seed_base=synth.S_IDS + 100, n_exp=E):
     sets = []
     for i in range(N_SETS):
-        ids, wts = synth.router(N_TOK, TOPK, E, stream=seed_base + i)
+        ids, wts = synth.router(N_TOK, TOPK, n_exp, stream=seed_base + i)
         h = synth.activations(N_TOK, H, stream=synth.S_H + 100 + i)
         x = synth.activations(HEAD_N, HEAD_K, stream=synth.S_HEAD_X + 100 + i)
         sets.append((ids, wts, h, x))
@@ -201,13 +205,13 @@ def gpu_ident(torch, local):
         return parts[local] if local < len(parts) else local
 
 
-def build_layer(torch, cbq):
-    """All 256 experts drawn from their seeded streams, repacked on device."""
-    gu = np.empty((E, 2 * F, H // QK, BB), dtype=np.uint8)
-    dn = np.empty((E, H, F // QK, BB), dtype=np.uint8)
-    synth.expert_blocks(E, 2 * F, H, stream=synth.S_GATE_UP, out=gu)
-    synth.expert_blocks(E, H, F, stream=synth.S_DOWN, out=dn)
-    L = cbq.Moe(gu, dn, E, H, F)
+def build_layer(torch, cbq, n_exp=E):
+    """All experts drawn from their seeded streams, repacked on device."""
+    gu = np.empty((n_exp, 2 * F, H // QK, BB), dtype=np.uint8)
+    dn = np.empty((n_exp, H, F // QK, BB), dtype=np.uint8)
+    synth.expert_blocks(n_exp, 2 * F, H, stream=synth.S_GATE_UP, out=gu)
+    synth.expert_blocks(n_exp, H, F, stream=synth.S_DOWN, out=dn)
+    L = cbq.Moe(gu, dn, n_exp, H, F)
     del gu, dn
     head = cbq.Weights(synth.weight_blocks(HEAD_M, HEAD_K, stream=synth.S_HEAD), HEAD_M, HEAD_K)
     return L, head
@@ -232,12 +236,13 @@ def run_gpu(args):
     build.build()  # no-op once built; each rank loads the same in-tree library
     cbq.load()
 
-    L, head = build_layer(torch, cbq)
-    sets = routing_sets()
+    n_exp = args.experts
+    L, head = build_layer(torch, cbq, n_exp)
+    sets = routing_sets(n_exp=n_exp)
     d_sets = []
     for ids, wts, h, x in sets:
         d_sets.append(tuple(torch.from_numpy(a).to(dev) for a in (ids, wts, h, x)))
-    distinct = [len(synth.distinct_experts(s[0], E)) for s in sets]
+    distinct = [len(synth.distinct_experts(s[0], n_exp)) for s in sets]
     y = torch.empty((N_TOK, H), dtype=torch.float32, device=dev)
     yh = torch.empty((HEAD_N, HEAD_M), dtype=torch.float32, device=dev)
     qx = torch.empty((HEAD_N, HEAD_K), dtype=torch.int8, device=dev)
@@ -302,6 +307,17 @@ def run_gpu(args):
     dom_ms, dom_bytes = kern[dom][0] / len(timed), kern[dom][1]
     peak, peak_kind = peaks()
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"profile": True, "ms_per_step": ms / args.steps, "experts": n_exp,
+                              "kernels_ms_per_step": {"k_moe_gate_up": sum(k_gate) / len(timed),
+                                                      "k_moe_down": sum(k_down) / len(timed),
+                                                      "head": sum(k_head) / len(timed)},
+                              "device_error": err}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     # end to end through the host-buffer entry points (pinned host memory)
     h_sets = []
