@@ -240,7 +240,7 @@ int cbq_matvec(const cbq_weights *W, const float *x_dev, int n, float *y_dev, vo
     CBQ_CUDA(scope.status());
     cudaStream_t s = as_stream(stream);
     CBQ_CUDA(cbq::launch_quantize(x_dev, W->K, n, W->ws_qx, W->ws_dx, s));
-    CBQ_CUDA(cbq::launch_matvec(W->mat, W->ws_qx, W->ws_dx, n, y_dev, s));
+    CBQ_CUDA(cbq::launch_matvec(W->mat, W->ws_qx, W->ws_dx, n, y_dev, s, /*pdl=*/true));
     return CBQ_OK;
 }
 

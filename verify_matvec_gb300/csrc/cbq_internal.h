@@ -50,8 +50,10 @@ constexpr int kMaxSlots = 80;  // CBQ_MAX_TOKENS * CBQ_MAX_TOPK
 
 cudaError_t launch_repack(const uint8_t *src, int64_t M, int nb, uint4 *qs, uint2 *sc, cudaStream_t s);
 cudaError_t launch_quantize(const float *x, int64_t K, int n, int8_t *qx, float *dx, cudaStream_t s);
+// pdl: launch as a programmatic dependent of the previous kernel on the
+// stream (only when that kernel is this library's own quantization).
 cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, int n, float *y,
-                          cudaStream_t s);
+                          cudaStream_t s, bool pdl = false);
 cudaError_t launch_block_dots(const DevMat &W, const int8_t *qx, int n, int32_t *sdot, cudaStream_t s);
 cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n_tok, const int32_t *ids,
                        const float *wts, int k, int swiglu, float *y, cudaStream_t s);

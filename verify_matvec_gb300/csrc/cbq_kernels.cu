@@ -27,6 +27,23 @@ namespace cbq {
 constexpr unsigned kErrBadExpertId = 0x1u;
 constexpr int kStages = 4;  // pipeline depth: 4 x 18 KB per CTA, two CTAs per SM
 
+// Launch with optional programmatic stream serialization (PDL).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_k(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t s, bool pdl,
+                            Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------- repack ------
 
 __global__ void k_repack(const uint8_t *__restrict__ src, int64_t M, int nb, int nbp, uint4 *__restrict__ qs,
@@ -67,6 +84,7 @@ cudaError_t launch_repack(const uint8_t *src, int64_t M, int nb, uint4 *qs, uint
 
 __global__ void k_quantize(const float *__restrict__ x, int64_t total, int8_t *__restrict__ qx,
                            float *__restrict__ dx) {
+    pdl_trigger();
     // total = n*K, a multiple of 32; one lane per value, one warp per block.
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx - (threadIdx.x & 31) < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -116,6 +134,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         }
         return;
     }
+    pdl_wait();  // the activations may come from the kernel launched just before
     {
         const int8_t *src[NC];
         const float *dsrc[NC];
@@ -238,23 +257,24 @@ static cudaError_t persistent_grid(Kernel kern, int threads, size_t smem, int64_
 }
 
 template <int NC>
-static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const float *dx, float *y, cudaStream_t s) {
+static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const float *dx, float *y, cudaStream_t s,
+                                   bool pdl) {
     const size_t smem = matvec_smem_bytes(W.nbp, NC);
     int grid = 0, chunk = 0;
     cudaError_t e = persistent_grid(k_matvec<NC>, kPipeThreads, smem, W.G, &grid, &chunk);
     if (e != cudaSuccess) return e;
-    k_matvec<NC><<<grid, kPipeThreads, smem, s>>>(W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx, dx, (int64_t)W.nb * kQK, y,
-                                              chunk);
-    return cudaGetLastError();
+    return launch_k(k_matvec<NC>, grid, kPipeThreads, smem, s, pdl, W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx, dx,
+                    (int64_t)W.nb * kQK, y, chunk);
 }
 
-cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, int n, float *y, cudaStream_t s) {
+cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, int n, float *y, cudaStream_t s,
+                          bool pdl) {
     switch (n) {
-        case 1: return launch_matvec_n<1>(W, qx, dx, y, s);
-        case 2: return launch_matvec_n<2>(W, qx, dx, y, s);
-        case 3: return launch_matvec_n<3>(W, qx, dx, y, s);
-        case 4: return launch_matvec_n<4>(W, qx, dx, y, s);
-        case 5: return launch_matvec_n<5>(W, qx, dx, y, s);
+        case 1: return launch_matvec_n<1>(W, qx, dx, y, s, pdl);
+        case 2: return launch_matvec_n<2>(W, qx, dx, y, s, pdl);
+        case 3: return launch_matvec_n<3>(W, qx, dx, y, s, pdl);
+        case 4: return launch_matvec_n<4>(W, qx, dx, y, s, pdl);
+        case 5: return launch_matvec_n<5>(W, qx, dx, y, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -409,6 +429,7 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
+    pdl_trigger();
     const int N = A.n_tok * A.k;
     route(A.ids, N, A.L.E, R, blockIdx.x == 0);
     const int Gf = A.L.F / 32;
@@ -440,6 +461,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
         }
         return;
     }
+    pdl_wait();  // the quantized tokens come from the kernel launched just before
     {
         const int8_t *src[kMaxCols + 1];
         const float *dsrc[kMaxCols + 1];
@@ -504,6 +526,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
     route(A.ids, N, A.L.E, R, false);
     const int Gd = A.L.H / 32;
     if (R.D == 0) {  // nothing routed: the output is zero
+        pdl_wait();
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < A.n_tok * A.L.H; i += gridDim.x * blockDim.x)
             A.y[i] = 0.0f;
         return;
@@ -532,6 +555,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
         }
         return;
     }
+    pdl_wait();  // qa/da come from the gate_up kernel launched just before
     Consumer co;
     int cur_u = -1;
     for (int it = i0; it < i1; ++it) {
@@ -562,8 +586,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
                 down_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane);
         }
         // Arrival count of row group g; the CTA completing the last of the D
-        // experts' items combines y for these rows in slot order.
-        __threadfence();
+        // experts' items combines y for these rows in slot order.  The warps
+        // that wrote obuf make their writes visible before the count.
+        if (warp < min(R.ns, kMaxCols)) __threadfence();
         consumer_sync();
         if (threadIdx.x == 0) {
             const unsigned old = atomicAdd(&A.ws.cnt[g], 1u);
@@ -614,8 +639,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
         int grid = 0, chunk = 0;
         e = persistent_grid(k_moe_gate_up, kPipeThreads, smem, max_experts * (L.F / 32), &grid, &chunk);
         if (e != cudaSuccess) return e;
-        k_moe_gate_up<<<grid, kPipeThreads, smem, s>>>(A);
-        e = cudaGetLastError();
+        e = launch_k(k_moe_gate_up, grid, kPipeThreads, smem, s, true, A);
         if (e != cudaSuccess) return e;
     }
     if (ws.ev[2] && (e = cudaEventRecord(ws.ev[2], s)) != cudaSuccess) return e;
@@ -624,8 +648,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
         int grid = 0, chunk = 0;
         e = persistent_grid(k_moe_down, kPipeThreads, smem, max_experts * (L.H / 32), &grid, &chunk);
         if (e != cudaSuccess) return e;
-        k_moe_down<<<grid, kPipeThreads, smem, s>>>(A);
-        e = cudaGetLastError();
+        e = launch_k(k_moe_down, grid, kPipeThreads, smem, s, true, A);
         if (e != cudaSuccess) return e;
     }
     if (ws.ev[3]) e = cudaEventRecord(ws.ev[3], s);
