@@ -21,6 +21,7 @@ struct cbq_weights {
     DevMat mat;
     uint4 *qs;
     uint2 *sc;
+    unsigned *sched; // work counters of the matvec kernel
     int8_t *ws_qx;   // CBQ_MAX_COLS x K
     float *ws_dx;    // CBQ_MAX_COLS x K/32
     float *st_x;     // host-entry staging: CBQ_MAX_COLS x K fp32
@@ -161,6 +162,7 @@ int cbq_weights_destroy(cbq_weights *W) {
     DeviceScope scope(W->device);
     cudaFree(W->qs);
     cudaFree(W->sc);
+    cudaFree(W->sched);
     cudaFree(W->ws_qx);
     cudaFree(W->ws_dx);
     cudaFree(W->st_x);
@@ -189,12 +191,17 @@ int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device, 
     W->K = K;
     if ((rc = dev_alloc(&W->qs, cbq::qs_elems(M, nb), &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->sc, cbq::sc_elems(M, nb), &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->sched, 2, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->ws_qx, (size_t)CBQ_MAX_COLS * K, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->ws_dx, (size_t)CBQ_MAX_COLS * nb, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->st_x, (size_t)CBQ_MAX_COLS * K, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->st_y, (size_t)CBQ_MAX_COLS * M, &W->bytes)) != CBQ_OK) {
         cbq_weights_destroy(W);
         return rc;
+    }
+    if (cudaMemsetAsync(W->sched, 0, 2 * sizeof(unsigned), as_stream(stream)) != cudaSuccess) {
+        cbq_weights_destroy(W);
+        return CBQ_ECUDA;
     }
     rc = repack_into(blocks, M, nb, on_device, W->qs, W->sc, as_stream(stream));
     if (rc != CBQ_OK) {
@@ -207,6 +214,7 @@ int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device, 
     W->mat.nb = nb;
     W->mat.nbp = nbp;
     W->mat.G = (int)((M + 31) / 32);
+    W->mat.sched = W->sched;
     *out = W;
     return CBQ_OK;
 }
@@ -281,6 +289,7 @@ int cbq_moe_destroy(cbq_moe *L) {
     cudaFree(L->ws.a_dbg);
     cudaFree(L->ws.obuf);
     cudaFree(L->ws.cnt);
+    cudaFree(L->ws.sched);
     cudaFree(L->st_h);
     cudaFree(L->st_ids);
     cudaFree(L->st_wts);
@@ -323,6 +332,7 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
         (rc = dev_alloc(&L->ws.a_dbg, slots * F, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.obuf, slots * H, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.cnt, (size_t)(H / 32), &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.sched, 4, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_h, (size_t)CBQ_MAX_TOKENS * H, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_ids, slots, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_wts, slots, &L->bytes)) != CBQ_OK ||
@@ -331,7 +341,8 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
         return rc;
     }
     cudaStream_t s = as_stream(stream);
-    if (cudaMemsetAsync(L->ws.cnt, 0, (size_t)(H / 32) * sizeof(unsigned), s) != cudaSuccess) {
+    if (cudaMemsetAsync(L->ws.cnt, 0, (size_t)(H / 32) * sizeof(unsigned), s) != cudaSuccess ||
+        cudaMemsetAsync(L->ws.sched, 0, 4 * sizeof(unsigned), s) != cudaSuccess) {
         cbq_moe_destroy(L);
         return CBQ_ECUDA;
     }
@@ -423,6 +434,7 @@ int cbq_moe_debug_block_dots(const cbq_moe *L, int e, int which, const int8_t *q
     }
     m.nbp = cbq::round_up4(m.nb);
     m.G = (int)((m.M + 31) / 32);
+    m.sched = nullptr;  // the block-dot kernel uses static ranges
     CBQ_CUDA(cbq::launch_block_dots(m, qx_dev, n, s_dev, as_stream(stream)));
     return CBQ_OK;
 }

@@ -15,6 +15,7 @@ struct DevMat {
     int nb;           // K / 32
     int nbp;          // nb rounded up to a multiple of 4
     int G;            // ceil(M / 32) row groups
+    unsigned *sched;  // 2 work counters of the matvec kernel (zero between launches)
 };
 
 inline int round_up4(int v) { return (v + 3) & ~3; }
@@ -42,6 +43,7 @@ struct MoeWork {
     float *a_dbg;     // slots x F (written when keep_a)
     float *obuf;      // slots x H, down-projection output per slot
     unsigned *cnt;    // H/32 arrival counters (zero between calls)
+    unsigned *sched;  // 4 work counters: gate_up (2), down (2), zero between launches
     int keep_a;
     cudaEvent_t ev[4];  // optional stage events (quant, gate_up, down, end)
 };

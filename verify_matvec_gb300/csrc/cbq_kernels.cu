@@ -111,16 +111,13 @@ size_t matvec_smem_bytes(int nbp, int n) { return pipe_smem_bytes(kStages, n, nb
 // Debug kernel smem: activations + scales only.
 static size_t dots_smem_bytes(int nbp, int n) { return (size_t)n * nbp * 36; }
 
-// Dense MMVQ: 32-row groups [g0, g1) of this CTA, all NC columns per pass.
+// Dense MMVQ: 32-row groups fetched dynamically, all NC columns per pass.
 template <int NC>
 __global__ void __launch_bounds__(kPipeThreads, 2)
     k_matvec(const uint4 *__restrict__ qs, const uint2 *__restrict__ sc, int64_t M, int G, int nb, int nbp,
              const int8_t *__restrict__ qx, const float *__restrict__ dx, int64_t K, float *__restrict__ y,
-             int chunk) {
+             unsigned *__restrict__ sched) {
     extern __shared__ __align__(128) unsigned char smem[];
-    const int g0 = blockIdx.x * chunk;
-    const int g1 = min(G, g0 + chunk);
-    if (g0 >= G) return;
     const PipeSmem S = carve_pipe(smem, kStages, NC, nbp);
     pipe_init(S.pipe);
     __syncthreads();
@@ -129,7 +126,15 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     if (warp == kConsumerWarps) {  // producer
         if (lane == 0) {
             Producer pr;
-            for (int g = g0; g < g1; ++g) pr.group(S.pipe, qs + (size_t)g * nbp * 32, sc + (size_t)g * nbq * 32, nbp);
+            unsigned nxt = atomicAdd(sched, 1u);
+            while (nxt < (unsigned)G && !pr.stopped) {
+                const unsigned g = nxt;
+                nxt = atomicAdd(sched, 1u);
+                pr.group(S.pipe, qs + (size_t)g * nbp * 32, sc + (size_t)g * nbq * 32, nbp, (int)g);
+            }
+            __threadfence();
+            sched_exit(sched);
+            pr.finish(S.pipe);
             pr.drain(S.pipe);
         }
         return;
@@ -154,7 +159,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         dxs[c] = S.dx + (size_t)c * nbp;
     }
     Consumer co;
-    for (int g = g0; g < g1; ++g) {
+    for (;;) {
+        const int g = co.peek(S.pipe);
+        if (g < 0) break;
         float acc[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
@@ -238,7 +245,7 @@ cudaError_t device_smem_limit(size_t *bytes) {
 }
 
 // Grid of a persistent kernel over `items` work items: at most resident
-// capacity, with contiguous equal chunks.
+// capacity, with contiguous equal chunks (also sets the smem attribute).
 template <typename Kernel>
 static cudaError_t persistent_grid(Kernel kern, int threads, size_t smem, int64_t items, int *grid, int *chunk) {
     int sms = 0, per_sm = 0;
@@ -256,15 +263,30 @@ static cudaError_t persistent_grid(Kernel kern, int threads, size_t smem, int64_
     return cudaSuccess;
 }
 
+// Grid of a persistent kernel that fetches its work dynamically: one CTA per
+// resident slot, at most one per item.
+template <typename Kernel>
+static cudaError_t dynamic_grid(Kernel kern, size_t smem, int64_t items, int *grid) {
+    int chunk = 0;
+    cudaError_t e = persistent_grid(kern, kPipeThreads, smem, items, grid, &chunk);
+    if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    e = num_sms(&sms);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPipeThreads, smem);
+    if (e != cudaSuccess) return e;
+    *grid = (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)sms * std::max(per_sm, 1)));
+    return cudaSuccess;
+}
+
 template <int NC>
 static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const float *dx, float *y, cudaStream_t s,
                                    bool pdl) {
     const size_t smem = matvec_smem_bytes(W.nbp, NC);
-    int grid = 0, chunk = 0;
-    cudaError_t e = persistent_grid(k_matvec<NC>, kPipeThreads, smem, W.G, &grid, &chunk);
+    int grid = 0;
+    cudaError_t e = dynamic_grid(k_matvec<NC>, smem, W.G, &grid);
     if (e != cudaSuccess) return e;
     return launch_k(k_matvec<NC>, grid, kPipeThreads, smem, s, pdl, W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx, dx,
-                    (int64_t)W.nb * kQK, y, chunk);
+                    (int64_t)W.nb * kQK, y, W.sched);
 }
 
 cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, int n, float *y, cudaStream_t s,
@@ -423,9 +445,9 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
     consumer_sync();
 }
 
-// Items are (expert rank u, 32-row-pair group g), u-major, one contiguous
-// range per CTA.  The producer streams, per item and column chunk, the gate
-// group g then the up group g + F/32 of expert uniq[u].
+// Items are (expert rank u, 32-row-pair group g), u-major, fetched one at a
+// time.  The producer streams, per item and column chunk, the gate group g
+// then the up group g + F/32 of expert uniq[u].
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
@@ -433,10 +455,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
     const int N = A.n_tok * A.k;
     route(A.ids, N, A.L.E, R, blockIdx.x == 0);
     const int Gf = A.L.F / 32;
-    const int total = R.D * Gf;
-    const int chunk = (total + gridDim.x - 1) / gridDim.x;
-    const int i0 = blockIdx.x * chunk, i1 = min(total, i0 + chunk);
-    if (i0 >= i1) return;
+    const unsigned total = (unsigned)(R.D * Gf);
+    unsigned *sched = A.ws.sched;
     const PipeSmem S = carve_pipe(smem, kStages, A.n_tok + 1, A.nbpH);
     pipe_init(S.pipe);
     __syncthreads();
@@ -445,7 +465,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
     if (warp == kConsumerWarps) {  // producer
         if (lane == 0) {
             Producer pr;
-            for (int it = i0; it < i1; ++it) {
+            unsigned nxt = atomicAdd(sched, 1u);
+            while (nxt < total && !pr.stopped) {
+                const int it = (int)nxt;
+                nxt = atomicAdd(sched, 1u);
                 const int u = it / Gf, g = it - u * Gf;
                 const size_t e = (size_t)R.uniq[u];
                 const int nch = col_chunks(expert_ns(R, u, N));
@@ -453,10 +476,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
                     for (int half = 0; half < 2; ++half) {
                         const size_t grp = (size_t)g + (size_t)half * Gf;
                         pr.group(S.pipe, A.L.gu_qs + e * A.L.gu_qs_stride + grp * A.nbpH * 32,
-                                 A.L.gu_sc + e * A.L.gu_sc_stride + grp * nbq * 32, A.nbpH);
+                                 A.L.gu_sc + e * A.L.gu_sc_stride + grp * nbq * 32, A.nbpH, it);
                     }
                 }
             }
+            __threadfence();
+            sched_exit(sched);
+            pr.finish(S.pipe);
             pr.drain(S.pipe);
         }
         return;
@@ -473,7 +499,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
     }
     Consumer co;
     int cur_u = -1;
-    for (int it = i0; it < i1; ++it) {
+    for (;;) {
+        const int it = co.peek(S.pipe);
+        if (it < 0) break;
         const int u = it / Gf, g = it - u * Gf;
         if (u != cur_u) {
             consumer_sync();
@@ -519,6 +547,11 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, co
     consumer_sync();
 }
 
+// Items are (expert rank u, 32-row group g), u-major, fetched kDownGrab at a
+// time so that consecutive items of a CTA mostly share their expert (and the
+// staged intermediate columns).
+constexpr int kDownGrab = 4;
+
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
@@ -531,10 +564,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
             A.y[i] = 0.0f;
         return;
     }
-    const int total = R.D * Gd;
-    const int chunk = (total + gridDim.x - 1) / gridDim.x;
-    const int i0 = blockIdx.x * chunk, i1 = min(total, i0 + chunk);
-    if (i0 >= i1) return;
+    const unsigned total = (unsigned)(R.D * Gd);
+    unsigned *sched = A.ws.sched + 2;
     const PipeSmem S = carve_pipe(smem, kStages, kMaxCols, A.nbpF);
     pipe_init(S.pipe);
     __syncthreads();
@@ -543,22 +574,32 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
     if (warp == kConsumerWarps) {  // producer
         if (lane == 0) {
             Producer pr;
-            for (int it = i0; it < i1; ++it) {
-                const int u = it / Gd, g = it - u * Gd;
-                const size_t e = (size_t)R.uniq[u];
-                const int nch = col_chunks(expert_ns(R, u, N));
-                for (int ch = 0; ch < nch; ++ch)
-                    pr.group(S.pipe, A.L.dn_qs + e * A.L.dn_qs_stride + (size_t)g * A.nbpF * 32,
-                             A.L.dn_sc + e * A.L.dn_sc_stride + (size_t)g * nbq * 32, A.nbpF);
+            unsigned nxt = atomicAdd(sched, (unsigned)kDownGrab);
+            while (nxt < total && !pr.stopped) {
+                const unsigned base = nxt;
+                nxt = atomicAdd(sched, (unsigned)kDownGrab);
+                for (unsigned it = base; it < min(total, base + kDownGrab) && !pr.stopped; ++it) {
+                    const int u = (int)it / Gd, g = (int)it - u * Gd;
+                    const size_t e = (size_t)R.uniq[u];
+                    const int nch = col_chunks(expert_ns(R, u, N));
+                    for (int ch = 0; ch < nch; ++ch)
+                        pr.group(S.pipe, A.L.dn_qs + e * A.L.dn_qs_stride + (size_t)g * A.nbpF * 32,
+                                 A.L.dn_sc + e * A.L.dn_sc_stride + (size_t)g * nbq * 32, A.nbpF, (int)it);
+                }
             }
+            __threadfence();
+            sched_exit(sched);
+            pr.finish(S.pipe);
             pr.drain(S.pipe);
         }
         return;
     }
     pdl_wait();  // qa/da come from the gate_up kernel launched just before
     Consumer co;
-    int cur_u = -1;
-    for (int it = i0; it < i1; ++it) {
+    int cur_u = -1, staged_u = -1;
+    for (;;) {
+        const int it = co.peek(S.pipe);
+        if (it < 0) break;
         const int u = it / Gd, g = it - u * Gd;
         if (u != cur_u) {
             consumer_sync();
@@ -568,7 +609,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
         for (int c0 = 0; c0 < R.ns; c0 += kMaxCols) {
             const int nc = min(kMaxCols, R.ns - c0);
             // (re)stage this chunk's columns when the expert or the chunk changed
-            if (it == i0 || g == 0 || R.ns > kMaxCols) {
+            if (staged_u != u || R.ns > kMaxCols) {
                 consumer_sync();
                 const int8_t *src[kMaxCols];
                 const float *dsrc[kMaxCols];
@@ -579,6 +620,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
                 }
                 stage_cols(src, dsrc, nc == 1 ? 1 : kMaxCols, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers);
                 consumer_sync();
+                staged_u = u;
             }
             if (nc == 1)
                 down_item<1>(A, R, S, co, g, c0, 1, warp, lane);
@@ -636,8 +678,8 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     const int64_t max_experts = std::min(n_tok * k, L.E);
     {
         const size_t smem = pipe_smem_bytes(kStages, n_tok + 1, A.nbpH);
-        int grid = 0, chunk = 0;
-        e = persistent_grid(k_moe_gate_up, kPipeThreads, smem, max_experts * (L.F / 32), &grid, &chunk);
+        int grid = 0;
+        e = dynamic_grid(k_moe_gate_up, smem, max_experts * (L.F / 32), &grid);
         if (e != cudaSuccess) return e;
         e = launch_k(k_moe_gate_up, grid, kPipeThreads, smem, s, true, A);
         if (e != cudaSuccess) return e;
@@ -645,8 +687,8 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     if (ws.ev[2] && (e = cudaEventRecord(ws.ev[2], s)) != cudaSuccess) return e;
     {
         const size_t smem = pipe_smem_bytes(kStages, kMaxCols, A.nbpF);
-        int grid = 0, chunk = 0;
-        e = persistent_grid(k_moe_down, kPipeThreads, smem, max_experts * (L.H / 32), &grid, &chunk);
+        int grid = 0;
+        e = dynamic_grid(k_moe_down, smem, max_experts * (L.H / 32) / kDownGrab + 1, &grid);
         if (e != cudaSuccess) return e;
         e = launch_k(k_moe_down, grid, kPipeThreads, smem, s, true, A);
         if (e != cudaSuccess) return e;

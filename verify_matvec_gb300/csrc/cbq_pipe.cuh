@@ -8,6 +8,12 @@
 // block columns, i.e. 16 KB of index fields plus 2 KB of scales, contiguous in
 // the device layout (cbq_device.cuh), so each stage is two bulk copies.
 //
+// Work is fetched dynamically: the producer takes item indices from a global
+// counter with atomicAdd (the last CTA to exit resets it), tags every stage
+// with its item in a small shared header, and closes the stream with a stage
+// tagged -1 that carries no bytes.  Consumers read the tag at each item
+// boundary, so CTAs of unequal speed share the work evenly.
+//
 // Every wait is bounded: after kSpinLimit polls it sets kErrPipeTimeout in the
 // device error word and a CTA-wide abort flag; the other waits of the CTA
 // then give up too, consumers keep their barrier sequence (so no named
@@ -79,6 +85,7 @@ struct Pipe {
     uint64_t *full;   // [S] stage filled (producer arrive + bulk bytes)
     uint64_t *empty;  // [S] stage released (one arrive per consumer warp)
     int *abort;       // CTA-wide give-up flag
+    int *tag;         // [S] item of each stage (-1: end of stream)
     unsigned char *ring;
     int S;
 };
@@ -100,22 +107,43 @@ struct Producer {
     uint32_t it = 0;
     bool stopped = false;
 
-    // Issue the stages of one 32-row group pass (blocks [0, nbp)).
-    __device__ __forceinline__ void group(const Pipe &P, const uint4 *qs_g, const uint2 *sc_g, int nbp) {
+    // Claim the next slot (waiting until the consumers released it).
+    __device__ __forceinline__ bool claim(const Pipe &P, uint32_t &slot) {
+        slot = it % P.S;
+        const uint32_t use = it / P.S;
+        if (stopped || (use > 0 && !pipe_wait(P, P.empty + slot, (use - 1) & 1u, true))) {
+            stopped = true;
+            return false;
+        }
+        return true;
+    }
+
+    // Issue the stages of one 32-row group pass (blocks [0, nbp)) of item `tag`.
+    __device__ __forceinline__ void group(const Pipe &P, const uint4 *qs_g, const uint2 *sc_g, int nbp, int tag) {
         for (int b0 = 0; b0 < nbp && !stopped; b0 += kChunkBlocks) {
             const int nblk = min(kChunkBlocks, nbp - b0);
-            const uint32_t slot = it % P.S, use = it / P.S;
-            if (use > 0 && !pipe_wait(P, P.empty + slot, (use - 1) & 1u, true)) {
-                stopped = true;
-                break;
-            }
+            uint32_t slot;
+            if (!claim(P, slot)) break;
             unsigned char *dst = P.ring + (size_t)slot * kStageBytes;
             const uint32_t bq = (uint32_t)nblk * 512u, bs = (uint32_t)nblk / 4u * 256u;
+            P.tag[slot] = tag;
             mbar_expect_tx(P.full + slot, bq + bs);
             bulk_g2s(dst, qs_g + (size_t)b0 * 32, bq, P.full + slot);
             bulk_g2s(dst + kStageQsBytes, sc_g + (size_t)(b0 / 4) * 32, bs, P.full + slot);
             ++it;
         }
+    }
+
+    // End of stream: a stage tagged -1 with no bytes.
+    __device__ __forceinline__ void finish(const Pipe &P) {
+        uint32_t slot;
+        if (!claim(P, slot)) {
+            *(volatile int *)P.abort = 1;  // consumers must not wait for it
+            return;
+        }
+        P.tag[slot] = -1;
+        mbar_arrive(P.full + slot);
+        ++it;
     }
 
     // Wait for the copies still in flight (the last S issued stages) so the
@@ -129,6 +157,14 @@ struct Producer {
 // Consumer side: the same running count, advanced in lock step.
 struct Consumer {
     uint32_t it = 0;
+
+    // Item of the next stage (-1 at the end of the stream or after a give-up),
+    // without consuming the stage.
+    __device__ __forceinline__ int peek(const Pipe &P) const {
+        const uint32_t slot = it % P.S, use = it / P.S;
+        if (!pipe_wait(P, P.full + slot, use & 1u, true)) return -1;
+        return *(volatile int *)(P.tag + slot);
+    }
 
     // Accumulate one 32-row group pass (blocks [0, nbp)) into acc.
     template <int NC>
@@ -178,7 +214,7 @@ struct PipeSmem {
     float *part;  // 2 x kConsumerWarps x kMaxCols x 32 (two partial sets)
 };
 
-__host__ __device__ inline size_t pipe_header_bytes(int S) { return ((size_t)16 * S + 4 + 127) / 128 * 128; }
+__host__ __device__ inline size_t pipe_header_bytes(int S) { return ((size_t)20 * S + 4 + 127) / 128 * 128; }
 
 __host__ __device__ inline size_t pipe_smem_bytes(int S, int ncols, int nbp) {
     return pipe_header_bytes(S) + (size_t)S * kStageBytes + (size_t)ncols * nbp * 36 +
@@ -190,12 +226,23 @@ __device__ __forceinline__ PipeSmem carve_pipe(unsigned char *smem, int S, int n
     L.pipe.full = reinterpret_cast<uint64_t *>(smem);
     L.pipe.empty = L.pipe.full + S;
     L.pipe.abort = reinterpret_cast<int *>(L.pipe.empty + S);
+    L.pipe.tag = L.pipe.abort + 1;
     L.pipe.ring = smem + pipe_header_bytes(S);
     L.pipe.S = S;
     L.act = reinterpret_cast<uint4 *>(L.pipe.ring + (size_t)S * kStageBytes);
     L.dx = reinterpret_cast<float *>(L.act + (size_t)ncols * nbp * 2);
     L.part = L.dx + (size_t)ncols * nbp;
     return L;
+}
+
+// Work counter of a persistent kernel: sched[0] next item, sched[1] CTAs
+// done.  Called once per CTA after its last fetch; the last CTA resets both
+// for the next launch.
+__device__ __forceinline__ void sched_exit(unsigned *sched) {
+    if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+        sched[0] = 0u;
+        sched[1] = 0u;
+    }
 }
 
 // Thread 0 initialises the barriers; all threads must then __syncthreads().
