@@ -359,20 +359,24 @@ def run_gpu(args):
             cbq.cbq_moe_matvec(L, t[2], t[0], t[1], y=yl)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        stage_ev = [[timing_event(torch, stream) for _ in range(4)] for _ in range(reps)]
         torch.cuda.synchronize()
         a.record(stream)
         nbytes = 0
         for i in range(reps):
             t = tabs[i % N_SETS]
+            cbq.cbq_moe_set_stage_events(L, stage_ev[i])
             cbq.cbq_moe_matvec(L, t[2], t[0], t[1], y=yl)
             nbytes += t[3] * EXPERT_BYTES
         b.record(stream)
         torch.cuda.synchronize()
+        cbq.cbq_moe_set_stage_events(L, None)
         us = 1e3 * a.elapsed_time(b) / reps
-        return us, nbytes / reps / (us * 1e-6) / 1e9
+        split = [1e3 * sum(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev) / reps for j in range(3)]
+        return us, nbytes / reps / (us * 1e-6) / 1e9, split
 
-    b1_us, b1_gbs = layer_us(1, 4)
-    b5_us, b5_gbs = layer_us(5, 8)
+    b1_us, b1_gbs, b1_split = layer_us(1, 4)
+    b5_us, b5_gbs, b5_split = layer_us(5, 8)
 
     # slowest rank decides; bytes add up over ranks
     my = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
@@ -406,7 +410,8 @@ def run_gpu(args):
                        "l2": "inputs larger than L2 (~0.8 GB of weights per step, 16 rotating routing tables)",
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": {"batch1_top4": b1_us, "batch5_top8": b5_us,
-                             "batch1_weight_gbs": b1_gbs, "batch5_weight_gbs": b5_gbs},
+                             "batch1_weight_gbs": b1_gbs, "batch5_weight_gbs": b5_gbs,
+                             "split_us_quant_gateup_down": {"batch1": b1_split, "batch5": b5_split}},
             "kernels_ms_per_step": {"quantize(x2)": sum(k_quant) / len(timed),
                                     "k_moe_gate_up": sum(k_gate) / len(timed),
                                     "k_moe_down": sum(k_down) / len(timed),

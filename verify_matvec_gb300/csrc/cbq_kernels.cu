@@ -25,7 +25,12 @@ __device__ unsigned int g_device_error;  // CBQ_DEVERR_* bits
 namespace cbq {
 
 constexpr unsigned kErrBadExpertId = 0x1u;
-constexpr int kStages = 4;  // pipeline depth: 4 x 18 KB per CTA, two CTAs per SM
+// Pipeline depth (stages of 18 KB per CTA, two CTAs per SM) and partial-sum
+// sets of each kernel, sized so two CTAs fit in an SM's shared memory.
+constexpr int kStages = 4;
+constexpr int kStagesGateUp = 3;
+constexpr int kSetsMatvec = 2;   // double-buffered
+constexpr int kSetsGateUp = 4;   // gate + up, double-buffered
 
 // Launch with optional programmatic stream serialization (PDL).
 template <typename... KArgs, typename... Args>
@@ -106,7 +111,7 @@ cudaError_t launch_quantize(const float *x, int64_t K, int n, int8_t *qx, float 
 
 // ---------------------------------------------------------- dense MMVQ -----
 
-size_t matvec_smem_bytes(int nbp, int n) { return pipe_smem_bytes(kStages, n, nbp); }
+size_t matvec_smem_bytes(int nbp, int n) { return pipe_smem_bytes(kStages, n, nbp, kSetsMatvec); }
 
 // Debug kernel smem: activations + scales only.
 static size_t dots_smem_bytes(int nbp, int n) { return (size_t)n * nbp * 36; }
@@ -159,24 +164,24 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         dxs[c] = S.dx + (size_t)c * nbp;
     }
     Consumer co;
-    for (;;) {
+    for (int item = 0;; ++item) {
         const int g = co.peek(S.pipe);
         if (g < 0) break;
         float acc[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
         co.group<NC>(S.pipe, nbp, act, dxs, acc, warp, lane);
+        float *part = S.part + (item & 1) * kPartSet;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) S.part[(warp * NC + c) * 32 + lane] = acc[c];
+        for (int c = 0; c < NC; ++c) part[(warp * NC + c) * 32 + lane] = acc[c];
         consumer_sync();
         if (warp < NC) {
             float v = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) v += S.part[(w * NC + warp) * 32 + lane];
+            for (int w = 0; w < kConsumerWarps; ++w) v += part[(w * NC + warp) * 32 + lane];
             const int64_t row = (int64_t)g * 32 + lane;
             if (row < M) y[(size_t)warp * M + row] = v;
         }
-        consumer_sync();
     }
 }
 
@@ -344,7 +349,6 @@ struct Routing {
     int slots[kMaxSlots];  // slots of the current expert, ascending
     int D;
     int ns;
-    int last;
 };
 
 __device__ void route(const int32_t *__restrict__ ids, int N, int E, Routing &R, bool report) {
@@ -403,7 +407,7 @@ __device__ __forceinline__ int col_chunks(int ns) { return (ns + kMaxCols - 1) /
 // reading the zero column staged after the tokens and their results dropped.
 template <int NC>
 __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
-                                             int g, int c0, int nc, int warp, int lane) {
+                                             int g, int c0, int nc, int warp, int lane, int buf) {
     const uint4 *act[NC];
     const float *dxs[NC];
 #pragma unroll
@@ -417,8 +421,8 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
     for (int c = 0; c < NC; ++c) accg[c] = accu[c] = 0.0f;
     co.group<NC>(S.pipe, A.nbpH, act, dxs, accg, warp, lane);
     co.group<NC>(S.pipe, A.nbpH, act, dxs, accu, warp, lane);
-    float *pg = S.part;
-    float *pu = S.part + kConsumerWarps * kMaxCols * 32;
+    float *pg = S.part + (2 * buf) * kPartSet;
+    float *pu = S.part + (2 * buf + 1) * kPartSet;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         pg[(warp * kMaxCols + c) * 32 + lane] = accg[c];
@@ -442,7 +446,6 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
         if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
         if (A.ws.keep_a) A.ws.a_dbg[o] = a;
     }
-    consumer_sync();
 }
 
 // Items are (expert rank u, 32-row-pair group g), u-major, fetched one at a
@@ -457,7 +460,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
     const int Gf = A.L.F / 32;
     const unsigned total = (unsigned)(R.D * Gf);
     unsigned *sched = A.ws.sched;
-    const PipeSmem S = carve_pipe(smem, kStages, A.n_tok + 1, A.nbpH);
+    const PipeSmem S = carve_pipe(smem, kStagesGateUp, A.n_tok + 1, A.nbpH);
     pipe_init(S.pipe);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -498,7 +501,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
         stage_cols(src, dsrc, A.n_tok + 1, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
     }
     Consumer co;
-    int cur_u = -1;
+    int cur_u = -1, item = 0;
     for (;;) {
         const int it = co.peek(S.pipe);
         if (it < 0) break;
@@ -508,21 +511,23 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
             expert_slots(R, u, N);
             cur_u = u;
         }
-        for (int c0 = 0; c0 < R.ns; c0 += kMaxCols) {
+        for (int c0 = 0; c0 < R.ns; c0 += kMaxCols, ++item) {
             const int nc = min(kMaxCols, R.ns - c0);
             if (nc == 1)
-                gate_up_item<1>(A, R, S, co, g, c0, 1, warp, lane);
+                gate_up_item<1>(A, R, S, co, g, c0, 1, warp, lane, item & 1);
             else
-                gate_up_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane);
+                gate_up_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane, item & 1);
         }
     }
 }
 
 // Down rows of one 32-row group for the columns staged in S (slots
-// R.slots[c0..c0+nc), zero columns after them), written per slot to obuf.
+// R.slots[c0..c0+nc), zero columns after them), written per slot to obuf by
+// warps 0..nc-1.  Returns after one CTA barrier; the writer warps then finish
+// the item alone (down_arrive).
 template <int NC>
 __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
-                                          int g, int c0, int nc, int warp, int lane) {
+                                          int g, int c0, int nc, int warp, int lane, int buf) {
     const uint4 *act[NC];
     const float *dxs[NC];
 #pragma unroll
@@ -534,23 +539,51 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, co
 #pragma unroll
     for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
     co.group<NC>(S.pipe, A.nbpF, act, dxs, acc, warp, lane);
+    float *part = S.part + buf * kPartSet;
 #pragma unroll
-    for (int c = 0; c < NC; ++c) S.part[(warp * kMaxCols + c) * 32 + lane] = acc[c];
+    for (int c = 0; c < NC; ++c) part[(warp * kMaxCols + c) * 32 + lane] = acc[c];
     consumer_sync();
     if (warp < nc) {
         float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) v += S.part[(w * kMaxCols + warp) * 32 + lane];
+        for (int w = 0; w < kConsumerWarps; ++w) v += part[(w * kMaxCols + warp) * 32 + lane];
         const int p = R.slots[c0 + warp];
         A.ws.obuf[(size_t)p * A.L.H + (size_t)g * 32 + lane] = v;
     }
-    consumer_sync();
+}
+
+// Arrival of one (expert, row group) item, by the writer warps 0..nw-1 only:
+// they make their obuf writes visible, warp 0 counts the arrival, and the
+// arrival that completes the D experts of row group g combines y for its 32
+// rows in slot order and resets the count.
+__device__ __forceinline__ void down_arrive(const MoeArgs &A, const Routing &R, int g, int nw, int warp,
+                                            int lane) {
+    if (warp >= nw) return;
+    __threadfence();
+    if (nw > 1) asm volatile("bar.sync 2, %0;" ::"r"(nw * 32) : "memory");
+    if (warp != 0) return;
+    unsigned old = 0;
+    if (lane == 0) old = atomicAdd(&A.ws.cnt[g], 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != (unsigned)R.D - 1u) return;
+    __threadfence();
+    const size_t row = (size_t)g * 32 + lane;
+    for (int t = 0; t < A.n_tok; ++t) {
+        float v = 0.0f;
+        for (int j = 0; j < A.k; ++j) {
+            const int p = t * A.k + j;
+            const int id = R.ids[p];
+            if (id >= 0 && id < A.L.E) v += A.wts[p] * __ldcg(A.ws.obuf + (size_t)p * A.L.H + row);
+        }
+        A.y[(size_t)t * A.L.H + row] = v;
+    }
+    if (lane == 0) A.ws.cnt[g] = 0u;
 }
 
 // Items are (expert rank u, 32-row group g), u-major, fetched kDownGrab at a
 // time so that consecutive items of a CTA mostly share their expert (and the
 // staged intermediate columns).
-constexpr int kDownGrab = 4;
+constexpr int kDownGrab = 2;
 
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -574,11 +607,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
     if (warp == kConsumerWarps) {  // producer
         if (lane == 0) {
             Producer pr;
-            unsigned nxt = atomicAdd(sched, (unsigned)kDownGrab);
+            // grab kDownGrab items at a time only when there are many per CTA
+            const unsigned grab = total >= 16u * gridDim.x ? (unsigned)kDownGrab : 1u;
+            unsigned nxt = atomicAdd(sched, grab);
             while (nxt < total && !pr.stopped) {
                 const unsigned base = nxt;
-                nxt = atomicAdd(sched, (unsigned)kDownGrab);
-                for (unsigned it = base; it < min(total, base + kDownGrab) && !pr.stopped; ++it) {
+                nxt = atomicAdd(sched, grab);
+                for (unsigned it = base; it < min(total, base + grab) && !pr.stopped; ++it) {
                     const int u = (int)it / Gd, g = (int)it - u * Gd;
                     const size_t e = (size_t)R.uniq[u];
                     const int nch = col_chunks(expert_ns(R, u, N));
@@ -596,7 +631,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
     }
     pdl_wait();  // qa/da come from the gate_up kernel launched just before
     Consumer co;
-    int cur_u = -1, staged_u = -1;
+    int cur_u = -1, staged_u = -1, item = 0;
     for (;;) {
         const int it = co.peek(S.pipe);
         if (it < 0) break;
@@ -623,35 +658,12 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
                 staged_u = u;
             }
             if (nc == 1)
-                down_item<1>(A, R, S, co, g, c0, 1, warp, lane);
+                down_item<1>(A, R, S, co, g, c0, 1, warp, lane, item & 1);
             else
-                down_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane);
+                down_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane, item & 1);
+            ++item;
         }
-        // Arrival count of row group g; the CTA completing the last of the D
-        // experts' items combines y for these rows in slot order.  The warps
-        // that wrote obuf make their writes visible before the count.
-        if (warp < min(R.ns, kMaxCols)) __threadfence();
-        consumer_sync();
-        if (threadIdx.x == 0) {
-            const unsigned old = atomicAdd(&A.ws.cnt[g], 1u);
-            R.last = (old == (unsigned)R.D - 1u);
-        }
-        consumer_sync();
-        if (R.last) {
-            __threadfence();
-            for (int i = threadIdx.x; i < A.n_tok * 32; i += kConsumers) {
-                const int t = i >> 5, l = i & 31;
-                const size_t row = (size_t)g * 32 + l;
-                float v = 0.0f;
-                for (int j = 0; j < A.k; ++j) {
-                    const int p = t * A.k + j;
-                    const int id = R.ids[p];
-                    if (id >= 0 && id < A.L.E) v += A.wts[p] * __ldcg(A.ws.obuf + (size_t)p * A.L.H + row);
-                }
-                A.y[(size_t)t * A.L.H + row] = v;
-            }
-            if (threadIdx.x == 0) A.ws.cnt[g] = 0u;
-        }
+        down_arrive(A, R, g, min(R.ns, kMaxCols), warp, lane);
     }
 }
 
@@ -677,7 +689,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
     const int64_t max_experts = std::min(n_tok * k, L.E);
     {
-        const size_t smem = pipe_smem_bytes(kStages, n_tok + 1, A.nbpH);
+        const size_t smem = pipe_smem_bytes(kStagesGateUp, n_tok + 1, A.nbpH, kSetsGateUp);
         int grid = 0;
         e = dynamic_grid(k_moe_gate_up, smem, max_experts * (L.F / 32), &grid);
         if (e != cudaSuccess) return e;
@@ -686,7 +698,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     }
     if (ws.ev[2] && (e = cudaEventRecord(ws.ev[2], s)) != cudaSuccess) return e;
     {
-        const size_t smem = pipe_smem_bytes(kStages, kMaxCols, A.nbpF);
+        const size_t smem = pipe_smem_bytes(kStages, kMaxCols, A.nbpF, kSetsMatvec);
         int grid = 0;
         e = dynamic_grid(k_moe_down, smem, max_experts * (L.H / 32) / kDownGrab + 1, &grid);
         if (e != cudaSuccess) return e;

@@ -206,19 +206,24 @@ struct Consumer {
 };
 
 // Dynamic shared memory of a pipelined kernel:
-//   [full S][empty S][abort] | ring S x kStageBytes | act ncols x nbp x 32 | dx | part
+//   [full S][empty S][abort][tags S] | ring S x kStageBytes | act ncols x nbp x 32 | dx | part
+// part holds nsets partial-sum sets of kConsumerWarps x kMaxCols x 32 floats;
+// kernels alternate between two halves item by item, so one barrier per item
+// separates the writers of an item from the readers of the item before.
 struct PipeSmem {
     Pipe pipe;
     uint4 *act;
     float *dx;
-    float *part;  // 2 x kConsumerWarps x kMaxCols x 32 (two partial sets)
+    float *part;  // nsets x kPartSet floats
 };
+
+constexpr int kPartSet = kConsumerWarps * kMaxCols * 32;
 
 __host__ __device__ inline size_t pipe_header_bytes(int S) { return ((size_t)20 * S + 4 + 127) / 128 * 128; }
 
-__host__ __device__ inline size_t pipe_smem_bytes(int S, int ncols, int nbp) {
+__host__ __device__ inline size_t pipe_smem_bytes(int S, int ncols, int nbp, int nsets) {
     return pipe_header_bytes(S) + (size_t)S * kStageBytes + (size_t)ncols * nbp * 36 +
-           (size_t)2 * kConsumerWarps * kMaxCols * 32 * 4;
+           (size_t)nsets * kConsumerWarps * kMaxCols * 32 * 4;
 }
 
 __device__ __forceinline__ PipeSmem carve_pipe(unsigned char *smem, int S, int ncols, int nbp) {
