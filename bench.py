@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--profile", action="store_true",
                     help="time the main loop only (no e2e, per-layer or oracle legs); for profiler runs")
+    ap.add_argument("--case", default="step", choices=["step", "b1", "b5"],
+                    help="profile mode only: the whole step, or the MoE layer alone at batch 1 (top-4) "
+                         "or batch 5 (top-8)")
     ap.add_argument("--experts", type=int, default=E,
                     help="experts in the layer (default 256); smaller layers keep profiler captures small")
     return ap.parse_args()
@@ -205,7 +208,7 @@ def gpu_ident(torch, local):
         return parts[local] if local < len(parts) else local
 
 
-def build_layer(torch, cbq, n_exp=E):
+def build_layer(torch, cbq, n_exp=E, with_head=True):
     """All experts drawn from their seeded streams, repacked on device."""
     gu = np.empty((n_exp, 2 * F, H // QK, BB), dtype=np.uint8)
     dn = np.empty((n_exp, H, F // QK, BB), dtype=np.uint8)
@@ -213,6 +216,8 @@ def build_layer(torch, cbq, n_exp=E):
     synth.expert_blocks(n_exp, H, F, stream=synth.S_DOWN, out=dn)
     L = cbq.Moe(gu, dn, n_exp, H, F)
     del gu, dn
+    if not with_head:
+        return L
     head = cbq.Weights(synth.weight_blocks(HEAD_M, HEAD_K, stream=synth.S_HEAD), HEAD_M, HEAD_K)
     return L, head
 
@@ -237,6 +242,30 @@ def run_gpu(args):
     cbq.load()
 
     n_exp = args.experts
+    if args.profile and args.case != "step":
+        L = build_layer(torch, cbq, n_exp, with_head=False)
+        n_tok, k = (1, 4) if args.case == "b1" else (N_TOK, TOPK)
+        tabs = []
+        for i in range(N_SETS):
+            ids_i, wts_i = synth.router(n_tok, k, n_exp, stream=synth.S_IDS + 300 + 17 * n_tok + i)
+            tabs.append(tuple(torch.from_numpy(a).to(dev) for a in
+                              (ids_i, wts_i, synth.activations(n_tok, H, stream=synth.S_H + 300 + i))))
+        yl = torch.empty((n_tok, H), dtype=torch.float32, device=dev)
+        for i in range(args.warmup):
+            t = tabs[i % N_SETS]
+            cbq.cbq_moe_matvec(L, t[2], t[0], t[1], y=yl)
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for i in range(args.steps):
+            t = tabs[i % N_SETS]
+            cbq.cbq_moe_matvec(L, t[2], t[0], t[1], y=yl)
+        a1.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": True, "case": args.case, "experts": n_exp,
+                          "us_per_layer": 1e3 * a0.elapsed_time(a1) / args.steps,
+                          "device_error": cbq.cbq_get_device_error()}), flush=True)
+        return
     L, head = build_layer(torch, cbq, n_exp)
     sets = routing_sets(n_exp=n_exp)
     d_sets = []

@@ -159,7 +159,8 @@ int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok,
 /* Stage timing: when set, cbq_moe_matvec records these CUDA events
  * (cudaEvent_t passed as void*) on its stream before the activation
  * quantization, before the gate_up kernel, before the down kernel and after
- * it.  Pass NULL for all four to stop.  The events stay owned by the caller. */
+ * the combine that ends the call.  Recording them separates the kernels (the
+ * overlap of one kernel's start with the previous one's end is lost).  Pass NULL for all four to stop.  The events stay owned by the caller. */
 int cbq_moe_set_stage_events(cbq_moe *L, void *ev_quant, void *ev_gate_up, void *ev_down, void *ev_end);
 
 /* Reads and clears the device error word of the current device (bits

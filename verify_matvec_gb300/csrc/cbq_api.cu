@@ -288,7 +288,6 @@ int cbq_moe_destroy(cbq_moe *L) {
     cudaFree(L->ws.da);
     cudaFree(L->ws.a_dbg);
     cudaFree(L->ws.obuf);
-    cudaFree(L->ws.cnt);
     cudaFree(L->ws.sched);
     cudaFree(L->st_h);
     cudaFree(L->st_ids);
@@ -331,7 +330,6 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
         (rc = dev_alloc(&L->ws.da, slots * nbF, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.a_dbg, slots * F, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.obuf, slots * H, &L->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&L->ws.cnt, (size_t)(H / 32), &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.sched, 4, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_h, (size_t)CBQ_MAX_TOKENS * H, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_ids, slots, &L->bytes)) != CBQ_OK ||
@@ -341,8 +339,7 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
         return rc;
     }
     cudaStream_t s = as_stream(stream);
-    if (cudaMemsetAsync(L->ws.cnt, 0, (size_t)(H / 32) * sizeof(unsigned), s) != cudaSuccess ||
-        cudaMemsetAsync(L->ws.sched, 0, 4 * sizeof(unsigned), s) != cudaSuccess) {
+    if (cudaMemsetAsync(L->ws.sched, 0, 4 * sizeof(unsigned), s) != cudaSuccess) {
         cbq_moe_destroy(L);
         return CBQ_ECUDA;
     }

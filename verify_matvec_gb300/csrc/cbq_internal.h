@@ -42,10 +42,9 @@ struct MoeWork {
     float *da;        // slots x F/32
     float *a_dbg;     // slots x F (written when keep_a)
     float *obuf;      // slots x H, down-projection output per slot
-    unsigned *cnt;    // H/32 arrival counters (zero between calls)
     unsigned *sched;  // 4 work counters: gate_up (2), down (2), zero between launches
     int keep_a;
-    cudaEvent_t ev[4];  // optional stage events (quant, gate_up, down, end)
+    cudaEvent_t ev[4];  // optional stage events (before quant, gate_up, down; after combine)
 };
 
 constexpr int kMaxSlots = 80;  // CBQ_MAX_TOKENS * CBQ_MAX_TOPK

@@ -523,8 +523,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
 
 // Down rows of one 32-row group for the columns staged in S (slots
 // R.slots[c0..c0+nc), zero columns after them), written per slot to obuf by
-// warps 0..nc-1.  Returns after one CTA barrier; the writer warps then finish
-// the item alone (down_arrive).
+// warps 0..nc-1 after one CTA barrier.
 template <int NC>
 __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
                                           int g, int c0, int nc, int warp, int lane, int buf) {
@@ -552,34 +551,6 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, co
     }
 }
 
-// Arrival of one (expert, row group) item, by the writer warps 0..nw-1 only:
-// they make their obuf writes visible, warp 0 counts the arrival, and the
-// arrival that completes the D experts of row group g combines y for its 32
-// rows in slot order and resets the count.
-__device__ __forceinline__ void down_arrive(const MoeArgs &A, const Routing &R, int g, int nw, int warp,
-                                            int lane) {
-    if (warp >= nw) return;
-    __threadfence();
-    if (nw > 1) asm volatile("bar.sync 2, %0;" ::"r"(nw * 32) : "memory");
-    if (warp != 0) return;
-    unsigned old = 0;
-    if (lane == 0) old = atomicAdd(&A.ws.cnt[g], 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old != (unsigned)R.D - 1u) return;
-    __threadfence();
-    const size_t row = (size_t)g * 32 + lane;
-    for (int t = 0; t < A.n_tok; ++t) {
-        float v = 0.0f;
-        for (int j = 0; j < A.k; ++j) {
-            const int p = t * A.k + j;
-            const int id = R.ids[p];
-            if (id >= 0 && id < A.L.E) v += A.wts[p] * __ldcg(A.ws.obuf + (size_t)p * A.L.H + row);
-        }
-        A.y[(size_t)t * A.L.H + row] = v;
-    }
-    if (lane == 0) A.ws.cnt[g] = 0u;
-}
-
 // Items are (expert rank u, 32-row group g), u-major, fetched kDownGrab at a
 // time so that consecutive items of a CTA mostly share their expert (and the
 // staged intermediate columns).
@@ -591,12 +562,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
     const int N = A.n_tok * A.k;
     route(A.ids, N, A.L.E, R, false);
     const int Gd = A.L.H / 32;
-    if (R.D == 0) {  // nothing routed: the output is zero
-        pdl_wait();
-        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < A.n_tok * A.L.H; i += gridDim.x * blockDim.x)
-            A.y[i] = 0.0f;
-        return;
-    }
+    pdl_trigger();  // the combine kernel may launch; it waits for this grid
+    if (R.D == 0) return;  // nothing routed: the combine writes zeros
     const unsigned total = (unsigned)(R.D * Gd);
     unsigned *sched = A.ws.sched + 2;
     const PipeSmem S = carve_pipe(smem, kStages, kMaxCols, A.nbpF);
@@ -663,7 +630,24 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
                 down_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane, item & 1);
             ++item;
         }
-        down_arrive(A, R, g, min(R.ns, kMaxCols), warp, lane);
+    }
+}
+
+// Router-weighted combine: y[t][r] = sum_j wts[t][j] * obuf[t*k+j][r], slots
+// in order j = 0..k-1, slots with an out-of-range id skipped.  One thread per
+// output; launched as a dependent of the down kernel.
+__global__ void __launch_bounds__(256) k_moe_combine(MoeArgs A) {
+    pdl_wait();
+    const int total = A.n_tok * A.L.H;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const int t = i / A.L.H, r = i - t * A.L.H;
+        float v = 0.0f;
+        for (int j = 0; j < A.k; ++j) {
+            const int p = t * A.k + j;
+            const int id = A.ids[p];
+            if (id >= 0 && id < A.L.E) v += A.wts[p] * A.ws.obuf[(size_t)p * A.L.H + r];
+        }
+        A.y[i] = v;
     }
 }
 
@@ -700,9 +684,14 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     {
         const size_t smem = pipe_smem_bytes(kStages, kMaxCols, A.nbpF, kSetsMatvec);
         int grid = 0;
-        e = dynamic_grid(k_moe_down, smem, max_experts * (L.H / 32) / kDownGrab + 1, &grid);
+        e = dynamic_grid(k_moe_down, smem, max_experts * (L.H / 32), &grid);
         if (e != cudaSuccess) return e;
         e = launch_k(k_moe_down, grid, kPipeThreads, smem, s, true, A);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const int grid = (int)std::min<int64_t>(((int64_t)n_tok * L.H + 255) / 256, 1024);
+        e = launch_k(k_moe_combine, grid, 256, 0, s, true, A);
         if (e != cudaSuccess) return e;
     }
     if (ws.ev[3]) e = cudaEventRecord(ws.ev[3], s);
