@@ -167,13 +167,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     for (int item = 0;; ++item) {
         const int g = co.peek(S.pipe);
         if (g < 0) break;
-        float acc[NC];
+        float2 acc[NC];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
+        for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
         co.group<NC>(S.pipe, nbp, act, dxs, acc, warp, lane);
         float *part = S.part + (item & 1) * kPartSet;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) part[(warp * NC + c) * 32 + lane] = acc[c];
+        for (int c = 0; c < NC; ++c) part[(warp * NC + c) * 32 + lane] = acc[c].x + acc[c].y;
         consumer_sync();
         if (warp < NC) {
             float v = 0.0f;
@@ -416,17 +416,23 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
         act[c] = S.act + (size_t)tok * A.nbpH * 2;
         dxs[c] = S.dx + (size_t)tok * A.nbpH;
     }
-    float accg[NC], accu[NC];
-#pragma unroll
-    for (int c = 0; c < NC; ++c) accg[c] = accu[c] = 0.0f;
-    co.group<NC>(S.pipe, A.nbpH, act, dxs, accg, warp, lane);
-    co.group<NC>(S.pipe, A.nbpH, act, dxs, accu, warp, lane);
     float *pg = S.part + (2 * buf) * kPartSet;
     float *pu = S.part + (2 * buf + 1) * kPartSet;
+    {
+        float2 acc[NC];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-        pg[(warp * kMaxCols + c) * 32 + lane] = accg[c];
-        pu[(warp * kMaxCols + c) * 32 + lane] = accu[c];
+        for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
+        co.group<NC>(S.pipe, A.nbpH, act, dxs, acc, warp, lane);  // gate rows
+#pragma unroll
+        for (int c = 0; c < NC; ++c) pg[(warp * kMaxCols + c) * 32 + lane] = acc[c].x + acc[c].y;
+    }
+    {
+        float2 acc[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
+        co.group<NC>(S.pipe, A.nbpH, act, dxs, acc, warp, lane);  // up rows
+#pragma unroll
+        for (int c = 0; c < NC; ++c) pu[(warp * kMaxCols + c) * 32 + lane] = acc[c].x + acc[c].y;
     }
     consumer_sync();
     if (warp < nc) {
@@ -534,13 +540,13 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, co
         act[c] = S.act + (size_t)c * A.nbpF * 2;
         dxs[c] = S.dx + (size_t)c * A.nbpF;
     }
-    float acc[NC];
+    float2 acc[NC];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) acc[c] = 0.0f;
+    for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
     co.group<NC>(S.pipe, A.nbpF, act, dxs, acc, warp, lane);
     float *part = S.part + buf * kPartSet;
 #pragma unroll
-    for (int c = 0; c < NC; ++c) part[(warp * kMaxCols + c) * 32 + lane] = acc[c];
+    for (int c = 0; c < NC; ++c) part[(warp * kMaxCols + c) * 32 + lane] = acc[c].x + acc[c].y;
     consumer_sync();
     if (warp < nc) {
         float v = 0.0f;
@@ -551,10 +557,11 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, co
     }
 }
 
-// Items are (expert rank u, 32-row group g), u-major, fetched kDownGrab at a
-// time so that consecutive items of a CTA mostly share their expert (and the
-// staged intermediate columns).
-constexpr int kDownGrab = 2;
+// Items are (expert rank u, 32-row group g), u-major, fetched by guided
+// self-scheduling: a grab takes about remaining/(2 x CTAs) consecutive items
+// (at most kDownGrab), so early grabs keep one expert's staged intermediate
+// columns for several items and the last grabs are single items.
+constexpr unsigned kDownGrab = 8;
 
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -574,12 +581,12 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
     if (warp == kConsumerWarps) {  // producer
         if (lane == 0) {
             Producer pr;
-            // grab kDownGrab items at a time only when there are many per CTA
-            const unsigned grab = total >= 16u * gridDim.x ? (unsigned)kDownGrab : 1u;
-            unsigned nxt = atomicAdd(sched, grab);
-            while (nxt < total && !pr.stopped) {
-                const unsigned base = nxt;
-                nxt = atomicAdd(sched, grab);
+            for (;;) {
+                const unsigned seen = *(volatile unsigned *)sched;
+                if (seen >= total || pr.stopped) break;
+                const unsigned grab = max(1u, min(kDownGrab, (total - seen) / (2u * gridDim.x)));
+                const unsigned base = atomicAdd(sched, grab);
+                if (base >= total) break;
                 for (unsigned it = base; it < min(total, base + grab) && !pr.stopped; ++it) {
                     const int u = (int)it / Gd, g = (int)it - u * Gd;
                     const size_t e = (size_t)R.uniq[u];

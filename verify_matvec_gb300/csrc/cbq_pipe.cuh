@@ -23,6 +23,8 @@
 
 #include <stdint.h>
 
+#include <cuda_fp16.h>
+
 #include "cbq_device.cuh"
 
 namespace cbq {
@@ -166,10 +168,13 @@ struct Consumer {
         return *(volatile int *)(P.tag + slot);
     }
 
-    // Accumulate one 32-row group pass (blocks [0, nbp)) into acc.
+    // Accumulate one 32-row group pass (blocks [0, nbp)) into acc2: two
+    // interleaved fp32 partial sums per column (even and odd blocks), updated
+    // with packed f32x2 arithmetic.  dxs[c] must be 8-byte aligned.
     template <int NC>
     __device__ __forceinline__ void group(const Pipe &P, int nbp, const uint4 *const *act, const float *const *dxs,
-                                          float acc[NC], int warp, int lane) {
+                                          float2 acc2[NC], int warp, int lane) {
+        const float2 neg_magic = make_float2(-kMagic, -kMagic);
         for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
             const int nq = min(kChunkBlocks, nbp - b0) / 4;
             const uint32_t slot = it % P.S, use = it / P.S;
@@ -181,19 +186,24 @@ struct Consumer {
                 const int q0 = warp * nq / kConsumerWarps, q1 = (warp + 1) * nq / kConsumerWarps;
                 for (int q = q0; q < q1; ++q) {
                     const uint2 s = sc_s[q * 32 + lane];
-                    const float dw[4] = {half_lo(s.x), half_hi(s.x), half_lo(s.y), half_hi(s.y)};
+                    const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
+                    const float2 dw23 = __half22float2(*reinterpret_cast<const __half2 *>(&s.y));
                     uint4 w[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) w[j] = qs_s[(q * 4 + j) * 32 + lane];
+                    const int bq = b0 + q * 4;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int b = b0 + q * 4 + j;
-                        int sd[NC];
-                        block_dots<NC>(w[j], act, b, sd);
+                    for (int jj = 0; jj < 4; jj += 2) {  // blocks in pairs: fewer live sums
+                        int sa[NC], sb[NC];
+                        block_dots<NC>(w[jj], act, bq + jj, sa);
+                        block_dots<NC>(w[jj + 1], act, bq + jj + 1, sb);
+                        const float2 dw = jj == 0 ? dw01 : dw23;
 #pragma unroll
                         for (int c = 0; c < NC; ++c) {
-                            const float sf = __int_as_float(sd[c]) - kMagic;
-                            acc[c] = fmaf(dw[j] * dxs[c][b], sf, acc[c]);
+                            const float2 dx2 = *reinterpret_cast<const float2 *>(dxs[c] + bq + jj);
+                            const float2 sf = __fadd2_rn(make_float2(__int_as_float(sa[c]), __int_as_float(sb[c])),
+                                                         neg_magic);
+                            acc2[c] = __ffma2_rn(__fmul2_rn(dw, dx2), sf, acc2[c]);
                         }
                     }
                 }
