@@ -450,7 +450,7 @@ def run_gpu(args):
                          "traffic": None},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": 6 * args.steps,  # per step: quantize, gate_up, down, combine; quantize, head matvec
             "clocks": clk,
             "device_error": err,
         }

@@ -454,10 +454,18 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
     }
 }
 
+// The 2..5-column variants (an expert serving several tokens) are rare at
+// batch <= 5 over many experts; keeping them out of line leaves the one-column
+// path its own register allocation.
+__device__ __noinline__ void gate_up_item_wide(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
+                                               int g, int c0, int nc, int warp, int lane, int buf) {
+    gate_up_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane, buf);
+}
+
 // Items are (expert rank u, 32-row-pair group g), u-major, fetched one at a
 // time.  The producer streams, per item and column chunk, the gate group g
 // then the up group g + F/32 of expert uniq[u].
-__global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
+__global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(const __grid_constant__ MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
     pdl_trigger();
@@ -522,7 +530,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(MoeArgs A) {
             if (nc == 1)
                 gate_up_item<1>(A, R, S, co, g, c0, 1, warp, lane, item & 1);
             else
-                gate_up_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane, item & 1);
+                gate_up_item_wide(A, R, S, co, g, c0, nc, warp, lane, item & 1);
         }
     }
 }
@@ -563,7 +571,12 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, co
 // columns for several items and the last grabs are single items.
 constexpr unsigned kDownGrab = 8;
 
-__global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
+__device__ __noinline__ void down_item_wide(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
+                                            int g, int c0, int nc, int warp, int lane, int buf) {
+    down_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane, buf);
+}
+
+__global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(const __grid_constant__ MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
     const int N = A.n_tok * A.k;
@@ -634,7 +647,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
             if (nc == 1)
                 down_item<1>(A, R, S, co, g, c0, 1, warp, lane, item & 1);
             else
-                down_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane, item & 1);
+                down_item_wide(A, R, S, co, g, c0, nc, warp, lane, item & 1);
             ++item;
         }
     }
@@ -643,7 +656,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(MoeArgs A) {
 // Router-weighted combine: y[t][r] = sum_j wts[t][j] * obuf[t*k+j][r], slots
 // in order j = 0..k-1, slots with an out-of-range id skipped.  One thread per
 // output; launched as a dependent of the down kernel.
-__global__ void __launch_bounds__(256) k_moe_combine(MoeArgs A) {
+__global__ void __launch_bounds__(256) k_moe_combine(const __grid_constant__ MoeArgs A) {
     pdl_wait();
     const int total = A.n_tok * A.L.H;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
