@@ -402,38 +402,19 @@ __device__ __forceinline__ int expert_ns(const Routing &R, int u, int N) {
 __device__ __forceinline__ int col_chunks(int ns) { return (ns + kMaxCols - 1) / kMaxCols; }
 
 // Gate rows (first pass) and up rows (second pass) of one 32-row-pair group
-// over the whole K, then the SwiGLU split and the requantization of the 32
-// outputs, per column.  NC is 1 (exact) or kMaxCols, with columns nc..NC-1
-// reading the zero column staged after the tokens and their results dropped.
-template <int NC>
+// over the whole K for the columns (slots) R.slots[c0..c0+nc), then the
+// SwiGLU split and the requantization of the 32 outputs of each column.
+// Partial sets: gate sums in set 2*buf, up sums in set 2*buf+1, each
+// [warp][column][lane].
 __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
                                              int g, int c0, int nc, int warp, int lane, int buf) {
-    const uint4 *act[NC];
-    const float *dxs[NC];
+    int col_off[kMaxCols];  // activation column of each slot: its token's column
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-        const int tok = c < nc ? R.slots[c0 + c] / A.k : A.n_tok;
-        act[c] = S.act + (size_t)tok * A.nbpH * 2;
-        dxs[c] = S.dx + (size_t)tok * A.nbpH;
-    }
+    for (int c = 0; c < kMaxCols; ++c) col_off[c] = (c < nc ? R.slots[c0 + c] / A.k : 0) * A.nbpH;
     float *pg = S.part + (2 * buf) * kPartSet;
     float *pu = S.part + (2 * buf + 1) * kPartSet;
-    {
-        float2 acc[NC];
-#pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
-        co.group<NC>(S.pipe, A.nbpH, act, dxs, acc, warp, lane);  // gate rows
-#pragma unroll
-        for (int c = 0; c < NC; ++c) pg[(warp * kMaxCols + c) * 32 + lane] = acc[c].x + acc[c].y;
-    }
-    {
-        float2 acc[NC];
-#pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
-        co.group<NC>(S.pipe, A.nbpH, act, dxs, acc, warp, lane);  // up rows
-#pragma unroll
-        for (int c = 0; c < NC; ++c) pu[(warp * kMaxCols + c) * 32 + lane] = acc[c].x + acc[c].y;
-    }
+    group_cols(co, S.pipe, A.nbpH, S.act, S.dx, col_off, nc, pg + warp * kMaxCols * 32, warp, lane);
+    group_cols(co, S.pipe, A.nbpH, S.act, S.dx, col_off, nc, pu + warp * kMaxCols * 32, warp, lane);
     consumer_sync();
     if (warp < nc) {
         const int c = warp;
@@ -454,14 +435,6 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
     }
 }
 
-// The 2..5-column variants (an expert serving several tokens) are rare at
-// batch <= 5 over many experts; keeping them out of line leaves the one-column
-// path its own register allocation.
-__device__ __noinline__ void gate_up_item_wide(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
-                                               int g, int c0, int nc, int warp, int lane, int buf) {
-    gate_up_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane, buf);
-}
-
 // Items are (expert rank u, 32-row-pair group g), u-major, fetched one at a
 // time.  The producer streams, per item and column chunk, the gate group g
 // then the up group g + F/32 of expert uniq[u].
@@ -474,7 +447,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(const __grid_co
     const int Gf = A.L.F / 32;
     const unsigned total = (unsigned)(R.D * Gf);
     unsigned *sched = A.ws.sched;
-    const PipeSmem S = carve_pipe(smem, kStagesGateUp, A.n_tok + 1, A.nbpH);
+    const PipeSmem S = carve_pipe(smem, kStagesGateUp, A.n_tok, A.nbpH);
     pipe_init(S.pipe);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -506,13 +479,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(const __grid_co
     }
     pdl_wait();  // the quantized tokens come from the kernel launched just before
     {
-        const int8_t *src[kMaxCols + 1];
-        const float *dsrc[kMaxCols + 1];
-        for (int t = 0; t <= A.n_tok; ++t) {  // column n_tok stays zero
-            src[t] = t < A.n_tok ? A.ws.qh + (size_t)t * A.L.H : nullptr;
-            dsrc[t] = t < A.n_tok ? A.ws.dh + (size_t)t * A.nbH : A.ws.dh;
+        const int8_t *src[kMaxCols];
+        const float *dsrc[kMaxCols];
+        for (int t = 0; t < A.n_tok; ++t) {
+            src[t] = A.ws.qh + (size_t)t * A.L.H;
+            dsrc[t] = A.ws.dh + (size_t)t * A.nbH;
         }
-        stage_cols(src, dsrc, A.n_tok + 1, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
+        stage_cols(src, dsrc, A.n_tok, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
     }
     Consumer co;
     int cur_u = -1, item = 0;
@@ -525,36 +498,21 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(const __grid_co
             expert_slots(R, u, N);
             cur_u = u;
         }
-        for (int c0 = 0; c0 < R.ns; c0 += kMaxCols, ++item) {
-            const int nc = min(kMaxCols, R.ns - c0);
-            if (nc == 1)
-                gate_up_item<1>(A, R, S, co, g, c0, 1, warp, lane, item & 1);
-            else
-                gate_up_item_wide(A, R, S, co, g, c0, nc, warp, lane, item & 1);
-        }
+        for (int c0 = 0; c0 < R.ns; c0 += kMaxCols, ++item)
+            gate_up_item(A, R, S, co, g, c0, min(kMaxCols, R.ns - c0), warp, lane, item & 1);
     }
 }
 
-// Down rows of one 32-row group for the columns staged in S (slots
-// R.slots[c0..c0+nc), zero columns after them), written per slot to obuf by
-// warps 0..nc-1 after one CTA barrier.
-template <int NC>
+// Down rows of one 32-row group for the nc columns staged in S (slots
+// R.slots[c0..c0+nc)), written per slot to obuf by warps 0..nc-1 after one
+// CTA barrier.
 __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
                                           int g, int c0, int nc, int warp, int lane, int buf) {
-    const uint4 *act[NC];
-    const float *dxs[NC];
+    int col_off[kMaxCols];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-        act[c] = S.act + (size_t)c * A.nbpF * 2;
-        dxs[c] = S.dx + (size_t)c * A.nbpF;
-    }
-    float2 acc[NC];
-#pragma unroll
-    for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
-    co.group<NC>(S.pipe, A.nbpF, act, dxs, acc, warp, lane);
+    for (int c = 0; c < kMaxCols; ++c) col_off[c] = c * A.nbpF;
     float *part = S.part + buf * kPartSet;
-#pragma unroll
-    for (int c = 0; c < NC; ++c) part[(warp * kMaxCols + c) * 32 + lane] = acc[c].x + acc[c].y;
+    group_cols(co, S.pipe, A.nbpF, S.act, S.dx, col_off, nc, part + warp * kMaxCols * 32, warp, lane);
     consumer_sync();
     if (warp < nc) {
         float v = 0.0f;
@@ -570,11 +528,6 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, co
 // (at most kDownGrab), so early grabs keep one expert's staged intermediate
 // columns for several items and the last grabs are single items.
 constexpr unsigned kDownGrab = 8;
-
-__device__ __noinline__ void down_item_wide(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
-                                            int g, int c0, int nc, int warp, int lane, int buf) {
-    down_item<kMaxCols>(A, R, S, co, g, c0, nc, warp, lane, buf);
-}
 
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(const __grid_constant__ MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -635,19 +588,16 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(const __grid_const
                 consumer_sync();
                 const int8_t *src[kMaxCols];
                 const float *dsrc[kMaxCols];
-                for (int c = 0; c < kMaxCols; ++c) {
-                    const int p = R.slots[c0 + min(c, nc - 1)];
-                    src[c] = c < nc ? A.ws.qa + (size_t)p * A.L.F : nullptr;
+                for (int c = 0; c < nc; ++c) {
+                    const int p = R.slots[c0 + c];
+                    src[c] = A.ws.qa + (size_t)p * A.L.F;
                     dsrc[c] = A.ws.da + (size_t)p * A.nbF;
                 }
-                stage_cols(src, dsrc, nc == 1 ? 1 : kMaxCols, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers);
+                stage_cols(src, dsrc, nc, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers);
                 consumer_sync();
                 staged_u = u;
             }
-            if (nc == 1)
-                down_item<1>(A, R, S, co, g, c0, 1, warp, lane, item & 1);
-            else
-                down_item_wide(A, R, S, co, g, c0, nc, warp, lane, item & 1);
+            down_item(A, R, S, co, g, c0, nc, warp, lane, item & 1);
             ++item;
         }
     }
@@ -693,7 +643,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
     const int64_t max_experts = std::min(n_tok * k, L.E);
     {
-        const size_t smem = pipe_smem_bytes(kStagesGateUp, n_tok + 1, A.nbpH, kSetsGateUp);
+        const size_t smem = pipe_smem_bytes(kStagesGateUp, n_tok, A.nbpH, kSetsGateUp);
         int grid = 0;
         e = dynamic_grid(k_moe_gate_up, smem, max_experts * (L.F / 32), &grid);
         if (e != cudaSuccess) return e;

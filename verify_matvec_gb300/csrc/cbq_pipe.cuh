@@ -215,6 +215,54 @@ struct Consumer {
     }
 };
 
+// One-column variant for the routed-expert kernels: ncols (runtime, >= 1)
+// columns, each swept separately over every stage from shared memory, so the
+// registers stay those of one column while the weight stream is still read
+// once.  The sum of this warp over the pass goes to part[c*32 + lane] (this
+// warp's slice of a partial set), written at the pass's first stage and
+// accumulated over the rest.
+__device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
+                                           const int *col_off, int ncols, float *part, int warp, int lane) {
+    const float2 neg_magic = make_float2(-kMagic, -kMagic);
+    for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
+        const int nq = min(kChunkBlocks, nbp - b0) / 4;
+        const uint32_t slot = co.it % P.S, use = co.it / P.S;
+        const bool ok = pipe_wait(P, P.full + slot, use & 1u, true);
+        if (ok) {
+            const unsigned char *st = P.ring + (size_t)slot * kStageBytes;
+            const uint4 *qs_s = reinterpret_cast<const uint4 *>(st);
+            const uint2 *sc_s = reinterpret_cast<const uint2 *>(st + kStageQsBytes);
+            const int q0 = warp * nq / kConsumerWarps, q1 = (warp + 1) * nq / kConsumerWarps;
+            for (int c = 0; c < ncols; ++c) {
+                const uint4 *act = act0 + (size_t)col_off[c] * 2;
+                const float *dxs = dx0 + col_off[c];
+                float2 acc = make_float2(0.0f, 0.0f);
+                for (int q = q0; q < q1; ++q) {
+                    const uint2 s = sc_s[q * 32 + lane];
+                    const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
+                    const float2 dw23 = __half22float2(*reinterpret_cast<const __half2 *>(&s.y));
+                    const int bq = b0 + q * 4;
+#pragma unroll
+                    for (int jj = 0; jj < 4; jj += 2) {
+                        int sa[1], sb[1];
+                        block_dots<1>(qs_s[(q * 4 + jj) * 32 + lane], &act, bq + jj, sa);
+                        block_dots<1>(qs_s[(q * 4 + jj + 1) * 32 + lane], &act, bq + jj + 1, sb);
+                        const float2 dx2 = *reinterpret_cast<const float2 *>(dxs + bq + jj);
+                        const float2 sf =
+                            __fadd2_rn(make_float2(__int_as_float(sa[0]), __int_as_float(sb[0])), neg_magic);
+                        acc = __ffma2_rn(__fmul2_rn(jj == 0 ? dw01 : dw23, dx2), sf, acc);
+                    }
+                }
+                float *dst = part + c * 32 + lane;
+                *dst = (b0 == 0 ? 0.0f : *dst) + (acc.x + acc.y);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(P.empty + slot);
+        ++co.it;
+    }
+}
+
 // Dynamic shared memory of a pipelined kernel:
 //   [full S][empty S][abort][tags S] | ring S x kStageBytes | act ncols x nbp x 32 | dx | part
 // part holds nsets partial-sum sets of kConsumerWarps x kMaxCols x 32 floats;
