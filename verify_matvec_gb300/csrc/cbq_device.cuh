@@ -36,6 +36,30 @@ constexpr uint32_t kCb3 = 0x71594535u;
 constexpr uint32_t kCbP0 = 0x271A0E02u;
 constexpr uint32_t kCbP1 = 0x725A4636u;
 
+// The codebook words held in registers for the whole kernel.  Produced by
+// opaque moves so the compiler keeps them in registers instead of
+// re-materialising the immediates before every permute.
+struct Codebook {
+    uint32_t t0, t1, t2, t3, p0, p1;
+};
+
+__device__ __forceinline__ uint32_t opaque(uint32_t v) {
+    uint32_t r;
+    asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+    return r;
+}
+
+__device__ __forceinline__ Codebook load_codebook() {
+    Codebook cb;
+    cb.t0 = opaque(kCb0);
+    cb.t1 = opaque(kCb1);
+    cb.t2 = opaque(kCb2);
+    cb.t3 = opaque(kCb3);
+    cb.p0 = opaque(kCbP0);
+    cb.p1 = opaque(kCbP1);
+    return cb;
+}
+
 // float(s) for |s| < 2^22 without an int->float conversion: the dp4a chain
 // starts from the bit pattern of 1.5*2^23, so the integer sum s lands in the
 // mantissa; subtracting 1.5*2^23 in fp32 is exact.
@@ -88,14 +112,14 @@ __device__ __forceinline__ float half_hi(uint32_t v) {
 // expand_select: exact codebook bytes.  Two permutes look the low three index
 // bits up in the lower and upper eight levels; a third, in sign mode, turns
 // index bit 3 into a byte mask that picks between them.  11 ALU ops per word.
-__device__ __forceinline__ void expand_select(uint32_t w, uint32_t &e0, uint32_t &e1) {
+__device__ __forceinline__ void expand_select(const Codebook &cb, uint32_t w, uint32_t &e0, uint32_t &e1) {
     const uint32_t s = w & 0x77777777u;
     const uint32_t a = w << 4;               // bit 3 of even nibbles -> byte sign bits
     const uint32_t m0 = prmt(a, w, 0xD9C8u); // masks of nibbles 0..3
     const uint32_t m1 = prmt(a, w, 0xFBEAu); // masks of nibbles 4..7
     const uint32_t s1 = s >> 16;
-    const uint32_t l0 = prmt(kCb0, kCb1, s), h0 = prmt(kCb2, kCb3, s);
-    const uint32_t l1 = prmt(kCb0, kCb1, s1), h1 = prmt(kCb2, kCb3, s1);
+    const uint32_t l0 = prmt(cb.t0, cb.t1, s), h0 = prmt(cb.t2, cb.t3, s);
+    const uint32_t l1 = prmt(cb.t0, cb.t1, s1), h1 = prmt(cb.t2, cb.t3, s1);
     e0 = (h0 & m0) | (l0 & ~m0);
     e1 = (h1 & m1) | (l1 & ~m1);
 }
@@ -106,13 +130,13 @@ __device__ __forceinline__ void expand_select(uint32_t w, uint32_t &e0, uint32_t
 // bit 3 flipped, the upper table (levels + 1, all positive) yields level+1 for
 // 8..15 and 0 for 0..7.  The dot is then dp4a(lo,x) + dp4a(hi,x): 7 ALU ops
 // and two dp4a per word and column -- cheaper for one or two columns.
-__device__ __forceinline__ void expand_split(uint32_t w, uint32_t &lo0, uint32_t &hi0,
+__device__ __forceinline__ void expand_split(const Codebook &cb, uint32_t w, uint32_t &lo0, uint32_t &hi0,
                                              uint32_t &lo1, uint32_t &hi1) {
     const uint32_t f = w ^ 0x88888888u;
-    lo0 = prmt(kCb0, kCb1, w);
-    hi0 = prmt(kCbP0, kCbP1, f);
-    lo1 = prmt(kCb0, kCb1, w >> 16);
-    hi1 = prmt(kCbP0, kCbP1, f >> 16);
+    lo0 = prmt(cb.t0, cb.t1, w);
+    hi0 = prmt(cb.p0, cb.p1, f);
+    lo1 = prmt(cb.t0, cb.t1, w >> 16);
+    hi1 = prmt(cb.p0, cb.p1, f >> 16);
 }
 
 template <int NC>
@@ -121,28 +145,29 @@ struct UseSplit { static constexpr bool value = NC <= 2; };
 // Exact int32 block dots (offset by kMagicBits) of one index block against NC
 // permuted activation blocks act[c][0..1] (8 words each).
 template <int NC>
-__device__ __forceinline__ void block_dots(const uint4 w, const uint4 *const *act, int b, int sdot[NC]) {
+__device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, const uint4 *const *act, int b,
+                                           int sdot[NC]) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
     if constexpr (UseSplit<NC>::value) {
         uint32_t lo[8], hi[8];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) expand_split(ws[m], lo[2 * m], hi[2 * m], lo[2 * m + 1], hi[2 * m + 1]);
+        for (int m = 0; m < 4; ++m) expand_split(cb, ws[m], lo[2 * m], hi[2 * m], lo[2 * m + 1], hi[2 * m + 1]);
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             const uint4 a0 = act[c][2 * b], a1 = act[c][2 * b + 1];
             const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            int s = kMagicBits;
+            int s = kMagicBits, t = 0;  // two chains: lower- and upper-table parts
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 s = __dp4a((int)lo[i], (int)av[i], s);
-                s = __dp4a((int)hi[i], (int)av[i], s);
+                t = __dp4a((int)hi[i], (int)av[i], t);
             }
-            sdot[c] = s;
+            sdot[c] = s + t;
         }
     } else {
         uint32_t e[8];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) expand_select(ws[m], e[2 * m], e[2 * m + 1]);
+        for (int m = 0; m < 4; ++m) expand_select(cb, ws[m], e[2 * m], e[2 * m + 1]);
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             const uint4 a0 = act[c][2 * b], a1 = act[c][2 * b + 1];

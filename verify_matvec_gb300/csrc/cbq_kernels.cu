@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbq = nbp / 4;
     const int q0 = warp * nbq / kWarps, q1 = (warp + 1) * nbq / kWarps;
+    const Codebook cb = load_codebook();
     for (int g = g0; g < g1; ++g) {
         const int64_t row = (int64_t)g * 32 + lane;
         for (int q = q0; q < q1; ++q) {
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int b = 4 * q + j;
                 const uint4 w = ld_stream16(qs + ((size_t)g * nbp + b) * 32 + lane);
                 int sd[NC];
-                block_dots<NC>(w, act, b, sd);
+                block_dots<NC>(cb, w, act, b, sd);
                 if (row < M && b < nb) {
 #pragma unroll
                     for (int c = 0; c < NC; ++c) sdot[((size_t)c * M + row) * nb + b] = sd[c] - kMagicBits;

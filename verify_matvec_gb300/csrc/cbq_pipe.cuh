@@ -111,8 +111,8 @@ struct Producer {
 
     // Claim the next slot (waiting until the consumers released it).
     __device__ __forceinline__ bool claim(const Pipe &P, uint32_t &slot) {
-        slot = it % P.S;
-        const uint32_t use = it / P.S;
+        const uint32_t use = it / (uint32_t)P.S;
+        slot = it - use * (uint32_t)P.S;
         if (stopped || (use > 0 && !pipe_wait(P, P.empty + slot, (use - 1) & 1u, true))) {
             stopped = true;
             return false;
@@ -156,15 +156,25 @@ struct Producer {
     }
 };
 
-// Consumer side: the same running count, advanced in lock step.
+// Consumer side: the same sequence of stages, advanced in lock step (slot
+// and phase parity kept incrementally).
 struct Consumer {
-    uint32_t it = 0;
+    uint32_t slot = 0, phase = 0;
+    Codebook cb;
+
+    __device__ __forceinline__ Consumer() : cb(load_codebook()) {}
+
+    __device__ __forceinline__ void advance(const Pipe &P) {
+        if (++slot == (uint32_t)P.S) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
 
     // Item of the next stage (-1 at the end of the stream or after a give-up),
     // without consuming the stage.
     __device__ __forceinline__ int peek(const Pipe &P) const {
-        const uint32_t slot = it % P.S, use = it / P.S;
-        if (!pipe_wait(P, P.full + slot, use & 1u, true)) return -1;
+        if (!pipe_wait(P, P.full + slot, phase, true)) return -1;
         return *(volatile int *)(P.tag + slot);
     }
 
@@ -177,8 +187,7 @@ struct Consumer {
         const float2 neg_magic = make_float2(-kMagic, -kMagic);
         for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
             const int nq = min(kChunkBlocks, nbp - b0) / 4;
-            const uint32_t slot = it % P.S, use = it / P.S;
-            const bool ok = pipe_wait(P, P.full + slot, use & 1u, true);
+            const bool ok = pipe_wait(P, P.full + slot, phase, true);
             if (ok) {
                 const unsigned char *st = P.ring + (size_t)slot * kStageBytes;
                 const uint4 *qs_s = reinterpret_cast<const uint4 *>(st);
@@ -195,8 +204,8 @@ struct Consumer {
 #pragma unroll
                     for (int jj = 0; jj < 4; jj += 2) {  // blocks in pairs: fewer live sums
                         int sa[NC], sb[NC];
-                        block_dots<NC>(w[jj], act, bq + jj, sa);
-                        block_dots<NC>(w[jj + 1], act, bq + jj + 1, sb);
+                        block_dots<NC>(cb, w[jj], act, bq + jj, sa);
+                        block_dots<NC>(cb, w[jj + 1], act, bq + jj + 1, sb);
                         const float2 dw = jj == 0 ? dw01 : dw23;
 #pragma unroll
                         for (int c = 0; c < NC; ++c) {
@@ -210,7 +219,7 @@ struct Consumer {
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(P.empty + slot);
-            ++it;
+            advance(P);
         }
     }
 };
@@ -226,8 +235,8 @@ __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp,
     const float2 neg_magic = make_float2(-kMagic, -kMagic);
     for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
         const int nq = min(kChunkBlocks, nbp - b0) / 4;
-        const uint32_t slot = co.it % P.S, use = co.it / P.S;
-        const bool ok = pipe_wait(P, P.full + slot, use & 1u, true);
+        const uint32_t slot = co.slot;
+        const bool ok = pipe_wait(P, P.full + slot, co.phase, true);
         if (ok) {
             const unsigned char *st = P.ring + (size_t)slot * kStageBytes;
             const uint4 *qs_s = reinterpret_cast<const uint4 *>(st);
@@ -245,8 +254,8 @@ __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp,
 #pragma unroll
                     for (int jj = 0; jj < 4; jj += 2) {
                         int sa[1], sb[1];
-                        block_dots<1>(qs_s[(q * 4 + jj) * 32 + lane], &act, bq + jj, sa);
-                        block_dots<1>(qs_s[(q * 4 + jj + 1) * 32 + lane], &act, bq + jj + 1, sb);
+                        block_dots<1>(co.cb, qs_s[(q * 4 + jj) * 32 + lane], &act, bq + jj, sa);
+                        block_dots<1>(co.cb, qs_s[(q * 4 + jj + 1) * 32 + lane], &act, bq + jj + 1, sb);
                         const float2 dx2 = *reinterpret_cast<const float2 *>(dxs + bq + jj);
                         const float2 sf =
                             __fadd2_rn(make_float2(__int_as_float(sa[0]), __int_as_float(sb[0])), neg_magic);
@@ -259,7 +268,7 @@ __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp,
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(P.empty + slot);
-        ++co.it;
+        co.advance(P);
     }
 }
 
