@@ -140,7 +140,7 @@ __device__ __forceinline__ void expand_split(const Codebook &cb, uint32_t w, uin
 }
 
 template <int NC>
-struct UseSplit { static constexpr bool value = NC <= 2; };
+struct UseSplit { static constexpr bool value = NC == 1; };
 
 // Exact int32 block dots (offset by kMagicBits) of one index block against NC
 // permuted activation blocks act[c][0..1] (8 words each).

@@ -179,12 +179,11 @@ struct Consumer {
     }
 
     // Accumulate one 32-row group pass (blocks [0, nbp)) into acc2: two
-    // interleaved fp32 partial sums per column (even and odd blocks), updated
-    // with packed f32x2 arithmetic.  dxs[c] must be 8-byte aligned.
+    // interleaved fp32 partial sums per column (even and odd blocks).
+    // dxs[c] must be 8-byte aligned.
     template <int NC>
     __device__ __forceinline__ void group(const Pipe &P, int nbp, const uint4 *const *act, const float *const *dxs,
                                           float2 acc2[NC], int warp, int lane) {
-        const float2 neg_magic = make_float2(-kMagic, -kMagic);
         for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
             const int nq = min(kChunkBlocks, nbp - b0) / 4;
             const bool ok = pipe_wait(P, P.full + slot, phase, true);
@@ -210,9 +209,8 @@ struct Consumer {
 #pragma unroll
                         for (int c = 0; c < NC; ++c) {
                             const float2 dx2 = *reinterpret_cast<const float2 *>(dxs[c] + bq + jj);
-                            const float2 sf = __fadd2_rn(make_float2(__int_as_float(sa[c]), __int_as_float(sb[c])),
-                                                         neg_magic);
-                            acc2[c] = __ffma2_rn(__fmul2_rn(dw, dx2), sf, acc2[c]);
+                            acc2[c].x = fmaf(dw.x * dx2.x, __int_as_float(sa[c]) - kMagic, acc2[c].x);
+                            acc2[c].y = fmaf(dw.y * dx2.y, __int_as_float(sb[c]) - kMagic, acc2[c].y);
                         }
                     }
                 }
@@ -232,7 +230,6 @@ struct Consumer {
 // accumulated over the rest.
 __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
                                            const int *col_off, int ncols, float *part, int warp, int lane) {
-    const float2 neg_magic = make_float2(-kMagic, -kMagic);
     for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
         const int nq = min(kChunkBlocks, nbp - b0) / 4;
         const uint32_t slot = co.slot;
@@ -257,9 +254,9 @@ __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp,
                         block_dots<1>(co.cb, qs_s[(q * 4 + jj) * 32 + lane], &act, bq + jj, sa);
                         block_dots<1>(co.cb, qs_s[(q * 4 + jj + 1) * 32 + lane], &act, bq + jj + 1, sb);
                         const float2 dx2 = *reinterpret_cast<const float2 *>(dxs + bq + jj);
-                        const float2 sf =
-                            __fadd2_rn(make_float2(__int_as_float(sa[0]), __int_as_float(sb[0])), neg_magic);
-                        acc = __ffma2_rn(__fmul2_rn(jj == 0 ? dw01 : dw23, dx2), sf, acc);
+                        const float2 dw = jj == 0 ? dw01 : dw23;
+                        acc.x = fmaf(dw.x * dx2.x, __int_as_float(sa[0]) - kMagic, acc.x);
+                        acc.y = fmaf(dw.y * dx2.y, __int_as_float(sb[0]) - kMagic, acc.y);
                     }
                 }
                 float *dst = part + c * 32 + lane;
