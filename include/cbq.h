@@ -163,6 +163,31 @@ int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok,
  * overlap of one kernel's start with the previous one's end is lost).  Pass NULL for all four to stop.  The events stay owned by the caller. */
 int cbq_moe_set_stage_events(cbq_moe *L, void *ev_quant, void *ev_gate_up, void *ev_down, void *ev_end);
 
+/* ---- allocation-free dense path --------------------------------------- */
+
+/* Largest K cbq_matvec_static accepts (its scratch holds CBQ_MAX_COLS columns
+ * of this many quantized values plus their scales: 92,160 bytes per device). */
+#define CBQ_STATIC_SCRATCH_MAX_K 16384
+
+/* cbq_matvec for callers that must not allocate device memory while they run:
+ * code recording a CUDA graph by stream capture (where a cudaMalloc would not
+ * be part of the graph and may break the capture), or hosts that fix their
+ * device memory budget at start-up and forbid allocation afterwards.  The
+ * pages describe no counterpart; it is the dense path of cbq_matvec with one
+ * difference: the quantized activations go to a scratch array the library
+ * declares statically on every device (it lives as long as the library is
+ * loaded), not to the handle's workspace.  Nothing is allocated or freed,
+ * here or in any library routine it calls.
+ *   - Arguments as cbq_matvec; K of W must be <= CBQ_STATIC_SCRATCH_MAX_K,
+ *     else CBQ_EINVAL (checked before anything runs).
+ *   - The first call on a device looks the scratch array up on that device
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - The scratch is one array per device shared by every call of this entry
+ *     point on that device, whatever the handle: calls that may overlap on the
+ *     GPU (different streams without ordering) race.  Every call rewrites the
+ *     part it reads, so no contents carry over from the previous call. */
+int cbq_matvec_static(const cbq_weights *W, const float *x_dev, int n, float *y_dev, void *stream);
+
 /* Reads and clears the device error word of the current device (bits
  * CBQ_DEVERR_*).  Synchronizes the device. */
 int cbq_get_device_error(unsigned int *code);

@@ -24,6 +24,7 @@ CBQ_MAX_COLS = 5
 CBQ_MAX_TOKENS = 5
 CBQ_MAX_TOPK = 16
 CBQ_DEVERR_BAD_EXPERT_ID = 0x1
+CBQ_STATIC_SCRATCH_MAX_K = 16384
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -38,6 +39,7 @@ _SIGS = {
     "cbq_matvec_q": ([_P, _P, _P, _I, _P, _P], _I),
     "cbq_matvec": ([_P, _P, _I, _P, _P], _I),
     "cbq_matvec_host": ([_P, _P, _I, _P, _P], _I),
+    "cbq_matvec_static": ([_P, _P, _I, _P, _P], _I),
     "cbq_moe_create": ([_P, _P, _I, _I64, _I64, _I, _P, ctypes.POINTER(_P)], _I),
     "cbq_moe_destroy": ([_P], _I),
     "cbq_moe_info": ([_P, ctypes.POINTER(_I), ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)], _I),
@@ -251,6 +253,18 @@ def cbq_matvec(W: Weights, x, y=None, stream=None):
     y = _y_out(y, n, W.M, x.device)
     _check(load().cbq_matvec(W.handle, _dev_ptr(x, torch.float32, "x"), n, _dev_ptr(y, torch.float32, "y"),
                              _stream(stream)), "cbq_matvec")
+    return y
+
+
+def cbq_matvec_static(W: Weights, x, y=None, stream=None):
+    """cbq_matvec without touching the handle's workspace: the quantized
+    activations go to the library's static per-device scratch (no device
+    memory is allocated by this call)."""
+    torch = _torch()
+    n = x.reshape(-1, W.K).shape[0]
+    y = _y_out(y, n, W.M, x.device)
+    _check(load().cbq_matvec_static(W.handle, _dev_ptr(x, torch.float32, "x"), n, _dev_ptr(y, torch.float32, "y"),
+                                    _stream(stream)), "cbq_matvec_static")
     return y
 
 

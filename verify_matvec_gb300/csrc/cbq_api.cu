@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 using cbq::DevMat;
@@ -262,6 +263,51 @@ int cbq_matvec_host(const cbq_weights *W, const float *x_host, int n, float *y_h
     if (rc != CBQ_OK) return rc;
     CBQ_CUDA(cudaMemcpyAsync(y_host, W->st_y, (size_t)n * W->mat.M * sizeof(float), cudaMemcpyDeviceToHost, s));
     CBQ_CUDA(cudaStreamSynchronize(s));
+    return CBQ_OK;
+}
+
+// ------------------------------------------------ allocation-free path ---
+
+// Scratch of cbq_matvec_static: quantized activations (CBQ_MAX_COLS x
+// CBQ_STATIC_SCRATCH_MAX_K int8) then their scales (CBQ_MAX_COLS x K/32
+// fp32), one copy per device for the life of the library.
+constexpr size_t kStaticQxBytes = (size_t)CBQ_MAX_COLS * CBQ_STATIC_SCRATCH_MAX_K;
+constexpr size_t kStaticDxBytes = (size_t)CBQ_MAX_COLS * (CBQ_STATIC_SCRATCH_MAX_K / CBQ_QK) * sizeof(float);
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticQxBytes + kStaticDxBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+unsigned char *g_static_ptr[kMaxDevices] = {};  // device address per device, found on first use
+
+// Device address of the scratch on the current device (looked up once per
+// device; the host-side symbol is not a device address).
+int static_scratch(int dev, unsigned char **out) {
+    if (dev < 0 || dev >= kMaxDevices) return CBQ_EDEVICE;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_static_scratch)");
+        g_static_ptr[dev] = static_cast<unsigned char *>(p);
+    }
+    *out = g_static_ptr[dev];
+    return CBQ_OK;
+}
+}  // namespace
+
+int cbq_matvec_static(const cbq_weights *W, const float *x_dev, int n, float *y_dev, void *stream) {
+    if (!W || !x_dev || !y_dev || n < 1 || n > CBQ_MAX_COLS || W->K > CBQ_STATIC_SCRATCH_MAX_K) return CBQ_EINVAL;
+    DeviceScope scope(W->device);
+    CBQ_CUDA(scope.status());
+    unsigned char *scratch = nullptr;
+    const int rc = static_scratch(W->device, &scratch);
+    if (rc != CBQ_OK) return rc;
+    int8_t *qx = reinterpret_cast<int8_t *>(scratch);
+    float *dx = reinterpret_cast<float *>(scratch + kStaticQxBytes);
+    cudaStream_t s = as_stream(stream);
+    CBQ_CUDA(cbq::launch_quantize(x_dev, W->K, n, qx, dx, s));
+    CBQ_CUDA(cbq::launch_matvec(W->mat, qx, dx, n, y_dev, s, /*pdl=*/true));
     return CBQ_OK;
 }
 
