@@ -35,7 +35,12 @@ constexpr int kPipeThreads = kConsumers + 32;   // + one producer warp
 constexpr int kChunkBlocks = 32;                 // block columns per stage
 constexpr int kStageQsBytes = kChunkBlocks * 512;
 constexpr int kStageBytes = kStageQsBytes + kChunkBlocks / 4 * 256;  // 18,432
-constexpr uint32_t kSpinLimit = 1u << 22;
+// Bounded waits: each poll may suspend the warp for up to kSuspendNs (it
+// resumes as soon as the phase completes), and at most kSpinLimit polls are
+// made (milliseconds to seconds, depending on how long each poll sleeps)
+// before the wait gives up.
+constexpr uint32_t kSuspendNs = 20000;
+constexpr uint32_t kSpinLimit = 1u << 18;
 constexpr unsigned kErrPipeTimeout = 0x100u;
 
 // The device error word, defined by the translation unit that includes this
@@ -53,10 +58,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -97,7 +102,7 @@ struct Pipe {
 __device__ __forceinline__ bool pipe_wait(const Pipe &P, uint64_t *bar, uint32_t parity, bool check_abort) {
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (check_abort && (i & 31u) == 31u && *(volatile int *)P.abort) return false;
+        if (check_abort && *(volatile int *)P.abort) return false;
     }
     atomicOr(&g_device_error, kErrPipeTimeout);
     *(volatile int *)P.abort = 1;
