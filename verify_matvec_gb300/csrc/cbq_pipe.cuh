@@ -35,12 +35,10 @@ constexpr int kPipeThreads = kConsumers + 32;   // + one producer warp
 constexpr int kChunkBlocks = 32;                 // block columns per stage
 constexpr int kStageQsBytes = kChunkBlocks * 512;
 constexpr int kStageBytes = kStageQsBytes + kChunkBlocks / 4 * 256;  // 18,432
-// Bounded waits: each poll may suspend the warp for up to kSuspendNs (it
-// resumes as soon as the phase completes), and at most kSpinLimit polls are
-// made (milliseconds to seconds, depending on how long each poll sleeps)
-// before the wait gives up.
-constexpr uint32_t kSuspendNs = 20000;
-constexpr uint32_t kSpinLimit = 1u << 18;
+// Bounded waits: each poll may suspend the warp for a hardware-chosen time
+// (it resumes as soon as the phase completes); at most kSpinLimit polls are
+// made before the wait gives up.
+constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr unsigned kErrPipeTimeout = 0x100u;
 
 // The device error word, defined by the translation unit that includes this
@@ -58,10 +56,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendNs)
+        : "r"(smem_addr(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
