@@ -33,8 +33,10 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 // Consumer warps form two teams of four; a pass's even stages go to team 0 and
 // its odd stages to team 1, each warp taking a quarter of its team's stages'
-// quads.  A warp thus handles 8 blocks per stage it takes and waits on half of
-// the stages, and a stage is released by the 4 warps of one team.
+// quads, so a warp handles 8 blocks per stage it takes and a stage is
+// released by the 4 warps of one team.  A team still waits for the stages it
+// skips (without reading or releasing them): mbarrier phases are told apart by
+// parity only, so no waiter may fall two uses of a slot behind.
 constexpr int kTeamWarps = kConsumerWarps / 2;
 constexpr int kPipeThreads = kConsumers + 32;   // + one producer warp
 constexpr int kChunkBlocks = 32;                 // block columns per stage
@@ -194,7 +196,8 @@ struct Consumer {
                                           float2 acc2[NC], int warp, int lane) {
         const int team = warp / kTeamWarps, tw = warp % kTeamWarps;
         for (int b0 = 0, st_i = 0; b0 < nbp; b0 += kChunkBlocks, ++st_i) {
-            if ((st_i & 1) != team) {  // the other team's stage
+            if ((st_i & 1) != team) {  // the other team's stage: keep phase step only
+                pipe_wait(P, P.full + slot, phase, true);
                 advance(P);
                 continue;
             }
@@ -245,9 +248,10 @@ __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp,
                                            const int *col_off, int ncols, float *part, int warp, int lane) {
     const int team = warp / kTeamWarps, tw = warp % kTeamWarps;
     for (int b0 = 0, st_i = 0; b0 < nbp; b0 += kChunkBlocks, ++st_i) {
-        if ((st_i & 1) != team) {  // the other team's stage
+        if ((st_i & 1) != team) {  // the other team's stage: keep phase step only
             if (b0 == 0)
                 for (int c = 0; c < ncols; ++c) part[c * 32 + lane] = 0.0f;
+            pipe_wait(P, P.full + co.slot, co.phase, true);
             co.advance(P);
             continue;
         }
