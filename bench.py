@@ -230,6 +230,20 @@ def gpu_ident(torch, local):
         return parts[local] if local < len(parts) else local
 
 
+def aggregate(times_ms, weight_bytes, world, device=None):
+    """Whole-job numbers of independent replicas: the slowest rank's time
+    (max over ranks of each entry of times_ms) and the bytes of all ranks.
+    Returns (max_times_ms list, GB/s of each time)."""
+    import torch
+    t = torch.tensor(list(times_ms), dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total = float(weight_bytes) * world
+    tmax = [float(v) for v in t.cpu()]
+    return tmax, [total / (v * 1e-3) / 1e9 for v in tmax]
+
+
 def build_layer(torch, cbq, n_exp=E, with_head=True):
     """All experts drawn from their seeded streams, repacked on device."""
     gu = np.empty((n_exp, 2 * F, H // QK, BB), dtype=np.uint8)
@@ -436,13 +450,7 @@ def run_gpu(args):
     b5_us, b5_gbs, b5_split = layer_us(5, 8)
 
     # slowest rank decides; bytes add up over ranks
-    my = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(my, op=dist.ReduceOp.MAX)
-    ms_max, e2e_max = float(my[0]), float(my[1])
-    total_bytes = sum(wbytes) * world
-    value = total_bytes / (ms_max * 1e-3) / 1e9
-    e2e_value = total_bytes / (e2e_max * 1e-3) / 1e9
+    (ms_max, e2e_max), (value, e2e_value) = aggregate([ms, e2e_ms], sum(wbytes), world, dev)
     h2d = N_TOK * H * 4 + 2 * slots * 4 + HEAD_N * HEAD_K * 4
     d2h = N_TOK * H * 4 + HEAD_N * HEAD_M * 4
 
