@@ -31,13 +31,6 @@ namespace cbq {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-// Consumer warps form two teams of four; a pass's even stages go to team 0 and
-// its odd stages to team 1, each warp taking a quarter of its team's stages'
-// quads, so a warp handles 8 blocks per stage it takes and a stage is
-// released by the 4 warps of one team.  A team still waits for the stages it
-// skips (without reading or releasing them): mbarrier phases are told apart by
-// parity only, so no waiter may fall two uses of a slot behind.
-constexpr int kTeamWarps = kConsumerWarps / 2;
 constexpr int kPipeThreads = kConsumers + 32;   // + one producer warp
 constexpr int kChunkBlocks = 32;                 // block columns per stage
 constexpr int kStageQsBytes = kChunkBlocks * 512;
@@ -194,20 +187,14 @@ struct Consumer {
     template <int NC>
     __device__ __forceinline__ void group(const Pipe &P, int nbp, const uint4 *const *act, const float *const *dxs,
                                           float2 acc2[NC], int warp, int lane) {
-        const int team = warp / kTeamWarps, tw = warp % kTeamWarps;
-        for (int b0 = 0, st_i = 0; b0 < nbp; b0 += kChunkBlocks, ++st_i) {
-            if ((st_i & 1) != team) {  // the other team's stage: keep phase step only
-                pipe_wait(P, P.full + slot, phase, true);
-                advance(P);
-                continue;
-            }
+        for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
             const int nq = min(kChunkBlocks, nbp - b0) / 4;
             const bool ok = pipe_wait(P, P.full + slot, phase, true);
             if (ok) {
                 const unsigned char *st = P.ring + (size_t)slot * kStageBytes;
                 const uint4 *qs_s = reinterpret_cast<const uint4 *>(st);
                 const uint2 *sc_s = reinterpret_cast<const uint2 *>(st + kStageQsBytes);
-                const int q0 = tw * nq / kTeamWarps, q1 = (tw + 1) * nq / kTeamWarps;
+                const int q0 = warp * nq / kConsumerWarps, q1 = (warp + 1) * nq / kConsumerWarps;
                 for (int q = q0; q < q1; ++q) {
                     const uint2 s = sc_s[q * 32 + lane];
                     const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
@@ -246,15 +233,7 @@ struct Consumer {
 // accumulated over the rest.
 __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
                                            const int *col_off, int ncols, float *part, int warp, int lane) {
-    const int team = warp / kTeamWarps, tw = warp % kTeamWarps;
-    for (int b0 = 0, st_i = 0; b0 < nbp; b0 += kChunkBlocks, ++st_i) {
-        if ((st_i & 1) != team) {  // the other team's stage: keep phase step only
-            if (b0 == 0)
-                for (int c = 0; c < ncols; ++c) part[c * 32 + lane] = 0.0f;
-            pipe_wait(P, P.full + co.slot, co.phase, true);
-            co.advance(P);
-            continue;
-        }
+    for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
         const int nq = min(kChunkBlocks, nbp - b0) / 4;
         const uint32_t slot = co.slot;
         const bool ok = pipe_wait(P, P.full + slot, co.phase, true);
@@ -262,7 +241,7 @@ __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp,
             const unsigned char *st = P.ring + (size_t)slot * kStageBytes;
             const uint4 *qs_s = reinterpret_cast<const uint4 *>(st);
             const uint2 *sc_s = reinterpret_cast<const uint2 *>(st + kStageQsBytes);
-            const int q0 = tw * nq / kTeamWarps, q1 = (tw + 1) * nq / kTeamWarps;
+            const int q0 = warp * nq / kConsumerWarps, q1 = (warp + 1) * nq / kConsumerWarps;
             for (int c = 0; c < ncols; ++c) {
                 const uint4 *act = act0 + (size_t)col_off[c] * 2;
                 const float *dxs = dx0 + col_off[c];
@@ -343,7 +322,7 @@ __device__ __forceinline__ void pipe_init(const Pipe &P) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < P.S; ++s) {
             mbar_init(P.full + s, 1);
-            mbar_init(P.empty + s, kTeamWarps);
+            mbar_init(P.empty + s, kConsumerWarps);
         }
         *P.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
