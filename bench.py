@@ -54,7 +54,7 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILED = {
     "source_digest": "ac63a93b947afbb0",
     "k_matvec<5> (head)": 297_941_760 + 11_359_488,          # one launch, 129280 x 4096, n=5
-    "k_moe_gate_up per expert": (339_849_728 + 9_504_256) / 36,  # launch with 36 distinct experts
+    "k_moe per expert": None,
 }
 
 
@@ -314,22 +314,21 @@ def run_gpu(args):
     dx = torch.empty((HEAD_N, HEAD_K // QK), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     total = args.warmup + args.steps
-    ev = [[timing_event(torch, stream) for _ in range(7)] for _ in range(total)]
+    ev = [[timing_event(torch, stream) for _ in range(5)] for _ in range(total)]
     torch.cuda.synchronize()
 
     def step(i, events):
+        # events: layer kernel start, combine start, combine end, head start, head end
         ids, wts, h, x = d_sets[i % N_SETS]
         if events is not None:
-            cbq.cbq_moe_set_stage_events(L, events[0:4])
+            cbq.cbq_moe_set_stage_events(L, events[0:3])
         cbq.cbq_moe_matvec(L, h, ids, wts, swiglu=1, y=y)
-        if events is not None:
-            events[4].record(stream)
         cbq.cbq_quantize_act(x, qx, dx)
         if events is not None:
-            events[5].record(stream)
+            events[3].record(stream)
         cbq.cbq_matvec_q(head, qx, dx, y=yh)
         if events is not None:
-            events[6].record(stream)
+            events[4].record(stream)
 
     # untimed warm-up
     for i in range(args.warmup):
@@ -355,18 +354,18 @@ def run_gpu(args):
 
     timed = range(args.warmup, total)
     wbytes = [distinct[i % N_SETS] * EXPERT_BYTES + HEAD_BYTES for i in timed]
-    k_gate = [ev[i][1].elapsed_time(ev[i][2]) for i in timed]
-    k_down = [ev[i][2].elapsed_time(ev[i][3]) for i in timed]
-    k_head = [ev[i][5].elapsed_time(ev[i][6]) for i in timed]
-    k_quant = [ev[i][0].elapsed_time(ev[i][1]) + ev[i][4].elapsed_time(ev[i][5]) for i in timed]
+    k_moe = [ev[i][0].elapsed_time(ev[i][1]) for i in timed]
+    k_comb = [ev[i][1].elapsed_time(ev[i][2]) for i in timed]
+    k_quant = [ev[i][2].elapsed_time(ev[i][3]) for i in timed]
+    k_head = [ev[i][3].elapsed_time(ev[i][4]) for i in timed]
     err = cbq.cbq_get_device_error()
 
     # per-launch algorithmic bytes: weights + activations read + outputs written
-    act_h = N_TOK * H * (1 + 4 / QK)
     slots = N_TOK * TOPK
-    gate_alg = [distinct[i % N_SETS] * GATE_UP_BYTES + act_h + slots * F * (1 + 4 / QK) for i in timed]
+    moe_io = 4 * N_TOK * H + 2 * slots * F * (1 + 4 / QK) + 4 * slots * H  # h in, qa/da out+in, obuf out
+    moe_alg = [distinct[i % N_SETS] * EXPERT_BYTES + moe_io for i in timed]
     head_alg = HEAD_BYTES + HEAD_N * HEAD_K * (1 + 4 / QK) + 4 * HEAD_N * HEAD_M
-    kern = {"k_moe_gate_up": (sum(k_gate), sum(gate_alg) / len(k_gate)),
+    kern = {"k_moe (quantize + gate_up + down)": (sum(k_moe), sum(moe_alg) / len(k_moe)),
             "k_matvec<5> (head)": (sum(k_head), head_alg)}
     dom = max(kern, key=lambda k: kern[k][0])
     dom_ms, dom_bytes = kern[dom][0] / len(timed), kern[dom][1]
@@ -377,13 +376,13 @@ def run_gpu(args):
         if dom.startswith("k_matvec"):
             traffic = PROFILED["k_matvec<5> (head)"]
         else:
-            traffic = PROFILED["k_moe_gate_up per expert"] * sum(distinct[i % N_SETS] for i in timed) / len(timed)
+            traffic = PROFILED["k_moe per expert"] * sum(distinct[i % N_SETS] for i in timed) / len(timed)
 
     if args.profile:
         if rank == 0:
             print(json.dumps({"profile": True, "ms_per_step": ms / args.steps, "experts": n_exp,
-                              "kernels_ms_per_step": {"k_moe_gate_up": sum(k_gate) / len(timed),
-                                                      "k_moe_down": sum(k_down) / len(timed),
+                              "kernels_ms_per_step": {"k_moe": sum(k_moe) / len(timed),
+                                                      "k_moe_combine": sum(k_comb) / len(timed),
                                                       "head": sum(k_head) / len(timed)},
                               "device_error": err}), flush=True)
         if world > 1:
@@ -430,7 +429,7 @@ def run_gpu(args):
             cbq.cbq_moe_matvec(L, t[2], t[0], t[1], y=yl)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        stage_ev = [[timing_event(torch, stream) for _ in range(4)] for _ in range(reps)]
+        stage_ev = [[timing_event(torch, stream) for _ in range(3)] for _ in range(reps)]
         torch.cuda.synchronize()
         a.record(stream)
         nbytes = 0
@@ -443,7 +442,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         cbq.cbq_moe_set_stage_events(L, None)
         us = 1e3 * a.elapsed_time(b) / reps
-        split = [1e3 * sum(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev) / reps for j in range(3)]
+        split = [1e3 * sum(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev) / reps for j in range(2)]
         return us, nbytes / reps / (us * 1e-6) / 1e9, split
 
     b1_us, b1_gbs, b1_split = layer_us(1, 4)
@@ -476,17 +475,17 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": {"batch1_top4": b1_us, "batch5_top8": b5_us,
                              "batch1_weight_gbs": b1_gbs, "batch5_weight_gbs": b5_gbs,
-                             "split_us_quant_gateup_down": {"batch1": b1_split, "batch5": b5_split}},
-            "kernels_ms_per_step": {"quantize(x2)": sum(k_quant) / len(timed),
-                                    "k_moe_gate_up": sum(k_gate) / len(timed),
-                                    "k_moe_down": sum(k_down) / len(timed),
+                             "split_us_layer_combine": {"batch1": b1_split, "batch5": b5_split}},
+            "kernels_ms_per_step": {"k_moe (quantize + gate_up + down)": sum(k_moe) / len(timed),
+                                    "k_moe_combine": sum(k_comb) / len(timed),
+                                    "k_quantize (head input)": sum(k_quant) / len(timed),
                                     "k_matvec<5> (head)": sum(k_head) / len(timed)},
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 6 * args.steps,  # per step: quantize, gate_up, down, combine; quantize, head matvec
+            "gpu_launches": 4 * args.steps,  # per step: layer kernel, combine; quantize, head matvec
             "clocks": clk,
             "device_error": err,
         }

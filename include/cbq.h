@@ -157,11 +157,12 @@ int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok,
                         float *y_host, void *stream);
 
 /* Stage timing: when set, cbq_moe_matvec records these CUDA events
- * (cudaEvent_t passed as void*) on its stream before the activation
- * quantization, before the gate_up kernel, before the down kernel and after
- * the combine that ends the call.  Recording them separates the kernels (the
- * overlap of one kernel's start with the previous one's end is lost).  Pass NULL for all four to stop.  The events stay owned by the caller. */
-int cbq_moe_set_stage_events(cbq_moe *L, void *ev_quant, void *ev_gate_up, void *ev_down, void *ev_end);
+ * (cudaEvent_t passed as void*) on its stream before the layer kernel
+ * (quantization, gate_up + SwiGLU + requantization, down), before the combine
+ * kernel and after it.  Recording them separates the two kernels (the overlap
+ * of the combine's start with the layer kernel's end is lost).  Pass NULL for
+ * all three to stop.  The events stay owned by the caller. */
+int cbq_moe_set_stage_events(cbq_moe *L, void *ev_layer, void *ev_combine, void *ev_end);
 
 /* ---- allocation-free dense path --------------------------------------- */
 

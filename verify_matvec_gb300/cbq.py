@@ -49,7 +49,7 @@ _SIGS = {
     "cbq_debug_block_dots": ([_P, _P, _I, _P, _P], _I),
     "cbq_moe_debug_block_dots": ([_P, _I, _I, _P, _I, _P, _P], _I),
     "cbq_moe_set_debug": ([_P, _I], _I),
-    "cbq_moe_set_stage_events": ([_P, _P, _P, _P, _P], _I),
+    "cbq_moe_set_stage_events": ([_P, _P, _P, _P], _I),
     "cbq_moe_debug_intermediate": ([_P, _I, _P, _P, _P, _P], _I),
 }
 
@@ -332,8 +332,8 @@ def cbq_moe_set_debug(L: Moe, keep: bool):
 
 
 def cbq_moe_set_stage_events(L: Moe, events=None):
-    """events: four torch.cuda.Event(enable_timing=True) or None to stop."""
-    ptrs = [None] * 4 if events is None else [ctypes.c_void_p(ev.cuda_event) for ev in events]
+    """events: three torch.cuda.Event(enable_timing=True) or None to stop."""
+    ptrs = [None] * 3 if events is None else [ctypes.c_void_p(ev.cuda_event) for ev in events]
     _check(load().cbq_moe_set_stage_events(L.handle, *ptrs), "cbq_moe_set_stage_events")
 
 

@@ -7,6 +7,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -335,6 +336,7 @@ int cbq_moe_destroy(cbq_moe *L) {
     cudaFree(L->ws.a_dbg);
     cudaFree(L->ws.obuf);
     cudaFree(L->ws.sched);
+    cudaFree(L->ws.done);
     cudaFree(L->st_h);
     cudaFree(L->st_ids);
     cudaFree(L->st_wts);
@@ -356,8 +358,8 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
     const int nbH = (int)(H / CBQ_QK), nbF = (int)(F / CBQ_QK);
     size_t smem_max = 0;
     CBQ_CUDA(cbq::device_smem_limit(&smem_max));
-    if (cbq::matvec_smem_bytes(cbq::round_up4(nbH), CBQ_MAX_TOKENS) > smem_max ||
-        cbq::matvec_smem_bytes(cbq::round_up4(nbF), CBQ_MAX_COLS) > smem_max)
+    if (cbq::moe_smem_bytes(std::max(CBQ_MAX_TOKENS * cbq::round_up4(nbH), CBQ_MAX_COLS * cbq::round_up4(nbF))) >
+        smem_max)
         return CBQ_EINVAL;
 
     cbq_moe *L = new (std::nothrow) cbq_moe();
@@ -377,6 +379,7 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
         (rc = dev_alloc(&L->ws.a_dbg, slots * F, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.obuf, slots * H, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.sched, 4, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.done, slots, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_h, (size_t)CBQ_MAX_TOKENS * H, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_ids, slots, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_wts, slots, &L->bytes)) != CBQ_OK ||
@@ -385,7 +388,8 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
         return rc;
     }
     cudaStream_t s = as_stream(stream);
-    if (cudaMemsetAsync(L->ws.sched, 0, 4 * sizeof(unsigned), s) != cudaSuccess) {
+    if (cudaMemsetAsync(L->ws.sched, 0, 4 * sizeof(unsigned), s) != cudaSuccess ||
+        cudaMemsetAsync(L->ws.done, 0, slots * sizeof(unsigned), s) != cudaSuccess) {
         cbq_moe_destroy(L);
         return CBQ_ECUDA;
     }
@@ -488,15 +492,14 @@ int cbq_moe_set_debug(cbq_moe *L, int keep_intermediate) {
     return CBQ_OK;
 }
 
-int cbq_moe_set_stage_events(cbq_moe *L, void *ev_quant, void *ev_gate_up, void *ev_down, void *ev_end) {
+int cbq_moe_set_stage_events(cbq_moe *L, void *ev_layer, void *ev_combine, void *ev_end) {
     if (!L) return CBQ_EINVAL;
-    const bool all = ev_quant && ev_gate_up && ev_down && ev_end;
-    const bool none = !ev_quant && !ev_gate_up && !ev_down && !ev_end;
+    const bool all = ev_layer && ev_combine && ev_end;
+    const bool none = !ev_layer && !ev_combine && !ev_end;
     if (!all && !none) return CBQ_EINVAL;
-    L->ws.ev[0] = reinterpret_cast<cudaEvent_t>(ev_quant);
-    L->ws.ev[1] = reinterpret_cast<cudaEvent_t>(ev_gate_up);
-    L->ws.ev[2] = reinterpret_cast<cudaEvent_t>(ev_down);
-    L->ws.ev[3] = reinterpret_cast<cudaEvent_t>(ev_end);
+    L->ws.ev[0] = reinterpret_cast<cudaEvent_t>(ev_layer);
+    L->ws.ev[1] = reinterpret_cast<cudaEvent_t>(ev_combine);
+    L->ws.ev[2] = reinterpret_cast<cudaEvent_t>(ev_end);
     return CBQ_OK;
 }
 

@@ -186,15 +186,18 @@ __device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, co
 // scales).  act_s: ncols x nbp x 2
 // uint4; dx_s: ncols x nbp floats.  Blocks nb..nbp-1 are zero.  Threads
 // tid = 0..nthr-1 share the work.
+// With l2_only the loads bypass L1 (data written by other CTAs of the same
+// kernel).
 __device__ __forceinline__ void stage_cols(const int8_t *const *src, const float *const *dsrc, int ncols,
-                                           int nb, int nbp, uint4 *act_s, float *dx_s, int tid, int nthr) {
+                                           int nb, int nbp, uint4 *act_s, float *dx_s, int tid, int nthr,
+                                           bool l2_only = false) {
     for (int idx = tid; idx < ncols * nbp; idx += nthr) {
         const int c = idx / nbp, b = idx - c * nbp;
         uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
         float d = 0.0f;
         if (b < nb && src[c]) {
             const uint4 *p = reinterpret_cast<const uint4 *>(src[c] + (size_t)b * kQK);
-            const uint4 x0 = p[0], x1 = p[1];
+            const uint4 x0 = l2_only ? __ldcg(p) : p[0], x1 = l2_only ? __ldcg(p + 1) : p[1];
             const uint32_t P[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
             // word 2m   = x[4m], x[4m+16], x[4m+1], x[4m+17]
             // word 2m+1 = x[4m+2], x[4m+18], x[4m+3], x[4m+19]
@@ -202,7 +205,7 @@ __device__ __forceinline__ void stage_cols(const int8_t *const *src, const float
             o0.z = prmt(P[1], P[5], 0x5140u); o0.w = prmt(P[1], P[5], 0x7362u);
             o1.x = prmt(P[2], P[6], 0x5140u); o1.y = prmt(P[2], P[6], 0x7362u);
             o1.z = prmt(P[3], P[7], 0x5140u); o1.w = prmt(P[3], P[7], 0x7362u);
-            if (dsrc) d = dsrc[c][b];
+            if (dsrc) d = l2_only ? __ldcg(dsrc[c] + b) : dsrc[c][b];
         }
         act_s[(size_t)idx * 2] = o0;
         act_s[(size_t)idx * 2 + 1] = o1;
@@ -227,6 +230,31 @@ __device__ __forceinline__ int8_t quant_lane(float v, float &d_out) {
     float q = rintf(v / d);
     q = fminf(fmaxf(q, -127.0f), 127.0f);
     return (int8_t)q;
+}
+
+// Quantize fp32 rows straight into the staged (expander-ordered) layout:
+// block k = t*nbp + b holds row t's values 32b..32b+31 (x[t*ld + 32b ..]);
+// blocks b >= nb are zero.  One warp per block, lane = element; warps w0,
+// w0+step, ... share the blocks.  Same rule and result as quant_lane.
+__device__ __forceinline__ void quant_stage_rows(const float *__restrict__ x, int64_t ld, int nrows, int nb, int nbp,
+                                                 uint4 *act_s, float *dx_s, int w0, int step, int lane) {
+    // byte of element `lane` in the expander order: word 2m+(r>>1), byte
+    // 2*(r&1) + (lane >= 16), with lane%16 = 4m + r
+    const int r4 = lane & 15, m = r4 >> 2, r = r4 & 3;
+    const int pos = (2 * m + (r >> 1)) * 4 + (r & 1) * 2 + (lane >> 4);
+    for (int k = w0; k < nrows * nbp; k += step) {
+        const int t = k / nbp, b = k - t * nbp;
+        unsigned char *blk = reinterpret_cast<unsigned char *>(act_s + (size_t)k * 2);
+        if (b < nb) {
+            float d;
+            const int8_t q = quant_lane(x[(size_t)t * ld + (size_t)b * kQK + lane], d);
+            blk[pos] = (unsigned char)q;
+            if (lane == 0) dx_s[k] = d;
+        } else {
+            if (lane < 8) reinterpret_cast<uint32_t *>(blk)[lane] = 0u;
+            if (lane == 0) dx_s[k] = 0.0f;
+        }
+    }
 }
 
 }  // namespace cbq

@@ -42,9 +42,10 @@ struct MoeWork {
     float *da;        // slots x F/32
     float *a_dbg;     // slots x F (written when keep_a)
     float *obuf;      // slots x H, down-projection output per slot
-    unsigned *sched;  // 4 work counters: gate_up (2), down (2), zero between launches
+    unsigned *sched;  // 4 work counters (items, producers done, CTAs done), zero between launches
+    unsigned *done;   // per expert rank: gate_up columns published (zero between launches)
     int keep_a;
-    cudaEvent_t ev[4];  // optional stage events (before quant, gate_up, down; after combine)
+    cudaEvent_t ev[3];  // optional stage events (before the layer kernel, before the combine, after it)
 };
 
 constexpr int kMaxSlots = 80;  // CBQ_MAX_TOKENS * CBQ_MAX_TOPK
@@ -60,6 +61,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
                        const float *wts, int k, int swiglu, float *y, cudaStream_t s);
 // Largest dynamic shared memory a matvec over K columns with n columns needs.
 size_t matvec_smem_bytes(int nbp, int n);
+size_t moe_smem_bytes(int act_blocks);
 cudaError_t device_smem_limit(size_t *bytes);
 cudaError_t read_and_clear_device_error(unsigned *code);
 

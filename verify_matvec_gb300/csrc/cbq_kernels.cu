@@ -28,9 +28,12 @@ constexpr unsigned kErrBadExpertId = 0x1u;
 // Pipeline depth (stages of 18 KB per CTA, two CTAs per SM) and partial-sum
 // sets of each kernel, sized so two CTAs fit in an SM's shared memory.
 constexpr int kStages = 4;
-constexpr int kStagesGateUp = 3;
+constexpr int kStagesMoe = 3;
 constexpr int kSetsMatvec = 2;   // double-buffered
-constexpr int kSetsGateUp = 4;   // gate + up, double-buffered
+constexpr int kSetsMoe = 4;      // gate + up, double-buffered (down uses two of them)
+
+// Dynamic shared memory of the routed-expert kernel.
+size_t moe_smem_bytes(int act_blocks) { return pipe_smem_bytes(kStagesMoe, 1, act_blocks, kSetsMoe); }
 
 // Launch with optional programmatic stream serialization (PDL).
 template <typename... KArgs, typename... Args>
@@ -334,11 +337,13 @@ cudaError_t launch_block_dots(const DevMat &W, const int8_t *qx, int n, int32_t 
 struct MoeArgs {
     DevMoe L;
     MoeWork ws;
+    const float *h;
     const int32_t *ids;
     const float *wts;
     float *y;
     int n_tok, k, swiglu;
     int nbH, nbpH, nbF, nbpF;
+    int act_blocks;  // staged-activation capacity in blocks (tokens, then down columns)
 };
 
 // Distinct in-range expert ids of the routing table, ascending, computed
@@ -402,13 +407,23 @@ __device__ __forceinline__ int expert_ns(const Routing &R, int u, int N) {
 
 __device__ __forceinline__ int col_chunks(int ns) { return (ns + kMaxCols - 1) / kMaxCols; }
 
+constexpr unsigned kErrDependencyTimeout = 0x200u;
+constexpr uint32_t kDependencyPolls = 1u << 22;
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Gate rows (first pass) and up rows (second pass) of one 32-row-pair group
 // over the whole K for the columns (slots) R.slots[c0..c0+nc), then the
 // SwiGLU split and the requantization of the 32 outputs of each column.
 // Partial sets: gate sums in set 2*buf, up sums in set 2*buf+1, each
-// [warp][column][lane].
+// [warp][column][lane].  Each writer warp then publishes its column for expert
+// rank u (fence, then one count in done[u]).
 __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
-                                             int g, int c0, int nc, int warp, int lane, int buf) {
+                                             int u, int g, int c0, int nc, int warp, int lane, int buf) {
     int col_off[kMaxCols];  // activation column of each slot: its token's column
 #pragma unroll
     for (int c = 0; c < kMaxCols; ++c) col_off[c] = (c < nc ? R.slots[c0 + c] / A.k : 0) * A.nbpH;
@@ -433,74 +448,9 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
         A.ws.qa[o] = q;
         if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
         if (A.ws.keep_a) A.ws.a_dbg[o] = a;
-    }
-}
-
-// Items are (expert rank u, 32-row-pair group g), u-major, fetched one at a
-// time.  The producer streams, per item and column chunk, the gate group g
-// then the up group g + F/32 of expert uniq[u].
-__global__ void __launch_bounds__(kPipeThreads, 2) k_moe_gate_up(const __grid_constant__ MoeArgs A) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ Routing R;
-    pdl_trigger();
-    const int N = A.n_tok * A.k;
-    route(A.ids, N, A.L.E, R, blockIdx.x == 0);
-    const int Gf = A.L.F / 32;
-    const unsigned total = (unsigned)(R.D * Gf);
-    unsigned *sched = A.ws.sched;
-    const PipeSmem S = carve_pipe(smem, kStagesGateUp, A.n_tok, A.nbpH);
-    pipe_init(S.pipe);
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nbq = A.nbpH / 4;
-    if (warp == kConsumerWarps) {  // producer
-        if (lane == 0) {
-            Producer pr;
-            unsigned nxt = atomicAdd(sched, 1u);
-            while (nxt < total && !pr.stopped) {
-                const int it = (int)nxt;
-                nxt = atomicAdd(sched, 1u);
-                const int u = it / Gf, g = it - u * Gf;
-                const size_t e = (size_t)R.uniq[u];
-                const int nch = col_chunks(expert_ns(R, u, N));
-                for (int ch = 0; ch < nch; ++ch) {
-                    for (int half = 0; half < 2; ++half) {
-                        const size_t grp = (size_t)g + (size_t)half * Gf;
-                        pr.group(S.pipe, A.L.gu_qs + e * A.L.gu_qs_stride + grp * A.nbpH * 32,
-                                 A.L.gu_sc + e * A.L.gu_sc_stride + grp * nbq * 32, A.nbpH, it);
-                    }
-                }
-            }
-            __threadfence();
-            sched_exit(sched);
-            pr.finish(S.pipe);
-            pr.drain(S.pipe);
-        }
-        return;
-    }
-    pdl_wait();  // the quantized tokens come from the kernel launched just before
-    {
-        const int8_t *src[kMaxCols];
-        const float *dsrc[kMaxCols];
-        for (int t = 0; t < A.n_tok; ++t) {
-            src[t] = A.ws.qh + (size_t)t * A.L.H;
-            dsrc[t] = A.ws.dh + (size_t)t * A.nbH;
-        }
-        stage_cols(src, dsrc, A.n_tok, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
-    }
-    Consumer co;
-    int cur_u = -1, item = 0;
-    for (;;) {
-        const int it = co.peek(S.pipe);
-        if (it < 0) break;
-        const int u = it / Gf, g = it - u * Gf;
-        if (u != cur_u) {
-            consumer_sync();
-            expert_slots(R, u, N);
-            cur_u = u;
-        }
-        for (int c0 = 0; c0 < R.ns; c0 += kMaxCols, ++item)
-            gate_up_item(A, R, S, co, g, c0, min(kMaxCols, R.ns - c0), warp, lane, item & 1);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(A.ws.done + u, 1u);
     }
 }
 
@@ -524,43 +474,56 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, co
     }
 }
 
-// Items are (expert rank u, 32-row group g), u-major, fetched by guided
-// self-scheduling: a grab takes about remaining/(2 x CTAs) consecutive items
-// (at most kDownGrab), so early grabs keep one expert's staged intermediate
-// columns for several items and the last grabs are single items.
-constexpr unsigned kDownGrab = 8;
-
-__global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(const __grid_constant__ MoeArgs A) {
+// The whole routed-expert layer but the combine, in one persistent kernel.
+// Work items, handed out in this order by one counter:
+//   it <  D*Gf : gate_up item (expert rank u, 32-row-pair group g), u-major;
+//   it >= D*Gf : down item (expert rank u, 32-row group g), u-major.
+// A CTA fetches a down item only after every gate_up item has been fetched,
+// and the fetched gate_up items are processed by running CTAs without waiting
+// on anything, so a down item's wait for its expert's intermediate
+// (done[u] == Gf * ns) always ends; it is bounded all the same.
+// The producer streams a down item's weights before that wait ends.
+__global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__ MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
-    const int N = A.n_tok * A.k;
-    route(A.ids, N, A.L.E, R, false);
-    const int Gd = A.L.H / 32;
     pdl_trigger();  // the combine kernel may launch; it waits for this grid
-    if (R.D == 0) return;  // nothing routed: the combine writes zeros
-    const unsigned total = (unsigned)(R.D * Gd);
-    unsigned *sched = A.ws.sched + 2;
-    const PipeSmem S = carve_pipe(smem, kStages, kMaxCols, A.nbpF);
+    const int N = A.n_tok * A.k;
+    route(A.ids, N, A.L.E, R, blockIdx.x == 0);
+    const int Gf = A.L.F / 32, Gd = A.L.H / 32;
+    const unsigned total_gu = (unsigned)(R.D * Gf);
+    const unsigned total = total_gu + (unsigned)(R.D * Gd);
+    unsigned *sched = A.ws.sched;
+    const PipeSmem S = carve_pipe(smem, kStagesMoe, 1, A.act_blocks);
     pipe_init(S.pipe);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nbq = A.nbpF / 4;
     if (warp == kConsumerWarps) {  // producer
         if (lane == 0) {
             Producer pr;
-            for (;;) {
-                const unsigned seen = *(volatile unsigned *)sched;
-                if (seen >= total || pr.stopped) break;
-                const unsigned grab = max(1u, min(kDownGrab, (total - seen) / (2u * gridDim.x)));
-                const unsigned base = atomicAdd(sched, grab);
-                if (base >= total) break;
-                for (unsigned it = base; it < min(total, base + grab) && !pr.stopped; ++it) {
-                    const int u = (int)it / Gd, g = (int)it - u * Gd;
+            const int nbqH = A.nbpH / 4, nbqF = A.nbpF / 4;
+            unsigned nxt = atomicAdd(sched, 1u);
+            while (nxt < total && !pr.stopped) {
+                const unsigned it = nxt;
+                nxt = atomicAdd(sched, 1u);
+                if (it < total_gu) {
+                    const int u = (int)it / Gf, g = (int)it - u * Gf;
+                    const size_t e = (size_t)R.uniq[u];
+                    const int nch = col_chunks(expert_ns(R, u, N));
+                    for (int ch = 0; ch < nch; ++ch) {
+                        for (int half = 0; half < 2; ++half) {
+                            const size_t grp = (size_t)g + (size_t)half * Gf;
+                            pr.group(S.pipe, A.L.gu_qs + e * A.L.gu_qs_stride + grp * A.nbpH * 32,
+                                     A.L.gu_sc + e * A.L.gu_sc_stride + grp * nbqH * 32, A.nbpH, (int)it);
+                        }
+                    }
+                } else {
+                    const int j = (int)(it - total_gu);
+                    const int u = j / Gd, g = j - u * Gd;
                     const size_t e = (size_t)R.uniq[u];
                     const int nch = col_chunks(expert_ns(R, u, N));
                     for (int ch = 0; ch < nch; ++ch)
                         pr.group(S.pipe, A.L.dn_qs + e * A.L.dn_qs_stride + (size_t)g * A.nbpF * 32,
-                                 A.L.dn_sc + e * A.L.dn_sc_stride + (size_t)g * nbq * 32, A.nbpF, (int)it);
+                                 A.L.dn_sc + e * A.L.dn_sc_stride + (size_t)g * nbqF * 32, A.nbpF, (int)it);
                 }
             }
             __threadfence();
@@ -570,22 +533,48 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(const __grid_const
         }
         return;
     }
-    pdl_wait();  // qa/da come from the gate_up kernel launched just before
+    // consumers: quantize the tokens straight into the staged layout
+    quant_stage_rows(A.h, A.L.H, A.n_tok, A.nbH, A.nbpH, S.act, S.dx, warp, kConsumerWarps, lane);
+    consumer_sync();
     Consumer co;
     int cur_u = -1, staged_u = -1, item = 0;
+    bool down_phase = false;
     for (;;) {
         const int it = co.peek(S.pipe);
         if (it < 0) break;
-        const int u = it / Gd, g = it - u * Gd;
-        if (u != cur_u) {
-            consumer_sync();
+        if ((unsigned)it < total_gu) {
+            const int u = it / Gf, g = it - u * Gf;
+            if (u != cur_u) {
+                consumer_sync();
+                expert_slots(R, u, N);
+                cur_u = u;
+            }
+            for (int c0 = 0; c0 < R.ns; c0 += kMaxCols, ++item)
+                gate_up_item(A, R, S, co, u, g, c0, min(kMaxCols, R.ns - c0), warp, lane, item & 1);
+            continue;
+        }
+        const int j = it - (int)total_gu;
+        const int u = j / Gd, g = j - u * Gd;
+        if (!down_phase || u != cur_u) {
+            consumer_sync();  // the tokens (or the previous columns) are no longer read
             expert_slots(R, u, N);
             cur_u = u;
+            down_phase = true;
         }
         for (int c0 = 0; c0 < R.ns; c0 += kMaxCols) {
             const int nc = min(kMaxCols, R.ns - c0);
-            // (re)stage this chunk's columns when the expert or the chunk changed
             if (staged_u != u || R.ns > kMaxCols) {
+                if (staged_u != u && threadIdx.x == 0) {  // wait for expert u's intermediate
+                    const unsigned target = (unsigned)(Gf * R.ns);
+                    uint32_t polls = 0;
+                    while (ld_acquire(A.ws.done + u) < target) {
+                        if (++polls == kDependencyPolls) {
+                            atomicOr(&g_device_error, kErrDependencyTimeout);
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                }
                 consumer_sync();
                 const int8_t *src[kMaxCols];
                 const float *dsrc[kMaxCols];
@@ -594,7 +583,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(const __grid_const
                     src[c] = A.ws.qa + (size_t)p * A.L.F;
                     dsrc[c] = A.ws.da + (size_t)p * A.nbF;
                 }
-                stage_cols(src, dsrc, nc, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers);
+                stage_cols(src, dsrc, nc, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers, true);
                 consumer_sync();
                 staged_u = u;
             }
@@ -602,11 +591,20 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe_down(const __grid_const
             ++item;
         }
     }
+    // the last CTA to finish resets the per-expert counts for the next call
+    consumer_sync();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(A.ws.sched + 2, 1u) == gridDim.x - 1) {
+            for (int u = 0; u < R.D; ++u) A.ws.done[u] = 0u;
+            A.ws.sched[2] = 0u;
+        }
+    }
 }
 
 // Router-weighted combine: y[t][r] = sum_j wts[t][j] * obuf[t*k+j][r], slots
 // in order j = 0..k-1, slots with an out-of-range id skipped.  One thread per
-// output; launched as a dependent of the down kernel.
+// output; launched as a dependent of the layer kernel.
 __global__ void __launch_bounds__(256) k_moe_combine(const __grid_constant__ MoeArgs A) {
     pdl_wait();
     const int total = A.n_tok * A.L.H;
@@ -627,6 +625,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     MoeArgs A;
     A.L = L;
     A.ws = ws;
+    A.h = h;
     A.ids = ids;
     A.wts = wts;
     A.y = y;
@@ -637,35 +636,25 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     A.nbpH = round_up4(A.nbH);
     A.nbF = L.F / kQK;
     A.nbpF = round_up4(A.nbF);
+    A.act_blocks = std::max(n_tok * A.nbpH, kMaxCols * A.nbpF);
     cudaError_t e = cudaSuccess;
     if (ws.ev[0] && (e = cudaEventRecord(ws.ev[0], s)) != cudaSuccess) return e;
-    e = launch_quantize(h, L.H, n_tok, ws.qh, ws.dh, s);
-    if (e != cudaSuccess) return e;
-    if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
     const int64_t max_experts = std::min(n_tok * k, L.E);
     {
-        const size_t smem = pipe_smem_bytes(kStagesGateUp, n_tok, A.nbpH, kSetsGateUp);
+        const size_t smem = moe_smem_bytes(A.act_blocks);
         int grid = 0;
-        e = dynamic_grid(k_moe_gate_up, smem, max_experts * (L.F / 32), &grid);
+        e = dynamic_grid(k_moe, smem, max_experts * (L.F / 32 + L.H / 32), &grid);
         if (e != cudaSuccess) return e;
-        e = launch_k(k_moe_gate_up, grid, kPipeThreads, smem, s, true, A);
+        e = launch_k(k_moe, grid, kPipeThreads, smem, s, false, A);
         if (e != cudaSuccess) return e;
     }
-    if (ws.ev[2] && (e = cudaEventRecord(ws.ev[2], s)) != cudaSuccess) return e;
-    {
-        const size_t smem = pipe_smem_bytes(kStages, kMaxCols, A.nbpF, kSetsMatvec);
-        int grid = 0;
-        e = dynamic_grid(k_moe_down, smem, max_experts * (L.H / 32), &grid);
-        if (e != cudaSuccess) return e;
-        e = launch_k(k_moe_down, grid, kPipeThreads, smem, s, true, A);
-        if (e != cudaSuccess) return e;
-    }
+    if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
     {
         const int grid = (int)std::min<int64_t>(((int64_t)n_tok * L.H + 255) / 256, 1024);
         e = launch_k(k_moe_combine, grid, 256, 0, s, true, A);
         if (e != cudaSuccess) return e;
     }
-    if (ws.ev[3]) e = cudaEventRecord(ws.ev[3], s);
+    if (ws.ev[2]) e = cudaEventRecord(ws.ev[2], s);
     return e;
 }
 
