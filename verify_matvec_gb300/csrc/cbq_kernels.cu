@@ -408,6 +408,7 @@ __device__ __forceinline__ int expert_ns(const Routing &R, int u, int N) {
 __device__ __forceinline__ int col_chunks(int ns) { return (ns + kMaxCols - 1) / kMaxCols; }
 
 constexpr unsigned kErrDependencyTimeout = 0x200u;
+constexpr unsigned kDownGrab = 8;
 constexpr uint32_t kDependencyPolls = 1u << 22;
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
@@ -501,29 +502,36 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
         if (lane == 0) {
             Producer pr;
             const int nbqH = A.nbpH / 4, nbqF = A.nbpF / 4;
-            unsigned nxt = atomicAdd(sched, 1u);
-            while (nxt < total && !pr.stopped) {
-                const unsigned it = nxt;
-                nxt = atomicAdd(sched, 1u);
-                if (it < total_gu) {
-                    const int u = (int)it / Gf, g = (int)it - u * Gf;
-                    const size_t e = (size_t)R.uniq[u];
-                    const int nch = col_chunks(expert_ns(R, u, N));
-                    for (int ch = 0; ch < nch; ++ch) {
-                        for (int half = 0; half < 2; ++half) {
-                            const size_t grp = (size_t)g + (size_t)half * Gf;
-                            pr.group(S.pipe, A.L.gu_qs + e * A.L.gu_qs_stride + grp * A.nbpH * 32,
-                                     A.L.gu_sc + e * A.L.gu_sc_stride + grp * nbqH * 32, A.nbpH, (int)it);
+            for (;;) {
+                // gate_up items one at a time; down items by guided grabs of up
+                // to kDownGrab consecutive items (same expert, same staged columns)
+                const unsigned seen = *(volatile unsigned *)sched;
+                if (seen >= total || pr.stopped) break;
+                const unsigned grab =
+                    seen < total_gu ? 1u : max(1u, min(kDownGrab, (total - seen) / (2u * gridDim.x)));
+                const unsigned base = atomicAdd(sched, grab);
+                if (base >= total) break;
+                for (unsigned it = base; it < min(total, base + grab) && !pr.stopped; ++it) {
+                    if (it < total_gu) {
+                        const int u = (int)it / Gf, g = (int)it - u * Gf;
+                        const size_t e = (size_t)R.uniq[u];
+                        const int nch = col_chunks(expert_ns(R, u, N));
+                        for (int ch = 0; ch < nch; ++ch) {
+                            for (int half = 0; half < 2; ++half) {
+                                const size_t grp = (size_t)g + (size_t)half * Gf;
+                                pr.group(S.pipe, A.L.gu_qs + e * A.L.gu_qs_stride + grp * A.nbpH * 32,
+                                         A.L.gu_sc + e * A.L.gu_sc_stride + grp * nbqH * 32, A.nbpH, (int)it);
+                            }
                         }
+                    } else {
+                        const int j = (int)(it - total_gu);
+                        const int u = j / Gd, g = j - u * Gd;
+                        const size_t e = (size_t)R.uniq[u];
+                        const int nch = col_chunks(expert_ns(R, u, N));
+                        for (int ch = 0; ch < nch; ++ch)
+                            pr.group(S.pipe, A.L.dn_qs + e * A.L.dn_qs_stride + (size_t)g * A.nbpF * 32,
+                                     A.L.dn_sc + e * A.L.dn_sc_stride + (size_t)g * nbqF * 32, A.nbpF, (int)it);
                     }
-                } else {
-                    const int j = (int)(it - total_gu);
-                    const int u = j / Gd, g = j - u * Gd;
-                    const size_t e = (size_t)R.uniq[u];
-                    const int nch = col_chunks(expert_ns(R, u, N));
-                    for (int ch = 0; ch < nch; ++ch)
-                        pr.group(S.pipe, A.L.dn_qs + e * A.L.dn_qs_stride + (size_t)g * A.nbpF * 32,
-                                 A.L.dn_sc + e * A.L.dn_sc_stride + (size_t)g * nbqF * 32, A.nbpF, (int)it);
                 }
             }
             __threadfence();
@@ -533,8 +541,17 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
         }
         return;
     }
-    // consumers: quantize the tokens straight into the staged layout
-    quant_stage_rows(A.h, A.L.H, A.n_tok, A.nbH, A.nbpH, S.act, S.dx, warp, kConsumerWarps, lane);
+    // consumers: stage the quantized tokens (written by the kernel launched just before)
+    pdl_wait();
+    {
+        const int8_t *src[kMaxCols];
+        const float *dsrc[kMaxCols];
+        for (int t = 0; t < A.n_tok; ++t) {
+            src[t] = A.ws.qh + (size_t)t * A.L.H;
+            dsrc[t] = A.ws.dh + (size_t)t * A.nbH;
+        }
+        stage_cols(src, dsrc, A.n_tok, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
+    }
     consumer_sync();
     Consumer co;
     int cur_u = -1, staged_u = -1, item = 0;
@@ -639,13 +656,15 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     A.act_blocks = std::max(n_tok * A.nbpH, kMaxCols * A.nbpF);
     cudaError_t e = cudaSuccess;
     if (ws.ev[0] && (e = cudaEventRecord(ws.ev[0], s)) != cudaSuccess) return e;
+    e = launch_quantize(h, L.H, n_tok, ws.qh, ws.dh, s);
+    if (e != cudaSuccess) return e;
     const int64_t max_experts = std::min(n_tok * k, L.E);
     {
         const size_t smem = moe_smem_bytes(A.act_blocks);
         int grid = 0;
         e = dynamic_grid(k_moe, smem, max_experts * (L.F / 32 + L.H / 32), &grid);
         if (e != cudaSuccess) return e;
-        e = launch_k(k_moe, grid, kPipeThreads, smem, s, false, A);
+        e = launch_k(k_moe, grid, kPipeThreads, smem, s, true, A);
         if (e != cudaSuccess) return e;
     }
     if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
