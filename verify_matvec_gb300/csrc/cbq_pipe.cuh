@@ -231,8 +231,11 @@ struct Consumer {
 // once.  The sum of this warp over the pass goes to part[c*32 + lane] (this
 // warp's slice of a partial set), written at the pass's first stage and
 // accumulated over the rest.
-__device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
-                                           const int *col_off, int ncols, float *part, int warp, int lane) {
+template <bool kOne>
+__device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int nbp, const uint4 *act0,
+                                                const float *dx0, const int *col_off, int ncols_rt, float *part,
+                                                int warp, int lane) {
+    const int ncols = kOne ? 1 : ncols_rt;
     for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
         const int nq = min(kChunkBlocks, nbp - b0) / 4;
         const uint32_t slot = co.slot;
@@ -270,6 +273,16 @@ __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp,
         if (lane == 0) mbar_arrive(P.empty + slot);
         co.advance(P);
     }
+}
+
+// ncols == 1 (the common case: one token per expert) gets its own copy of the
+// loop with the column count known at compile time.
+__device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
+                                           const int *col_off, int ncols, float *part, int warp, int lane) {
+    if (ncols == 1)
+        group_cols_impl<true>(co, P, nbp, act0, dx0, col_off, 1, part, warp, lane);
+    else
+        group_cols_impl<false>(co, P, nbp, act0, dx0, col_off, ncols, part, warp, lane);
 }
 
 // Dynamic shared memory of a pipelined kernel:
