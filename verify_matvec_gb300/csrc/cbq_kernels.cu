@@ -352,9 +352,7 @@ struct Routing {
     int ids[kMaxSlots];
     int first[kMaxSlots];
     int uniq[kMaxSlots];
-    int slots[kMaxSlots];  // slots of the current expert, ascending
     int D;
-    int ns;
 };
 
 __device__ void route(const int32_t *__restrict__ ids, int N, int E, Routing &R, bool report) {
@@ -385,16 +383,32 @@ __device__ void route(const int32_t *__restrict__ ids, int N, int E, Routing &R,
     __syncthreads();
 }
 
-// Slots of expert uniq[u], ascending, into R.slots / R.ns.  Consumer threads.
-__device__ void expert_slots(Routing &R, int u, int N) {
-    if (threadIdx.x == 0) {
-        const int e = R.uniq[u];
-        int ns = 0;
-        for (int p = 0; p < N; ++p)
-            if (R.ids[p] == e) R.slots[ns++] = p;
-        R.ns = ns;
+// Slots of expert e (ascending) found by one warp with ballots over the
+// routing table, without shared state or a CTA barrier: returns the slot
+// count and the slots with ranks c0..c0+kMaxCols-1 in sl[] (-1 past the end).
+struct Slots {
+    int ns;
+    int sl[kMaxCols];
+};
+
+__device__ __forceinline__ Slots warp_slots(const Routing &R, int e, int N, int c0, int lane) {
+    Slots S;
+    S.ns = 0;
+#pragma unroll
+    for (int c = 0; c < kMaxCols; ++c) S.sl[c] = -1;
+    for (int base = 0; base < N; base += 32) {
+        const bool hit = base + lane < N && R.ids[base + lane] == e;
+        unsigned mask = __ballot_sync(0xffffffffu, hit);
+        while (mask) {
+            const int p = base + __ffs(mask) - 1;
+            mask &= mask - 1;
+            const int r = S.ns++ - c0;
+#pragma unroll
+            for (int c = 0; c < kMaxCols; ++c)
+                if (r == c) S.sl[c] = p;
+        }
     }
-    consumer_sync();
+    return S;
 }
 
 // Number of slots of expert uniq[u] (any thread, from the routing table).
@@ -418,16 +432,16 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
 }
 
 // Gate rows (first pass) and up rows (second pass) of one 32-row-pair group
-// over the whole K for the columns (slots) R.slots[c0..c0+nc), then the
+// over the whole K for the columns (slots) sl.sl[0..nc), then the
 // SwiGLU split and the requantization of the 32 outputs of each column.
 // Partial sets: gate sums in set 2*buf, up sums in set 2*buf+1, each
 // [warp][column][lane].  Each writer warp then publishes its column for expert
 // rank u (fence, then one count in done[u]).
-__device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
-                                             int u, int g, int c0, int nc, int warp, int lane, int buf) {
+__device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Slots &sl, const PipeSmem &S, Consumer &co,
+                                             int u, int g, int nc, int warp, int lane, int buf) {
     int col_off[kMaxCols];  // activation column of each slot: its token's column
 #pragma unroll
-    for (int c = 0; c < kMaxCols; ++c) col_off[c] = (c < nc ? R.slots[c0 + c] / A.k : 0) * A.nbpH;
+    for (int c = 0; c < kMaxCols; ++c) col_off[c] = (c < nc ? sl.sl[c] / A.k : 0) * A.nbpH;
     float *pg = S.part + (2 * buf) * kPartSet;
     float *pu = S.part + (2 * buf + 1) * kPartSet;
     group_cols(co, S.pipe, A.nbpH, S.act, S.dx, col_off, nc, pg + warp * kMaxCols * 32, warp, lane);
@@ -444,7 +458,10 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
         const float a = A.swiglu ? gs / (1.0f + expf(-gs)) * us : gs * us;
         float d;
         const int8_t q = quant_lane(a, d);
-        const int p = R.slots[c0 + c];
+        int p = sl.sl[0];
+#pragma unroll
+        for (int cc = 1; cc < kMaxCols; ++cc)
+            if (c == cc) p = sl.sl[cc];
         const size_t o = (size_t)p * A.L.F + (size_t)g * 32 + lane;
         A.ws.qa[o] = q;
         if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
@@ -456,10 +473,10 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Routing &R,
 }
 
 // Down rows of one 32-row group for the nc columns staged in S (slots
-// R.slots[c0..c0+nc)), written per slot to obuf by warps 0..nc-1 after one
-// CTA barrier.
-__device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, const PipeSmem &S, Consumer &co,
-                                          int g, int c0, int nc, int warp, int lane, int buf) {
+// sl.sl[0..nc)), written per slot to obuf by warps 0..nc-1 after one CTA
+// barrier.
+__device__ __forceinline__ void down_item(const MoeArgs &A, const Slots &sl, const PipeSmem &S, Consumer &co,
+                                          int g, int nc, int warp, int lane, int buf) {
     int col_off[kMaxCols];
 #pragma unroll
     for (int c = 0; c < kMaxCols; ++c) col_off[c] = c * A.nbpF;
@@ -470,7 +487,10 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Routing &R, co
         float v = 0.0f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) v += part[(w * kMaxCols + warp) * 32 + lane];
-        const int p = R.slots[c0 + warp];
+        int p = sl.sl[0];
+#pragma unroll
+        for (int cc = 1; cc < kMaxCols; ++cc)
+            if (warp == cc) p = sl.sl[cc];
         A.ws.obuf[(size_t)p * A.L.H + (size_t)g * 32 + lane] = v;
     }
 }
@@ -554,35 +574,31 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
     }
     consumer_sync();
     Consumer co;
-    int cur_u = -1, staged_u = -1, item = 0;
-    bool down_phase = false;
+    int staged_u = -1, item = 0;
     for (;;) {
         const int it = co.peek(S.pipe);
         if (it < 0) break;
         if ((unsigned)it < total_gu) {
             const int u = it / Gf, g = it - u * Gf;
-            if (u != cur_u) {
-                consumer_sync();
-                expert_slots(R, u, N);
-                cur_u = u;
+            const int e = R.uniq[u];
+            for (int c0 = 0;; c0 += kMaxCols, ++item) {
+                const Slots sl = warp_slots(R, e, N, c0, lane);
+                gate_up_item(A, sl, S, co, u, g, min(kMaxCols, sl.ns - c0), warp, lane, item & 1);
+                if (c0 + kMaxCols >= sl.ns) break;
             }
-            for (int c0 = 0; c0 < R.ns; c0 += kMaxCols, ++item)
-                gate_up_item(A, R, S, co, u, g, c0, min(kMaxCols, R.ns - c0), warp, lane, item & 1);
+            ++item;
             continue;
         }
         const int j = it - (int)total_gu;
         const int u = j / Gd, g = j - u * Gd;
-        if (!down_phase || u != cur_u) {
-            consumer_sync();  // the tokens (or the previous columns) are no longer read
-            expert_slots(R, u, N);
-            cur_u = u;
-            down_phase = true;
-        }
-        for (int c0 = 0; c0 < R.ns; c0 += kMaxCols) {
-            const int nc = min(kMaxCols, R.ns - c0);
-            if (staged_u != u || R.ns > kMaxCols) {
+        const int e = R.uniq[u];
+        for (int c0 = 0;; c0 += kMaxCols) {
+            const Slots sl = warp_slots(R, e, N, c0, lane);
+            const int nc = min(kMaxCols, sl.ns - c0);
+            if (staged_u != u || sl.ns > kMaxCols) {
+                consumer_sync();  // the tokens (or the previous columns) are no longer read
                 if (staged_u != u && threadIdx.x == 0) {  // wait for expert u's intermediate
-                    const unsigned target = (unsigned)(Gf * R.ns);
+                    const unsigned target = (unsigned)(Gf * sl.ns);
                     uint32_t polls = 0;
                     while (ld_acquire(A.ws.done + u) < target) {
                         if (++polls == kDependencyPolls) {
@@ -595,8 +611,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                 consumer_sync();
                 const int8_t *src[kMaxCols];
                 const float *dsrc[kMaxCols];
-                for (int c = 0; c < nc; ++c) {
-                    const int p = R.slots[c0 + c];
+#pragma unroll
+                for (int c = 0; c < kMaxCols; ++c) {
+                    const int p = sl.sl[c] < 0 ? 0 : sl.sl[c];
                     src[c] = A.ws.qa + (size_t)p * A.L.F;
                     dsrc[c] = A.ws.da + (size_t)p * A.nbF;
                 }
@@ -604,8 +621,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                 consumer_sync();
                 staged_u = u;
             }
-            down_item(A, R, S, co, g, c0, nc, warp, lane, item & 1);
+            down_item(A, sl, S, co, g, nc, warp, lane, item & 1);
             ++item;
+            if (c0 + kMaxCols >= sl.ns) break;
         }
     }
     // the last CTA to finish resets the per-expert counts for the next call
