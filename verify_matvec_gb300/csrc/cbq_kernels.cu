@@ -431,31 +431,14 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     return v;
 }
 
-// Arrival of one consumer warp at the end of an item whose partial sums it has
-// written: true for the warp that arrives last (it then finishes the item
-// alone while the others go on).  The counter is reset by that warp.
-__device__ __forceinline__ bool last_arrival(unsigned *counter, int lane) {
-    __syncwarp();
-    __threadfence_block();
-    unsigned old = 0;
-    if (lane == 0) old = atomicAdd(counter, 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old != (unsigned)kConsumerWarps - 1u) return false;
-    __threadfence_block();
-    return true;
-}
-
 // Gate rows (first pass) and up rows (second pass) of one 32-row-pair group
 // over the whole K for the columns (slots) sl.sl[0..nc), then the
 // SwiGLU split and the requantization of the 32 outputs of each column.
 // Partial sets: gate sums in set 2*buf, up sums in set 2*buf+1, each
-// [warp][column][lane].  The last warp to finish reduces them, applies SwiGLU,
-// requantizes and publishes the columns for expert rank u (fence, then nc
-// counts in done[u]); the other warps go on to the next item without waiting.
-// Two partial-set pairs suffice: a warp can run at most the ring's depth
-// (3 stages) ahead of the slowest, never into the item after next.
+// [warp][column][lane].  Each writer warp then publishes its column for expert
+// rank u (fence, then one count in done[u]).
 __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Slots &sl, const PipeSmem &S, Consumer &co,
-                                             unsigned *arrivals, int u, int g, int nc, int warp, int lane, int buf) {
+                                             int u, int g, int nc, int warp, int lane, int buf) {
     int col_off[kMaxCols];  // activation column of each slot: its token's column
 #pragma unroll
     for (int c = 0; c < kMaxCols; ++c) col_off[c] = (c < nc ? sl.sl[c] / A.k : 0) * A.nbpH;
@@ -463,9 +446,9 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Slots &sl, 
     float *pu = S.part + (2 * buf + 1) * kPartSet;
     group_cols(co, S.pipe, A.nbpH, S.act, S.dx, col_off, nc, pg + warp * kMaxCols * 32, warp, lane);
     group_cols(co, S.pipe, A.nbpH, S.act, S.dx, col_off, nc, pu + warp * kMaxCols * 32, warp, lane);
-    if (!last_arrival(arrivals + buf, lane)) return;
-    // the last warp of the eight: reduce, SwiGLU, requantize and publish
-    for (int c = 0; c < nc; ++c) {
+    consumer_sync();
+    if (warp < nc) {
+        const int c = warp;
         float gs = 0.0f, us = 0.0f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
@@ -483,39 +466,33 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Slots &sl, 
         A.ws.qa[o] = q;
         if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
         if (A.ws.keep_a) A.ws.a_dbg[o] = a;
-    }
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) {
-        atomicAdd(A.ws.done + u, (unsigned)nc);
-        arrivals[buf] = 0u;
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(A.ws.done + u, 1u);
     }
 }
 
 // Down rows of one 32-row group for the nc columns staged in S (slots
-// sl.sl[0..nc)), written per slot to obuf by the last warp to finish.  Warps
-// write their partial sums at every stage, and with 2-stage items and a
-// 3-stage ring a fast warp can start the item after next while the last warp
-// still reduces; so down items rotate over three partial sets (buf = item % 3).
+// sl.sl[0..nc)), written per slot to obuf by warps 0..nc-1 after one CTA
+// barrier.
 __device__ __forceinline__ void down_item(const MoeArgs &A, const Slots &sl, const PipeSmem &S, Consumer &co,
-                                          unsigned *arrivals, int g, int nc, int warp, int lane, int buf) {
+                                          int g, int nc, int warp, int lane, int buf) {
     int col_off[kMaxCols];
 #pragma unroll
     for (int c = 0; c < kMaxCols; ++c) col_off[c] = c * A.nbpF;
     float *part = S.part + buf * kPartSet;
     group_cols(co, S.pipe, A.nbpF, S.act, S.dx, col_off, nc, part + warp * kMaxCols * 32, warp, lane);
-    if (!last_arrival(arrivals + buf, lane)) return;
-    for (int c = 0; c < nc; ++c) {
+    consumer_sync();
+    if (warp < nc) {
         float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) v += part[(w * kMaxCols + c) * 32 + lane];
+        for (int w = 0; w < kConsumerWarps; ++w) v += part[(w * kMaxCols + warp) * 32 + lane];
         int p = sl.sl[0];
 #pragma unroll
         for (int cc = 1; cc < kMaxCols; ++cc)
-            if (c == cc) p = sl.sl[cc];
+            if (warp == cc) p = sl.sl[cc];
         A.ws.obuf[(size_t)p * A.L.H + (size_t)g * 32 + lane] = v;
     }
-    if (lane == 0) arrivals[buf] = 0u;
 }
 
 // The whole routed-expert layer but the combine, in one persistent kernel.
@@ -530,9 +507,7 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Slots &sl, con
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__ MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
-    __shared__ unsigned arrivals[3];  // warps done with the item of each partial-set buffer
     pdl_trigger();  // the combine kernel may launch; it waits for this grid
-    if (threadIdx.x < 3) arrivals[threadIdx.x] = 0u;
     const int N = A.n_tok * A.k;
     route(A.ids, N, A.L.E, R, blockIdx.x == 0);
     const int Gf = A.L.F / 32, Gd = A.L.H / 32;
@@ -608,7 +583,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
             const int e = R.uniq[u];
             for (int c0 = 0;; c0 += kMaxCols, ++item) {
                 const Slots sl = warp_slots(R, e, N, c0, lane);
-                gate_up_item(A, sl, S, co, arrivals, u, g, min(kMaxCols, sl.ns - c0), warp, lane, item & 1);
+                gate_up_item(A, sl, S, co, u, g, min(kMaxCols, sl.ns - c0), warp, lane, item & 1);
                 if (c0 + kMaxCols >= sl.ns) break;
             }
             ++item;
@@ -646,7 +621,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                 consumer_sync();
                 staged_u = u;
             }
-            down_item(A, sl, S, co, arrivals, g, nc, warp, lane, item % 3);
+            down_item(A, sl, S, co, g, nc, warp, lane, item & 1);
             ++item;
             if (c0 + kMaxCols >= sl.ns) break;
         }
