@@ -180,23 +180,42 @@ __device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, co
     }
 }
 
+// v[c] for a run-time c < kMaxCols, by a compare chain: the array stays in
+// registers (a dynamic index would place it in local memory).
+__device__ __forceinline__ int pick(const int (&v)[kMaxCols], int c) {
+    int r = v[0];
+#pragma unroll
+    for (int cc = 1; cc < kMaxCols; ++cc)
+        if (c == cc) r = v[cc];
+    return r;
+}
+
+// Sources of the activation columns to stage: column c is row row[c] of a
+// row-major int8 matrix q (qstride bytes per row, rows 16-byte aligned) and of
+// its fp32 block-scale matrix d (dstride floats per row; d == nullptr stages
+// zero scales).
+static_assert(kMaxCols == 5, "ColSrc initialisers list five rows");
+struct ColSrc {
+    const int8_t *q;
+    const float *d;
+    size_t qstride, dstride;
+    int row[kMaxCols];
+};
+
 // Stage activation columns into shared memory in the expander's element
-// order.  src[c] = plain int8 column (K bytes, 16-byte aligned; nullptr
-// stages a zero column), dsrc[c] its K/32 scales (dsrc == nullptr stages zero
-// scales).  act_s: ncols x nbp x 2
-// uint4; dx_s: ncols x nbp floats.  Blocks nb..nbp-1 are zero.  Threads
-// tid = 0..nthr-1 share the work.
+// order.  act_s: ncols x nbp x 2 uint4; dx_s: ncols x nbp floats.  Blocks
+// nb..nbp-1 are zero.  Threads tid = 0..nthr-1 share the work.
 // With l2_only the loads bypass L1 (data written by other CTAs of the same
 // kernel).
-__device__ __forceinline__ void stage_cols(const int8_t *const *src, const float *const *dsrc, int ncols,
-                                           int nb, int nbp, uint4 *act_s, float *dx_s, int tid, int nthr,
-                                           bool l2_only = false) {
+__device__ __forceinline__ void stage_cols(const ColSrc &src, int ncols, int nb, int nbp, uint4 *act_s,
+                                           float *dx_s, int tid, int nthr, bool l2_only = false) {
     for (int idx = tid; idx < ncols * nbp; idx += nthr) {
         const int c = idx / nbp, b = idx - c * nbp;
         uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
         float d = 0.0f;
-        if (b < nb && src[c]) {
-            const uint4 *p = reinterpret_cast<const uint4 *>(src[c] + (size_t)b * kQK);
+        if (b < nb) {
+            const size_t r = (size_t)pick(src.row, c);
+            const uint4 *p = reinterpret_cast<const uint4 *>(src.q + r * src.qstride + (size_t)b * kQK);
             const uint4 x0 = l2_only ? __ldcg(p) : p[0], x1 = l2_only ? __ldcg(p + 1) : p[1];
             const uint32_t P[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
             // word 2m   = x[4m], x[4m+16], x[4m+1], x[4m+17]
@@ -205,7 +224,10 @@ __device__ __forceinline__ void stage_cols(const int8_t *const *src, const float
             o0.z = prmt(P[1], P[5], 0x5140u); o0.w = prmt(P[1], P[5], 0x7362u);
             o1.x = prmt(P[2], P[6], 0x5140u); o1.y = prmt(P[2], P[6], 0x7362u);
             o1.z = prmt(P[3], P[7], 0x5140u); o1.w = prmt(P[3], P[7], 0x7362u);
-            if (dsrc) d = l2_only ? __ldcg(dsrc[c] + b) : dsrc[c][b];
+            if (src.d) {
+                const float *dp = src.d + r * src.dstride + b;
+                d = l2_only ? __ldcg(dp) : *dp;
+            }
         }
         act_s[(size_t)idx * 2] = o0;
         act_s[(size_t)idx * 2 + 1] = o1;

@@ -149,14 +149,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     }
     pdl_wait();  // the activations may come from the kernel launched just before
     {
-        const int8_t *src[NC];
-        const float *dsrc[NC];
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            src[c] = qx + (size_t)c * K;
-            dsrc[c] = dx + (size_t)c * nb;
-        }
-        stage_cols(src, dsrc, NC, nb, nbp, S.act, S.dx, threadIdx.x, kConsumers);
+        ColSrc src{qx, dx, (size_t)K, (size_t)nb, {0, 1, 2, 3, 4}};
+        stage_cols(src, NC, nb, nbp, S.act, S.dx, threadIdx.x, kConsumers);
     }
     consumer_sync();
     const uint4 *act[NC];
@@ -200,10 +194,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *dx_s = reinterpret_cast<float *>(act_s + (size_t)NC * nbp * 2);
     {
         // the activation scales do not enter the integer dots: stage zeros
-        const int8_t *src[NC];
-#pragma unroll
-        for (int c = 0; c < NC; ++c) src[c] = qx + (size_t)c * K;
-        stage_cols(src, nullptr, NC, nb, nbp, act_s, dx_s, threadIdx.x, blockDim.x);
+        ColSrc src{qx, nullptr, (size_t)K, 0, {0, 1, 2, 3, 4}};
+        stage_cols(src, NC, nb, nbp, act_s, dx_s, threadIdx.x, blockDim.x);
     }
     __syncthreads();
     const uint4 *act[NC];
@@ -564,13 +556,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
     // consumers: stage the quantized tokens (written by the kernel launched just before)
     pdl_wait();
     {
-        const int8_t *src[kMaxCols];
-        const float *dsrc[kMaxCols];
-        for (int t = 0; t < A.n_tok; ++t) {
-            src[t] = A.ws.qh + (size_t)t * A.L.H;
-            dsrc[t] = A.ws.dh + (size_t)t * A.nbH;
-        }
-        stage_cols(src, dsrc, A.n_tok, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
+        ColSrc src{A.ws.qh, A.ws.dh, (size_t)A.L.H, (size_t)A.nbH, {0, 1, 2, 3, 4}};
+        stage_cols(src, A.n_tok, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
     }
     consumer_sync();
     Consumer co;
@@ -609,15 +596,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                     }
                 }
                 consumer_sync();
-                const int8_t *src[kMaxCols];
-                const float *dsrc[kMaxCols];
+                ColSrc src{A.ws.qa, A.ws.da, (size_t)A.L.F, (size_t)A.nbF, {}};
 #pragma unroll
-                for (int c = 0; c < kMaxCols; ++c) {
-                    const int p = sl.sl[c] < 0 ? 0 : sl.sl[c];
-                    src[c] = A.ws.qa + (size_t)p * A.L.F;
-                    dsrc[c] = A.ws.da + (size_t)p * A.nbF;
-                }
-                stage_cols(src, dsrc, nc, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers, true);
+                for (int c = 0; c < kMaxCols; ++c) src.row[c] = max(sl.sl[c], 0);
+                stage_cols(src, nc, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers, true);
                 consumer_sync();
                 staged_u = u;
             }

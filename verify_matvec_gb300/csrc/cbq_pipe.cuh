@@ -233,7 +233,7 @@ struct Consumer {
 // accumulated over the rest.
 template <bool kOne>
 __device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int nbp, const uint4 *act0,
-                                                const float *dx0, const int *col_off, int ncols_rt, float *part,
+                                                const float *dx0, const int (&col_off)[kMaxCols], int ncols_rt, float *part,
                                                 int warp, int lane) {
     const int ncols = kOne ? 1 : ncols_rt;
     for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
@@ -246,8 +246,9 @@ __device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int
             const uint2 *sc_s = reinterpret_cast<const uint2 *>(st + kStageQsBytes);
             const int q0 = warp * nq / kConsumerWarps, q1 = (warp + 1) * nq / kConsumerWarps;
             for (int c = 0; c < ncols; ++c) {
-                const uint4 *act = act0 + (size_t)col_off[c] * 2;
-                const float *dxs = dx0 + col_off[c];
+                const int off = kOne ? col_off[0] : pick(col_off, c);
+                const uint4 *act = act0 + (size_t)off * 2;
+                const float *dxs = dx0 + off;
                 float2 acc = make_float2(0.0f, 0.0f);
                 for (int q = q0; q < q1; ++q) {
                     const uint2 s = sc_s[q * 32 + lane];
@@ -278,7 +279,7 @@ __device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int
 // ncols == 1 (the common case: one token per expert) gets its own copy of the
 // loop with the column count known at compile time.
 __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
-                                           const int *col_off, int ncols, float *part, int warp, int lane) {
+                                           const int (&col_off)[kMaxCols], int ncols, float *part, int warp, int lane) {
     if (ncols == 1)
         group_cols_impl<true>(co, P, nbp, act0, dx0, col_off, 1, part, warp, lane);
     else
