@@ -365,7 +365,7 @@ def run_gpu(args):
 
     # per-launch algorithmic bytes: weights + activations read + outputs written
     slots = N_TOK * TOPK
-    moe_io = 4 * N_TOK * H + 2 * slots * F * (1 + 4 / QK) + 4 * slots * H  # h in, qa/da out+in, obuf out
+    moe_io = 8 * N_TOK * H + 8 * slots  # h in, y out, ids + router weights in (intermediates stay in L2)
     moe_alg = [distinct[i % N_SETS] * EXPERT_BYTES + moe_io for i in timed]
     head_alg = HEAD_BYTES + HEAD_N * HEAD_K * (1 + 4 / QK) + 4 * HEAD_N * HEAD_M
     # the MoE call is three PDL-chained launches; events go around the whole

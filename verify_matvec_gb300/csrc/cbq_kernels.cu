@@ -621,17 +621,38 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
 
 // Router-weighted combine: y[t][r] = sum_j wts[t][j] * obuf[t*k+j][r], slots
 // in order j = 0..k-1, slots with an out-of-range id skipped.  One thread per
-// output; launched as a dependent of the layer kernel.
+// output; launched as a dependent of the layer kernel.  The ids and weights
+// are inputs of the call, complete before its first kernel started, so they
+// are read into shared memory before the wait; a token's k loads of obuf are
+// then issued together.
+constexpr int kMaxTopk = 16;  // routed experts per token (the ABI's limit)
+
 __global__ void __launch_bounds__(256) k_moe_combine(const __grid_constant__ MoeArgs A) {
+    __shared__ float w_s[kMaxSlots];  // router weight of each slot, 0 for a skipped slot
+    __shared__ int ok_s[kMaxSlots];   // slot has an in-range id
+    const int N = A.n_tok * A.k;
+    if ((int)threadIdx.x < N) {
+        const int id = A.ids[threadIdx.x];
+        ok_s[threadIdx.x] = id >= 0 && id < A.L.E;
+        w_s[threadIdx.x] = A.wts[threadIdx.x];
+    }
+    __syncthreads();
     pdl_wait();
     const int total = A.n_tok * A.L.H;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
         const int t = i / A.L.H, r = i - t * A.L.H;
+        const int p0 = t * A.k;
+        float o[kMaxTopk];
+#pragma unroll
+        for (int j = 0; j < kMaxTopk; ++j) {
+            const int p = min(p0 + j, kMaxSlots - 1);
+            o[j] = j < A.k && ok_s[p] ? A.ws.obuf[(size_t)p * A.L.H + r] : 0.0f;
+        }
         float v = 0.0f;
-        for (int j = 0; j < A.k; ++j) {
-            const int p = t * A.k + j;
-            const int id = A.ids[p];
-            if (id >= 0 && id < A.L.E) v += A.wts[p] * A.ws.obuf[(size_t)p * A.L.H + r];
+#pragma unroll
+        for (int j = 0; j < kMaxTopk; ++j) {
+            const int p = min(p0 + j, kMaxSlots - 1);
+            if (j < A.k && ok_s[p]) v += w_s[p] * o[j];
         }
         A.y[i] = v;
     }
