@@ -143,10 +143,10 @@ template <int NC>
 struct UseSplit { static constexpr bool value = NC == 1; };
 
 // Exact int32 block dots (offset by kMagicBits) of one index block against NC
-// permuted activation blocks act[c][0..1] (8 words each).
+// permuted activation blocks: column c's two words at actb[2c], actb[2c+1]
+// (the block-major staging below puts a block's columns side by side).
 template <int NC>
-__device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, const uint4 *const *act, int b,
-                                           int sdot[NC]) {
+__device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, const uint4 *actb, int sdot[NC]) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
     if constexpr (UseSplit<NC>::value) {
         uint32_t lo[8], hi[8];
@@ -154,7 +154,7 @@ __device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, co
         for (int m = 0; m < 4; ++m) expand_split(cb, ws[m], lo[2 * m], hi[2 * m], lo[2 * m + 1], hi[2 * m + 1]);
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-            const uint4 a0 = act[c][2 * b], a1 = act[c][2 * b + 1];
+            const uint4 a0 = actb[2 * c], a1 = actb[2 * c + 1];
             const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             int s = kMagicBits, t = 0;  // two chains: lower- and upper-table parts
 #pragma unroll
@@ -170,7 +170,7 @@ __device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, co
         for (int m = 0; m < 4; ++m) expand_select(cb, ws[m], e[2 * m], e[2 * m + 1]);
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-            const uint4 a0 = act[c][2 * b], a1 = act[c][2 * b + 1];
+            const uint4 a0 = actb[2 * c], a1 = actb[2 * c + 1];
             const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             int s = kMagicBits;
 #pragma unroll
@@ -178,6 +178,14 @@ __device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, co
             sdot[c] = s;
         }
     }
+}
+
+// Scaled accumulation of two consecutive blocks' dots of one column:
+// acc += (dw0*dx0 * s0, dw1*dx1 * s1) with the packed fp32x2 pipe; the same
+// three roundings per block as a scalar multiply, add and fused multiply-add.
+__device__ __forceinline__ float2 scale_acc2(float2 acc, float2 dw, float2 dx, int sa, int sb) {
+    const float2 s = __fadd2_rn(make_float2(__int_as_float(sa), __int_as_float(sb)), make_float2(-kMagic, -kMagic));
+    return __ffma2_rn(__fmul2_rn(dw, dx), s, acc);
 }
 
 // v[c] for a run-time c < kMaxCols, by a compare chain: the array stays in
@@ -203,14 +211,21 @@ struct ColSrc {
 };
 
 // Stage activation columns into shared memory in the expander's element
-// order.  act_s: ncols x nbp x 2 uint4; dx_s: ncols x nbp floats.  Blocks
-// nb..nbp-1 are zero.  Threads tid = 0..nthr-1 share the work.
-// With l2_only the loads bypass L1 (data written by other CTAs of the same
-// kernel).
+// order.  Blocks nb..nbp-1 are zero (nbp even).  Threads tid = 0..nthr-1
+// share the work.  Layouts (act_s in uint4 pairs, one pair per block):
+//   column-major (block_major == false): block b of column c at pair c*nbp + b,
+//     its scale at dx_s[c*nbp + b];
+//   block-major: block b of column c at pair b*ncols + c, its scale at
+//     dx_s[((b/2)*ncols + c)*2 + b%2] (a float2 per column and block pair).
+// With one column the two coincide.  With l2_only the loads bypass L1 (data
+// written by other CTAs of the same kernel).
 __device__ __forceinline__ void stage_cols(const ColSrc &src, int ncols, int nb, int nbp, uint4 *act_s,
-                                           float *dx_s, int tid, int nthr, bool l2_only = false) {
+                                           float *dx_s, int tid, int nthr, bool l2_only = false,
+                                           bool block_major = false) {
     for (int idx = tid; idx < ncols * nbp; idx += nthr) {
         const int c = idx / nbp, b = idx - c * nbp;
+        const int ai = block_major ? b * ncols + c : idx;
+        const int di = block_major ? ((b >> 1) * ncols + c) * 2 + (b & 1) : idx;
         uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
         float d = 0.0f;
         if (b < nb) {
@@ -229,9 +244,9 @@ __device__ __forceinline__ void stage_cols(const ColSrc &src, int ncols, int nb,
                 d = l2_only ? __ldcg(dp) : *dp;
             }
         }
-        act_s[(size_t)idx * 2] = o0;
-        act_s[(size_t)idx * 2 + 1] = o1;
-        dx_s[idx] = d;
+        act_s[(size_t)ai * 2] = o0;
+        act_s[(size_t)ai * 2 + 1] = o1;
+        dx_s[di] = d;
     }
 }
 

@@ -150,16 +150,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     pdl_wait();  // the activations may come from the kernel launched just before
     {
         ColSrc src{qx, dx, (size_t)K, (size_t)nb, {0, 1, 2, 3, 4}};
-        stage_cols(src, NC, nb, nbp, S.act, S.dx, threadIdx.x, kConsumers);
+        stage_cols(src, NC, nb, nbp, S.act, S.dx, threadIdx.x, kConsumers, false, true);
     }
     consumer_sync();
-    const uint4 *act[NC];
-    const float *dxs[NC];
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-        act[c] = S.act + (size_t)c * nbp * 2;
-        dxs[c] = S.dx + (size_t)c * nbp;
-    }
+    const float2 *dxp = reinterpret_cast<const float2 *>(S.dx);
     Consumer co;
     for (int item = 0;; ++item) {
         const int g = co.peek(S.pipe);
@@ -167,7 +161,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         float2 acc[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
-        co.group<NC>(S.pipe, nbp, act, dxs, acc, warp, lane);
+        co.group<NC>(S.pipe, nbp, S.act, dxp, acc, warp, lane);
         float *part = S.part + (item & 1) * kPartSet;
 #pragma unroll
         for (int c = 0; c < NC; ++c) part[(warp * NC + c) * 32 + lane] = acc[c].x + acc[c].y;
@@ -195,12 +189,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     {
         // the activation scales do not enter the integer dots: stage zeros
         ColSrc src{qx, nullptr, (size_t)K, 0, {0, 1, 2, 3, 4}};
-        stage_cols(src, NC, nb, nbp, act_s, dx_s, threadIdx.x, blockDim.x);
+        stage_cols(src, NC, nb, nbp, act_s, dx_s, threadIdx.x, blockDim.x, false, true);
     }
     __syncthreads();
-    const uint4 *act[NC];
-#pragma unroll
-    for (int c = 0; c < NC; ++c) act[c] = act_s + (size_t)c * nbp * 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbq = nbp / 4;
     const int q0 = warp * nbq / kWarps, q1 = (warp + 1) * nbq / kWarps;
@@ -213,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int b = 4 * q + j;
                 const uint4 w = ld_stream16(qs + ((size_t)g * nbp + b) * 32 + lane);
                 int sd[NC];
-                block_dots<NC>(cb, w, act, b, sd);
+                block_dots<NC>(cb, w, act_s + (size_t)b * NC * 2, sd);
                 if (row < M && b < nb) {
 #pragma unroll
                     for (int c = 0; c < NC; ++c) sdot[((size_t)c * M + row) * nb + b] = sd[c] - kMagicBits;

@@ -183,9 +183,9 @@ struct Consumer {
 
     // Accumulate one 32-row group pass (blocks [0, nbp)) into acc2: two
     // interleaved fp32 partial sums per column (even and odd blocks).
-    // dxs[c] must be 8-byte aligned.
+    // act/dxp: the NC columns staged block-major (stage_cols).
     template <int NC>
-    __device__ __forceinline__ void group(const Pipe &P, int nbp, const uint4 *const *act, const float *const *dxs,
+    __device__ __forceinline__ void group(const Pipe &P, int nbp, const uint4 *act, const float2 *dxp,
                                           float2 acc2[NC], int warp, int lane) {
         for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
             const int nq = min(kChunkBlocks, nbp - b0) / 4;
@@ -203,18 +203,16 @@ struct Consumer {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) w[j] = qs_s[(q * 4 + j) * 32 + lane];
                     const int bq = b0 + q * 4;
+                    const uint4 *aq = act + (size_t)bq * NC * 2;
+                    const float2 *dq = dxp + (size_t)(bq >> 1) * NC;
 #pragma unroll
                     for (int jj = 0; jj < 4; jj += 2) {  // blocks in pairs: fewer live sums
                         int sa[NC], sb[NC];
-                        block_dots<NC>(cb, w[jj], act, bq + jj, sa);
-                        block_dots<NC>(cb, w[jj + 1], act, bq + jj + 1, sb);
+                        block_dots<NC>(cb, w[jj], aq + jj * NC * 2, sa);
+                        block_dots<NC>(cb, w[jj + 1], aq + (jj + 1) * NC * 2, sb);
                         const float2 dw = jj == 0 ? dw01 : dw23;
 #pragma unroll
-                        for (int c = 0; c < NC; ++c) {
-                            const float2 dx2 = *reinterpret_cast<const float2 *>(dxs[c] + bq + jj);
-                            acc2[c].x = fmaf(dw.x * dx2.x, __int_as_float(sa[c]) - kMagic, acc2[c].x);
-                            acc2[c].y = fmaf(dw.y * dx2.y, __int_as_float(sb[c]) - kMagic, acc2[c].y);
-                        }
+                        for (int c = 0; c < NC; ++c) acc2[c] = scale_acc2(acc2[c], dw, dq[(jj >> 1) * NC + c], sa[c], sb[c]);
                     }
                 }
             }
@@ -258,12 +256,11 @@ __device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int
 #pragma unroll
                     for (int jj = 0; jj < 4; jj += 2) {
                         int sa[1], sb[1];
-                        block_dots<1>(co.cb, qs_s[(q * 4 + jj) * 32 + lane], &act, bq + jj, sa);
-                        block_dots<1>(co.cb, qs_s[(q * 4 + jj + 1) * 32 + lane], &act, bq + jj + 1, sb);
+                        block_dots<1>(co.cb, qs_s[(q * 4 + jj) * 32 + lane], act + (size_t)(bq + jj) * 2, sa);
+                        block_dots<1>(co.cb, qs_s[(q * 4 + jj + 1) * 32 + lane], act + (size_t)(bq + jj + 1) * 2, sb);
                         const float2 dx2 = *reinterpret_cast<const float2 *>(dxs + bq + jj);
                         const float2 dw = jj == 0 ? dw01 : dw23;
-                        acc.x = fmaf(dw.x * dx2.x, __int_as_float(sa[0]) - kMagic, acc.x);
-                        acc.y = fmaf(dw.y * dx2.y, __int_as_float(sb[0]) - kMagic, acc.y);
+                        acc = scale_acc2(acc, dw, dx2, sa[0], sb[0]);
                     }
                 }
                 float *dst = part + c * 32 + lane;
