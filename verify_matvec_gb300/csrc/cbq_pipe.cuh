@@ -14,11 +14,11 @@
 // tagged -1 that carries no bytes.  Consumers read the tag at each item
 // boundary, so CTAs of unequal speed share the work evenly.
 //
-// Every wait is bounded: after kSpinLimit polls it sets kErrPipeTimeout in the
-// device error word and a CTA-wide abort flag; the other waits of the CTA
-// then give up too, consumers keep their barrier sequence (so no named
-// barrier is left waiting), and the producer waits for its own copies in
-// flight before the CTA exits.
+// Every wait is bounded: once it has waited kWaitLimitNs (global timer) it
+// sets kErrPipeTimeout in the device error word and a CTA-wide abort flag; the
+// other waits of the CTA then give up too, consumers keep their barrier
+// sequence (so no named barrier is left waiting), and the producer waits for
+// its own copies in flight before the CTA exits.
 #pragma once
 
 #include <stdint.h>
@@ -35,10 +35,11 @@ constexpr int kPipeThreads = kConsumers + 32;   // + one producer warp
 constexpr int kChunkBlocks = 32;                 // block columns per stage
 constexpr int kStageQsBytes = kChunkBlocks * 512;
 constexpr int kStageBytes = kStageQsBytes + kChunkBlocks / 4 * 256;  // 18,432
-// Bounded waits: each poll may suspend the warp for a hardware-chosen time
-// (it resumes as soon as the phase completes); at most kSpinLimit polls are
-// made before the wait gives up.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// Bounded waits: each poll suspends the warp until the phase completes or
+// kWaitHintNs pass (so a waiting warp takes no issue slots from the warps that
+// compute); a wait gives up after kWaitLimitNs in all.
+constexpr uint32_t kWaitHintNs = 20000;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr unsigned kErrPipeTimeout = 0x100u;
 
 // The device error word, defined by the translation unit that includes this
@@ -56,12 +57,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "n"(kWaitHintNs)
         : "memory");
     return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
@@ -98,9 +105,12 @@ struct Pipe {
 // Bounded wait for phase `parity` of bar.  Returns false on timeout or when
 // the CTA already gave up (check_abort).
 __device__ __forceinline__ bool pipe_wait(const Pipe &P, uint64_t *bar, uint32_t parity, bool check_abort) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
         if (check_abort && *(volatile int *)P.abort) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) break;
     }
     atomicOr(&g_device_error, kErrPipeTimeout);
     *(volatile int *)P.abort = 1;
