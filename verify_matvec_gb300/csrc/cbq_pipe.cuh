@@ -95,7 +95,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 // Shared part of the pipeline (carved from dynamic shared memory).
 struct Pipe {
     uint64_t *full;   // [S] stage filled (producer arrive + bulk bytes)
-    uint64_t *empty;  // [S] stage released (one arrive per consumer warp)
+    uint64_t *empty;  // [S] stage released (one arrive per consumer thread)
     int *abort;       // CTA-wide give-up flag
     int *tag;         // [S] item of each stage (-1: end of stream)
     unsigned char *ring;
@@ -204,7 +204,8 @@ struct Consumer {
                 const unsigned char *st = P.ring + (size_t)slot * kStageBytes;
                 const uint4 *qs_s = reinterpret_cast<const uint4 *>(st);
                 const uint2 *sc_s = reinterpret_cast<const uint2 *>(st + kStageQsBytes);
-                const int q0 = warp * nq / kConsumerWarps, q1 = (warp + 1) * nq / kConsumerWarps;
+                const int q0 = (int)((unsigned)(warp * nq) / kConsumerWarps);
+                const int q1 = (int)((unsigned)((warp + 1) * nq) / kConsumerWarps);
                 for (int q = q0; q < q1; ++q) {
                     const uint2 s = sc_s[q * 32 + lane];
                     const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
@@ -226,8 +227,7 @@ struct Consumer {
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(P.empty + slot);
+            mbar_arrive(P.empty + slot);  // every consumer thread, after its own reads
             advance(P);
         }
     }
@@ -237,13 +237,16 @@ struct Consumer {
 // columns, each swept separately over every stage from shared memory, so the
 // registers stay those of one column while the weight stream is still read
 // once.  The sum of this warp over the pass goes to part[c*32 + lane] (this
-// warp's slice of a partial set), written at the pass's first stage and
+// warp's slice of a partial set).  With one column (kOne) the running sums
+// stay in registers over the whole pass and are stored once at its end;
+// otherwise each column's slice is written at the pass's first stage and
 // accumulated over the rest.
 template <bool kOne>
 __device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int nbp, const uint4 *act0,
                                                 const float *dx0, const int (&col_off)[kMaxCols], int ncols_rt, float *part,
                                                 int warp, int lane) {
     const int ncols = kOne ? 1 : ncols_rt;
+    float2 run = make_float2(0.0f, 0.0f);  // kOne: even- and odd-block sums of the pass
     for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
         const int nq = min(kChunkBlocks, nbp - b0) / 4;
         const uint32_t slot = co.slot;
@@ -252,12 +255,13 @@ __device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int
             const unsigned char *st = P.ring + (size_t)slot * kStageBytes;
             const uint4 *qs_s = reinterpret_cast<const uint4 *>(st);
             const uint2 *sc_s = reinterpret_cast<const uint2 *>(st + kStageQsBytes);
-            const int q0 = warp * nq / kConsumerWarps, q1 = (warp + 1) * nq / kConsumerWarps;
+            const int q0 = (int)((unsigned)(warp * nq) / kConsumerWarps);
+            const int q1 = (int)((unsigned)((warp + 1) * nq) / kConsumerWarps);
             for (int c = 0; c < ncols; ++c) {
                 const int off = kOne ? col_off[0] : pick(col_off, c);
-                const uint4 *act = act0 + (size_t)off * 2;
+                const uint4 *act = act0 + off * 2;
                 const float *dxs = dx0 + off;
-                float2 acc = make_float2(0.0f, 0.0f);
+                float2 acc = kOne ? run : make_float2(0.0f, 0.0f);
                 for (int q = q0; q < q1; ++q) {
                     const uint2 s = sc_s[q * 32 + lane];
                     const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
@@ -266,21 +270,25 @@ __device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int
 #pragma unroll
                     for (int jj = 0; jj < 4; jj += 2) {
                         int sa[1], sb[1];
-                        block_dots<1>(co.cb, qs_s[(q * 4 + jj) * 32 + lane], act + (size_t)(bq + jj) * 2, sa);
-                        block_dots<1>(co.cb, qs_s[(q * 4 + jj + 1) * 32 + lane], act + (size_t)(bq + jj + 1) * 2, sb);
+                        block_dots<1>(co.cb, qs_s[(q * 4 + jj) * 32 + lane], act + (bq + jj) * 2, sa);
+                        block_dots<1>(co.cb, qs_s[(q * 4 + jj + 1) * 32 + lane], act + (bq + jj + 1) * 2, sb);
                         const float2 dx2 = *reinterpret_cast<const float2 *>(dxs + bq + jj);
                         const float2 dw = jj == 0 ? dw01 : dw23;
                         acc = scale_acc2(acc, dw, dx2, sa[0], sb[0]);
                     }
                 }
-                float *dst = part + c * 32 + lane;
-                *dst = (b0 == 0 ? 0.0f : *dst) + (acc.x + acc.y);
+                if constexpr (kOne) {
+                    run = acc;
+                } else {
+                    float *dst = part + c * 32 + lane;
+                    *dst = (b0 == 0 ? 0.0f : *dst) + (acc.x + acc.y);
+                }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(P.empty + slot);
+        mbar_arrive(P.empty + slot);  // every consumer thread, after its own reads
         co.advance(P);
     }
+    if constexpr (kOne) part[lane] = run.x + run.y;
 }
 
 // ncols == 1 (the common case: one token per expert) gets its own copy of the
@@ -343,7 +351,7 @@ __device__ __forceinline__ void pipe_init(const Pipe &P) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < P.S; ++s) {
             mbar_init(P.full + s, 1);
-            mbar_init(P.empty + s, kConsumerWarps);
+            mbar_init(P.empty + s, kConsumers);
         }
         *P.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
