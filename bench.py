@@ -52,9 +52,10 @@ FALLBACK_HBM_GBS = 6800.0
 # one ncu capture of each kernel (summaries in profiles/), valid only for the
 # kernel sources they were taken on (digest below); otherwise reported as null.
 PROFILED = {
-    "source_digest": "ac63a93b947afbb0",
-    "k_matvec<5> (head)": 297_941_760 + 11_359_488,          # one launch, 129280 x 4096, n=5
-    "moe call per expert": None,
+    "source_digest": "a052c4af5c9958cd",
+    "k_matvec<5> (head)": 297_924_096 + 4_864_256,          # one launch, 129280 x 4096, n=5
+    # one layer call (k_quantize + k_moe + k_moe_combine) with 28 distinct experts
+    "moe call per expert": (97_280 + 396_641_536 + 3_222_016 + 666_112) / 28,
 }
 
 
