@@ -52,23 +52,32 @@ FALLBACK_HBM_GBS = 6800.0
 # one ncu capture of each kernel (summaries in profiles/), valid only for the
 # kernel sources they were taken on (digest below); otherwise reported as null.
 PROFILED = {
-    "source_digest": "a052c4af5c9958cd",
+    "source_digest": "41c0470bd95c1e98",
     "k_matvec<5> (head)": 297_924_096 + 4_864_256,          # one launch, 129280 x 4096, n=5
     # one layer call (k_quantize + k_moe + k_moe_combine) with 28 distinct experts
     "moe call per expert": (97_280 + 396_641_536 + 3_222_016 + 666_112) / 28,
 }
 
 
-def source_digest():
-    """Digest of the CUDA sources of the library, to match profiler captures."""
+def source_digest(csrc=None):
+    """Digest of the CUDA sources of the library (code only: comments and
+    whitespace runs are dropped), to match profiler captures."""
     import hashlib
-    d = os.path.join(ROOT, "verify_matvec_gb300", "csrc")
+    import re
+    token = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"|\s+', re.S)
+
+    def code(text):
+        text = token.sub(lambda m: m.group(0) if m.group(0).startswith('"') else
+                         (" " if m.group(0)[0].isspace() else ""), text)
+        return re.sub(r"\s+", " ", text).strip()
+
+    d = csrc or os.path.join(ROOT, "verify_matvec_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(d)):
         if f.endswith((".cu", ".cuh", ".h")):
             h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+            with open(os.path.join(d, f), encoding="utf-8") as fh:
+                h.update(code(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

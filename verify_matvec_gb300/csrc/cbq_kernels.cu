@@ -5,12 +5,14 @@
 //   k_quantize        activation quantization, one warp per 32-value block
 //   k_matvec<NC>      dense MMVQ over NC <= 5 columns, one pass over the weights
 //   k_block_dots<NC>  the same integer path, exporting every per-block dot
-//   k_moe_gate_up     routed experts: gate+up rows, SwiGLU split, requantization
-//   k_moe_down        routed experts: down rows, router-weighted combine
+//   k_moe             routed experts, one kernel per layer call: gate+up rows,
+//                     SwiGLU split, requantization, then down rows per slot
+//   k_moe_combine     router-weighted combine of the per-slot down outputs
 //
-// All matvec-type kernels are persistent: a grid of at most (SMs x resident
-// CTAs) CTAs, each taking a contiguous range of 32-row work items, so the
-// activations are staged into shared memory once per CTA.
+// The matvec-type kernels are persistent: a grid of at most (SMs x resident
+// CTAs) CTAs whose producer warps take 32-row work items from a global
+// counter, so the activations are staged into shared memory once per CTA
+// (k_block_dots, a debug path, takes static ranges).
 #include "cbq_device.cuh"
 #include "cbq_internal.h"
 
