@@ -156,13 +156,13 @@ __device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, co
         for (int c = 0; c < NC; ++c) {
             const uint4 a0 = actb[2 * c], a1 = actb[2 * c + 1];
             const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            int s = kMagicBits, t = 0;  // two chains: lower- and upper-table parts
+            int s = kMagicBits;  // one chain over the lower- and upper-table parts
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 s = __dp4a((int)lo[i], (int)av[i], s);
-                t = __dp4a((int)hi[i], (int)av[i], t);
+                s = __dp4a((int)hi[i], (int)av[i], s);
             }
-            sdot[c] = s + t;
+            sdot[c] = s;
         }
     } else {
         uint32_t e[8];
