@@ -180,3 +180,45 @@ def test_full_layer_batch5_top8(torch, full):
     gu, dn, L, _, (ids, wts) = full
     h = synth.activations(5, H, stream=synth.S_H + 1)
     _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, 1)
+
+
+# ------------------------------------------------------------- edge shapes -
+
+@pytest.fixture(scope="module")
+def wide(torch):
+    """20 experts, so 5 tokens can each route top-16 (80 slots, the maximum)."""
+    E_, H_, F_ = 20, 256, 128
+    gu = synth.expert_blocks(E_, 2 * F_, H_, stream=620)
+    dn = synth.expert_blocks(E_, H_, F_, stream=621)
+    return gu, dn, cbq.Moe(gu, dn, E_, H_, F_), (E_, H_, F_)
+
+
+def test_maximum_slots_5x16(torch, wide):
+    gu, dn, L, (E_, H_, F_) = wide
+    h = synth.activations(5, H_, stream=622)
+    ids, wts = synth.router(5, 16, E_, stream=623)
+    _check_layer(torch, L, gu, dn, E_, H_, F_, h, ids, wts, 1)
+
+
+def test_expert_serving_more_than_five_slots(torch, wide):
+    """Expert 3 takes 8 slots (repeated ids are served as extra columns), so
+    its items run as two column chunks (5 + 3)."""
+    gu, dn, L, (E_, H_, F_) = wide
+    h = synth.activations(5, H_, stream=624)
+    ids = np.array([[3, 3, 3], [3, 3, 1], [3, 0, 2], [3, 5, 6], [7, 3, 19]], dtype=np.int32)
+    wts = np.random.default_rng(5).random((5, 3)).astype(np.float32)
+    _check_layer(torch, L, gu, dn, E_, H_, F_, h, ids, wts, 1)
+
+
+@pytest.mark.parametrize("H_,F_", [(160, 96), (1120, 352)])
+def test_ragged_layer_dims(torch, H_, F_):
+    """Block counts that are not multiples of 4 (padded blocks) or of 32
+    (a partial last stage), in both the gate_up and the down passes."""
+    E_ = 6
+    gu = synth.expert_blocks(E_, 2 * F_, H_, stream=630 + H_)
+    dn = synth.expert_blocks(E_, H_, F_, stream=631 + F_)
+    L = cbq.Moe(gu, dn, E_, H_, F_)
+    for n_tok, k in ((1, 2), (5, 4)):
+        h = synth.activations(n_tok, H_, stream=632 + n_tok)
+        ids, wts = synth.router(n_tok, k, E_, stream=633 + k)
+        _check_layer(torch, L, gu, dn, E_, H_, F_, h, ids, wts, 1)
