@@ -429,7 +429,35 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
 
-    # microseconds per layer at batch 1 (top-4) and batch 5 (top-8)
+    # microseconds per layer at batch 1 (top-4) and batch 5 (top-8).  A decode
+    # loop replays its launches from a CUDA graph, so the per-call figure is
+    # the replay of 16 captured calls (one per routing table) divided by 16;
+    # the host-driven loop (one Python call per layer) is reported beside it,
+    # with the split into the token quantization and the rest of the call.
+    def graph_us(fn, n_calls=N_SETS, replays=25):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for i in range(3):
+                fn(i)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_calls):
+                fn(i)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(replays):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return 1e3 * a.elapsed_time(b) / (replays * n_calls)
+
     def layer_us(n_tok, k, reps=50):
         tabs = []
         for i in range(N_SETS):
@@ -446,21 +474,34 @@ def run_gpu(args):
         stage_ev = [[timing_event(torch, stream) for _ in range(3)] for _ in range(reps)]
         torch.cuda.synchronize()
         a.record(stream)
-        nbytes = 0
         for i in range(reps):
             t = tabs[i % N_SETS]
             cbq.cbq_moe_set_stage_events(L, stage_ev[i])
             cbq.cbq_moe_matvec(L, t[2], t[0], t[1], y=yl)
-            nbytes += t[3] * EXPERT_BYTES
         b.record(stream)
         torch.cuda.synchronize()
         cbq.cbq_moe_set_stage_events(L, None)
-        us = 1e3 * a.elapsed_time(b) / reps
+        eager = 1e3 * a.elapsed_time(b) / reps
         split = [1e3 * sum(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev) / reps for j in range(2)]
-        return us, nbytes / reps / (us * 1e-6) / 1e9, split
+        us = graph_us(lambda i: cbq.cbq_moe_matvec(L, tabs[i][2], tabs[i][0], tabs[i][1], y=yl))
+        nbytes = sum(t[3] for t in tabs) / N_SETS * EXPERT_BYTES
+        return us, nbytes / (us * 1e-6) / 1e9, eager, split
 
-    b1_us, b1_gbs, b1_split = layer_us(1, 4)
-    b5_us, b5_gbs, b5_split = layer_us(5, 8)
+    b1_us, b1_gbs, b1_eager, b1_split = layer_us(1, 4)
+    b5_us, b5_gbs, b5_eager, b5_split = layer_us(5, 8)
+
+    # dense decode projections (4096x4096, 16384x4096) through cbq_matvec, by
+    # graph replay over copies whose bytes together exceed L2
+    dense = {}
+    for M, K, copies in ((4096, 4096, 16), (16384, 4096, 8)):
+        Ws = [cbq.Weights(synth.weight_blocks(M, K, stream=synth.S_W * 1000 + 17 * i + M // 4096), M, K)
+              for i in range(copies)]
+        for nc in (1, 5):
+            xx = torch.from_numpy(synth.activations(nc, K, stream=synth.S_X)).to(dev)
+            yy = torch.empty((nc, M), dtype=torch.float32, device=dev)
+            us = graph_us(lambda i: cbq.cbq_matvec(Ws[i % copies], xx, y=yy))
+            dense[f"{M}x{K}_n{nc}"] = {"us": us, "weight_gbs": M * (K // QK) * BB / (us * 1e-6) / 1e9}
+        del Ws
 
     # slowest rank decides; bytes add up over ranks
     (ms_max, e2e_max), (value, e2e_value) = aggregate([ms, e2e_ms], sum(wbytes), world, dev)
@@ -489,7 +530,10 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": {"batch1_top4": b1_us, "batch5_top8": b5_us,
                              "batch1_weight_gbs": b1_gbs, "batch5_weight_gbs": b5_gbs,
-                             "split_us_layer_combine": {"batch1": b1_split, "batch5": b5_split}},
+                             "timing": "CUDA-graph replay of 16 captured calls",
+                             "eager_host_loop": {"batch1": b1_eager, "batch5": b5_eager},
+                             "eager_split_us_layer_combine": {"batch1": b1_split, "batch5": b5_split}},
+            "us_per_call_dense": dense,
             "kernels_ms_per_step": {"moe layer call (k_quantize + k_moe + k_moe_combine)": sum(k_moe) / len(timed),
                                     "k_quantize (head input)": sum(k_quant) / len(timed),
                                     "k_matvec<5> (head)": sum(k_head) / len(timed)},
