@@ -93,7 +93,11 @@ const char *cbq_last_cuda_error(void);
  * memory).  The blocks are repacked into the device layout (16-byte index
  * stream interleaved by 32-row groups plus a separate fp16 scale stream); the
  * source is not retained.  Synchronizes `stream`.
- * Errors: EINVAL (null, M < 1, K < 32, K % 32 != 0), ENOMEM, ECUDA, EDEVICE. */
+ * K is bounded by the shared-memory staging of CBQ_MAX_COLS quantized
+ * activation columns next to the weight ring: K <= 26,368 on GB300 (227 KB
+ * of shared memory per CTA).
+ * Errors: EINVAL (null, M < 1, K < 32, K % 32 != 0, K above that bound),
+ * ENOMEM, ECUDA, EDEVICE. */
 int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device,
                        void *stream, cbq_weights **out);
 int cbq_weights_destroy(cbq_weights *W);
@@ -129,7 +133,9 @@ int cbq_matvec_host(const cbq_weights *W, const float *x_host, int n, float *y_h
 /* Create an MoE layer handle from canonical blocks of E experts, contiguous
  * per expert: gate_up = E x (2F rows x H cols), rows 0..F-1 the gate
  * projection and rows F..2F-1 the up projection; down = E x (H rows x F cols).
- * H % 32 == 0, F % 32 == 0, E >= 1.  Host memory if on_device == 0.
+ * H % 32 == 0, F % 32 == 0, E >= 1, H and F <= 27,648 on GB300 (shared-memory
+ * staging of CBQ_MAX_TOKENS token columns, or CBQ_MAX_COLS intermediate
+ * columns, next to the weight ring).  Host memory if on_device == 0.
  * Synchronizes `stream`.  Errors as cbq_weights_create. */
 int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int64_t F,
                    int on_device, void *stream, cbq_moe **out);

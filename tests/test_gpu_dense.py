@@ -160,3 +160,19 @@ def test_output_head_sampled_bench_shape(torch):
 def test_no_device_error_left(torch):
     """No kernel of this module recorded a pipeline timeout or a bad id."""
     assert cbq.cbq_get_device_error() == 0
+
+
+def test_largest_k_accepted_and_correct(torch):
+    """K = 26,368 (824 blocks: the most the 5-column staging fits beside the
+    weight ring in 227 KB), ragged M, a partial last stage."""
+    M, K = 70, 26368
+    W = synth.weight_blocks(M, K, stream=450)
+    for n in (1, 5):
+        _check_matvec(torch, W, M, K, synth.activations(n, K, stream=451 + n, outliers=True))
+
+
+def test_k_beyond_staging_limit_refused(torch):
+    M, K = 32, 26400
+    with pytest.raises(cbq.CbqError) as info:
+        cbq.Weights(synth.weight_blocks(M, K, stream=452), M, K)
+    assert info.value.status == cbq.CBQ_EINVAL

@@ -222,3 +222,23 @@ def test_ragged_layer_dims(torch, H_, F_):
         h = synth.activations(n_tok, H_, stream=632 + n_tok)
         ids, wts = synth.router(n_tok, k, E_, stream=633 + k)
         _check_layer(torch, L, gu, dn, E_, H_, F_, h, ids, wts, 1)
+
+
+def test_largest_hidden_accepted_and_correct(torch):
+    """H = 27,648: the most the 5-token staging fits beside the weight ring
+    and the layer kernel's static shared memory."""
+    E_, H_, F_ = 3, 27648, 64
+    gu = synth.expert_blocks(E_, 2 * F_, H_, stream=640)
+    dn = synth.expert_blocks(E_, H_, F_, stream=641)
+    L = cbq.Moe(gu, dn, E_, H_, F_)
+    h = synth.activations(5, H_, stream=642)
+    ids, wts = synth.router(5, 2, E_, stream=643)
+    _check_layer(torch, L, gu, dn, E_, H_, F_, h, ids, wts, 1)
+
+
+def test_hidden_beyond_staging_limit_refused(torch):
+    E_, H_, F_ = 1, 27680, 32
+    with pytest.raises(cbq.CbqError) as info:
+        cbq.Moe(synth.expert_blocks(E_, 2 * F_, H_, stream=644), synth.expert_blocks(E_, H_, F_, stream=645),
+                E_, H_, F_)
+    assert info.value.status == cbq.CBQ_EINVAL

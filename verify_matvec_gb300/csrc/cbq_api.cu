@@ -357,7 +357,7 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
     if (rc != CBQ_OK) return rc;
     const int nbH = (int)(H / CBQ_QK), nbF = (int)(F / CBQ_QK);
     size_t smem_max = 0;
-    CBQ_CUDA(cbq::device_smem_limit(&smem_max));
+    CBQ_CUDA(cbq::moe_smem_limit(&smem_max));
     if (cbq::moe_smem_bytes(std::max(CBQ_MAX_TOKENS * cbq::round_up4(nbH), CBQ_MAX_COLS * cbq::round_up4(nbF))) >
         smem_max)
         return CBQ_EINVAL;

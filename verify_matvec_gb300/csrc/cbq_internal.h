@@ -63,6 +63,8 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
 size_t matvec_smem_bytes(int nbp, int n);
 size_t moe_smem_bytes(int act_blocks);
 cudaError_t device_smem_limit(size_t *bytes);
+// Dynamic shared memory the layer kernel may use (opt-in limit less its static part).
+cudaError_t moe_smem_limit(size_t *bytes);
 cudaError_t read_and_clear_device_error(unsigned *code);
 
 }  // namespace cbq

@@ -17,6 +17,10 @@
 #include "cbq_internal.h"
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <utility>
 
 namespace cbq {
 __device__ unsigned int g_device_error;  // CBQ_DEVERR_* bits
@@ -216,17 +220,55 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-static int g_num_sms = 0;
+// Per-device launch facts, looked up once under a lock: the SM count, and per
+// (kernel, dynamic shared memory, block size) the resident CTAs per SM.  The
+// first time a kernel is seen on a device its dynamic shared-memory ceiling
+// is raised to the device's opt-in maximum (less its static shared memory),
+// so no launch has to set it.
+struct LaunchFacts {
+    std::mutex m;
+    std::map<int, int> sms;
+    std::map<std::pair<int, const void *>, bool> raised;
+    std::map<std::tuple<int, const void *, size_t, int>, int> per_sm;
+};
+static LaunchFacts g_launch;
 
-static cudaError_t num_sms(int *out) {
-    if (g_num_sms == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
+template <typename Kernel>
+static cudaError_t resident(Kernel kern, int threads, size_t smem, int *sms, int *per_sm) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const void *id = reinterpret_cast<const void *>(kern);
+    std::lock_guard<std::mutex> lock(g_launch.m);
+    auto s = g_launch.sms.find(dev);
+    if (s == g_launch.sms.end()) {
+        int v = 0;
+        e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
+        s = g_launch.sms.emplace(dev, v).first;
     }
-    *out = g_num_sms;
+    *sms = s->second;
+    const auto key = std::make_tuple(dev, id, smem, threads);
+    auto p = g_launch.per_sm.find(key);
+    if (p == g_launch.per_sm.end()) {
+        bool &raised = g_launch.raised[std::make_pair(dev, id)];
+        if (!raised) {  // the opt-in maximum less the kernel's static shared memory
+            int optin = 0;
+            cudaFuncAttributes fa;
+            e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+            if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         optin - (int)fa.sharedSizeBytes);
+            if (e != cudaSuccess) return e;
+            raised = true;
+        }
+        int v = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, smem);
+        if (e != cudaSuccess) return e;
+        p = g_launch.per_sm.emplace(key, v).first;
+    }
+    *per_sm = p->second;
     return cudaSuccess;
 }
 
@@ -239,15 +281,11 @@ cudaError_t device_smem_limit(size_t *bytes) {
 }
 
 // Grid of a persistent kernel over `items` work items: at most resident
-// capacity, with contiguous equal chunks (also sets the smem attribute).
+// capacity, with contiguous equal chunks.
 template <typename Kernel>
 static cudaError_t persistent_grid(Kernel kern, int threads, size_t smem, int64_t items, int *grid, int *chunk) {
     int sms = 0, per_sm = 0;
-    cudaError_t e = num_sms(&sms);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    const cudaError_t e = resident(kern, threads, smem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
     const int64_t cap = (int64_t)sms * std::max(per_sm, 1);
     const int64_t g = std::max<int64_t>(1, std::min<int64_t>(items, cap));
@@ -261,12 +299,8 @@ static cudaError_t persistent_grid(Kernel kern, int threads, size_t smem, int64_
 // resident slot, at most one per item.
 template <typename Kernel>
 static cudaError_t dynamic_grid(Kernel kern, size_t smem, int64_t items, int *grid) {
-    int chunk = 0;
-    cudaError_t e = persistent_grid(kern, kPipeThreads, smem, items, grid, &chunk);
-    if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
-    e = num_sms(&sms);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPipeThreads, smem);
+    const cudaError_t e = resident(kern, kPipeThreads, smem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
     *grid = (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)sms * std::max(per_sm, 1)));
     return cudaSuccess;
@@ -688,6 +722,15 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
         if (e != cudaSuccess) return e;
     }
     if (ws.ev[2]) e = cudaEventRecord(ws.ev[2], s);
+    return e;
+}
+
+cudaError_t moe_smem_limit(size_t *bytes) {
+    size_t optin = 0;
+    cudaFuncAttributes fa;
+    cudaError_t e = device_smem_limit(&optin);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k_moe);
+    *bytes = e == cudaSuccess ? optin - fa.sharedSizeBytes : 0;
     return e;
 }
 
