@@ -52,10 +52,10 @@ FALLBACK_HBM_GBS = 6800.0
 # one ncu capture of each kernel (summaries in profiles/), valid only for the
 # kernel sources they were taken on (digest below); otherwise reported as null.
 PROFILED = {
-    "source_digest": "41c0470bd95c1e98",
-    "k_matvec<5> (head)": 297_924_096 + 4_864_256,          # one launch, 129280 x 4096, n=5
+    "source_digest": "116ad76332bac780",
+    "k_matvec<5> (head)": 297_925_120 + 4_823_552,          # one launch, 129280 x 4096, n=5
     # one layer call (k_quantize + k_moe + k_moe_combine) with 28 distinct experts
-    "moe call per expert": (97_280 + 396_641_536 + 3_222_016 + 666_112) / 28,
+    "moe call per expert": (97_280 + 396_601_600 + 3_591_936 + 666_112) / 28,
 }
 
 
@@ -320,29 +320,24 @@ def run_gpu(args):
     distinct = [len(synth.distinct_experts(s[0], n_exp)) for s in sets]
     y = torch.empty((N_TOK, H), dtype=torch.float32, device=dev)
     yh = torch.empty((HEAD_N, HEAD_M), dtype=torch.float32, device=dev)
-    qx = torch.empty((HEAD_N, HEAD_K), dtype=torch.int8, device=dev)
-    dx = torch.empty((HEAD_N, HEAD_K // QK), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     total = args.warmup + args.steps
-    ev = [[timing_event(torch, stream) for _ in range(4)] for _ in range(total)]
+    ev = [[timing_event(torch, stream) for _ in range(3)] for _ in range(total)]
     torch.cuda.synchronize()
 
     def step(i, events):
-        # events around whole calls only (none between the layer call's own
-        # kernels, whose programmatic-dependent-launch overlap they would cut):
-        # MoE call start, MoE call end, head matvec start, head matvec end
+        # events around whole calls only (none between a call's own kernels,
+        # whose programmatic-dependent-launch overlap they would cut): MoE call
+        # start, MoE call end = head call start, head call end
         ids, wts, h, x = d_sets[i % N_SETS]
         if events is not None:
             events[0].record(stream)
         cbq.cbq_moe_matvec(L, h, ids, wts, swiglu=1, y=y)
         if events is not None:
             events[1].record(stream)
-        cbq.cbq_quantize_act(x, qx, dx)
+        cbq.cbq_matvec(head, x, y=yh)
         if events is not None:
             events[2].record(stream)
-        cbq.cbq_matvec_q(head, qx, dx, y=yh)
-        if events is not None:
-            events[3].record(stream)
 
     # untimed warm-up
     for i in range(args.warmup):
@@ -369,19 +364,18 @@ def run_gpu(args):
     timed = range(args.warmup, total)
     wbytes = [distinct[i % N_SETS] * EXPERT_BYTES + HEAD_BYTES for i in timed]
     k_moe = [ev[i][0].elapsed_time(ev[i][1]) for i in timed]
-    k_quant = [ev[i][1].elapsed_time(ev[i][2]) for i in timed]
-    k_head = [ev[i][2].elapsed_time(ev[i][3]) for i in timed]
+    k_head = [ev[i][1].elapsed_time(ev[i][2]) for i in timed]
     err = cbq.cbq_get_device_error()
 
     # per-launch algorithmic bytes: weights + activations read + outputs written
     slots = N_TOK * TOPK
     moe_io = 8 * N_TOK * H + 8 * slots  # h in, y out, ids + router weights in (intermediates stay in L2)
     moe_alg = [distinct[i % N_SETS] * EXPERT_BYTES + moe_io for i in timed]
-    head_alg = HEAD_BYTES + HEAD_N * HEAD_K * (1 + 4 / QK) + 4 * HEAD_N * HEAD_M
-    # the MoE call is three PDL-chained launches; events go around the whole
-    # call, so k_moe's figure includes its short quantize and combine launches
+    head_alg = HEAD_BYTES + 4 * HEAD_N * HEAD_K + 4 * HEAD_N * HEAD_M  # weights, x in, y out
+    # each call is a chain of PDL launches and events go around whole calls,
+    # so a kernel's figure includes the short launches of its call
     kern = {"k_moe (with its k_quantize and k_moe_combine launches)": (sum(k_moe), sum(moe_alg) / len(k_moe)),
-            "k_matvec<5> (head)": (sum(k_head), head_alg)}
+            "k_matvec<5> (head, with its k_quantize launch)": (sum(k_head), head_alg)}
     dom = max(kern, key=lambda k: kern[k][0])
     dom_ms, dom_bytes = kern[dom][0] / len(timed), kern[dom][1]
     peak, peak_kind = peaks()
@@ -535,8 +529,7 @@ def run_gpu(args):
                              "eager_split_us_layer_combine": {"batch1": b1_split, "batch5": b5_split}},
             "us_per_call_dense": dense,
             "kernels_ms_per_step": {"moe layer call (k_quantize + k_moe + k_moe_combine)": sum(k_moe) / len(timed),
-                                    "k_quantize (head input)": sum(k_quant) / len(timed),
-                                    "k_matvec<5> (head)": sum(k_head) / len(timed)},
+                                    "head call (k_quantize + k_matvec<5>)": sum(k_head) / len(timed)},
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes},
