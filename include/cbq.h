@@ -120,8 +120,13 @@ int cbq_quantize_act(const float *x_dev, int64_t K, int n, int8_t *qx_dev, float
 int cbq_matvec_q(const cbq_weights *W, const int8_t *qx_dev, const float *dx_dev, int n,
                  float *y_dev, void *stream);
 
-/* The whole dense path: quantize x_dev (n x K fp32) into the handle's
- * workspace, then cbq_matvec_q into y_dev (n x M fp32). */
+/* The whole dense path: quantize x_dev (n x K fp32) with the rule of
+ * cbq_quantize_act, then the matvec of cbq_matvec_q into y_dev (n x M fp32);
+ * the result has the same bits as those two calls.  For n == 1 with x_dev
+ * 16-byte aligned this is one kernel launch (the matvec kernel quantizes x
+ * while its weight stream starts); otherwise the quantization kernel writes
+ * the handle's workspace first and the matvec kernel follows it as a
+ * programmatic dependent.  One call at a time per handle. */
 int cbq_matvec(const cbq_weights *W, const float *x_dev, int n, float *y_dev, void *stream);
 
 /* Same with HOST buffers: copies x (n x K fp32) to the device, runs

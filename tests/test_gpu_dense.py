@@ -115,10 +115,15 @@ def test_matvec_16384_sampled(torch, n):
     _check_matvec(torch, W, M, K, synth.activations(n, K, stream=synth.S_X + 50, outliers=True), rows=rows)
 
 
-def test_matvec_q_equals_matvec_and_host_entry(torch):
-    M, K, n = 300, 1024, 4
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("K", [1024, 1056])
+def test_matvec_q_equals_matvec_and_host_entry(torch, n, K):
+    """cbq_matvec quantizes inside the matvec kernel for one 16-byte aligned
+    column and through the quantization kernel otherwise; both, the
+    pre-quantized entry and the host entry give the same bits."""
+    M = 300
     W = synth.weight_blocks(M, K, stream=401)
-    x = synth.activations(n, K, stream=402)
+    x = synth.activations(n, K, stream=402 + n, outliers=True)
     Wh = cbq.Weights(W, M, K)
     y = cbq.cbq_matvec(Wh, _dev(torch, x)).cpu().numpy()
     qx, dx = cbq.cbq_quantize_act(_dev(torch, x))
@@ -126,6 +131,11 @@ def test_matvec_q_equals_matvec_and_host_entry(torch):
     np.testing.assert_array_equal(yq, y)
     yh = cbq.cbq_matvec_host(Wh, x)
     np.testing.assert_array_equal(yh, y)
+    buf = torch.zeros(n * K + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = _dev(torch, x).reshape(-1)
+    xm = buf[1:].view(n, K)  # 4 bytes past a 16-byte boundary
+    assert xm.data_ptr() % 16 == 4
+    np.testing.assert_array_equal(cbq.cbq_matvec(Wh, xm).cpu().numpy(), y)
 
 
 def test_matvec_exact_invariants(torch):

@@ -249,6 +249,13 @@ int cbq_matvec(const cbq_weights *W, const float *x_dev, int n, float *y_dev, vo
     DeviceScope scope(W->device);
     CBQ_CUDA(scope.status());
     cudaStream_t s = as_stream(stream);
+    // one column: one launch, the matvec kernel quantizes x itself (with more
+    // columns the separate quantization kernel, which spreads the divisions
+    // over n*K threads, is faster)
+    if (n == 1 && aligned16(x_dev)) {
+        CBQ_CUDA(cbq::launch_matvec_f32(W->mat, x_dev, n, y_dev, s));
+        return CBQ_OK;
+    }
     CBQ_CUDA(cbq::launch_quantize(x_dev, W->K, n, W->ws_qx, W->ws_dx, s));
     CBQ_CUDA(cbq::launch_matvec(W->mat, W->ws_qx, W->ws_dx, n, y_dev, s, /*pdl=*/true));
     return CBQ_OK;

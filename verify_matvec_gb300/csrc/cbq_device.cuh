@@ -269,28 +269,76 @@ __device__ __forceinline__ int8_t quant_lane(float v, float &d_out) {
     return (int8_t)q;
 }
 
-// Quantize fp32 rows straight into the staged (expander-ordered) layout:
-// block k = t*nbp + b holds row t's values 32b..32b+31 (x[t*ld + 32b ..]);
-// blocks b >= nb are zero.  One warp per block, lane = element; warps w0,
-// w0+step, ... share the blocks.  Same rule and result as quant_lane.
-__device__ __forceinline__ void quant_stage_rows(const float *__restrict__ x, int64_t ld, int nrows, int nb, int nbp,
-                                                 uint4 *act_s, float *dx_s, int w0, int step, int lane) {
-    // byte of element `lane` in the expander order: word 2m+(r>>1), byte
-    // 2*(r&1) + (lane >= 16), with lane%16 = 4m + r
-    const int r4 = lane & 15, m = r4 >> 2, r = r4 & 3;
-    const int pos = (2 * m + (r >> 1)) * 4 + (r & 1) * 2 + (lane >> 4);
-    for (int k = w0; k < nrows * nbp; k += step) {
-        const int t = k / nbp, b = k - t * nbp;
-        unsigned char *blk = reinterpret_cast<unsigned char *>(act_s + (size_t)k * 2);
-        if (b < nb) {
-            float d;
-            const int8_t q = quant_lane(x[(size_t)t * ld + (size_t)b * kQK + lane], d);
-            blk[pos] = (unsigned char)q;
-            if (lane == 0) dx_s[k] = d;
-        } else {
-            if (lane < 8) reinterpret_cast<uint32_t *>(blk)[lane] = 0u;
-            if (lane == 0) dx_s[k] = 0.0f;
+// Quantize NC fp32 columns (x[c*K ..], 16-byte aligned) straight into the
+// block-major staged layout of stage_cols, by thread pairs: the even thread
+// of a pair holds values 0..15 of a block, the odd thread 16..31 (four 16-byte
+// loads each).  Same rule and bits as quant_lane: d = max|v|/127 in IEEE fp32
+// division (the max over the pair is exact in any order), q = rint(v/d)
+// clamped, q = 0 when d == 0.  Expander order: word 2m+h of a block holds
+// values 4m+2h, 4m+2h+16, 4m+2h+1, 4m+2h+17, i.e. the pair (4m+2h, 4m+2h+1)
+// of each thread, even thread's bytes at 0 and 2.  Blocks nb..nbp-1 are zero.
+// Threads tid = 0..nthr-1 (nthr even) share the work.
+template <int NC>
+__device__ __forceinline__ void quant_stage_cols(const float *__restrict__ x, int64_t K, int nb, int nbp,
+                                                 uint4 *act_s, float *dx_s, int tid, int nthr) {
+    const int half = tid & 1;
+    // the loop test reads the pair index of lane 0, so a warp runs the same
+    // number of rounds (its shuffles are full-warp); past the end a pair idles
+    for (int k = tid >> 1; k - ((tid & 31) >> 1) < NC * nb; k += nthr >> 1) {
+        const bool live = k < NC * nb;
+        const int c = k / nb, b = k - c * nb;
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+        if (live) {
+            const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)c * K + (size_t)b * kQK + half * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 f = src[i];
+                v[4 * i] = f.x;
+                v[4 * i + 1] = f.y;
+                v[4 * i + 2] = f.z;
+                v[4 * i + 3] = f.w;
+            }
         }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        const float d = amax / 127.0f;
+        uint32_t pr[4];  // pr[u] = pairs 2u (low half) and 2u+1 (high half) of this thread
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float q = 0.0f;
+                if (d != 0.0f) q = fminf(fmaxf(rintf(v[4 * u + e] / d), -127.0f), 127.0f);
+                w |= ((uint32_t)(int)q & 0xFFu) << (8 * e);
+            }
+            pr[u] = w;
+        }
+        // the even thread builds words 0..3 (pairs 0..3), the odd thread 4..7
+        const uint32_t give0 = half ? pr[0] : pr[2], give1 = half ? pr[1] : pr[3];
+        const uint32_t got0 = __shfl_xor_sync(0xffffffffu, give0, 1);
+        const uint32_t got1 = __shfl_xor_sync(0xffffffffu, give1, 1);
+        const uint32_t own0 = half ? pr[2] : pr[0], own1 = half ? pr[3] : pr[1];
+        const uint32_t e0 = half ? got0 : own0, o0 = half ? own0 : got0;  // even / odd thread's pairs
+        const uint32_t e1 = half ? got1 : own1, o1 = half ? own1 : got1;
+        const uint4 out = make_uint4(prmt(e0, o0, 0x5140u), prmt(e0, o0, 0x7362u), prmt(e1, o1, 0x5140u),
+                                     prmt(e1, o1, 0x7362u));
+        if (live) {
+            const int ai = b * NC + c;
+            act_s[(size_t)ai * 2 + half] = out;
+            if (!half) dx_s[((b >> 1) * NC + c) * 2 + (b & 1)] = d;
+        }
+    }
+    for (int k = tid; k < NC * (nbp - nb); k += nthr) {  // padded blocks
+        const int c = k / (nbp - nb), b = nb + k - c * (nbp - nb);
+        const int ai = b * NC + c;
+        act_s[(size_t)ai * 2] = make_uint4(0, 0, 0, 0);
+        act_s[(size_t)ai * 2 + 1] = make_uint4(0, 0, 0, 0);
+        dx_s[((b >> 1) * NC + c) * 2 + (b & 1)] = 0.0f;
     }
 }
 

@@ -56,6 +56,9 @@ cudaError_t launch_quantize(const float *x, int64_t K, int n, int8_t *qx, float 
 // stream (only when that kernel is this library's own quantization).
 cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, int n, float *y,
                           cudaStream_t s, bool pdl = false);
+// The matvec from one fp32 column x (K values, 16-byte aligned), quantized
+// inside the kernel (one launch).
+cudaError_t launch_matvec_f32(const DevMat &W, const float *x, int n, float *y, cudaStream_t s);
 cudaError_t launch_block_dots(const DevMat &W, const int8_t *qx, int n, int32_t *sdot, cudaStream_t s);
 cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n_tok, const int32_t *ids,
                        const float *wts, int k, int swiglu, float *y, cudaStream_t s);

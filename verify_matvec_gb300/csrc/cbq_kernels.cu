@@ -126,11 +126,15 @@ size_t matvec_smem_bytes(int nbp, int n) { return pipe_smem_bytes(kStages, n, nb
 static size_t dots_smem_bytes(int nbp, int n) { return (size_t)n * nbp * 36; }
 
 // Dense MMVQ: 32-row groups fetched dynamically, all NC columns per pass.
-template <int NC>
+// kF32: the consumers quantize the fp32 columns xf themselves while the
+// producer starts the weight stream (no quantization kernel before it);
+// otherwise they stage qx/dx written by the quantization kernel launched just
+// before (a programmatic dependency).
+template <int NC, bool kF32>
 __global__ void __launch_bounds__(kPipeThreads, 2)
     k_matvec(const uint4 *__restrict__ qs, const uint2 *__restrict__ sc, int64_t M, int G, int nb, int nbp,
-             const int8_t *__restrict__ qx, const float *__restrict__ dx, int64_t K, float *__restrict__ y,
-             unsigned *__restrict__ sched) {
+             const int8_t *__restrict__ qx, const float *__restrict__ dx, const float *__restrict__ xf, int64_t K,
+             float *__restrict__ y, unsigned *__restrict__ sched) {
     extern __shared__ __align__(128) unsigned char smem[];
     const PipeSmem S = carve_pipe(smem, kStages, NC, nbp);
     pipe_init(S.pipe);
@@ -153,8 +157,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
         }
         return;
     }
-    pdl_wait();  // the activations may come from the kernel launched just before
-    {
+    if constexpr (kF32) {
+        quant_stage_cols<NC>(xf, K, nb, nbp, S.act, S.dx, threadIdx.x, kConsumers);
+    } else {
+        pdl_wait();  // the activations come from the kernel launched just before
         ColSrc src{qx, dx, (size_t)K, (size_t)nb, {0, 1, 2, 3, 4}};
         stage_cols(src, NC, nb, nbp, S.act, S.dx, threadIdx.x, kConsumers, false, true);
     }
@@ -306,27 +312,32 @@ static cudaError_t dynamic_grid(Kernel kern, size_t smem, int64_t items, int *gr
     return cudaSuccess;
 }
 
-template <int NC>
-static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const float *dx, float *y, cudaStream_t s,
-                                   bool pdl) {
+template <int NC, bool kF32>
+static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const float *dx, const float *xf, float *y,
+                                   cudaStream_t s, bool pdl) {
     const size_t smem = matvec_smem_bytes(W.nbp, NC);
     int grid = 0;
-    cudaError_t e = dynamic_grid(k_matvec<NC>, smem, W.G, &grid);
+    cudaError_t e = dynamic_grid(k_matvec<NC, kF32>, smem, W.G, &grid);
     if (e != cudaSuccess) return e;
-    return launch_k(k_matvec<NC>, grid, kPipeThreads, smem, s, pdl, W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx, dx,
-                    (int64_t)W.nb * kQK, y, W.sched);
+    return launch_k(k_matvec<NC, kF32>, grid, kPipeThreads, smem, s, pdl, W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx,
+                    dx, xf, (int64_t)W.nb * kQK, y, W.sched);
 }
 
 cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, int n, float *y, cudaStream_t s,
                           bool pdl) {
     switch (n) {
-        case 1: return launch_matvec_n<1>(W, qx, dx, y, s, pdl);
-        case 2: return launch_matvec_n<2>(W, qx, dx, y, s, pdl);
-        case 3: return launch_matvec_n<3>(W, qx, dx, y, s, pdl);
-        case 4: return launch_matvec_n<4>(W, qx, dx, y, s, pdl);
-        case 5: return launch_matvec_n<5>(W, qx, dx, y, s, pdl);
+        case 1: return launch_matvec_n<1, false>(W, qx, dx, nullptr, y, s, pdl);
+        case 2: return launch_matvec_n<2, false>(W, qx, dx, nullptr, y, s, pdl);
+        case 3: return launch_matvec_n<3, false>(W, qx, dx, nullptr, y, s, pdl);
+        case 4: return launch_matvec_n<4, false>(W, qx, dx, nullptr, y, s, pdl);
+        case 5: return launch_matvec_n<5, false>(W, qx, dx, nullptr, y, s, pdl);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_matvec_f32(const DevMat &W, const float *x, int n, float *y, cudaStream_t s) {
+    if (n != 1) return cudaErrorInvalidValue;
+    return launch_matvec_n<1, true>(W, nullptr, nullptr, x, y, s, false);
 }
 
 template <int NC>
