@@ -161,8 +161,10 @@ int cbq_moe_info(const cbq_moe *L, int *E, int64_t *H, int64_t *F, int64_t *devi
  * The sum over j runs in slot order (deterministic, no atomics on y).
  * Three kernel launches on `stream`, each a programmatic dependent of the one
  * before: the token quantization, the layer kernel (gate_up, SwiGLU,
- * requantization, down), the combine.  One call at a time per handle (its
- * workspace and counters are shared by the calls).
+ * requantization, down), the combine.  With one token and h_dev 16-byte
+ * aligned, two: the layer kernel quantizes the token itself (same bits).  One
+ * call at a time per handle (its workspace and counters are shared by the
+ * calls).
  * 1 <= n_tok <= CBQ_MAX_TOKENS, 1 <= topk <= min(CBQ_MAX_TOPK, E). */
 int cbq_moe_matvec(const cbq_moe *L, const float *h_dev, int n_tok, const int32_t *ids_dev,
                    const float *wts_dev, int topk, int swiglu, float *y_dev, void *stream);

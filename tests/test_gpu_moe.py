@@ -242,3 +242,18 @@ def test_hidden_beyond_staging_limit_refused(torch):
         cbq.Moe(synth.expert_blocks(E_, 2 * F_, H_, stream=644), synth.expert_blocks(E_, H_, F_, stream=645),
                 E_, H_, F_)
     assert info.value.status == cbq.CBQ_EINVAL
+
+
+def test_one_token_quantized_in_kernel_matches_kernel_path(torch, small):
+    """One token with h 16-byte aligned is quantized inside the layer kernel;
+    shifted by 4 bytes it goes through the quantization kernel: same bits."""
+    gu, dn, L = small
+    h = synth.activations(1, H_S, stream=650, outliers=True)
+    ids, wts = synth.router(1, 4, E_S, stream=651)
+    y = cbq.cbq_moe_matvec(L, _dev(torch, h), _dev(torch, ids), _dev(torch, wts)).cpu().numpy()
+    buf = torch.zeros(H_S + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = _dev(torch, h).reshape(-1)
+    hm = buf[1:].view(1, H_S)
+    assert hm.data_ptr() % 16 == 4
+    ym = cbq.cbq_moe_matvec(L, hm, _dev(torch, ids), _dev(torch, wts)).cpu().numpy()
+    np.testing.assert_array_equal(ym, y)

@@ -374,6 +374,7 @@ struct MoeArgs {
     int n_tok, k, swiglu;
     int nbH, nbpH, nbF, nbpF;
     int act_blocks;  // staged-activation capacity in blocks (tokens, then down columns)
+    int quant_tokens;  // the consumers quantize h themselves (one token, h 16-byte aligned)
 };
 
 // Distinct in-range expert ids of the routing table, ascending, computed
@@ -591,9 +592,12 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
         }
         return;
     }
-    // consumers: stage the quantized tokens (written by the kernel launched just before)
-    pdl_wait();
-    {
+    // consumers: stage the quantized tokens, quantizing one token here or
+    // reading those of the quantization kernel launched just before
+    if (A.quant_tokens) {
+        quant_stage_cols<1>(A.h, A.L.H, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
+    } else {
+        pdl_wait();
         ColSrc src{A.ws.qh, A.ws.dh, (size_t)A.L.H, (size_t)A.nbH, {0, 1, 2, 3, 4}};
         stage_cols(src, A.n_tok, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
     }
@@ -713,17 +717,23 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     A.nbF = L.F / kQK;
     A.nbpF = round_up4(A.nbF);
     A.act_blocks = std::max(n_tok * A.nbpH, kMaxCols * A.nbpF);
+    // one token: the layer kernel quantizes it (one launch fewer); the layer
+    // kernel then follows the stream's earlier work in plain order, since it
+    // reads the routing table before any dependency wait
+    A.quant_tokens = n_tok == 1 && ((uintptr_t)h & 15u) == 0;
     cudaError_t e = cudaSuccess;
     if (ws.ev[0] && (e = cudaEventRecord(ws.ev[0], s)) != cudaSuccess) return e;
-    e = launch_quantize(h, L.H, n_tok, ws.qh, ws.dh, s);
-    if (e != cudaSuccess) return e;
+    if (!A.quant_tokens) {
+        e = launch_quantize(h, L.H, n_tok, ws.qh, ws.dh, s);
+        if (e != cudaSuccess) return e;
+    }
     const int64_t max_experts = std::min(n_tok * k, L.E);
     {
         const size_t smem = moe_smem_bytes(A.act_blocks);
         int grid = 0;
         e = dynamic_grid(k_moe, smem, max_experts * (L.F / 32 + L.H / 32), &grid);
         if (e != cudaSuccess) return e;
-        e = launch_k(k_moe, grid, kPipeThreads, smem, s, true, A);
+        e = launch_k(k_moe, grid, kPipeThreads, smem, s, !A.quant_tokens, A);
         if (e != cudaSuccess) return e;
     }
     if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
