@@ -52,10 +52,10 @@ FALLBACK_HBM_GBS = 6800.0
 # one ncu capture of each kernel (summaries in profiles/), valid only for the
 # kernel sources they were taken on (digest below); otherwise reported as null.
 PROFILED = {
-    "source_digest": "116ad76332bac780",
-    "k_matvec<5> (head)": 297_925_120 + 4_823_552,          # one launch, 129280 x 4096, n=5
+    "source_digest": "07e9e29618d79afc",
+    "k_matvec<5> (head)": 297_925_632 + 5_171_712,          # one launch, 129280 x 4096, n=5
     # one layer call (k_quantize + k_moe + k_moe_combine) with 28 distinct experts
-    "moe call per expert": (97_280 + 396_601_600 + 3_591_936 + 666_112) / 28,
+    "moe call per expert": (97_536 + 396_587_264 + 3_898_368 + 666_112) / 28,
 }
 
 
