@@ -47,6 +47,7 @@ WORKLOAD = ("MoE verify layer: 5 tokens x top-8 of 256 codebook-4bit experts (ga
             "down 4096 rows x 2048) with fused SwiGLU and weighted combine, plus the 129280x4096 "
             "output head at n=5")
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
 # one ncu capture of each kernel (summaries in profiles/), valid only for the
@@ -122,9 +123,14 @@ def routing_sets(seed_base=synth.S_IDS + 100, n_exp=E):
 
 # -------------------------------------------------------------- oracle -----
 
-def oracle_sample(sets, n_steps, per_step_seconds_hint=None):
+def oracle_sample(sets, n_steps, threads=1):
     """Time the CPU oracle on a bounded sample of the workload: token 0 of the
-    MoE layer (its 8 slots) plus 1/16 of the head rows at n = 5, per step."""
+    MoE layer (its 8 slots) plus 1/16 of the head rows at n = 5, per step.
+    With threads > 1 the same oracle calls are split over a thread pool (the
+    slots one per task, the head rows in one chunk per thread; the C oracle
+    runs without the interpreter lock), as a row-split baseline on all cores."""
+    from concurrent.futures import ThreadPoolExecutor
+
     from oracle import oracle as O
     ids, wts, h, x = sets[0]
     used = synth.distinct_experts(ids[:1], E)
@@ -137,13 +143,27 @@ def oracle_sample(sets, n_steps, per_step_seconds_hint=None):
     head = synth.weight_blocks(rows, HEAD_K, stream=synth.S_HEAD)
     step_bytes = len(used) * EXPERT_BYTES + rows * (HEAD_K // QK) * BB
     times = []
-    for _ in range(n_steps):
-        t0 = time.perf_counter()
-        O.moe(gu, dn, E, H, F, h[:1], ids[:1], wts[:1], swiglu=1)
-        O.matvec(head, rows, HEAD_K, x)
-        times.append(time.perf_counter() - t0)
+    if threads <= 1:
+        for _ in range(n_steps):
+            t0 = time.perf_counter()
+            O.moe(gu, dn, E, H, F, h[:1], ids[:1], wts[:1], swiglu=1)
+            O.matvec(head, rows, HEAD_K, x)
+            times.append(time.perf_counter() - t0)
+        kind = "single-threaded oracle"
+    else:
+        bounds = np.linspace(0, rows, threads + 1).astype(int)
+        tasks = [(lambda j=j: O.moe(gu, dn, E, H, F, h[:1], ids[:1, j:j + 1], wts[:1, j:j + 1], swiglu=1))
+                 for j in range(ids.shape[1])]
+        tasks += [(lambda a=a, b=b: O.matvec(head[a:b], b - a, HEAD_K, x))
+                  for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+        with ThreadPoolExecutor(max_workers=threads) as pool:
+            for _ in range(n_steps):
+                t0 = time.perf_counter()
+                list(pool.map(lambda f: f(), tasks))
+                times.append(time.perf_counter() - t0)
+        kind = f"oracle split over {threads} threads (slots, head row chunks)"
     sample = (f"per step: token 0 of the batch-5 MoE layer ({len(used)} experts, "
-              f"{len(used) * EXPERT_BYTES} B) + {rows} of {HEAD_M} head rows at n=5; single-threaded oracle")
+              f"{len(used) * EXPERT_BYTES} B) + {rows} of {HEAD_M} head rows at n=5; {kind}")
     return step_bytes, times, sample
 
 
@@ -477,12 +497,16 @@ def run_gpu(args):
         cbq.cbq_moe_set_stage_events(L, None)
         eager = 1e3 * a.elapsed_time(b) / reps
         split = [1e3 * sum(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev) / reps for j in range(2)]
-        us = graph_us(lambda i: cbq.cbq_moe_matvec(L, tabs[i][2], tabs[i][0], tabs[i][1], y=yl))
+        trials = [graph_us(lambda i: cbq.cbq_moe_matvec(L, tabs[i][2], tabs[i][0], tabs[i][1], y=yl))
+                  for _ in range(5)]
+        us = statistics.median(trials)
+        half = 2.776 * statistics.stdev(trials) / 5 ** 0.5  # 95% CI of the mean, 4 degrees of freedom
+        ci = [statistics.mean(trials) - half, statistics.mean(trials) + half]
         nbytes = sum(t[3] for t in tabs) / N_SETS * EXPERT_BYTES
-        return us, nbytes / (us * 1e-6) / 1e9, eager, split
+        return us, nbytes / (us * 1e-6) / 1e9, eager, split, ci
 
-    b1_us, b1_gbs, b1_eager, b1_split = layer_us(1, 4)
-    b5_us, b5_gbs, b5_eager, b5_split = layer_us(5, 8)
+    b1_us, b1_gbs, b1_eager, b1_split, b1_ci = layer_us(1, 4)
+    b5_us, b5_gbs, b5_eager, b5_split, b5_ci = layer_us(5, 8)
 
     # dense decode projections (4096x4096, 16384x4096) through cbq_matvec, by
     # graph replay over copies whose bytes together exceed L2
@@ -502,7 +526,7 @@ def run_gpu(args):
     h2d = N_TOK * H * 4 + 2 * slots * 4 + HEAD_N * HEAD_K * 4
     d2h = N_TOK * H * 4 + HEAD_N * HEAD_M * 4
 
-    cpu = None
+    cpu = cpu_mt = None
     if rank == 0 and world == 1:
         n_cpu = 1
         _, t1s = oracle_sample(sets, 1)[0:2]
@@ -510,6 +534,11 @@ def run_gpu(args):
         step_bytes, times, sample = oracle_sample(sets, n_cpu)
         cpu = {"value": step_bytes * len(times) / sum(times) / 1e9, "unit": "GB/s", "cores": 1,
                "kind": "oracle", "sample": f"{n_cpu} repetitions; " + sample}
+        cores = os.cpu_count() or 1
+        n_mt = max(1, min(40, int(5.0 * cores / max(t1s[0], 1e-3))))
+        step_bytes, times, sample = oracle_sample(sets, n_mt, threads=cores)
+        cpu_mt = {"value": step_bytes * len(times) / sum(times) / 1e9, "unit": "GB/s", "cores": cores,
+                  "kind": "oracle", "sample": f"{n_mt} repetitions; " + sample}
 
     if rank == 0:
         line = {
@@ -524,7 +553,9 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": {"batch1_top4": b1_us, "batch5_top8": b5_us,
                              "batch1_weight_gbs": b1_gbs, "batch5_weight_gbs": b5_gbs,
-                             "timing": "CUDA-graph replay of 16 captured calls",
+                             "timing": "CUDA-graph replay of 16 captured calls x 25; median of 5 trials",
+                             "ci95_us": {"batch1": b1_ci, "batch5": b5_ci},
+                             "batch1_frac_of_peak": b1_gbs / peak, "batch5_frac_of_peak": b5_gbs / peak,
                              "eager_host_loop": {"batch1": b1_eager, "batch5": b5_eager},
                              "eager_split_us_layer_combine": {"batch1": b1_split, "batch5": b5_split}},
             "us_per_call_dense": dense,
@@ -532,8 +563,10 @@ def run_gpu(args):
                                     "head call (k_quantize + k_matvec<5>)": sum(k_head) / len(timed)},
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
+                         "peak_nominal": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS,
                          "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes},
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_mt,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 5 * args.steps,  # per step: quantize, layer kernel, combine; quantize, head matvec
             "clocks": clk,

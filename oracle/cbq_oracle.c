@@ -282,3 +282,31 @@ int oracle_moe_down_combine(const uint8_t *down, int E, int64_t H, int64_t F,
     }
     return bad;
 }
+
+/* Top-k by repeated selection of the largest remaining logit (the lowest
+ * index among equal ones), then the softmax of the selected logits. */
+void oracle_router_topk(const float *logits, int n_tok, int E, int k, int32_t *ids, double *wts) {
+    unsigned char *taken = (unsigned char *)calloc((size_t)E, 1);
+    for (int t = 0; t < n_tok; ++t) {
+        const float *l = logits + (int64_t)t * E;
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e;
+            }
+            taken[best] = 1;
+            ids[t * k + j] = best;
+        }
+        const double lmax = (double)l[ids[t * k]];
+        double sum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const double w = exp((double)l[ids[t * k + j]] - lmax);
+            wts[t * k + j] = w;
+            sum += w;
+        }
+        for (int j = 0; j < k; ++j) wts[t * k + j] /= sum;
+    }
+    free(taken);
+}

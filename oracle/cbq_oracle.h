@@ -129,6 +129,15 @@ int oracle_moe_down_combine(const uint8_t *down, int E, int64_t H, int64_t F,
                             const int8_t *qa, const float *da,
                             double *y, double *ybound);
 
+/* Routed-expert selection from router logits (the "configured routed-expert
+ * top-k" of "feat(ds4): add DSpark speculative decoding"; the pages give no
+ * formula, the plain reading is used): for every token t, ids[t][0..k) are
+ * the indices of the k largest logits[t][0..E) in descending order, equal
+ * logits ordered by the lower index first; wts[t][j] is the softmax over the
+ * k selected logits, computed in fp64 (exp(l_j - l_max) / sum).
+ * 1 <= k <= E. */
+void oracle_router_topk(const float *logits, int n_tok, int E, int k, int32_t *ids, double *wts);
+
 #ifdef __cplusplus
 }
 #endif

@@ -72,6 +72,8 @@ def _load():
         lib.oracle_moe.restype = I
         lib.oracle_moe_down_combine.argtypes = [P, I, I64, I64, I, P, P, I, P, P, P, P]
         lib.oracle_moe_down_combine.restype = I
+        lib.oracle_router_topk.argtypes = [P, I, I, I, P, P]
+        lib.oracle_router_topk.restype = None
         _lib = lib
         return lib
 
@@ -202,3 +204,13 @@ def moe_down_combine(down, E, H, F, ids, wts, qa, da):
     nbad = _load().oracle_moe_down_combine(_p(down), E, H, F, n_tok, _p(ids), _p(wts), k,
                                            _p(qa), _p(da), _p(y), _p(yb))
     return y, yb, nbad
+
+
+def router_topk(logits, k):
+    """ids (n_tok, k) int32 and fp64 softmax weights of the k largest logits."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    n_tok, E = logits.shape
+    ids = np.empty((n_tok, k), dtype=np.int32)
+    wts = np.empty((n_tok, k), dtype=np.float64)
+    _load().oracle_router_topk(_p(logits), n_tok, E, k, _p(ids), _p(wts))
+    return ids, wts

@@ -422,3 +422,65 @@ def test_moe_large_gate_makes_silu_identity(tiny_layer):
     _, a0, _, _, _ = O.moe(big, dn, E_, H_, F_, h, np.array([[0]]), np.array([[1.0]]),
                            swiglu=0, want_intermediate=True)
     np.testing.assert_allclose(a1, a0, rtol=1e-6)
+
+
+# ------------------------------------------------------------- router top-k --
+
+def _read_router_cases(golden_dir):
+    cases, cur = [], {}
+    with open(os.path.join(golden_dir, "router_topk.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, val = line.split(":", 1)
+            cur[key] = val.split()
+            if key == "terms":
+                cases.append(cur)
+                cur = {}
+    return cases
+
+
+def test_router_topk_golden(golden_dir):
+    cases = _read_router_cases(golden_dir)
+    assert len(cases) == 4
+    for c in cases:
+        k = int(c["k"][0])
+        logits = np.array([[float(v) for v in c["logits"]]], dtype=np.float32)
+        ids, wts = O.router_topk(logits, k)
+        np.testing.assert_array_equal(ids[0], [int(v) for v in c["ids"]])
+        terms = np.exp(np.array([float(v) for v in c["terms"]]))
+        np.testing.assert_allclose(wts[0], terms / terms.sum(), rtol=1e-15)
+
+
+def test_router_topk_matches_stable_sort_and_library_softmax():
+    """Ids against a stable descending argsort (lower index first among
+    equal logits); weights against scipy's softmax of the selected logits."""
+    special = pytest.importorskip("scipy.special")
+    g = np.random.default_rng(21)
+    for E, k in ((8, 1), (16, 4), (64, 8), (256, 8), (20, 16), (7, 7)):
+        logits = g.standard_normal((5, E)).astype(np.float32)
+        logits[1, 3] = logits[1, 5] = logits[1].max() + 1  # a tie at the top
+        logits[2] = np.round(logits[2])  # many ties
+        ids, wts = O.router_topk(logits, k)
+        for t in range(5):
+            ref = np.argsort(-logits[t].astype(np.float64), kind="stable")[:k]
+            np.testing.assert_array_equal(ids[t], ref)
+            np.testing.assert_allclose(wts[t], special.softmax(logits[t][ref].astype(np.float64)), rtol=1e-13)
+
+
+def test_router_topk_invariants():
+    g = np.random.default_rng(22)
+    logits = np.round(g.standard_normal((5, 64)) * 64).astype(np.float32) / 64  # exact after +8
+    ids, wts = O.router_topk(logits, 8)
+    np.testing.assert_allclose(wts.sum(axis=1), 1.0, rtol=1e-15)
+    assert np.all(np.diff(wts, axis=1) <= 0)  # descending logits give descending weights
+    ids2, wts2 = O.router_topk(logits + np.float32(8.0), 8)  # a common shift changes nothing
+    np.testing.assert_array_equal(ids2, ids)
+    np.testing.assert_allclose(wts2, wts, rtol=1e-14)
+    distinct = (g.permutation(5 * 64).reshape(5, 64) / 64.0).astype(np.float32)
+    ids_d, wts_d = O.router_topk(distinct, 8)
+    perm = g.permutation(64)  # relabelled experts: the same choices under the new labels
+    ids3, wts3 = O.router_topk(distinct[:, perm], 8)
+    np.testing.assert_array_equal(perm[ids3], ids_d)
+    np.testing.assert_array_equal(wts3, wts_d)
