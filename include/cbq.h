@@ -169,6 +169,28 @@ int cbq_moe_info(const cbq_moe *L, int *E, int64_t *H, int64_t *F, int64_t *devi
 int cbq_moe_matvec(const cbq_moe *L, const float *h_dev, int n_tok, const int32_t *ids_dev,
                    const float *wts_dev, int topk, int swiglu, float *y_dev, void *stream);
 
+/* Largest expert count of the router entry points (its logits are staged in
+ * shared memory). */
+#define CBQ_ROUTER_MAX_E 16384
+
+/* Routed-expert selection from router logits: logits_dev n_tok x E fp32;
+ * for every token t, ids_dev[t][0..topk) = the indices of the topk largest
+ * logits in descending order (equal logits: lower index first) and
+ * wts_dev[t][j] = softmax over those topk logits, computed in fp64 and
+ * rounded to fp32.  The pages name a "configured routed-expert top-k"
+ * ("feat(ds4): add DSpark speculative decoding") without a formula; this is
+ * the plain reading.  Logits must be finite.  1 <= n_tok <= 65535,
+ * 1 <= E <= CBQ_ROUTER_MAX_E, 1 <= topk <= min(CBQ_MAX_TOPK, E).  One kernel
+ * launch on `stream`; the caller owns every buffer. */
+int cbq_router_topk(const float *logits_dev, int n_tok, int E, int topk, int32_t *ids_dev, float *wts_dev,
+                    void *stream);
+
+/* cbq_router_topk into the handle's staging buffers, then cbq_moe_matvec with
+ * those ids and weights: the routed layer from router logits with no host
+ * round trip (one launch more than cbq_moe_matvec).  Same limits as both. */
+int cbq_moe_matvec_logits(const cbq_moe *L, const float *h_dev, int n_tok, const float *logits_dev, int topk,
+                          int swiglu, float *y_dev, void *stream);
+
 /* Same with HOST buffers (h, ids, wts in; y out), then synchronizes `stream`. */
 int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok,
                         const int32_t *ids_host, const float *wts_host, int topk, int swiglu,

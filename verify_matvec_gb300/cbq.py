@@ -25,6 +25,7 @@ CBQ_MAX_TOKENS = 5
 CBQ_MAX_TOPK = 16
 CBQ_DEVERR_BAD_EXPERT_ID = 0x1
 CBQ_STATIC_SCRATCH_MAX_K = 16384
+CBQ_ROUTER_MAX_E = 16384
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -45,6 +46,8 @@ _SIGS = {
     "cbq_moe_info": ([_P, ctypes.POINTER(_I), ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)], _I),
     "cbq_moe_matvec": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
     "cbq_moe_matvec_host": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
+    "cbq_router_topk": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "cbq_moe_matvec_logits": ([_P, _P, _I, _P, _I, _I, _P, _P], _I),
     "cbq_get_device_error": ([ctypes.POINTER(ctypes.c_uint)], _I),
     "cbq_debug_block_dots": ([_P, _P, _I, _P, _P], _I),
     "cbq_moe_debug_block_dots": ([_P, _I, _I, _P, _I, _P, _P], _I),
@@ -285,6 +288,34 @@ def cbq_moe_matvec(L: Moe, h, ids, wts, swiglu: int = 1, y=None, stream=None):
     _check(load().cbq_moe_matvec(L.handle, _dev_ptr(h, torch.float32, "h"), n_tok, _dev_ptr(ids, torch.int32, "ids"),
                                  _dev_ptr(wts, torch.float32, "wts"), k, int(swiglu),
                                  _dev_ptr(y, torch.float32, "y"), _stream(stream)), "cbq_moe_matvec")
+    return y
+
+
+def cbq_router_topk(logits, k: int, ids=None, wts=None, stream=None):
+    """ids (n_tok, k) int32 and fp32 softmax weights of the k largest logits
+    of each row of logits (n_tok, E) fp32, on the device."""
+    torch = _torch()
+    n_tok, E = logits.shape
+    if ids is None:
+        ids = torch.empty((n_tok, k), dtype=torch.int32, device=logits.device)
+    if wts is None:
+        wts = torch.empty((n_tok, k), dtype=torch.float32, device=logits.device)
+    _check(load().cbq_router_topk(_dev_ptr(logits, torch.float32, "logits"), n_tok, E, k,
+                                  _dev_ptr(ids, torch.int32, "ids"), _dev_ptr(wts, torch.float32, "wts"),
+                                  _stream(stream)), "cbq_router_topk")
+    return ids, wts
+
+
+def cbq_moe_matvec_logits(L: Moe, h, logits, k: int, swiglu: int = 1, y=None, stream=None):
+    """The routed layer from router logits (n_tok, E): top-k selection and
+    softmax weights on the device, then cbq_moe_matvec."""
+    torch = _torch()
+    n_tok = logits.shape[0]
+    if y is None:
+        y = torch.empty((n_tok, L.H), dtype=torch.float32, device=h.device)
+    _check(load().cbq_moe_matvec_logits(L.handle, _dev_ptr(h, torch.float32, "h"), n_tok,
+                                        _dev_ptr(logits, torch.float32, "logits"), k, int(swiglu),
+                                        _dev_ptr(y, torch.float32, "y"), _stream(stream)), "cbq_moe_matvec_logits")
     return y
 
 

@@ -448,6 +448,31 @@ int cbq_moe_matvec(const cbq_moe *L, const float *h_dev, int n_tok, const int32_
     return CBQ_OK;
 }
 
+int cbq_router_topk(const float *logits_dev, int n_tok, int E, int topk, int32_t *ids_dev, float *wts_dev,
+                    void *stream) {
+    if (!logits_dev || !ids_dev || !wts_dev || n_tok < 1 || n_tok > 65535 || E < 1 || E > CBQ_ROUTER_MAX_E ||
+        topk < 1 || topk > CBQ_MAX_TOPK || topk > E)
+        return CBQ_EINVAL;
+    int dev = 0;
+    const int rc = check_device(&dev);
+    if (rc != CBQ_OK) return rc;
+    CBQ_CUDA(cbq::launch_router_topk(logits_dev, n_tok, E, topk, ids_dev, wts_dev, as_stream(stream)));
+    return CBQ_OK;
+}
+
+int cbq_moe_matvec_logits(const cbq_moe *L, const float *h_dev, int n_tok, const float *logits_dev, int topk,
+                          int swiglu, float *y_dev, void *stream) {
+    if (!L || !h_dev || !logits_dev || !y_dev || n_tok < 1 || n_tok > CBQ_MAX_TOKENS || topk < 1 ||
+        topk > CBQ_MAX_TOPK || topk > L->L.E || L->L.E > CBQ_ROUTER_MAX_E || (swiglu != 0 && swiglu != 1))
+        return CBQ_EINVAL;
+    DeviceScope scope(L->device);
+    CBQ_CUDA(scope.status());
+    cudaStream_t s = as_stream(stream);
+    CBQ_CUDA(cbq::launch_router_topk(logits_dev, n_tok, L->L.E, topk, L->st_ids, L->st_wts, s));
+    CBQ_CUDA(cbq::launch_moe(L->L, L->ws, h_dev, n_tok, L->st_ids, L->st_wts, topk, swiglu, y_dev, s));
+    return CBQ_OK;
+}
+
 int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok, const int32_t *ids_host,
                         const float *wts_host, int topk, int swiglu, float *y_host, void *stream) {
     if (!L || !h_host || !ids_host || !wts_host || !y_host || n_tok < 1 || n_tok > CBQ_MAX_TOKENS || topk < 1 ||

@@ -66,6 +66,9 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
 size_t matvec_smem_bytes(int nbp, int n);
 size_t moe_smem_bytes(int act_blocks);
 cudaError_t device_smem_limit(size_t *bytes);
+// Top-k expert ids and softmax weights per token from router logits (n_tok x E).
+cudaError_t launch_router_topk(const float *logits, int n_tok, int E, int k, int32_t *ids, float *wts,
+                               cudaStream_t s);
 // Dynamic shared memory the layer kernel may use (opt-in limit less its static part).
 cudaError_t moe_smem_limit(size_t *bytes);
 cudaError_t read_and_clear_device_error(unsigned *code);

@@ -746,6 +746,79 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     return e;
 }
 
+// ------------------------------------------------------ router top-k ------
+
+// Routed-expert selection, one warp per token: the logits are staged in
+// shared memory; k rounds each take the largest logit not yet taken (equal
+// logits: the lower index), by a warp reduction over (value, index).  The
+// weights are the softmax of the k selected logits, in fp64 (the differences
+// of fp32 logits are exact there) and rounded once to fp32.
+__global__ void __launch_bounds__(32) k_router_topk(const float *__restrict__ logits, int E, int k,
+                                                    int32_t *__restrict__ ids, float *__restrict__ wts) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    float *l = reinterpret_cast<float *>(smem);
+    unsigned char *taken = smem + (size_t)E * sizeof(float);
+    const int t = blockIdx.x, lane = threadIdx.x;
+    const float *lt = logits + (size_t)t * E;
+    for (int e = lane; e < E; e += 32) {
+        l[e] = lt[e];
+        taken[e] = 0;
+    }
+    __syncwarp();
+    float sel[kMaxTopk];
+    int pick[kMaxTopk];
+#pragma unroll
+    for (int j = 0; j < kMaxTopk; ++j) {
+        sel[j] = 0.0f;
+        pick[j] = 0;
+        if (j >= k) continue;
+        float bv = 0.0f;
+        int bi = -1;
+        for (int e = lane; e < E; e += 32)
+            if (!taken[e] && (bi < 0 || l[e] > bv)) {  // ascending e: the first of equal values stays
+                bv = l[e];
+                bi = e;
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        sel[j] = bv;
+        pick[j] = bi;
+        if (lane == 0) taken[bi] = 1;
+        __syncwarp();
+    }
+    if (lane == 0) {
+        double w[kMaxTopk], sum = 0.0;
+#pragma unroll
+        for (int j = 0; j < kMaxTopk; ++j) {
+            w[j] = j < k ? exp((double)sel[j] - (double)sel[0]) : 0.0;
+            sum += w[j];
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxTopk; ++j)
+            if (j < k) {
+                ids[(size_t)t * k + j] = pick[j];
+                wts[(size_t)t * k + j] = (float)(w[j] / sum);
+            }
+    }
+}
+
+cudaError_t launch_router_topk(const float *logits, int n_tok, int E, int k, int32_t *ids, float *wts,
+                               cudaStream_t s) {
+    const size_t smem = (size_t)E * (sizeof(float) + 1);
+    int sms = 0, per_sm = 0;
+    cudaError_t e = resident(k_router_topk, 32, smem, &sms, &per_sm);
+    if (e != cudaSuccess) return e;
+    k_router_topk<<<n_tok, 32, smem, s>>>(logits, E, k, ids, wts);
+    return cudaGetLastError();
+}
+
 cudaError_t moe_smem_limit(size_t *bytes) {
     size_t optin = 0;
     cudaFuncAttributes fa;
