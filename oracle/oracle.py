@@ -10,6 +10,7 @@ package build compiles ahead of time).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -45,37 +46,58 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def _bind(lib):
+    """Declare the argument and result types of the oracle's C functions."""
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    I = ctypes.c_int
+    lib.oracle_half_to_float.argtypes = [ctypes.c_uint16]
+    lib.oracle_half_to_float.restype = ctypes.c_float
+    lib.oracle_block_index.argtypes = [P, I]
+    lib.oracle_block_index.restype = I
+    lib.oracle_dequantize_block.argtypes = [P, P]
+    lib.oracle_quantize_act.argtypes = [P, I64, I, P, P]
+    lib.oracle_block_dots.argtypes = [P, I64, I64, P, I, P]
+    lib.oracle_matvec_q.argtypes = [P, I64, I64, P, P, I, P]
+    lib.oracle_matvec_q_rows.argtypes = [P, I64, I64, P, P, I, P, I64, P]
+    lib.oracle_matvec.argtypes = [P, I64, I64, P, I, P]
+    lib.oracle_matvec_bound.argtypes = [P, I64, I64, P, P, I, P]
+    lib.oracle_matvec_bound_rows.argtypes = [P, I64, I64, P, P, I, P, I64, P]
+    lib.oracle_silu.argtypes = [ctypes.c_double]
+    lib.oracle_silu.restype = ctypes.c_double
+    lib.oracle_moe.argtypes = [P, P, I, I64, I64, P, I, P, P, I, I, P, P, P, P]
+    lib.oracle_moe.restype = I
+    lib.oracle_moe_down_combine.argtypes = [P, I, I64, I64, I, P, P, I, P, P, P, P]
+    lib.oracle_moe_down_combine.restype = I
+    lib.oracle_router_topk.argtypes = [P, I, I, I, P, P]
+    lib.oracle_router_topk.restype = None
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
-        P = ctypes.c_void_p
-        I64 = ctypes.c_int64
-        I = ctypes.c_int
-        lib.oracle_half_to_float.argtypes = [ctypes.c_uint16]
-        lib.oracle_half_to_float.restype = ctypes.c_float
-        lib.oracle_block_index.argtypes = [P, I]
-        lib.oracle_block_index.restype = I
-        lib.oracle_dequantize_block.argtypes = [P, P]
-        lib.oracle_quantize_act.argtypes = [P, I64, I, P, P]
-        lib.oracle_block_dots.argtypes = [P, I64, I64, P, I, P]
-        lib.oracle_matvec_q.argtypes = [P, I64, I64, P, P, I, P]
-        lib.oracle_matvec_q_rows.argtypes = [P, I64, I64, P, P, I, P, I64, P]
-        lib.oracle_matvec.argtypes = [P, I64, I64, P, I, P]
-        lib.oracle_matvec_bound.argtypes = [P, I64, I64, P, P, I, P]
-        lib.oracle_matvec_bound_rows.argtypes = [P, I64, I64, P, P, I, P, I64, P]
-        lib.oracle_silu.argtypes = [ctypes.c_double]
-        lib.oracle_silu.restype = ctypes.c_double
-        lib.oracle_moe.argtypes = [P, P, I, I64, I64, P, I, P, P, I, I, P, P, P, P]
-        lib.oracle_moe.restype = I
-        lib.oracle_moe_down_combine.argtypes = [P, I, I64, I64, I, P, P, I, P, P, P, P]
-        lib.oracle_moe_down_combine.restype = I
-        lib.oracle_router_topk.argtypes = [P, I, I, I, P, P]
-        lib.oracle_router_topk.restype = None
-        _lib = lib
-        return lib
+        _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+@contextlib.contextmanager
+def using_library(path):
+    """Run the wrappers of this module against another build of the oracle's
+    C source (the mutation tests plant one mistake per build) for the
+    duration of the block."""
+    global _lib
+    other = _bind(ctypes.CDLL(path))
+    with _lock:
+        saved = _lib
+        _lib = other
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = saved
 
 
 def _p(a: np.ndarray):
