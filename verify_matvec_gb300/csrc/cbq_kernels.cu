@@ -98,6 +98,11 @@ cudaError_t launch_repack(const uint8_t *src, int64_t M, int nb, uint4 *qs, uint
 
 __global__ void k_quantize(const float *__restrict__ x, int64_t total, int8_t *__restrict__ qx,
                            float *__restrict__ dx) {
+    // launched as a programmatic dependent of whatever ran before on the
+    // stream: wait for it (x may be its output), then let this call's
+    // next kernel launch -- it may read the routing table or a handle's
+    // counters before its own wait, so it must not start any earlier
+    pdl_wait();
     pdl_trigger();
     // total = n*K, a multiple of 32; one lane per value, one warp per block.
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx - (threadIdx.x & 31) < total;
@@ -114,8 +119,7 @@ cudaError_t launch_quantize(const float *x, int64_t K, int n, int8_t *qx, float 
     const int64_t total = (int64_t)n * K;
     if (total == 0) return cudaSuccess;
     const int grid = (int)std::min<int64_t>((total + 255) / 256, 4096);
-    k_quantize<<<grid, 256, 0, s>>>(x, total, qx, dx);
-    return cudaGetLastError();
+    return launch_k(k_quantize, grid, 256, 0, s, true, x, total, qx, dx);
 }
 
 // ---------------------------------------------------------- dense MMVQ -----
@@ -136,6 +140,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
              const int8_t *__restrict__ qx, const float *__restrict__ dx, const float *__restrict__ xf, int64_t K,
              float *__restrict__ y, unsigned *__restrict__ sched) {
     extern __shared__ __align__(128) unsigned char smem[];
+    if constexpr (kF32) pdl_wait();  // first kernel of its call: the previous work, x included, is done
+    pdl_trigger();  // the next call's first kernel may launch; it waits for this grid
     const PipeSmem S = carve_pipe(smem, kStages, NC, nbp);
     pipe_init(S.pipe);
     __syncthreads();
@@ -337,7 +343,7 @@ cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, in
 
 cudaError_t launch_matvec_f32(const DevMat &W, const float *x, int n, float *y, cudaStream_t s) {
     if (n != 1) return cudaErrorInvalidValue;
-    return launch_matvec_n<1, true>(W, nullptr, nullptr, x, y, s, false);
+    return launch_matvec_n<1, true>(W, nullptr, nullptr, x, y, s, true);
 }
 
 template <int NC>
@@ -679,6 +685,7 @@ __global__ void __launch_bounds__(256) k_moe_combine(const __grid_constant__ Moe
         w_s[threadIdx.x] = A.wts[threadIdx.x];
     }
     __syncthreads();
+    pdl_trigger();  // the next call's first kernel may launch; it waits for this grid
     pdl_wait();
     const int total = A.n_tok * A.L.H;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
