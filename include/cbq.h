@@ -51,6 +51,13 @@
  *   - the workspace of a handle is shared by its calls: two calls on one
  *     handle that overlap on the GPU (different streams without ordering)
  *     race.  Calls on one stream are ordered and safe;
+ *   - kernels are launched as programmatic dependents (programmatic stream
+ *     serialization) where that hides launch latency: such a kernel may
+ *     become resident before the work ahead of it on the stream has ended,
+ *     but it waits for that work (griddepcontrol.wait) before it reads any
+ *     input of the call or any counter of a handle, so results are those of
+ *     plain stream order, also after a caller's kernel that signals its
+ *     dependents early;
  *   - no call allocates or frees memory except *_create / *_destroy.
  */
 #ifndef CBQ_H
