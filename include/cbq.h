@@ -54,10 +54,11 @@
  *   - kernels are launched as programmatic dependents (programmatic stream
  *     serialization) where that hides launch latency: such a kernel may
  *     become resident before the work ahead of it on the stream has ended,
- *     but it waits for that work (griddepcontrol.wait) before it reads any
- *     input of the call or any counter of a handle, so results are those of
- *     plain stream order, also after a caller's kernel that signals its
- *     dependents early;
+ *     but it reads an input of the call or a counter of a handle only once
+ *     all work enqueued before the call has ended (the call's first kernel
+ *     waits for it with griddepcontrol.wait before it lets the call's next
+ *     kernel start), so results are those of plain stream order, also after
+ *     a caller's kernel that signals its dependents early;
  *   - no call allocates or frees memory except *_create / *_destroy.
  */
 #ifndef CBQ_H
