@@ -3,11 +3,13 @@
 //
 //   k_repack          canonical 18-byte blocks -> device layout (handle creation)
 //   k_quantize        activation quantization, one warp per 32-value block
-//   k_matvec<NC>      dense MMVQ over NC <= 5 columns, one pass over the weights
+//   k_matvec<NC,F32>  dense MMVQ over NC <= 5 columns, one pass over the weights
+//                     (F32: one fp32 column, quantized inside the kernel)
 //   k_block_dots<NC>  the same integer path, exporting every per-block dot
 //   k_moe             routed experts, one kernel per layer call: gate+up rows,
 //                     SwiGLU split, requantization, then down rows per slot
 //   k_moe_combine     router-weighted combine of the per-slot down outputs
+//   k_router_topk     top-k expert ids and softmax weights from router logits
 //
 // The matvec-type kernels are persistent: a grid of at most (SMs x resident
 // CTAs) CTAs whose producer warps take 32-row work items from a global
@@ -541,6 +543,10 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Slots &sl, con
 // on anything, so a down item's wait for its expert's intermediate
 // (done[u] == Gf * ns) always ends; it is bounded all the same.
 // The producer streams a down item's weights before that wait ends.
+// The routing table and the handle's counters are read before any wait: the
+// kernel is launched in plain stream order (one token, quantized here) or as
+// the dependent of the quantization kernel, which lets it start only once all
+// earlier work has ended.
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__ MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
