@@ -93,3 +93,26 @@ def test_layer_from_logits(torch, layer, n_tok, k):
     ids_np, wts_np = ids.cpu().numpy(), wts.cpu().numpy()
     np.testing.assert_array_equal(ids_np, O.router_topk(lg, k)[0])
     _check_layer(torch, L, gu, dn, E_W, H_W, F_W, h, ids_np, wts_np, 1)
+
+
+def test_full_layer_from_logits_batch5_top8(torch):
+    """The 256-expert layer (4096 x 2048) from router logits of 5 tokens: the
+    GPU picks the oracle's experts and the layer matches the oracle's."""
+    from tests.test_gpu_moe import E, F, H
+    g = np.random.default_rng(730)
+    lg = g.standard_normal((5, E)).astype(np.float32)
+    ids_r, _ = O.router_topk(lg, 8)
+    used = synth.distinct_experts(ids_r, E)
+    gu = np.zeros((E, 2 * F, H // 32, 18), dtype=np.uint8)
+    dn = np.zeros((E, H, F // 32, 18), dtype=np.uint8)
+    for e in used:
+        gu[e] = synth.weight_blocks(2 * F, H, stream=synth.S_GATE_UP * 1000 + int(e))
+        dn[e] = synth.weight_blocks(H, F, stream=synth.S_DOWN * 1000 + int(e))
+    L = cbq.Moe(gu, dn, E, H, F)
+    h = synth.activations(5, H, stream=731)
+    y = cbq.cbq_moe_matvec_logits(L, _dev(torch, h), _dev(torch, lg), 8).cpu().numpy()
+    ids, wts = cbq.cbq_router_topk(_dev(torch, lg), 8)
+    ids_np, wts_np = ids.cpu().numpy(), wts.cpu().numpy()
+    np.testing.assert_array_equal(ids_np, ids_r)
+    y2 = _check_layer(torch, L, gu, dn, E, H, F, h, ids_np, wts_np, 1)
+    np.testing.assert_array_equal(y, y2)
