@@ -186,3 +186,36 @@ def test_k_beyond_staging_limit_refused(torch):
     with pytest.raises(cbq.CbqError) as info:
         cbq.Weights(synth.weight_blocks(M, K, stream=452), M, K)
     assert info.value.status == cbq.CBQ_EINVAL
+
+
+@pytest.mark.parametrize("n", [1, 2, 5])
+def test_back_to_back_calls_on_one_handle(torch, n):
+    """Many calls on one handle, enqueued without a synchronization between
+    them (each call's first kernel may become resident while the previous call
+    still runs), give the bits of calls made one at a time; so do the
+    pre-quantized entry and the static-scratch entry."""
+    M, K = 1000, 2048
+    Wh = cbq.Weights(synth.weight_blocks(M, K, stream=460), M, K)
+    xs = [_dev(torch, synth.activations(n, K, stream=461 + i)) for i in range(4)]
+    ref = []
+    for x in xs:
+        ref.append(cbq.cbq_matvec(Wh, x).cpu().numpy())
+        torch.cuda.synchronize()
+    ys = [torch.empty((n, M), dtype=torch.float32, device="cuda") for _ in range(40)]
+    for i, y in enumerate(ys):
+        cbq.cbq_matvec(Wh, xs[i % 4], y=y)
+    torch.cuda.synchronize()
+    for i, y in enumerate(ys):
+        np.testing.assert_array_equal(y.cpu().numpy(), ref[i % 4])
+    qd = [cbq.cbq_quantize_act(x) for x in xs]
+    for i, y in enumerate(ys):  # the three entry points interleaved, still unsynchronized
+        if i % 3 == 0:
+            cbq.cbq_matvec_q(Wh, qd[i % 4][0], qd[i % 4][1], y=y)
+        elif i % 3 == 1:
+            cbq.cbq_matvec_static(Wh, xs[i % 4], y=y)
+        else:
+            cbq.cbq_matvec(Wh, xs[i % 4], y=y)
+    torch.cuda.synchronize()
+    for i, y in enumerate(ys):
+        np.testing.assert_array_equal(y.cpu().numpy(), ref[i % 4])
+    assert cbq.cbq_get_device_error() == 0

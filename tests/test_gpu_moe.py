@@ -257,3 +257,33 @@ def test_one_token_quantized_in_kernel_matches_kernel_path(torch, small):
     assert hm.data_ptr() % 16 == 4
     ym = cbq.cbq_moe_matvec(L, hm, _dev(torch, ids), _dev(torch, wts)).cpu().numpy()
     np.testing.assert_array_equal(ym, y)
+
+
+@pytest.mark.parametrize("n_tok,k", [(1, 4), (5, 8)])
+def test_back_to_back_layer_calls(torch, small, n_tok, k):
+    """Layer calls on one handle enqueued without a synchronization between
+    them, alternating routing tables and the ids and logits entries, give the
+    bits of calls made one at a time."""
+    gu, dn, L = small
+    tabs = []
+    for i in range(3):
+        h = _dev(torch, synth.activations(n_tok, H_S, stream=660 + i))
+        ids, wts = synth.router(n_tok, k, E_S, stream=663 + i)
+        tabs.append((h, _dev(torch, ids), _dev(torch, wts)))
+    ref = []
+    for h, ids, wts in tabs:
+        ref.append(cbq.cbq_moe_matvec(L, h, ids, wts).cpu().numpy())
+        torch.cuda.synchronize()
+    lg = _dev(torch, np.random.default_rng(666).standard_normal((n_tok, E_S)).astype(np.float32))
+    y_lg = cbq.cbq_moe_matvec_logits(L, tabs[0][0], lg, k).cpu().numpy()
+    ys = [torch.empty((n_tok, H_S), dtype=torch.float32, device="cuda") for _ in range(30)]
+    for i, y in enumerate(ys):
+        if i % 4 == 3:
+            cbq.cbq_moe_matvec_logits(L, tabs[0][0], lg, k, y=y)
+        else:
+            h, ids, wts = tabs[i % 3]
+            cbq.cbq_moe_matvec(L, h, ids, wts, y=y)
+    torch.cuda.synchronize()
+    for i, y in enumerate(ys):
+        np.testing.assert_array_equal(y.cpu().numpy(), y_lg if i % 4 == 3 else ref[i % 3])
+    assert cbq.cbq_get_device_error() == 0
