@@ -448,7 +448,7 @@ def run_gpu(args):
     # the replay of 16 captured calls (one per routing table) divided by 16;
     # the host-driven loop (one Python call per layer) is reported beside it,
     # with the split into the token quantization and the rest of the call.
-    def graph_us(fn, n_calls=N_SETS, replays=25):
+    def graph_us(fn, n_calls=N_SETS, replays=25, samples=False):
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
@@ -463,14 +463,15 @@ def run_gpu(args):
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(replays):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
+        ev[0].record()
+        for r in range(replays):
             g.replay()
-        b.record()
+            ev[r + 1].record()
         torch.cuda.synchronize()
-        return 1e3 * a.elapsed_time(b) / (replays * n_calls)
+        per_call = [1e3 * ev[r].elapsed_time(ev[r + 1]) / n_calls for r in range(replays)]
+        return (1e3 * ev[0].elapsed_time(ev[-1]) / (replays * n_calls), per_call) if samples else \
+            1e3 * ev[0].elapsed_time(ev[-1]) / (replays * n_calls)
 
     def layer_us(n_tok, k, reps=50):
         tabs = []
@@ -497,16 +498,22 @@ def run_gpu(args):
         cbq.cbq_moe_set_stage_events(L, None)
         eager = 1e3 * a.elapsed_time(b) / reps
         split = [1e3 * sum(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev) / reps for j in range(2)]
-        trials = [graph_us(lambda i: cbq.cbq_moe_matvec(L, tabs[i][2], tabs[i][0], tabs[i][1], y=yl))
-                  for _ in range(5)]
+        trials, per_replay = [], []
+        for _ in range(5):
+            mean, each = graph_us(lambda i: cbq.cbq_moe_matvec(L, tabs[i][2], tabs[i][0], tabs[i][1], y=yl),
+                                  samples=True)
+            trials.append(mean)
+            per_replay += each
         us = statistics.median(trials)
         half = 2.776 * statistics.stdev(trials) / 5 ** 0.5  # 95% CI of the mean, 4 degrees of freedom
         ci = [statistics.mean(trials) - half, statistics.mean(trials) + half]
+        q = statistics.quantiles(per_replay, n=10)  # per replay of the 16 calls, 5 x 25 replays
+        spread = {"p10": q[0], "p50": statistics.median(per_replay), "p90": q[-1]}
         nbytes = sum(t[3] for t in tabs) / N_SETS * EXPERT_BYTES
-        return us, nbytes / (us * 1e-6) / 1e9, eager, split, ci
+        return us, nbytes / (us * 1e-6) / 1e9, eager, split, ci, spread
 
-    b1_us, b1_gbs, b1_eager, b1_split, b1_ci = layer_us(1, 4)
-    b5_us, b5_gbs, b5_eager, b5_split, b5_ci = layer_us(5, 8)
+    b1_us, b1_gbs, b1_eager, b1_split, b1_ci, b1_q = layer_us(1, 4)
+    b5_us, b5_gbs, b5_eager, b5_split, b5_ci, b5_q = layer_us(5, 8)
 
     # dense decode projections (4096x4096, 16384x4096) through cbq_matvec, by
     # graph replay over copies whose bytes together exceed L2
@@ -555,6 +562,7 @@ def run_gpu(args):
                              "batch1_weight_gbs": b1_gbs, "batch5_weight_gbs": b5_gbs,
                              "timing": "CUDA-graph replay of 16 captured calls x 25; median of 5 trials",
                              "ci95_us": {"batch1": b1_ci, "batch5": b5_ci},
+                             "per_replay_us": {"batch1": b1_q, "batch5": b5_q},
                              "batch1_frac_of_peak": b1_gbs / peak, "batch5_frac_of_peak": b5_gbs / peak,
                              "eager_host_loop": {"batch1": b1_eager, "batch5": b5_eager},
                              "eager_split_us_layer_combine": {"batch1": b1_split, "batch5": b5_split}},

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from oracle import oracle as O
-from tests.gpu_util import assert_within_bound, cuda
+from tests.gpu_util import Guarded, assert_within_bound, cuda
 from verify_matvec_gb300 import cbq, synth
 
 pytestmark = pytest.mark.gpu
@@ -32,7 +32,10 @@ def test_quantize_bit_exact(torch, n, K, outliers):
     x = synth.activations(n, K, stream=101 + K + n, outliers=outliers)
     x[0, :32] = 0.0                         # an all-zero block
     x[-1, 32 * (K // 64):32 * (K // 64) + 32] = 3.0  # a constant block
-    qx, dx = cbq.cbq_quantize_act(_dev(torch, x))
+    gq, gd = Guarded(torch, (n, K), torch.int8), Guarded(torch, (n, K // 32), torch.float32)
+    qx, dx = cbq.cbq_quantize_act(_dev(torch, x), qx=gq.view, dx=gd.view)
+    gq.check()
+    gd.check()
     qr, dr = O.quantize_act(x)
     np.testing.assert_array_equal(qx.cpu().numpy(), qr)
     np.testing.assert_array_equal(dx.cpu().numpy().view(np.uint32), dr.view(np.uint32))
@@ -77,7 +80,9 @@ def test_block_dots_every_codebook_entry(torch):
 
 def _check_matvec(torch, W, M, K, x, rows=None):
     Wh = cbq.Weights(W, M, K)
-    y = cbq.cbq_matvec(Wh, _dev(torch, x)).cpu().numpy()
+    g = Guarded(torch, (x.shape[0], M), torch.float32)
+    y = cbq.cbq_matvec(Wh, _dev(torch, x), y=g.view).cpu().numpy()
+    g.check()
     qx, dx = O.quantize_act(x)
     yr = O.matvec_q(W, M, K, qx, dx, rows=rows)
     b = O.matvec_bound(W, M, K, qx, dx, rows=rows)

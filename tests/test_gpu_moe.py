@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 from oracle import oracle as O
-from tests.gpu_util import TOL, assert_within_bound, cuda
+from tests.gpu_util import TOL, Guarded, assert_within_bound, cuda
 from tests.test_oracle import _np_dequant
 from verify_matvec_gb300 import cbq, synth
 
@@ -32,7 +32,10 @@ def _dev(torch, a):
 def _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, swiglu, expect_bad=0):
     n_tok, k = ids.shape
     cbq.cbq_moe_set_debug(L, True)
-    y = cbq.cbq_moe_matvec(L, _dev(torch, h), _dev(torch, ids), _dev(torch, wts), swiglu=swiglu).cpu().numpy()
+    g = Guarded(torch, (n_tok, H), torch.float32)
+    y = cbq.cbq_moe_matvec(L, _dev(torch, h), _dev(torch, ids), _dev(torch, wts), swiglu=swiglu,
+                           y=g.view).cpu().numpy()
+    g.check()
     a_g, qa_g, da_g = (t.cpu().numpy() for t in cbq.cbq_moe_debug_intermediate(L, n_tok * k))
     err = cbq.cbq_get_device_error()
     assert err == (cbq.CBQ_DEVERR_BAD_EXPERT_ID if expect_bad else 0)

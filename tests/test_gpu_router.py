@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from oracle import oracle as O
-from tests.gpu_util import cuda
+from tests.gpu_util import Guarded, cuda
 from tests.test_gpu_moe import _check_layer
 from verify_matvec_gb300 import cbq, synth
 
@@ -34,7 +34,10 @@ def _logits(n_tok, E, seed, ties=False):
 
 
 def _check_router(torch, lg, k):
-    ids, wts = cbq.cbq_router_topk(_dev(torch, lg), k)
+    gi, gw = Guarded(torch, (lg.shape[0], k), torch.int32), Guarded(torch, (lg.shape[0], k), torch.float32)
+    ids, wts = cbq.cbq_router_topk(_dev(torch, lg), k, ids=gi.view, wts=gw.view)
+    gi.check()
+    gw.check()
     ids, wts = ids.cpu().numpy(), wts.cpu().numpy()
     ids_r, wts_r = O.router_topk(lg, k)
     np.testing.assert_array_equal(ids, ids_r)
