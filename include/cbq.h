@@ -205,11 +205,13 @@ int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok,
                         float *y_host, void *stream);
 
 /* Stage timing: when set, cbq_moe_matvec records these CUDA events
- * (cudaEvent_t passed as void*) on its stream before the token quantization,
- * before the combine kernel (so the first interval spans the quantization and
- * the layer kernel: gate_up + SwiGLU + requantization, down) and after it.  Recording them separates the two kernels (the overlap
- * of the combine's start with the layer kernel's end is lost).  Pass NULL for
- * all three to stop.  The events stay owned by the caller. */
+ * (cudaEvent_t passed as void*) on its stream before its first kernel (the
+ * token quantization, or the layer kernel for one aligned token), before the
+ * combine kernel (so the first interval spans the quantization and the layer
+ * kernel: gate_up + SwiGLU + requantization, down) and after it.  Recording
+ * them separates the kernels (the overlap of the combine's start with the
+ * layer kernel's end is lost).  Pass NULL for all three to stop; a mix of NULL
+ * and non-NULL is CBQ_EINVAL.  The events stay owned by the caller. */
 int cbq_moe_set_stage_events(cbq_moe *L, void *ev_layer, void *ev_combine, void *ev_end);
 
 /* ---- allocation-free dense path --------------------------------------- */
