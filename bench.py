@@ -90,9 +90,10 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--profile", action="store_true",
                     help="time the main loop only (no e2e, per-layer or oracle legs); for profiler runs")
-    ap.add_argument("--case", default="step", choices=["step", "b1", "b5"],
-                    help="profile mode only: the whole step, or the MoE layer alone at batch 1 (top-4) "
-                         "or batch 5 (top-8)")
+    ap.add_argument("--case", default="step", choices=["step", "b1", "b5", "dense1"],
+                    help="profile mode only: the whole step, the MoE layer alone at batch 1 (top-4) "
+                         "or batch 5 (top-8), or the 4096x4096 dense projection at n=1 (cbq_matvec over "
+                         "16 weight copies, more than L2)")
     ap.add_argument("--experts", type=int, default=E,
                     help="experts in the layer (default 256); smaller layers keep profiler captures small")
     return ap.parse_args()
@@ -308,6 +309,23 @@ def run_gpu(args):
     cbq.load()
 
     n_exp = args.experts
+    if args.profile and args.case == "dense1":
+        Ws = [cbq.Weights(synth.weight_blocks(4096, 4096, stream=synth.S_W * 1000 + 17 * i + 1), 4096, 4096)
+              for i in range(16)]
+        xx = torch.from_numpy(synth.activations(1, 4096, stream=synth.S_X)).to(dev)
+        yy = torch.empty((1, 4096), dtype=torch.float32, device=dev)
+        for i in range(args.warmup):
+            cbq.cbq_matvec(Ws[i % 16], xx, y=yy)
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for i in range(args.steps):
+            cbq.cbq_matvec(Ws[i % 16], xx, y=yy)
+        a1.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": True, "case": args.case, "us_per_call": 1e3 * a0.elapsed_time(a1) / args.steps,
+                          "device_error": cbq.cbq_get_device_error()}), flush=True)
+        return
     if args.profile and args.case != "step":
         L = build_layer(torch, cbq, n_exp, with_head=False)
         n_tok, k = (1, 4) if args.case == "b1" else (N_TOK, TOPK)
