@@ -247,6 +247,26 @@ int oracle_moe(const uint8_t *gate_up, const uint8_t *down, int E, int64_t H, in
     return bad;
 }
 
+int oracle_moe_shared(const uint8_t *gate_up, const uint8_t *down, int E, int64_t H, int64_t F,
+                      const uint8_t *sh_gate_up, const uint8_t *sh_down,
+                      const float *h, int n_tok, const int32_t *ids, const float *wts, int k,
+                      int swiglu, double *y)
+{
+    const int bad = oracle_moe(gate_up, down, E, H, F, h, n_tok, ids, wts, k, swiglu, y, NULL, NULL, NULL);
+    /* the shared expert as a one-expert table: every token routed to its
+     * expert 0 with weight 1 */
+    double *ys = (double *)malloc((size_t)n_tok * (size_t)H * sizeof(double));
+    int32_t *sh_ids = (int32_t *)calloc((size_t)n_tok, sizeof(int32_t));
+    float *sh_wts = (float *)malloc((size_t)n_tok * sizeof(float));
+    for (int t = 0; t < n_tok; ++t) sh_wts[t] = 1.0f;
+    oracle_moe(sh_gate_up, sh_down, 1, H, F, h, n_tok, sh_ids, sh_wts, 1, swiglu, ys, NULL, NULL, NULL);
+    for (int64_t i = 0; i < (int64_t)n_tok * H; ++i) y[i] += ys[i];
+    free(ys);
+    free(sh_ids);
+    free(sh_wts);
+    return bad;
+}
+
 int oracle_moe_down_combine(const uint8_t *down, int E, int64_t H, int64_t F,
                             int n_tok, const int32_t *ids, const float *wts, int k,
                             const int8_t *qa, const float *da,

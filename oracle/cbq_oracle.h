@@ -121,6 +121,20 @@ int oracle_moe(const uint8_t *gate_up, const uint8_t *down, int E, int64_t H, in
                const float *h, int n_tok, const int32_t *ids, const float *wts, int k,
                int swiglu, double *y, float *a_out, int8_t *qa_out, float *da_out);
 
+/* Routed layer plus one shared expert that every token passes through with
+ * router weight 1 (the DS4 FFN block's always-on expert; the pages name the
+ * routed layer only, so the shared expert is read as one more expert of the
+ * same shape, applied to every token after its routed slots):
+ *   y_t = sum_j wts[t][j] * o_{ids[t][j]}(h_t)  +  o_sh(h_t)
+ * where o_sh is the per-slot computation of oracle_moe with the weights
+ * sh_gate_up (2F x H) and sh_down (H x F).  The routed sum is formed first
+ * and the shared output added to it (fp64).  Returns the number of routed
+ * slots whose id is outside [0,E). */
+int oracle_moe_shared(const uint8_t *gate_up, const uint8_t *down, int E, int64_t H, int64_t F,
+                      const uint8_t *sh_gate_up, const uint8_t *sh_down,
+                      const float *h, int n_tok, const int32_t *ids, const float *wts, int k,
+                      int swiglu, double *y);
+
 /* The down projection + combine alone, from given per-slot quantized
  * intermediates qa[p][F], da[p][F/32] (p = t*k + j).  Also returns the
  * tolerance base ybound[t][H] = sum_j |wts| * sum_i |wd_i * ahat_i|. */

@@ -67,6 +67,8 @@ def _bind(lib):
     lib.oracle_silu.restype = ctypes.c_double
     lib.oracle_moe.argtypes = [P, P, I, I64, I64, P, I, P, P, I, I, P, P, P, P]
     lib.oracle_moe.restype = I
+    lib.oracle_moe_shared.argtypes = [P, P, I, I64, I64, P, P, P, I, P, P, I, I, P]
+    lib.oracle_moe_shared.restype = I
     lib.oracle_moe_down_combine.argtypes = [P, I, I64, I64, I, P, P, I, P, P, P, P]
     lib.oracle_moe_down_combine.restype = I
     lib.oracle_router_topk.argtypes = [P, I, I, I, P, P]
@@ -212,6 +214,26 @@ def moe(gate_up, down, E, H, F, h, ids, wts, swiglu=1, want_intermediate=False):
     if want_intermediate:
         return y, a, qa, da, nbad
     return y
+
+
+def moe_shared(gate_up, down, E, H, F, sh_gate_up, sh_down, h, ids, wts, swiglu=1):
+    """Routed layer plus the shared expert (weight 1 for every token).
+    Returns y (n_tok, H) fp64 and the number of out-of-range routed ids."""
+    h = np.ascontiguousarray(h, dtype=np.float32).reshape(-1, H)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    n_tok, k = ids.shape
+    wts = np.ascontiguousarray(wts, dtype=np.float32).reshape(n_tok, k)
+    gate_up = np.ascontiguousarray(gate_up, dtype=np.uint8)
+    down = np.ascontiguousarray(down, dtype=np.uint8)
+    sh_gate_up = np.ascontiguousarray(sh_gate_up, dtype=np.uint8)
+    sh_down = np.ascontiguousarray(sh_down, dtype=np.uint8)
+    gu1, dn1 = 2 * F * (H // QK) * BLOCK_BYTES, H * (F // QK) * BLOCK_BYTES
+    if gate_up.size != E * gu1 or down.size != E * dn1 or sh_gate_up.size != gu1 or sh_down.size != dn1:
+        raise ValueError("expert weights do not match E, H, F")
+    y = np.empty((n_tok, H), dtype=np.float64)
+    nbad = _load().oracle_moe_shared(_p(gate_up), _p(down), E, H, F, _p(sh_gate_up), _p(sh_down), _p(h), n_tok,
+                                     _p(ids), _p(wts), k, int(swiglu), _p(y))
+    return y, nbad
 
 
 def moe_down_combine(down, E, H, F, ids, wts, qa, da):

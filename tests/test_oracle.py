@@ -424,6 +424,68 @@ def test_moe_large_gate_makes_silu_identity(tiny_layer):
     np.testing.assert_allclose(a1, a0, rtol=1e-6)
 
 
+# ------------------------------------------------------ shared expert ------
+
+def _shared(tiny_layer, e):
+    """Expert e of the tiny table as a stand-alone shared expert."""
+    gu, dn = tiny_layer
+    return gu[e].copy(), dn[e].copy()
+
+
+def test_moe_shared_zero_scales_give_the_routed_layer(tiny_layer):
+    gu, dn = tiny_layer
+    sgu, sdn = _shared(tiny_layer, 5)
+    sdn.reshape(H_, F_ // QK, 18)[:, :, 0:2] = 0  # every down scale zero: o_sh == 0
+    h = synth.activations(3, H_, stream=42)
+    ids, wts = synth.router(3, 2, E_, stream=43)
+    y, nbad = O.moe_shared(gu, dn, E_, H_, F_, sgu, sdn, h, ids, wts)
+    assert nbad == 0
+    np.testing.assert_array_equal(y, O.moe(gu, dn, E_, H_, F_, h, ids, wts))
+
+
+@pytest.mark.parametrize("swiglu", [1, 0])
+def test_moe_shared_alone_is_one_dense_ffn(tiny_layer, swiglu):
+    """Every routed id out of range: each token gets exactly the shared
+    expert's FFN, built here from the pinned matvec pieces."""
+    gu, dn = tiny_layer
+    sgu, sdn = _shared(tiny_layer, 2)
+    h = synth.activations(2, H_, stream=44)
+    ids = np.array([[-1, E_], [E_ + 3, -9]], dtype=np.int32)
+    y, nbad = O.moe_shared(gu, dn, E_, H_, F_, sgu, sdn, h, ids, np.ones((2, 2), np.float32), swiglu=swiglu)
+    assert nbad == 4
+    for t in range(2):
+        want, _ = _expert_slot(sgu[None], sdn[None], 0, h[t], swiglu)
+        np.testing.assert_array_equal(y[t], want)
+
+
+def test_moe_shared_is_one_more_slot_of_weight_one(tiny_layer):
+    """The shared expert appended to the table as expert E and to every
+    token's slots (last, weight 1) gives the same layer."""
+    gu, dn = tiny_layer
+    sgu, sdn = _shared(tiny_layer, 1)
+    sgu[0, 0] ^= 0x5A  # differ from every routed expert
+    h = synth.activations(4, H_, stream=45)
+    ids, wts = synth.router(4, 3, E_, stream=46)
+    y, _ = O.moe_shared(gu, dn, E_, H_, F_, sgu, sdn, h, ids, wts)
+    ids_a = np.concatenate([ids, np.full((4, 1), E_, np.int32)], axis=1)
+    wts_a = np.concatenate([wts, np.ones((4, 1), np.float32)], axis=1)
+    y_a = O.moe(np.concatenate([gu, sgu[None]]), np.concatenate([dn, sdn[None]]), E_ + 1, H_, F_, h, ids_a, wts_a)
+    np.testing.assert_allclose(y, y_a, rtol=1e-12, atol=1e-14)
+
+
+def test_moe_shared_equal_to_a_routed_expert(tiny_layer):
+    """Shared expert == routed expert e, top-1 to e with weight w:
+    y = (w + 1) * o_e, token by token."""
+    gu, dn = tiny_layer
+    sgu, sdn = _shared(tiny_layer, 4)
+    h = synth.activations(3, H_, stream=47)
+    ids = np.full((3, 1), 4, np.int32)
+    wts = np.array([[0.25], [0.5], [2.0]], np.float32)
+    y, _ = O.moe_shared(gu, dn, E_, H_, F_, sgu, sdn, h, ids, wts)
+    y1 = O.moe(gu, dn, E_, H_, F_, h, ids, np.ones_like(wts))
+    np.testing.assert_allclose(y, (wts.astype(np.float64) + 1.0) * y1, rtol=1e-12, atol=1e-14)
+
+
 # ------------------------------------------------------------- router top-k --
 
 def _read_router_cases(golden_dir):

@@ -33,6 +33,8 @@ MUTANTS = {
         "const double g = row_dot(gu + (F + r) * nbH * ORACLE_BLOCK_BYTES, nbH, qh, dh);\n"
         "                const double u = row_dot(gu + r * nbH * ORACLE_BLOCK_BYTES, nbH, qh, dh);"),
     "router weight of the slot index only": ("const double wj = (double)wts[p];", "const double wj = (double)wts[j];"),
+    "shared expert weighted by slot 0's router weight": ("sh_wts[t] = 1.0f;", "sh_wts[t] = wts[t * k];"),
+    "shared expert output dropped": ("y[i] += ys[i];", "y[i] += 0.0 * ys[i];"),
     "router ties to the higher index": ("l[e] > l[best]", "l[e] >= l[best]"),
     "router weights not normalised": ("for (int j = 0; j < k; ++j) wts[t * k + j] /= sum;", ""),
 }
@@ -63,6 +65,10 @@ def _pins():
         lambda: T.test_moe_tokens_are_independent(tiny),
         lambda: T.test_moe_bad_ids_and_duplicates(tiny),
         lambda: T.test_moe_down_combine_matches_full(tiny),
+        lambda: T.test_moe_shared_zero_scales_give_the_routed_layer(tiny),
+        lambda: T.test_moe_shared_alone_is_one_dense_ffn(tiny, 1),
+        lambda: T.test_moe_shared_is_one_more_slot_of_weight_one(tiny),
+        lambda: T.test_moe_shared_equal_to_a_routed_expert(tiny),
         lambda: T.test_router_topk_golden(GOLDEN),
         lambda: T.test_router_topk_invariants(),
     ]
