@@ -491,7 +491,7 @@ def run_gpu(args):
         return (1e3 * ev[0].elapsed_time(ev[-1]) / (replays * n_calls), per_call) if samples else \
             1e3 * ev[0].elapsed_time(ev[-1]) / (replays * n_calls)
 
-    def layer_us(n_tok, k, reps=50):
+    def layer_us(n_tok, k, reps=50, extra_experts=0):
         tabs = []
         for i in range(N_SETS):
             ids_i, wts_i = synth.router(n_tok, k, E, stream=synth.S_IDS + 300 + 17 * n_tok + i)
@@ -527,11 +527,21 @@ def run_gpu(args):
         ci = [statistics.mean(trials) - half, statistics.mean(trials) + half]
         q = statistics.quantiles(per_replay, n=10)  # per replay of the 16 calls, 5 x 25 replays
         spread = {"p10": q[0], "p50": statistics.median(per_replay), "p90": q[-1]}
-        nbytes = sum(t[3] for t in tabs) / N_SETS * EXPERT_BYTES
+        nbytes = (sum(t[3] for t in tabs) / N_SETS + extra_experts) * EXPERT_BYTES
         return us, nbytes / (us * 1e-6) / 1e9, eager, split, ci, spread
 
     b1_us, b1_gbs, b1_eager, b1_split, b1_ci, b1_q = layer_us(1, 4)
     b5_us, b5_gbs, b5_eager, b5_split, b5_ci, b5_q = layer_us(5, 8)
+
+    # the same layers with an always-on shared expert of the routed shape
+    # (one more expert's bytes per call, read in the same layer kernel)
+    cbq.cbq_moe_set_shared(L, synth.weight_blocks(2 * F, H, stream=synth.S_GATE_UP * 1000 + 999),
+                           synth.weight_blocks(H, F, stream=synth.S_DOWN * 1000 + 999))
+    shared = {}
+    for name, (n_tok, k) in (("batch1_top4", (1, 4)), ("batch5_top8", (5, 8))):
+        us, gbs, _, _, ci, _ = layer_us(n_tok, k, reps=10, extra_experts=1)
+        shared[name] = {"us": us, "weight_gbs": gbs, "frac_of_peak": gbs / peak, "ci95_us": ci}
+    cbq.cbq_moe_set_shared(L, None, None)
 
     # dense decode projections (4096x4096, 16384x4096) through cbq_matvec, by
     # graph replay over copies whose bytes together exceed L2
@@ -584,6 +594,7 @@ def run_gpu(args):
                              "batch1_frac_of_peak": b1_gbs / peak, "batch5_frac_of_peak": b5_gbs / peak,
                              "eager_host_loop": {"batch1": b1_eager, "batch5": b5_eager},
                              "eager_split_us_layer_combine": {"batch1": b1_split, "batch5": b5_split}},
+            "us_per_layer_with_shared_expert": shared,
             "us_per_call_dense": dense,
             "kernels_ms_per_step": {"moe layer call (k_quantize + k_moe + k_moe_combine)": sum(k_moe) / len(timed),
                                     "head call (k_quantize + k_matvec<5>)": sum(k_head) / len(timed)},

@@ -153,6 +153,23 @@ int cbq_matvec_host(const cbq_weights *W, const float *x_host, int n, float *y_h
 int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int64_t F,
                    int on_device, void *stream, cbq_moe **out);
 int cbq_moe_destroy(cbq_moe *L);
+
+/* Give the layer a shared expert: one more gate_up (2F x H) and down (H x F)
+ * pair in canonical blocks, the same shapes as a routed expert, that every
+ * token passes through with weight 1 in each later cbq_moe_matvec* call:
+ *   y_t = sum_j wts[t][j] * o_{ids[t][j]}(h_t) + o_sh(h_t),
+ * o_sh computed exactly as a routed slot (SwiGLU split, requantization, down)
+ * and added after the routed sum.  The pages name only the routed layer
+ * ("feat(ds4): add DSpark speculative decoding" routes each token to its
+ * configured top-k); the always-on expert of the DS4 FFN block is read here
+ * as one more expert of the same shape.  Its weights are read once per call,
+ * in the same layer kernel, like any routed expert.  Host memory if
+ * on_device == 0; the blocks are repacked and not retained.  gate_up == down
+ * == NULL removes the shared expert.  Synchronizes `stream` first (a call
+ * still running on another stream must have ended).
+ * Errors: EINVAL (exactly one of gate_up, down NULL), ENOMEM, ECUDA. */
+int cbq_moe_set_shared(cbq_moe *L, const void *gate_up, const void *down, int on_device, void *stream);
+
 int cbq_moe_info(const cbq_moe *L, int *E, int64_t *H, int64_t *F, int64_t *device_bytes);
 
 /* Routed-expert FFN (mul_mat_id with the SwiGLU split and the weighted
@@ -167,6 +184,7 @@ int cbq_moe_info(const cbq_moe *L, int *E, int64_t *H, int64_t *F, int64_t *devi
  * token; a repeated id is served as an extra column and summed on its own.
  * An id outside [0,E) skips its slot and sets CBQ_DEVERR_BAD_EXPERT_ID.
  * The sum over j runs in slot order (deterministic, no atomics on y).
+ * With a shared expert (cbq_moe_set_shared) its output is added last.
  * Three kernel launches on `stream`, each a programmatic dependent of the one
  * before: the token quantization, the layer kernel (gate_up, SwiGLU,
  * requantization, down), the combine.  With one token and h_dev 16-byte
@@ -251,7 +269,8 @@ int cbq_get_device_error(unsigned int *code);
 int cbq_debug_block_dots(const cbq_weights *W, const int8_t *qx_dev, int n, int32_t *s_dev,
                          void *stream);
 
-/* Same for expert e of an MoE layer: which = 0 gate_up, 1 down. */
+/* Same for expert e of an MoE layer: which = 0 gate_up, 1 down; e == E
+ * names the shared expert (CBQ_EINVAL when there is none). */
 int cbq_moe_debug_block_dots(const cbq_moe *L, int e, int which, const int8_t *qx_dev, int n,
                              int32_t *s_dev, void *stream);
 
@@ -260,9 +279,10 @@ int cbq_moe_debug_block_dots(const cbq_moe *L, int e, int which, const int8_t *q
 int cbq_moe_set_debug(cbq_moe *L, int keep_intermediate);
 
 /* Copy the intermediate of the last cbq_moe_matvec on this handle, for
- * slots p = t*topk + j < nslots: a_dev[p][F] fp32 (needs debug on),
- * qa_dev[p][F] int8, da_dev[p][F/32] fp32 (any may be NULL).  Slots whose id
- * was out of range hold stale data. */
+ * slots p < nslots (at most CBQ_MAX_TOKENS * (CBQ_MAX_TOPK + 1)): routed
+ * slots p = t*topk + j, then the shared expert's slots p = n_tok*topk + t;
+ * a_dev[p][F] fp32 (needs debug on), qa_dev[p][F] int8, da_dev[p][F/32] fp32
+ * (any may be NULL).  Slots whose id was out of range hold stale data. */
 int cbq_moe_debug_intermediate(const cbq_moe *L, int nslots, float *a_dev, int8_t *qa_dev,
                                float *da_dev, void *stream);
 

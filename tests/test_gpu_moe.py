@@ -29,16 +29,38 @@ def _dev(torch, a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, swiglu, expect_bad=0):
+def _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, swiglu, expect_bad=0, shared=None):
+    """shared = (gate_up, down) blocks of the shared expert L holds, or None."""
     n_tok, k = ids.shape
+    N = n_tok * k
     cbq.cbq_moe_set_debug(L, True)
     g = Guarded(torch, (n_tok, H), torch.float32)
     y = cbq.cbq_moe_matvec(L, _dev(torch, h), _dev(torch, ids), _dev(torch, wts), swiglu=swiglu,
                            y=g.view).cpu().numpy()
     g.check()
-    a_g, qa_g, da_g = (t.cpu().numpy() for t in cbq.cbq_moe_debug_intermediate(L, n_tok * k))
+    a_g, qa_g, da_g = (t.cpu().numpy() for t in
+                       cbq.cbq_moe_debug_intermediate(L, N + (n_tok if shared is not None else 0)))
     err = cbq.cbq_get_device_error()
     assert err == (cbq.CBQ_DEVERR_BAD_EXPERT_ID if expect_bad else 0)
+    if shared is not None:
+        sgu, sdn = shared
+        y_sh, nbad_sh = O.moe_shared(gu, dn, E, H, F, sgu, sdn, h, ids, wts, swiglu=swiglu)
+        assert nbad_sh == expect_bad
+        # The checks below then run on an equivalent routed layer: the experts
+        # the tokens use, then the shared one, in a compact table; every token
+        # gets one more slot (last, weight 1) on the shared expert.  The GPU
+        # keeps the shared slots after the routed ones (N + t).
+        used = np.unique(ids[(ids >= 0) & (ids < E)])
+        remap = {int(e): i for i, e in enumerate(used)}
+        ids_c = np.array([[remap.get(int(e), -1) for e in row] for row in ids], dtype=np.int32)
+        gu = np.concatenate([gu[used], sgu[None]])
+        dn = np.concatenate([dn[used], sdn[None]])
+        E = len(used) + 1
+        ids = np.concatenate([ids_c, np.full((n_tok, 1), E - 1, np.int32)], axis=1)
+        wts = np.concatenate([wts, np.ones((n_tok, 1), np.float32)], axis=1)
+        gpu_slot = [t * k + j if j < k else N + t for t in range(n_tok) for j in range(k + 1)]
+        a_g, qa_g, da_g = a_g[gpu_slot], qa_g[gpu_slot], da_g[gpu_slot]
+        k += 1
     valid = ((ids >= 0) & (ids < E)).ravel()
 
     # stage 1: a per slot against the oracle's g, u and their bounds
@@ -81,6 +103,8 @@ def _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, swiglu, expect_bad=0):
         if np.any(dah):
             extra[t] += abs(float(wts.ravel()[p])) * (np.abs(_np_dequant(dn[e], H, F)) @ dah)
     assert_within_bound(y, y_ref, yb + extra / TOL, what="y (end to end)")
+    if shared is not None:
+        assert_within_bound(y, y_sh, yb + extra / TOL, what="y (end to end, shared-expert oracle)")
     return y
 
 
@@ -290,3 +314,117 @@ def test_back_to_back_layer_calls(torch, small, n_tok, k):
     for i, y in enumerate(ys):
         np.testing.assert_array_equal(y.cpu().numpy(), y_lg if i % 4 == 3 else ref[i % 3])
     assert cbq.cbq_get_device_error() == 0
+
+
+# ----------------------------------------------------------- shared expert -
+
+@pytest.fixture(scope="module")
+def small_shared(torch):
+    """The small layer on its own handle, with a shared expert drawn apart
+    from the routed ones."""
+    gu = synth.expert_blocks(E_S, 2 * F_S, H_S, stream=601)
+    dn = synth.expert_blocks(E_S, H_S, F_S, stream=602)
+    sgu = synth.expert_blocks(1, 2 * F_S, H_S, stream=670)[0]
+    sdn = synth.expert_blocks(1, H_S, F_S, stream=671)[0]
+    L = cbq.Moe(gu, dn, E_S, H_S, F_S)
+    cbq.cbq_moe_set_shared(L, sgu, sdn)
+    return gu, dn, (sgu, sdn), L
+
+
+@pytest.mark.parametrize("n_tok,k", [(1, 1), (1, 4), (3, 2), (5, 8)])
+@pytest.mark.parametrize("swiglu", [1, 0])
+def test_shared_expert_small(torch, small_shared, n_tok, k, swiglu):
+    gu, dn, sh, L = small_shared
+    h = synth.activations(n_tok, H_S, stream=672 + n_tok)
+    ids, wts = synth.router(n_tok, k, E_S, stream=673 + k)
+    _check_layer(torch, L, gu, dn, E_S, H_S, F_S, h, ids, wts, swiglu, shared=sh)
+
+
+def test_shared_expert_bad_ids_are_not_the_shared_one(torch, small_shared):
+    """A routed id equal to E (the shared expert's place in the kernels) or
+    any other out-of-range id skips its slot; the shared slot still runs."""
+    gu, dn, sh, L = small_shared
+    h = synth.activations(3, H_S, stream=680)
+    ids = np.array([[E_S, 1], [-1, E_S], [2, 2]], dtype=np.int32)
+    wts = np.random.default_rng(11).random((3, 2)).astype(np.float32)
+    _check_layer(torch, L, gu, dn, E_S, H_S, F_S, h, ids, wts, 1, expect_bad=3, shared=sh)
+
+
+def test_shared_expert_alone(torch, small_shared):
+    """Every routed id out of range: y is the shared expert's FFN."""
+    gu, dn, sh, L = small_shared
+    h = synth.activations(2, H_S, stream=681)
+    ids = np.array([[-3, E_S + 1], [E_S, -1]], dtype=np.int32)
+    y = _check_layer(torch, L, gu, dn, E_S, H_S, F_S, h, ids, np.ones((2, 2), np.float32), 1, expect_bad=4,
+                     shared=sh)
+    assert np.any(y != 0)
+
+
+def test_shared_expert_block_dots(torch, small_shared):
+    gu, dn, (sgu, sdn), L = small_shared
+    qx = np.random.default_rng(12).integers(-127, 128, size=(2, H_S)).astype(np.int8)
+    s = cbq.cbq_moe_debug_block_dots(L, E_S, 0, _dev(torch, qx)).cpu().numpy()
+    np.testing.assert_array_equal(s, O.block_dots(sgu, 2 * F_S, H_S, qx))
+    qx = np.random.default_rng(13).integers(-127, 128, size=(4, F_S)).astype(np.int8)
+    s = cbq.cbq_moe_debug_block_dots(L, E_S, 1, _dev(torch, qx)).cpu().numpy()
+    np.testing.assert_array_equal(s, O.block_dots(sdn, H_S, F_S, qx))
+
+
+def test_shared_expert_set_replace_remove(torch, small):
+    """Setting a shared expert, replacing it (from device memory) and removing
+    it: each state computes its own layer, and removal gives back the routed
+    layer's bits and the handle's byte count."""
+    gu, dn, L = small
+    h_np = synth.activations(5, H_S, stream=682)
+    ids_np, wts_np = synth.router(5, 3, E_S, stream=683)
+    h, ids, wts = _dev(torch, h_np), _dev(torch, ids_np), _dev(torch, wts_np)
+    y0 = cbq.cbq_moe_matvec(L, h, ids, wts).cpu().numpy()
+    b0 = L.device_bytes()
+    with pytest.raises(cbq.CbqError):  # no shared expert: id E names nothing
+        cbq.cbq_moe_debug_block_dots(L, E_S, 0, _dev(torch, np.zeros((1, H_S), np.int8)))
+    try:
+        cbq.cbq_moe_set_shared(L, gu[1], dn[1])  # a copy of routed expert 1
+        assert L.device_bytes() > b0
+        _check_layer(torch, L, gu, dn, E_S, H_S, F_S, h_np, ids_np, wts_np, 1, shared=(gu[1], dn[1]))
+        cbq.cbq_moe_set_shared(L, _dev(torch, gu[4]), _dev(torch, dn[4]))
+        _check_layer(torch, L, gu, dn, E_S, H_S, F_S, h_np, ids_np, wts_np, 1, shared=(gu[4], dn[4]))
+        # every router weight 0: the shared expert's output alone, whatever the ids
+        z = np.zeros_like(wts_np)
+        o4 = _check_layer(torch, L, gu, dn, E_S, H_S, F_S, h_np, ids_np, z, 1, shared=(gu[4], dn[4]))
+        o4b = cbq.cbq_moe_matvec(L, h, _dev(torch, np.full((5, 1), 1, np.int32)), _dev(torch, z[:, :1]))
+        np.testing.assert_array_equal(o4b.cpu().numpy(), o4)
+    finally:
+        cbq.cbq_moe_set_shared(L, None, None)
+    assert L.device_bytes() == b0
+    np.testing.assert_array_equal(cbq.cbq_moe_matvec(L, h, ids, wts).cpu().numpy(), y0)
+    with pytest.raises(ValueError):
+        cbq.cbq_moe_set_shared(L, gu[1][:-1], dn[1])
+
+
+def test_shared_expert_with_maximum_slots(torch, wide):
+    """5 tokens x top-16 plus 5 shared slots: 85 columns, the most a call
+    has."""
+    gu, dn, L, (E_, H_, F_) = wide
+    sgu = synth.expert_blocks(1, 2 * F_, H_, stream=684)[0]
+    sdn = synth.expert_blocks(1, H_, F_, stream=685)[0]
+    h = synth.activations(5, H_, stream=686)
+    ids, wts = synth.router(5, 16, E_, stream=687)
+    cbq.cbq_moe_set_shared(L, sgu, sdn)
+    try:
+        _check_layer(torch, L, gu, dn, E_, H_, F_, h, ids, wts, 1, shared=(sgu, sdn))
+    finally:
+        cbq.cbq_moe_set_shared(L, None, None)
+
+
+@pytest.mark.parametrize("n_tok,k", [(1, 4), (5, 8)])
+def test_shared_expert_full_size(torch, full, n_tok, k):
+    gu, dn, L, t1, t5 = full
+    ids, wts = t1 if n_tok == 1 else t5
+    sgu = synth.weight_blocks(2 * F, H, stream=synth.S_GATE_UP * 1000 + 999)
+    sdn = synth.weight_blocks(H, F, stream=synth.S_DOWN * 1000 + 999)
+    h = synth.activations(n_tok, H, stream=synth.S_H + 7 + n_tok)
+    cbq.cbq_moe_set_shared(L, sgu, sdn)
+    try:
+        _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, 1, shared=(sgu, sdn))
+    finally:
+        cbq.cbq_moe_set_shared(L, None, None)

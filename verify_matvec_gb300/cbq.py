@@ -43,6 +43,7 @@ _SIGS = {
     "cbq_matvec_static": ([_P, _P, _I, _P, _P], _I),
     "cbq_moe_create": ([_P, _P, _I, _I64, _I64, _I, _P, ctypes.POINTER(_P)], _I),
     "cbq_moe_destroy": ([_P], _I),
+    "cbq_moe_set_shared": ([_P, _P, _P, _I, _P], _I),
     "cbq_moe_info": ([_P, ctypes.POINTER(_I), ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)], _I),
     "cbq_moe_matvec": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
     "cbq_moe_matvec_host": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
@@ -194,12 +195,36 @@ class Moe:
         _check(lib.cbq_moe_create(p1, p2, E, H, F, on_dev, _stream(stream), ctypes.byref(h)), "cbq_moe_create")
         self._h = h
         self.E, self.H, self.F = E, H, F
+        self.shared = False
 
     @property
     def handle(self):
         if self._h is None:
             raise ValueError("destroyed handle")
         return self._h
+
+    def set_shared(self, gate_up, down, stream=None):
+        """cbq_moe_set_shared: a shared expert of the layer's shapes (blocks of
+        one gate_up 2F x H and one down H x F), or None, None to remove it."""
+        torch = _torch()
+        lib = load()
+        if gate_up is None and down is None:
+            _check(lib.cbq_moe_set_shared(self.handle, None, None, 0, _stream(stream)), "cbq_moe_set_shared")
+            self.shared = False
+            return
+        nbH, nbF = self.H // CBQ_QK, self.F // CBQ_QK
+        if isinstance(gate_up, torch.Tensor):
+            p1, p2, on_dev = _dev_ptr(gate_up, torch.uint8, "gate_up"), _dev_ptr(down, torch.uint8, "down"), 1
+            n_gu, n_dn = gate_up.numel(), down.numel()
+        else:
+            gate_up = np.ascontiguousarray(gate_up, dtype=np.uint8)
+            down = np.ascontiguousarray(down, dtype=np.uint8)
+            p1, p2, on_dev = gate_up.ctypes.data_as(_P), down.ctypes.data_as(_P), 0
+            n_gu, n_dn = gate_up.size, down.size
+        if n_gu != 2 * self.F * nbH * CBQ_BLOCK_BYTES or n_dn != self.H * nbF * CBQ_BLOCK_BYTES:
+            raise ValueError("shared expert blocks do not match H, F")
+        _check(lib.cbq_moe_set_shared(self.handle, p1, p2, on_dev, _stream(stream)), "cbq_moe_set_shared")
+        self.shared = True
 
     def device_bytes(self) -> int:
         b = ctypes.c_int64()
@@ -289,6 +314,12 @@ def cbq_moe_matvec(L: Moe, h, ids, wts, swiglu: int = 1, y=None, stream=None):
                                  _dev_ptr(wts, torch.float32, "wts"), k, int(swiglu),
                                  _dev_ptr(y, torch.float32, "y"), _stream(stream)), "cbq_moe_matvec")
     return y
+
+
+def cbq_moe_set_shared(L: Moe, gate_up, down, stream=None):
+    """Give L a shared expert (canonical blocks, host array or device tensor),
+    or remove it with gate_up = down = None."""
+    L.set_shared(gate_up, down, stream=stream)
 
 
 def cbq_router_topk(logits, k: int, ids=None, wts=None, stream=None):

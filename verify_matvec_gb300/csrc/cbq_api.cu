@@ -37,6 +37,9 @@ struct cbq_moe {
     DevMoe L;
     uint4 *gu_qs, *dn_qs;
     uint2 *gu_sc, *dn_sc;
+    uint4 *sh_gu_qs, *sh_dn_qs;  // shared expert (null when unset)
+    uint2 *sh_gu_sc, *sh_dn_sc;
+    int64_t sh_bytes;
     MoeWork ws;
     float *st_h;      // CBQ_MAX_TOKENS x H
     int32_t *st_ids;  // kMaxSlots
@@ -329,9 +332,29 @@ int cbq_debug_block_dots(const cbq_weights *W, const int8_t *qx_dev, int n, int3
 
 // --------------------------------------------------------------- MoE -----
 
+namespace {
+
+// Frees the shared expert of L and stops the kernels from using it.
+void drop_shared(cbq_moe *L) {
+    cudaFree(L->sh_gu_qs);
+    cudaFree(L->sh_gu_sc);
+    cudaFree(L->sh_dn_qs);
+    cudaFree(L->sh_dn_sc);
+    L->sh_gu_qs = L->sh_dn_qs = nullptr;
+    L->sh_gu_sc = L->sh_dn_sc = nullptr;
+    L->bytes -= L->sh_bytes;
+    L->sh_bytes = 0;
+    L->L.sh_gu_qs = L->L.sh_dn_qs = nullptr;
+    L->L.sh_gu_sc = L->L.sh_dn_sc = nullptr;
+    L->L.shared = 0;
+}
+
+}  // namespace
+
 int cbq_moe_destroy(cbq_moe *L) {
     if (!L) return CBQ_EINVAL;
     DeviceScope scope(L->device);
+    drop_shared(L);
     cudaFree(L->gu_qs);
     cudaFree(L->gu_sc);
     cudaFree(L->dn_qs);
@@ -428,6 +451,48 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
     return CBQ_OK;
 }
 
+int cbq_moe_set_shared(cbq_moe *L, const void *gate_up, const void *down, int on_device, void *stream) {
+    if (!L || !gate_up != !down) return CBQ_EINVAL;
+    DeviceScope scope(L->device);
+    CBQ_CUDA(scope.status());
+    cudaStream_t s = as_stream(stream);
+    CBQ_CUDA(cudaStreamSynchronize(s));  // no call of this stream may still read the old weights
+    if (!gate_up) {
+        drop_shared(L);
+        return CBQ_OK;
+    }
+    const int64_t H = L->L.H, F = L->L.F;
+    const int nbH = (int)(H / CBQ_QK), nbF = (int)(F / CBQ_QK);
+    int rc = CBQ_OK;
+    if (!L->sh_gu_qs) {
+        int64_t got = 0;
+        if ((rc = dev_alloc(&L->sh_gu_qs, cbq::qs_elems(2 * F, nbH), &got)) != CBQ_OK ||
+            (rc = dev_alloc(&L->sh_gu_sc, cbq::sc_elems(2 * F, nbH), &got)) != CBQ_OK ||
+            (rc = dev_alloc(&L->sh_dn_qs, cbq::qs_elems(H, nbF), &got)) != CBQ_OK ||
+            (rc = dev_alloc(&L->sh_dn_sc, cbq::sc_elems(H, nbF), &got)) != CBQ_OK) {
+            L->bytes += got;
+            L->sh_bytes = got;
+            drop_shared(L);
+            return rc;
+        }
+        L->bytes += got;
+        L->sh_bytes = got;
+    }
+    L->L.shared = 0;  // partly rewritten weights are never used
+    rc = repack_into(gate_up, 2 * F, nbH, on_device, L->sh_gu_qs, L->sh_gu_sc, s);
+    if (rc == CBQ_OK) rc = repack_into(down, H, nbF, on_device, L->sh_dn_qs, L->sh_dn_sc, s);
+    if (rc != CBQ_OK) {
+        drop_shared(L);
+        return rc;
+    }
+    L->L.sh_gu_qs = L->sh_gu_qs;
+    L->L.sh_gu_sc = L->sh_gu_sc;
+    L->L.sh_dn_qs = L->sh_dn_qs;
+    L->L.sh_dn_sc = L->sh_dn_sc;
+    L->L.shared = 1;
+    return CBQ_OK;
+}
+
 int cbq_moe_info(const cbq_moe *L, int *E, int64_t *H, int64_t *F, int64_t *device_bytes) {
     if (!L) return CBQ_EINVAL;
     if (E) *E = L->L.E;
@@ -494,20 +559,21 @@ int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok, const 
 
 int cbq_moe_debug_block_dots(const cbq_moe *L, int e, int which, const int8_t *qx_dev, int n, int32_t *s_dev,
                              void *stream) {
-    if (!L || e < 0 || e >= L->L.E || (which != 0 && which != 1) || !qx_dev || !s_dev || n < 1 ||
-        n > CBQ_MAX_COLS || !aligned16(qx_dev))
+    if (!L || e < 0 || e > L->L.E || (e == L->L.E && !L->L.shared) || (which != 0 && which != 1) || !qx_dev ||
+        !s_dev || n < 1 || n > CBQ_MAX_COLS || !aligned16(qx_dev))
         return CBQ_EINVAL;
     DeviceScope scope(L->device);
     CBQ_CUDA(scope.status());
+    const bool sh = e == L->L.E;
     DevMat m;
     if (which == 0) {
-        m.qs = L->gu_qs + e * L->L.gu_qs_stride;
-        m.sc = L->gu_sc + e * L->L.gu_sc_stride;
+        m.qs = sh ? L->sh_gu_qs : L->gu_qs + e * L->L.gu_qs_stride;
+        m.sc = sh ? L->sh_gu_sc : L->gu_sc + e * L->L.gu_sc_stride;
         m.M = 2 * (int64_t)L->L.F;
         m.nb = L->L.H / CBQ_QK;
     } else {
-        m.qs = L->dn_qs + e * L->L.dn_qs_stride;
-        m.sc = L->dn_sc + e * L->L.dn_sc_stride;
+        m.qs = sh ? L->sh_dn_qs : L->dn_qs + e * L->L.dn_qs_stride;
+        m.sc = sh ? L->sh_dn_sc : L->dn_sc + e * L->L.dn_sc_stride;
         m.M = L->L.H;
         m.nb = L->L.F / CBQ_QK;
     }

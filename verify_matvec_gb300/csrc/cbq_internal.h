@@ -32,6 +32,13 @@ struct DevMoe {
     const uint2 *dn_sc;
     int E, H, F;
     size_t gu_qs_stride, gu_sc_stride, dn_qs_stride, dn_sc_stride;  // per expert
+    // Optional shared expert (same shapes), applied to every token with
+    // weight 1; the kernels address it as expert id E.  Null when absent.
+    const uint4 *sh_gu_qs;
+    const uint2 *sh_gu_sc;
+    const uint4 *sh_dn_qs;
+    const uint2 *sh_dn_sc;
+    int shared;
 };
 
 // Per-call scratch of an MoE layer handle (device memory it owns).
@@ -48,7 +55,7 @@ struct MoeWork {
     cudaEvent_t ev[3];  // optional stage events (before the layer kernel, before the combine, after it)
 };
 
-constexpr int kMaxSlots = 80;  // CBQ_MAX_TOKENS * CBQ_MAX_TOPK
+constexpr int kMaxSlots = 85;  // CBQ_MAX_TOKENS * (CBQ_MAX_TOPK routed + 1 shared)
 
 cudaError_t launch_repack(const uint8_t *src, int64_t M, int nb, uint4 *qs, uint2 *sc, cudaStream_t s);
 cudaError_t launch_quantize(const float *x, int64_t K, int n, int8_t *qx, float *dx, cudaStream_t s);

@@ -385,41 +385,75 @@ struct MoeArgs {
     int quant_tokens;  // the consumers quantize h themselves (one token, h 16-byte aligned)
 };
 
-// Distinct in-range expert ids of the routing table, ascending, computed
-// redundantly by every CTA from the <= 80 ids (no host round trip).
+// Distinct in-range expert ids of the routing table, ascending but the shared
+// expert first (its items, with a column for every token, are the slowest:
+// handed out first, they do not form the tail of a pass), computed
+// redundantly by every CTA from the <= 85 slots (no host round trip).  Slots
+// 0..N-1 are the routed ones (p = t*k + j); with a shared expert, slots
+// N..N+n_tok-1 hold its virtual id E, one per token.  An out-of-range routed
+// id is stored as -1, so it matches no expert, the shared one included.
 struct Routing {
     int ids[kMaxSlots];
-    int first[kMaxSlots];
     int uniq[kMaxSlots];
+    unsigned char first[kMaxSlots];
     int D;
 };
 
-__device__ void route(const int32_t *__restrict__ ids, int N, int E, Routing &R, bool report) {
+__device__ void route(const int32_t *__restrict__ ids, int N, int n_all, int E, Routing &R, bool report) {
     const int t = threadIdx.x;
-    if (t < N) R.ids[t] = ids[t];
-    __syncthreads();
-    if (t < N) {
-        const int e = R.ids[t];
-        const bool valid = e >= 0 && e < E;
-        int f = valid ? 1 : 0;
-        for (int p = 0; p < t; ++p)
-            if (R.ids[p] == e) f = 0;
-        R.first[t] = f;
-        if (!valid && report) atomicOr(&g_device_error, kErrBadExpertId);
+    if (t < n_all) {
+        int e = E;  // a shared-expert slot
+        if (t < N) {
+            e = ids[t];
+            if (e < 0 || e >= E) {
+                if (report) atomicOr(&g_device_error, kErrBadExpertId);
+                e = -1;
+            }
+        }
+        R.ids[t] = e;
     }
     __syncthreads();
-    if (t < N && R.first[t]) {
+    if (t < n_all) {
+        const int e = R.ids[t];
+        int f = e >= 0 ? 1 : 0;
+        for (int p = 0; p < t; ++p)
+            if (R.ids[p] == e) f = 0;
+        R.first[t] = (unsigned char)f;
+    }
+    __syncthreads();
+    if (t < n_all && R.first[t]) {
+        auto key = [E](int e) { return e == E ? -1 : e; };
+        const int kt = key(R.ids[t]);
         int rank = 0;
-        for (int p = 0; p < N; ++p)
-            if (R.first[p] && R.ids[p] < R.ids[t]) ++rank;
+        for (int p = 0; p < n_all; ++p)
+            if (R.first[p] && key(R.ids[p]) < kt) ++rank;
         R.uniq[rank] = R.ids[t];
     }
     if (t == 0) {
         int D = 0;
-        for (int p = 0; p < N; ++p) D += R.first[p];
+        for (int p = 0; p < n_all; ++p) D += R.first[p];
         R.D = D;
     }
     __syncthreads();
+}
+
+// Token of slot p: routed slots are t*k + j, shared-expert slots N + t.
+__device__ __forceinline__ int slot_token(int p, int N, int k) { return p < N ? p / k : p - N; }
+
+// Weights of expert e, the shared expert for e == E.
+struct ExpertMat {
+    const uint4 *qs;
+    const uint2 *sc;
+};
+
+__device__ __forceinline__ ExpertMat gate_up_of(const DevMoe &L, int e) {
+    if (e < L.E) return {L.gu_qs + (size_t)e * L.gu_qs_stride, L.gu_sc + (size_t)e * L.gu_sc_stride};
+    return {L.sh_gu_qs, L.sh_gu_sc};
+}
+
+__device__ __forceinline__ ExpertMat down_of(const DevMoe &L, int e) {
+    if (e < L.E) return {L.dn_qs + (size_t)e * L.dn_qs_stride, L.dn_sc + (size_t)e * L.dn_sc_stride};
+    return {L.sh_dn_qs, L.sh_dn_sc};
 }
 
 // Slots of expert e (ascending) found by one warp with ballots over the
@@ -480,7 +514,8 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Slots &sl, 
                                              int u, int g, int nc, int warp, int lane, int buf) {
     int col_off[kMaxCols];  // activation column of each slot: its token's column
 #pragma unroll
-    for (int c = 0; c < kMaxCols; ++c) col_off[c] = (c < nc ? sl.sl[c] / A.k : 0) * A.nbpH;
+    for (int c = 0; c < kMaxCols; ++c)
+        col_off[c] = (c < nc ? slot_token(sl.sl[c], A.n_tok * A.k, A.k) : 0) * A.nbpH;
     float *pg = S.part + (2 * buf) * kPartSet;
     float *pu = S.part + (2 * buf + 1) * kPartSet;
     group_cols(co, S.pipe, A.nbpH, S.act, S.dx, col_off, nc, pg + warp * kMaxCols * 32, warp, lane);
@@ -551,8 +586,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
     pdl_trigger();  // the combine kernel may launch; it waits for this grid
-    const int N = A.n_tok * A.k;
-    route(A.ids, N, A.L.E, R, blockIdx.x == 0);
+    const int N = A.n_tok * A.k + (A.L.shared ? A.n_tok : 0);  // routed slots, then shared ones
+    route(A.ids, A.n_tok * A.k, N, A.L.E, R, blockIdx.x == 0);
     const int Gf = A.L.F / 32, Gd = A.L.H / 32;
     const unsigned total_gu = (unsigned)(R.D * Gf);
     const unsigned total = total_gu + (unsigned)(R.D * Gd);
@@ -577,23 +612,22 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                 for (unsigned it = base; it < min(total, base + grab) && !pr.stopped; ++it) {
                     if (it < total_gu) {
                         const int u = (int)it / Gf, g = (int)it - u * Gf;
-                        const size_t e = (size_t)R.uniq[u];
+                        const ExpertMat w = gate_up_of(A.L, R.uniq[u]);
                         const int nch = col_chunks(expert_ns(R, u, N));
                         for (int ch = 0; ch < nch; ++ch) {
                             for (int half = 0; half < 2; ++half) {
                                 const size_t grp = (size_t)g + (size_t)half * Gf;
-                                pr.group(S.pipe, A.L.gu_qs + e * A.L.gu_qs_stride + grp * A.nbpH * 32,
-                                         A.L.gu_sc + e * A.L.gu_sc_stride + grp * nbqH * 32, A.nbpH, (int)it);
+                                pr.group(S.pipe, w.qs + grp * A.nbpH * 32, w.sc + grp * nbqH * 32, A.nbpH, (int)it);
                             }
                         }
                     } else {
                         const int j = (int)(it - total_gu);
                         const int u = j / Gd, g = j - u * Gd;
-                        const size_t e = (size_t)R.uniq[u];
+                        const ExpertMat w = down_of(A.L, R.uniq[u]);
                         const int nch = col_chunks(expert_ns(R, u, N));
                         for (int ch = 0; ch < nch; ++ch)
-                            pr.group(S.pipe, A.L.dn_qs + e * A.L.dn_qs_stride + (size_t)g * A.nbpF * 32,
-                                     A.L.dn_sc + e * A.L.dn_sc_stride + (size_t)g * nbqF * 32, A.nbpF, (int)it);
+                            pr.group(S.pipe, w.qs + (size_t)g * A.nbpF * 32, w.sc + (size_t)g * nbqF * 32, A.nbpF,
+                                     (int)it);
                     }
                 }
             }
@@ -674,7 +708,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
 }
 
 // Router-weighted combine: y[t][r] = sum_j wts[t][j] * obuf[t*k+j][r], slots
-// in order j = 0..k-1, slots with an out-of-range id skipped.  One thread per
+// in order j = 0..k-1, slots with an out-of-range id skipped, then plus the
+// shared expert's output obuf[N+t][r] when the layer has one.  One thread per
 // output; launched as a dependent of the layer kernel.  The ids and weights
 // are inputs of the call, complete before its first kernel started, so they
 // are read into shared memory before the wait; a token's k loads of obuf are
@@ -703,13 +738,14 @@ __global__ void __launch_bounds__(256) k_moe_combine(const __grid_constant__ Moe
             const int p = min(p0 + j, kMaxSlots - 1);
             o[j] = j < A.k && ok_s[p] ? A.ws.obuf[(size_t)p * A.L.H + r] : 0.0f;
         }
+        const float osh = A.L.shared ? A.ws.obuf[(size_t)(N + t) * A.L.H + r] : 0.0f;
         float v = 0.0f;
 #pragma unroll
         for (int j = 0; j < kMaxTopk; ++j) {
             const int p = min(p0 + j, kMaxSlots - 1);
             if (j < A.k && ok_s[p]) v += w_s[p] * o[j];
         }
-        A.y[i] = v;
+        A.y[i] = v + osh;
     }
 }
 
@@ -740,7 +776,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
         e = launch_quantize(h, L.H, n_tok, ws.qh, ws.dh, s);
         if (e != cudaSuccess) return e;
     }
-    const int64_t max_experts = std::min(n_tok * k, L.E);
+    const int64_t max_experts = std::min(n_tok * k, L.E) + (L.shared ? 1 : 0);
     {
         const size_t smem = moe_smem_bytes(A.act_blocks);
         int grid = 0;
