@@ -578,23 +578,25 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Slots &sl, con
 // on anything, so a down item's wait for its expert's intermediate
 // (done[u] == Gf * ns) always ends; it is bounded all the same.
 // The producer streams a down item's weights before that wait ends.
-// The routing table and the handle's counters are read before any wait: the
-// kernel is launched in plain stream order (one token, quantized here) or as
-// the dependent of the quantization kernel, which lets it start only once all
-// earlier work has ended.
+// Launched as a programmatic dependent either way.  With one token (quantized
+// here) this is the call's first kernel: it sets up its pipeline, then waits
+// for all earlier work before it reads anything or lets the combine start.
+// Otherwise it follows the quantization kernel, which starts it only once all
+// earlier work has ended, so the routing table and the handle's counters are
+// read before the wait for the quantized tokens.
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__ MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
+    const PipeSmem S = carve_pipe(smem, kStagesMoe, 1, A.act_blocks);
+    pipe_init(S.pipe);
+    if (A.quant_tokens) pdl_wait();
     pdl_trigger();  // the combine kernel may launch; it waits for this grid
     const int N = A.n_tok * A.k + (A.L.shared ? A.n_tok : 0);  // routed slots, then shared ones
-    route(A.ids, A.n_tok * A.k, N, A.L.E, R, blockIdx.x == 0);
+    route(A.ids, A.n_tok * A.k, N, A.L.E, R, blockIdx.x == 0);  // ends with a CTA barrier
     const int Gf = A.L.F / 32, Gd = A.L.H / 32;
     const unsigned total_gu = (unsigned)(R.D * Gf);
     const unsigned total = total_gu + (unsigned)(R.D * Gd);
     unsigned *sched = A.ws.sched;
-    const PipeSmem S = carve_pipe(smem, kStagesMoe, 1, A.act_blocks);
-    pipe_init(S.pipe);
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == kConsumerWarps) {  // producer
         if (lane == 0) {
@@ -766,9 +768,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     A.nbF = L.F / kQK;
     A.nbpF = round_up4(A.nbF);
     A.act_blocks = std::max(n_tok * A.nbpH, kMaxCols * A.nbpF);
-    // one token: the layer kernel quantizes it (one launch fewer); the layer
-    // kernel then follows the stream's earlier work in plain order, since it
-    // reads the routing table before any dependency wait
+    // one token: the layer kernel quantizes it (one launch fewer)
     A.quant_tokens = n_tok == 1 && ((uintptr_t)h & 15u) == 0;
     cudaError_t e = cudaSuccess;
     if (ws.ev[0] && (e = cudaEventRecord(ws.ev[0], s)) != cudaSuccess) return e;
@@ -782,7 +782,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
         int grid = 0;
         e = dynamic_grid(k_moe, smem, max_experts * (L.F / 32 + L.H / 32), &grid);
         if (e != cudaSuccess) return e;
-        e = launch_k(k_moe, grid, kPipeThreads, smem, s, !A.quant_tokens, A);
+        e = launch_k(k_moe, grid, kPipeThreads, smem, s, true, A);
         if (e != cudaSuccess) return e;
     }
     if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
