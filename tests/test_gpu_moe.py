@@ -428,3 +428,32 @@ def test_shared_expert_full_size(torch, full, n_tok, k):
         _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, 1, shared=(sgu, sdn))
     finally:
         cbq.cbq_moe_set_shared(L, None, None)
+
+
+@pytest.mark.parametrize("n_tok,k", [(1, 4), (5, 8)])
+def test_inputs_written_just_before_the_call(torch, small, n_tok, k):
+    """Each call's token and routing table are written by a device copy on the
+    same stream right before it (no synchronization in between), so the
+    call's first kernel must wait for that copy before it reads them."""
+    gu, dn, L = small
+    tabs = []
+    for i in range(4):
+        h = _dev(torch, synth.activations(n_tok, H_S, stream=690 + i))
+        ids, wts = synth.router(n_tok, k, E_S, stream=694 + i)
+        tabs.append((h, _dev(torch, ids), _dev(torch, wts)))
+    ref = []
+    for h, ids, wts in tabs:
+        ref.append(cbq.cbq_moe_matvec(L, h, ids, wts).cpu().numpy())
+        torch.cuda.synchronize()
+    hb, ib, wb = (torch.empty_like(t) for t in tabs[0])
+    ys = [torch.empty((n_tok, H_S), dtype=torch.float32, device="cuda") for _ in range(16)]
+    for i, y in enumerate(ys):
+        h, ids, wts = tabs[i % 4]
+        hb.copy_(h)
+        ib.copy_(ids)
+        wb.copy_(wts)
+        cbq.cbq_moe_matvec(L, hb, ib, wb, y=y)
+    torch.cuda.synchronize()
+    for i, y in enumerate(ys):
+        np.testing.assert_array_equal(y.cpu().numpy(), ref[i % 4])
+    assert cbq.cbq_get_device_error() == 0
