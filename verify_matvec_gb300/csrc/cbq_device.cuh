@@ -180,6 +180,29 @@ __device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, co
     }
 }
 
+// The same dots (NC >= 2, shared expansion) with column c's two words at
+// act0[2*(off[c] + b)] and [+1]: the routed-expert kernel stages its columns
+// one after another, not block-major.
+template <int NC, int M>
+__device__ __forceinline__ void block_dots_cols(const Codebook &cb, const uint4 w, const uint4 *act0,
+                                                const int (&off)[M], int b, int sdot[NC]) {
+    static_assert(NC <= M, "a column offset for every column");
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t e[8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) expand_select(cb, ws[m], e[2 * m], e[2 * m + 1]);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const uint4 *a = act0 + 2 * (off[c] + b);
+        const uint4 a0 = a[0], a1 = a[1];
+        const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        int s = kMagicBits;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s = __dp4a((int)e[i], (int)av[i], s);
+        sdot[c] = s;
+    }
+}
+
 // Scaled accumulation of two consecutive blocks' dots of one column:
 // acc += (dw0*dx0 * s0, dw1*dx1 * s1) with the packed fp32x2 pipe; the same
 // three roundings per block as a scalar multiply, add and fused multiply-add.

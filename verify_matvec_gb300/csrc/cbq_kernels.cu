@@ -516,6 +516,10 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Slots &sl, 
 #pragma unroll
     for (int c = 0; c < kMaxCols; ++c)
         col_off[c] = (c < nc ? slot_token(sl.sl[c], A.n_tok * A.k, A.k) : 0) * A.nbpH;
+    int p = sl.sl[0];  // the slot this warp writes (warp < nc), taken before the sweeps
+#pragma unroll
+    for (int cc = 1; cc < kMaxCols; ++cc)
+        if (warp == cc) p = sl.sl[cc];
     float *pg = S.part + (2 * buf) * kPartSet;
     float *pu = S.part + (2 * buf + 1) * kPartSet;
     group_cols(co, S.pipe, A.nbpH, S.act, S.dx, col_off, nc, pg + warp * kMaxCols * 32, warp, lane);
@@ -532,10 +536,6 @@ __device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Slots &sl, 
         const float a = A.swiglu ? gs / (1.0f + expf(-gs)) * us : gs * us;
         float d;
         const int8_t q = quant_lane(a, d);
-        int p = sl.sl[0];
-#pragma unroll
-        for (int cc = 1; cc < kMaxCols; ++cc)
-            if (c == cc) p = sl.sl[cc];
         const size_t o = (size_t)p * A.L.F + (size_t)g * 32 + lane;
         A.ws.qa[o] = q;
         if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
@@ -554,6 +554,10 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Slots &sl, con
     int col_off[kMaxCols];
 #pragma unroll
     for (int c = 0; c < kMaxCols; ++c) col_off[c] = c * A.nbpF;
+    int p = sl.sl[0];  // the slot this warp writes (warp < nc), taken before the sweep
+#pragma unroll
+    for (int cc = 1; cc < kMaxCols; ++cc)
+        if (warp == cc) p = sl.sl[cc];
     float *part = S.part + buf * kPartSet;
     group_cols(co, S.pipe, A.nbpF, S.act, S.dx, col_off, nc, part + warp * kMaxCols * 32, warp, lane);
     consumer_sync();
@@ -561,10 +565,6 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Slots &sl, con
         float v = 0.0f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) v += part[(w * kMaxCols + warp) * 32 + lane];
-        int p = sl.sl[0];
-#pragma unroll
-        for (int cc = 1; cc < kMaxCols; ++cc)
-            if (warp == cc) p = sl.sl[cc];
         A.ws.obuf[(size_t)p * A.L.H + (size_t)g * 32 + lane] = v;
     }
 }

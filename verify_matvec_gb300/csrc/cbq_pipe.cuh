@@ -233,14 +233,16 @@ struct Consumer {
     }
 };
 
-// One-column variant for the routed-expert kernels: ncols (runtime, >= 1)
-// columns, each swept separately over every stage from shared memory, so the
-// registers stay those of one column while the weight stream is still read
-// once.  The sum of this warp over the pass goes to part[c*32 + lane] (this
-// warp's slice of a partial set).  With one column (kOne) the running sums
-// stay in registers over the whole pass and are stored once at its end;
-// otherwise each column's slice is written at the pass's first stage and
-// accumulated over the rest.
+// Sweeps of the routed-expert kernels over one 32-row group pass (blocks
+// [0, nbp)) for the columns at col_off[0..ncols): this warp's sum over the pass
+// goes to part[c*32 + lane] (its slice of a partial set).
+//   - one column (kOne, the common case: one token per expert): the two-word
+//     expansion, running sums in registers over the whole pass;
+//   - more columns: at every stage, the columns two at a time share one
+//     expansion (an odd last column takes the one-column expansion), and each
+//     column's stage sum is added to its slice in shared memory, so the
+//     registers stay those of two columns while the weight stream is still
+//     read once.
 template <bool kOne>
 __device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int nbp, const uint4 *act0,
                                                 const float *dx0, const int (&col_off)[kMaxCols], int ncols_rt, float *part,
@@ -257,31 +259,59 @@ __device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int
             const uint2 *sc_s = reinterpret_cast<const uint2 *>(st + kStageQsBytes);
             const int q0 = (int)((unsigned)(warp * nq) / kConsumerWarps);
             const int q1 = (int)((unsigned)((warp + 1) * nq) / kConsumerWarps);
-            for (int c = 0; c < ncols; ++c) {
-                const int off = kOne ? col_off[0] : pick(col_off, c);
-                const uint4 *act = act0 + off * 2;
-                const float *dxs = dx0 + off;
-                float2 acc = kOne ? run : make_float2(0.0f, 0.0f);
-                for (int q = q0; q < q1; ++q) {
-                    const uint2 s = sc_s[q * 32 + lane];
-                    const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
-                    const float2 dw23 = __half22float2(*reinterpret_cast<const __half2 *>(&s.y));
-                    const int bq = b0 + q * 4;
+            for (int c = 0; c < ncols; c += 2) {
+                if (kOne || c + 1 == ncols) {  // one column
+                    const int off = kOne ? col_off[0] : pick(col_off, c);
+                    const uint4 *act = act0 + off * 2;
+                    const float *dxs = dx0 + off;
+                    float2 acc = kOne ? run : make_float2(0.0f, 0.0f);
+                    for (int q = q0; q < q1; ++q) {
+                        const uint2 s = sc_s[q * 32 + lane];
+                        const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
+                        const float2 dw23 = __half22float2(*reinterpret_cast<const __half2 *>(&s.y));
+                        const int bq = b0 + q * 4;
 #pragma unroll
-                    for (int jj = 0; jj < 4; jj += 2) {
-                        int sa[1], sb[1];
-                        block_dots<1>(co.cb, qs_s[(q * 4 + jj) * 32 + lane], act + (bq + jj) * 2, sa);
-                        block_dots<1>(co.cb, qs_s[(q * 4 + jj + 1) * 32 + lane], act + (bq + jj + 1) * 2, sb);
-                        const float2 dx2 = *reinterpret_cast<const float2 *>(dxs + bq + jj);
-                        const float2 dw = jj == 0 ? dw01 : dw23;
-                        acc = scale_acc2(acc, dw, dx2, sa[0], sb[0]);
+                        for (int jj = 0; jj < 4; jj += 2) {
+                            int sa[1], sb[1];
+                            block_dots<1>(co.cb, qs_s[(q * 4 + jj) * 32 + lane], act + (bq + jj) * 2, sa);
+                            block_dots<1>(co.cb, qs_s[(q * 4 + jj + 1) * 32 + lane], act + (bq + jj + 1) * 2, sb);
+                            const float2 dx2 = *reinterpret_cast<const float2 *>(dxs + bq + jj);
+                            const float2 dw = jj == 0 ? dw01 : dw23;
+                            acc = scale_acc2(acc, dw, dx2, sa[0], sb[0]);
+                        }
                     }
-                }
-                if constexpr (kOne) {
-                    run = acc;
-                } else {
-                    float *dst = part + c * 32 + lane;
-                    *dst = (b0 == 0 ? 0.0f : *dst) + (acc.x + acc.y);
+                    if constexpr (kOne) {
+                        run = acc;
+                    } else {
+                        float *dst = part + c * 32 + lane;
+                        *dst = (b0 == 0 ? 0.0f : *dst) + (acc.x + acc.y);
+                    }
+                } else {  // columns c and c+1, one expansion
+                    const int off2[2] = {pick(col_off, c), pick(col_off, c + 1)};
+                    float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+                    for (int q = q0; q < q1; ++q) {
+                        const uint2 s = sc_s[q * 32 + lane];
+                        const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
+                        const float2 dw23 = __half22float2(*reinterpret_cast<const __half2 *>(&s.y));
+                        const int bq = b0 + q * 4;
+#pragma unroll
+                        for (int jj = 0; jj < 4; jj += 2) {
+                            int sa[2], sb[2];
+                            block_dots_cols<2>(co.cb, qs_s[(q * 4 + jj) * 32 + lane], act0, off2, bq + jj, sa);
+                            block_dots_cols<2>(co.cb, qs_s[(q * 4 + jj + 1) * 32 + lane], act0, off2, bq + jj + 1, sb);
+                            const float2 dw = jj == 0 ? dw01 : dw23;
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                const float2 dx2 = *reinterpret_cast<const float2 *>(dx0 + off2[i] + bq + jj);
+                                acc[i] = scale_acc2(acc[i], dw, dx2, sa[i], sb[i]);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        float *dst = part + (c + i) * 32 + lane;
+                        *dst = (b0 == 0 ? 0.0f : *dst) + (acc[i].x + acc[i].y);
+                    }
                 }
             }
         }
@@ -291,12 +321,61 @@ __device__ __forceinline__ void group_cols_impl(Consumer &co, const Pipe &P, int
     if constexpr (kOne) part[lane] = run.x + run.y;
 }
 
-// ncols == 1 (the common case: one token per expert) gets its own copy of the
-// loop with the column count known at compile time.
+// NC columns in one sweep: each 32-block index word is expanded once and its
+// levels dotted with every column (as the dense kernel does), the running sums
+// kept in registers over the whole pass and stored once at its end.  Used for
+// two columns (more would not fit the layer kernel's 96 registers).
+template <int NC>
+__device__ __forceinline__ void group_cols_n(Consumer &co, const Pipe &P, int nbp, const uint4 *act0,
+                                             const float *dx0, const int (&col_off)[kMaxCols], float *part, int warp,
+                                             int lane) {
+    float2 acc[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
+    for (int b0 = 0; b0 < nbp; b0 += kChunkBlocks) {
+        const int nq = min(kChunkBlocks, nbp - b0) / 4;
+        const uint32_t slot = co.slot;
+        const bool ok = pipe_wait(P, P.full + slot, co.phase, true);
+        if (ok) {
+            const unsigned char *st = P.ring + (size_t)slot * kStageBytes;
+            const uint4 *qs_s = reinterpret_cast<const uint4 *>(st);
+            const uint2 *sc_s = reinterpret_cast<const uint2 *>(st + kStageQsBytes);
+            const int q0 = (int)((unsigned)(warp * nq) / kConsumerWarps);
+            const int q1 = (int)((unsigned)((warp + 1) * nq) / kConsumerWarps);
+            for (int q = q0; q < q1; ++q) {
+                const uint2 s = sc_s[q * 32 + lane];
+                const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
+                const float2 dw23 = __half22float2(*reinterpret_cast<const __half2 *>(&s.y));
+                const int bq = b0 + q * 4;
+#pragma unroll
+                for (int jj = 0; jj < 4; jj += 2) {  // blocks in pairs: fewer live sums
+                    int sa[NC], sb[NC];
+                    block_dots_cols<NC>(co.cb, qs_s[(q * 4 + jj) * 32 + lane], act0, col_off, bq + jj, sa);
+                    block_dots_cols<NC>(co.cb, qs_s[(q * 4 + jj + 1) * 32 + lane], act0, col_off, bq + jj + 1, sb);
+                    const float2 dw = jj == 0 ? dw01 : dw23;
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        const float2 dx2 = *reinterpret_cast<const float2 *>(dx0 + col_off[c] + bq + jj);
+                        acc[c] = scale_acc2(acc[c], dw, dx2, sa[c], sb[c]);
+                    }
+                }
+            }
+        }
+        mbar_arrive(P.empty + slot);  // every consumer thread, after its own reads
+        co.advance(P);
+    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) part[c * 32 + lane] = acc[c].x + acc[c].y;
+}
+
+// One column, two columns (one shared expansion, sums in registers over the
+// pass) and three or more (pairs per stage) each get their own loop.
 __device__ __forceinline__ void group_cols(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
                                            const int (&col_off)[kMaxCols], int ncols, float *part, int warp, int lane) {
     if (ncols == 1)
         group_cols_impl<true>(co, P, nbp, act0, dx0, col_off, 1, part, warp, lane);
+    else if (ncols == 2)
+        group_cols_n<2>(co, P, nbp, act0, dx0, col_off, part, warp, lane);
     else
         group_cols_impl<false>(co, P, nbp, act0, dx0, col_off, ncols, part, warp, lane);
 }
