@@ -53,10 +53,10 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure
 # one ncu capture of each kernel (summaries in profiles/), valid only for the
 # kernel sources they were taken on (digest below); otherwise reported as null.
 PROFILED = {
-    "source_digest": "6f39703d766c66fd",
-    "k_matvec<5> (head)": 297_925_376 + 5_142_272,          # one launch, 129280 x 4096, n=5
+    "source_digest": "b2cdcff04e9c4cab",
+    "k_matvec<5> (head)": 297_926_912 + 5_238_784,          # one launch, 129280 x 4096, n=5
     # one layer call (k_quantize + k_moe + k_moe_combine) with 28 distinct experts
-    "moe call per expert": (97_792 + 396_585_216 + 3_563_776 + 673_280) / 28,
+    "moe call per expert": (97_536 + 396_610_048 + 3_514_880 + 673_536) / 28,
 }
 
 
