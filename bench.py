@@ -94,6 +94,9 @@ def parse():
                     help="profile mode only: the whole step, the MoE layer alone at batch 1 (top-4) "
                          "or batch 5 (top-8), or the 4096x4096 dense projection at n=1 (cbq_matvec over "
                          "16 weight copies, more than L2)")
+    ap.add_argument("--shared", action="store_true",
+                    help="profile mode, b1/b5 cases: give the layer a shared expert (one more expert of the "
+                         "routed shape that every token passes through)")
     ap.add_argument("--experts", type=int, default=E,
                     help="experts in the layer (default 256); smaller layers keep profiler captures small")
     return ap.parse_args()
@@ -376,6 +379,9 @@ def run_gpu(args):
         return
     if args.profile and args.case != "step":
         L = build_layer(torch, cbq, n_exp, with_head=False)
+        if args.shared:
+            cbq.cbq_moe_set_shared(L, synth.weight_blocks(2 * F, H, stream=synth.S_GATE_UP * 1000 + 999),
+                                   synth.weight_blocks(H, F, stream=synth.S_DOWN * 1000 + 999))
         n_tok, k = (1, 4) if args.case == "b1" else (N_TOK, TOPK)
         tabs = []
         for i in range(N_SETS):
@@ -394,7 +400,7 @@ def run_gpu(args):
             cbq.cbq_moe_matvec(L, t[2], t[0], t[1], y=yl)
         a1.record()
         torch.cuda.synchronize()
-        print(json.dumps({"profile": True, "case": args.case, "experts": n_exp,
+        print(json.dumps({"profile": True, "case": args.case, "experts": n_exp, "shared_expert": args.shared,
                           "us_per_layer": 1e3 * a0.elapsed_time(a1) / args.steps,
                           "device_error": cbq.cbq_get_device_error()}), flush=True)
         return
