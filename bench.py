@@ -198,6 +198,12 @@ def oracle_units(sets):
     return units, desc
 
 
+def units_per_step(per_unit_s, n_steps, n_units):
+    """Sample units per reference step so that n_steps steps take about
+    REFERENCE_BUDGET_S: at least one unit, at most the whole sample."""
+    return int(max(1, min(n_units, REFERENCE_BUDGET_S / max(n_steps, 1) / per_unit_s)))
+
+
 def run_reference(args):
     """The CPU oracle on the arm's workload: each step runs the next n of the
     16 sample units (round robin), n chosen from one untimed pass over all of
@@ -211,7 +217,7 @@ def run_reference(args):
     for _, call in units:  # calibration pass, untimed
         call()
     per_unit = (time.perf_counter() - t0) / len(units)
-    n = int(max(1, min(len(units), REFERENCE_BUDGET_S / max(args.warmup + args.steps, 1) / per_unit)))
+    n = units_per_step(per_unit, args.warmup + args.steps, len(units))
     nbytes, times, k = 0, [], 0
     for step in range(args.warmup + args.steps):
         b = 0
