@@ -49,6 +49,14 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.cbq_weights_destroy(None) == EINVAL
     assert lib.cbq_moe_destroy(None) == EINVAL
     assert lib.cbq_get_device_error(None) == EINVAL
+    assert lib.cbq_moe_set_shared(None, dummy, dummy, 0, None) == EINVAL
+    assert lib.cbq_moe_set_shared(None, None, None, 0, None) == EINVAL
+    assert lib.cbq_router_topk(None, 1, 8, 2, dummy, dummy, None) == EINVAL
+    assert lib.cbq_router_topk(dummy, 1, 0, 1, dummy, dummy, None) == EINVAL                      # E < 1
+    assert lib.cbq_router_topk(dummy, 1, 4, 5, dummy, dummy, None) == EINVAL                      # topk > E
+    assert lib.cbq_router_topk(dummy, 1, cbq.CBQ_ROUTER_MAX_E + 1, 2, dummy, dummy, None) == EINVAL
+    assert lib.cbq_router_topk(dummy, 0, 8, 2, dummy, dummy, None) == EINVAL                      # no token
+    assert lib.cbq_moe_matvec_logits(None, dummy, 1, dummy, 2, 1, dummy, None) == EINVAL
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
