@@ -6,8 +6,9 @@
 //   k_matvec<NC,F32>  dense MMVQ over NC <= 5 columns, one pass over the weights
 //                     (F32: one fp32 column, quantized inside the kernel)
 //   k_block_dots<NC>  the same integer path, exporting every per-block dot
-//   k_moe             routed experts, one kernel per layer call: gate+up rows,
-//                     SwiGLU split, requantization, then down rows per slot
+//   k_moe             routed experts (and an optional shared expert), one
+//                     kernel per layer call: gate+up rows, SwiGLU split,
+//                     requantization, then down rows per slot
 //   k_moe_combine     router-weighted combine of the per-slot down outputs
 //   k_router_topk     top-k expert ids and softmax weights from router logits
 //
