@@ -206,9 +206,11 @@ class Moe:
     def set_shared(self, gate_up, down, stream=None):
         """cbq_moe_set_shared: a shared expert of the layer's shapes (blocks of
         one gate_up 2F x H and one down H x F), or None, None to remove it."""
+        if (gate_up is None) != (down is None):
+            raise ValueError("pass both gate_up and down blocks, or neither to remove the shared expert")
         torch = _torch()
         lib = load()
-        if gate_up is None and down is None:
+        if gate_up is None:
             _check(lib.cbq_moe_set_shared(self.handle, None, None, 0, _stream(stream)), "cbq_moe_set_shared")
             self.shared = False
             return
