@@ -381,7 +381,7 @@ def run_gpu(args):
         a1.record()
         torch.cuda.synchronize()
         print(json.dumps({"profile": True, "case": args.case, "us_per_call": 1e3 * a0.elapsed_time(a1) / args.steps,
-                          "device_error": cbq.cbq_get_device_error()}), flush=True)
+                          "device_error": max(cbq.cbq_weights_get_error(w) for w in Ws)}), flush=True)
         return
     if args.profile and args.case != "step":
         L = build_layer(torch, cbq, n_exp, with_head=False)
@@ -408,7 +408,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile": True, "case": args.case, "experts": n_exp, "shared_expert": args.shared,
                           "us_per_layer": 1e3 * a0.elapsed_time(a1) / args.steps,
-                          "device_error": cbq.cbq_get_device_error()}), flush=True)
+                          "device_error": cbq.cbq_moe_get_error(L)}), flush=True)
         return
     L, head = build_layer(torch, cbq, n_exp)
     sets = routing_sets(n_exp=n_exp)
@@ -463,7 +463,7 @@ def run_gpu(args):
     wbytes = [distinct[i % N_SETS] * EXPERT_BYTES + HEAD_BYTES for i in timed]
     k_moe = [ev[i][0].elapsed_time(ev[i][1]) for i in timed]
     k_head = [ev[i][1].elapsed_time(ev[i][2]) for i in timed]
-    err = cbq.cbq_get_device_error()
+    err = cbq.cbq_moe_get_error(L) | cbq.cbq_weights_get_error(head)
 
     # per-launch algorithmic bytes: weights + activations read + outputs written
     slots = N_TOK * TOPK

@@ -59,7 +59,15 @@
  *     waits for it with griddepcontrol.wait before it lets the call's next
  *     kernel start), so results are those of plain stream order, also after
  *     a caller's kernel that signals its dependents early;
- *   - no call allocates or frees memory except *_create / *_destroy.
+ *   - no call allocates or frees device memory except *_create, *_destroy
+ *     and cbq_moe_set_shared (which allocates the shared expert's weights the
+ *     first time, frees them on removal, and uses a temporary device buffer
+ *     for host blocks);
+ *   - errors found by a kernel while it runs (an expert id out of range, a
+ *     bounded wait that gave up) set bits in an error word that belongs to
+ *     the handle; cbq_weights_get_error / cbq_moe_get_error read and clear it
+ *     in the order of a stream.  Outputs of a call that set a *_TIMEOUT bit
+ *     are undefined.
  */
 #ifndef CBQ_H
 #define CBQ_H
@@ -84,8 +92,11 @@ typedef enum {
     CBQ_EDEVICE = -4   /* no usable sm_103 device */
 } cbq_status;
 
-/* Bits of the device error word (cbq_get_device_error). */
-#define CBQ_DEVERR_BAD_EXPERT_ID 0x1u /* an id outside [0,E): that slot was skipped */
+/* Bits of a handle's error word (cbq_weights_get_error, cbq_moe_get_error). */
+#define CBQ_DEVERR_BAD_EXPERT_ID 0x1u          /* an id outside [0,E): that slot was skipped */
+#define CBQ_DEVERR_PIPE_TIMEOUT 0x100u         /* a weight-stream wait gave up after 1 s */
+#define CBQ_DEVERR_DEPENDENCY_TIMEOUT 0x200u   /* a down-projection item gave up waiting 1 s for its
+                                                  expert's intermediate; its outputs were not written */
 
 typedef struct cbq_weights cbq_weights; /* one dense M x K matrix, repacked on device */
 typedef struct cbq_moe cbq_moe;         /* E experts: gate_up (2F x H) and down (H x F) */
@@ -257,9 +268,15 @@ int cbq_moe_set_stage_events(cbq_moe *L, void *ev_layer, void *ev_combine, void 
  *     part it reads, so no contents carry over from the previous call. */
 int cbq_matvec_static(const cbq_weights *W, const float *x_dev, int n, float *y_dev, void *stream);
 
-/* Reads and clears the device error word of the current device (bits
- * CBQ_DEVERR_*).  Synchronizes the device. */
-int cbq_get_device_error(unsigned int *code);
+/* Read the error word of a handle (bits CBQ_DEVERR_*: every error of the
+ * handle's calls since the last read) into *code and clear it.  The copy and
+ * the clear are enqueued on `stream`, which is then synchronized (no other
+ * stream or device-wide synchronization): calls enqueued on `stream` before
+ * this one are covered, and a call on another stream is covered once it is
+ * ordered before `stream` (an event, or a synchronization).  Errors: EINVAL
+ * (null), ECUDA. */
+int cbq_weights_get_error(const cbq_weights *W, void *stream, unsigned int *code);
+int cbq_moe_get_error(const cbq_moe *L, void *stream, unsigned int *code);
 
 /* ---- checking entry points (used by the parity tests) ---------------- */
 
@@ -277,6 +294,15 @@ int cbq_moe_debug_block_dots(const cbq_moe *L, int e, int which, const int8_t *q
 /* Keep (1) or stop keeping (0) the fp32 intermediate a of each slot in the
  * workspace during cbq_moe_matvec (costs 4*F bytes of writes per slot). */
 int cbq_moe_set_debug(cbq_moe *L, int keep_intermediate);
+
+/* Give-up test mode of the layer kernel, for the tests of its bounded waits
+ * (0 turns it off): mode 1 makes every down-projection item wait for an
+ * intermediate count that is never reached, so that wait gives up after its
+ * 1 s limit (CBQ_DEVERR_DEPENDENCY_TIMEOUT) and the CTA stops; mode 2 makes
+ * the first CTA's first weight stage never arrive, so its consumers' wait
+ * gives up (CBQ_DEVERR_PIPE_TIMEOUT).  A call in either mode returns after
+ * a few seconds with undefined outputs and leaves the handle usable. */
+int cbq_moe_debug_stall(cbq_moe *L, int mode);
 
 /* Copy the intermediate of the last cbq_moe_matvec on this handle, for
  * slots p < nslots (at most CBQ_MAX_TOKENS * (CBQ_MAX_TOPK + 1)): routed

@@ -48,7 +48,11 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.cbq_moe_matvec(None, dummy, 1, dummy, dummy, 1, 1, dummy, None) == EINVAL
     assert lib.cbq_weights_destroy(None) == EINVAL
     assert lib.cbq_moe_destroy(None) == EINVAL
-    assert lib.cbq_get_device_error(None) == EINVAL
+    assert lib.cbq_weights_get_error(None, None, ctypes.byref(ctypes.c_uint())) == EINVAL
+    assert lib.cbq_moe_get_error(None, None, ctypes.byref(ctypes.c_uint())) == EINVAL
+    assert lib.cbq_weights_get_error(dummy, None, None) == EINVAL                            # no output word
+    assert lib.cbq_moe_get_error(dummy, None, None) == EINVAL
+    assert lib.cbq_moe_debug_stall(None, 1) == EINVAL
     assert lib.cbq_moe_set_shared(None, dummy, dummy, 0, None) == EINVAL
     assert lib.cbq_moe_set_shared(None, None, None, 0, None) == EINVAL
     assert lib.cbq_router_topk(None, 1, 8, 2, dummy, dummy, None) == EINVAL

@@ -87,6 +87,7 @@ def _check_matvec(torch, W, M, K, x, rows=None):
     yr = O.matvec_q(W, M, K, qx, dx, rows=rows)
     b = O.matvec_bound(W, M, K, qx, dx, rows=rows)
     assert_within_bound(y if rows is None else y[:, rows], yr, b)
+    assert cbq.cbq_weights_get_error(Wh) == 0
     return Wh, y
 
 
@@ -172,11 +173,6 @@ def test_output_head_sampled_bench_shape(torch):
     _check_matvec(torch, W, M, K, x, rows=rows)
 
 
-def test_no_device_error_left(torch):
-    """No kernel of this module recorded a pipeline timeout or a bad id."""
-    assert cbq.cbq_get_device_error() == 0
-
-
 def test_largest_k_accepted_and_correct(torch):
     """K = 26,368 (824 blocks: the most the 5-column staging fits beside the
     weight ring in 227 KB), ragged M, a partial last stage."""
@@ -223,4 +219,4 @@ def test_back_to_back_calls_on_one_handle(torch, n):
     torch.cuda.synchronize()
     for i, y in enumerate(ys):
         np.testing.assert_array_equal(y.cpu().numpy(), ref[i % 4])
-    assert cbq.cbq_get_device_error() == 0
+    assert cbq.cbq_weights_get_error(Wh) == 0

@@ -40,7 +40,7 @@ def _check_layer(torch, L, gu, dn, E, H, F, h, ids, wts, swiglu, expect_bad=0, s
     g.check()
     a_g, qa_g, da_g = (t.cpu().numpy() for t in
                        cbq.cbq_moe_debug_intermediate(L, N + (n_tok if shared is not None else 0)))
-    err = cbq.cbq_get_device_error()
+    err = cbq.cbq_moe_get_error(L)
     assert err == (cbq.CBQ_DEVERR_BAD_EXPERT_ID if expect_bad else 0)
     if shared is not None:
         sgu, sdn = shared
@@ -144,8 +144,8 @@ def test_nothing_routed_gives_zero(torch, small):
     wts = np.ones((2, 2), dtype=np.float32)
     y = cbq.cbq_moe_matvec(L, _dev(torch, h), _dev(torch, ids), _dev(torch, wts)).cpu().numpy()
     assert np.all(y == 0)
-    assert cbq.cbq_get_device_error() == cbq.CBQ_DEVERR_BAD_EXPERT_ID
-    assert cbq.cbq_get_device_error() == 0  # read clears
+    assert cbq.cbq_moe_get_error(L) == cbq.CBQ_DEVERR_BAD_EXPERT_ID
+    assert cbq.cbq_moe_get_error(L) == 0  # read clears
 
 
 def test_host_entry_matches(torch, small):
@@ -313,7 +313,7 @@ def test_back_to_back_layer_calls(torch, small, n_tok, k):
     torch.cuda.synchronize()
     for i, y in enumerate(ys):
         np.testing.assert_array_equal(y.cpu().numpy(), y_lg if i % 4 == 3 else ref[i % 3])
-    assert cbq.cbq_get_device_error() == 0
+    assert cbq.cbq_moe_get_error(L) == 0
 
 
 # ----------------------------------------------------------- shared expert -
@@ -456,4 +456,4 @@ def test_inputs_written_just_before_the_call(torch, small, n_tok, k):
     torch.cuda.synchronize()
     for i, y in enumerate(ys):
         np.testing.assert_array_equal(y.cpu().numpy(), ref[i % 4])
-    assert cbq.cbq_get_device_error() == 0
+    assert cbq.cbq_moe_get_error(L) == 0

@@ -24,6 +24,8 @@ CBQ_MAX_COLS = 5
 CBQ_MAX_TOKENS = 5
 CBQ_MAX_TOPK = 16
 CBQ_DEVERR_BAD_EXPERT_ID = 0x1
+CBQ_DEVERR_PIPE_TIMEOUT = 0x100
+CBQ_DEVERR_DEPENDENCY_TIMEOUT = 0x200
 CBQ_STATIC_SCRATCH_MAX_K = 16384
 CBQ_ROUTER_MAX_E = 16384
 
@@ -49,7 +51,9 @@ _SIGS = {
     "cbq_moe_matvec_host": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
     "cbq_router_topk": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "cbq_moe_matvec_logits": ([_P, _P, _I, _P, _I, _I, _P, _P], _I),
-    "cbq_get_device_error": ([ctypes.POINTER(ctypes.c_uint)], _I),
+    "cbq_weights_get_error": ([_P, _P, ctypes.POINTER(ctypes.c_uint)], _I),
+    "cbq_moe_get_error": ([_P, _P, ctypes.POINTER(ctypes.c_uint)], _I),
+    "cbq_moe_debug_stall": ([_P, _I], _I),
     "cbq_debug_block_dots": ([_P, _P, _I, _P, _P], _I),
     "cbq_moe_debug_block_dots": ([_P, _I, _I, _P, _I, _P, _P], _I),
     "cbq_moe_set_debug": ([_P, _I], _I),
@@ -364,10 +368,25 @@ def cbq_moe_matvec_host(L: Moe, h: np.ndarray, ids: np.ndarray, wts: np.ndarray,
     return y
 
 
-def cbq_get_device_error() -> int:
+def cbq_weights_get_error(W: Weights, stream=None) -> int:
+    """Read and clear W's error word (CBQ_DEVERR_* bits) in the order of the
+    stream (default: torch's current stream), then wait for that stream."""
     code = ctypes.c_uint()
-    _check(load().cbq_get_device_error(ctypes.byref(code)), "cbq_get_device_error")
+    _check(load().cbq_weights_get_error(W.handle, _stream(stream), ctypes.byref(code)), "cbq_weights_get_error")
     return code.value
+
+
+def cbq_moe_get_error(L: Moe, stream=None) -> int:
+    """Read and clear L's error word (CBQ_DEVERR_* bits) in stream order."""
+    code = ctypes.c_uint()
+    _check(load().cbq_moe_get_error(L.handle, _stream(stream), ctypes.byref(code)), "cbq_moe_get_error")
+    return code.value
+
+
+def cbq_moe_debug_stall(L: Moe, mode: int):
+    """Give-up test mode of the layer kernel (0 off; 1 a dependency never met;
+    2 a weight stage never filled)."""
+    _check(load().cbq_moe_debug_stall(L.handle, int(mode)), "cbq_moe_debug_stall")
 
 
 def cbq_debug_block_dots(W: Weights, qx, s=None, stream=None):

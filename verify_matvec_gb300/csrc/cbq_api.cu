@@ -24,6 +24,7 @@ struct cbq_weights {
     uint4 *qs;
     uint2 *sc;
     unsigned *sched; // work counters of the matvec kernel
+    unsigned *err;   // the handle's error word
     int8_t *ws_qx;   // CBQ_MAX_COLS x K
     float *ws_dx;    // CBQ_MAX_COLS x K/32
     float *st_x;     // host-entry staging: CBQ_MAX_COLS x K fp32
@@ -168,6 +169,7 @@ int cbq_weights_destroy(cbq_weights *W) {
     cudaFree(W->qs);
     cudaFree(W->sc);
     cudaFree(W->sched);
+    cudaFree(W->err);
     cudaFree(W->ws_qx);
     cudaFree(W->ws_dx);
     cudaFree(W->st_x);
@@ -190,6 +192,8 @@ int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device, 
     CBQ_CUDA(cbq::device_smem_limit(&smem_max));
     if (cbq::matvec_smem_bytes(nbp, CBQ_MAX_COLS) > smem_max) return CBQ_EINVAL;
 
+    const int G = (int)((M + 31) / 32);
+
     cbq_weights *W = new (std::nothrow) cbq_weights();
     if (!W) return CBQ_ENOMEM;
     W->device = dev;
@@ -197,6 +201,7 @@ int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device, 
     if ((rc = dev_alloc(&W->qs, cbq::qs_elems(M, nb), &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->sc, cbq::sc_elems(M, nb), &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->sched, 2, &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->err, 1, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->ws_qx, (size_t)CBQ_MAX_COLS * K, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->ws_dx, (size_t)CBQ_MAX_COLS * nb, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->st_x, (size_t)CBQ_MAX_COLS * K, &W->bytes)) != CBQ_OK ||
@@ -204,7 +209,8 @@ int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device, 
         cbq_weights_destroy(W);
         return rc;
     }
-    if (cudaMemsetAsync(W->sched, 0, 2 * sizeof(unsigned), as_stream(stream)) != cudaSuccess) {
+    if (cudaMemsetAsync(W->sched, 0, 2 * sizeof(unsigned), as_stream(stream)) != cudaSuccess ||
+        cudaMemsetAsync(W->err, 0, sizeof(unsigned), as_stream(stream)) != cudaSuccess) {
         cbq_weights_destroy(W);
         return CBQ_ECUDA;
     }
@@ -218,8 +224,9 @@ int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device, 
     W->mat.M = M;
     W->mat.nb = nb;
     W->mat.nbp = nbp;
-    W->mat.G = (int)((M + 31) / 32);
+    W->mat.G = G;
     W->mat.sched = W->sched;
+    W->mat.err = W->err;
     *out = W;
     return CBQ_OK;
 }
@@ -367,6 +374,7 @@ int cbq_moe_destroy(cbq_moe *L) {
     cudaFree(L->ws.obuf);
     cudaFree(L->ws.sched);
     cudaFree(L->ws.done);
+    cudaFree(L->ws.err);
     cudaFree(L->st_h);
     cudaFree(L->st_ids);
     cudaFree(L->st_wts);
@@ -388,7 +396,7 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
     const int nbH = (int)(H / CBQ_QK), nbF = (int)(F / CBQ_QK);
     size_t smem_max = 0;
     CBQ_CUDA(cbq::moe_smem_limit(&smem_max));
-    if (cbq::moe_smem_bytes(std::max(CBQ_MAX_TOKENS * cbq::round_up4(nbH), CBQ_MAX_COLS * cbq::round_up4(nbF))) >
+    if (cbq::moe_smem_bytes(std::max(CBQ_MAX_TOKENS * cbq::round_up4(nbH), CBQ_MAX_COLS * cbq::round_up4(nbF)), 3) >
         smem_max)
         return CBQ_EINVAL;
 
@@ -410,6 +418,7 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
         (rc = dev_alloc(&L->ws.obuf, slots * H, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.sched, 4, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.done, slots, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.err, 1, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_h, (size_t)CBQ_MAX_TOKENS * H, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_ids, slots, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_wts, slots, &L->bytes)) != CBQ_OK ||
@@ -419,7 +428,8 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
     }
     cudaStream_t s = as_stream(stream);
     if (cudaMemsetAsync(L->ws.sched, 0, 4 * sizeof(unsigned), s) != cudaSuccess ||
-        cudaMemsetAsync(L->ws.done, 0, slots * sizeof(unsigned), s) != cudaSuccess) {
+        cudaMemsetAsync(L->ws.done, 0, slots * sizeof(unsigned), s) != cudaSuccess ||
+        cudaMemsetAsync(L->ws.err, 0, sizeof(unsigned), s) != cudaSuccess) {
         cbq_moe_destroy(L);
         return CBQ_ECUDA;
     }
@@ -580,6 +590,7 @@ int cbq_moe_debug_block_dots(const cbq_moe *L, int e, int which, const int8_t *q
     m.nbp = cbq::round_up4(m.nb);
     m.G = (int)((m.M + 31) / 32);
     m.sched = nullptr;  // the block-dot kernel uses static ranges
+    m.err = L->ws.err;
     CBQ_CUDA(cbq::launch_block_dots(m, qx_dev, n, s_dev, as_stream(stream)));
     return CBQ_OK;
 }
@@ -615,9 +626,35 @@ int cbq_moe_debug_intermediate(const cbq_moe *L, int nslots, float *a_dev, int8_
     return CBQ_OK;
 }
 
-int cbq_get_device_error(unsigned int *code) {
-    if (!code) return CBQ_EINVAL;
-    CBQ_CUDA(cbq::read_and_clear_device_error(code));
+namespace {
+
+// Copy a handle's error word to *code and clear it, both in the order of
+// `stream`, then wait for that stream only.
+int read_and_clear(unsigned *err, int device, void *stream, unsigned *code) {
+    DeviceScope scope(device);
+    CBQ_CUDA(scope.status());
+    cudaStream_t s = as_stream(stream);
+    CBQ_CUDA(cudaMemcpyAsync(code, err, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
+    CBQ_CUDA(cudaMemsetAsync(err, 0, sizeof(unsigned), s));
+    CBQ_CUDA(cudaStreamSynchronize(s));
+    return CBQ_OK;
+}
+
+}  // namespace
+
+int cbq_weights_get_error(const cbq_weights *W, void *stream, unsigned int *code) {
+    if (!W || !code) return CBQ_EINVAL;
+    return read_and_clear(W->err, W->device, stream, code);
+}
+
+int cbq_moe_get_error(const cbq_moe *L, void *stream, unsigned int *code) {
+    if (!L || !code) return CBQ_EINVAL;
+    return read_and_clear(L->ws.err, L->device, stream, code);
+}
+
+int cbq_moe_debug_stall(cbq_moe *L, int mode) {
+    if (!L || mode < 0 || mode > 2) return CBQ_EINVAL;
+    L->ws.stall = mode;
     return CBQ_OK;
 }
 

@@ -36,35 +36,37 @@ constexpr uint32_t kCb3 = 0x71594535u;
 constexpr uint32_t kCbP0 = 0x271A0E02u;
 constexpr uint32_t kCbP1 = 0x725A4636u;
 
-// The codebook words held in registers for the whole kernel.  Produced by
-// opaque moves so the compiler keeps them in registers instead of
-// re-materialising the immediates before every permute.
+// The codebook words and the dp4a seed (kMagicBits, below), held in registers
+// for a whole kernel.  They are read from shared memory, where thread 0 wrote
+// them at kernel start: built from immediates, the assembler would rebuild
+// each one into a register before every permute and dp4a that uses it (about
+// 13 extra instructions per 32-weight block, measured with per-pipe counters).
 struct Codebook {
     uint32_t t0, t1, t2, t3, p0, p1;
+    int seed;
 };
-
-__device__ __forceinline__ uint32_t opaque(uint32_t v) {
-    uint32_t r;
-    asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
-    return r;
-}
-
-__device__ __forceinline__ Codebook load_codebook() {
-    Codebook cb;
-    cb.t0 = opaque(kCb0);
-    cb.t1 = opaque(kCb1);
-    cb.t2 = opaque(kCb2);
-    cb.t3 = opaque(kCb3);
-    cb.p0 = opaque(kCbP0);
-    cb.p1 = opaque(kCbP1);
-    return cb;
-}
 
 // float(s) for |s| < 2^22 without an int->float conversion: the dp4a chain
 // starts from the bit pattern of 1.5*2^23, so the integer sum s lands in the
 // mantissa; subtracting 1.5*2^23 in fp32 is exact.
 constexpr int kMagicBits = 0x4B400000;
 constexpr float kMagic = 12582912.0f;
+
+// Shared-memory words of the codebook and seed (Codebook); write_consts by one
+// thread, then a barrier, then read_consts by every thread that needs them.
+__device__ __forceinline__ void write_consts(uint32_t *s) {
+    s[0] = kCb0;
+    s[1] = kCb1;
+    s[2] = kCb2;
+    s[3] = kCb3;
+    s[4] = kCbP0;
+    s[5] = kCbP1;
+    s[6] = (uint32_t)kMagicBits;
+}
+
+__device__ __forceinline__ Codebook read_consts(const uint32_t *s) {
+    return Codebook{s[0], s[1], s[2], s[3], s[4], s[5], (int)s[6]};
+}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
@@ -156,7 +158,7 @@ __device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, co
         for (int c = 0; c < NC; ++c) {
             const uint4 a0 = actb[2 * c], a1 = actb[2 * c + 1];
             const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            int s = kMagicBits;  // one chain over the lower- and upper-table parts
+            int s = cb.seed;  // one chain over the lower- and upper-table parts
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 s = __dp4a((int)lo[i], (int)av[i], s);
@@ -172,7 +174,7 @@ __device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, co
         for (int c = 0; c < NC; ++c) {
             const uint4 a0 = actb[2 * c], a1 = actb[2 * c + 1];
             const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            int s = kMagicBits;
+            int s = cb.seed;
 #pragma unroll
             for (int i = 0; i < 8; ++i) s = __dp4a((int)e[i], (int)av[i], s);
             sdot[c] = s;
@@ -180,26 +182,59 @@ __device__ __forceinline__ void block_dots(const Codebook &cb, const uint4 w, co
     }
 }
 
-// The same dots (NC >= 2, shared expansion) with column c's two words at
-// act0[2*(off[c] + b)] and [+1]: the routed-expert kernel stages its columns
-// one after another, not block-major.
-template <int NC, int M>
-__device__ __forceinline__ void block_dots_cols(const Codebook &cb, const uint4 w, const uint4 *act0,
-                                                const int (&off)[M], int b, int sdot[NC]) {
-    static_assert(NC <= M, "a column offset for every column");
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    uint32_t e[8];
+// One column, two rows: the dots (offset by the seed) of index blocks wa
+// (row set 0) and wb (row set 1) against the activation block at actb[0..1],
+// by the two-word expansion; the activation words are loaded once for both.
+__device__ __forceinline__ void block_dots_2rows(const Codebook &cb, const uint4 wa, const uint4 wb,
+                                                 const uint4 *actb, int &sa, int &sb) {
+    const uint4 a0 = actb[0], a1 = actb[1];
+    const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t wsa[4] = {wa.x, wa.y, wa.z, wa.w}, wsb[4] = {wb.x, wb.y, wb.z, wb.w};
+    int s0 = cb.seed, s1 = cb.seed;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) expand_select(cb, ws[m], e[2 * m], e[2 * m + 1]);
+    for (int m = 0; m < 4; ++m) {
+        uint32_t lo0, hi0, lo1, hi1;
+        expand_split(cb, wsa[m], lo0, hi0, lo1, hi1);
+        s0 = __dp4a((int)lo0, (int)av[2 * m], s0);
+        s0 = __dp4a((int)hi0, (int)av[2 * m], s0);
+        s0 = __dp4a((int)lo1, (int)av[2 * m + 1], s0);
+        s0 = __dp4a((int)hi1, (int)av[2 * m + 1], s0);
+        expand_split(cb, wsb[m], lo0, hi0, lo1, hi1);
+        s1 = __dp4a((int)lo0, (int)av[2 * m], s1);
+        s1 = __dp4a((int)hi0, (int)av[2 * m], s1);
+        s1 = __dp4a((int)lo1, (int)av[2 * m + 1], s1);
+        s1 = __dp4a((int)hi1, (int)av[2 * m + 1], s1);
+    }
+    sa = s0;
+    sb = s1;
+}
+
+// Two columns, two rows: index blocks wa (row set 0) and wb (row set 1), each
+// expanded once (exact bytes), dotted with block b of the columns staged at
+// offsets off[0], off[1] (their words at act0[2*(off[c] + b)] and [+1]).
+__device__ __forceinline__ void block_dots_2rows_cols2(const Codebook &cb, const uint4 wa, const uint4 wb,
+                                                       const uint4 *act0, const int (&off)[2], int b, int sa[2],
+                                                       int sb[2]) {
+    const uint32_t wsa[4] = {wa.x, wa.y, wa.z, wa.w}, wsb[4] = {wb.x, wb.y, wb.z, wb.w};
+    uint32_t ea[8], eb[8];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
+    for (int m = 0; m < 4; ++m) {
+        expand_select(cb, wsa[m], ea[2 * m], ea[2 * m + 1]);
+        expand_select(cb, wsb[m], eb[2 * m], eb[2 * m + 1]);
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
         const uint4 *a = act0 + 2 * (off[c] + b);
         const uint4 a0 = a[0], a1 = a[1];
         const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        int s = kMagicBits;
+        int s0 = cb.seed, s1 = cb.seed;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s = __dp4a((int)e[i], (int)av[i], s);
-        sdot[c] = s;
+        for (int i = 0; i < 8; ++i) {
+            s0 = __dp4a((int)ea[i], (int)av[i], s0);
+            s1 = __dp4a((int)eb[i], (int)av[i], s1);
+        }
+        sa[c] = s0;
+        sb[c] = s1;
     }
 }
 

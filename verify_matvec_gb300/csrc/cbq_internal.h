@@ -16,6 +16,7 @@ struct DevMat {
     int nbp;          // nb rounded up to a multiple of 4
     int G;            // ceil(M / 32) row groups
     unsigned *sched;  // 2 work counters of the matvec kernel (zero between launches)
+    unsigned *err;    // the handle's error word (CBQ_DEVERR_* bits)
 };
 
 inline int round_up4(int v) { return (v + 3) & ~3; }
@@ -51,7 +52,9 @@ struct MoeWork {
     float *obuf;      // slots x H, down-projection output per slot
     unsigned *sched;  // 4 work counters (items, producers done, CTAs done), zero between launches
     unsigned *done;   // per expert rank: gate_up columns published (zero between launches)
+    unsigned *err;    // the handle's error word (CBQ_DEVERR_* bits)
     int keep_a;
+    int stall;        // give-up test mode: 0 off, 1 a dependency never met, 2 a stage never filled
     cudaEvent_t ev[3];  // optional stage events (before the layer kernel, before the combine, after it)
 };
 
@@ -71,13 +74,12 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
                        const float *wts, int k, int swiglu, float *y, cudaStream_t s);
 // Largest dynamic shared memory a matvec over K columns with n columns needs.
 size_t matvec_smem_bytes(int nbp, int n);
-size_t moe_smem_bytes(int act_blocks);
+size_t moe_smem_bytes(int act_blocks, int stages);
 cudaError_t device_smem_limit(size_t *bytes);
 // Top-k expert ids and softmax weights per token from router logits (n_tok x E).
 cudaError_t launch_router_topk(const float *logits, int n_tok, int E, int k, int32_t *ids, float *wts,
                                cudaStream_t s);
 // Dynamic shared memory the layer kernel may use (opt-in limit less its static part).
 cudaError_t moe_smem_limit(size_t *bytes);
-cudaError_t read_and_clear_device_error(unsigned *code);
 
 }  // namespace cbq

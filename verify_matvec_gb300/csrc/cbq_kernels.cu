@@ -25,10 +25,6 @@
 #include <tuple>
 #include <utility>
 
-namespace cbq {
-__device__ unsigned int g_device_error;  // CBQ_DEVERR_* bits
-}  // namespace cbq
-
 #include "cbq_pipe.cuh"
 
 namespace cbq {
@@ -37,12 +33,13 @@ constexpr unsigned kErrBadExpertId = 0x1u;
 // Pipeline depth (stages of 18 KB per CTA, two CTAs per SM) and partial-sum
 // sets of each kernel, sized so two CTAs fit in an SM's shared memory.
 constexpr int kStages = 4;
-constexpr int kStagesMoe = 3;
 constexpr int kSetsMatvec = 2;   // double-buffered
-constexpr int kSetsMoe = 4;      // gate + up, double-buffered (down uses two of them)
+constexpr int kSetsMoe = 2;      // double-buffered, format B (two row sets)
 
-// Dynamic shared memory of the routed-expert kernel.
-size_t moe_smem_bytes(int act_blocks) { return pipe_smem_bytes(kStagesMoe, 1, act_blocks, kSetsMoe); }
+// Dynamic shared memory of the routed-expert kernel with S stages.
+size_t moe_smem_bytes(int act_blocks, int S) {
+    return pipe_smem_bytes(S, act_blocks, kSetsMoe * kPartSetB);
+}
 
 // Launch with optional programmatic stream serialization (PDL).
 template <typename... KArgs, typename... Args>
@@ -127,63 +124,80 @@ cudaError_t launch_quantize(const float *x, int64_t K, int n, int8_t *qx, float 
 
 // ---------------------------------------------------------- dense MMVQ -----
 
-size_t matvec_smem_bytes(int nbp, int n) { return pipe_smem_bytes(kStages, n, nbp, kSetsMatvec); }
+size_t matvec_smem_bytes(int nbp, int n) { return pipe_smem_bytes(kStages, n * nbp, kSetsMatvec * kPartSetA); }
 
 // Debug kernel smem: activations + scales only.
 static size_t dots_smem_bytes(int nbp, int n) { return (size_t)n * nbp * 36; }
 
-// Dense MMVQ: 32-row groups fetched dynamically, all NC columns per pass.
-// kF32: the consumers quantize the fp32 columns xf themselves while the
+struct MatvecArgs {
+    DevMat W;
+    const int8_t *qx;  // quantized columns (kF32 == false)
+    const float *dx;
+    const float *xf;   // fp32 column (kF32 == true)
+    int64_t K;
+    float *y;
+};
+
+// Dense MMVQ: 32-row groups fetched per CTA, all NC columns per pass.
+// kF32: the consumers quantize the fp32 column xf themselves while the
 // producer starts the weight stream (no quantization kernel before it);
 // otherwise they stage qx/dx written by the quantization kernel launched just
 // before (a programmatic dependency).
 template <int NC, bool kF32>
-__global__ void __launch_bounds__(kPipeThreads, 2)
-    k_matvec(const uint4 *__restrict__ qs, const uint2 *__restrict__ sc, int64_t M, int G, int nb, int nbp,
-             const int8_t *__restrict__ qx, const float *__restrict__ dx, const float *__restrict__ xf, int64_t K,
-             float *__restrict__ y, unsigned *__restrict__ sched) {
+__global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constant__ MatvecArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
-    if constexpr (kF32) pdl_wait();  // first kernel of its call: the previous work, x included, is done
-    pdl_trigger();  // the next call's first kernel may launch; it waits for this grid
-    const PipeSmem S = carve_pipe(smem, kStages, NC, nbp);
+    pdl_trigger();  // the next kernel may launch; it waits for this grid before touching what it writes
+    const DevMat &W = A.W;
+    const PipeSmem S = carve_pipe(smem, kStages, NC * W.nbp, W.err);
     pipe_init(S.pipe);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nbq = nbp / 4;
+    const int nbq = W.nbp / 4;
+    const unsigned total = (unsigned)W.G;
     if (warp == kConsumerWarps) {  // producer
         if (lane == 0) {
             Producer pr;
-            unsigned nxt = atomicAdd(sched, 1u);
-            while (nxt < (unsigned)G && !pr.stopped) {
-                const unsigned g = nxt;
-                nxt = atomicAdd(sched, 1u);
-                pr.group(S.pipe, qs + (size_t)g * nbp * 32, sc + (size_t)g * nbq * 32, nbp, (int)g);
+            // the first item is the CTA index (the grid never exceeds the item
+            // count): its weights stream before the wait for the work ahead of
+            // this kernel, which the work counter needs (a call still running
+            // on the handle owns it)
+            unsigned item = blockIdx.x;
+            pr.group_a(S.pipe, W.qs + (size_t)item * W.nbp * 32, W.sc + (size_t)item * nbq * 32, 0, W.nbp, (int)item);
+            pdl_wait();
+            unsigned next = gridDim.x + atomicAdd(W.sched, 1u);
+            while (next < total && !pr.stopped) {
+                item = next;
+                // the following item's index is fetched before this item's
+                // stages are issued, so the atomic's latency overlaps them
+                next = gridDim.x + atomicAdd(W.sched, 1u);
+                pr.group_a(S.pipe, W.qs + (size_t)item * W.nbp * 32, W.sc + (size_t)item * nbq * 32, 0, W.nbp,
+                           (int)item);
             }
             __threadfence();
-            sched_exit(sched);
+            sched_exit(W.sched);
             pr.finish(S.pipe);
             pr.drain(S.pipe);
         }
         return;
     }
+    pdl_wait();  // the activations belong to the work ahead
     if constexpr (kF32) {
-        quant_stage_cols<NC>(xf, K, nb, nbp, S.act, S.dx, threadIdx.x, kConsumers);
+        quant_stage_cols<NC>(A.xf, A.K, W.nb, W.nbp, S.act, S.dx, threadIdx.x, kConsumers);
     } else {
-        pdl_wait();  // the activations come from the kernel launched just before
-        ColSrc src{qx, dx, (size_t)K, (size_t)nb, {0, 1, 2, 3, 4}};
-        stage_cols(src, NC, nb, nbp, S.act, S.dx, threadIdx.x, kConsumers, false, true);
+        ColSrc src{A.qx, A.dx, (size_t)A.K, (size_t)W.nb, {0, 1, 2, 3, 4}};
+        stage_cols(src, NC, W.nb, W.nbp, S.act, S.dx, threadIdx.x, kConsumers, false, true);
     }
     consumer_sync();
     const float2 *dxp = reinterpret_cast<const float2 *>(S.dx);
-    Consumer co;
-    for (int item = 0;; ++item) {
-        const int g = co.peek(S.pipe);
-        if (g < 0) break;
+    Consumer co(S.pipe);
+    for (int n = 0;; ++n) {
+        const int it = co.next_item(S.pipe);
+        if (it < 0) break;
         float2 acc[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
-        co.group<NC>(S.pipe, nbp, S.act, dxp, acc, warp, lane);
-        float *part = S.part + (item & 1) * kPartSet;
+        sweep_a<NC>(co, S.pipe, 0, W.nbp, S.act, dxp, acc, warp, lane);
+        float *part = S.part + (n & 1) * kPartSetA;
 #pragma unroll
         for (int c = 0; c < NC; ++c) part[(warp * NC + c) * 32 + lane] = acc[c].x + acc[c].y;
         consumer_sync();
@@ -191,11 +205,12 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
             float v = 0.0f;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) v += part[(w * NC + warp) * 32 + lane];
-            const int64_t row = (int64_t)g * 32 + lane;
-            if (row < M) y[(size_t)warp * M + row] = v;
+            const int64_t row = (int64_t)it * 32 + lane;
+            if (row < W.M) A.y[(size_t)warp * W.M + row] = v;
         }
     }
 }
+
 
 template <int NC>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -213,10 +228,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         stage_cols(src, NC, nb, nbp, act_s, dx_s, threadIdx.x, blockDim.x, false, true);
     }
     __syncthreads();
+    __shared__ uint32_t consts[kConstWords];
+    if (threadIdx.x == 0) write_consts(consts);
+    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbq = nbp / 4;
     const int q0 = warp * nbq / kWarps, q1 = (warp + 1) * nbq / kWarps;
-    const Codebook cb = load_codebook();
+    const Codebook cb = read_consts(consts);
     for (int g = g0; g < g1; ++g) {
         const int64_t row = (int64_t)g * 32 + lane;
         for (int q = q0; q < q1; ++q) {
@@ -228,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 block_dots<NC>(cb, w, act_s + (size_t)b * NC * 2, sd);
                 if (row < M && b < nb) {
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) sdot[((size_t)c * M + row) * nb + b] = sd[c] - kMagicBits;
+                    for (int c = 0; c < NC; ++c) sdot[((size_t)c * M + row) * nb + b] = sd[c] - cb.seed;
                 }
             }
         }
@@ -328,8 +346,14 @@ static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const floa
     int grid = 0;
     cudaError_t e = dynamic_grid(k_matvec<NC, kF32>, smem, W.G, &grid);
     if (e != cudaSuccess) return e;
-    return launch_k(k_matvec<NC, kF32>, grid, kPipeThreads, smem, s, pdl, W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx,
-                    dx, xf, (int64_t)W.nb * kQK, y, W.sched);
+    MatvecArgs A;
+    A.W = W;
+    A.qx = qx;
+    A.dx = dx;
+    A.xf = xf;
+    A.K = (int64_t)W.nb * kQK;
+    A.y = y;
+    return launch_k(k_matvec<NC, kF32>, grid, kPipeThreads, smem, s, pdl, A);
 }
 
 cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, int n, float *y, cudaStream_t s,
@@ -382,8 +406,9 @@ struct MoeArgs {
     float *y;
     int n_tok, k, swiglu;
     int nbH, nbpH, nbF, nbpF;
-    int act_blocks;  // staged-activation capacity in blocks (tokens, then down columns)
+    int act_blocks;    // staged-activation capacity in blocks (tokens, then down columns)
     int quant_tokens;  // the consumers quantize h themselves (one token, h 16-byte aligned)
+    int stages;        // pipeline depth (3 or 4: as many as two CTAs per SM allow)
 };
 
 // Distinct in-range expert ids of the routing table, ascending but the shared
@@ -400,14 +425,14 @@ struct Routing {
     int D;
 };
 
-__device__ void route(const int32_t *__restrict__ ids, int N, int n_all, int E, Routing &R, bool report) {
+__device__ void route(const int32_t *__restrict__ ids, int N, int n_all, int E, Routing &R, unsigned *err) {
     const int t = threadIdx.x;
     if (t < n_all) {
         int e = E;  // a shared-expert slot
         if (t < N) {
             e = ids[t];
             if (e < 0 || e >= E) {
-                if (report) atomicOr(&g_device_error, kErrBadExpertId);
+                if (err) atomicOr(err, kErrBadExpertId);
                 e = -1;
             }
         }
@@ -496,8 +521,7 @@ __device__ __forceinline__ int expert_ns(const Routing &R, int u, int N) {
 __device__ __forceinline__ int col_chunks(int ns) { return (ns + kMaxCols - 1) / kMaxCols; }
 
 constexpr unsigned kErrDependencyTimeout = 0x200u;
-constexpr unsigned kDownGrab = 8;
-constexpr uint32_t kDependencyPolls = 1u << 22;
+constexpr unsigned kDownGrab = 4;
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     unsigned v;
@@ -505,79 +529,36 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     return v;
 }
 
-// Gate rows (first pass) and up rows (second pass) of one 32-row-pair group
-// over the whole K for the columns (slots) sl.sl[0..nc), then the
-// SwiGLU split and the requantization of the 32 outputs of each column.
-// Partial sets: gate sums in set 2*buf, up sums in set 2*buf+1, each
-// [warp][column][lane].  Each writer warp then publishes its column for expert
-// rank u (fence, then one count in done[u]).
-__device__ __forceinline__ void gate_up_item(const MoeArgs &A, const Slots &sl, const PipeSmem &S, Consumer &co,
-                                             int u, int g, int nc, int warp, int lane, int buf) {
-    int col_off[kMaxCols];  // activation column of each slot: its token's column
-#pragma unroll
-    for (int c = 0; c < kMaxCols; ++c)
-        col_off[c] = (c < nc ? slot_token(sl.sl[c], A.n_tok * A.k, A.k) : 0) * A.nbpH;
-    int p = sl.sl[0];  // the slot this warp writes (warp < nc), taken before the sweeps
-#pragma unroll
-    for (int cc = 1; cc < kMaxCols; ++cc)
-        if (warp == cc) p = sl.sl[cc];
-    float *pg = S.part + (2 * buf) * kPartSet;
-    float *pu = S.part + (2 * buf + 1) * kPartSet;
-    group_cols(co, S.pipe, A.nbpH, S.act, S.dx, col_off, nc, pg + warp * kMaxCols * 32, warp, lane);
-    group_cols(co, S.pipe, A.nbpH, S.act, S.dx, col_off, nc, pu + warp * kMaxCols * 32, warp, lane);
-    consumer_sync();
-    if (warp < nc) {
-        const int c = warp;
-        float gs = 0.0f, us = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            gs += pg[(w * kMaxCols + c) * 32 + lane];
-            us += pu[(w * kMaxCols + c) * 32 + lane];
-        }
-        const float a = A.swiglu ? gs / (1.0f + expf(-gs)) * us : gs * us;
-        float d;
-        const int8_t q = quant_lane(a, d);
-        const size_t o = (size_t)p * A.L.F + (size_t)g * 32 + lane;
-        A.ws.qa[o] = q;
-        if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
-        if (A.ws.keep_a) A.ws.a_dbg[o] = a;
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(A.ws.done + u, 1u);
+// Bounded wait (thread 0) for expert rank u's intermediate columns: all its
+// gate_up items published (done[u] == target).  On timeout it sets
+// kErrDependencyTimeout and the CTA's abort flag; it returns false then, or
+// at once when the CTA already gave up.
+__device__ __forceinline__ bool wait_dependency(const unsigned *done, unsigned target, const Pipe &P) {
+    if (ld_acquire(done) >= target) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (*(volatile int *)P.abort) return false;
+        __nanosleep(64);
+        if (ld_acquire(done) >= target) return true;
+        if (global_ns() - t0 > kWaitLimitNs) break;
     }
-}
-
-// Down rows of one 32-row group for the nc columns staged in S (slots
-// sl.sl[0..nc)), written per slot to obuf by warps 0..nc-1 after one CTA
-// barrier.
-__device__ __forceinline__ void down_item(const MoeArgs &A, const Slots &sl, const PipeSmem &S, Consumer &co,
-                                          int g, int nc, int warp, int lane, int buf) {
-    int col_off[kMaxCols];
-#pragma unroll
-    for (int c = 0; c < kMaxCols; ++c) col_off[c] = c * A.nbpF;
-    int p = sl.sl[0];  // the slot this warp writes (warp < nc), taken before the sweep
-#pragma unroll
-    for (int cc = 1; cc < kMaxCols; ++cc)
-        if (warp == cc) p = sl.sl[cc];
-    float *part = S.part + buf * kPartSet;
-    group_cols(co, S.pipe, A.nbpF, S.act, S.dx, col_off, nc, part + warp * kMaxCols * 32, warp, lane);
-    consumer_sync();
-    if (warp < nc) {
-        float v = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) v += part[(w * kMaxCols + warp) * 32 + lane];
-        A.ws.obuf[(size_t)p * A.L.H + (size_t)g * 32 + lane] = v;
-    }
+    atomicOr(P.err, kErrDependencyTimeout);
+    *(volatile int *)P.abort = 1;
+    return false;
 }
 
 // The whole routed-expert layer but the combine, in one persistent kernel.
-// Work items, handed out in this order by one counter:
-//   it <  D*Gf : gate_up item (expert rank u, 32-row-pair group g), u-major;
-//   it >= D*Gf : down item (expert rank u, 32-row group g), u-major.
-// A CTA fetches a down item only after every gate_up item has been fetched,
-// and the fetched gate_up items are processed by running CTAs without waiting
-// on anything, so a down item's wait for its expert's intermediate
-// (done[u] == Gf * ns) always ends; it is bounded all the same.
+// Work items, handed out in this order (the first per CTA is its index, the
+// rest come from one counter):
+//   it <  D*Gf : gate_up item (expert rank u, 32-row-pair group g), u-major:
+//                gate rows 32g.. and up rows F+32g.. in one format-B pass,
+//                then the SwiGLU split and the requantization of the 32
+//                outputs of each column;
+//   it >= D*Gf : down item (expert rank u, 64-row group g: 32-row groups 2g
+//                and 2g+1), u-major, per-slot outputs to obuf.
+// A CTA takes a down item only after every gate_up item has been taken, and
+// taken gate_up items never wait, so a down item's wait for its expert's
+// intermediate (done[u] == Gf * ns) always ends; it is bounded all the same.
 // The producer streams a down item's weights before that wait ends.
 // Launched as a programmatic dependent either way.  With one token (quantized
 // here) this is the call's first kernel: it sets up its pipeline, then waits
@@ -588,51 +569,62 @@ __device__ __forceinline__ void down_item(const MoeArgs &A, const Slots &sl, con
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__ MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
-    const PipeSmem S = carve_pipe(smem, kStagesMoe, 1, A.act_blocks);
+    __shared__ int dep_ok;
+    const PipeSmem S = carve_pipe(smem, A.stages, A.act_blocks, A.ws.err);
     pipe_init(S.pipe);
     if (A.quant_tokens) pdl_wait();
     pdl_trigger();  // the combine kernel may launch; it waits for this grid
     const int N = A.n_tok * A.k + (A.L.shared ? A.n_tok : 0);  // routed slots, then shared ones
-    route(A.ids, A.n_tok * A.k, N, A.L.E, R, blockIdx.x == 0);  // ends with a CTA barrier
-    const int Gf = A.L.F / 32, Gd = A.L.H / 32;
+    route(A.ids, A.n_tok * A.k, N, A.L.E, R, blockIdx.x == 0 ? A.ws.err : nullptr);  // ends with a CTA barrier
+    const int Gf = A.L.F / 32, Gd = A.L.H / 32, Gd2 = (Gd + 1) / 2;
     const unsigned total_gu = (unsigned)(R.D * Gf);
-    const unsigned total = total_gu + (unsigned)(R.D * Gd);
+    const unsigned total = total_gu + (unsigned)(R.D * Gd2);
     unsigned *sched = A.ws.sched;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == kConsumerWarps) {  // producer
         if (lane == 0) {
             Producer pr;
             const int nbqH = A.nbpH / 4, nbqF = A.nbpF / 4;
-            for (;;) {
-                // gate_up items one at a time; down items by guided grabs of up
-                // to kDownGrab consecutive items (same expert, same staged columns)
-                const unsigned seen = *(volatile unsigned *)sched;
-                if (seen >= total || pr.stopped) break;
-                const unsigned grab =
-                    seen < total_gu ? 1u : max(1u, min(kDownGrab, (total - seen) / (2u * gridDim.x)));
-                const unsigned base = atomicAdd(sched, grab);
-                if (base >= total) break;
+            unsigned base = blockIdx.x, grab = 1;  // first item: the CTA index
+            while (base < total && !pr.stopped) {
+                // the next grab (gate_up items one at a time; down items by
+                // guided grabs of up to kDownGrab consecutive items of one
+                // expert, which share staged columns) is fetched before this
+                // one's stages are issued, so the atomic's latency overlaps them
+                const unsigned seen = gridDim.x + *(volatile unsigned *)sched;
+                const unsigned ngrab = seen < total_gu ? 1u : max(1u, min(kDownGrab, (total - seen) / (2u * gridDim.x)));
+                const unsigned nbase = seen < total ? gridDim.x + atomicAdd(sched, ngrab) : total;
                 for (unsigned it = base; it < min(total, base + grab) && !pr.stopped; ++it) {
                     if (it < total_gu) {
                         const int u = (int)it / Gf, g = (int)it - u * Gf;
                         const ExpertMat w = gate_up_of(A.L, R.uniq[u]);
+                        const size_t ga = (size_t)g, gb = (size_t)g + Gf;
                         const int nch = col_chunks(expert_ns(R, u, N));
                         for (int ch = 0; ch < nch; ++ch) {
-                            for (int half = 0; half < 2; ++half) {
-                                const size_t grp = (size_t)g + (size_t)half * Gf;
-                                pr.group(S.pipe, w.qs + grp * A.nbpH * 32, w.sc + grp * nbqH * 32, A.nbpH, (int)it);
+                            if (A.ws.stall == 2 && blockIdx.x == 0 && pr.it == 0) {
+                                // give-up test mode: CTA 0's first stage is claimed and
+                                // tagged but never filled, so its consumers' wait runs out
+                                pr.tag_only(S.pipe, (int)it);
+                                continue;
                             }
+                            pr.group_b(S.pipe, w.qs + ga * A.nbpH * 32, w.sc + ga * nbqH * 32, w.qs + gb * A.nbpH * 32,
+                                       w.sc + gb * nbqH * 32, A.nbpH, (int)it);
                         }
                     } else {
                         const int j = (int)(it - total_gu);
-                        const int u = j / Gd, g = j - u * Gd;
+                        const int u = j / Gd2, g = j - u * Gd2;
                         const ExpertMat w = down_of(A.L, R.uniq[u]);
+                        const size_t ga = 2 * (size_t)g, gb = ga + 1;
+                        const bool two = (int)gb < Gd;
                         const int nch = col_chunks(expert_ns(R, u, N));
                         for (int ch = 0; ch < nch; ++ch)
-                            pr.group(S.pipe, w.qs + (size_t)g * A.nbpF * 32, w.sc + (size_t)g * nbqF * 32, A.nbpF,
-                                     (int)it);
+                            pr.group_b(S.pipe, w.qs + ga * A.nbpF * 32, w.sc + ga * nbqF * 32,
+                                       two ? w.qs + gb * A.nbpF * 32 : nullptr, w.sc + gb * nbqF * 32, A.nbpF,
+                                       (int)it);
                     }
                 }
+                base = nbase;
+                grab = ngrab;
             }
             __threadfence();
             sched_exit(sched);
@@ -651,53 +643,90 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
         stage_cols(src, A.n_tok, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
     }
     consumer_sync();
-    Consumer co;
-    int staged_u = -1, item = 0;
+    Consumer co(S.pipe);
+    int staged_u = -1, n = 0;
+    bool dead = false;  // a dependency wait gave up: no later item computes or writes
     for (;;) {
-        const int it = co.peek(S.pipe);
+        const int it = co.next_item(S.pipe);
         if (it < 0) break;
-        if ((unsigned)it < total_gu) {
-            const int u = it / Gf, g = it - u * Gf;
-            const int e = R.uniq[u];
-            for (int c0 = 0;; c0 += kMaxCols, ++item) {
-                const Slots sl = warp_slots(R, e, N, c0, lane);
-                gate_up_item(A, sl, S, co, u, g, min(kMaxCols, sl.ns - c0), warp, lane, item & 1);
-                if (c0 + kMaxCols >= sl.ns) break;
-            }
-            ++item;
-            continue;
+        const bool gu = (unsigned)it < total_gu;
+        int u, g;
+        if (gu) {
+            u = it / Gf;
+            g = it - u * Gf;
+        } else {
+            const int j = it - (int)total_gu;
+            u = j / Gd2;
+            g = j - u * Gd2;
         }
-        const int j = it - (int)total_gu;
-        const int u = j / Gd, g = j - u * Gd;
         const int e = R.uniq[u];
-        for (int c0 = 0;; c0 += kMaxCols) {
+        for (int c0 = 0;; c0 += kMaxCols, ++n) {
             const Slots sl = warp_slots(R, e, N, c0, lane);
             const int nc = min(kMaxCols, sl.ns - c0);
-            if (staged_u != u || sl.ns > kMaxCols) {
-                consumer_sync();  // the tokens (or the previous columns) are no longer read
-                if (staged_u != u && threadIdx.x == 0) {  // wait for expert u's intermediate
-                    const unsigned target = (unsigned)(Gf * sl.ns);
-                    uint32_t polls = 0;
-                    while (ld_acquire(A.ws.done + u) < target) {
-                        if (++polls == kDependencyPolls) {
-                            atomicOr(&g_device_error, kErrDependencyTimeout);
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                }
-                consumer_sync();
-                ColSrc src{A.ws.qa, A.ws.da, (size_t)A.L.F, (size_t)A.nbF, {}};
+            int col_off[kMaxCols];
+            if (gu) {
 #pragma unroll
-                for (int c = 0; c < kMaxCols; ++c) src.row[c] = max(sl.sl[c], 0);
-                stage_cols(src, nc, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers, true);
-                consumer_sync();
-                staged_u = u;
+                for (int c = 0; c < kMaxCols; ++c)
+                    col_off[c] = (c < nc ? slot_token(sl.sl[c], A.n_tok * A.k, A.k) : 0) * A.nbpH;
+            } else {
+#pragma unroll
+                for (int c = 0; c < kMaxCols; ++c) col_off[c] = c * A.nbpF;
+                if (staged_u != u || sl.ns > kMaxCols) {
+                    consumer_sync();  // the tokens (or the previous columns) are no longer read
+                    if (threadIdx.x == 0)  // wait for expert u's intermediate
+                        dep_ok = !dead && wait_dependency(A.ws.done + u, A.ws.stall == 1 ? ~0u : (unsigned)(Gf * sl.ns),
+                                                          S.pipe);
+                    consumer_sync();
+                    dead = dead || !dep_ok;
+                    if (!dead) {
+                        ColSrc src{A.ws.qa, A.ws.da, (size_t)A.L.F, (size_t)A.nbF, {}};
+#pragma unroll
+                        for (int c = 0; c < kMaxCols; ++c) src.row[c] = max(sl.sl[c], 0);
+                        stage_cols(src, nc, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers, true);
+                    }
+                    consumer_sync();
+                    staged_u = u;
+                }
             }
-            down_item(A, sl, S, co, g, nc, warp, lane, item & 1);
-            ++item;
+            float *P0 = S.part + (n & 1) * kPartSetB;
+            sweep_b(co, S.pipe, gu ? A.nbpH : A.nbpF, S.act, S.dx, col_off, nc, P0 + warp * (2 * kMaxCols * 32),
+                    !dead, warp, lane);
+            consumer_sync();
+            if (!dead && gu && warp < nc) {
+                // SwiGLU split and requantization of column `warp`: gate sums in
+                // row set 0, up sums in row set 1 of every warp's slice
+                const int c = warp;
+                float gs = 0.0f, us = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    gs += P0[(w * 2 * kMaxCols + c) * 32 + lane];
+                    us += P0[(w * 2 * kMaxCols + kMaxCols + c) * 32 + lane];
+                }
+                const float a = A.swiglu ? gs / (1.0f + expf(-gs)) * us : gs * us;
+                float d;
+                const int8_t q = quant_lane(a, d);
+                const int p = pick(sl.sl, c);
+                const size_t o = (size_t)p * A.L.F + (size_t)g * 32 + lane;
+                A.ws.qa[o] = q;
+                if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
+                if (A.ws.keep_a) A.ws.a_dbg[o] = a;
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(A.ws.done + u, 1u);
+            } else if (!dead && !gu) {
+                // down outputs: row set r of column c, for i = 2c + r
+                for (int i = warp; i < 2 * nc; i += kConsumerWarps) {
+                    const int c = i >> 1, r = i & 1;
+                    float v = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) v += P0[(w * 2 * kMaxCols + r * kMaxCols + c) * 32 + lane];
+                    const int grp = 2 * g + r;
+                    if (grp < Gd) A.ws.obuf[(size_t)pick(sl.sl, c) * A.L.H + (size_t)grp * 32 + lane] = v;
+                }
+            }
             if (c0 + kMaxCols >= sl.ns) break;
         }
+        ++n;
     }
     // the last CTA to finish resets the per-expert counts for the next call
     consumer_sync();
@@ -768,9 +797,9 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     A.nbpH = round_up4(A.nbH);
     A.nbF = L.F / kQK;
     A.nbpF = round_up4(A.nbF);
-    A.act_blocks = std::max(n_tok * A.nbpH, kMaxCols * A.nbpF);
     // one token: the layer kernel quantizes it (one launch fewer)
     A.quant_tokens = n_tok == 1 && ((uintptr_t)h & 15u) == 0;
+    A.act_blocks = std::max((A.quant_tokens ? 1 : n_tok) * A.nbpH, kMaxCols * A.nbpF);
     cudaError_t e = cudaSuccess;
     if (ws.ev[0] && (e = cudaEventRecord(ws.ev[0], s)) != cudaSuccess) return e;
     if (!A.quant_tokens) {
@@ -778,10 +807,19 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
         if (e != cudaSuccess) return e;
     }
     const int64_t max_experts = std::min(n_tok * k, L.E) + (L.shared ? 1 : 0);
+    const int64_t items = max_experts * (L.F / 32 + (L.H / 32 + 1) / 2);
     {
-        const size_t smem = moe_smem_bytes(A.act_blocks);
-        int grid = 0;
-        e = dynamic_grid(k_moe, smem, max_experts * (L.F / 32 + L.H / 32), &grid);
+        // four stages when two CTAs per SM still fit, else three
+        int grid = 0, sms = 0, per_sm = 0;
+        A.stages = 4;
+        size_t smem = moe_smem_bytes(A.act_blocks, A.stages);
+        e = resident(k_moe, kPipeThreads, smem, &sms, &per_sm);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 2) {
+            A.stages = 3;
+            smem = moe_smem_bytes(A.act_blocks, A.stages);
+        }
+        e = dynamic_grid(k_moe, smem, items, &grid);
         if (e != cudaSuccess) return e;
         e = launch_k(k_moe, grid, kPipeThreads, smem, s, true, A);
         if (e != cudaSuccess) return e;
@@ -878,13 +916,5 @@ cudaError_t moe_smem_limit(size_t *bytes) {
     return e;
 }
 
-cudaError_t read_and_clear_device_error(unsigned *code) {
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return e;
-    e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(unsigned));
-    if (e != cudaSuccess) return e;
-    const unsigned zero = 0;
-    return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned));
-}
 
 }  // namespace cbq
