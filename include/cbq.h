@@ -113,8 +113,8 @@ const char *cbq_last_cuda_error(void);
  * stream interleaved by 32-row groups plus a separate fp16 scale stream); the
  * source is not retained.  Synchronizes `stream`.
  * K is bounded by the shared-memory staging of CBQ_MAX_COLS quantized
- * activation columns next to the weight ring: K <= 26,368 on GB300 (227 KB
- * of shared memory per CTA).
+ * activation columns next to the weight ring and the partial-sum sets:
+ * K <= 26,240 on GB300 (227 KB of shared memory per CTA).
  * Errors: EINVAL (null, M < 1, K < 32, K % 32 != 0, K above that bound),
  * ENOMEM, ECUDA, EDEVICE. */
 int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device,
@@ -157,9 +157,8 @@ int cbq_matvec_host(const cbq_weights *W, const float *x_host, int n, float *y_h
 /* Create an MoE layer handle from canonical blocks of E experts, contiguous
  * per expert: gate_up = E x (2F rows x H cols), rows 0..F-1 the gate
  * projection and rows F..2F-1 the up projection; down = E x (H rows x F cols).
- * H % 32 == 0, F % 32 == 0, E >= 1, H and F <= 27,648 on GB300 (shared-memory
- * staging of CBQ_MAX_TOKENS token columns, or CBQ_MAX_COLS intermediate
- * columns, next to the weight ring).  Host memory if on_device == 0.
+ * H % 32 == 0, F % 32 == 0, E >= 1, H and F <= 1,048,576.  Host memory if
+ * on_device == 0.
  * Synchronizes `stream`.  Errors as cbq_weights_create. */
 int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int64_t F,
                    int on_device, void *stream, cbq_moe **out);
@@ -291,8 +290,9 @@ int cbq_debug_block_dots(const cbq_weights *W, const int8_t *qx_dev, int n, int3
 int cbq_moe_debug_block_dots(const cbq_moe *L, int e, int which, const int8_t *qx_dev, int n,
                              int32_t *s_dev, void *stream);
 
-/* Keep (1) or stop keeping (0) the fp32 intermediate a of each slot in the
- * workspace during cbq_moe_matvec (costs 4*F bytes of writes per slot). */
+/* Keep (1) or stop keeping (0) the intermediate of each slot -- a (fp32) and
+ * its quantization (qa int8, da fp32) in plain slot order -- in the workspace
+ * during cbq_moe_matvec (costs about 5*F bytes of writes per slot). */
 int cbq_moe_set_debug(cbq_moe *L, int keep_intermediate);
 
 /* Give-up test mode of the layer kernel, for the tests of its bounded waits
@@ -307,8 +307,9 @@ int cbq_moe_debug_stall(cbq_moe *L, int mode);
 /* Copy the intermediate of the last cbq_moe_matvec on this handle, for
  * slots p < nslots (at most CBQ_MAX_TOKENS * (CBQ_MAX_TOPK + 1)): routed
  * slots p = t*topk + j, then the shared expert's slots p = n_tok*topk + t;
- * a_dev[p][F] fp32 (needs debug on), qa_dev[p][F] int8, da_dev[p][F/32] fp32
- * (any may be NULL).  Slots whose id was out of range hold stale data. */
+ * a_dev[p][F] fp32, qa_dev[p][F] int8, da_dev[p][F/32] fp32 (any may be
+ * NULL), as kept by the last call made with debug on (cbq_moe_set_debug).
+ * Slots whose id was out of range hold stale data. */
 int cbq_moe_debug_intermediate(const cbq_moe *L, int nslots, float *a_dev, int8_t *qa_dev,
                                float *da_dev, void *stream);
 

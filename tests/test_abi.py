@@ -45,6 +45,8 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.cbq_matvec_q(None, dummy, dummy, 1, dummy, None) == EINVAL
     assert lib.cbq_moe_create(dummy, dummy, 0, 64, 64, 0, None, ctypes.byref(h)) == EINVAL
     assert lib.cbq_moe_create(dummy, dummy, 4, 60, 64, 0, None, ctypes.byref(h)) == EINVAL
+    assert lib.cbq_moe_create(dummy, dummy, 1, (1 << 20) + 32, 64, 0, None, ctypes.byref(h)) == EINVAL  # H cap
+    assert lib.cbq_moe_create(dummy, dummy, 1, 64, (1 << 20) + 32, 0, None, ctypes.byref(h)) == EINVAL  # F cap
     assert lib.cbq_moe_matvec(None, dummy, 1, dummy, dummy, 1, 1, dummy, None) == EINVAL
     assert lib.cbq_weights_destroy(None) == EINVAL
     assert lib.cbq_moe_destroy(None) == EINVAL

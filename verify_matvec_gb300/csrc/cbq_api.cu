@@ -21,8 +21,7 @@ using cbq::MoeWork;
 struct cbq_weights {
     int device;
     DevMat mat;
-    uint4 *qs;
-    uint2 *sc;
+    uint8_t *w;      // repacked weights (cbq_internal.h layout)
     unsigned *sched; // work counters of the matvec kernel
     unsigned *err;   // the handle's error word
     int8_t *ws_qx;   // CBQ_MAX_COLS x K
@@ -36,10 +35,8 @@ struct cbq_weights {
 struct cbq_moe {
     int device;
     DevMoe L;
-    uint4 *gu_qs, *dn_qs;
-    uint2 *gu_sc, *dn_sc;
-    uint4 *sh_gu_qs, *sh_dn_qs;  // shared expert (null when unset)
-    uint2 *sh_gu_sc, *sh_dn_sc;
+    uint8_t *gu, *dn;        // repacked experts, one after another
+    uint8_t *sh_gu, *sh_dn;  // shared expert (null when unset)
     int64_t sh_bytes;
     MoeWork ws;
     float *st_h;      // CBQ_MAX_TOKENS x H
@@ -120,8 +117,9 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// Repack canonical blocks (host or device) of an M x K matrix into qs/sc.
-int repack_into(const void *blocks, int64_t M, int nb, int on_device, uint4 *qs, uint2 *sc, cudaStream_t s) {
+// Repack canonical blocks (host or device) of an M x K matrix into w (split:
+// the gate/up pairing of a gate_up matrix, 0 otherwise).
+int repack_into(const void *blocks, int64_t M, int nb, int split, int on_device, uint8_t *w, cudaStream_t s) {
     const size_t nbytes = (size_t)M * (size_t)nb * CBQ_BLOCK_BYTES;
     const uint8_t *src = static_cast<const uint8_t *>(blocks);
     uint8_t *tmp = nullptr;
@@ -137,7 +135,7 @@ int repack_into(const void *blocks, int64_t M, int nb, int on_device, uint4 *qs,
         }
         src = tmp;
     }
-    cudaError_t e = cbq::launch_repack(src, M, nb, qs, sc, s);
+    cudaError_t e = cbq::launch_repack(src, M, nb, split, w, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (tmp) cudaFree(tmp);
     if (e != cudaSuccess) return cuda_fail(e, "repack");
@@ -166,8 +164,7 @@ const char *cbq_last_cuda_error(void) { return t_last_error; }
 int cbq_weights_destroy(cbq_weights *W) {
     if (!W) return CBQ_EINVAL;
     DeviceScope scope(W->device);
-    cudaFree(W->qs);
-    cudaFree(W->sc);
+    cudaFree(W->w);
     cudaFree(W->sched);
     cudaFree(W->err);
     cudaFree(W->ws_qx);
@@ -189,17 +186,17 @@ int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device, 
     const int nb = (int)(K / CBQ_QK);
     const int nbp = cbq::round_up4(nb);
     size_t smem_max = 0;
-    CBQ_CUDA(cbq::device_smem_limit(&smem_max));
+    CBQ_CUDA(cbq::matvec_smem_limit(&smem_max));
     if (cbq::matvec_smem_bytes(nbp, CBQ_MAX_COLS) > smem_max) return CBQ_EINVAL;
 
     const int G = (int)((M + 31) / 32);
+    const int64_t P = cbq::mat_pairs(M);
 
     cbq_weights *W = new (std::nothrow) cbq_weights();
     if (!W) return CBQ_ENOMEM;
     W->device = dev;
     W->K = K;
-    if ((rc = dev_alloc(&W->qs, cbq::qs_elems(M, nb), &W->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&W->sc, cbq::sc_elems(M, nb), &W->bytes)) != CBQ_OK ||
+    if ((rc = dev_alloc(&W->w, cbq::mat_bytes(M, nb), &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->sched, 2, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->err, 1, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->ws_qx, (size_t)CBQ_MAX_COLS * K, &W->bytes)) != CBQ_OK ||
@@ -214,17 +211,18 @@ int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device, 
         cbq_weights_destroy(W);
         return CBQ_ECUDA;
     }
-    rc = repack_into(blocks, M, nb, on_device, W->qs, W->sc, as_stream(stream));
+    rc = repack_into(blocks, M, nb, 0, on_device, W->w, as_stream(stream));
     if (rc != CBQ_OK) {
         cbq_weights_destroy(W);
         return rc;
     }
-    W->mat.qs = W->qs;
-    W->mat.sc = W->sc;
+    W->mat.w = W->w;
     W->mat.M = M;
     W->mat.nb = nb;
     W->mat.nbp = nbp;
     W->mat.G = G;
+    W->mat.P = (int)P;
+    W->mat.split = 0;
     W->mat.sched = W->sched;
     W->mat.err = W->err;
     *out = W;
@@ -343,16 +341,12 @@ namespace {
 
 // Frees the shared expert of L and stops the kernels from using it.
 void drop_shared(cbq_moe *L) {
-    cudaFree(L->sh_gu_qs);
-    cudaFree(L->sh_gu_sc);
-    cudaFree(L->sh_dn_qs);
-    cudaFree(L->sh_dn_sc);
-    L->sh_gu_qs = L->sh_dn_qs = nullptr;
-    L->sh_gu_sc = L->sh_dn_sc = nullptr;
+    cudaFree(L->sh_gu);
+    cudaFree(L->sh_dn);
+    L->sh_gu = L->sh_dn = nullptr;
     L->bytes -= L->sh_bytes;
     L->sh_bytes = 0;
-    L->L.sh_gu_qs = L->L.sh_dn_qs = nullptr;
-    L->L.sh_gu_sc = L->L.sh_dn_sc = nullptr;
+    L->L.sh_gu = L->L.sh_dn = nullptr;
     L->L.shared = 0;
 }
 
@@ -362,18 +356,16 @@ int cbq_moe_destroy(cbq_moe *L) {
     if (!L) return CBQ_EINVAL;
     DeviceScope scope(L->device);
     drop_shared(L);
-    cudaFree(L->gu_qs);
-    cudaFree(L->gu_sc);
-    cudaFree(L->dn_qs);
-    cudaFree(L->dn_sc);
+    cudaFree(L->gu);
+    cudaFree(L->dn);
     cudaFree(L->ws.qh);
-    cudaFree(L->ws.dh);
+    cudaFree(L->ws.qa_bm);
+    cudaFree(L->ws.dep);
     cudaFree(L->ws.qa);
     cudaFree(L->ws.da);
     cudaFree(L->ws.a_dbg);
     cudaFree(L->ws.obuf);
     cudaFree(L->ws.sched);
-    cudaFree(L->ws.done);
     cudaFree(L->ws.err);
     cudaFree(L->st_h);
     cudaFree(L->st_ids);
@@ -394,30 +386,24 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
     int rc = check_device(&dev);
     if (rc != CBQ_OK) return rc;
     const int nbH = (int)(H / CBQ_QK), nbF = (int)(F / CBQ_QK);
-    size_t smem_max = 0;
-    CBQ_CUDA(cbq::moe_smem_limit(&smem_max));
-    if (cbq::moe_smem_bytes(std::max(CBQ_MAX_TOKENS * cbq::round_up4(nbH), CBQ_MAX_COLS * cbq::round_up4(nbF)), 3) >
-        smem_max)
-        return CBQ_EINVAL;
 
     cbq_moe *L = new (std::nothrow) cbq_moe();
     if (!L) return CBQ_ENOMEM;
     L->device = dev;
-    const size_t guq = cbq::qs_elems(2 * F, nbH), gus = cbq::sc_elems(2 * F, nbH);
-    const size_t dnq = cbq::qs_elems(H, nbF), dns = cbq::sc_elems(H, nbF);
+    const size_t gub = cbq::mat_bytes(2 * F, nbH), dnb = cbq::mat_bytes(H, nbF);
     const size_t slots = cbq::kMaxSlots;
-    if ((rc = dev_alloc(&L->gu_qs, guq * E, &L->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&L->gu_sc, gus * E, &L->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&L->dn_qs, dnq * E, &L->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&L->dn_sc, dns * E, &L->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&L->ws.qh, (size_t)CBQ_MAX_TOKENS * H, &L->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&L->ws.dh, (size_t)CBQ_MAX_TOKENS * nbH, &L->bytes)) != CBQ_OK ||
+    const size_t nbpH = (size_t)cbq::round_up4(nbH), nbpF = (size_t)cbq::round_up4(nbF);
+    const size_t nsF = (nbpF + 15) / 16;  // down stages of 16 blocks
+    if ((rc = dev_alloc(&L->gu, gub * E, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->dn, dnb * E, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.qh, cbq::act_bytes((int)nbpH, CBQ_MAX_TOKENS), &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.qa_bm, slots * cbq::act_bytes((int)nbpF, CBQ_MAX_COLS), &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.dep, slots * nsF, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.qa, slots * F, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.da, slots * nbF, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.a_dbg, slots * F, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.obuf, slots * H, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.sched, 4, &L->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&L->ws.done, slots, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.err, 1, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_h, (size_t)CBQ_MAX_TOKENS * H, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_ids, slots, &L->bytes)) != CBQ_OK ||
@@ -427,8 +413,10 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
         return rc;
     }
     cudaStream_t s = as_stream(stream);
+    // the intermediate's padded blocks are never written: zero keeps them finite
     if (cudaMemsetAsync(L->ws.sched, 0, 4 * sizeof(unsigned), s) != cudaSuccess ||
-        cudaMemsetAsync(L->ws.done, 0, slots * sizeof(unsigned), s) != cudaSuccess ||
+        cudaMemsetAsync(L->ws.dep, 0, slots * nsF * sizeof(unsigned), s) != cudaSuccess ||
+        cudaMemsetAsync(L->ws.qa_bm, 0, slots * cbq::act_bytes((int)nbpF, CBQ_MAX_COLS), s) != cudaSuccess ||
         cudaMemsetAsync(L->ws.err, 0, sizeof(unsigned), s) != cudaSuccess) {
         cbq_moe_destroy(L);
         return CBQ_ECUDA;
@@ -436,27 +424,23 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
     const size_t gu_bytes = (size_t)2 * F * nbH * CBQ_BLOCK_BYTES;
     const size_t dn_bytes = (size_t)H * nbF * CBQ_BLOCK_BYTES;
     for (int e = 0; e < E; ++e) {
-        rc = repack_into(static_cast<const uint8_t *>(gate_up) + e * gu_bytes, 2 * F, nbH, on_device,
-                         L->gu_qs + e * guq, L->gu_sc + e * gus, s);
+        rc = repack_into(static_cast<const uint8_t *>(gate_up) + e * gu_bytes, 2 * F, nbH, (int)(F / CBQ_QK),
+                         on_device, L->gu + e * gub, s);
         if (rc == CBQ_OK)
-            rc = repack_into(static_cast<const uint8_t *>(down) + e * dn_bytes, H, nbF, on_device, L->dn_qs + e * dnq,
-                             L->dn_sc + e * dns, s);
+            rc = repack_into(static_cast<const uint8_t *>(down) + e * dn_bytes, H, nbF, 0, on_device, L->dn + e * dnb,
+                             s);
         if (rc != CBQ_OK) {
             cbq_moe_destroy(L);
             return rc;
         }
     }
-    L->L.gu_qs = L->gu_qs;
-    L->L.gu_sc = L->gu_sc;
-    L->L.dn_qs = L->dn_qs;
-    L->L.dn_sc = L->dn_sc;
+    L->L.gu = L->gu;
+    L->L.dn = L->dn;
     L->L.E = E;
     L->L.H = (int)H;
     L->L.F = (int)F;
-    L->L.gu_qs_stride = guq;
-    L->L.gu_sc_stride = gus;
-    L->L.dn_qs_stride = dnq;
-    L->L.dn_sc_stride = dns;
+    L->L.gu_stride = gub;
+    L->L.dn_stride = dnb;
     *out = L;
     return CBQ_OK;
 }
@@ -474,12 +458,10 @@ int cbq_moe_set_shared(cbq_moe *L, const void *gate_up, const void *down, int on
     const int64_t H = L->L.H, F = L->L.F;
     const int nbH = (int)(H / CBQ_QK), nbF = (int)(F / CBQ_QK);
     int rc = CBQ_OK;
-    if (!L->sh_gu_qs) {
+    if (!L->sh_gu) {
         int64_t got = 0;
-        if ((rc = dev_alloc(&L->sh_gu_qs, cbq::qs_elems(2 * F, nbH), &got)) != CBQ_OK ||
-            (rc = dev_alloc(&L->sh_gu_sc, cbq::sc_elems(2 * F, nbH), &got)) != CBQ_OK ||
-            (rc = dev_alloc(&L->sh_dn_qs, cbq::qs_elems(H, nbF), &got)) != CBQ_OK ||
-            (rc = dev_alloc(&L->sh_dn_sc, cbq::sc_elems(H, nbF), &got)) != CBQ_OK) {
+        if ((rc = dev_alloc(&L->sh_gu, cbq::mat_bytes(2 * F, nbH), &got)) != CBQ_OK ||
+            (rc = dev_alloc(&L->sh_dn, cbq::mat_bytes(H, nbF), &got)) != CBQ_OK) {
             L->bytes += got;
             L->sh_bytes = got;
             drop_shared(L);
@@ -489,16 +471,14 @@ int cbq_moe_set_shared(cbq_moe *L, const void *gate_up, const void *down, int on
         L->sh_bytes = got;
     }
     L->L.shared = 0;  // partly rewritten weights are never used
-    rc = repack_into(gate_up, 2 * F, nbH, on_device, L->sh_gu_qs, L->sh_gu_sc, s);
-    if (rc == CBQ_OK) rc = repack_into(down, H, nbF, on_device, L->sh_dn_qs, L->sh_dn_sc, s);
+    rc = repack_into(gate_up, 2 * F, nbH, (int)(F / CBQ_QK), on_device, L->sh_gu, s);
+    if (rc == CBQ_OK) rc = repack_into(down, H, nbF, 0, on_device, L->sh_dn, s);
     if (rc != CBQ_OK) {
         drop_shared(L);
         return rc;
     }
-    L->L.sh_gu_qs = L->sh_gu_qs;
-    L->L.sh_gu_sc = L->sh_gu_sc;
-    L->L.sh_dn_qs = L->sh_dn_qs;
-    L->L.sh_dn_sc = L->sh_dn_sc;
+    L->L.sh_gu = L->sh_gu;
+    L->L.sh_dn = L->sh_dn;
     L->L.shared = 1;
     return CBQ_OK;
 }
@@ -575,20 +555,21 @@ int cbq_moe_debug_block_dots(const cbq_moe *L, int e, int which, const int8_t *q
     DeviceScope scope(L->device);
     CBQ_CUDA(scope.status());
     const bool sh = e == L->L.E;
-    DevMat m;
+    DevMat m = {};
     if (which == 0) {
-        m.qs = sh ? L->sh_gu_qs : L->gu_qs + e * L->L.gu_qs_stride;
-        m.sc = sh ? L->sh_gu_sc : L->gu_sc + e * L->L.gu_sc_stride;
+        m.w = sh ? L->sh_gu : L->gu + e * L->L.gu_stride;
         m.M = 2 * (int64_t)L->L.F;
         m.nb = L->L.H / CBQ_QK;
+        m.split = L->L.F / CBQ_QK;
     } else {
-        m.qs = sh ? L->sh_dn_qs : L->dn_qs + e * L->L.dn_qs_stride;
-        m.sc = sh ? L->sh_dn_sc : L->dn_sc + e * L->L.dn_sc_stride;
+        m.w = sh ? L->sh_dn : L->dn + e * L->L.dn_stride;
         m.M = L->L.H;
         m.nb = L->L.F / CBQ_QK;
+        m.split = 0;
     }
     m.nbp = cbq::round_up4(m.nb);
     m.G = (int)((m.M + 31) / 32);
+    m.P = (int)cbq::mat_pairs(m.M);
     m.sched = nullptr;  // the block-dot kernel uses static ranges
     m.err = L->ws.err;
     CBQ_CUDA(cbq::launch_block_dots(m, qx_dev, n, s_dev, as_stream(stream)));

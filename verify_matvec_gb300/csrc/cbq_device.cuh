@@ -210,11 +210,10 @@ __device__ __forceinline__ void block_dots_2rows(const Codebook &cb, const uint4
 }
 
 // Two columns, two rows: index blocks wa (row set 0) and wb (row set 1), each
-// expanded once (exact bytes), dotted with block b of the columns staged at
-// offsets off[0], off[1] (their words at act0[2*(off[c] + b)] and [+1]).
+// expanded once (exact bytes), dotted with the activation blocks of two
+// columns (their words at a0[0..1] and a1[0..1]).
 __device__ __forceinline__ void block_dots_2rows_cols2(const Codebook &cb, const uint4 wa, const uint4 wb,
-                                                       const uint4 *act0, const int (&off)[2], int b, int sa[2],
-                                                       int sb[2]) {
+                                                       const uint4 *a0, const uint4 *a1, int sa[2], int sb[2]) {
     const uint32_t wsa[4] = {wa.x, wa.y, wa.z, wa.w}, wsb[4] = {wb.x, wb.y, wb.z, wb.w};
     uint32_t ea[8], eb[8];
 #pragma unroll
@@ -222,11 +221,11 @@ __device__ __forceinline__ void block_dots_2rows_cols2(const Codebook &cb, const
         expand_select(cb, wsa[m], ea[2 * m], ea[2 * m + 1]);
         expand_select(cb, wsb[m], eb[2 * m], eb[2 * m + 1]);
     }
+    const uint4 *ap[2] = {a0, a1};
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        const uint4 *a = act0 + 2 * (off[c] + b);
-        const uint4 a0 = a[0], a1 = a[1];
-        const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint4 x0 = ap[c][0], x1 = ap[c][1];
+        const uint32_t av[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         int s0 = cb.seed, s1 = cb.seed;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -236,6 +235,14 @@ __device__ __forceinline__ void block_dots_2rows_cols2(const Codebook &cb, const
         sa[c] = s0;
         sb[c] = s1;
     }
+}
+
+// Byte position of element r (0..31) of a block in the expander order of the
+// staged activations (stage_cols): word 2m+h holds elements 4m+2h, 4m+2h+16,
+// 4m+2h+1, 4m+2h+17.
+__device__ __forceinline__ int expander_pos(int r) {
+    const int e = r & 15, m = e >> 2, i = e & 3;
+    return 8 * m + 4 * (i >> 1) + 2 * (i & 1) + (r >> 4);
 }
 
 // Scaled accumulation of two consecutive blocks' dots of one column:

@@ -33,13 +33,10 @@ constexpr unsigned kErrBadExpertId = 0x1u;
 // Pipeline depth (stages of 18 KB per CTA, two CTAs per SM) and partial-sum
 // sets of each kernel, sized so two CTAs fit in an SM's shared memory.
 constexpr int kStages = 4;
-constexpr int kSetsMatvec = 2;   // double-buffered
-constexpr int kSetsMoe = 2;      // double-buffered, format B (two row sets)
 
-// Dynamic shared memory of the routed-expert kernel with S stages.
-size_t moe_smem_bytes(int act_blocks, int S) {
-    return pipe_smem_bytes(S, act_blocks, kSetsMoe * kPartSetB);
-}
+// Dynamic shared memory of the routed-expert kernel with S stages and
+// act_blocks persistently staged blocks (the one token it quantizes itself).
+size_t moe_smem_bytes(int act_blocks, int S) { return pipe_smem_bytes(S, kStageBytesAct, kSetBytes, 2, act_blocks); }
 
 // Launch with optional programmatic stream serialization (PDL).
 template <typename... KArgs, typename... Args>
@@ -60,37 +57,45 @@ static cudaError_t launch_k(void (*kern)(KArgs...), int grid, int block, size_t 
 
 // ------------------------------------------------------------- repack ------
 
-__global__ void k_repack(const uint8_t *__restrict__ src, int64_t M, int nb, int nbp, uint4 *__restrict__ qs,
-                         uint16_t *__restrict__ sc16) {
-    const int64_t total = ((M + 31) / 32) * (int64_t)nbp * 32;
-    const int nbq = nbp / 4;
+// One thread per (pair p, half h, block b, lane): the 16 index bytes and the
+// fp16 scale of row 32g + lane, block b, g the source group of (p, h) --
+// 2p + h, or with split = Gf > 0 (a gate_up matrix) p for h = 0 and Gf + p for
+// h = 1.  Rows beyond M and blocks beyond nb are zero.
+__global__ void k_repack(const uint8_t *__restrict__ src, int64_t M, int nb, int nbp, int split, int64_t P,
+                         uint8_t *__restrict__ w) {
+    const int64_t total = P * 2 * nbp * 32;
+    const size_t pb = pair_bytes(nbp);
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int lane = (int)(idx & 31);
-        const int64_t gb = idx >> 5;
-        const int b = (int)(gb % nbp);
-        const int64_t g = gb / nbp;
+        int64_t t = idx >> 5;
+        const int b = (int)(t % nbp);
+        t /= nbp;
+        const int h = (int)(t & 1);
+        const int64_t p = t >> 1;
+        const int64_t g = split ? (h ? split + p : p) : 2 * p + h;
         const int64_t row = g * 32 + lane;
-        uint32_t w[4] = {0, 0, 0, 0};
+        uint32_t q[4] = {0, 0, 0, 0};
         uint16_t scale = 0;
         if (row < M && b < nb) {
-            const uint8_t *p = src + ((size_t)row * nb + b) * 18;
-            scale = (uint16_t)(p[0] | (p[1] << 8));
+            const uint8_t *s8 = src + ((size_t)row * nb + b) * 18;
+            scale = (uint16_t)(s8[0] | (s8[1] << 8));
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                w[i] = (uint32_t)p[2 + 4 * i] | ((uint32_t)p[3 + 4 * i] << 8) | ((uint32_t)p[4 + 4 * i] << 16) |
-                       ((uint32_t)p[5 + 4 * i] << 24);
+                q[i] = (uint32_t)s8[2 + 4 * i] | ((uint32_t)s8[3 + 4 * i] << 8) | ((uint32_t)s8[4 + 4 * i] << 16) |
+                       ((uint32_t)s8[5 + 4 * i] << 24);
         }
-        qs[idx] = make_uint4(w[0], w[1], w[2], w[3]);
-        sc16[((g * nbq + b / 4) * 32 + lane) * 4 + (b & 3)] = scale;
+        uint8_t *base = w + (size_t)p * pb;
+        *reinterpret_cast<uint4 *>(base + field_offset(nbp, h, b, lane)) = make_uint4(q[0], q[1], q[2], q[3]);
+        *reinterpret_cast<uint16_t *>(base + scale_offset(nbp, h, b, lane)) = scale;
     }
 }
 
-cudaError_t launch_repack(const uint8_t *src, int64_t M, int nb, uint4 *qs, uint2 *sc, cudaStream_t s) {
+cudaError_t launch_repack(const uint8_t *src, int64_t M, int nb, int split, uint8_t *w, cudaStream_t s) {
     const int nbp = round_up4(nb);
-    const int64_t total = ((M + 31) / 32) * (int64_t)nbp * 32;
+    const int64_t P = mat_pairs(M), total = P * 2 * nbp * 32;
     const int grid = (int)std::min<int64_t>((total + 255) / 256, 65535);
-    k_repack<<<grid, 256, 0, s>>>(src, M, nb, nbp, qs, reinterpret_cast<uint16_t *>(sc));
+    k_repack<<<grid, 256, 0, s>>>(src, M, nb, nbp, split, P, w);
     return cudaGetLastError();
 }
 
@@ -122,9 +127,41 @@ cudaError_t launch_quantize(const float *x, int64_t K, int n, int8_t *qx, float 
     return launch_k(k_quantize, grid, 256, 0, s, true, x, total, qx, dx);
 }
 
+
+// The layer's tokens quantized into the chunked activation layout (n
+// columns), so a stage copies the slice of all tokens for its 16 blocks with
+// one bulk copy.  Blocks nb..nbp-1 are zero.  One warp per (block, token);
+// launched as a programmatic dependent.
+__global__ void k_quantize_chunked(const float *__restrict__ x, int K, int n, int nbp, int8_t *__restrict__ qh) {
+    pdl_wait();
+    pdl_trigger();
+    const int nb = K / kQK, lane = threadIdx.x & 31;
+    for (int w = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); w < nbp * n;
+         w += (int)((gridDim.x * blockDim.x) >> 5)) {
+        const int b = w / n, t = w - b * n;
+        const int c = b / kChunk, j = b - c * kChunk, nblk = chunk_blocks(nbp, c);
+        float d = 0.0f;
+        int8_t q = 0;
+        if (b < nb) q = quant_lane(x[(size_t)t * K + (size_t)b * kQK + lane], d);
+        int8_t *base = qh + act_chunk_offset(c, n);
+        base[(size_t)(j * n + t) * 32 + expander_pos(lane)] = q;
+        if (lane == 0)
+            *reinterpret_cast<float *>(base + (size_t)32 * n * nblk + ((size_t)(j >> 1) * n + t) * 8 + (j & 1) * 4) = d;
+    }
+}
+
+cudaError_t launch_quantize_chunked(const float *x, int K, int n, int8_t *qh, cudaStream_t s) {
+    const int nbp = round_up4(K / kQK);
+    const int grid = std::min((nbp * n * 32 + 255) / 256, 4096);
+    return launch_k(k_quantize_chunked, grid, 256, 0, s, true, x, K, n, nbp, qh);
+}
+
 // ---------------------------------------------------------- dense MMVQ -----
 
-size_t matvec_smem_bytes(int nbp, int n) { return pipe_smem_bytes(kStages, n * nbp, kSetsMatvec * kPartSetA); }
+// One partial-sum set: the epilogue warp reads a pair's sums long before the
+// consumers finish the next pair, and the second set's room goes to keeping
+// two CTAs per SM with five staged columns.
+size_t matvec_smem_bytes(int nbp, int n) { return pipe_smem_bytes(kStages, kStageWeightBytes, kSetBytes, 1, n * nbp); }
 
 // Debug kernel smem: activations + scales only.
 static size_t dots_smem_bytes(int nbp, int n) { return (size_t)n * nbp * 36; }
@@ -138,88 +175,180 @@ struct MatvecArgs {
     float *y;
 };
 
-// Dense MMVQ: 32-row groups fetched per CTA, all NC columns per pass.
-// kF32: the consumers quantize the fp32 column xf themselves while the
-// producer starts the weight stream (no quantization kernel before it);
-// otherwise they stage qx/dx written by the quantization kernel launched just
-// before (a programmatic dependency).
+// The end of a persistent kernel: after a CTA barrier, the last CTA to get
+// here resets the work counters (sched[0] items taken, sched[1] CTAs done).
+__device__ __forceinline__ bool last_cta(unsigned *sched) {
+    __shared__ int last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(sched + 1, 1u) == gridDim.x - 1;
+        if (last) {
+            sched[0] = 0u;
+            sched[1] = 0u;
+        }
+    }
+    __syncthreads();
+    return last != 0;
+}
+
+// One 4-block quad of one row (this lane) for NC columns: the quad's index
+// words at qs[0], qs[32], qs[64], qs[96]; its four fp16 scales in s; the
+// activations block-major at act (block j of column c at act[(j*NC + c)*2]);
+// the activation scales as float2 pairs at dxp (blocks 0-1 of column c at
+// dxp[c], blocks 2-3 at dxp[NC + c]).
+template <int NC>
+__device__ __forceinline__ void quad(const Codebook &cb, const uint4 *qs, uint2 s, const uint4 *act,
+                                     const float2 *dxp, float2 acc[NC]) {
+    const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
+    const float2 dw23 = __half22float2(*reinterpret_cast<const __half2 *>(&s.y));
+    uint4 w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = qs[j * 32];
+#pragma unroll
+    for (int jj = 0; jj < 4; jj += 2) {  // blocks in pairs: fewer live sums
+        int sa[NC], sb[NC];
+        block_dots<NC>(cb, w[jj], act + jj * NC * 2, sa);
+        block_dots<NC>(cb, w[jj + 1], act + (jj + 1) * NC * 2, sb);
+        const float2 dw = jj == 0 ? dw01 : dw23;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[c] = scale_acc2(acc[c], dw, dxp[(jj >> 1) * NC + c], sa[c], sb[c]);
+    }
+}
+
+// One item pass of the dense kernel over a pair for NC columns staged
+// block-major (act, dx: stride NC), one row per lane: warp w takes row set
+// w / 4 (the pair's first or second group) and quad w % 4 of each 16-block
+// stage, so its sums (acc) are those of one group.  False on a give-up.
+template <int NC>
+__device__ __forceinline__ bool dense_pass(Consumer &co, const Pipe &P, int nbp, const uint4 *act, const float *dx,
+                                           float2 acc[NC], int warp, int lane) {
+    const int h = warp >> 2, q = warp & 3;
+    bool ok = true;
+    for (int b = 0; b < nbp; b += kChunk) {
+        if (b > 0) ok = ok && co.wait(P);
+        const int nblk = min(kChunk, nbp - b);
+        if (ok && 4 * q < nblk) {
+            const unsigned char *half = co.st + (size_t)h * nblk * kBlockBytes;
+            const uint4 *qs = reinterpret_cast<const uint4 *>(half) + q * 128 + lane;
+            const uint2 s = reinterpret_cast<const uint2 *>(half + (size_t)nblk * 512)[q * 32 + lane];
+            const int bq = b + 4 * q;
+            quad<NC>(co.cb, qs, s, act + (size_t)bq * NC * 2, reinterpret_cast<const float2 *>(dx) + (bq >> 1) * NC,
+                     acc);
+        }
+        co.release(P);
+    }
+    return ok;
+}
+
+// Dense MMVQ: pairs of 32-row groups fetched per CTA, all NC columns per
+// pass; the epilogue warp adds the consumer warps' sums of a pair (four per
+// group) and stores its 64 rows of y.  kF32: the consumers quantize the fp32
+// column xf themselves while the producer starts the weight stream (no
+// quantization kernel before it); otherwise they stage qx/dx written by the
+// quantization kernel launched just before (a programmatic dependency).
 template <int NC, bool kF32>
 __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constant__ MatvecArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_trigger();  // the next kernel may launch; it waits for this grid before touching what it writes
     const DevMat &W = A.W;
-    const PipeSmem S = carve_pipe(smem, kStages, NC * W.nbp, W.err);
+    const PipeSmem S = carve_pipe(smem, kStages, kStageWeightBytes, kSetBytes, 1, NC * W.nbp, W.err);
     pipe_init(S.pipe);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nbq = W.nbp / 4;
-    const unsigned total = (unsigned)W.G;
-    if (warp == kConsumerWarps) {  // producer
+    const unsigned total = (unsigned)W.P;
+    const size_t pb = pair_bytes(W.nbp);
+    const int nch = (W.nbp + kChunk - 1) / kChunk;
+    if (warp == kProducerWarp) {
         if (lane == 0) {
             Producer pr;
-            // the first item is the CTA index (the grid never exceeds the item
-            // count): its weights stream before the wait for the work ahead of
-            // this kernel, which the work counter needs (a call still running
-            // on the handle owns it)
-            unsigned item = blockIdx.x;
-            pr.group_a(S.pipe, W.qs + (size_t)item * W.nbp * 32, W.sc + (size_t)item * nbq * 32, 0, W.nbp, (int)item);
+            // The first item is the CTA index (the launcher sizes the grid to
+            // at most the item count): its weights stream before the wait for
+            // the work ahead of this kernel, which the work counter needs (a
+            // call still running on the handle owns it).  The index of the
+            // next item is fetched when an item starts and used once its
+            // stages are issued, so the atomic's latency overlaps them.
+            if (blockIdx.x < total) pr.pass(S.pipe, W.w + blockIdx.x * pb, W.nbp, 0, nch, (int)blockIdx.x);
             pdl_wait();
             unsigned next = gridDim.x + atomicAdd(W.sched, 1u);
             while (next < total && !pr.stopped) {
-                item = next;
-                // the following item's index is fetched before this item's
-                // stages are issued, so the atomic's latency overlaps them
+                const unsigned item = next;
                 next = gridDim.x + atomicAdd(W.sched, 1u);
-                pr.group_a(S.pipe, W.qs + (size_t)item * W.nbp * 32, W.sc + (size_t)item * nbq * 32, 0, W.nbp,
-                           (int)item);
+                pr.pass(S.pipe, W.w + item * pb, W.nbp, 0, nch, (int)item);
             }
-            __threadfence();
-            sched_exit(W.sched);
             pr.finish(S.pipe);
             pr.drain(S.pipe);
         }
-        return;
-    }
-    pdl_wait();  // the activations belong to the work ahead
-    if constexpr (kF32) {
-        quant_stage_cols<NC>(A.xf, A.K, W.nb, W.nbp, S.act, S.dx, threadIdx.x, kConsumers);
+    } else if (warp == kEpilogueWarp) {
+        SetReader rd;
+        for (;;) {
+            const int *tag;
+            const float *part;
+            if (!rd.wait(S.pipe, tag, part)) break;
+            const int it = *(volatile const int *)tag;
+            if (it < 0) break;
+            float v[2][NC];
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    v[r][c] = 0.0f;
+#pragma unroll
+                    for (int w = 4 * r; w < 4 * r + 4; ++w) v[r][c] += part[(w * 2 * kMaxCols + c) * 32 + lane];
+                }
+            rd.release(S.pipe);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int64_t row = (int64_t)(2 * it + r) * 32 + lane;
+                if (row < W.M) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) A.y[(size_t)c * W.M + row] = v[r][c];
+                }
+            }
+        }
     } else {
-        ColSrc src{A.qx, A.dx, (size_t)A.K, (size_t)W.nb, {0, 1, 2, 3, 4}};
-        stage_cols(src, NC, W.nb, W.nbp, S.act, S.dx, threadIdx.x, kConsumers, false, true);
-    }
-    consumer_sync();
-    const float2 *dxp = reinterpret_cast<const float2 *>(S.dx);
-    Consumer co(S.pipe);
-    for (int n = 0;; ++n) {
-        const int it = co.next_item(S.pipe);
-        if (it < 0) break;
-        float2 acc[NC];
-#pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
-        sweep_a<NC>(co, S.pipe, 0, W.nbp, S.act, dxp, acc, warp, lane);
-        float *part = S.part + (n & 1) * kPartSetA;
-#pragma unroll
-        for (int c = 0; c < NC; ++c) part[(warp * NC + c) * 32 + lane] = acc[c].x + acc[c].y;
+        pdl_wait();  // the activations belong to the work ahead
+        if constexpr (kF32) {
+            quant_stage_cols<NC>(A.xf, A.K, W.nb, W.nbp, S.act, S.dx, threadIdx.x, kConsumers);
+        } else {
+            ColSrc src{A.qx, A.dx, (size_t)A.K, (size_t)W.nb, {0, 1, 2, 3, 4}};
+            stage_cols(src, NC, W.nb, W.nbp, S.act, S.dx, threadIdx.x, kConsumers, false, true);
+        }
         consumer_sync();
-        if (warp < NC) {
-            float v = 0.0f;
+        Consumer co(S.pipe);
+        SetWriter wr;
+        for (;;) {
+            const int it = co.wait(S.pipe) ? co.tag(S.pipe) : -1;
+            int *tag;
+            float *part;
+            if (!wr.acquire(S.pipe, tag, part)) break;
+            if (it < 0) {
+                if (threadIdx.x == 0) *tag = -1;
+                wr.publish(S.pipe);
+                break;
+            }
+            float2 acc[NC];
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) v += part[(w * NC + warp) * 32 + lane];
-            const int64_t row = (int64_t)it * 32 + lane;
-            if (row < W.M) A.y[(size_t)warp * W.M + row] = v;
+            for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
+            const bool ok = dense_pass<NC>(co, S.pipe, W.nbp, S.act, S.dx, acc, warp, lane);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) part[(warp * 2 * kMaxCols + c) * 32 + lane] = acc[c].x + acc[c].y;
+            if (threadIdx.x == 0) *tag = it;
+            wr.publish(S.pipe);
+            if (!ok) break;
         }
     }
+    last_cta(W.sched);
 }
-
 
 template <int NC>
 __global__ void __launch_bounds__(kThreads, 2)
-    k_block_dots(const uint4 *__restrict__ qs, const uint2 *__restrict__ sc, int64_t M, int G, int nb, int nbp,
-                 const int8_t *__restrict__ qx, int64_t K, int32_t *__restrict__ sdot, int chunk) {
+    k_block_dots(const DevMat W, const int8_t *__restrict__ qx, int64_t K, int32_t *__restrict__ sdot, int chunk) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int g0 = blockIdx.x * chunk;
-    const int g1 = min(G, g0 + chunk);
-    if (g0 >= G) return;
+    const int g1 = min(W.G, g0 + chunk);
+    if (g0 >= W.G) return;
+    const int nb = W.nb, nbp = W.nbp;
     uint4 *act_s = reinterpret_cast<uint4 *>(smem);
     float *dx_s = reinterpret_cast<float *>(act_s + (size_t)NC * nbp * 2);
     {
@@ -227,7 +356,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         ColSrc src{qx, nullptr, (size_t)K, 0, {0, 1, 2, 3, 4}};
         stage_cols(src, NC, nb, nbp, act_s, dx_s, threadIdx.x, blockDim.x, false, true);
     }
-    __syncthreads();
     __shared__ uint32_t consts[kConstWords];
     if (threadIdx.x == 0) write_consts(consts);
     __syncthreads();
@@ -237,16 +365,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     const Codebook cb = read_consts(consts);
     for (int g = g0; g < g1; ++g) {
         const int64_t row = (int64_t)g * 32 + lane;
+        // the pair and half of logical group g
+        const int p = W.split ? (g < W.split ? g : g - W.split) : g >> 1;
+        const int h = W.split ? (g < W.split ? 0 : 1) : g & 1;
+        const uint8_t *pw = W.w + (size_t)p * pair_bytes(nbp);
         for (int q = q0; q < q1; ++q) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int b = 4 * q + j;
-                const uint4 w = ld_stream16(qs + ((size_t)g * nbp + b) * 32 + lane);
+                const uint4 w = ld_stream16(reinterpret_cast<const uint4 *>(pw + field_offset(nbp, h, b, lane)));
                 int sd[NC];
                 block_dots<NC>(cb, w, act_s + (size_t)b * NC * 2, sd);
-                if (row < M && b < nb) {
+                if (row < W.M && b < nb) {
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) sdot[((size_t)c * M + row) * nb + b] = sd[c] - cb.seed;
+                    for (int c = 0; c < NC; ++c) sdot[((size_t)c * W.M + row) * nb + b] = sd[c] - cb.seed;
                 }
             }
         }
@@ -305,6 +437,22 @@ static cudaError_t resident(Kernel kern, int threads, size_t smem, int *sms, int
     return cudaSuccess;
 }
 
+// Dynamic shared memory the dense kernels may use: the opt-in limit less
+// the largest static shared memory of their instances.
+cudaError_t matvec_smem_limit(size_t *bytes) {
+    size_t optin = 0, st = 0;
+    cudaError_t e = device_smem_limit(&optin);
+    void (*kerns[])(const MatvecArgs) = {k_matvec<1, true>,  k_matvec<1, false>, k_matvec<2, false>,
+                                         k_matvec<3, false>, k_matvec<4, false>, k_matvec<5, false>};
+    for (auto k : kerns) {
+        cudaFuncAttributes fa;
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k);
+        if (e == cudaSuccess) st = std::max(st, fa.sharedSizeBytes);
+    }
+    *bytes = e == cudaSuccess ? optin - st : 0;
+    return e;
+}
+
 cudaError_t device_smem_limit(size_t *bytes) {
     int dev = 0, v = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -344,7 +492,7 @@ static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const floa
                                    cudaStream_t s, bool pdl) {
     const size_t smem = matvec_smem_bytes(W.nbp, NC);
     int grid = 0;
-    cudaError_t e = dynamic_grid(k_matvec<NC, kF32>, smem, W.G, &grid);
+    cudaError_t e = dynamic_grid(k_matvec<NC, kF32>, smem, W.P, &grid);
     if (e != cudaSuccess) return e;
     MatvecArgs A;
     A.W = W;
@@ -379,8 +527,7 @@ static cudaError_t launch_block_dots_n(const DevMat &W, const int8_t *qx, int32_
     int grid = 0, chunk = 0;
     cudaError_t e = persistent_grid(k_block_dots<NC>, kThreads, smem, W.G, &grid, &chunk);
     if (e != cudaSuccess) return e;
-    k_block_dots<NC><<<grid, kThreads, smem, s>>>(W.qs, W.sc, W.M, W.G, W.nb, W.nbp, qx, (int64_t)W.nb * kQK, sdot,
-                                                  chunk);
+    k_block_dots<NC><<<grid, kThreads, smem, s>>>(W, qx, (int64_t)W.nb * kQK, sdot, chunk);
     return cudaGetLastError();
 }
 
@@ -397,6 +544,9 @@ cudaError_t launch_block_dots(const DevMat &W, const int8_t *qx, int n, int32_t 
 
 // --------------------------------------------------------- routed experts --
 
+// Largest token (in blocks of 32) the layer kernel stages for itself.
+constexpr int kMaxStagedBlocks = 1024;
+
 struct MoeArgs {
     DevMoe L;
     MoeWork ws;
@@ -406,23 +556,29 @@ struct MoeArgs {
     float *y;
     int n_tok, k, swiglu;
     int nbH, nbpH, nbF, nbpF;
-    int act_blocks;    // staged-activation capacity in blocks (tokens, then down columns)
-    int quant_tokens;  // the consumers quantize h themselves (one token, h 16-byte aligned)
-    int stages;        // pipeline depth (3 or 4: as many as two CTAs per SM allow)
+    int quant_tokens;  // one token, h 16-byte aligned: the consumers quantize it themselves
+    int stages;        // pipeline depth (4, or 3 where two CTAs per SM allow no more)
 };
 
-// Distinct in-range expert ids of the routing table, ascending but the shared
-// expert first (its items, with a column for every token, are the slowest:
-// handed out first, they do not form the tail of a pass), computed
-// redundantly by every CTA from the <= 85 slots (no host round trip).  Slots
-// 0..N-1 are the routed ones (p = t*k + j); with a shared expert, slots
-// N..N+n_tok-1 hold its virtual id E, one per token.  An out-of-range routed
-// id is stored as -1, so it matches no expert, the shared one included.
+// The routing table of one call, derived redundantly by every CTA from the
+// <= 85 slots (no host round trip).  Slots 0..N-1 are the routed ones
+// (p = t*k + j); with a shared expert, slots N..N+n_tok-1 hold its virtual
+// id E, one per token.  An out-of-range routed id is stored as -1, so it
+// matches no expert, the shared one included.  The distinct experts are
+// ordered with the shared expert first (its items, with a column for every
+// token, are the slowest: handed out first, they do not form the tail of a
+// pass), then by id; each is split into column groups of at most kMaxCols
+// slots (more slots than that only with repeated ids), its "virtual
+// experts": every item works on one virtual expert.
 struct Routing {
     int ids[kMaxSlots];
-    int uniq[kMaxSlots];
     unsigned char first[kMaxSlots];
-    int D;
+    int uniq[kMaxSlots];
+    int v0[kMaxSlots];                       // first virtual expert of distinct expert u
+    int vexp[kMaxSlots];                     // expert id of virtual expert v
+    unsigned char vnc[kMaxSlots];            // its columns (1..kMaxCols)
+    unsigned char vslot[kMaxSlots][kMaxCols];  // its slots, ascending
+    int D, V;
 };
 
 __device__ void route(const int32_t *__restrict__ ids, int N, int n_all, int E, Routing &R, unsigned *err) {
@@ -461,64 +617,50 @@ __device__ void route(const int32_t *__restrict__ ids, int N, int n_all, int E, 
         R.D = D;
     }
     __syncthreads();
+    int ns = 0;  // slots of distinct expert t
+    if (t < R.D) {
+        for (int p = 0; p < n_all; ++p) ns += R.ids[p] == R.uniq[t];
+        R.v0[t] = (ns + kMaxCols - 1) / kMaxCols;  // its virtual experts, made a prefix sum below
+    }
+    __syncthreads();
+    if (t == 0) {
+        int v = 0;
+        for (int u = 0; u < R.D; ++u) {
+            const int c = R.v0[u];
+            R.v0[u] = v;
+            v += c;
+        }
+        R.V = v;
+    }
+    __syncthreads();
+    if (t < R.D) {
+        const int e = R.uniq[t];
+        int n = 0;
+        for (int p = 0; p < n_all; ++p) {
+            if (R.ids[p] != e) continue;
+            const int v = R.v0[t] + n / kMaxCols, c = n % kMaxCols;
+            R.vslot[v][c] = (unsigned char)p;
+            if (c == 0) {
+                R.vexp[v] = e;
+                R.vnc[v] = (unsigned char)min(kMaxCols, ns - n);
+            }
+            ++n;
+        }
+    }
+    __syncthreads();
 }
 
 // Token of slot p: routed slots are t*k + j, shared-expert slots N + t.
 __device__ __forceinline__ int slot_token(int p, int N, int k) { return p < N ? p / k : p - N; }
 
 // Weights of expert e, the shared expert for e == E.
-struct ExpertMat {
-    const uint4 *qs;
-    const uint2 *sc;
-};
-
-__device__ __forceinline__ ExpertMat gate_up_of(const DevMoe &L, int e) {
-    if (e < L.E) return {L.gu_qs + (size_t)e * L.gu_qs_stride, L.gu_sc + (size_t)e * L.gu_sc_stride};
-    return {L.sh_gu_qs, L.sh_gu_sc};
+__device__ __forceinline__ const uint8_t *gate_up_of(const DevMoe &L, int e) {
+    return e < L.E ? L.gu + (size_t)e * L.gu_stride : L.sh_gu;
 }
 
-__device__ __forceinline__ ExpertMat down_of(const DevMoe &L, int e) {
-    if (e < L.E) return {L.dn_qs + (size_t)e * L.dn_qs_stride, L.dn_sc + (size_t)e * L.dn_sc_stride};
-    return {L.sh_dn_qs, L.sh_dn_sc};
+__device__ __forceinline__ const uint8_t *down_of(const DevMoe &L, int e) {
+    return e < L.E ? L.dn + (size_t)e * L.dn_stride : L.sh_dn;
 }
-
-// Slots of expert e (ascending) found by one warp with ballots over the
-// routing table, without shared state or a CTA barrier: returns the slot
-// count and the slots with ranks c0..c0+kMaxCols-1 in sl[] (-1 past the end).
-struct Slots {
-    int ns;
-    int sl[kMaxCols];
-};
-
-__device__ __forceinline__ Slots warp_slots(const Routing &R, int e, int N, int c0, int lane) {
-    Slots S;
-    S.ns = 0;
-#pragma unroll
-    for (int c = 0; c < kMaxCols; ++c) S.sl[c] = -1;
-    for (int base = 0; base < N; base += 32) {
-        const bool hit = base + lane < N && R.ids[base + lane] == e;
-        unsigned mask = __ballot_sync(0xffffffffu, hit);
-        while (mask) {
-            const int p = base + __ffs(mask) - 1;
-            mask &= mask - 1;
-            const int r = S.ns++ - c0;
-#pragma unroll
-            for (int c = 0; c < kMaxCols; ++c)
-                if (r == c) S.sl[c] = p;
-        }
-    }
-    return S;
-}
-
-// Number of slots of expert uniq[u] (any thread, from the routing table).
-__device__ __forceinline__ int expert_ns(const Routing &R, int u, int N) {
-    const int e = R.uniq[u];
-    int ns = 0;
-    for (int p = 0; p < N; ++p) ns += R.ids[p] == e;
-    return ns;
-}
-
-__device__ __forceinline__ int col_chunks(int ns) { return (ns + kMaxCols - 1) / kMaxCols; }
 
 constexpr unsigned kErrDependencyTimeout = 0x200u;
 constexpr unsigned kDownGrab = 4;
@@ -529,212 +671,235 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     return v;
 }
 
-// Bounded wait (thread 0) for expert rank u's intermediate columns: all its
-// gate_up items published (done[u] == target).  On timeout it sets
-// kErrDependencyTimeout and the CTA's abort flag; it returns false then, or
-// at once when the CTA already gave up.
-__device__ __forceinline__ bool wait_dependency(const unsigned *done, unsigned target, const Pipe &P) {
-    if (ld_acquire(done) >= target) return true;
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        if (*(volatile int *)P.abort) return false;
-        __nanosleep(64);
-        if (ld_acquire(done) >= target) return true;
-        if (global_ns() - t0 > kWaitLimitNs) break;
+// Bounded wait (the producer lane) until *cnt >= target: the intermediate
+// columns a down stage reads are all published.  On timeout it sets
+// kErrDependencyTimeout; it returns false then, or at once when the CTA
+// already gave up.  On success the bulk copies issued next may read what the
+// publishing CTAs wrote (the acquire load orders it, the proxy fence carries
+// that order to the copy engine).
+__device__ __forceinline__ bool wait_dependency(const unsigned *cnt, unsigned target, const Pipe &P) {
+    if (ld_acquire(cnt) < target) {
+        const uint64_t t0 = global_ns();
+        for (;;) {
+            if (*(volatile int *)P.abort) return false;
+            __nanosleep(100);
+            if (ld_acquire(cnt) >= target) break;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                atomicOr(P.err, kErrDependencyTimeout);
+                return false;
+            }
+        }
     }
-    atomicOr(P.err, kErrDependencyTimeout);
-    *(volatile int *)P.abort = 1;
-    return false;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
 }
 
 // The whole routed-expert layer but the combine, in one persistent kernel.
-// Work items, handed out in this order (the first per CTA is its index, the
-// rest come from one counter):
-//   it <  D*Gf : gate_up item (expert rank u, 32-row-pair group g), u-major:
-//                gate rows 32g.. and up rows F+32g.. in one format-B pass,
-//                then the SwiGLU split and the requantization of the 32
-//                outputs of each column;
-//   it >= D*Gf : down item (expert rank u, 64-row group g: 32-row groups 2g
-//                and 2g+1), u-major, per-slot outputs to obuf.
-// A CTA takes a down item only after every gate_up item has been taken, and
-// taken gate_up items never wait, so a down item's wait for its expert's
-// intermediate (done[u] == Gf * ns) always ends; it is bounded all the same.
-// The producer streams a down item's weights before that wait ends.
-// Launched as a programmatic dependent either way.  With one token (quantized
-// here) this is the call's first kernel: it sets up its pipeline, then waits
-// for all earlier work before it reads anything or lets the combine start.
+// Work items, in this order (the first per CTA is its index, the rest come
+// from one counter):
+//   it <  V*Gf : gate_up item (virtual expert v, 32-row-pair group g), v-major:
+//                gate rows 32g.. and up rows F+32g.. in one format-B pass; the
+//                epilogue warp applies the SwiGLU split and requantizes the
+//                32 outputs of each column (block g of the column's a);
+//   it >= V*Gf : down item (virtual expert v, 64-row group g: 32-row groups 2g
+//                and 2g+1), v-major, per-slot outputs to obuf.
+// A down stage covering blocks [16s, 16s+16) of a reads only the blocks that
+// gate_up groups 16s..16s+15 of its virtual expert wrote: the producer waits
+// (bounded) for that count before it copies the slice.  The gate_up items are
+// all handed out before any down item, and taken items never wait for later
+// ones, so the wait always ends.
+// With one token (quantized here) this is the call's first kernel, launched
+// as a programmatic dependent: it sets up its pipeline, then waits for all
+// earlier work before it reads anything or lets the combine start.
 // Otherwise it follows the quantization kernel, which starts it only once all
 // earlier work has ended, so the routing table and the handle's counters are
-// read before the wait for the quantized tokens.
+// read at once; the producer waits for the quantized tokens before it copies
+// their first slice.
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__ MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
-    __shared__ int dep_ok;
-    const PipeSmem S = carve_pipe(smem, A.stages, A.act_blocks, A.ws.err);
+    PipeSmem S = carve_pipe(smem, A.stages, kStageBytesAct, kSetBytes, 2, A.quant_tokens ? A.nbpH : 0, A.ws.err);
     pipe_init(S.pipe);
     if (A.quant_tokens) pdl_wait();
     pdl_trigger();  // the combine kernel may launch; it waits for this grid
-    const int N = A.n_tok * A.k + (A.L.shared ? A.n_tok : 0);  // routed slots, then shared ones
-    route(A.ids, A.n_tok * A.k, N, A.L.E, R, blockIdx.x == 0 ? A.ws.err : nullptr);  // ends with a CTA barrier
+    const int N = A.n_tok * A.k, n_all = N + (A.L.shared ? A.n_tok : 0);  // routed slots, then shared ones
+    route(A.ids, N, n_all, A.L.E, R, blockIdx.x == 0 ? A.ws.err : nullptr);  // ends with a CTA barrier
     const int Gf = A.L.F / 32, Gd = A.L.H / 32, Gd2 = (Gd + 1) / 2;
-    const unsigned total_gu = (unsigned)(R.D * Gf);
-    const unsigned total = total_gu + (unsigned)(R.D * Gd2);
+    const int nsF = (A.nbpF + kChunk - 1) / kChunk;  // down stages (dependency counters per virtual expert)
+    const int nchH = (A.nbpH + kChunk - 1) / kChunk;
+    const unsigned total_gu = (unsigned)(R.V * Gf);
+    const unsigned total = total_gu + (unsigned)(R.V * Gd2);
+    const size_t qa_region = act_bytes(A.nbpF, kMaxCols);
+    const size_t pbH = pair_bytes(A.nbpH), pbF = pair_bytes(A.nbpF);
     unsigned *sched = A.ws.sched;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == kConsumerWarps) {  // producer
+    if (warp == kProducerWarp) {
         if (lane == 0) {
             Producer pr;
-            const int nbqH = A.nbpH / 4, nbqF = A.nbpF / 4;
+            bool tokens_ready = A.quant_tokens != 0;  // else the quantization kernel's output needs the wait
             unsigned base = blockIdx.x, grab = 1;  // first item: the CTA index
             while (base < total && !pr.stopped) {
                 // the next grab (gate_up items one at a time; down items by
                 // guided grabs of up to kDownGrab consecutive items of one
-                // expert, which share staged columns) is fetched before this
-                // one's stages are issued, so the atomic's latency overlaps them
-                const unsigned seen = gridDim.x + *(volatile unsigned *)sched;
-                const unsigned ngrab = seen < total_gu ? 1u : max(1u, min(kDownGrab, (total - seen) / (2u * gridDim.x)));
-                const unsigned nbase = seen < total ? gridDim.x + atomicAdd(sched, ngrab) : total;
+                // virtual expert, sized from where this CTA's last grab ended)
+                // is fetched when this one starts and used once its stages are
+                // issued, so the atomic's latency overlaps them
+                const unsigned seen = base + grab;
+                const unsigned ngrab = seen < total_gu ? 1u : max(1u, min(kDownGrab, (total - min(total, seen)) / (2u * gridDim.x)));
+                const unsigned nbase = gridDim.x + atomicAdd(sched, ngrab);
                 for (unsigned it = base; it < min(total, base + grab) && !pr.stopped; ++it) {
                     if (it < total_gu) {
-                        const int u = (int)it / Gf, g = (int)it - u * Gf;
-                        const ExpertMat w = gate_up_of(A.L, R.uniq[u]);
-                        const size_t ga = (size_t)g, gb = (size_t)g + Gf;
-                        const int nch = col_chunks(expert_ns(R, u, N));
-                        for (int ch = 0; ch < nch; ++ch) {
-                            if (A.ws.stall == 2 && blockIdx.x == 0 && pr.it == 0) {
-                                // give-up test mode: CTA 0's first stage is claimed and
-                                // tagged but never filled, so its consumers' wait runs out
-                                pr.tag_only(S.pipe, (int)it);
-                                continue;
-                            }
-                            pr.group_b(S.pipe, w.qs + ga * A.nbpH * 32, w.sc + ga * nbqH * 32, w.qs + gb * A.nbpH * 32,
-                                       w.sc + gb * nbqH * 32, A.nbpH, (int)it);
+                        const int v = (int)it / Gf, g = (int)it - v * Gf;
+                        const uint8_t *w = gate_up_of(A.L, R.vexp[v]) + (size_t)g * pbH;
+                        if (A.ws.stall == 2 && blockIdx.x == 0 && pr.it == 0) {
+                            // give-up test mode: CTA 0's first stage is claimed and
+                            // tagged but never filled, so its consumers' wait runs out
+                            pr.tag_only(S.pipe, (int)it);
+                            continue;
                         }
+                        if (!tokens_ready) {
+                            pdl_wait();
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                            tokens_ready = true;
+                        }
+                        const ActSlice act{A.ws.qh, A.quant_tokens ? 0 : A.n_tok};
+                        pr.pass(S.pipe, w, A.nbpH, 0, nchH, (int)it, act, [](int) { return true; });
                     } else {
-                        const int j = (int)(it - total_gu);
-                        const int u = j / Gd2, g = j - u * Gd2;
-                        const ExpertMat w = down_of(A.L, R.uniq[u]);
-                        const size_t ga = 2 * (size_t)g, gb = ga + 1;
-                        const bool two = (int)gb < Gd;
-                        const int nch = col_chunks(expert_ns(R, u, N));
-                        for (int ch = 0; ch < nch; ++ch)
-                            pr.group_b(S.pipe, w.qs + ga * A.nbpF * 32, w.sc + ga * nbqF * 32,
-                                       two ? w.qs + gb * A.nbpF * 32 : nullptr, w.sc + gb * nbqF * 32, A.nbpF,
-                                       (int)it);
+                        const int j = (int)(it - total_gu), v = j / Gd2, g = j - v * Gd2;
+                        const uint8_t *w = down_of(A.L, R.vexp[v]) + (size_t)g * pbF;
+                        const ActSlice act{A.ws.qa_bm + v * qa_region, R.vnc[v]};
+                        const unsigned *cnt = A.ws.dep + (size_t)v * nsF;
+                        auto dep = [&](int c) {
+                            const unsigned target =
+                                A.ws.stall == 1 ? ~0u : (unsigned)min(kChunk, Gf - c * kChunk);
+                            return wait_dependency(cnt + c, target, S.pipe);
+                        };
+                        pr.pass(S.pipe, w, A.nbpF, 0, nsF, (int)it, act, dep);
                     }
                 }
                 base = nbase;
                 grab = ngrab;
             }
-            __threadfence();
-            sched_exit(sched);
             pr.finish(S.pipe);
             pr.drain(S.pipe);
         }
-        return;
-    }
-    // consumers: stage the quantized tokens, quantizing one token here or
-    // reading those of the quantization kernel launched just before
-    if (A.quant_tokens) {
-        quant_stage_cols<1>(A.h, A.L.H, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
-    } else {
-        pdl_wait();
-        ColSrc src{A.ws.qh, A.ws.dh, (size_t)A.L.H, (size_t)A.nbH, {0, 1, 2, 3, 4}};
-        stage_cols(src, A.n_tok, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
-    }
-    consumer_sync();
-    Consumer co(S.pipe);
-    int staged_u = -1, n = 0;
-    bool dead = false;  // a dependency wait gave up: no later item computes or writes
-    for (;;) {
-        const int it = co.next_item(S.pipe);
-        if (it < 0) break;
-        const bool gu = (unsigned)it < total_gu;
-        int u, g;
-        if (gu) {
-            u = it / Gf;
-            g = it - u * Gf;
-        } else {
-            const int j = it - (int)total_gu;
-            u = j / Gd2;
-            g = j - u * Gd2;
-        }
-        const int e = R.uniq[u];
-        for (int c0 = 0;; c0 += kMaxCols, ++n) {
-            const Slots sl = warp_slots(R, e, N, c0, lane);
-            const int nc = min(kMaxCols, sl.ns - c0);
-            int col_off[kMaxCols];
-            if (gu) {
+    } else if (warp == kEpilogueWarp) {
+        SetReader rd;
+        for (;;) {
+            const int *tagp;
+            const float *part;
+            if (!rd.wait(S.pipe, tagp, part)) break;
+            const int it = *(volatile const int *)tagp;
+            if (it < 0) break;
+            if ((unsigned)it < total_gu) {
+                // gate sums in row set 0, up sums in row set 1 of every warp's slice
+                const int v = it / Gf, g = it - v * Gf, nc = R.vnc[v];
+                float gs[kMaxCols], us[kMaxCols];
 #pragma unroll
-                for (int c = 0; c < kMaxCols; ++c)
-                    col_off[c] = (c < nc ? slot_token(sl.sl[c], A.n_tok * A.k, A.k) : 0) * A.nbpH;
-            } else {
+                for (int c = 0; c < kMaxCols; ++c) {
+                    gs[c] = us[c] = 0.0f;
+                    if (c < nc) {
 #pragma unroll
-                for (int c = 0; c < kMaxCols; ++c) col_off[c] = c * A.nbpF;
-                if (staged_u != u || sl.ns > kMaxCols) {
-                    consumer_sync();  // the tokens (or the previous columns) are no longer read
-                    if (threadIdx.x == 0)  // wait for expert u's intermediate
-                        dep_ok = !dead && wait_dependency(A.ws.done + u, A.ws.stall == 1 ? ~0u : (unsigned)(Gf * sl.ns),
-                                                          S.pipe);
-                    consumer_sync();
-                    dead = dead || !dep_ok;
-                    if (!dead) {
-                        ColSrc src{A.ws.qa, A.ws.da, (size_t)A.L.F, (size_t)A.nbF, {}};
-#pragma unroll
-                        for (int c = 0; c < kMaxCols; ++c) src.row[c] = max(sl.sl[c], 0);
-                        stage_cols(src, nc, A.nbF, A.nbpF, S.act, S.dx, threadIdx.x, kConsumers, true);
+                        for (int w = 0; w < kConsumerWarps; ++w) {
+                            gs[c] += part[(w * 2 * kMaxCols + c) * 32 + lane];
+                            us[c] += part[(w * 2 * kMaxCols + kMaxCols + c) * 32 + lane];
+                        }
                     }
-                    consumer_sync();
-                    staged_u = u;
                 }
-            }
-            float *P0 = S.part + (n & 1) * kPartSetB;
-            sweep_b(co, S.pipe, gu ? A.nbpH : A.nbpF, S.act, S.dx, col_off, nc, P0 + warp * (2 * kMaxCols * 32),
-                    !dead, warp, lane);
-            consumer_sync();
-            if (!dead && gu && warp < nc) {
-                // SwiGLU split and requantization of column `warp`: gate sums in
-                // row set 0, up sums in row set 1 of every warp's slice
-                const int c = warp;
-                float gs = 0.0f, us = 0.0f;
+                rd.release(S.pipe);
+                // block g of the intermediate: chunk c, block j of the chunk
+                const int ca = g / kChunk, j = g - ca * kChunk, nblk = chunk_blocks(A.nbpF, ca);
+                int8_t *base = A.ws.qa_bm + v * qa_region + act_chunk_offset(ca, nc);
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    gs += P0[(w * 2 * kMaxCols + c) * 32 + lane];
-                    us += P0[(w * 2 * kMaxCols + kMaxCols + c) * 32 + lane];
+                for (int c = 0; c < kMaxCols; ++c) {
+                    if (c >= nc) continue;
+                    const float a = A.swiglu ? gs[c] / (1.0f + expf(-gs[c])) * us[c] : gs[c] * us[c];
+                    float d;
+                    const int8_t q = quant_lane(a, d);
+                    base[(size_t)(j * nc + c) * 32 + expander_pos(lane)] = q;
+                    if (lane == 0)
+                        *reinterpret_cast<float *>(base + (size_t)32 * nc * nblk + ((size_t)(j >> 1) * nc + c) * 8 +
+                                                   (j & 1) * 4) = d;
+                    if (A.ws.keep_a) {  // the intermediate by slot, in plain order (checking entry points)
+                        const int p = R.vslot[v][c];
+                        const size_t o = (size_t)p * A.L.F + (size_t)g * 32 + lane;
+                        A.ws.a_dbg[o] = a;
+                        A.ws.qa[o] = q;
+                        if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
+                    }
                 }
-                const float a = A.swiglu ? gs / (1.0f + expf(-gs)) * us : gs * us;
-                float d;
-                const int8_t q = quant_lane(a, d);
-                const int p = pick(sl.sl, c);
-                const size_t o = (size_t)p * A.L.F + (size_t)g * 32 + lane;
-                A.ws.qa[o] = q;
-                if (lane == 0) A.ws.da[(size_t)p * A.nbF + g] = d;
-                if (A.ws.keep_a) A.ws.a_dbg[o] = a;
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) atomicAdd(A.ws.done + u, 1u);
-            } else if (!dead && !gu) {
+                if (lane == 0) atomicAdd(A.ws.dep + (size_t)v * nsF + g / kChunk, 1u);
+            } else {
                 // down outputs: row set r of column c, for i = 2c + r
-                for (int i = warp; i < 2 * nc; i += kConsumerWarps) {
-                    const int c = i >> 1, r = i & 1;
-                    float v = 0.0f;
+                const int j = it - (int)total_gu, v = j / Gd2, g = j - v * Gd2, nc = R.vnc[v];
+                float o[2 * kMaxCols];
 #pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) v += P0[(w * 2 * kMaxCols + r * kMaxCols + c) * 32 + lane];
-                    const int grp = 2 * g + r;
-                    if (grp < Gd) A.ws.obuf[(size_t)pick(sl.sl, c) * A.L.H + (size_t)grp * 32 + lane] = v;
+                for (int i = 0; i < 2 * kMaxCols; ++i) {
+                    o[i] = 0.0f;
+                    if (i < 2 * nc) {
+#pragma unroll
+                        for (int w = 0; w < kConsumerWarps; ++w)
+                            o[i] += part[(w * 2 * kMaxCols + (i & 1) * kMaxCols + (i >> 1)) * 32 + lane];
+                    }
+                }
+                rd.release(S.pipe);
+#pragma unroll
+                for (int i = 0; i < 2 * kMaxCols; ++i) {
+                    const int grp = 2 * g + (i & 1);
+                    if (i < 2 * nc && grp < Gd)
+                        A.ws.obuf[(size_t)R.vslot[v][i >> 1] * A.L.H + (size_t)grp * 32 + lane] = o[i];
                 }
             }
-            if (c0 + kMaxCols >= sl.ns) break;
         }
-        ++n;
+    } else {
+        if (A.quant_tokens) quant_stage_cols<1>(A.h, A.L.H, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
+        consumer_sync();
+        Consumer co(S.pipe);
+        SetWriter wr;
+        for (;;) {
+            const int it = co.wait(S.pipe) ? co.tag(S.pipe) : -1;
+            int *tagw;
+            float *part;
+            if (!wr.acquire(S.pipe, tagw, part)) break;
+            if (it < 0) {
+                if (threadIdx.x == 0) *tagw = -1;
+                wr.publish(S.pipe);
+                break;
+            }
+            const bool gu = (unsigned)it < total_gu;
+            const int v = gu ? it / Gf : (it - (int)total_gu) / Gd2;
+            const int nc = R.vnc[v], nbp = gu ? A.nbpH : A.nbpF;
+            int col[kMaxCols];
+            ActView V;
+            if (!gu) {  // the stage's slice holds the virtual expert's columns
+                V = ActView{nullptr, nullptr, nc, true};
+#pragma unroll
+                for (int c = 0; c < kMaxCols; ++c) col[c] = c;
+            } else if (A.quant_tokens) {  // the one token, staged here
+                V = ActView{S.act, S.dx, 1, false};
+#pragma unroll
+                for (int c = 0; c < kMaxCols; ++c) col[c] = 0;
+            } else {  // the stage's slice holds every token: a column's slot is its token
+                V = ActView{nullptr, nullptr, A.n_tok, true};
+#pragma unroll
+                for (int c = 0; c < kMaxCols; ++c) col[c] = c < nc ? slot_token(R.vslot[v][c], N, A.k) : 0;
+            }
+            const bool ok = sweep_b(co, S.pipe, 0, nbp, nbp, V, col, nc, part + warp * (2 * kMaxCols * 32), warp, lane);
+            if (threadIdx.x == 0) *tagw = it;
+            wr.publish(S.pipe);
+            if (!ok) break;
+        }
     }
-    // the last CTA to finish resets the per-expert counts for the next call
-    consumer_sync();
+    // the last CTA to finish resets the counters for the next call
+    __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        if (atomicAdd(A.ws.sched + 2, 1u) == gridDim.x - 1) {
-            for (int u = 0; u < R.D; ++u) A.ws.done[u] = 0u;
-            A.ws.sched[2] = 0u;
+        if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+            for (int i = 0; i < R.V * nsF; ++i) A.ws.dep[i] = 0u;
+            sched[0] = 0u;
+            sched[1] = 0u;
         }
     }
 }
@@ -797,29 +962,29 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     A.nbpH = round_up4(A.nbH);
     A.nbF = L.F / kQK;
     A.nbpF = round_up4(A.nbF);
-    // one token: the layer kernel quantizes it (one launch fewer)
-    A.quant_tokens = n_tok == 1 && ((uintptr_t)h & 15u) == 0;
-    A.act_blocks = std::max((A.quant_tokens ? 1 : n_tok) * A.nbpH, kMaxCols * A.nbpF);
+    // one token: the layer kernel quantizes it (one launch fewer), as long as
+    // its staging leaves room for the pipeline in shared memory
+    A.quant_tokens = n_tok == 1 && ((uintptr_t)h & 15u) == 0 && A.nbpH <= kMaxStagedBlocks;
     cudaError_t e = cudaSuccess;
     if (ws.ev[0] && (e = cudaEventRecord(ws.ev[0], s)) != cudaSuccess) return e;
     if (!A.quant_tokens) {
-        e = launch_quantize(h, L.H, n_tok, ws.qh, ws.dh, s);
+        e = launch_quantize_chunked(h, L.H, n_tok, ws.qh, s);
         if (e != cudaSuccess) return e;
     }
-    const int64_t max_experts = std::min(n_tok * k, L.E) + (L.shared ? 1 : 0);
-    const int64_t items = max_experts * (L.F / 32 + (L.H / 32 + 1) / 2);
     {
         // four stages when two CTAs per SM still fit, else three
+        const int act_blocks = A.quant_tokens ? A.nbpH : 0;
         int grid = 0, sms = 0, per_sm = 0;
         A.stages = 4;
-        size_t smem = moe_smem_bytes(A.act_blocks, A.stages);
+        size_t smem = moe_smem_bytes(act_blocks, A.stages);
         e = resident(k_moe, kPipeThreads, smem, &sms, &per_sm);
         if (e != cudaSuccess) return e;
         if (per_sm < 2) {
             A.stages = 3;
-            smem = moe_smem_bytes(A.act_blocks, A.stages);
+            smem = moe_smem_bytes(act_blocks, A.stages);
         }
-        e = dynamic_grid(k_moe, smem, items, &grid);
+        const int64_t n_all = (int64_t)n_tok * k + (L.shared ? n_tok : 0);
+        e = dynamic_grid(k_moe, smem, n_all * (L.F / 32 + (L.H / 32 + 1) / 2), &grid);
         if (e != cudaSuccess) return e;
         e = launch_k(k_moe, grid, kPipeThreads, smem, s, true, A);
         if (e != cudaSuccess) return e;
@@ -905,15 +1070,6 @@ cudaError_t launch_router_topk(const float *logits, int n_tok, int E, int k, int
     if (e != cudaSuccess) return e;
     k_router_topk<<<n_tok, 32, smem, s>>>(logits, E, k, ids, wts);
     return cudaGetLastError();
-}
-
-cudaError_t moe_smem_limit(size_t *bytes) {
-    size_t optin = 0;
-    cudaFuncAttributes fa;
-    cudaError_t e = device_smem_limit(&optin);
-    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k_moe);
-    *bytes = e == cudaSuccess ? optin - fa.sharedSizeBytes : 0;
-    return e;
 }
 
 

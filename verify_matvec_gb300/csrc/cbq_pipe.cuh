@@ -1,33 +1,38 @@
-// cbq_pipe.cuh -- the weight-stream pipeline of the matvec kernels.
+// cbq_pipe.cuh -- warp-specialised weight-stream pipeline of the matvec kernels.
 //
-// One producer warp per CTA moves the weight stream from HBM into a ring of
-// shared-memory stages with 1-D bulk copies (cp.async.bulk, the TMA's
-// non-tensor form), each stage completing on an mbarrier.  Eight consumer
-// warps wait for a stage, expand and dot it from shared memory, and release it
-// through a second mbarrier.  Every stage is 18 KB (16 KB of index fields,
-// 2 KB of scales) in one of two formats:
-//   format A: 32 block columns of one 32-row group (two bulk copies); warp w
-//             takes the 4-block quad w;
-//   format B: 16 block columns of two 32-row groups -- the gate and up rows of
-//             one SwiGLU group, or two down-projection groups -- (four bulk
-//             copies); warp w takes blocks 2w and 2w+1 of both groups, so the
-//             two rows of a lane share every activation load.
-// Both layouts are contiguous slices of the device layout (cbq_device.cuh).
+// A CTA has three roles:
+//   - a producer warp (one active lane) moves weight chunks from global memory
+//     into a ring of shared-memory stages with 1-D bulk copies (cp.async.bulk,
+//     the TMA's non-tensor form), each stage completing on an mbarrier; in the
+//     routed-expert kernel a stage also carries the activation slice its
+//     blocks are dotted with;
+//   - eight consumer warps wait for a stage, expand and dot it, release it
+//     through a second mbarrier, and at the end of a work item write their
+//     partial sums into one of two shared-memory sets;
+//   - an epilogue warp adds the eight partial sums of each item and finishes
+//     it (outputs, or SwiGLU, requantization and counters), then frees the set.
+// Consumer warps never wait for one another: each reads an item's tag from
+// the item's first stage, and the only barrier among them is the one after
+// the activations are staged at the start.
 //
-// Work is fetched per CTA: its first item is the CTA index (streamed at once,
-// before the kernel waits for the work ahead of it on the stream: weights are
-// never written by a call), later ones come from a global counter (atomicAdd;
-// the last CTA to exit resets it).  The producer tags every stage with its
-// item in a small shared header and closes the stream with a stage tagged -1
-// that carries no bytes.
+// A stage is one chunk of the device layout (cbq_internal.h): 16 block
+// columns of a pair of 32-row groups -- the gate and up rows of one SwiGLU
+// group, or two down-projection or dense groups -- with their scales, one
+// contiguous span brought in by one bulk copy; in the routed-expert kernel it
+// is followed by the activation slice of those 16 blocks (a second copy).
+// Warp w takes blocks 2w and 2w+1 of both groups, so the two rows of a lane
+// share every activation load.
+//
+// Work is fetched per CTA: its first item is the CTA index, later ones come
+// from a global counter (atomicAdd) whose result is fetched one item ahead.
+// The producer tags every stage with its item and closes the stream with a
+// stage tagged -1 that carries no bytes.
 //
 // Every wait is bounded: once it has waited kWaitLimitNs (global timer) it
-// sets kErrPipeTimeout in the handle's error word and a CTA-wide abort flag;
-// the other waits of the CTA then give up too.  Consumers decide at item
-// boundaries together (thread 0 reads the next tag and a barrier publishes
-// it), so every consumer warp runs the same sequence of stages and barriers
-// whatever fails; the producer waits for its own copies in flight before the
-// CTA exits.
+// sets kErrPipeTimeout in the handle's error word and a CTA-wide abort flag,
+// after which the other waits of the CTA give up at once.  A role that gives
+// up leaves its loop; no barrier inside the loops can be left waiting, and the
+// producer waits for its own copies in flight before the CTA exits.
 #pragma once
 
 #include <stdint.h>
@@ -35,17 +40,20 @@
 #include <cuda_fp16.h>
 
 #include "cbq_device.cuh"
+#include "cbq_internal.h"
 
 namespace cbq {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kPipeThreads = kConsumers + 32;   // + one producer warp
-constexpr int kStageQsBytes = 16384;
-constexpr int kStageScBytes = 2048;
-constexpr int kStageBytes = kStageQsBytes + kStageScBytes;  // 18,432
-constexpr int kChunkA = 32;  // block columns per format-A stage
-constexpr int kChunkB = 16;  // block columns per format-B stage (each of two row groups)
+constexpr int kEpilogueWarp = kConsumerWarps;      // warp 8
+constexpr int kProducerWarp = kConsumerWarps + 1;  // warp 9
+constexpr int kPipeThreads = (kConsumerWarps + 2) * 32;
+constexpr int kStageWeightBytes = kChunkBytes;  // 18,432: the weights of a full chunk
+// A stage with an activation slice: the weights, then up to kChunk x kMaxCols
+// staged blocks (32 bytes each) and their scales (4 bytes each).
+constexpr int kStageActBytes = kChunk * kMaxCols * 36;
+constexpr int kStageBytesAct = kStageWeightBytes + kStageActBytes;  // 21,312
 // Bounded waits: each poll suspends the warp until the phase completes or
 // kWaitHintNs pass (so a waiting warp takes no issue slots from the warps that
 // compute); a wait gives up after kWaitLimitNs in all.
@@ -100,15 +108,20 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 
 // Shared part of the pipeline (carved from dynamic shared memory).
 struct Pipe {
-    uint32_t *consts;  // kConstWords words: codebook and dp4a seed (read_consts)
-    uint32_t full0;    // shared address of full[0]: stage filled (producer arrive + bulk bytes)
-    uint32_t empty0;   // shared address of empty[0]: stage released (one arrive per consumer thread)
-    int *abort;        // CTA-wide give-up flag
-    int *tag;          // [S] item of each stage (-1: end of stream)
-    int *next;         // the item consumers take next (published by thread 0)
-    unsigned char *ring;
-    unsigned *err;     // error word of the handle (global memory)
+    uint32_t *consts;     // kConstWords words: codebook and dp4a seed (read_consts)
+    uint32_t full0;       // shared address of full[0]: stage filled (producer arrive + bulk bytes)
+    uint32_t empty0;      // shared address of empty[0]: stage released (one arrive per consumer thread)
+    uint32_t setfull0;    // shared address of setfull[0]: partial sums written (one arrive per consumer thread)
+    uint32_t setempty0;   // shared address of setempty[0]: set read (one arrive per epilogue lane)
+    int *abort;           // CTA-wide give-up flag
+    int *tag;             // [S] item of each stage (-1: end of stream)
+    unsigned char *ring;  // S stages of stage_bytes
+    unsigned char *sets;  // nsets sets of set_bytes: [item tag (16 bytes)][partial sums]
+    unsigned *err;        // error word of the handle (global memory)
     int S;
+    uint32_t stage_bytes;
+    uint32_t set_bytes;
+    uint32_t nsets;       // 1 or 2
 };
 
 // Bounded wait for phase `parity` of the barrier at shared address bar.
@@ -126,6 +139,14 @@ __device__ __forceinline__ bool pipe_wait(const Pipe &P, uint32_t bar, uint32_t 
     return false;
 }
 
+// Source of a stage's activation slice: `cols` columns in the chunked
+// activation layout (act_chunk_offset); the stage of chunk c copies its 36 *
+// cols * nblk bytes.  cols == 0: no slice.
+struct ActSlice {
+    const int8_t *base;
+    int cols;
+};
+
 // Producer side: a running count of issued stages.
 struct Producer {
     uint32_t it = 0;
@@ -142,46 +163,39 @@ struct Producer {
         return true;
     }
 
-    // Format A: the stages of one 32-row group over blocks [b0, b1) of its
-    // pass (qs_g, sc_g: the group's index and scale streams), tagged `tag`.
-    __device__ __forceinline__ void group_a(const Pipe &P, const uint4 *qs_g, const uint2 *sc_g, int b0, int b1,
-                                            int tag) {
-        for (int b = b0; b < b1 && !stopped; b += kChunkA) {
-            const int nblk = min(kChunkA, b1 - b);
+    // The stages of chunks [c0, c1) of a pass over a pair (its bytes at w,
+    // nbp blocks), tagged `tag`, each with its chunk of `act`.  dep(c) is
+    // called after chunk c's weight copy is issued and before its activation
+    // copy: it waits until the slice may be read and returns false to give up
+    // (the producer then stops).
+    template <typename Dep>
+    __device__ __forceinline__ void pass(const Pipe &P, const uint8_t *w, int nbp, int c0, int c1, int tag,
+                                         const ActSlice &act, Dep &&dep) {
+        for (int c = c0; c < c1 && !stopped; ++c) {
+            const int nblk = chunk_blocks(nbp, c);
             uint32_t slot;
             if (!claim(P, slot)) break;
-            const uint32_t dst = smem_addr(P.ring) + slot * (uint32_t)kStageBytes;
+            const uint32_t dst = smem_addr(P.ring) + slot * P.stage_bytes;
             const uint32_t bar = P.full0 + 8u * slot;
-            const uint32_t bq = (uint32_t)nblk * 512u, bs = (uint32_t)nblk / 4u * 256u;
+            const uint32_t bw = (uint32_t)nblk * (2 * kBlockBytes), ba = (uint32_t)(nblk * act.cols) * 36u;
             P.tag[slot] = tag;
-            mbar_expect_tx(bar, bq + bs);
-            bulk_g2s(dst, qs_g + (size_t)b * 32, bq, bar);
-            bulk_g2s(dst + kStageQsBytes, sc_g + (size_t)(b / 4) * 32, bs, bar);
+            mbar_expect_tx(bar, bw + ba);
+            bulk_g2s(dst, w + (size_t)c * kChunkBytes, bw, bar);
+            if (act.cols) {
+                if (!dep(c)) {  // the slice will never be ready: stop (the stage stays incomplete)
+                    stopped = true;
+                    *(volatile int *)P.abort = 1;
+                    ++it;
+                    break;
+                }
+                bulk_g2s(dst + kStageWeightBytes, act.base + act_chunk_offset(c, act.cols), ba, bar);
+            }
             ++it;
         }
     }
 
-    // Format B: the stages of two 32-row groups (a, and b unless qs_b is
-    // null) over blocks [0, nbp), tagged `tag`.
-    __device__ __forceinline__ void group_b(const Pipe &P, const uint4 *qs_a, const uint2 *sc_a, const uint4 *qs_b,
-                                            const uint2 *sc_b, int nbp, int tag) {
-        for (int b = 0; b < nbp && !stopped; b += kChunkB) {
-            const int nblk = min(kChunkB, nbp - b);
-            uint32_t slot;
-            if (!claim(P, slot)) break;
-            const uint32_t dst = smem_addr(P.ring) + slot * (uint32_t)kStageBytes;
-            const uint32_t bar = P.full0 + 8u * slot;
-            const uint32_t bq = (uint32_t)nblk * 512u, bs = (uint32_t)nblk / 4u * 256u;
-            P.tag[slot] = tag;
-            mbar_expect_tx(bar, qs_b ? 2u * (bq + bs) : bq + bs);
-            bulk_g2s(dst, qs_a + (size_t)b * 32, bq, bar);
-            bulk_g2s(dst + kStageQsBytes, sc_a + (size_t)(b / 4) * 32, bs, bar);
-            if (qs_b) {
-                bulk_g2s(dst + kStageQsBytes / 2, qs_b + (size_t)b * 32, bq, bar);
-                bulk_g2s(dst + kStageQsBytes + kStageScBytes / 2, sc_b + (size_t)(b / 4) * 32, bs, bar);
-            }
-            ++it;
-        }
+    __device__ __forceinline__ void pass(const Pipe &P, const uint8_t *w, int nbp, int c0, int c1, int tag) {
+        pass(P, w, nbp, c0, c1, tag, ActSlice{nullptr, 0}, [](int) { return true; });
     }
 
     // Give-up test mode only: claim a slot and tag it, but never fill it (the
@@ -208,7 +222,7 @@ struct Producer {
     // Wait for the copies still in flight (the last S issued stages) so the
     // CTA never exits while the TMA writes into its shared memory.  Each wait
     // is bounded like every other; a copy from mapped memory always completes,
-    // so the limit is only a guard against a broken device.
+    // so the limit only guards against a broken device.
     __device__ __forceinline__ void drain(const Pipe &P) {
         const uint32_t first = it > (uint32_t)P.S ? it - P.S : 0u;
         for (uint32_t k = first; k < it; ++k) pipe_wait(P, P.full0 + 8u * (k % P.S), (k / P.S) & 1u, false);
@@ -228,6 +242,9 @@ struct Consumer {
 
     __device__ __forceinline__ bool wait(const Pipe &P) { return pipe_wait(P, full, phase, true); }
 
+    // The item of the current stage (after a successful wait).
+    __device__ __forceinline__ int tag(const Pipe &P) const { return *(volatile int *)(P.tag + slot); }
+
     // Release the current stage (every consumer thread, after its own reads)
     // and move to the next slot.
     __device__ __forceinline__ void release(const Pipe &P) {
@@ -241,259 +258,334 @@ struct Consumer {
         } else {
             full += 8u;
             empty += 8u;
-            st += kStageBytes;
+            st += P.stage_bytes;
         }
-    }
-
-    // The item of the next stage, the same for every consumer warp: thread 0
-    // waits for the stage and reads its tag (-1 at the end of the stream or
-    // after a give-up), a consumer barrier publishes it.  The stage is not
-    // consumed.  Must be called by all consumer threads, with at least one
-    // consumer barrier between two calls (every item ends with one), so no
-    // warp still reads P.next when thread 0 rewrites it.
-    __device__ __forceinline__ int next_item(const Pipe &P) {
-        if (threadIdx.x == 0) *P.next = wait(P) ? *(volatile int *)(P.tag + slot) : -1;
-        consumer_sync();
-        return *(volatile int *)P.next;
     }
 };
 
-// ------------------------------------------------------ format A sweeps ---
+// The partial-sum sets (one or two), written in turn by the consumers (one
+// set per item) and read in the same turn by the epilogue warp.
+struct SetWriter {
+    uint32_t n = 0;  // items written
 
-// One 4-block quad of one row (this lane) for NC columns: the quad's index
-// words at qs[0], qs[32], qs[64], qs[96]; its four fp16 scales in s; the
-// activations block-major at act (block j of column c at act[(j*NC + c)*2]);
-// the activation scales as float2 pairs at dxp (blocks 0-1 of column c at
-// dxp[c], blocks 2-3 at dxp[NC + c]).
-template <int NC>
-__device__ __forceinline__ void quad_a(const Codebook &cb, const uint4 *qs, uint2 s, const uint4 *act,
-                                       const float2 *dxp, float2 acc[NC]) {
-    const float2 dw01 = __half22float2(*reinterpret_cast<const __half2 *>(&s.x));
-    const float2 dw23 = __half22float2(*reinterpret_cast<const __half2 *>(&s.y));
-    uint4 w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = qs[j * 32];
-#pragma unroll
-    for (int jj = 0; jj < 4; jj += 2) {  // blocks in pairs: fewer live sums
-        int sa[NC], sb[NC];
-        block_dots<NC>(cb, w[jj], act + jj * NC * 2, sa);
-        block_dots<NC>(cb, w[jj + 1], act + (jj + 1) * NC * 2, sb);
-        const float2 dw = jj == 0 ? dw01 : dw23;
-#pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = scale_acc2(acc[c], dw, dxp[(jj >> 1) * NC + c], sa[c], sb[c]);
+    // Wait until set n % nsets is free (the epilogue has read item n - nsets);
+    // gives its tag word and partial sums, or returns false on a give-up.
+    __device__ __forceinline__ bool acquire(const Pipe &P, int *&tag, float *&part) {
+        const uint32_t use = n / P.nsets, k = n - use * P.nsets;
+        if (use > 0 && !pipe_wait(P, P.setempty0 + 8u * k, (use - 1) & 1u, true)) return false;
+        tag = reinterpret_cast<int *>(P.sets + k * P.set_bytes);
+        part = reinterpret_cast<float *>(P.sets + k * P.set_bytes + 16);
+        return true;
+    }
+
+    // Every consumer thread, after its own writes to the set.
+    __device__ __forceinline__ void publish(const Pipe &P) {
+        mbar_arrive(P.setfull0 + 8u * (n % P.nsets));
+        ++n;
+    }
+};
+
+struct SetReader {
+    uint32_t n = 0;  // items read
+
+    __device__ __forceinline__ bool wait(const Pipe &P, const int *&tag, const float *&part) {
+        const uint32_t use = n / P.nsets, k = n - use * P.nsets;
+        if (!pipe_wait(P, P.setfull0 + 8u * k, use & 1u, true)) return false;
+        tag = reinterpret_cast<const int *>(P.sets + k * P.set_bytes);
+        part = reinterpret_cast<const float *>(P.sets + k * P.set_bytes + 16);
+        return true;
+    }
+
+    // Every epilogue lane, after its own reads of the set.
+    __device__ __forceinline__ void release(const Pipe &P) {
+        mbar_arrive(P.setempty0 + 8u * (n % P.nsets));
+        ++n;
+    }
+};
+
+// ------------------------------------------------------------- sweeps ---
+// The activations of a stage's blocks are staged block-major: block j (0..15
+// of the stage) of column slot x has its two words at act[(j*stride + x)*2]
+// and its scale at dx[((j>>1)*stride + x)*2 + (j&1)] (the scales of a block
+// pair side by side).  ActView gives, per stage, where block 0 of the stage
+// sits; col[] holds each column's slot x.  Each lane owns row `lane` of both
+// groups (row sets 0 and 1) of the stage.
+struct ActView {
+    const uint4 *act;  // persistent staging (stage_act == false) indexed from block 0
+    const float *dx;
+    int stride;        // column slots per block
+    bool stage_act;    // the stage carries its own slice (block 0 of the stage at its start)
+};
+
+__device__ __forceinline__ void stage_act_ptrs(const ActView &V, const unsigned char *st, int b, int nblk,
+                                               const uint4 *&a, const float *&d) {
+    if (V.stage_act) {
+        a = reinterpret_cast<const uint4 *>(st + kStageWeightBytes);
+        d = reinterpret_cast<const float *>(st + kStageWeightBytes + (size_t)nblk * V.stride * 32);
+    } else {
+        a = V.act + (size_t)b * V.stride * 2;
+        d = V.dx + (size_t)b * V.stride;
     }
 }
 
-// The stages of one format-A pass over blocks [b0, b1) for NC columns staged
-// block-major (act, dxp as quad_a, indexed from block 0), summed into acc.
-template <int NC>
-__device__ __forceinline__ void sweep_a(Consumer &co, const Pipe &P, int b0, int b1, const uint4 *act,
-                                        const float2 *dxp, float2 acc[NC], int warp, int lane) {
-    const uint4 *a = act + (size_t)(b0 + 4 * warp) * NC * 2;
-    const float2 *d = dxp + (size_t)((b0 + 4 * warp) >> 1) * NC;
-    for (int b = b0; b < b1; b += kChunkA) {
-        const bool ok = co.wait(P);
-        if (ok && b + 4 * warp < b1) {
-            const uint4 *qs = reinterpret_cast<const uint4 *>(co.st) + warp * 128 + lane;
-            const uint2 s = reinterpret_cast<const uint2 *>(co.st + kStageQsBytes)[warp * 32 + lane];
-            quad_a<NC>(co.cb, qs, s, a, d, acc);
-        }
-        co.release(P);
-        a += kChunkA * NC * 2;
-        d += kChunkA / 2 * NC;
-    }
+// The index fields of this lane's rows for this warp's first block in a
+// stage of nblk blocks (row set 0 at q0[0], q0[32]; row set 1 likewise at q1).
+__device__ __forceinline__ void stage_fields(const unsigned char *st, int nblk, int warp, int lane, const uint4 *&q0,
+                                             const uint4 *&q1) {
+    q0 = reinterpret_cast<const uint4 *>(st) + warp * 64 + lane;
+    q1 = reinterpret_cast<const uint4 *>(st + (size_t)nblk * kBlockBytes) + warp * 64 + lane;
 }
 
-// ------------------------------------------------------ format B sweeps ---
-// Columns are staged one after another (block b of the column at offset o
-// has its two words at act0[2*(o + b)] and its scale at dx0[o + b]); col_off
-// holds each column's offset o.  Each lane owns row `lane` of both row groups
-// (set 0, set 1) of the stage.
-
-// The fp16 scale pair of this warp's two blocks in row set r of the stage.
-__device__ __forceinline__ float2 stage_dw_b(const unsigned char *st, int r, int warp, int lane) {
-    const uint2 s = reinterpret_cast<const uint2 *>(st + kStageQsBytes + r * (kStageScBytes / 2))[(warp >> 1) * 32 + lane];
+// The fp16 scale pair of this warp's two blocks in row set r of a stage of
+// nblk blocks.
+__device__ __forceinline__ float2 stage_dw(const unsigned char *st, int nblk, int r, int warp, int lane) {
+    const uint2 s = reinterpret_cast<const uint2 *>(st + (size_t)(r * nblk) * kBlockBytes + (size_t)nblk * 512)
+        [(warp >> 1) * 32 + lane];
     const uint32_t h = (warp & 1) ? s.y : s.x;
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
-// One column: the two-word expansion, running sums of both row sets in
-// registers over the pass; written to part[r*kMaxCols*32 + lane] at its end.
-__device__ __forceinline__ void sweep_b1(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
-                                         int off, float *part, bool live, int warp, int lane) {
+// One column at slot x: the two-word expansion; running sums of both row
+// sets in registers over the pass, written to part[r*kMaxCols*32 + lane].
+__device__ __forceinline__ bool sweep_b1(Consumer &co, const Pipe &P, int b0, int b1, int nbp, const ActView &V, int x,
+                                         float *part, int warp, int lane) {
     float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
-    const uint4 *a = act0 + 2 * (off + 2 * warp);
-    const float *d = dx0 + off + 2 * warp;
-    for (int b = 0; b < nbp; b += kChunkB) {
-        const bool ok = co.wait(P);
-        if (ok && live && b + 2 * warp < nbp) {
-            const uint4 *q0 = reinterpret_cast<const uint4 *>(co.st) + warp * 64 + lane;
-            const uint4 *q1 = q0 + kChunkB * 32;
-            const float2 dw0 = stage_dw_b(co.st, 0, warp, lane), dw1 = stage_dw_b(co.st, 1, warp, lane);
-            const float2 dx2 = *reinterpret_cast<const float2 *>(d);
+    const int j = 2 * warp;  // this warp's first block in a stage
+    bool ok = true;
+    for (int b = b0; b < b1; b += kChunk) {
+        if (b > b0) ok = ok && co.wait(P);
+        const int nblk = min(kChunk, nbp - b);
+        if (ok && j < nblk) {
+            const uint4 *a, *q0, *q1;
+            const float *d;
+            stage_act_ptrs(V, co.st, b, nblk, a, d);
+            stage_fields(co.st, nblk, warp, lane, q0, q1);
+            const float2 dw0 = stage_dw(co.st, nblk, 0, warp, lane), dw1 = stage_dw(co.st, nblk, 1, warp, lane);
+            const float2 dx2 = *reinterpret_cast<const float2 *>(d + ((j >> 1) * V.stride + x) * 2);
             int s0a, s0b, s1a, s1b;
-            block_dots_2rows(co.cb, q0[0], q1[0], a, s0a, s1a);
-            block_dots_2rows(co.cb, q0[32], q1[32], a + 2, s0b, s1b);
+            block_dots_2rows(co.cb, q0[0], q1[0], a + (j * V.stride + x) * 2, s0a, s1a);
+            block_dots_2rows(co.cb, q0[32], q1[32], a + ((j + 1) * V.stride + x) * 2, s0b, s1b);
             acc0 = scale_acc2(acc0, dw0, dx2, s0a, s0b);
             acc1 = scale_acc2(acc1, dw1, dx2, s1a, s1b);
         }
         co.release(P);
-        a += 2 * kChunkB;
-        d += kChunkB;
     }
     part[lane] = acc0.x + acc0.y;
     part[kMaxCols * 32 + lane] = acc1.x + acc1.y;
+    return ok;
 }
 
-// Two columns c0, c1 sharing one exact expansion per index word, both row
-// sets; sums in registers over the pass, written to part[(r*kMaxCols + c)*32
-// + lane].  With acc_smem the stage sums are added to part instead (the pass
-// then sweeps other columns in between; first == true starts the sums).
-__device__ __forceinline__ void pair_b_stage(const Codebook &cb, const unsigned char *st, const uint4 *act0,
-                                             const float *dx0, int o0, int o1, int bq, float2 acc[2][2], int warp,
-                                             int lane) {
-    const uint4 *q0 = reinterpret_cast<const uint4 *>(st) + warp * 64 + lane;
-    const uint4 *q1 = q0 + kChunkB * 32;
-    const float2 dw0 = stage_dw_b(st, 0, warp, lane), dw1 = stage_dw_b(st, 1, warp, lane);
-    const int off[2] = {o0, o1};
+// Columns at slots x0, x1 sharing one exact expansion per index word, both row
+// sets, this warp's two blocks of the current stage, added into acc[r][c].
+__device__ __forceinline__ void pair_stage(const Codebook &cb, const unsigned char *st, int nblk, const uint4 *a,
+                                           const float *d, int stride, int x0, int x1, float2 acc[2][2], int warp,
+                                           int lane) {
+    const int j = 2 * warp;
+    const uint4 *q0, *q1;
+    stage_fields(st, nblk, warp, lane, q0, q1);
+    const float2 dw0 = stage_dw(st, nblk, 0, warp, lane), dw1 = stage_dw(st, nblk, 1, warp, lane);
     int s0[2][2], s1[2][2];  // [block][column]
 #pragma unroll
-    for (int j = 0; j < 2; ++j) block_dots_2rows_cols2(cb, q0[32 * j], q1[32 * j], act0, off, bq + j, s0[j], s1[j]);
+    for (int jj = 0; jj < 2; ++jj)
+        block_dots_2rows_cols2(cb, q0[32 * jj], q1[32 * jj], a + ((j + jj) * stride + x0) * 2,
+                               a + ((j + jj) * stride + x1) * 2, s0[jj], s1[jj]);
+    const int xs[2] = {x0, x1};
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        const float2 dx2 = *reinterpret_cast<const float2 *>(dx0 + off[c] + bq);
+        const float2 dx2 = *reinterpret_cast<const float2 *>(d + ((j >> 1) * stride + xs[c]) * 2);
         acc[0][c] = scale_acc2(acc[0][c], dw0, dx2, s0[0][c], s0[1][c]);
         acc[1][c] = scale_acc2(acc[1][c], dw1, dx2, s1[0][c], s1[1][c]);
     }
 }
 
-__device__ __forceinline__ void sweep_b2(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
-                                         int o0, int o1, float *part, bool live, int warp, int lane) {
+// Two columns: sums in registers over the pass.
+__device__ __forceinline__ bool sweep_b2(Consumer &co, const Pipe &P, int b0, int b1, int nbp, const ActView &V,
+                                         int x0, int x1, float *part, int warp, int lane) {
     float2 acc[2][2] = {{make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)},
                         {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)}};
-    for (int b = 0; b < nbp; b += kChunkB) {
-        const bool ok = co.wait(P);
-        if (ok && live && b + 2 * warp < nbp) pair_b_stage(co.cb, co.st, act0, dx0, o0, o1, b + 2 * warp, acc, warp, lane);
+    bool ok = true;
+    for (int b = b0; b < b1; b += kChunk) {
+        if (b > b0) ok = ok && co.wait(P);
+        const int nblk = min(kChunk, nbp - b);
+        if (ok && 2 * warp < nblk) {
+            const uint4 *a;
+            const float *d;
+            stage_act_ptrs(V, co.st, b, nblk, a, d);
+            pair_stage(co.cb, co.st, nblk, a, d, V.stride, x0, x1, acc, warp, lane);
+        }
         co.release(P);
     }
 #pragma unroll
     for (int r = 0; r < 2; ++r)
 #pragma unroll
         for (int c = 0; c < 2; ++c) part[(r * kMaxCols + c) * 32 + lane] = acc[r][c].x + acc[r][c].y;
+    return ok;
 }
 
 // Three or more columns: at every stage the columns two at a time (an odd
 // last one alone) with the stage sums added to part, so the registers stay
 // those of two columns while the weight stream is still read once.
-__device__ __forceinline__ void sweep_bn(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
-                                         const int (&col_off)[kMaxCols], int ncols, float *part, bool live, int warp,
-                                         int lane) {
-    for (int b = 0; b < nbp; b += kChunkB) {
-        const bool ok = co.wait(P);
-        const int bq = b + 2 * warp;
-        if (ok && live && bq < nbp) {
+__device__ __forceinline__ bool sweep_bn(Consumer &co, const Pipe &P, int b0, int b1, int nbp, const ActView &V,
+                                         const int (&col)[kMaxCols], int ncols, float *part, int warp, int lane) {
+    for (int c = 0; c < ncols; ++c) {
+        part[c * 32 + lane] = 0.0f;
+        part[(kMaxCols + c) * 32 + lane] = 0.0f;
+    }
+    const int j = 2 * warp;
+    bool ok = true;
+    for (int b = b0; b < b1; b += kChunk) {
+        if (b > b0) ok = ok && co.wait(P);
+        const int nblk = min(kChunk, nbp - b);
+        if (ok && j < nblk) {
+            const uint4 *a;
+            const float *d;
+            stage_act_ptrs(V, co.st, b, nblk, a, d);
             for (int c = 0; c < ncols; c += 2) {
                 float2 acc[2][2] = {{make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)},
                                     {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)}};
-                const int o0 = pick(col_off, c);
+                const int x0 = pick(col, c);
                 if (c + 1 < ncols) {
-                    pair_b_stage(co.cb, co.st, act0, dx0, o0, pick(col_off, c + 1), bq, acc, warp, lane);
+                    pair_stage(co.cb, co.st, nblk, a, d, V.stride, x0, pick(col, c + 1), acc, warp, lane);
                 } else {
-                    const uint4 *q0 = reinterpret_cast<const uint4 *>(co.st) + warp * 64 + lane;
-                    const uint4 *q1 = q0 + kChunkB * 32;
-                    const float2 dw0 = stage_dw_b(co.st, 0, warp, lane), dw1 = stage_dw_b(co.st, 1, warp, lane);
-                    const uint4 *a = act0 + 2 * (o0 + bq);
-                    const float2 dx2 = *reinterpret_cast<const float2 *>(dx0 + o0 + bq);
+                    const uint4 *q0, *q1;
+                    stage_fields(co.st, nblk, warp, lane, q0, q1);
+                    const float2 dw0 = stage_dw(co.st, nblk, 0, warp, lane), dw1 = stage_dw(co.st, nblk, 1, warp, lane);
+                    const float2 dx2 = *reinterpret_cast<const float2 *>(d + ((j >> 1) * V.stride + x0) * 2);
                     int s0a, s0b, s1a, s1b;
-                    block_dots_2rows(co.cb, q0[0], q1[0], a, s0a, s1a);
-                    block_dots_2rows(co.cb, q0[32], q1[32], a + 2, s0b, s1b);
+                    block_dots_2rows(co.cb, q0[0], q1[0], a + (j * V.stride + x0) * 2, s0a, s1a);
+                    block_dots_2rows(co.cb, q0[32], q1[32], a + ((j + 1) * V.stride + x0) * 2, s0b, s1b);
                     acc[0][0] = scale_acc2(acc[0][0], dw0, dx2, s0a, s0b);
                     acc[1][0] = scale_acc2(acc[1][0], dw1, dx2, s1a, s1b);
                 }
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        if (c + i >= ncols) continue;
-                        float *dst = part + (r * kMaxCols + c + i) * 32 + lane;
-                        *dst = (b == 0 ? 0.0f : *dst) + (acc[r][i].x + acc[r][i].y);
-                    }
-            }
-        } else if (b == 0) {  // no block of this warp in the first stage: start the sums at zero
-            for (int c = 0; c < ncols; ++c) {
-                part[c * 32 + lane] = 0.0f;
-                part[(kMaxCols + c) * 32 + lane] = 0.0f;
+                    for (int i = 0; i < 2; ++i)
+                        if (c + i < ncols) part[(r * kMaxCols + c + i) * 32 + lane] += acc[r][i].x + acc[r][i].y;
             }
         }
         co.release(P);
     }
+    return ok;
 }
 
-// One item pass of format B for the ncols columns at col_off: each warp's
-// sums go to its slice part (row set r, column c at part[(r*kMaxCols + c)*32
-// + lane]).  One column, two columns (one shared expansion, sums in
-// registers) and three or more (pairs per stage) each get their own loop.
-// live == false runs the stage waits and releases without computing.
-__device__ __forceinline__ void sweep_b(Consumer &co, const Pipe &P, int nbp, const uint4 *act0, const float *dx0,
-                                        const int (&col_off)[kMaxCols], int ncols, float *part, bool live, int warp,
-                                        int lane) {
-    if (ncols == 1)
-        sweep_b1(co, P, nbp, act0, dx0, col_off[0], part, live, warp, lane);
-    else if (ncols == 2)
-        sweep_b2(co, P, nbp, act0, dx0, col_off[0], col_off[1], part, live, warp, lane);
-    else
-        sweep_bn(co, P, nbp, act0, dx0, col_off, ncols, part, live, warp, lane);
+// NC (3..5) columns with every sum in registers, both row sets: each index
+// word expanded once (exact bytes) and dotted with all columns.
+template <int NC>
+__device__ __forceinline__ bool sweep_bk(Consumer &co, const Pipe &P, int b0, int b1, int nbp, const ActView &V,
+                                         float *part, int warp, int lane) {
+    float2 acc[2][NC];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[r][c] = make_float2(0.0f, 0.0f);
+    const int j = 2 * warp;
+    bool ok = true;
+    for (int b = b0; b < b1; b += kChunk) {
+        if (b > b0) ok = ok && co.wait(P);
+        const int nblk = min(kChunk, nbp - b);
+        if (ok && j < nblk) {
+            const uint4 *a, *q0, *q1;
+            const float *d;
+            stage_act_ptrs(V, co.st, b, nblk, a, d);
+            stage_fields(co.st, nblk, warp, lane, q0, q1);
+            const float2 dw0 = stage_dw(co.st, nblk, 0, warp, lane), dw1 = stage_dw(co.st, nblk, 1, warp, lane);
+            int s0[2][NC], s1[2][NC];  // [block][column]
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const uint4 wa = q0[32 * jj], wb = q1[32 * jj];
+                const uint32_t wsa[4] = {wa.x, wa.y, wa.z, wa.w}, wsb[4] = {wb.x, wb.y, wb.z, wb.w};
+                uint32_t ea[8], eb[8];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    expand_select(co.cb, wsa[m], ea[2 * m], ea[2 * m + 1]);
+                    expand_select(co.cb, wsb[m], eb[2 * m], eb[2 * m + 1]);
+                }
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    const uint4 *ac = a + ((j + jj) * V.stride + c) * 2;
+                    const uint4 x0 = ac[0], x1 = ac[1];
+                    const uint32_t av[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    int t0 = co.cb.seed, t1 = co.cb.seed;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        t0 = __dp4a((int)ea[i], (int)av[i], t0);
+                        t1 = __dp4a((int)eb[i], (int)av[i], t1);
+                    }
+                    s0[jj][c] = t0;
+                    s1[jj][c] = t1;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                const float2 dx2 = *reinterpret_cast<const float2 *>(d + ((j >> 1) * V.stride + c) * 2);
+                acc[0][c] = scale_acc2(acc[0][c], dw0, dx2, s0[0][c], s0[1][c]);
+                acc[1][c] = scale_acc2(acc[1][c], dw1, dx2, s1[0][c], s1[1][c]);
+            }
+        }
+        co.release(P);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) part[(r * kMaxCols + c) * 32 + lane] = acc[r][c].x + acc[r][c].y;
+    return ok;
+}
+
+// One item pass over blocks [b0, b1) of a pair (nbp blocks in all) for the
+// ncols columns at slots col[]: this warp's sums go to its slice part (row
+// set r, column c at part[(r*kMaxCols + c)*32 + lane]).  One column, two
+// columns (one shared expansion, sums in registers) and three or more (pairs
+// per stage) each get their own loop.
+__device__ __forceinline__ bool sweep_b(Consumer &co, const Pipe &P, int b0, int b1, int nbp, const ActView &V,
+                                        const int (&col)[kMaxCols], int ncols, float *part, int warp, int lane) {
+    if (ncols == 1) return sweep_b1(co, P, b0, b1, nbp, V, col[0], part, warp, lane);
+    if (ncols == 2) return sweep_b2(co, P, b0, b1, nbp, V, col[0], col[1], part, warp, lane);
+    return sweep_bn(co, P, b0, b1, nbp, V, col, ncols, part, warp, lane);
 }
 
 // Dynamic shared memory of a pipelined kernel:
-//   [consts][full S][empty S][abort][next][tags S] | ring S x kStageBytes | act | dx | part
-// act holds act_blocks staged blocks (two uint4 each), dx their scales; part
-// holds nsets partial-sum sets of kPartSet floats.
+//   [consts][full S][empty S][setfull 2][setempty 2][abort][tags S] | ring S x stage_bytes
+//   | sets nsets x set_bytes | act act_blocks x 32 bytes | dx act_blocks x 4 bytes
 struct PipeSmem {
     Pipe pipe;
-    uint4 *act;
+    uint4 *act;  // persistent activation staging
     float *dx;
-    float *part;
 };
 
 constexpr int kConstWords = 8;
-constexpr int kPartSetA = kConsumerWarps * kMaxCols * 32;      // format A: [warp][column][lane]
-constexpr int kPartSetB = kConsumerWarps * 2 * kMaxCols * 32;  // format B: [warp][row set][column][lane]
+constexpr uint32_t kSetBytes = 16 + kConsumerWarps * 2 * kMaxCols * 32 * 4;  // [warp][row set][column][lane]
 
 __host__ __device__ inline size_t pipe_header_bytes(int S) {
-    return ((size_t)4 * kConstWords + 20 * (size_t)S + 8 + 127) / 128 * 128;
+    return ((size_t)4 * kConstWords + 16 * (size_t)S + 32 + 4 + 4 * (size_t)S + 127) / 128 * 128;
 }
 
-__host__ __device__ inline size_t pipe_smem_bytes(int S, int act_blocks, int part_floats) {
-    return pipe_header_bytes(S) + (size_t)S * kStageBytes + (size_t)act_blocks * 36 + (size_t)part_floats * 4;
+__host__ __device__ inline size_t pipe_smem_bytes(int S, uint32_t stage_bytes, uint32_t set_bytes, int nsets,
+                                                  int act_blocks) {
+    return pipe_header_bytes(S) + (size_t)S * stage_bytes + (size_t)nsets * set_bytes + (size_t)act_blocks * 36;
 }
 
-__device__ __forceinline__ PipeSmem carve_pipe(unsigned char *smem, int S, int act_blocks, unsigned *err) {
+__device__ __forceinline__ PipeSmem carve_pipe(unsigned char *smem, int S, uint32_t stage_bytes, uint32_t set_bytes,
+                                               int nsets, int act_blocks, unsigned *err) {
     PipeSmem L;
     L.pipe.consts = reinterpret_cast<uint32_t *>(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 4 * kConstWords);
     L.pipe.full0 = smem_addr(bars);
     L.pipe.empty0 = smem_addr(bars + S);
-    L.pipe.abort = reinterpret_cast<int *>(bars + 2 * S);
-    L.pipe.next = L.pipe.abort + 1;
-    L.pipe.tag = L.pipe.abort + 2;
+    L.pipe.setfull0 = smem_addr(bars + 2 * S);
+    L.pipe.setempty0 = smem_addr(bars + 2 * S + 2);
+    L.pipe.abort = reinterpret_cast<int *>(bars + 2 * S + 4);
+    L.pipe.tag = L.pipe.abort + 1;
     L.pipe.ring = smem + pipe_header_bytes(S);
+    L.pipe.sets = L.pipe.ring + (size_t)S * stage_bytes;
     L.pipe.err = err;
     L.pipe.S = S;
-    L.act = reinterpret_cast<uint4 *>(L.pipe.ring + (size_t)S * kStageBytes);
+    L.pipe.stage_bytes = stage_bytes;
+    L.pipe.set_bytes = set_bytes;
+    L.pipe.nsets = (uint32_t)nsets;
+    L.act = reinterpret_cast<uint4 *>(L.pipe.sets + (size_t)nsets * set_bytes);
     L.dx = reinterpret_cast<float *>(L.act + (size_t)act_blocks * 2);
-    L.part = L.dx + act_blocks;
     return L;
-}
-
-// Work counter of a persistent kernel: sched[0] dynamic items taken, sched[1]
-// CTAs done.  Called once per CTA after its last fetch; the last CTA resets
-// both for the next launch.
-__device__ __forceinline__ void sched_exit(unsigned *sched) {
-    if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
-        sched[0] = 0u;
-        sched[1] = 0u;
-    }
 }
 
 // Thread 0 writes the constants and initialises the barriers; all threads
@@ -504,6 +596,10 @@ __device__ __forceinline__ void pipe_init(const Pipe &P) {
         for (int s = 0; s < P.S; ++s) {
             mbar_init(P.full0 + 8u * s, 1);
             mbar_init(P.empty0 + 8u * s, kConsumers);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(P.setfull0 + 8u * k, kConsumers);
+            mbar_init(P.setempty0 + 8u * k, 32);
         }
         *P.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
