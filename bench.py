@@ -653,7 +653,7 @@ def run_gpu(args):
                              "per_replay_us": {"batch1": b1_q, "batch5": b5_q},
                              "batch1_frac_of_peak": b1_gbs / peak, "batch5_frac_of_peak": b5_gbs / peak,
                              "eager_host_loop": {"batch1": b1_eager, "batch5": b5_eager},
-                             "eager_split_us_layer_combine": {"batch1": b1_split, "batch5": b5_split}},
+                             "eager_split_us_quantize_layer": {"batch1": b1_split, "batch5": b5_split}},
             "us_per_layer_with_shared_expert": shared,
             "us_per_call_dense": dense,
             "kernels_ms_per_step": {"moe layer call (k_quantize + k_moe + k_moe_combine)": sum(k_moe) / len(timed),

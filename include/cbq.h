@@ -113,8 +113,8 @@ const char *cbq_last_cuda_error(void);
  * stream interleaved by 32-row groups plus a separate fp16 scale stream); the
  * source is not retained.  Synchronizes `stream`.
  * K is bounded by the shared-memory staging of CBQ_MAX_COLS quantized
- * activation columns next to the weight ring and the partial-sum sets:
- * K <= 26,240 on GB300 (227 KB of shared memory per CTA).
+ * activation columns next to a four-stage weight ring and the partial-sum
+ * set: K <= 27,136 on GB300 (227 KB of shared memory per CTA).
  * Errors: EINVAL (null, M < 1, K < 32, K % 32 != 0, K above that bound),
  * ENOMEM, ECUDA, EDEVICE. */
 int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device,
@@ -197,8 +197,9 @@ int cbq_moe_info(const cbq_moe *L, int *E, int64_t *H, int64_t *F, int64_t *devi
  * With a shared expert (cbq_moe_set_shared) its output is added last.
  * Three kernel launches on `stream`, each a programmatic dependent of the one
  * before: the token quantization, the layer kernel (gate_up, SwiGLU,
- * requantization, down), the combine.  With one token and h_dev 16-byte
- * aligned, two: the layer kernel quantizes the token itself (same bits).  One
+ * requantization, down), the combine.  With one token the layer kernel forms
+ * the combine itself (same order, same bits), and with h_dev also 16-byte
+ * aligned it quantizes the token itself too (same bits): one launch.  One
  * call at a time per handle (its workspace and counters are shared by the
  * calls).
  * 1 <= n_tok <= CBQ_MAX_TOKENS, 1 <= topk <= min(CBQ_MAX_TOPK, E). */
@@ -233,14 +234,14 @@ int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok,
                         float *y_host, void *stream);
 
 /* Stage timing: when set, cbq_moe_matvec records these CUDA events
- * (cudaEvent_t passed as void*) on its stream before its first kernel (the
- * token quantization, or the layer kernel for one aligned token), before the
- * combine kernel (so the first interval spans the quantization and the layer
- * kernel: gate_up + SwiGLU + requantization, down) and after it.  Recording
- * them separates the kernels (the overlap of the combine's start with the
- * layer kernel's end is lost).  Pass NULL for all three to stop; a mix of NULL
- * and non-NULL is CBQ_EINVAL.  The events stay owned by the caller. */
-int cbq_moe_set_stage_events(cbq_moe *L, void *ev_layer, void *ev_combine, void *ev_end);
+ * (cudaEvent_t passed as void*) on its stream before its first kernel,
+ * before the layer kernel (right after ev_start when the layer kernel
+ * quantizes the one token itself; else after the token quantization) and
+ * after the call's last kernel (the layer kernel, or the combine).  Recording them separates the kernels (the overlap
+ * of a kernel's start with the previous one's end is lost).  Pass NULL for
+ * all three to stop; a mix of NULL and non-NULL is CBQ_EINVAL.  The events
+ * stay owned by the caller. */
+int cbq_moe_set_stage_events(cbq_moe *L, void *ev_start, void *ev_layer, void *ev_end);
 
 /* ---- allocation-free dense path --------------------------------------- */
 

@@ -33,7 +33,7 @@ def test_comments_and_whitespace_keep_the_digest(tmp_path):
 def test_code_changes_the_digest(tmp_path):
     d = _copy(tmp_path)
     base = bench.source_digest(str(d))
-    _edit(d, "cbq_kernels.cu", "constexpr int kStages = 4;", "constexpr int kStages = 3;")
+    _edit(d, "cbq_kernels.cu", "constexpr int kMinStages = 4;", "constexpr int kMinStages = 3;")
     assert bench.source_digest(str(d)) != base
 
 

@@ -174,17 +174,17 @@ def test_output_head_sampled_bench_shape(torch):
 
 
 def test_largest_k_accepted_and_correct(torch):
-    """K = 26,240 (820 blocks: the most the 5-column staging fits beside the
-    weight ring and the partial-sum set in 227 KB), ragged M, a partial last
-    stage."""
-    M, K = 70, 26240
+    """K = 27,136 (848 blocks: the most the 5-column staging fits beside a
+    four-stage weight ring and the 5-column partial-sum set in 227 KB), ragged
+    M, a partial last stage."""
+    M, K = 70, 27136
     W = synth.weight_blocks(M, K, stream=450)
     for n in (1, 5):
         _check_matvec(torch, W, M, K, synth.activations(n, K, stream=451 + n, outliers=True))
 
 
 def test_k_beyond_staging_limit_refused(torch):
-    M, K = 32, 26272
+    M, K = 32, 27168
     with pytest.raises(cbq.CbqError) as info:
         cbq.Weights(synth.weight_blocks(M, K, stream=452), M, K)
     assert info.value.status == cbq.CBQ_EINVAL

@@ -361,6 +361,7 @@ int cbq_moe_destroy(cbq_moe *L) {
     cudaFree(L->ws.qh);
     cudaFree(L->ws.qa_bm);
     cudaFree(L->ws.dep);
+    cudaFree(L->ws.pcnt);
     cudaFree(L->ws.qa);
     cudaFree(L->ws.da);
     cudaFree(L->ws.a_dbg);
@@ -394,16 +395,18 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
     const size_t slots = cbq::kMaxSlots;
     const size_t nbpH = (size_t)cbq::round_up4(nbH), nbpF = (size_t)cbq::round_up4(nbF);
     const size_t nsF = (nbpF + 15) / 16;  // down stages of 16 blocks
+    const size_t gd2 = (size_t)(H / CBQ_QK + 1) / 2;  // 64-row output groups
     if ((rc = dev_alloc(&L->gu, gub * E, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->dn, dnb * E, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.qh, cbq::act_bytes((int)nbpH, CBQ_MAX_TOKENS), &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.qa_bm, slots * cbq::act_bytes((int)nbpF, CBQ_MAX_COLS), &L->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&L->ws.dep, slots * nsF, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.dep, 2 * slots * nsF, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.pcnt, 2 * gd2, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.qa, slots * F, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.da, slots * nbF, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.a_dbg, slots * F, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.obuf, slots * H, &L->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&L->ws.sched, 4, &L->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&L->ws.sched, 8, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->ws.err, 1, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_h, (size_t)CBQ_MAX_TOKENS * H, &L->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&L->st_ids, slots, &L->bytes)) != CBQ_OK ||
@@ -414,13 +417,15 @@ int cbq_moe_create(const void *gate_up, const void *down, int E, int64_t H, int6
     }
     cudaStream_t s = as_stream(stream);
     // the intermediate's padded blocks are never written: zero keeps them finite
-    if (cudaMemsetAsync(L->ws.sched, 0, 4 * sizeof(unsigned), s) != cudaSuccess ||
-        cudaMemsetAsync(L->ws.dep, 0, slots * nsF * sizeof(unsigned), s) != cudaSuccess ||
+    if (cudaMemsetAsync(L->ws.sched, 0, 8 * sizeof(unsigned), s) != cudaSuccess ||
+        cudaMemsetAsync(L->ws.dep, 0, 2 * slots * nsF * sizeof(unsigned), s) != cudaSuccess ||
+        cudaMemsetAsync(L->ws.pcnt, 0, 2 * gd2 * sizeof(unsigned), s) != cudaSuccess ||
         cudaMemsetAsync(L->ws.qa_bm, 0, slots * cbq::act_bytes((int)nbpF, CBQ_MAX_COLS), s) != cudaSuccess ||
         cudaMemsetAsync(L->ws.err, 0, sizeof(unsigned), s) != cudaSuccess) {
         cbq_moe_destroy(L);
         return CBQ_ECUDA;
     }
+    L->ws.dep_set = slots * nsF;
     const size_t gu_bytes = (size_t)2 * F * nbH * CBQ_BLOCK_BYTES;
     const size_t dn_bytes = (size_t)H * nbF * CBQ_BLOCK_BYTES;
     for (int e = 0; e < E; ++e) {
@@ -582,13 +587,13 @@ int cbq_moe_set_debug(cbq_moe *L, int keep_intermediate) {
     return CBQ_OK;
 }
 
-int cbq_moe_set_stage_events(cbq_moe *L, void *ev_layer, void *ev_combine, void *ev_end) {
+int cbq_moe_set_stage_events(cbq_moe *L, void *ev_start, void *ev_layer, void *ev_end) {
     if (!L) return CBQ_EINVAL;
-    const bool all = ev_layer && ev_combine && ev_end;
-    const bool none = !ev_layer && !ev_combine && !ev_end;
+    const bool all = ev_start && ev_layer && ev_end;
+    const bool none = !ev_start && !ev_layer && !ev_end;
     if (!all && !none) return CBQ_EINVAL;
-    L->ws.ev[0] = reinterpret_cast<cudaEvent_t>(ev_layer);
-    L->ws.ev[1] = reinterpret_cast<cudaEvent_t>(ev_combine);
+    L->ws.ev[0] = reinterpret_cast<cudaEvent_t>(ev_start);
+    L->ws.ev[1] = reinterpret_cast<cudaEvent_t>(ev_layer);
     L->ws.ev[2] = reinterpret_cast<cudaEvent_t>(ev_end);
     return CBQ_OK;
 }

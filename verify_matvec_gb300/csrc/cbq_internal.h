@@ -83,16 +83,18 @@ struct DevMoe {
 struct MoeWork {
     int8_t *qh;       // the tokens quantized, in the chunked activation layout (act_bytes)
     int8_t *qa_bm;    // per virtual expert: its quantized intermediate, the same layout (kMaxCols columns' room)
-    unsigned *dep;    // per virtual expert and down stage: gate_up groups published (zero between launches)
+    unsigned *dep;    // two sets (by call parity) of: per virtual expert and down stage, gate_up groups published
+    size_t dep_set;   // words of one dep set (kMaxSlots x down stages)
+    unsigned *pcnt;   // two sets of: per 64-row output group, virtual experts whose down item finished
     int8_t *qa;       // slots x F, plain order (written when keep_a)
     float *da;        // slots x F/32 (written when keep_a)
     float *a_dbg;     // slots x F (written when keep_a)
     float *obuf;      // slots x H, down-projection output per slot
-    unsigned *sched;  // work counters (items taken, CTAs done), zero between launches
+    unsigned *sched;  // items taken, CTAs done taking, call count, dep words used per set (5 words)
     unsigned *err;    // the handle's error word (CBQ_DEVERR_* bits)
     int keep_a;
     int stall;        // give-up test mode: 0 off, 1 a dependency never met, 2 a stage never filled
-    cudaEvent_t ev[3];  // optional stage events (before the layer kernel, before the combine, after it)
+    cudaEvent_t ev[3];  // optional events: before the call, before the layer kernel, after it
 };
 
 // The chunked activation layout the layer kernel's stages copy: `cols`

@@ -30,9 +30,11 @@
 namespace cbq {
 
 constexpr unsigned kErrBadExpertId = 0x1u;
-// Pipeline depth (stages of 18 KB per CTA, two CTAs per SM) and partial-sum
-// sets of each kernel, sized so two CTAs fit in an SM's shared memory.
-constexpr int kStages = 4;
+// Pipeline depth of the dense kernel: the deepest ring (stages of 18 KB) that
+// still lets two CTAs share an SM, at least kMinStages (the shape limit of a
+// handle is checked at that depth) and at most kMaxStages.
+constexpr int kMinStages = 4;
+constexpr int kMaxStages = 6;
 
 // Dynamic shared memory of the routed-expert kernel with S stages and
 // act_blocks persistently staged blocks (the one token it quantizes itself).
@@ -158,10 +160,14 @@ cudaError_t launch_quantize_chunked(const float *x, int K, int n, int8_t *qh, cu
 
 // ---------------------------------------------------------- dense MMVQ -----
 
-// One partial-sum set: the epilogue warp reads a pair's sums long before the
-// consumers finish the next pair, and the second set's room goes to keeping
-// two CTAs per SM with five staged columns.
-size_t matvec_smem_bytes(int nbp, int n) { return pipe_smem_bytes(kStages, kStageWeightBytes, kSetBytes, 1, n * nbp); }
+// One partial-sum set of NC columns per warp (one row per lane): the
+// epilogue warp reads a pair's sums long before the consumers finish the next
+// pair, and the room a second set would take goes to the ring.
+__host__ __device__ inline uint32_t dense_set_bytes(int n) { return 16u + (uint32_t)(kConsumerWarps * n * 32 * 4); }
+static size_t dense_smem_bytes(int S, int nbp, int n) {
+    return pipe_smem_bytes(S, kStageWeightBytes, dense_set_bytes(n), 1, n * nbp);
+}
+size_t matvec_smem_bytes(int nbp, int n) { return dense_smem_bytes(kMinStages, nbp, n); }
 
 // Debug kernel smem: activations + scales only.
 static size_t dots_smem_bytes(int nbp, int n) { return (size_t)n * nbp * 36; }
@@ -173,23 +179,20 @@ struct MatvecArgs {
     const float *xf;   // fp32 column (kF32 == true)
     int64_t K;
     float *y;
+    int S;             // pipeline stages
 };
 
-// The end of a persistent kernel: after a CTA barrier, the last CTA to get
-// here resets the work counters (sched[0] items taken, sched[1] CTAs done).
-__device__ __forceinline__ bool last_cta(unsigned *sched) {
-    __shared__ int last;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        last = atomicAdd(sched + 1, 1u) == gridDim.x - 1;
-        if (last) {
-            sched[0] = 0u;
-            sched[1] = 0u;
-        }
-    }
-    __syncthreads();
-    return last != 0;
+// Work counters of a persistent kernel (sched[0] items taken, sched[1] CTAs
+// done taking items).  Each CTA's producer counts itself done once it has
+// taken its last item; the last CTA to do so resets both words at once (no
+// CTA of this launch reads them again, and the next launch reads them only
+// after this grid has completed), so no CTA waits on a counter at its end.
+__device__ __forceinline__ bool done_taking(unsigned *sched) {
+    return atomicAdd(sched + 1, 1u) == gridDim.x - 1;
+}
+__device__ __forceinline__ void reset_sched(unsigned *sched) {
+    sched[0] = 0u;
+    sched[1] = 0u;
 }
 
 // One 4-block quad of one row (this lane) for NC columns: the quad's index
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_trigger();  // the next kernel may launch; it waits for this grid before touching what it writes
     const DevMat &W = A.W;
-    const PipeSmem S = carve_pipe(smem, kStages, kStageWeightBytes, kSetBytes, 1, NC * W.nbp, W.err);
+    const PipeSmem S = carve_pipe(smem, A.S, kStageWeightBytes, dense_set_bytes(NC), 1, NC * W.nbp, W.err);
     pipe_init(S.pipe);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -276,8 +279,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
                 next = gridDim.x + atomicAdd(W.sched, 1u);
                 pr.pass(S.pipe, W.w + item * pb, W.nbp, 0, nch, (int)item);
             }
+            const bool last = done_taking(W.sched);
             pr.finish(S.pipe);
             pr.drain(S.pipe);
+            if (last) reset_sched(W.sched);
         }
     } else if (warp == kEpilogueWarp) {
         SetReader rd;
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
                 for (int c = 0; c < NC; ++c) {
                     v[r][c] = 0.0f;
 #pragma unroll
-                    for (int w = 4 * r; w < 4 * r + 4; ++w) v[r][c] += part[(w * 2 * kMaxCols + c) * 32 + lane];
+                    for (int w = 4 * r; w < 4 * r + 4; ++w) v[r][c] += part[(w * NC + c) * 32 + lane];
                 }
             rd.release(S.pipe);
 #pragma unroll
@@ -332,13 +337,12 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
             for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
             const bool ok = dense_pass<NC>(co, S.pipe, W.nbp, S.act, S.dx, acc, warp, lane);
 #pragma unroll
-            for (int c = 0; c < NC; ++c) part[(warp * 2 * kMaxCols + c) * 32 + lane] = acc[c].x + acc[c].y;
+            for (int c = 0; c < NC; ++c) part[(warp * NC + c) * 32 + lane] = acc[c].x + acc[c].y;
             if (threadIdx.x == 0) *tag = it;
             wr.publish(S.pipe);
             if (!ok) break;
         }
     }
-    last_cta(W.sched);
 }
 
 template <int NC>
@@ -490,9 +494,23 @@ static cudaError_t dynamic_grid(Kernel kern, size_t smem, int64_t items, int *gr
 template <int NC, bool kF32>
 static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const float *dx, const float *xf, float *y,
                                    cudaStream_t s, bool pdl) {
-    const size_t smem = matvec_smem_bytes(W.nbp, NC);
+    // the deepest ring that keeps the residency of the kMinStages ring (two
+    // CTAs per SM where that fits), so the next call's weights stream sooner
+    int S = kMinStages, sms = 0, base = 0;
+    cudaError_t e = resident(k_matvec<NC, kF32>, kPipeThreads, dense_smem_bytes(S, W.nbp, NC), &sms, &base);
+    if (e != cudaSuccess) return e;
+    for (int t = kMaxStages; t > kMinStages; --t) {
+        int per_sm = 0;
+        e = resident(k_matvec<NC, kF32>, kPipeThreads, dense_smem_bytes(t, W.nbp, NC), &sms, &per_sm);
+        if (e != cudaSuccess) return e;
+        if (per_sm >= std::min(base, 2)) {
+            S = t;
+            break;
+        }
+    }
+    const size_t smem = dense_smem_bytes(S, W.nbp, NC);
     int grid = 0;
-    cudaError_t e = dynamic_grid(k_matvec<NC, kF32>, smem, W.P, &grid);
+    e = dynamic_grid(k_matvec<NC, kF32>, smem, W.P, &grid);
     if (e != cudaSuccess) return e;
     MatvecArgs A;
     A.W = W;
@@ -501,6 +519,7 @@ static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const floa
     A.xf = xf;
     A.K = (int64_t)W.nb * kQK;
     A.y = y;
+    A.S = S;
     return launch_k(k_matvec<NC, kF32>, grid, kPipeThreads, smem, s, pdl, A);
 }
 
@@ -557,97 +576,144 @@ struct MoeArgs {
     int n_tok, k, swiglu;
     int nbH, nbpH, nbF, nbpF;
     int quant_tokens;  // one token, h 16-byte aligned: the consumers quantize it themselves
+    int fuse_combine;  // one token: the layer kernel writes y itself (no combine kernel)
     int stages;        // pipeline depth (4, or 3 where two CTAs per SM allow no more)
 };
 
-// The routing table of one call, derived redundantly by every CTA from the
-// <= 85 slots (no host round trip).  Slots 0..N-1 are the routed ones
-// (p = t*k + j); with a shared expert, slots N..N+n_tok-1 hold its virtual
-// id E, one per token.  An out-of-range routed id is stored as -1, so it
-// matches no expert, the shared one included.  The distinct experts are
-// ordered with the shared expert first (its items, with a column for every
-// token, are the slowest: handed out first, they do not form the tail of a
-// pass), then by id; each is split into column groups of at most kMaxCols
-// slots (more slots than that only with repeated ids), its "virtual
-// experts": every item works on one virtual expert.
+// The routing table of one call, derived redundantly by every CTA (by its
+// producer warp, in registers) from the <= 85 slots (no host round trip).
+// Slots 0..N-1 are the routed ones (p = t*k + j); with a shared expert, slots
+// N..N+n_tok-1 hold its virtual id E, one per token.  An out-of-range routed
+// id is stored as -1 and takes part in no expert.  The slots are scanned with
+// the shared expert's first, then the routed ones in order, and the distinct
+// experts are ordered by their first slot in that scan (the shared expert's
+// items, with a column for every token, are the slowest: handed out first,
+// they do not form the tail of a pass).  Each distinct expert is split into
+// column groups of at most kMaxCols of its slots (more slots than that only
+// with repeated ids), its "virtual experts": every item works on one virtual
+// expert.
 struct Routing {
-    int ids[kMaxSlots];
-    unsigned char first[kMaxSlots];
-    int uniq[kMaxSlots];
-    int v0[kMaxSlots];                       // first virtual expert of distinct expert u
-    int vexp[kMaxSlots];                     // expert id of virtual expert v
-    unsigned char vnc[kMaxSlots];            // its columns (1..kMaxCols)
+    int ids[kMaxSlots];                        // expert of each slot (-1: out of range)
+    float w[kMaxSlots];                        // router weight of each slot (shared-expert slots: 1)
+    int vbase[kMaxSlots];                      // by scan position of an expert's first slot: its first virtual expert
+    int vexp[kMaxSlots];                       // expert id of virtual expert v
+    unsigned char vnc[kMaxSlots];              // its columns (1..kMaxCols)
     unsigned char vslot[kMaxSlots][kMaxCols];  // its slots, ascending
     int D, V;
+    unsigned epoch;                            // the handle's call count (selects the counter set)
 };
 
-__device__ void route(const int32_t *__restrict__ ids, int N, int n_all, int E, Routing &R, unsigned *err) {
-    const int t = threadIdx.x;
-    if (t < n_all) {
-        int e = E;  // a shared-expert slot
-        if (t < N) {
-            e = ids[t];
-            if (e < 0 || e >= E) {
-                if (err) atomicOr(err, kErrBadExpertId);
-                e = -1;
+// Words of a layer handle's ws.sched: items taken, CTAs done taking items,
+// the call count (epoch), and per counter set the dependency words its last
+// call used.
+constexpr int kSchedFetch = 0, kSchedDone = 1, kSchedEpoch = 2, kSchedUsed = 3;
+
+// The routing table, built by the 32 lanes of one warp: lane l holds scan
+// positions l, l+32, l+64.  Equal ids are found with a warp match inside a
+// pass of 32 positions and with shuffles across passes; the distinct experts'
+// ranks come from ballots and their first virtual experts from a warp scan.
+// The ids, router weights and epoch are loaded in one round trip.
+__device__ void route_warp(const int32_t *__restrict__ ids, const float *__restrict__ wts, const unsigned *sched,
+                           int N, int n_all, int E, Routing &R, unsigned *err, int lane) {
+    static_assert(kMaxSlots <= 3 * 32, "three scan positions per lane");
+    constexpr unsigned kFull = 0xffffffffu;
+    const unsigned below = (1u << lane) - 1u;
+    const int n_sh = n_all - N;  // shared-expert slots, scanned first
+    int p[3], e[3];
+    float w[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const int s = lane + 32 * i;
+        p[i] = s < n_sh ? N + s : s - n_sh;
+        e[i] = -2;  // no slot here
+        w[i] = 1.0f;
+        if (s < n_all) {
+            e[i] = E;  // a shared-expert slot
+            if (p[i] < N) {
+                e[i] = ids[p[i]];
+                w[i] = wts[p[i]];
             }
         }
-        R.ids[t] = e;
     }
-    __syncthreads();
-    if (t < n_all) {
-        const int e = R.ids[t];
-        int f = e >= 0 ? 1 : 0;
-        for (int p = 0; p < t; ++p)
-            if (R.ids[p] == e) f = 0;
-        R.first[t] = (unsigned char)f;
-    }
-    __syncthreads();
-    if (t < n_all && R.first[t]) {
-        auto key = [E](int e) { return e == E ? -1 : e; };
-        const int kt = key(R.ids[t]);
-        int rank = 0;
-        for (int p = 0; p < n_all; ++p)
-            if (R.first[p] && key(R.ids[p]) < kt) ++rank;
-        R.uniq[rank] = R.ids[t];
-    }
-    if (t == 0) {
-        int D = 0;
-        for (int p = 0; p < n_all; ++p) D += R.first[p];
-        R.D = D;
-    }
-    __syncthreads();
-    int ns = 0;  // slots of distinct expert t
-    if (t < R.D) {
-        for (int p = 0; p < n_all; ++p) ns += R.ids[p] == R.uniq[t];
-        R.v0[t] = (ns + kMaxCols - 1) / kMaxCols;  // its virtual experts, made a prefix sum below
-    }
-    __syncthreads();
-    if (t == 0) {
-        int v = 0;
-        for (int u = 0; u < R.D; ++u) {
-            const int c = R.v0[u];
-            R.v0[u] = v;
-            v += c;
+    const unsigned epoch = lane == 0 ? *(volatile const unsigned *)(sched + kSchedEpoch) : 0u;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        if (lane + 32 * i >= n_all) continue;
+        if (p[i] < N && (e[i] < 0 || e[i] >= E)) {
+            if (err) atomicOr(err, kErrBadExpertId);
+            e[i] = -1;
         }
-        R.V = v;
+        R.ids[p[i]] = e[i];
+        R.w[p[i]] = w[i];
     }
-    __syncthreads();
-    if (t < R.D) {
-        const int e = R.uniq[t];
-        int n = 0;
-        for (int p = 0; p < n_all; ++p) {
-            if (R.ids[p] != e) continue;
-            const int v = R.v0[t] + n / kMaxCols, c = n % kMaxCols;
-            R.vslot[v][c] = (unsigned char)p;
-            if (c == 0) {
-                R.vexp[v] = e;
-                R.vnc[v] = (unsigned char)min(kMaxCols, ns - n);
+    // per position: equal ids before it and in all, and the first of them
+    const int npass = (n_all + 31) / 32;
+    int before[3], total[3], first_pos[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const unsigned m = __match_any_sync(kFull, e[i]);
+        before[i] = __popc(m & below);
+        total[i] = __popc(m);
+        first_pos[i] = 32 * i + __ffs(m) - 1;
+    }
+    if (npass > 1) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            if (j >= npass) break;
+            for (int l = 0; l < 32; ++l) {
+                const int v = __shfl_sync(kFull, e[j], l);
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    if (i == j || v != e[i]) continue;
+                    ++total[i];
+                    if (j < i) {
+                        ++before[i];
+                        first_pos[i] = min(first_pos[i], 32 * j + l);
+                    }
+                }
             }
-            ++n;
         }
     }
-    __syncthreads();
+    // distinct experts: positions holding the first slot of a valid id
+    bool first[3];
+    unsigned bal[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        first[i] = e[i] >= 0 && before[i] == 0;
+        bal[i] = __ballot_sync(kFull, first[i]);
+    }
+    // first virtual expert of each distinct expert: exclusive scan of
+    // ceil(slots / kMaxCols) over the first slots in scan order
+    int carry = 0;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const int nv = first[i] ? (total[i] + kMaxCols - 1) / kMaxCols : 0;
+        int x = nv;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(kFull, x, d);
+            if (lane >= d) x += y;
+        }
+        if (first[i]) R.vbase[lane + 32 * i] = carry + x - nv;
+        carry += __shfl_sync(kFull, x, 31);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        if (e[i] < 0) continue;
+        const int v = R.vbase[first_pos[i]] + before[i] / kMaxCols, c = before[i] % kMaxCols;
+        R.vslot[v][c] = (unsigned char)p[i];
+        if (c == 0) {
+            R.vexp[v] = e[i];
+            R.vnc[v] = (unsigned char)min(kMaxCols, total[i] - before[i]);
+        }
+    }
+    if (lane == 0) {
+        R.V = carry;
+        R.D = __popc(bal[0]) + __popc(bal[1]) + __popc(bal[2]);
+        R.epoch = epoch;
+    }
+    __syncwarp();
 }
 
 // Token of slot p: routed slots are t*k + j, shared-expert slots N + t.
@@ -664,6 +730,7 @@ __device__ __forceinline__ const uint8_t *down_of(const DevMoe &L, int e) {
 
 constexpr unsigned kErrDependencyTimeout = 0x200u;
 constexpr unsigned kDownGrab = 4;
+constexpr int kMaxTopk = 16;  // routed experts per token (the ABI's limit)
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     unsigned v;
@@ -694,46 +761,63 @@ __device__ __forceinline__ bool wait_dependency(const unsigned *cnt, unsigned ta
     return true;
 }
 
-// The whole routed-expert layer but the combine, in one persistent kernel.
+// The whole routed-expert layer, combine included, in one persistent kernel.
 // Work items, in this order (the first per CTA is its index, the rest come
 // from one counter):
 //   it <  V*Gf : gate_up item (virtual expert v, 32-row-pair group g), v-major:
-//                gate rows 32g.. and up rows F+32g.. in one format-B pass; the
-//                epilogue warp applies the SwiGLU split and requantizes the
-//                32 outputs of each column (block g of the column's a);
+//                gate rows 32g.. and up rows F+32g.. in one pass; the epilogue
+//                warp applies the SwiGLU split and requantizes the 32 outputs
+//                of each column (block g of the column's a);
 //   it >= V*Gf : down item (virtual expert v, 64-row group g: 32-row groups 2g
 //                and 2g+1), v-major, per-slot outputs to obuf.
 // A down stage covering blocks [16s, 16s+16) of a reads only the blocks that
 // gate_up groups 16s..16s+15 of its virtual expert wrote: the producer waits
 // (bounded) for that count before it copies the slice.  The gate_up items are
 // all handed out before any down item, and taken items never wait for later
-// ones, so the wait always ends.
+// ones, so the wait always ends.  The down item that completes a 64-row group
+// for the last of the V virtual experts (a per-group count) adds the group's
+// slot outputs into y: the router-weighted sum in slot order, then the shared
+// expert's output.
+// Counters: the dependency and group counts come in two sets, used by calls
+// of even and odd epoch; the last CTA to finish taking items zeroes the set of
+// the previous call (complete by then), resets the item counters and advances
+// the epoch, so no CTA waits on a counter at its end.
 // With one token (quantized here) this is the call's first kernel, launched
 // as a programmatic dependent: it sets up its pipeline, then waits for all
-// earlier work before it reads anything or lets the combine start.
-// Otherwise it follows the quantization kernel, which starts it only once all
-// earlier work has ended, so the routing table and the handle's counters are
-// read at once; the producer waits for the quantized tokens before it copies
-// their first slice.
+// earlier work before it reads anything.  Otherwise it follows the
+// quantization kernel, which starts it only once all earlier work has ended,
+// so the routing table and the handle's counters are read at once; the
+// producer waits for the quantized tokens before it copies their first slice.
 __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__ MoeArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
+    __shared__ __align__(8) uint64_t route_bar;  // the routing table is ready (one arrive per producer lane)
     PipeSmem S = carve_pipe(smem, A.stages, kStageBytesAct, kSetBytes, 2, A.quant_tokens ? A.nbpH : 0, A.ws.err);
     pipe_init(S.pipe);
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&route_bar), 32);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
     if (A.quant_tokens) pdl_wait();
-    pdl_trigger();  // the combine kernel may launch; it waits for this grid
+    pdl_trigger();  // the next kernel may launch (the combine, or the next call's first); it waits for this grid
     const int N = A.n_tok * A.k, n_all = N + (A.L.shared ? A.n_tok : 0);  // routed slots, then shared ones
-    route(A.ids, N, n_all, A.L.E, R, blockIdx.x == 0 ? A.ws.err : nullptr);  // ends with a CTA barrier
     const int Gf = A.L.F / 32, Gd = A.L.H / 32, Gd2 = (Gd + 1) / 2;
     const int nsF = (A.nbpF + kChunk - 1) / kChunk;  // down stages (dependency counters per virtual expert)
     const int nchH = (A.nbpH + kChunk - 1) / kChunk;
-    const unsigned total_gu = (unsigned)(R.V * Gf);
-    const unsigned total = total_gu + (unsigned)(R.V * Gd2);
     const size_t qa_region = act_bytes(A.nbpF, kMaxCols);
     const size_t pbH = pair_bytes(A.nbpH), pbF = pair_bytes(A.nbpF);
     unsigned *sched = A.ws.sched;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rbar = smem_addr(&route_bar);
     if (warp == kProducerWarp) {
+        route_warp(A.ids, A.wts, sched, N, n_all, A.L.E, R, blockIdx.x == 0 ? A.ws.err : nullptr, lane);
+        mbar_arrive(rbar);
+        const unsigned total_gu = (unsigned)(R.V * Gf);
+        const unsigned total = total_gu + (unsigned)(R.V * Gd2);
+        const unsigned set = R.epoch & 1u;
+        const unsigned *dep_set = A.ws.dep + set * A.ws.dep_set;
+        bool last = false;
         if (lane == 0) {
             Producer pr;
             bool tokens_ready = A.quant_tokens != 0;  // else the quantization kernel's output needs the wait
@@ -746,7 +830,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                 // issued, so the atomic's latency overlaps them
                 const unsigned seen = base + grab;
                 const unsigned ngrab = seen < total_gu ? 1u : max(1u, min(kDownGrab, (total - min(total, seen)) / (2u * gridDim.x)));
-                const unsigned nbase = gridDim.x + atomicAdd(sched, ngrab);
+                const unsigned nbase = gridDim.x + atomicAdd(sched + kSchedFetch, ngrab);
                 for (unsigned it = base; it < min(total, base + grab) && !pr.stopped; ++it) {
                     if (it < total_gu) {
                         const int v = (int)it / Gf, g = (int)it - v * Gf;
@@ -768,7 +852,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                         const int j = (int)(it - total_gu), v = j / Gd2, g = j - v * Gd2;
                         const uint8_t *w = down_of(A.L, R.vexp[v]) + (size_t)g * pbF;
                         const ActSlice act{A.ws.qa_bm + v * qa_region, R.vnc[v]};
-                        const unsigned *cnt = A.ws.dep + (size_t)v * nsF;
+                        const unsigned *cnt = dep_set + (size_t)v * nsF;
                         auto dep = [&](int c) {
                             const unsigned target =
                                 A.ws.stall == 1 ? ~0u : (unsigned)min(kChunk, Gf - c * kChunk);
@@ -780,10 +864,36 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                 base = nbase;
                 grab = ngrab;
             }
+            last = atomicAdd(sched + kSchedDone, 1u) == gridDim.x - 1;
             pr.finish(S.pipe);
             pr.drain(S.pipe);
         }
+        if (__shfl_sync(0xffffffffu, last ? 1 : 0, 0)) {
+            // every CTA of this launch has taken its last item and read the
+            // epoch: zero the previous call's counter set, reset the item
+            // counters, record this call's dependency words, advance the epoch
+            const unsigned o = set ^ 1u;
+            unsigned *dep_o = A.ws.dep + o * A.ws.dep_set;
+            unsigned *pc_o = A.ws.pcnt + (size_t)o * Gd2;
+            const unsigned used_o = sched[kSchedUsed + o];
+            for (unsigned i = lane; i < used_o; i += 32) dep_o[i] = 0u;
+            for (int i = lane; i < Gd2; i += 32) pc_o[i] = 0u;
+            if (lane == 0) {
+                sched[kSchedFetch] = 0u;
+                sched[kSchedDone] = 0u;
+                sched[kSchedUsed + set] = (unsigned)(R.V * nsF);
+                sched[kSchedEpoch] = R.epoch + 1u;
+            }
+        }
     } else if (warp == kEpilogueWarp) {
+        if (!pipe_wait(S.pipe, rbar, 0, true)) return;
+        if (A.fuse_combine && R.V == 0 && blockIdx.x == 0) {  // no slot has an expert: y is zero
+            for (int i = lane; i < A.n_tok * A.L.H; i += 32) A.y[i] = 0.0f;
+        }
+        const unsigned total_gu = (unsigned)(R.V * Gf);
+        const unsigned set = R.epoch & 1u;
+        unsigned *dep_set = A.ws.dep + set * A.ws.dep_set;
+        unsigned *pcnt = A.ws.pcnt + (size_t)set * Gd2;
         SetReader rd;
         for (;;) {
             const int *tagp;
@@ -830,7 +940,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                 }
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) atomicAdd(A.ws.dep + (size_t)v * nsF + g / kChunk, 1u);
+                if (lane == 0) atomicAdd(dep_set + (size_t)v * nsF + g / kChunk, 1u);
             } else {
                 // down outputs: row set r of column c, for i = 2c + r
                 const int j = it - (int)total_gu, v = j / Gd2, g = j - v * Gd2, nc = R.vnc[v];
@@ -851,11 +961,47 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                     if (i < 2 * nc && grp < Gd)
                         A.ws.obuf[(size_t)R.vslot[v][i >> 1] * A.L.H + (size_t)grp * 32 + lane] = o[i];
                 }
+                if (!A.fuse_combine) continue;
+                __threadfence();
+                __syncwarp();
+                unsigned done = 0;
+                if (lane == 0) done = atomicAdd(pcnt + g, 1u);
+                if (__shfl_sync(0xffffffffu, done, 0) == (unsigned)R.V - 1u) {
+                    // all V virtual experts have written this group: y rows
+                    // of both its 32-row groups (the one token)
+                    __threadfence();
+                    {
+                        const int t = 0;
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const int grp = 2 * g + r;
+                            if (grp >= Gd) continue;
+                            const size_t row = (size_t)grp * 32 + lane;
+                            const int p0 = t * A.k;
+                            float ov[kMaxTopk];
+#pragma unroll
+                            for (int jj = 0; jj < kMaxTopk; ++jj) {
+                                const int p = min(p0 + jj, kMaxSlots - 1);
+                                ov[jj] = jj < A.k && R.ids[p] >= 0 ? __ldcg(A.ws.obuf + (size_t)p * A.L.H + row) : 0.0f;
+                            }
+                            const float osh = A.L.shared ? __ldcg(A.ws.obuf + (size_t)(N + t) * A.L.H + row) : 0.0f;
+                            float acc = 0.0f;
+#pragma unroll
+                            for (int jj = 0; jj < kMaxTopk; ++jj) {
+                                const int p = min(p0 + jj, kMaxSlots - 1);
+                                if (jj < A.k && R.ids[p] >= 0) acc += R.w[p] * ov[jj];
+                            }
+                            A.y[(size_t)t * A.L.H + row] = acc + osh;
+                        }
+                    }
+                }
             }
         }
     } else {
         if (A.quant_tokens) quant_stage_cols<1>(A.h, A.L.H, A.nbH, A.nbpH, S.act, S.dx, threadIdx.x, kConsumers);
         consumer_sync();
+        if (!pipe_wait(S.pipe, rbar, 0, true)) return;
+        const unsigned total_gu = (unsigned)(R.V * Gf);
         Consumer co(S.pipe);
         SetWriter wr;
         for (;;) {
@@ -892,29 +1038,18 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
             if (!ok) break;
         }
     }
-    // the last CTA to finish resets the counters for the next call
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
-            for (int i = 0; i < R.V * nsF; ++i) A.ws.dep[i] = 0u;
-            sched[0] = 0u;
-            sched[1] = 0u;
-        }
-    }
 }
 
-// Router-weighted combine: y[t][r] = sum_j wts[t][j] * obuf[t*k+j][r], slots
-// in order j = 0..k-1, slots with an out-of-range id skipped, then plus the
-// shared expert's output obuf[N+t][r] when the layer has one.  One thread per
-// output; launched as a dependent of the layer kernel.  The ids and weights
-// are inputs of the call, complete before its first kernel started, so they
-// are read into shared memory before the wait; a token's k loads of obuf are
-// then issued together.
-constexpr int kMaxTopk = 16;  // routed experts per token (the ABI's limit)
-
+// Router-weighted combine of a call with more than one token: y[t][r] =
+// sum_j wts[t][j] * obuf[t*k+j][r], slots in order j = 0..k-1, slots with an
+// out-of-range id skipped, then plus the shared expert's output obuf[N+t][r]
+// when the layer has one (the sum the layer kernel forms itself for one
+// token).  One thread per output; launched as a dependent of the layer
+// kernel.  The ids and weights are inputs of the call, complete before its
+// first kernel started, so they are read into shared memory before the wait;
+// a token's k loads of obuf are then issued together.
 __global__ void __launch_bounds__(256) k_moe_combine(const __grid_constant__ MoeArgs A) {
-    __shared__ float w_s[kMaxSlots];  // router weight of each slot, 0 for a skipped slot
+    __shared__ float w_s[kMaxSlots];  // router weight of each slot
     __shared__ int ok_s[kMaxSlots];   // slot has an in-range id
     const int N = A.n_tok * A.k;
     if ((int)threadIdx.x < N) {
@@ -965,12 +1100,14 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     // one token: the layer kernel quantizes it (one launch fewer), as long as
     // its staging leaves room for the pipeline in shared memory
     A.quant_tokens = n_tok == 1 && ((uintptr_t)h & 15u) == 0 && A.nbpH <= kMaxStagedBlocks;
+    A.fuse_combine = n_tok == 1;
     cudaError_t e = cudaSuccess;
     if (ws.ev[0] && (e = cudaEventRecord(ws.ev[0], s)) != cudaSuccess) return e;
     if (!A.quant_tokens) {
         e = launch_quantize_chunked(h, L.H, n_tok, ws.qh, s);
         if (e != cudaSuccess) return e;
     }
+    if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
     {
         // four stages when two CTAs per SM still fit, else three
         const int act_blocks = A.quant_tokens ? A.nbpH : 0;
@@ -989,8 +1126,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
         e = launch_k(k_moe, grid, kPipeThreads, smem, s, true, A);
         if (e != cudaSuccess) return e;
     }
-    if (ws.ev[1] && (e = cudaEventRecord(ws.ev[1], s)) != cudaSuccess) return e;
-    {
+    if (!A.fuse_combine) {
         const int grid = (int)std::min<int64_t>(((int64_t)n_tok * L.H + 255) / 256, 1024);
         e = launch_k(k_moe_combine, grid, 256, 0, s, true, A);
         if (e != cudaSuccess) return e;
