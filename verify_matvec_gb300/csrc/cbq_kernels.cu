@@ -823,14 +823,18 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
             bool tokens_ready = A.quant_tokens != 0;  // else the quantization kernel's output needs the wait
             unsigned base = blockIdx.x, grab = 1;  // first item: the CTA index
             while (base < total && !pr.stopped) {
-                // the next grab (gate_up items one at a time; down items by
+                // the next grab: gate_up items one at a time, down items by
                 // guided grabs of up to kDownGrab consecutive items of one
-                // virtual expert, sized from where this CTA's last grab ended)
-                // is fetched when this one starts and used once its stages are
-                // issued, so the atomic's latency overlaps them
+                // virtual expert, sized from where this CTA's last grab ended.
+                // During a gate_up item it is fetched when the item starts (the
+                // atomic's latency overlaps its stages); during down items, whose
+                // stages wait on the gate_up results, only once their stages are
+                // issued, so a CTA holding down items does not take more while
+                // CTAs still on gate_up items will want them.
                 const unsigned seen = base + grab;
                 const unsigned ngrab = seen < total_gu ? 1u : max(1u, min(kDownGrab, (total - min(total, seen)) / (2u * gridDim.x)));
-                const unsigned nbase = gridDim.x + atomicAdd(sched + kSchedFetch, ngrab);
+                const bool early = base < total_gu;
+                unsigned nbase = early ? gridDim.x + atomicAdd(sched + kSchedFetch, ngrab) : 0u;
                 for (unsigned it = base; it < min(total, base + grab) && !pr.stopped; ++it) {
                     if (it < total_gu) {
                         const int v = (int)it / Gf, g = (int)it - v * Gf;
@@ -861,6 +865,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                         pr.pass(S.pipe, w, A.nbpF, 0, nsF, (int)it, act, dep);
                     }
                 }
+                if (!early) nbase = gridDim.x + atomicAdd(sched + kSchedFetch, ngrab);
                 base = nbase;
                 grab = ngrab;
             }
