@@ -732,6 +732,12 @@ constexpr unsigned kErrDependencyTimeout = 0x200u;
 constexpr unsigned kDownGrab = 4;
 constexpr int kMaxTopk = 16;  // routed experts per token (the ABI's limit)
 
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -760,6 +766,49 @@ __device__ __forceinline__ bool wait_dependency(const unsigned *cnt, unsigned ta
     asm volatile("fence.proxy.async.global;" ::: "memory");
     return true;
 }
+
+// The slices of a down pass: chunk c of the intermediate of virtual expert v
+// (cnt: its per-chunk counts) is ready once all of its min(16, Gf - 16c)
+// gate_up groups are published.  all_ready() polls every chunk's count in
+// batches of relaxed loads issued together (then one acquire fence), and
+// remembers a virtual expert found complete in a per-CTA bit (counts only
+// grow within a call), so the down items of an expert whose gate_up work is
+// long done cost no polls at all; ready() polls one chunk, wait() waits for
+// it (bounded).  In give-up test mode 1 a slice is never ready.  Every true
+// result is followed by a proxy fence, so the bulk copies issued next see
+// what the publishers wrote.
+struct DownDep {
+    const unsigned *cnt;
+    int Gf, stall;
+    const Pipe *P;
+    unsigned *vready;  // shared-memory bits: virtual experts whose slices are all ready
+    int v;
+    __device__ __forceinline__ unsigned target(int c) const {
+        return stall == 1 ? ~0u : (unsigned)min(kChunk, Gf - c * kChunk);
+    }
+    __device__ __forceinline__ bool all_ready(int c0, int c1) const {
+        if (vready[v >> 5] & (1u << (v & 31))) return true;
+        constexpr int kBatch = 8;
+        for (int c = c0; c < c1; c += kBatch) {
+            unsigned got[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) got[i] = c + i < c1 ? ld_relaxed(cnt + c + i) : ~0u;
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                if (c + i < c1 && got[i] < target(c + i)) return false;
+        }
+        vready[v >> 5] |= 1u << (v & 31);
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        return true;
+    }
+    __device__ __forceinline__ bool ready(int c) const {
+        if (ld_acquire(cnt + c) < target(c)) return false;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        return true;
+    }
+    __device__ __forceinline__ bool wait(int c) const { return wait_dependency(cnt + c, target(c), *P); }
+};
 
 // The whole routed-expert layer, combine included, in one persistent kernel.
 // Work items, in this order (the first per CTA is its index, the rest come
@@ -792,8 +841,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Routing R;
     __shared__ __align__(8) uint64_t route_bar;  // the routing table is ready (one arrive per producer lane)
+    __shared__ unsigned vready[(kMaxSlots + 31) / 32];  // producer: virtual experts with all slices ready
     PipeSmem S = carve_pipe(smem, A.stages, kStageBytesAct, kSetBytes, 2, A.quant_tokens ? A.nbpH : 0, A.ws.err);
     pipe_init(S.pipe);
+    if (threadIdx.x < (kMaxSlots + 31) / 32) vready[threadIdx.x] = 0u;
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&route_bar), 32);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -851,17 +902,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_moe(const __grid_constant__
                             tokens_ready = true;
                         }
                         const ActSlice act{A.ws.qh, A.quant_tokens ? 0 : A.n_tok};
-                        pr.pass(S.pipe, w, A.nbpH, 0, nchH, (int)it, act, [](int) { return true; });
+                        Producer::NoDep nd;
+                        pr.pass(S.pipe, w, A.nbpH, 0, nchH, (int)it, act, nd);
                     } else {
                         const int j = (int)(it - total_gu), v = j / Gd2, g = j - v * Gd2;
                         const uint8_t *w = down_of(A.L, R.vexp[v]) + (size_t)g * pbF;
                         const ActSlice act{A.ws.qa_bm + v * qa_region, R.vnc[v]};
-                        const unsigned *cnt = dep_set + (size_t)v * nsF;
-                        auto dep = [&](int c) {
-                            const unsigned target =
-                                A.ws.stall == 1 ? ~0u : (unsigned)min(kChunk, Gf - c * kChunk);
-                            return wait_dependency(cnt + c, target, S.pipe);
-                        };
+                        DownDep dep{dep_set + (size_t)v * nsF, Gf, A.ws.stall, &S.pipe, vready, v};
                         pr.pass(S.pipe, w, A.nbpF, 0, nsF, (int)it, act, dep);
                     }
                 }

@@ -163,39 +163,92 @@ struct Producer {
         return true;
     }
 
+    // One stage: claim its slot, tag it, expect its bytes (weights and, with
+    // act.cols, its slice) and issue its weight copy.  False when stopped.
+    __device__ __forceinline__ bool issue_weights(const Pipe &P, const uint8_t *w, int nbp, int c, int tag,
+                                                  const ActSlice &act, uint32_t &dst, uint32_t &bar) {
+        const int nblk = chunk_blocks(nbp, c);
+        uint32_t slot;
+        if (!claim(P, slot)) return false;
+        dst = smem_addr(P.ring) + slot * P.stage_bytes;
+        bar = P.full0 + 8u * slot;
+        const uint32_t bw = (uint32_t)nblk * (2 * kBlockBytes), ba = (uint32_t)(nblk * act.cols) * 36u;
+        P.tag[slot] = tag;
+        mbar_expect_tx(bar, bw + ba);
+        bulk_g2s(dst, w + (size_t)c * kChunkBytes, bw, bar);
+        ++it;
+        return true;
+    }
+
+    __device__ __forceinline__ void issue_act(const Pipe &P, int nbp, int c, const ActSlice &act, uint32_t dst,
+                                              uint32_t bar) {
+        const uint32_t ba = (uint32_t)(chunk_blocks(nbp, c) * act.cols) * 36u;
+        bulk_g2s(dst + kStageWeightBytes, act.base + act_chunk_offset(c, act.cols), ba, bar);
+    }
+
     // The stages of chunks [c0, c1) of a pass over a pair (its bytes at w,
-    // nbp blocks), tagged `tag`, each with its chunk of `act`.  dep(c) is
-    // called after chunk c's weight copy is issued and before its activation
-    // copy: it waits until the slice may be read and returns false to give up
-    // (the producer then stops).
+    // nbp blocks), tagged `tag`, each with its chunk of `act`.  When
+    // dep.all_ready(c0, c1) finds every slice readable (one batch of polls),
+    // each stage's two copies go out together.  Otherwise the weight copies
+    // run ahead of the slices: a slice is issued, in order, once dep.ready(c)
+    // (a poll) says it may be read, and waited for (dep.wait(c), bounded;
+    // false gives up and stops the producer) only before a slot it would
+    // block is claimed and at the end of the pass.
     template <typename Dep>
     __device__ __forceinline__ void pass(const Pipe &P, const uint8_t *w, int nbp, int c0, int c1, int tag,
-                                         const ActSlice &act, Dep &&dep) {
-        for (int c = c0; c < c1 && !stopped; ++c) {
-            const int nblk = chunk_blocks(nbp, c);
-            uint32_t slot;
-            if (!claim(P, slot)) break;
-            const uint32_t dst = smem_addr(P.ring) + slot * P.stage_bytes;
-            const uint32_t bar = P.full0 + 8u * slot;
-            const uint32_t bw = (uint32_t)nblk * (2 * kBlockBytes), ba = (uint32_t)(nblk * act.cols) * 36u;
-            P.tag[slot] = tag;
-            mbar_expect_tx(bar, bw + ba);
-            bulk_g2s(dst, w + (size_t)c * kChunkBytes, bw, bar);
-            if (act.cols) {
-                if (!dep(c)) {  // the slice will never be ready: stop (the stage stays incomplete)
-                    stopped = true;
-                    *(volatile int *)P.abort = 1;
-                    ++it;
-                    break;
-                }
-                bulk_g2s(dst + kStageWeightBytes, act.base + act_chunk_offset(c, act.cols), ba, bar);
+                                         const ActSlice &act, Dep &dep) {
+        if (!act.cols || dep.all_ready(c0, c1)) {
+            for (int c = c0; c < c1 && !stopped; ++c) {
+                uint32_t dst, bar;
+                if (!issue_weights(P, w, nbp, c, tag, act, dst, bar)) break;
+                if (act.cols) issue_act(P, nbp, c, act, dst, bar);
             }
-            ++it;
+            return;
+        }
+        int owed = c0;              // first chunk whose slice is not issued yet
+        uint32_t owed_it = it;      // its stage
+        auto settle = [&](int upto, bool must) -> bool {
+            while (owed < upto) {
+                if (!dep.ready(owed)) {
+                    if (!must) return true;
+                    if (!dep.wait(owed)) return false;
+                }
+                const uint32_t slot = owed_it % (uint32_t)P.S;
+                issue_act(P, nbp, owed, act, smem_addr(P.ring) + slot * P.stage_bytes, P.full0 + 8u * slot);
+                ++owed;
+                ++owed_it;
+            }
+            return true;
+        };
+        for (int c = c0; c < c1 && !stopped; ++c) {
+            // chunk c's slot held chunk c - S of this pass, if any: its slice
+            // must be out before the consumers can free the slot
+            if (!settle(c - P.S + 1, true)) {
+                stopped = true;
+                *(volatile int *)P.abort = 1;
+                break;
+            }
+            uint32_t dst, bar;
+            if (!issue_weights(P, w, nbp, c, tag, act, dst, bar)) break;
+            settle(c + 1, false);
+        }
+        if (!stopped && !settle(c1, true)) {
+            // a slice that will never be ready: stop (its stage stays incomplete)
+            stopped = true;
+            *(volatile int *)P.abort = 1;
         }
     }
 
+    // A pass whose slices are always ready (or that has none).
+    struct NoDep {
+        __device__ __forceinline__ bool all_ready(int, int) const { return true; }
+        __device__ __forceinline__ bool ready(int) const { return true; }
+        __device__ __forceinline__ bool wait(int) const { return true; }
+    };
+
     __device__ __forceinline__ void pass(const Pipe &P, const uint8_t *w, int nbp, int c0, int c1, int tag) {
-        pass(P, w, nbp, c0, c1, tag, ActSlice{nullptr, 0}, [](int) { return true; });
+        NoDep nd;
+        pass(P, w, nbp, c0, c1, tag, ActSlice{nullptr, 0}, nd);
     }
 
     // Give-up test mode only: claim a slot and tag it, but never fill it (the
