@@ -249,19 +249,20 @@ int cbq_moe_set_stage_events(cbq_moe *L, void *ev_start, void *ev_layer, void *e
  * of this many quantized values plus their scales: 92,160 bytes per device). */
 #define CBQ_STATIC_SCRATCH_MAX_K 16384
 
-/* cbq_matvec for callers that must not allocate device memory while they run:
- * code recording a CUDA graph by stream capture (where a cudaMalloc would not
- * be part of the graph and may break the capture), or hosts that fix their
- * device memory budget at start-up and forbid allocation afterwards.  The
- * pages describe no counterpart; it is the dense path of cbq_matvec with one
- * difference: the quantized activations go to a scratch array the library
- * declares statically on every device (it lives as long as the library is
- * loaded), not to the handle's workspace.  Nothing is allocated or freed,
- * here or in any library routine it calls.
+/* cbq_matvec for callers that must not allocate device memory while they run,
+ * e.g. hosts that fix their device memory budget at start-up and forbid
+ * allocation afterwards.  The pages describe no counterpart; it is the dense
+ * path of cbq_matvec with one difference: with more than one column, or x_dev
+ * not 16-byte aligned, the quantized activations go to a scratch array the
+ * library declares statically on every device (it lives as long as the
+ * library is loaded), not to the handle's workspace; one aligned column is
+ * quantized inside the matvec kernel (one launch), as cbq_matvec does, and
+ * needs no scratch.  Nothing is allocated or freed, here or in any library
+ * routine it calls.  Same bits as cbq_matvec.
  *   - Arguments as cbq_matvec; K of W must be <= CBQ_STATIC_SCRATCH_MAX_K,
  *     else CBQ_EINVAL (checked before anything runs).
  *   - The first call on a device looks the scratch array up on that device
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress).
  *   - The scratch is one array per device shared by every call of this entry
  *     point on that device, whatever the handle: calls that may overlap on the
  *     GPU (different streams without ordering) race.  Every call rewrites the
@@ -299,10 +300,15 @@ int cbq_moe_set_debug(cbq_moe *L, int keep_intermediate);
 /* Give-up test mode of the layer kernel, for the tests of its bounded waits
  * (0 turns it off): mode 1 makes every down-projection item wait for an
  * intermediate count that is never reached, so that wait gives up after its
- * 1 s limit (CBQ_DEVERR_DEPENDENCY_TIMEOUT) and the CTA stops; mode 2 makes
- * the first CTA's first weight stage never arrive, so its consumers' wait
- * gives up (CBQ_DEVERR_PIPE_TIMEOUT).  A call in either mode returns after
- * a few seconds with undefined outputs and leaves the handle usable. */
+ * 1 s limit (CBQ_DEVERR_DEPENDENCY_TIMEOUT, or CBQ_DEVERR_PIPE_TIMEOUT when
+ * the consumers' own 1 s wait for that stage runs out first) and the CTA
+ * stops; mode 2 makes the first CTA's first weight stage never arrive, so its
+ * consumers' wait gives up (CBQ_DEVERR_PIPE_TIMEOUT; the down items that
+ * need that CTA's gate_up results then give up too).  Either way the CTA
+ * issues no copy after giving up and waits (bounded) for those in flight, so
+ * none is left running when it exits.  A call in either mode returns after a
+ * few seconds with undefined outputs, sets only timeout bits, and leaves the
+ * handle usable: the next call is correct. */
 int cbq_moe_debug_stall(cbq_moe *L, int mode);
 
 /* Copy the intermediate of the last cbq_moe_matvec on this handle, for

@@ -112,13 +112,11 @@ def test_matvec_4096_full(torch, n):
     _check_matvec(torch, W, M, K, synth.activations(n, K, stream=synth.S_X + n, outliers=(n == 1)))
 
 
-@pytest.mark.parametrize("n", [1, 5])
-def test_matvec_16384_sampled(torch, n):
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_matvec_16384_all_rows(torch, n):
     M, K = 16384, 4096
     W = synth.weight_blocks(M, K, stream=synth.S_W + 50)
-    rows = np.unique(np.concatenate([np.arange(0, 40), np.arange(M - 40, M),
-                                     np.random.default_rng(1).integers(0, M, 400)]))
-    _check_matvec(torch, W, M, K, synth.activations(n, K, stream=synth.S_X + 50, outliers=True), rows=rows)
+    _check_matvec(torch, W, M, K, synth.activations(n, K, stream=synth.S_X + 50, outliers=True))
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
@@ -163,14 +161,13 @@ def test_matvec_exact_invariants(torch):
     np.testing.assert_array_equal(y2, 2 * y)
 
 
-def test_output_head_sampled_bench_shape(torch):
-    """The 129280 x 4096 head at n = 5, launched as the benchmark launches it."""
+def test_output_head_all_rows_bench_shape(torch):
+    """The 129280 x 4096 head at n = 5, launched as the benchmark launches it,
+    every row against the oracle."""
     M, K, n = 129280, 4096, 5
     W = synth.weight_blocks(M, K, stream=synth.S_HEAD)
     x = synth.activations(n, K, stream=synth.S_HEAD_X)
-    rows = np.unique(np.concatenate([np.arange(0, 32), np.arange(M - 64, M),
-                                     np.random.default_rng(2).integers(0, M, 300)]))
-    _check_matvec(torch, W, M, K, x, rows=rows)
+    _check_matvec(torch, W, M, K, x)
 
 
 def test_largest_k_accepted_and_correct(torch):

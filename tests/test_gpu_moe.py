@@ -148,6 +148,32 @@ def test_nothing_routed_gives_zero(torch, small):
     assert cbq.cbq_moe_get_error(L) == 0  # read clears
 
 
+def test_nothing_routed_gives_zero_one_token(torch, small):
+    """One token (the layer kernel forms y itself): no valid id still writes y."""
+    gu, dn, L = small
+    h = synth.activations(1, H_S, stream=614)
+    ids = np.array([[-3, 8, 11]], dtype=np.int32)
+    wts = np.ones((1, 3), dtype=np.float32)
+    y = cbq.cbq_moe_matvec(L, _dev(torch, h), _dev(torch, ids), _dev(torch, wts),
+                           y=torch.full((1, H_S), 7.0, device="cuda")).cpu().numpy()
+    assert np.all(y == 0)
+    assert cbq.cbq_moe_get_error(L) == cbq.CBQ_DEVERR_BAD_EXPERT_ID
+
+
+def test_error_word_is_per_handle(torch, small):
+    """A bad id on one handle shows in that handle's error word only."""
+    gu, dn, L = small
+    L2 = cbq.Moe(gu, dn, E_S, H_S, F_S)
+    h = synth.activations(2, H_S, stream=615)
+    bad = np.array([[1, 99], [2, 3]], dtype=np.int32)
+    ids, wts = synth.router(2, 2, E_S, stream=616)
+    cbq.cbq_moe_matvec(L, _dev(torch, h), _dev(torch, bad), _dev(torch, wts))
+    cbq.cbq_moe_matvec(L2, _dev(torch, h), _dev(torch, ids), _dev(torch, wts))
+    torch.cuda.synchronize()
+    assert cbq.cbq_moe_get_error(L2) == 0
+    assert cbq.cbq_moe_get_error(L) == cbq.CBQ_DEVERR_BAD_EXPERT_ID
+
+
 def test_host_entry_matches(torch, small):
     gu, dn, L = small
     h = synth.activations(4, H_S, stream=612)

@@ -322,6 +322,10 @@ int cbq_matvec_static(const cbq_weights *W, const float *x_dev, int n, float *y_
     int8_t *qx = reinterpret_cast<int8_t *>(scratch);
     float *dx = reinterpret_cast<float *>(scratch + kStaticQxBytes);
     cudaStream_t s = as_stream(stream);
+    if (n == 1 && aligned16(x_dev)) {  // as cbq_matvec: one launch, no scratch
+        CBQ_CUDA(cbq::launch_matvec_f32(W->mat, x_dev, n, y_dev, s));
+        return CBQ_OK;
+    }
     CBQ_CUDA(cbq::launch_quantize(x_dev, W->K, n, qx, dx, s));
     CBQ_CUDA(cbq::launch_matvec(W->mat, qx, dx, n, y_dev, s, /*pdl=*/true));
     return CBQ_OK;
