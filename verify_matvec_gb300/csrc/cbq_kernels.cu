@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
             const int it = co.wait(S.pipe) ? co.tag(S.pipe) : -1;
             int *tag;
             float *part;
-            if (!wr.acquire(S.pipe, tag, part)) break;
             if (it < 0) {
+                if (!wr.acquire(S.pipe, tag, part)) break;
                 if (threadIdx.x == 0) *tag = -1;
                 wr.publish(S.pipe);
                 break;
@@ -336,6 +336,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
 #pragma unroll
             for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
             const bool ok = dense_pass<NC>(co, S.pipe, W.nbp, S.act, S.dx, acc, warp, lane);
+            // the set is taken only now: the epilogue had the whole pass to free it
+            if (!wr.acquire(S.pipe, tag, part)) break;
 #pragma unroll
             for (int c = 0; c < NC; ++c) part[(warp * NC + c) * 32 + lane] = acc[c].x + acc[c].y;
             if (threadIdx.x == 0) *tag = it;
@@ -1196,7 +1198,7 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
 // of fp32 logits are exact there) and rounded once to fp32.
 __global__ void __launch_bounds__(32) k_router_topk(const float *__restrict__ logits, int E, int k,
                                                     int32_t *__restrict__ ids, float *__restrict__ wts) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     float *l = reinterpret_cast<float *>(smem);
     unsigned char *taken = smem + (size_t)E * sizeof(float);
     const int t = blockIdx.x, lane = threadIdx.x;
