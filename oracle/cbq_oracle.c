@@ -330,3 +330,63 @@ void oracle_router_topk(const float *logits, int n_tok, int E, int k, int32_t *i
     }
     free(taken);
 }
+
+/* binary16 has 11 significant bits: a value in [2^(e-1), 2^e) is a multiple
+ * of 2^(e-11); below 2^-14 (subnormals) every value is a multiple of 2^-24.
+ * Scaling by a power of two is exact in fp64, so nearbyint() (the default
+ * rounding mode: nearest, ties to even) is the one rounding. */
+uint16_t oracle_float_to_half(float f)
+{
+    const uint16_t sign = signbit(f) ? 0x8000u : 0u;
+    if (isnan(f)) return (uint16_t)(sign | 0x7e00u);
+    const double a = fabs((double)f);
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7c00u);
+    if (a < ldexp(1.0, -14)) {
+        const double q = nearbyint(ldexp(a, 24));  /* 1024 is the smallest normal */
+        return (uint16_t)(sign | (uint16_t)q);
+    }
+    int e;
+    frexp(a, &e);                                  /* a in [2^(e-1), 2^e) */
+    double q = nearbyint(ldexp(a, 11 - e));        /* in [1024, 2048] */
+    int expo = e + 14;                             /* biased exponent of 2^(e-1) */
+    if (q == 2048.0) {
+        q = 1024.0;
+        expo += 1;
+    }
+    return (uint16_t)(sign | (uint16_t)(expo << 10) | (uint16_t)((int)q - 1024));
+}
+
+void oracle_quantize_weights_block(const float *w, uint8_t *blk)
+{
+    memset(blk, 0, ORACLE_BLOCK_BYTES);
+    int imax = 0;
+    for (int i = 1; i < ORACLE_QK; ++i)
+        if (fabsf(w[i]) > fabsf(w[imax])) imax = i;
+    const float m = w[imax];
+    if (m == 0.0f) return;
+    const uint16_t hb = oracle_float_to_half(m / -127.0f);
+    const double dw = (double)oracle_half_to_float(hb);
+    blk[0] = (uint8_t)(hb & 0xff);
+    blk[1] = (uint8_t)(hb >> 8);
+    for (int i = 0; i < ORACLE_QK; ++i) {
+        int best = 0;
+        double best_d = fabs((double)w[i] - dw * (double)oracle_codebook[0]);
+        for (int j = 1; j < 16; ++j) {
+            const double d = fabs((double)w[i] - dw * (double)oracle_codebook[j]);
+            if (d < best_d) {
+                best = j;
+                best_d = d;
+            }
+        }
+        if (i < 16) blk[2 + i] |= (uint8_t)best;
+        else blk[2 + i - 16] |= (uint8_t)(best << 4);
+    }
+}
+
+void oracle_quantize_weights(const float *w, int64_t M, int64_t K, uint8_t *blocks)
+{
+    const int64_t nb = K / ORACLE_QK;
+    for (int64_t r = 0; r < M; ++r)
+        for (int64_t b = 0; b < nb; ++b)
+            oracle_quantize_weights_block(w + r * K + b * ORACLE_QK, blocks + (r * nb + b) * ORACLE_BLOCK_BYTES);
+}

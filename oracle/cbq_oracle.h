@@ -45,7 +45,10 @@
  * nearest/tie-to-even properties; block dots against the per-entry table,
  * one-hot positions and a hand-worked block; the matvec against an fp64
  * dequantize-then-dot; scale linearity, sign symmetry and zero scales; the MoE
- * against its k=1 reduction, the silu odd-part identity and token independence.
+ * against its k=1 reduction, the silu odd-part identity and token independence;
+ * the weight converter against numpy's binary16 rounding, hand-worked blocks
+ * (ties, a negative maximum, a zero block), an exact round trip of weights on
+ * the codebook grid and an exact-rational nearest-level search.
  */
 #ifndef CBQ_ORACLE_H
 #define CBQ_ORACLE_H
@@ -151,6 +154,29 @@ int oracle_moe_down_combine(const uint8_t *down, int E, int64_t H, int64_t F,
  * k selected logits, computed in fp64 (exp(l_j - l_max) / sum).
  * 1 <= k <= E. */
 void oracle_router_topk(const float *logits, int n_tok, int E, int k, int32_t *ids, double *wts);
+
+/* IEEE 754 binary32 -> binary16, rounded to nearest, ties to even; values of
+ * magnitude 65520 and above (and infinities) give infinity, NaN a quiet NaN. */
+uint16_t oracle_float_to_half(float f);
+
+/* The weight converter: fp32 weights to the 4-bit codebook format (the
+ * "CPU reference conversions" of the quant types in "feat(ds4): add DSpark
+ * speculative runtime + optimizations" #496; the pages give no rule, this is
+ * the plain reading).  For one block of 32 weights w[0..32):
+ *   m = the weight of largest magnitude (the first one among equal
+ *       magnitudes); if m == 0 the block is all zero bytes;
+ *   dw = binary16(m / -127): the fp32 division, then rounding to nearest
+ *       even -- -127 is the codebook level of largest magnitude, so m lands
+ *       on it;
+ *   index_i = the j minimising |w_i - dw * codebook[j]| (distances exact in
+ *       fp64), the lowest j among equal distances;
+ * packed as the format says (dw little-endian in bytes 0-1, element i's index
+ * in the low nibble of byte 2+i for i < 16, in the high nibble of byte
+ * 2+i-16 otherwise).  |m| must stay below 127 * 65520 (a finite scale). */
+void oracle_quantize_weights_block(const float *w, uint8_t *blk);
+
+/* A row-major M x K fp32 matrix (K % 32 == 0) to M x (K/32) blocks. */
+void oracle_quantize_weights(const float *w, int64_t M, int64_t K, uint8_t *blocks);
 
 #ifdef __cplusplus
 }

@@ -73,6 +73,10 @@ def _bind(lib):
     lib.oracle_moe_down_combine.restype = I
     lib.oracle_router_topk.argtypes = [P, I, I, I, P, P]
     lib.oracle_router_topk.restype = None
+    lib.oracle_float_to_half.argtypes = [ctypes.c_float]
+    lib.oracle_float_to_half.restype = ctypes.c_uint16
+    lib.oracle_quantize_weights_block.argtypes = [P, P]
+    lib.oracle_quantize_weights.argtypes = [P, I64, I64, P]
     return lib
 
 
@@ -258,3 +262,16 @@ def router_topk(logits, k):
     wts = np.empty((n_tok, k), dtype=np.float64)
     _load().oracle_router_topk(_p(logits), n_tok, E, k, _p(ids), _p(wts))
     return ids, wts
+
+
+def float_to_half(x: float) -> int:
+    """binary16 bits of fp32 x, rounded to nearest even."""
+    return int(_load().oracle_float_to_half(float(np.float32(x))))
+
+
+def quantize_weights(w: np.ndarray, M: int, K: int) -> np.ndarray:
+    """The weight converter: fp32 w (M, K) -> blocks (M, K/32, 18) uint8."""
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(M, K)
+    out = np.empty((M, K // QK, BLOCK_BYTES), dtype=np.uint8)
+    _load().oracle_quantize_weights(_p(w), M, K, _p(out))
+    return out

@@ -546,3 +546,109 @@ def test_router_topk_invariants():
     ids3, wts3 = O.router_topk(distinct[:, perm], 8)
     np.testing.assert_array_equal(perm[ids3], ids_d)
     np.testing.assert_array_equal(wts3, wts_d)
+
+
+# ------------------------------------------------------ weight converter ---
+
+def _read_convert_cases(golden_dir):
+    cases = []
+    with open(os.path.join(golden_dir, "convert_blocks.txt")) as f:
+        for line in f:
+            if not line.startswith("convert "):
+                continue
+            head, tail = line.split("=")
+            parts = head.split()
+            w = np.array([float(v) for v in parts[2:]], dtype=np.float32)
+            blk = np.array([int(b, 16) for b in tail.split()], dtype=np.uint8)
+            assert w.size == 32 and blk.size == 18
+            cases.append((parts[1], w, blk))
+    return cases
+
+
+def test_float_to_half_matches_numpy():
+    """binary16 rounding against numpy's float32 -> float16 conversion: every
+    finite binary16 value, the midpoints between neighbours (ties to even),
+    and random float32 across the subnormal, normal and overflow ranges."""
+    bits = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    h = bits.view(np.float16)
+    finite = np.isfinite(h)
+    vals = [h[finite].astype(np.float32)]
+    hs = np.sort(np.unique(np.abs(h[finite].astype(np.float64))))
+    mids = (hs[:-1] + hs[1:]) / 2  # exact in fp32 (12 significant bits)
+    vals += [mids.astype(np.float32), -mids.astype(np.float32)]
+    rng = np.random.default_rng(11)
+    for lo, hi in ((-30, -24), (-24, -14), (-14, 16), (15, 17)):
+        e = rng.uniform(lo, hi, 4000)
+        vals.append((np.sign(rng.standard_normal(4000)) * 2.0 ** e).astype(np.float32))
+    vals.append(np.array([65504, 65519.99, 65520, 1e30, np.inf, -np.inf, 0.0, -0.0], dtype=np.float32))
+    for v in np.concatenate(vals):
+        want = int(np.float32(v).astype(np.float16).view(np.uint16))
+        assert O.float_to_half(v) == want, (float(v), hex(want))
+
+
+def test_convert_golden_blocks(golden_dir):
+    for name, w, blk in _read_convert_cases(golden_dir):
+        np.testing.assert_array_equal(O.quantize_weights(w, 1, 32).ravel(), blk, err_msg=name)
+
+
+def test_convert_grid_round_trip():
+    """Weights that are exactly dw * codebook[index] with a level -127 present
+    (the unique largest magnitude) come back as exactly those bytes: the
+    scale rule, the index search, the nibble packing and the byte order."""
+    rng = np.random.default_rng(12)
+    M, K = 7, 96
+    nb = K // 32
+    blocks = np.zeros((M, nb, 18), dtype=np.uint8)
+    w = np.zeros((M, K), dtype=np.float32)
+    for r in range(M):
+        for b in range(nb):
+            dw = np.float16(rng.uniform(1e-3, 1e-2) * rng.choice([-1, 1]))
+            idx = rng.integers(1, 16, 32)
+            idx[rng.integers(0, 32)] = 0
+            hb = int(np.array(dw).view(np.uint16))
+            blocks[r, b, 0], blocks[r, b, 1] = hb & 0xFF, hb >> 8
+            blocks[r, b, 2:] = (idx[:16] | (idx[16:] << 4)).astype(np.uint8)
+            w[r, 32 * b:32 * b + 32] = (np.float32(dw) * O.CODEBOOK[idx].astype(np.float32))
+    np.testing.assert_array_equal(O.quantize_weights(w, M, K), blocks)
+
+
+def test_convert_brute_force_exact():
+    """Random blocks: the scale by numpy (fp32 division, float16 rounding) and
+    every index by an exact-rational search over the 16 levels (lowest index
+    among equal distances)."""
+    rng = np.random.default_rng(13)
+    w = (rng.standard_normal((5, 64)) * rng.uniform(0.01, 3.0, (5, 1))).astype(np.float32)
+    w[2, 40] = w[2, 33] = -np.abs(w[2]).max() * 1.5  # equal largest magnitudes: the first one counts
+    got = O.quantize_weights(w, 5, 64)
+    for r in range(5):
+        for b in range(2):
+            x = w[r, 32 * b:32 * b + 32]
+            m = x[int(np.argmax(np.abs(x)))]  # argmax takes the first of equal values
+            dw = np.float16(np.float32(m) / np.float32(-127.0))
+            blk = got[r, b]
+            assert int(blk[0]) | (int(blk[1]) << 8) == int(np.array(dw).view(np.uint16))
+            D = Fraction(float(dw))
+            for i in range(32):
+                dist = [abs(Fraction(float(x[i])) - D * int(O.CODEBOOK[j])) for j in range(16)]
+                want = dist.index(min(dist))
+                have = int(blk[2 + i] & 0xF) if i < 16 else int(blk[2 + i - 16] >> 4)
+                assert have == want, (r, b, i)
+
+
+def test_convert_error_bound_and_zero_blocks():
+    """Every weight comes back within 14 scale units of itself (half the widest
+    gap between levels is 12; a weight of the other sign than the largest one
+    can sit 127 - 113 = 14 units past the last level), plus the scale's own
+    rounding; an all-zero block converts to zero bytes."""
+    rng = np.random.default_rng(14)
+    M, K = 6, 128
+    w = rng.standard_normal((M, K)).astype(np.float32)
+    w[3, 32:64] = 0.0
+    blocks = O.quantize_weights(w, M, K)
+    assert not blocks[3, 1].any()
+    for r in range(M):
+        for b in range(K // 32):
+            dq = O.dequantize_block(blocks[r, b])
+            x = w[r, 32 * b:32 * b + 32].astype(np.float64)
+            dw = abs(O.half_to_float(int(blocks[r, b, 0]) | (int(blocks[r, b, 1]) << 8)))
+            assert np.all(np.abs(dq - x) <= 14 * dw + 127 * dw * 2.0 ** -10)

@@ -37,6 +37,15 @@ MUTANTS = {
     "shared expert output dropped": ("y[i] += ys[i];", "y[i] += 0.0 * ys[i];"),
     "router ties to the higher index": ("l[e] > l[best]", "l[e] >= l[best]"),
     "router weights not normalised": ("for (int j = 0; j < k; ++j) wts[t * k + j] /= sum;", ""),
+    "converter ties to the higher index": ("if (d < best_d) {", "if (d <= best_d) {"),
+    "converter scale over -128": ("oracle_float_to_half(m / -127.0f)", "oracle_float_to_half(m / -128.0f)"),
+    "converter scale sign flipped": ("oracle_float_to_half(m / -127.0f)", "oracle_float_to_half(m / 127.0f)"),
+    "converter keeps the last largest weight": ("if (fabsf(w[i]) > fabsf(w[imax])) imax = i;",
+                                                "if (fabsf(w[i]) >= fabsf(w[imax])) imax = i;"),
+    "converter nibble halves swapped": ("if (i < 16) blk[2 + i] |= (uint8_t)best;\n        else blk[2 + i - 16] |= (uint8_t)(best << 4);",
+                                        "if (i < 16) blk[2 + i] |= (uint8_t)(best << 4);\n        else blk[2 + i - 16] |= (uint8_t)best;"),
+    "half rounding truncates": ("double q = nearbyint(ldexp(a, 11 - e));", "double q = floor(ldexp(a, 11 - e));"),
+    "half subnormals flushed": ("const double q = nearbyint(ldexp(a, 24));", "const double q = 0.0;"),
 }
 
 
@@ -71,6 +80,11 @@ def _pins():
         lambda: T.test_moe_shared_equal_to_a_routed_expert(tiny),
         lambda: T.test_router_topk_golden(GOLDEN),
         lambda: T.test_router_topk_invariants(),
+        lambda: T.test_float_to_half_matches_numpy(),
+        lambda: T.test_convert_golden_blocks(GOLDEN),
+        lambda: T.test_convert_grid_round_trip(),
+        lambda: T.test_convert_brute_force_exact(),
+        lambda: T.test_convert_error_bound_and_zero_blocks(),
     ]
 
 
