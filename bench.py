@@ -629,6 +629,18 @@ def run_gpu(args):
                                        "rotating_copies": copies, "rotating_bytes": copies * wb}
         del Ws
 
+    # the weight converter (fp32 matrix -> codebook blocks) on a 16384 x 4096
+    # matrix: 268 MB read, 38 MB written per call, two inputs alternating
+    # (more than four times L2 between two reads of one input)
+    Mc, Kc = 16384, 4096
+    wc = [torch.randn((Mc, Kc), dtype=torch.float32, device=dev) * 0.02 for _ in range(2)]
+    bc = torch.empty((Mc, Kc // QK, BB), dtype=torch.uint8, device=dev)
+    conv_us = graph_us(lambda i: cbq.cbq_quantize_weights(wc[i % 2], out=bc), n_calls=2, replays=10)
+    conv_bytes = Mc * Kc * 4 + Mc * (Kc // QK) * BB
+    converter = {"shape": [Mc, Kc], "us": conv_us, "bytes_per_call": conv_bytes,
+                 "gbs": conv_bytes / (conv_us * 1e-6) / 1e9, "frac_of_peak": conv_bytes / (conv_us * 1e-6) / 1e9 / peak}
+    del wc, bc
+
     # slowest rank decides; bytes add up over ranks
     (ms_max, e2e_max), (value, e2e_value) = aggregate([ms, e2e_ms], sum(wbytes), world, dev)
     h2d = N_TOK * H * 4 + 2 * slots * 4 + HEAD_N * HEAD_K * 4
@@ -676,6 +688,7 @@ def run_gpu(args):
                              "eager_split_us_quantize_layer": {"batch1": b1_split, "batch5": b5_split}},
             "us_per_layer_with_shared_expert": shared,
             "us_per_call_dense": dense,
+            "weight_converter": converter,
             "kernels_ms_per_step": {"moe layer call (k_quantize + k_moe + k_moe_combine)": sum(k_moe) / len(timed),
                                     "head call (k_quantize + k_matvec<5>)": sum(k_head) / len(timed)},
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

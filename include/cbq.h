@@ -222,6 +222,26 @@ int cbq_moe_matvec(const cbq_moe *L, const float *h_dev, int n_tok, const int32_
 int cbq_router_topk(const float *logits_dev, int n_tok, int E, int topk, int32_t *ids_dev, float *wts_dev,
                     void *stream);
 
+/* The weight converter: a row-major M x K fp32 matrix on the device to the
+ * M x (K/32) canonical 18-byte blocks that cbq_weights_create and
+ * cbq_moe_create read (on_device = 1).  The pages name "CPU reference
+ * conversions" of the quant types ("feat(ds4): add DSpark speculative
+ * runtime + optimizations" #496) without a rule; this is the plain reading,
+ * per block of 32 weights:
+ *   m = the weight of largest magnitude (the first among equal ones);
+ *   scale = binary16(m / -127): IEEE fp32 division, then rounding to nearest
+ *           even (-127 is the codebook level of largest magnitude, so m lands
+ *           on it); an all-zero block gives 18 zero bytes;
+ *   index_i = the level j whose reconstruction scale * codebook[j] is nearest
+ *           to w_i, the lowest j among equal distances (index 0 everywhere
+ *           when the scale rounds to zero).
+ * The decisions are exact (no rounding can move a weight to another level),
+ * so the bytes are the same on every run.  Weights must be finite with
+ * |m| < 127 * 65520 (a finite scale).  w_dev 16-byte aligned, blocks_dev
+ * 2-byte aligned, both owned by the caller; M >= 1, K >= 32, K % 32 == 0,
+ * else CBQ_EINVAL.  One kernel launch on `stream`. */
+int cbq_quantize_weights(const float *w_dev, int64_t M, int64_t K, void *blocks_dev, void *stream);
+
 /* cbq_router_topk into the handle's staging buffers, then cbq_moe_matvec with
  * those ids and weights: the routed layer from router logits with no host
  * round trip (one launch more than cbq_moe_matvec).  Same limits as both. */

@@ -50,6 +50,7 @@ _SIGS = {
     "cbq_moe_matvec": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
     "cbq_moe_matvec_host": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
     "cbq_router_topk": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "cbq_quantize_weights": ([_P, _I64, _I64, _P, _P], _I),
     "cbq_moe_matvec_logits": ([_P, _P, _I, _P, _I, _I, _P, _P], _I),
     "cbq_weights_get_error": ([_P, _P, ctypes.POINTER(ctypes.c_uint)], _I),
     "cbq_moe_get_error": ([_P, _P, ctypes.POINTER(ctypes.c_uint)], _I),
@@ -430,3 +431,17 @@ def cbq_moe_debug_intermediate(L: Moe, nslots: int, stream=None):
                                              _dev_ptr(qa, torch.int8, "qa"), _dev_ptr(da, torch.float32, "da"),
                                              _stream(stream)), "cbq_moe_debug_intermediate")
     return a, qa, da
+
+
+def cbq_quantize_weights(w, out=None, stream=None):
+    """Canonical blocks (M, K/32, 18) uint8 of the fp32 matrix w (M, K), both
+    on the device (the weight converter)."""
+    torch = _torch()
+    M, K = w.shape
+    if out is None:
+        out = torch.empty((M, K // CBQ_QK, CBQ_BLOCK_BYTES), dtype=torch.uint8, device=w.device)
+    if not out.is_contiguous() or out.dtype != torch.uint8 or out.numel() != M * (K // CBQ_QK) * CBQ_BLOCK_BYTES:
+        raise ValueError("out must be a contiguous uint8 tensor of M x K/32 x 18 bytes")
+    _check(load().cbq_quantize_weights(_dev_ptr(w, torch.float32, "w"), M, K, ctypes.c_void_p(out.data_ptr()),
+                                       _stream(stream)), "cbq_quantize_weights")
+    return out

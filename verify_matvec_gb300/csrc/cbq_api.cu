@@ -524,6 +524,18 @@ int cbq_router_topk(const float *logits_dev, int n_tok, int E, int topk, int32_t
     return CBQ_OK;
 }
 
+int cbq_quantize_weights(const float *w_dev, int64_t M, int64_t K, void *blocks_dev, void *stream) {
+    if (!w_dev || !blocks_dev || M < 1 || K < CBQ_QK || K % CBQ_QK || !aligned16(w_dev) ||
+        (reinterpret_cast<uintptr_t>(blocks_dev) & 1u) || M > INT64_MAX / K)
+        return CBQ_EINVAL;
+    int dev = 0;
+    const int rc = check_device(&dev);
+    if (rc != CBQ_OK) return rc;
+    CBQ_CUDA(cbq::launch_quantize_weights(w_dev, M * (K / CBQ_QK), static_cast<uint8_t *>(blocks_dev),
+                                          as_stream(stream)));
+    return CBQ_OK;
+}
+
 int cbq_moe_matvec_logits(const cbq_moe *L, const float *h_dev, int n_tok, const float *logits_dev, int topk,
                           int swiglu, float *y_dev, void *stream) {
     if (!L || !h_dev || !logits_dev || !y_dev || n_tok < 1 || n_tok > CBQ_MAX_TOKENS || topk < 1 ||

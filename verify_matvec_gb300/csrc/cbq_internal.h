@@ -126,6 +126,10 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
 size_t matvec_smem_bytes(int nbp, int n);
 cudaError_t device_smem_limit(size_t *bytes);
 cudaError_t matvec_smem_limit(size_t *bytes);
+// Bytes of one block of the canonical format (2-byte fp16 scale, 16 index bytes).
+constexpr int kBlockBytesCanonical = 18;
+// fp32 weights (16-byte aligned) to nblocks canonical blocks at out (2-byte aligned).
+cudaError_t launch_quantize_weights(const float *w, int64_t nblocks, uint8_t *out, cudaStream_t s);
 // Top-k expert ids and softmax weights per token from router logits (n_tok x E).
 cudaError_t launch_router_topk(const float *logits, int n_tok, int E, int k, int32_t *ids, float *wts,
                                cudaStream_t s);

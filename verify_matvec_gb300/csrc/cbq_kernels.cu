@@ -1189,6 +1189,106 @@ cudaError_t launch_moe(const DevMoe &L, const MoeWork &ws, const float *h, int n
     return e;
 }
 
+// --------------------------------------------------- weight converter ----
+
+// The codebook levels (a constant of the format), ascending with the index,
+// and the half-sums of neighbours, (L_j + L_{j+1}) / 2: the boundaries of the
+// nearest-level cells in units of the scale.
+constexpr int8_t kLevels[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
+struct HalfSums {
+    float h[15];
+    constexpr HalfSums() : h() {
+        for (int j = 0; j < 15; ++j) h[j] = 0.5f * (float)(kLevels[j] + kLevels[j + 1]);
+    }
+};
+__constant__ HalfSums kHalf = HalfSums();
+
+// Nearest level of w for scale dw: the reconstructions dw*L_j are monotone in
+// j, so the nearest one is found by counting the cell boundaries
+// |dw|*(L_j+L_{j+1})/2 that lie strictly below sign(dw)*w -- on a boundary
+// (equal distances) that gives the lower index.  Every boundary is exact in
+// fp32 (an 11-bit scale times a half-integer of at most 8 bits), so the
+// comparisons decide exactly.  dw == 0: every level reconstructs 0, index 0.
+__device__ __forceinline__ unsigned nearest_level(float w, float dw) {
+    const float adw = fabsf(dw), s = dw > 0.0f ? w : -w;
+    unsigned n = 0;
+#pragma unroll
+    for (int j = 0; j < 15; ++j) n += __fmul_rn(adw, kHalf.h[j]) < s ? 1u : 0u;
+    return dw == 0.0f ? 0u : n;
+}
+
+// fp32 weights to 18-byte codebook blocks, for nblocks consecutive blocks of
+// 32 weights (a row-major M x K matrix is M*K/32 of them, in order).  Per
+// block: m = the weight of largest magnitude (the first among equal ones),
+// dw = binary16(m / -127) (IEEE fp32 division, then rounding to nearest
+// even), index_i = the nearest level of w_i; an all-zero block gives zero
+// bytes.  A warp converts four blocks per step: lane l holds elements 4l..4l+3
+// of the 128 (one 16-byte load), eight lanes per block.  Two steps are loaded
+// before either is converted.
+__global__ void __launch_bounds__(256) k_quantize_weights(const float4 *__restrict__ w, int64_t nblocks,
+                                                          uint8_t *__restrict__ out) {
+    constexpr unsigned kFull = 0xffffffffu;
+    const int lane = threadIdx.x & 31, gl = lane & 7;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t steps = (nblocks + 3) / 4;
+    auto convert = [&](int64_t st, float4 v) {
+        const int64_t blk = st * 4 + (lane >> 3);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+        float best = x[0];
+        int pos = 4 * gl;
+#pragma unroll
+        for (int k = 1; k < 4; ++k)
+            if (fabsf(x[k]) > fabsf(best)) {
+                best = x[k];
+                pos = 4 * gl + k;
+            }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const float ob = __shfl_xor_sync(kFull, best, o);
+            const int op = __shfl_xor_sync(kFull, pos, o);
+            if (fabsf(ob) > fabsf(best) || (fabsf(ob) == fabsf(best) && op < pos)) {
+                best = ob;
+                pos = op;
+            }
+        }
+        const unsigned short hb = best == 0.0f ? (unsigned short)0 : __half_as_ushort(__float2half_rn(best / -127.0f));
+        const float dw = __half2float(__ushort_as_half(hb));
+        const unsigned mine = nearest_level(x[0], dw) | nearest_level(x[1], dw) << 8 |
+                              nearest_level(x[2], dw) << 16 | nearest_level(x[3], dw) << 24;
+        const unsigned high = __shfl_down_sync(kFull, mine, 4);  // elements 16 + 4gl.. of the block
+        if (blk < nblocks && gl < 4) {
+            const unsigned word = mine | high << 4;
+            uint8_t *o = out + blk * kBlockBytesCanonical;
+            unsigned short *o16 = reinterpret_cast<unsigned short *>(o + 2 + 4 * gl);  // 2-byte aligned
+            o16[0] = (unsigned short)(word & 0xFFFFu);
+            o16[1] = (unsigned short)(word >> 16);
+            if (gl == 0) *reinterpret_cast<unsigned short *>(o) = hb;
+        }
+    };
+    for (int64_t st = warp; st < steps; st += 2 * warps) {
+        const int64_t st2 = st + warps;
+        const int64_t e0 = st * 32 + lane, e1 = st2 * 32 + lane;  // float4 index: block*8 + gl
+        const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        const float4 v0 = e0 < nblocks * 8 ? __ldcs(w + e0) : z;
+        const float4 v1 = st2 < steps && e1 < nblocks * 8 ? __ldcs(w + e1) : z;
+        convert(st, v0);
+        if (st2 < steps) convert(st2, v1);
+    }
+}
+
+cudaError_t launch_quantize_weights(const float *w, int64_t nblocks, uint8_t *out, cudaStream_t s) {
+    if (nblocks <= 0) return cudaSuccess;
+    int sms = 0, per_sm = 0;
+    cudaError_t e = resident(k_quantize_weights, 256, 0, &sms, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t steps = (nblocks + 3) / 4;
+    const int64_t want = (steps + 15) / 16;  // two steps per warp per round, eight warps per CTA
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * std::max(per_sm, 1)));
+    k_quantize_weights<<<grid, 256, 0, s>>>(reinterpret_cast<const float4 *>(w), nblocks, out);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------ router top-k ------
 
 // Routed-expert selection, one warp per token: the logits are staged in
