@@ -1,6 +1,6 @@
 """The weight converter (cbq_quantize_weights) on the GPU against the oracle's
 converter, byte for byte: random matrices of several shapes (a block count
-that is not a multiple of the four blocks a warp takes per step included),
+that is not a multiple of the eight blocks a warp takes per step included),
 blocks built to hit every decision edge (weights on the codebook grid,
 weights exactly between two levels, equal largest magnitudes of either
 sign, all-zero blocks, scales that round to zero or to a binary16
@@ -64,8 +64,8 @@ def test_decision_edges_bit_exact(torch):
     w = _edge_blocks()
     M = w.shape[0]
     np.testing.assert_array_equal(_convert(torch, w), O.quantize_weights(w, M, 32))
-    # the same blocks laid along K, in every position of a warp's four-block step
-    for shift in range(4):
+    # the same blocks laid along K, in every position of a warp's eight-block step
+    for shift in range(8):
         wk = np.concatenate([np.zeros((1, 32 * shift), np.float32), w.reshape(1, -1)], axis=1)
         np.testing.assert_array_equal(_convert(torch, wk), O.quantize_weights(wk, 1, wk.shape[1]))
 

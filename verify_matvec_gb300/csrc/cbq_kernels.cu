@@ -1204,17 +1204,43 @@ struct HalfSums {
 __constant__ HalfSums kHalf = HalfSums();
 
 // Nearest level of w for scale dw: the reconstructions dw*L_j are monotone in
-// j, so the nearest one is found by counting the cell boundaries
-// |dw|*(L_j+L_{j+1})/2 that lie strictly below sign(dw)*w -- on a boundary
-// (equal distances) that gives the lower index.  Every boundary is exact in
-// fp32 (an 11-bit scale times a half-integer of at most 8 bits), so the
-// comparisons decide exactly.  dw == 0: every level reconstructs 0, index 0.
-__device__ __forceinline__ unsigned nearest_level(float w, float dw) {
+// j, so the nearest one is the number of cell boundaries |dw|*H_j, H_j =
+// (L_j+L_{j+1})/2, that lie strictly below sign(dw)*w -- on a boundary (equal
+// distances) that gives the lower index.  Every boundary is exact in fp32 (an
+// 11-bit scale times a half-integer of at most 8 bits), so comparing with it
+// decides exactly.  A candidate count comes from an approximate scaled value
+// u = 2*s/|dw| and the table cnt[t] = #{j : 2*H_j <= t} at t = ceil(u) - 1
+// (the boundaries are half-integers); the approximation can only misplace s
+// across one boundary (they lie at least 5.5 scale units apart), which the
+// exact comparisons with the candidate's two boundaries (hpair[c]: H_{c-1},
+// H_c, infinite at the ends) put right.  dw == 0: every level reconstructs
+// 0, index 0.
+constexpr int kCntLo = -232, kCntHi = 202;  // t range of the table: below -231 count 0, from 202 on count 15
+struct LevelTables {
+    unsigned char cnt[kCntHi - kCntLo + 1];
+    float2 hpair[16];
+};
+
+__device__ __forceinline__ void level_tables_init(LevelTables &T) {
+    for (int i = threadIdx.x; i < kCntHi - kCntLo + 1; i += blockDim.x) {
+        int n = 0;
+        for (int j = 0; j < 15; ++j) n += (int)(2.0f * kHalf.h[j]) <= i + kCntLo;
+        T.cnt[i] = (unsigned char)n;
+    }
+    if (threadIdx.x < 16) {
+        const int c = threadIdx.x;
+        T.hpair[c] = make_float2(c > 0 ? kHalf.h[c - 1] : -INFINITY, c < 15 ? kHalf.h[c] : INFINITY);
+    }
+}
+
+__device__ __forceinline__ unsigned nearest_level(const LevelTables &T, float w, float dw, float r2) {
     const float adw = fabsf(dw), s = dw > 0.0f ? w : -w;
-    unsigned n = 0;
-#pragma unroll
-    for (int j = 0; j < 15; ++j) n += __fmul_rn(adw, kHalf.h[j]) < s ? 1u : 0u;
-    return dw == 0.0f ? 0u : n;
+    int t = __float2int_ru(s * r2) - 1;
+    t = min(max(t, kCntLo), kCntHi);
+    const int c = T.cnt[t - kCntLo];
+    const float2 hp = T.hpair[c];
+    const int n = c - (__fmul_rn(adw, hp.x) < s ? 0 : 1) + (__fmul_rn(adw, hp.y) < s ? 1 : 0);
+    return dw == 0.0f ? 0u : (unsigned)n;
 }
 
 // fp32 weights to 18-byte codebook blocks, for nblocks consecutive blocks of
@@ -1222,29 +1248,33 @@ __device__ __forceinline__ unsigned nearest_level(float w, float dw) {
 // block: m = the weight of largest magnitude (the first among equal ones),
 // dw = binary16(m / -127) (IEEE fp32 division, then rounding to nearest
 // even), index_i = the nearest level of w_i; an all-zero block gives zero
-// bytes.  A warp converts four blocks per step: lane l holds elements 4l..4l+3
-// of the 128 (one 16-byte load), eight lanes per block.  Two steps are loaded
-// before either is converted.
+// bytes.  A warp converts eight blocks per step: lane l holds elements
+// 8l..8l+7 of the 256 (two 16-byte loads), four lanes per block; lanes 0-1 of
+// a block hold its elements 0-15 (the low nibbles), lanes 2-3 elements 16-31.
+// Two steps are loaded before either is converted.
 __global__ void __launch_bounds__(256) k_quantize_weights(const float4 *__restrict__ w, int64_t nblocks,
                                                           uint8_t *__restrict__ out) {
     constexpr unsigned kFull = 0xffffffffu;
-    const int lane = threadIdx.x & 31, gl = lane & 7;
+    __shared__ LevelTables T;
+    level_tables_init(T);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, gl = lane & 3;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int64_t steps = (nblocks + 3) / 4;
-    auto convert = [&](int64_t st, float4 v) {
-        const int64_t blk = st * 4 + (lane >> 3);
-        const float x[4] = {v.x, v.y, v.z, v.w};
+    const int64_t steps = (nblocks + 7) / 8;
+    auto convert = [&](int64_t st, float4 va, float4 vb) {
+        const int64_t blk = st * 8 + (lane >> 2);
+        const float x[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
         float best = x[0];
-        int pos = 4 * gl;
+        int pos = 8 * gl;
 #pragma unroll
-        for (int k = 1; k < 4; ++k)
+        for (int k = 1; k < 8; ++k)
             if (fabsf(x[k]) > fabsf(best)) {
                 best = x[k];
-                pos = 4 * gl + k;
+                pos = 8 * gl + k;
             }
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
+        for (int o = 1; o < 4; o <<= 1) {
             const float ob = __shfl_xor_sync(kFull, best, o);
             const int op = __shfl_xor_sync(kFull, pos, o);
             if (fabsf(ob) > fabsf(best) || (fabsf(ob) == fabsf(best) && op < pos)) {
@@ -1254,26 +1284,35 @@ __global__ void __launch_bounds__(256) k_quantize_weights(const float4 *__restri
         }
         const unsigned short hb = best == 0.0f ? (unsigned short)0 : __half_as_ushort(__float2half_rn(best / -127.0f));
         const float dw = __half2float(__ushort_as_half(hb));
-        const unsigned mine = nearest_level(x[0], dw) | nearest_level(x[1], dw) << 8 |
-                              nearest_level(x[2], dw) << 16 | nearest_level(x[3], dw) << 24;
-        const unsigned high = __shfl_down_sync(kFull, mine, 4);  // elements 16 + 4gl.. of the block
-        if (blk < nblocks && gl < 4) {
-            const unsigned word = mine | high << 4;
+        const float r2 = __fdividef(2.0f, fabsf(dw));  // approximate: only picks the candidate
+        unsigned mine[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            mine[h] = nearest_level(T, x[4 * h], dw, r2) | nearest_level(T, x[4 * h + 1], dw, r2) << 8 |
+                      nearest_level(T, x[4 * h + 2], dw, r2) << 16 | nearest_level(T, x[4 * h + 3], dw, r2) << 24;
+        const unsigned high0 = __shfl_down_sync(kFull, mine[0], 2);  // elements 16 + 8gl.. of the block
+        const unsigned high1 = __shfl_down_sync(kFull, mine[1], 2);
+        if (blk < nblocks && gl < 2) {
+            const unsigned w0 = mine[0] | high0 << 4, w1 = mine[1] | high1 << 4;
             uint8_t *o = out + blk * kBlockBytesCanonical;
-            unsigned short *o16 = reinterpret_cast<unsigned short *>(o + 2 + 4 * gl);  // 2-byte aligned
-            o16[0] = (unsigned short)(word & 0xFFFFu);
-            o16[1] = (unsigned short)(word >> 16);
+            unsigned short *o16 = reinterpret_cast<unsigned short *>(o + 2 + 8 * gl);  // 2-byte aligned
+            o16[0] = (unsigned short)(w0 & 0xFFFFu);
+            o16[1] = (unsigned short)(w0 >> 16);
+            o16[2] = (unsigned short)(w1 & 0xFFFFu);
+            o16[3] = (unsigned short)(w1 >> 16);
             if (gl == 0) *reinterpret_cast<unsigned short *>(o) = hb;
         }
     };
+    const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const int64_t n4 = nblocks * 8;  // float4s in all
     for (int64_t st = warp; st < steps; st += 2 * warps) {
         const int64_t st2 = st + warps;
-        const int64_t e0 = st * 32 + lane, e1 = st2 * 32 + lane;  // float4 index: block*8 + gl
-        const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        const float4 v0 = e0 < nblocks * 8 ? __ldcs(w + e0) : z;
-        const float4 v1 = st2 < steps && e1 < nblocks * 8 ? __ldcs(w + e1) : z;
-        convert(st, v0);
-        if (st2 < steps) convert(st2, v1);
+        const int64_t e0 = st * 64 + 2 * lane, e1 = st2 * 64 + 2 * lane;  // block*8 + 2*gl
+        const float4 a0 = e0 < n4 ? __ldg(w + e0) : z, b0 = e0 < n4 ? __ldg(w + e0 + 1) : z;
+        const bool two = st2 < steps;
+        const float4 a1 = two && e1 < n4 ? __ldg(w + e1) : z, b1 = two && e1 < n4 ? __ldg(w + e1 + 1) : z;
+        convert(st, a0, b0);
+        if (two) convert(st2, a1, b1);
     }
 }
 
@@ -1282,7 +1321,7 @@ cudaError_t launch_quantize_weights(const float *w, int64_t nblocks, uint8_t *ou
     int sms = 0, per_sm = 0;
     cudaError_t e = resident(k_quantize_weights, 256, 0, &sms, &per_sm);
     if (e != cudaSuccess) return e;
-    const int64_t steps = (nblocks + 3) / 4;
+    const int64_t steps = (nblocks + 7) / 8;
     const int64_t want = (steps + 15) / 16;  // two steps per warp per round, eight warps per CTA
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * std::max(per_sm, 1)));
     k_quantize_weights<<<grid, 256, 0, s>>>(reinterpret_cast<const float4 *>(w), nblocks, out);
