@@ -263,6 +263,33 @@ int cbq_moe_matvec_host(const cbq_moe *L, const float *h_host, int n_tok,
  * stay owned by the caller. */
 int cbq_moe_set_stage_events(cbq_moe *L, void *ev_start, void *ev_layer, void *ev_end);
 
+/* ---- tensor-core path for larger batches ------------------------------ */
+
+/* Most columns of cbq_matmat. */
+#define CBQ_MAX_MMQ_COLS 16
+
+/* The dense product for 1 <= n <= CBQ_MAX_MMQ_COLS columns on the tensor
+ * cores (tcgen05): the MMQ tile the pages name for larger batches ("#497
+ * RDNA MMQ tile, LUCE_MMQ_DP_MAX_NE1", "fix(ds4): correct layer-split HC
+ * handoff and per-device state" #507), read for this format.  Same result
+ * definition as cbq_matvec (the activation quantization, exact per-block
+ * integer dots, y = sum_b dw*dx*s in fp32 with the same three roundings per
+ * block), blocks summed in ascending order: every block dot is exact, so y is
+ * within the same bound of the plain definition.  A level enters the MMA as
+ * the fp16 value 1152 + level, an int8 activation as fp16; each 32-wide block
+ * sum is an integer below 2^24 (exact in the fp32 accumulator), and the bias
+ * 1152 * sum q is subtracted exactly.  Arguments as cbq_matvec (x_dev n x K
+ * fp32, y_dev n x M fp32, both owned by the caller).  Three launches on
+ * `stream`: the quantization, the B tiles, the tiles of W.  One call at a
+ * time per handle (its workspace is shared by the calls). */
+int cbq_matmat(const cbq_weights *W, const float *x_dev, int n, float *y_dev, void *stream);
+
+/* Checking: the exact block dots s[c][r][b] (n x M x K/32 int32) of W's
+ * blocks with the int8 columns qx_dev (n x K), taken by the tensor-core path
+ * (cbq_debug_block_dots takes them by the dp4a path).  1 <= n <=
+ * CBQ_MAX_MMQ_COLS. */
+int cbq_debug_mmq_block_dots(const cbq_weights *W, const int8_t *qx_dev, int n, int32_t *s_dev, void *stream);
+
 /* ---- allocation-free dense path --------------------------------------- */
 
 /* Largest K cbq_matvec_static accepts (its scratch holds CBQ_MAX_COLS columns

@@ -63,6 +63,8 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.cbq_router_topk(dummy, 1, cbq.CBQ_ROUTER_MAX_E + 1, 2, dummy, dummy, None) == EINVAL
     assert lib.cbq_router_topk(dummy, 0, 8, 2, dummy, dummy, None) == EINVAL                      # no token
     assert lib.cbq_moe_matvec_logits(None, dummy, 1, dummy, 2, 1, dummy, None) == EINVAL
+    assert lib.cbq_matmat(None, dummy, 8, dummy, None) == EINVAL
+    assert lib.cbq_debug_mmq_block_dots(None, dummy, 8, dummy, None) == EINVAL
     aligned = ctypes.c_void_p(0x1000)
     assert lib.cbq_quantize_weights(None, 4, 64, aligned, None) == EINVAL                      # no weights
     assert lib.cbq_quantize_weights(aligned, 4, 64, None, None) == EINVAL                      # no output

@@ -28,6 +28,7 @@ CBQ_DEVERR_PIPE_TIMEOUT = 0x100
 CBQ_DEVERR_DEPENDENCY_TIMEOUT = 0x200
 CBQ_STATIC_SCRATCH_MAX_K = 16384
 CBQ_ROUTER_MAX_E = 16384
+CBQ_MAX_MMQ_COLS = 16
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -51,6 +52,8 @@ _SIGS = {
     "cbq_moe_matvec_host": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
     "cbq_router_topk": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "cbq_quantize_weights": ([_P, _I64, _I64, _P, _P], _I),
+    "cbq_matmat": ([_P, _P, _I, _P, _P], _I),
+    "cbq_debug_mmq_block_dots": ([_P, _P, _I, _P, _P], _I),
     "cbq_moe_matvec_logits": ([_P, _P, _I, _P, _I, _I, _P, _P], _I),
     "cbq_weights_get_error": ([_P, _P, ctypes.POINTER(ctypes.c_uint)], _I),
     "cbq_moe_get_error": ([_P, _P, ctypes.POINTER(ctypes.c_uint)], _I),
@@ -445,3 +448,25 @@ def cbq_quantize_weights(w, out=None, stream=None):
     _check(load().cbq_quantize_weights(_dev_ptr(w, torch.float32, "w"), M, K, ctypes.c_void_p(out.data_ptr()),
                                        _stream(stream)), "cbq_quantize_weights")
     return out
+
+
+def cbq_matmat(W: Weights, x, y=None, stream=None):
+    """y (n, M) fp32 = W applied to the n <= 16 fp32 columns x (n, K), by the
+    tensor-core path; x and y on the device."""
+    torch = _torch()
+    n = x.shape[0]
+    if y is None:
+        y = torch.empty((n, W.M), dtype=torch.float32, device=x.device)
+    _check(load().cbq_matmat(W.handle, _dev_ptr(x, torch.float32, "x"), n, _dev_ptr(y, torch.float32, "y"),
+                             _stream(stream)), "cbq_matmat")
+    return y
+
+
+def cbq_debug_mmq_block_dots(W: Weights, qx, stream=None):
+    """The exact block dots (n, M, K/32) int32 of W with int8 columns qx (n, K), by the tensor-core path."""
+    torch = _torch()
+    n = qx.shape[0]
+    s = torch.empty((n, W.M, W.K // CBQ_QK), dtype=torch.int32, device=qx.device)
+    _check(load().cbq_debug_mmq_block_dots(W.handle, _dev_ptr(qx, torch.int8, "qx"), n,
+                                           _dev_ptr(s, torch.int32, "s"), _stream(stream)), "cbq_debug_mmq_block_dots")
+    return s

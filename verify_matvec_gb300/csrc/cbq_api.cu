@@ -28,6 +28,10 @@ struct cbq_weights {
     float *ws_dx;    // CBQ_MAX_COLS x K/32
     float *st_x;     // host-entry staging: CBQ_MAX_COLS x K fp32
     float *st_y;     // CBQ_MAX_COLS x M fp32
+    int8_t *mq_qx;   // tensor-core path: CBQ_MAX_MMQ_COLS x K
+    float *mq_dx;    // CBQ_MAX_MMQ_COLS x K/32
+    uint8_t *mq_b;   // its B tiles (1 KB per block)
+    float *mq_meta;  // its block metadata
     int64_t K;
     int64_t bytes;
 };
@@ -171,6 +175,10 @@ int cbq_weights_destroy(cbq_weights *W) {
     cudaFree(W->ws_dx);
     cudaFree(W->st_x);
     cudaFree(W->st_y);
+    cudaFree(W->mq_qx);
+    cudaFree(W->mq_dx);
+    cudaFree(W->mq_b);
+    cudaFree(W->mq_meta);
     delete W;
     return CBQ_OK;
 }
@@ -202,7 +210,11 @@ int cbq_weights_create(const void *blocks, int64_t M, int64_t K, int on_device, 
         (rc = dev_alloc(&W->ws_qx, (size_t)CBQ_MAX_COLS * K, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->ws_dx, (size_t)CBQ_MAX_COLS * nb, &W->bytes)) != CBQ_OK ||
         (rc = dev_alloc(&W->st_x, (size_t)CBQ_MAX_COLS * K, &W->bytes)) != CBQ_OK ||
-        (rc = dev_alloc(&W->st_y, (size_t)CBQ_MAX_COLS * M, &W->bytes)) != CBQ_OK) {
+        (rc = dev_alloc(&W->st_y, (size_t)CBQ_MAX_COLS * M, &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->mq_qx, (size_t)CBQ_MAX_MMQ_COLS * K, &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->mq_dx, (size_t)CBQ_MAX_MMQ_COLS * nb, &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->mq_b, cbq::mmq_bimg_bytes(nb), &W->bytes)) != CBQ_OK ||
+        (rc = dev_alloc(&W->mq_meta, cbq::mmq_meta_bytes(nb) / sizeof(float), &W->bytes)) != CBQ_OK) {
         cbq_weights_destroy(W);
         return rc;
     }
@@ -328,6 +340,27 @@ int cbq_matvec_static(const cbq_weights *W, const float *x_dev, int n, float *y_
     }
     CBQ_CUDA(cbq::launch_quantize(x_dev, W->K, n, qx, dx, s));
     CBQ_CUDA(cbq::launch_matvec(W->mat, qx, dx, n, y_dev, s, /*pdl=*/true));
+    return CBQ_OK;
+}
+
+int cbq_matmat(const cbq_weights *W, const float *x_dev, int n, float *y_dev, void *stream) {
+    if (!W || !x_dev || !y_dev || n < 1 || n > CBQ_MAX_MMQ_COLS) return CBQ_EINVAL;
+    DeviceScope scope(W->device);
+    CBQ_CUDA(scope.status());
+    cudaStream_t s = as_stream(stream);
+    CBQ_CUDA(cbq::launch_quantize(x_dev, W->K, n, W->mq_qx, W->mq_dx, s));
+    CBQ_CUDA(cbq::launch_mmq_prep(W->mq_qx, W->mq_dx, n, W->K, W->mq_b, W->mq_meta, s));
+    CBQ_CUDA(cbq::launch_mmq(W->mat, W->mq_b, W->mq_meta, n, y_dev, nullptr, s));
+    return CBQ_OK;
+}
+
+int cbq_debug_mmq_block_dots(const cbq_weights *W, const int8_t *qx_dev, int n, int32_t *s_dev, void *stream) {
+    if (!W || !qx_dev || !s_dev || n < 1 || n > CBQ_MAX_MMQ_COLS) return CBQ_EINVAL;
+    DeviceScope scope(W->device);
+    CBQ_CUDA(scope.status());
+    cudaStream_t s = as_stream(stream);
+    CBQ_CUDA(cbq::launch_mmq_prep(qx_dev, nullptr, n, W->K, W->mq_b, W->mq_meta, s));
+    CBQ_CUDA(cbq::launch_mmq(W->mat, W->mq_b, W->mq_meta, n, nullptr, s_dev, s));
     return CBQ_OK;
 }
 

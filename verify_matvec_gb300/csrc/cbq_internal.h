@@ -130,6 +130,17 @@ cudaError_t matvec_smem_limit(size_t *bytes);
 constexpr int kBlockBytesCanonical = 18;
 // fp32 weights (16-byte aligned) to nblocks canonical blocks at out (2-byte aligned).
 cudaError_t launch_quantize_weights(const float *w, int64_t nblocks, uint8_t *out, cudaStream_t s);
+// The tensor-core (tcgen05) path for up to kMaxMmqCols columns: the B tiles
+// and block metadata from quantized columns (qx[c][K], dx[c][K/32]; dx null
+// gives zero scales), then the tiles of W; dbg, when not null, receives the
+// exact block dots s[c][row][b].
+constexpr int kMaxMmqCols = 16;
+size_t mmq_bimg_bytes(int nb);
+size_t mmq_meta_bytes(int nb);
+cudaError_t launch_mmq_prep(const int8_t *qx, const float *dx, int n, int64_t K, uint8_t *bimg, float *meta,
+                            cudaStream_t s);
+cudaError_t launch_mmq(const DevMat &W, const uint8_t *bimg, const float *meta, int n, float *y, int32_t *dbg,
+                       cudaStream_t s);
 // Top-k expert ids and softmax weights per token from router logits (n_tok x E).
 cudaError_t launch_router_topk(const float *logits, int n_tok, int E, int k, int32_t *ids, float *wts,
                                cudaStream_t s);
