@@ -37,22 +37,15 @@ namespace cbq {
 
 constexpr int kMmqN = 16;                    // MMA N: activation columns (zero-padded)
 constexpr int kMmqM = 128;                   // MMA M: weight rows of a tile
-constexpr int kMmqChunk = 4;                 // blocks per batch of MMAs
 constexpr int kMmqATile = kMmqM * 32 * 2;    // 8 KB: the fp16 A tile of one block
 constexpr int kMmqBTile = kMmqN * 32 * 2;    // 1 KB: the fp16 B tile of one block
 constexpr int kMmqMetaFloats = 2 * kMmqN;    // per block: dx[16], then 1152 * sum q [16]
 constexpr float kMmqBias = 1152.0f;
-constexpr uint32_t kMmqTmemCols = 2 * kMmqChunk * kMmqN;  // 128: D of two chunks
-constexpr int kMmqThreads = 128;
 
 // Byte offset of element (row, k) in a tile of the core-matrix layout.
 __host__ __device__ inline uint32_t mmq_core_off(int row, int k) {
     return (uint32_t)(((row >> 3) * 4 + (k >> 3)) * 128 + (row & 7) * 16 + (k & 7) * 2);
 }
-
-// Dynamic shared memory of k_mmq: A and B tiles of two chunks, block
-// metadata of three.
-constexpr size_t kMmqSmem = 2 * kMmqChunk * (kMmqATile + kMmqBTile) + 3 * kMmqChunk * kMmqMetaFloats * 4;
 
 // --------------------------------------------------------------- tcgen05 --
 
@@ -94,6 +87,18 @@ __device__ __forceinline__ void mmq_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane, as raw
+// words; complete once tmem_wait_ld() returns.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 16 consecutive fp32 columns of this thread's tensor-memory lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -148,18 +153,6 @@ struct MmqArgs {
 
 constexpr unsigned kErrMmqTimeout = 0x100u;  // the pipeline's timeout bit: an MMA batch never completed
 
-__device__ __forceinline__ bool mmq_wait(uint32_t bar, uint32_t parity, unsigned *err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) {
-            atomicOr(err, kErrMmqTimeout);
-            return false;
-        }
-    }
-    return true;
-}
-
 // The 8 fp16 weights 4m..4m+3 (lo) and 4m+16..4m+19 (hi) of index word m,
 // from its expanded biased level bytes e0 (elements 4m, 4m+16, 4m+1, 4m+17)
 // and e1 (4m+2, 4m+18, 4m+3, 4m+19): each pair's bytes next to 0x64.
@@ -171,157 +164,328 @@ __device__ __forceinline__ void mmq_halves(uint32_t e0, uint32_t e1, uint32_t (&
     hi[1] = prmt(e1, k64, 0x4341u);
 }
 
-// One CTA (128 threads, thread = row of a 128-row tile: pair 2t + tid/64,
-// group (tid/32)%2, lane tid%32) per tile at a time, tiles strided over the
-// grid.  Per chunk of four blocks: every thread expands its row into the A
-// tiles and copies its share of the B tiles and block metadata; after a CTA
-// barrier thread 0 issues the chunk's MMAs (two per block, into 16 tensor-
-// memory columns each) and commits them to the chunk's mbarrier; meanwhile
-// the threads read the previous chunk's sums from tensor memory (warp w owns
-// lanes 32w..32w+31) and scale them into their row's n running sums.  A and B
-// tiles and the two chunks' sums are double-buffered, the metadata (read by
-// the threads themselves) triple-buffered.  The index words and scales of
-// the next chunk are loaded one chunk ahead.
-__global__ void __launch_bounds__(kMmqThreads) k_mmq(const __grid_constant__ MmqArgs A) {
+// Warp-specialised tiles, one CTA per SM (its tensor-memory ring takes half
+// of the SM's 512 columns), tiles strided over the grid; every role walks the
+// same sequence (tile, stage of 16 blocks, unit of up to 4 blocks, block):
+//   warp 12, the producer: per stage, bulk copies of the tile's two pairs'
+//     weight chunk, the 16 B tiles and their metadata into a ring of stages;
+//   warps 4-11, the expanders: thread (row, parity) expands the row's blocks
+//     of that parity into a ring of A units (four block tiles each);
+//   warp 13, the MMA issuer: per unit, two MMAs per block from the A tiles and
+//     the stage's B tiles into a ring of units of sums in tensor memory (16
+//     columns per block), then commits that free the A unit and publish the
+//     sums (and, after a stage's last unit, free the stage's B tiles);
+//   warps 0-3, the epilogue: thread = row (warp w reads tensor-memory lanes
+//     32w..32w+31); per unit it reads the sums, frees their slot and scales
+//     them into the row's n running sums; y at the end of a tile.
+// Synchronising per unit rather than per block keeps the barrier and commit
+// traffic of the single MMA thread and of the epilogue to a quarter.
+// Every wait is bounded (kWaitLimitNs): a give-up sets kErrMmqTimeout and a
+// CTA-wide abort flag, after which every role leaves its loop; the producer
+// then waits (bounded) for its copies in flight and the MMA issuer for its
+// MMAs before the CTA frees its tensor memory.
+constexpr int kM2Stages = 2;
+constexpr int kM2Unit = 4;                               // blocks per unit
+constexpr int kM2AUnits = 3;                             // A ring (units)
+constexpr int kM2DUnits = 4;                             // tensor-memory ring (units)
+constexpr int kM2WBytes = kChunkBytes;                  // one pair's weight chunk (at most)
+constexpr int kM2BOff = 2 * kM2WBytes;                  // B tiles of the stage's blocks
+constexpr int kM2MetaOff = kM2BOff + kChunk * kMmqBTile; // their metadata
+constexpr int kM2StageBytes = kM2MetaOff + kChunk * kMmqMetaFloats * 4;  // 55,296
+constexpr int kM2EpWarps = 8, kM2ExWarps = 4;  // multiples of 4 (one warp per tensor-memory lane quadrant)
+constexpr int kM2EpGroups = kM2EpWarps / 4;     // epilogue groups: group g reads the units u with u % groups == g
+constexpr int kM2ExGroups = kM2ExWarps / 4;     // expander groups: group g expands blocks i == g (mod groups) of a unit
+constexpr int kM2EpBatch = 2;  // blocks whose sums the epilogue loads before one wait
+constexpr int kM2ProducerWarp = kM2EpWarps + kM2ExWarps, kM2MmaWarp = kM2ProducerWarp + 1;
+constexpr int kM2Threads = (kM2MmaWarp + 1) * 32;      // 448
+constexpr int kM2StageArrivals = kM2ExWarps * 32 + kM2EpWarps * 32 + 1;
+constexpr uint32_t kM2TmemCols = kM2DUnits * kM2Unit * kMmqN;  // 256
+constexpr size_t kM2AUnitBytes = (size_t)kM2Unit * kMmqATile;  // 32 KB
+constexpr size_t kM2PartBytes = (size_t)(kM2EpGroups - 1) * kMmqM * kMmqN * 4;  // partial sums of groups 1..
+constexpr size_t kM2Smem = (size_t)kM2Stages * kM2StageBytes + (size_t)kM2AUnits * kM2AUnitBytes + kM2PartBytes;
+
+struct M2Shared {
+    uint64_t sfull[kM2Stages], sempty[kM2Stages];
+    uint64_t afull[kM2AUnits], aempty[kM2AUnits];
+    uint64_t dfull[kM2DUnits], dempty[kM2DUnits];
+    uint64_t done;  // the MMA issuer's last commit
+    uint32_t tmem_slot;
+    uint32_t cbw[4];
+    int abort;
+};
+
+__device__ __forceinline__ bool m2_wait(M2Shared &S, uint64_t &bar, uint32_t parity, unsigned *err) {
+    const uint32_t b = smem_addr(&bar);
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (*(volatile int *)&S.abort) return false;
+        if (mbar_try_wait(b, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) break;
+    }
+    atomicOr(err, kErrMmqTimeout);
+    *(volatile int *)&S.abort = 1;
+    return false;
+}
+
+__global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ MmqArgs A) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ uint32_t tmem_slot;
-    __shared__ __align__(8) uint64_t bars[2];
-    __shared__ uint32_t cbw[4];
-    unsigned char *sA = smem;                                           // [2][4] A tiles
-    unsigned char *sB = sA + 2 * kMmqChunk * kMmqATile;                 // [2][4] B tiles
-    float *sMeta = reinterpret_cast<float *>(sB + 2 * kMmqChunk * kMmqBTile);  // [3][4][32]
+    __shared__ M2Shared S;
+    unsigned char *stages = smem;
+    unsigned char *aunits = smem + (size_t)kM2Stages * kM2StageBytes;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const DevMat &W = A.W;
-    if (warp == 0) tmem_alloc(smem_addr(&tmem_slot), kMmqTmemCols);
-    if (tid == 0) {
-        mbar_init(smem_addr(&bars[0]), 1);
-        mbar_init(smem_addr(&bars[1]), 1);
+    unsigned *err = W.err;
+    if (warp == 0) tmem_alloc(smem_addr(&S.tmem_slot), kM2TmemCols);
+    if (tid == 32) {
+        for (int i = 0; i < kM2Stages; ++i) {
+            mbar_init(smem_addr(&S.sfull[i]), 1);
+            mbar_init(smem_addr(&S.sempty[i]), kM2StageArrivals);
+        }
+        for (int i = 0; i < kM2AUnits; ++i) {
+            mbar_init(smem_addr(&S.afull[i]), kM2ExWarps * 32);
+            mbar_init(smem_addr(&S.aempty[i]), 1);
+        }
+        for (int i = 0; i < kM2DUnits; ++i) {
+            mbar_init(smem_addr(&S.dfull[i]), 1);
+            mbar_init(smem_addr(&S.dempty[i]), kMmqM);
+        }
+        mbar_init(smem_addr(&S.done), 1);
+        S.abort = 0;
+        S.cbw[0] = kCb0 ^ 0x80808080u;  // the codebook words, every level biased by 128
+        S.cbw[1] = kCb1 ^ 0x80808080u;
+        S.cbw[2] = kCb2 ^ 0x80808080u;
+        S.cbw[3] = kCb3 ^ 0x80808080u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        // the codebook words with every level biased by 128 (level XOR 0x80)
-        cbw[0] = kCb0 ^ 0x80808080u;
-        cbw[1] = kCb1 ^ 0x80808080u;
-        cbw[2] = kCb2 ^ 0x80808080u;
-        cbw[3] = kCb3 ^ 0x80808080u;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     pdl_wait();
     pdl_trigger();
-    const uint32_t tmem = tmem_slot;
-    const Codebook cb{cbw[0], cbw[1], cbw[2], cbw[3], 0u, 0u, 0};
+    const uint32_t tmem = S.tmem_slot;
     const int nb = W.nb, nbp = W.nbp, n = A.n;
-    const int T = (W.P + 1) / 2, nch = (nb + kMmqChunk - 1) / kMmqChunk;
+    const int T = (W.P + 1) / 2, nch = (nb + kChunk - 1) / kChunk;
     const size_t pb = pair_bytes(nbp);
-    const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB);
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    uint32_t phases = 0u;  // bit i: the phase of bars[i] to wait for next
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        const int pair = 2 * t + (tid >> 6), h = (tid >> 5) & 1;
-        const bool live = pair < W.P;
-        const uint8_t *wp = W.w + (size_t)(live ? pair : 0) * pb;
-        const int64_t row = (int64_t)pair * 64 + h * 32 + lane;
-        float acc[kMmqN];
-#pragma unroll
-        for (int c = 0; c < kMmqN; ++c) acc[c] = 0.0f;
-        uint4 q[kMmqChunk];
-        uint2 sc = make_uint2(0u, 0u), sc_rd = sc, sc_keep = sc;  // scales: fetched chunk, chunk read out, chunk issued
-        auto fetch = [&](int ch) {
-#pragma unroll
-            for (int j = 0; j < kMmqChunk; ++j) {
-                const int b = ch * kMmqChunk + j;
-                q[j] = live && b < nb ? *reinterpret_cast<const uint4 *>(wp + field_offset(nbp, h, b, lane))
-                                      : make_uint4(0u, 0u, 0u, 0u);
-            }
-            sc = live ? *reinterpret_cast<const uint2 *>(wp + scale_offset(nbp, h, ch * kMmqChunk, lane))
-                      : make_uint2(0u, 0u);
-        };
-        if (nch > 0) fetch(0);
-        for (int ch = 0; ch <= nch; ++ch) {
-            const int buf = ch & 1;
-            const int nv = ch < nch ? min(kMmqChunk, nb - ch * kMmqChunk) : 0;
-            if (ch < nch) {
-                // this row of the chunk's A tiles
-#pragma unroll
-                for (int j = 0; j < kMmqChunk; ++j) {
-                    if (j >= nv) break;
-                    const uint32_t ws[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
-                    uint32_t lo[4][2], hi[4][2];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        uint32_t e0, e1;
-                        expand_select(cb, ws[m], e0, e1);
-                        mmq_halves(e0, e1, lo[m], hi[m]);
+
+    if (warp == kM2ProducerWarp) {
+        if (lane == 0) {
+            uint32_t k = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+                const int p0 = 2 * t, p1 = 2 * t + 1;
+                for (int c = 0; c < nch && ok; ++c, ++k) {
+                    const uint32_t slot = k % kM2Stages, use = k / kM2Stages;
+                    if (use > 0 && !m2_wait(S, S.sempty[slot], (use - 1) & 1u, err)) {
+                        ok = false;
+                        break;
                     }
-                    unsigned char *at = sA + (buf * kMmqChunk + j) * kMmqATile;
-                    *reinterpret_cast<uint4 *>(at + mmq_core_off(tid, 0)) = make_uint4(lo[0][0], lo[0][1], lo[1][0], lo[1][1]);
-                    *reinterpret_cast<uint4 *>(at + mmq_core_off(tid, 8)) = make_uint4(lo[2][0], lo[2][1], lo[3][0], lo[3][1]);
-                    *reinterpret_cast<uint4 *>(at + mmq_core_off(tid, 16)) = make_uint4(hi[0][0], hi[0][1], hi[1][0], hi[1][1]);
-                    *reinterpret_cast<uint4 *>(at + mmq_core_off(tid, 24)) = make_uint4(hi[2][0], hi[2][1], hi[3][0], hi[3][1]);
-                }
-                // the chunk's B tiles and metadata
-                const uint4 *gb = reinterpret_cast<const uint4 *>(A.bimg + (size_t)ch * kMmqChunk * kMmqBTile);
-                uint4 *sb = reinterpret_cast<uint4 *>(sB + buf * kMmqChunk * kMmqBTile);
-                for (int i = tid; i < nv * (kMmqBTile / 16); i += kMmqThreads) sb[i] = gb[i];
-                const uint4 *gm = reinterpret_cast<const uint4 *>(A.meta + (size_t)ch * kMmqChunk * kMmqMetaFloats);
-                uint4 *sm = reinterpret_cast<uint4 *>(sMeta + (ch % 3) * kMmqChunk * kMmqMetaFloats);
-                if (tid < nv * (kMmqMetaFloats / 4)) sm[tid] = gm[tid];
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                sc_keep = sc;
-                if (ch + 1 < nch) fetch(ch + 1);
-            }
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-            if (tid == 0 && nv > 0) {
-                for (int j = 0; j < nv; ++j) {
-                    const uint32_t d = tmem + (uint32_t)((buf * kMmqChunk + j) * kMmqN);
-                    const uint32_t at = a0 + (uint32_t)((buf * kMmqChunk + j) * kMmqATile);
-                    const uint32_t bt = b0 + (uint32_t)((buf * kMmqChunk + j) * kMmqBTile);
-                    mmq_mma(d, mmq_desc(at, 128, 512), mmq_desc(bt, 128, 512), 0);
-                    mmq_mma(d, mmq_desc(at + 256, 128, 512), mmq_desc(bt + 256, 128, 512), 1);
-                }
-                mmq_commit(smem_addr(&bars[buf]));
-            }
-            if (ch > 0) {
-                // the previous chunk's sums
-                const int pc = ch - 1, pbuf = pc & 1, pnv = min(kMmqChunk, nb - pc * kMmqChunk);
-                mmq_wait(smem_addr(&bars[pbuf]), (phases >> pbuf) & 1u, W.err);
-                phases ^= 1u << pbuf;
-                tc_fence_after();
-                const float *mt = sMeta + (pc % 3) * kMmqChunk * kMmqMetaFloats;
-#pragma unroll
-                for (int j = 0; j < kMmqChunk; ++j) {
-                    if (j >= pnv) break;
-                    float d[kMmqN];
-                    tmem_ld16(tmem + lane_base + (uint32_t)((pbuf * kMmqChunk + j) * kMmqN), d);
-                    const uint32_t scw = j < 2 ? sc_rd.x : sc_rd.y;
-                    const float dw = (j & 1) ? half_hi(scw) : half_lo(scw);
-                    const float *md = mt + j * kMmqMetaFloats;
-#pragma unroll
-                    for (int c = 0; c < kMmqN; ++c) {
-                        const float s = __fsub_rn(d[c], md[kMmqN + c]);
-                        acc[c] = __fmaf_rn(__fmul_rn(dw, md[c]), s, acc[c]);
-                    }
-                    if (A.dbg && live && row < W.M) {
-                        const int b = pc * kMmqChunk + j;
-#pragma unroll
-                        for (int c = 0; c < kMmqN; ++c)
-                            if (c < n) A.dbg[((size_t)c * W.M + row) * nb + b] = (int32_t)__fsub_rn(d[c], md[kMmqN + c]);
-                    }
+                    const int nblk = chunk_blocks(nbp, c), nv = min(kChunk, nb - c * kChunk);
+                    const uint32_t bw = (uint32_t)nblk * (2 * kBlockBytes);
+                    const uint32_t bytes = bw * (p1 < W.P ? 2u : 1u) + (uint32_t)nv * (kMmqBTile + kMmqMetaFloats * 4);
+                    const uint32_t dst = smem_addr(stages) + slot * kM2StageBytes, bar = smem_addr(&S.sfull[slot]);
+                    mbar_expect_tx(bar, bytes);
+                    bulk_g2s(dst, W.w + (size_t)p0 * pb + (size_t)c * kChunkBytes, bw, bar);
+                    if (p1 < W.P) bulk_g2s(dst + kM2WBytes, W.w + (size_t)p1 * pb + (size_t)c * kChunkBytes, bw, bar);
+                    bulk_g2s(dst + kM2BOff, A.bimg + (size_t)c * kChunk * kMmqBTile, (uint32_t)nv * kMmqBTile, bar);
+                    bulk_g2s(dst + kM2MetaOff, A.meta + (size_t)c * kChunk * kMmqMetaFloats,
+                             (uint32_t)nv * kMmqMetaFloats * 4, bar);
                 }
             }
-            sc_rd = sc_keep;
+            // the copies still in flight land before the CTA may exit
+            const uint32_t first = k > (uint32_t)kM2Stages ? k - kM2Stages : 0u;
+            for (uint32_t q = first; q < k; ++q) {
+                const uint32_t b = smem_addr(&S.sfull[q % kM2Stages]);
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(b, (q / kM2Stages) & 1u) && global_ns() - t0 < kWaitLimitNs) {}
+            }
         }
-        if (A.y && live && row < W.M) {
+    } else if (warp == kM2MmaWarp) {
+        if (lane == 0) {
+            uint32_t k = 0, u = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+                for (int c = 0; c < nch && ok; ++c, ++k) {
+                    const uint32_t slot = k % kM2Stages;
+                    if (!m2_wait(S, S.sfull[slot], (k / kM2Stages) & 1u, err)) {
+                        ok = false;
+                        break;
+                    }
+                    const int nv = min(kChunk, nb - c * kChunk);
+                    const uint32_t bt0 = smem_addr(stages) + slot * kM2StageBytes + kM2BOff;
+                    for (int j0 = 0; j0 < nv; j0 += kM2Unit, ++u) {
+                        const uint32_t as = u % kM2AUnits, ds = u % kM2DUnits, du = u / kM2DUnits;
+                        if (!m2_wait(S, S.afull[as], (u / kM2AUnits) & 1u, err) ||
+                            (du > 0 && !m2_wait(S, S.dempty[ds], (du - 1) & 1u, err))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int nu = min(kM2Unit, nv - j0);
+                        for (int i = 0; i < nu; ++i) {
+                            const uint32_t d = tmem + (ds * kM2Unit + (uint32_t)i) * kMmqN;
+                            const uint32_t at = smem_addr(aunits) + (uint32_t)(as * kM2AUnitBytes) + (uint32_t)i * kMmqATile;
+                            const uint32_t bt = bt0 + (uint32_t)(j0 + i) * kMmqBTile;
+                            mmq_mma(d, mmq_desc(at, 128, 512), mmq_desc(bt, 128, 512), 0);
+                            mmq_mma(d, mmq_desc(at + 256, 128, 512), mmq_desc(bt + 256, 128, 512), 1);
+                        }
+                        mmq_commit(smem_addr(&S.aempty[as]));
+                        mmq_commit(smem_addr(&S.dfull[ds]));
+                    }
+                    if (ok) mmq_commit(smem_addr(&S.sempty[slot]));
+                }
+            }
+            // every MMA issued here is done before the tensor memory is freed
+            mmq_commit(smem_addr(&S.done));
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(smem_addr(&S.done), 0u) && global_ns() - t0 < kWaitLimitNs) {}
+        }
+    } else if (warp >= kM2EpWarps) {
+        // expanders: thread (row, group) -- blocks i == group (mod groups) of a unit
+        const int e = tid - kM2EpWarps * 32, row = e & (kMmqM - 1), par = e >> 7;
+        const int pl = row >> 6, h = (row >> 5) & 1, rl = row & 31;
+        const Codebook cb{S.cbw[0], S.cbw[1], S.cbw[2], S.cbw[3], 0u, 0u, 0};
+        uint32_t k = 0, u = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+            const bool live = 2 * t + pl < W.P;
+            for (int c = 0; c < nch && ok; ++c, ++k) {
+                const uint32_t slot = k % kM2Stages;
+                if (!m2_wait(S, S.sfull[slot], (k / kM2Stages) & 1u, err)) {
+                    ok = false;
+                    break;
+                }
+                const int nblk = chunk_blocks(nbp, c), nv = min(kChunk, nb - c * kChunk);
+                const unsigned char *wst = stages + (size_t)slot * kM2StageBytes + pl * kM2WBytes +
+                                           (size_t)h * nblk * kBlockBytes;
+                for (int j0 = 0; j0 < nv; j0 += kM2Unit, ++u) {
+                    const uint32_t as = u % kM2AUnits, au = u / kM2AUnits;
+                    if (au > 0 && !m2_wait(S, S.aempty[as], (au - 1) & 1u, err)) {
+                        ok = false;
+                        break;
+                    }
+                    const int nu = min(kM2Unit, nv - j0);
+                    for (int i = par; i < nu; i += kM2ExGroups) {
+                        const int j = j0 + i;
+                        const uint4 q = live ? *reinterpret_cast<const uint4 *>(wst + ((size_t)j * 32 + rl) * 16)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                        const uint32_t ws[4] = {q.x, q.y, q.z, q.w};
+                        uint32_t lo[4][2], hi[4][2];
 #pragma unroll
-            for (int c = 0; c < kMmqN; ++c)
-                if (c < n) A.y[(size_t)c * W.M + row] = acc[c];
+                        for (int m = 0; m < 4; ++m) {
+                            uint32_t e0, e1;
+                            expand_select(cb, ws[m], e0, e1);
+                            mmq_halves(e0, e1, lo[m], hi[m]);
+                        }
+                        unsigned char *at = aunits + (size_t)as * kM2AUnitBytes + (size_t)i * kMmqATile;
+                        *reinterpret_cast<uint4 *>(at + mmq_core_off(row, 0)) = make_uint4(lo[0][0], lo[0][1], lo[1][0], lo[1][1]);
+                        *reinterpret_cast<uint4 *>(at + mmq_core_off(row, 8)) = make_uint4(lo[2][0], lo[2][1], lo[3][0], lo[3][1]);
+                        *reinterpret_cast<uint4 *>(at + mmq_core_off(row, 16)) = make_uint4(hi[0][0], hi[0][1], hi[1][0], hi[1][1]);
+                        *reinterpret_cast<uint4 *>(at + mmq_core_off(row, 24)) = make_uint4(hi[2][0], hi[2][1], hi[3][0], hi[3][1]);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive(smem_addr(&S.afull[as]));
+                }
+                mbar_arrive(smem_addr(&S.sempty[slot]));
+            }
+        }
+    } else {
+        // epilogue: thread (row, group) -- the units u == group (mod groups)
+        const int row = tid & (kMmqM - 1), eg = tid >> 7, pl = row >> 6, h = (row >> 5) & 1, rl = row & 31;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        float *part = reinterpret_cast<float *>(aunits + (size_t)kM2AUnits * kM2AUnitBytes);
+        uint32_t k = 0, u = 0;
+        bool ok = true;
+        // every epilogue thread walks every tile (after a give-up without work)
+        // so all of them reach the group barriers below equally often
+        for (int t = blockIdx.x; t < T; t += gridDim.x) {
+            const int pair = 2 * t + pl;
+            const bool live = pair < W.P;
+            const int64_t grow = (int64_t)pair * 64 + h * 32 + rl;
+            float acc[kMmqN];
+#pragma unroll
+            for (int c = 0; c < kMmqN; ++c) acc[c] = 0.0f;
+            for (int c = 0; c < nch && ok; ++c, ++k) {
+                const uint32_t slot = k % kM2Stages;
+                if (!m2_wait(S, S.sfull[slot], (k / kM2Stages) & 1u, err)) {
+                    ok = false;
+                    break;
+                }
+                const int nblk = chunk_blocks(nbp, c), nv = min(kChunk, nb - c * kChunk);
+                const unsigned char *st = stages + (size_t)slot * kM2StageBytes;
+                const uint2 *scp = reinterpret_cast<const uint2 *>(st + pl * kM2WBytes + (size_t)h * nblk * kBlockBytes +
+                                                                  (size_t)nblk * 512) + rl;
+                const float *mt = reinterpret_cast<const float *>(st + kM2MetaOff);
+                for (int j0 = 0; j0 < nv && ok; j0 += kM2Unit, ++u) {
+                    if ((int)(u % kM2EpGroups) != eg) continue;
+                    const uint32_t ds = u % kM2DUnits;
+                    if (!m2_wait(S, S.dfull[ds], (u / kM2DUnits) & 1u, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nu = min(kM2Unit, nv - j0);
+                    const uint2 sq = live ? scp[(j0 >> 2) * 32] : make_uint2(0u, 0u);  // the unit's four scales
+                    for (int i0 = 0; i0 < nu; i0 += kM2EpBatch) {
+                        uint32_t d[kM2EpBatch][kMmqN];
+#pragma unroll
+                        for (int i = 0; i < kM2EpBatch; ++i)
+                            if (i0 + i < nu)
+                                tmem_ld16_issue(tmem + lane_base + (ds * kM2Unit + (uint32_t)(i0 + i)) * kMmqN, d[i]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < kM2EpBatch; ++i) {
+                            if (i0 + i >= nu) break;
+                            const int jj = i0 + i, j = j0 + jj;
+                            const uint32_t sw = (jj & 2) ? sq.y : sq.x;
+                            const float dw = (jj & 1) ? half_hi(sw) : half_lo(sw);
+                            const float *md = mt + j * kMmqMetaFloats;
+#pragma unroll
+                            for (int cc = 0; cc < kMmqN; ++cc) {
+                                if (cc >= n) break;
+                                const float sdot = __fsub_rn(__uint_as_float(d[i][cc]), md[kMmqN + cc]);
+                                acc[cc] = __fmaf_rn(__fmul_rn(dw, md[cc]), sdot, acc[cc]);
+                            }
+                            if (A.dbg && live && grow < W.M) {
+                                const int b = c * kChunk + j;
+#pragma unroll
+                                for (int cc = 0; cc < kMmqN; ++cc)
+                                    if (cc < n)
+                                        A.dbg[((size_t)cc * W.M + grow) * nb + b] =
+                                            (int32_t)__fsub_rn(__uint_as_float(d[i][cc]), md[kMmqN + cc]);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(smem_addr(&S.dempty[ds]));
+                }
+                mbar_arrive(smem_addr(&S.sempty[slot]));
+            }
+            if (kM2EpGroups > 1) {
+                // the groups' partial sums of this tile: groups 1.. hand theirs
+                // to group 0 through shared memory (epilogue threads only)
+                if (eg > 0) {
+#pragma unroll
+                    for (int cc = 0; cc < kMmqN; ++cc) part[((eg - 1) * kMmqN + cc) * kMmqM + row] = acc[cc];
+                }
+                asm volatile("bar.sync 2, %0;" ::"n"(kM2EpWarps * 32) : "memory");
+                if (eg == 0) {
+                    for (int g2 = 1; g2 < kM2EpGroups; ++g2)
+#pragma unroll
+                        for (int cc = 0; cc < kMmqN; ++cc) acc[cc] += part[((g2 - 1) * kMmqN + cc) * kMmqM + row];
+                }
+                asm volatile("bar.sync 2, %0;" ::"n"(kM2EpWarps * 32) : "memory");
+            }
+            if (eg == 0 && ok && A.y && live && grow < W.M) {
+#pragma unroll
+                for (int cc = 0; cc < kMmqN; ++cc)
+                    if (cc < n) A.y[(size_t)cc * W.M + grow] = acc[cc];
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kMmqTmemCols);
+    if (warp == 0) tmem_dealloc(tmem, kM2TmemCols);
 }
 
 size_t mmq_bimg_bytes(int nb) { return (size_t)nb * kMmqBTile; }
@@ -347,27 +511,24 @@ cudaError_t launch_mmq(const DevMat &W, const uint8_t *bimg, const float *meta, 
                        cudaStream_t s) {
     static bool raised = false;  // the dynamic shared memory above the default 48 KB
     if (!raised) {
-        cudaError_t e = cudaFuncSetAttribute(k_mmq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmqSmem);
+        cudaError_t e = cudaFuncSetAttribute(k_mmq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kM2Smem);
         if (e != cudaSuccess) return e;
         raised = true;
     }
-    int dev = 0, sms = 0, per_sm = 0;
+    int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_mmq, kMmqThreads, kMmqSmem);
     if (e != cudaSuccess) return e;
-    // tensor memory: kMmqTmemCols columns per resident CTA, 512 per SM
-    per_sm = std::max(1, std::min(per_sm, (int)(512 / kMmqTmemCols)));
     const int T = (int)((W.P + 1) / 2);
-    const int grid = std::max(1, std::min(T, sms * per_sm));
+    const int grid = std::max(1, std::min(T, sms));  // one CTA per SM
     MmqArgs A{W, bimg, meta, n, y, dbg};
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kMmqThreads);
-    cfg.dynamicSmemBytes = kMmqSmem;
+    cfg.blockDim = dim3(kM2Threads);
+    cfg.dynamicSmemBytes = kM2Smem;
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = 1;
