@@ -629,6 +629,31 @@ def run_gpu(args):
                                        "rotating_copies": copies, "rotating_bytes": copies * wb}
         del Ws
 
+    # the tensor-core path (cbq_matmat) for 8 and 16 columns against
+    # ceil(n/5) passes of the dp4a path, on the 16384 x 4096 projection and on
+    # the head shape (graph replay; the head is larger than L2 by itself)
+    mmq = {}
+    for M, K, copies in ((16384, 4096, -(-4 * l2_bytes // (16384 * (4096 // QK) * BB))), (HEAD_M, HEAD_K, 1)):
+        Ws = [head] if M == HEAD_M else [cbq.Weights(synth.weight_blocks(M, K, stream=synth.S_W * 1000 + 31 * i + 7),
+                                                     M, K) for i in range(copies)]
+        for nc in (8, 16):
+            xx = torch.from_numpy(synth.activations(nc, K, stream=synth.S_X + nc)).to(dev)
+            yy = torch.empty((nc, M), dtype=torch.float32, device=dev)
+            t_mmq = graph_us(lambda i: cbq.cbq_matmat(Ws[i % len(Ws)], xx, y=yy), n_calls=len(Ws), replays=8)
+            parts = [(c0, min(5, nc - c0)) for c0 in range(0, nc, 5)]
+            xs = [xx[c0:c0 + kk].contiguous() for c0, kk in parts]
+            ys = [torch.empty((kk, M), dtype=torch.float32, device=dev) for _, kk in parts]
+
+            def passes(i):
+                for xp, yp in zip(xs, ys):
+                    cbq.cbq_matvec(Ws[i % len(Ws)], xp, y=yp)
+            t_dp = graph_us(passes, n_calls=len(Ws), replays=8)
+            wb = M * (K // QK) * BB
+            mmq[f"{M}x{K}_n{nc}"] = {"tensor_core_us": t_mmq, "dp4a_passes_us": t_dp, "dp4a_passes": len(parts),
+                                      "tensor_core_weight_gbs": wb / (t_mmq * 1e-6) / 1e9,
+                                      "speedup_vs_dp4a": t_dp / t_mmq}
+        del Ws
+
     # the weight converter (fp32 matrix -> codebook blocks) on a 16384 x 4096
     # matrix: 268 MB read, 38 MB written per call, two inputs alternating
     # (more than four times L2 between two reads of one input)
@@ -689,6 +714,7 @@ def run_gpu(args):
             "us_per_layer_with_shared_expert": shared,
             "us_per_call_dense": dense,
             "weight_converter": converter,
+            "tensor_core_path": mmq,
             "kernels_ms_per_step": {"moe layer call (k_quantize + k_moe + k_moe_combine)": sum(k_moe) / len(timed),
                                     "head call (k_quantize + k_matvec<5>)": sum(k_head) / len(timed)},
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -274,8 +274,9 @@ int cbq_moe_set_stage_events(cbq_moe *L, void *ev_start, void *ev_layer, void *e
  * handoff and per-device state" #507), read for this format.  Same result
  * definition as cbq_matvec (the activation quantization, exact per-block
  * integer dots, y = sum_b dw*dx*s in fp32 with the same three roundings per
- * block), blocks summed in ascending order: every block dot is exact, so y is
- * within the same bound of the plain definition.  A level enters the MMA as
+ * block); the blocks, in units of four, alternate between two running sums
+ * added at the end of the row: every block dot is exact, so y is within the
+ * same bound of the plain definition.  A level enters the MMA as
  * the fp16 value 1152 + level, an int8 activation as fp16; each 32-wide block
  * sum is an integer below 2^24 (exact in the fp32 accumulator), and the bias
  * 1152 * sum q is subtracted exactly.  Arguments as cbq_matvec (x_dev n x K

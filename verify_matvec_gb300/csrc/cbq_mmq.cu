@@ -14,7 +14,8 @@
 // integer below 2^24, so the fp32 accumulator holds the exact block sum; s =
 // sum - 1152 * sum_k q_k (the second term per column and block, exact in
 // fp32) is the exact integer dot.  The scaling then repeats the dp4a path's
-// roundings: acc = fma(dw*dx, s, acc), blocks in ascending order.
+// roundings per block, acc = fma(dw*dx, s, acc), with the row's blocks (in
+// units of four) alternating between two running sums added at the end.
 //
 // Tile.  One MMA is M = 128 weight rows (two pairs of 32-row groups of the
 // repacked layout) x N = 16 columns x K = 16; a block of 32 weights is two
