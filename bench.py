@@ -53,10 +53,10 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure
 # one ncu capture of each kernel (summaries in profiles/), valid only for the
 # kernel sources they were taken on (digest below); otherwise reported as null.
 PROFILED = {
-    "source_digest": "b2cdcff04e9c4cab",
-    "k_matvec<5> (head)": 297_926_912 + 5_238_784,          # one launch, 129280 x 4096, n=5
-    # one layer call (k_quantize + k_moe + k_moe_combine) with 28 distinct experts
-    "moe call per expert": (97_536 + 396_610_048 + 3_514_880 + 673_536) / 28,
+    "source_digest": "d7cc04691493f254",
+    "k_matvec<5> (head)": 297_937_920 + 5_145_856,          # one launch, 129280 x 4096, n=5
+    # one layer call (k_quantize_chunked + k_moe + k_moe_combine) with 28 distinct experts
+    "moe call per expert": (90_880 + 396_650_496 + 3_427_584 + 673_536) / 28,
 }
 
 
@@ -90,10 +90,12 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--profile", action="store_true",
                     help="time the main loop only (no e2e, per-layer or oracle legs); for profiler runs")
-    ap.add_argument("--case", default="step", choices=["step", "b1", "b5", "dense1"],
+    ap.add_argument("--case", default="step", choices=["step", "b1", "b5", "dense1", "convert", "mmq16"],
                     help="profile mode only: the whole step, the MoE layer alone at batch 1 (top-4) "
-                         "or batch 5 (top-8), or the 4096x4096 dense projection at n=1 (cbq_matvec over "
-                         "16 weight copies, more than L2)")
+                         "or batch 5 (top-8), the 4096x4096 dense projection at n=1 (cbq_matvec over "
+                         "16 weight copies, more than L2), the weight converter on 16384x4096 fp32 "
+                         "(two inputs, alternating), or the tensor-core path on 16384x4096 at n=16 "
+                         "(cbq_matmat over 8 weight copies, more than L2)")
     ap.add_argument("--shared", action="store_true",
                     help="profile mode, b1/b5 cases: give the layer a shared expert (one more expert of the "
                          "routed shape that every token passes through)")
@@ -389,6 +391,32 @@ def run_gpu(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile": True, "case": args.case, "us_per_call": 1e3 * a0.elapsed_time(a1) / args.steps,
                           "device_error": max(cbq.cbq_weights_get_error(w) for w in Ws)}), flush=True)
+        return
+    if args.profile and args.case in ("convert", "mmq16"):
+        M, K = 16384, 4096
+        if args.case == "convert":
+            ws = [torch.randn((M, K), device=dev, generator=torch.Generator(device=dev).manual_seed(5 + i)) * 0.02
+                  for i in range(2)]
+            out = torch.empty((M, K // 32, 18), dtype=torch.uint8, device=dev)
+            call = lambda i: cbq.cbq_quantize_weights(ws[i % 2], out=out)
+            err = lambda: 0
+        else:
+            Ws = [cbq.Weights(synth.weight_blocks(M, K, stream=synth.S_W * 1000 + 31 * i + 3), M, K) for i in range(8)]
+            xx = torch.from_numpy(synth.activations(16, K, stream=synth.S_X)).to(dev)
+            yy = torch.empty((16, M), dtype=torch.float32, device=dev)
+            call = lambda i: cbq.cbq_matmat(Ws[i % 8], xx, y=yy)
+            err = lambda: max(cbq.cbq_weights_get_error(w) for w in Ws)
+        for i in range(args.warmup):
+            call(i)
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for i in range(args.steps):
+            call(i)
+        a1.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": True, "case": args.case, "us_per_call": 1e3 * a0.elapsed_time(a1) / args.steps,
+                          "device_error": err()}), flush=True)
         return
     if args.profile and args.case != "step":
         L = build_layer(torch, cbq, n_exp, with_head=False)

@@ -170,15 +170,17 @@ __device__ __forceinline__ void mmq_halves(uint32_t e0, uint32_t e1, uint32_t (&
 // same sequence (tile, stage of 16 blocks, unit of up to 4 blocks, block):
 //   warp 12, the producer: per stage, bulk copies of the tile's two pairs'
 //     weight chunk, the 16 B tiles and their metadata into a ring of stages;
-//   warps 4-11, the expanders: thread (row, parity) expands the row's blocks
-//     of that parity into a ring of A units (four block tiles each);
+//   warps 8-11, the expanders: thread = row; it expands the row's blocks of
+//     each unit into a ring of A units (four block tiles each);
 //   warp 13, the MMA issuer: per unit, two MMAs per block from the A tiles and
 //     the stage's B tiles into a ring of units of sums in tensor memory (16
 //     columns per block), then commits that free the A unit and publish the
 //     sums (and, after a stage's last unit, free the stage's B tiles);
-//   warps 0-3, the epilogue: thread = row (warp w reads tensor-memory lanes
-//     32w..32w+31); per unit it reads the sums, frees their slot and scales
-//     them into the row's n running sums; y at the end of a tile.
+//   warps 0-7, the epilogue, in two groups of four warps that take alternate
+//     units: thread = row (warp w reads tensor-memory lanes 32(w%4)..+31);
+//     per unit it reads the sums, frees their slot and scales them into the
+//     row's n running sums; at the end of a tile group 1 hands its sums to
+//     group 0 through shared memory, which adds them and stores y.
 // Synchronising per unit rather than per block keeps the barrier and commit
 // traffic of the single MMA thread and of the epilogue to a quarter.
 // Every wait is bounded (kWaitLimitNs): a give-up sets kErrMmqTimeout and a
