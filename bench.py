@@ -90,12 +90,13 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--profile", action="store_true",
                     help="time the main loop only (no e2e, per-layer or oracle legs); for profiler runs")
-    ap.add_argument("--case", default="step", choices=["step", "b1", "b5", "dense1", "convert", "mmq16"],
+    ap.add_argument("--case", default="step", choices=["step", "b1", "b5", "dense1", "convert", "mmq16", "hc"],
                     help="profile mode only: the whole step, the MoE layer alone at batch 1 (top-4) "
                          "or batch 5 (top-8), the 4096x4096 dense projection at n=1 (cbq_matvec over "
                          "16 weight copies, more than L2), the weight converter on 16384x4096 fp32 "
                          "(two inputs, alternating), or the tensor-core path on 16384x4096 at n=16 "
-                         "(cbq_matmat over 8 weight copies, more than L2)")
+                         "(cbq_matmat over 8 weight copies, more than L2), or the sinkhorn normalisation of "
+                         "2^21 hyper-connection matrices, 20 rounds (two inputs alternating)")
     ap.add_argument("--shared", action="store_true",
                     help="profile mode, b1/b5 cases: give the layer a shared expert (one more expert of the "
                          "routed shape that every token passes through)")
@@ -392,9 +393,15 @@ def run_gpu(args):
         print(json.dumps({"profile": True, "case": args.case, "us_per_call": 1e3 * a0.elapsed_time(a1) / args.steps,
                           "device_error": max(cbq.cbq_weights_get_error(w) for w in Ws)}), flush=True)
         return
-    if args.profile and args.case in ("convert", "mmq16"):
+    if args.profile and args.case in ("convert", "mmq16", "hc"):
         M, K = 16384, 4096
-        if args.case == "convert":
+        if args.case == "hc":
+            hb = [torch.from_numpy(synth.hc_logits(1 << 21, stream=synth.S_HC * 1000 + 100 + i)).to(dev)
+                  for i in range(2)]
+            hb_out = torch.empty_like(hb[0])
+            call = lambda i: cbq.cbq_hc_sinkhorn(hb[i % 2], 20, out=hb_out)
+            err = lambda: 0
+        elif args.case == "convert":
             ws = [torch.randn((M, K), device=dev, generator=torch.Generator(device=dev).manual_seed(5 + i)) * 0.02
                   for i in range(2)]
             out = torch.empty((M, K // 32, 18), dtype=torch.uint8, device=dev)
@@ -694,6 +701,28 @@ def run_gpu(args):
                  "gbs": conv_bytes / (conv_us * 1e-6) / 1e9, "frac_of_peak": conv_bytes / (conv_us * 1e-6) / 1e9 / peak}
     del wc, bc
 
+    # the hyper-connection Sinkhorn normalisation (4 x 4 per token, 20 rounds):
+    # a decoded token runs it twice per layer, 86 times over the model; timed
+    # here on a verify batch of five tokens per call (86 calls per replay), and
+    # on 2^21 matrices per call (134 MB in, 134 MB out, two inputs alternating)
+    # for its throughput
+    hc_iters, hc_calls = 20, 86
+    hs = [torch.from_numpy(synth.hc_logits(N_TOK, stream=synth.S_HC * 1000 + i)).to(dev) for i in range(hc_calls)]
+    hs_out = torch.empty_like(hs[0])
+    hc_dec_us = graph_us(lambda i: cbq.cbq_hc_sinkhorn(hs[i], hc_iters, out=hs_out), n_calls=hc_calls, replays=10)
+    n_hc = 1 << 21
+    hb = [torch.from_numpy(synth.hc_logits(n_hc, stream=synth.S_HC * 1000 + 100 + i)).to(dev) for i in range(2)]
+    hb_out = torch.empty_like(hb[0])
+    hc_big_us = graph_us(lambda i: cbq.cbq_hc_sinkhorn(hb[i % 2], hc_iters, out=hb_out), n_calls=2, replays=10)
+    hc_bytes = n_hc * 2 * cbq.CBQ_HC_NHC * cbq.CBQ_HC_NHC * 4
+    hc = {"nhc": cbq.CBQ_HC_NHC, "iters": hc_iters,
+          "verify_batch5_us_per_call": hc_dec_us, "calls_per_token": hc_calls,
+          "us_per_token": hc_dec_us * hc_calls,
+          "large_batch": {"matrices": n_hc, "us": hc_big_us, "matrices_per_s": n_hc / (hc_big_us * 1e-6),
+                          "gbs": hc_bytes / (hc_big_us * 1e-6) / 1e9,
+                          "frac_of_hbm_peak": hc_bytes / (hc_big_us * 1e-6) / 1e9 / peak}}
+    del hs, hs_out, hb, hb_out
+
     # slowest rank decides; bytes add up over ranks
     (ms_max, e2e_max), (value, e2e_value) = aggregate([ms, e2e_ms], sum(wbytes), world, dev)
     h2d = N_TOK * H * 4 + 2 * slots * 4 + HEAD_N * HEAD_K * 4
@@ -743,6 +772,7 @@ def run_gpu(args):
             "us_per_call_dense": dense,
             "weight_converter": converter,
             "tensor_core_path": mmq,
+            "hc_sinkhorn": hc,
             "kernels_ms_per_step": {"moe layer call (k_quantize + k_moe + k_moe_combine)": sum(k_moe) / len(timed),
                                     "head call (k_quantize + k_matvec<5>)": sum(k_head) / len(timed)},
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -242,6 +242,36 @@ int cbq_router_topk(const float *logits_dev, int n_tok, int E, int topk, int32_t
  * else CBQ_EINVAL.  One kernel launch on `stream`. */
 int cbq_quantize_weights(const float *w_dev, int64_t M, int64_t K, void *blocks_dev, void *stream);
 
+/* Streams of the hyper-connection state (the NHC of the pages' NHC = 4
+ * specialisation), and the most normalisation rounds one call accepts. */
+#define CBQ_HC_NHC 4
+#define CBQ_HC_MAX_ITERS 1024
+#define CBQ_HC_MAX_N (1ll << 28)
+
+/* Sinkhorn normalisation of the hyper-connection mixing matrices (the
+ * register-resident sinkhorn kernel of the fused DS4 hyper-connection op,
+ * "feat(ds4): add DSpark speculative runtime + optimizations" #496, in its
+ * NHC = 4 form, "fix(ds4): keep ROCmFPX generation byte-safe" #494).  The
+ * pages give neither the iteration count nor the update; the plain reading
+ * of a Sinkhorn normalisation is used.  For each of the n row-major
+ * CBQ_HC_NHC x CBQ_HC_NHC matrices c of fp32 logits at logits_dev:
+ *   P = exp(c - max c);
+ *   `iters` rounds of: every row of P scaled to sum 1, then every column
+ *   (a sum in index order, times its reciprocal from the hardware
+ *   approximation, within 1 ulp);
+ *   out_dev = P after the last round (columns sum to 1 within rounding; rows
+ *   approach 1 as the rounds converge); iters = 0 gives exp(c - max c).
+ * The result agrees with an fp64 evaluation of the same rounds within
+ * (8 + 16 * iters) * 2^-24 per entry.  In contract: finite logits whose
+ * spread within a matrix (max - min) is at most 80, so every entry stays a
+ * normal fp32 number.  Arguments: both pointers 16-byte aligned (out_dev may
+ * equal logits_dev: each matrix is read before it is written; otherwise the
+ * buffers must not overlap); 1 <= n <= CBQ_HC_MAX_N; 0 <= iters <=
+ * CBQ_HC_MAX_ITERS; else CBQ_EINVAL.  One kernel launch on `stream` (a
+ * programmatic dependent of the work ahead, like every kernel here), one
+ * thread per matrix; the caller owns both buffers. */
+int cbq_hc_sinkhorn(const float *logits_dev, int64_t n, int iters, float *out_dev, void *stream);
+
 /* cbq_router_topk into the handle's staging buffers, then cbq_moe_matvec with
  * those ids and weights: the routed layer from router logits with no host
  * round trip (one launch more than cbq_moe_matvec).  Same limits as both. */
@@ -358,6 +388,17 @@ int cbq_moe_set_debug(cbq_moe *L, int keep_intermediate);
  * few seconds with undefined outputs, sets only timeout bits, and leaves the
  * handle usable: the next call is correct. */
 int cbq_moe_debug_stall(cbq_moe *L, int mode);
+
+/* Give-up test mode of the tensor-core path (cbq_matmat and its block-dot
+ * checking entry; 0 turns it off): with mode 1 the first CTA's producer
+ * issues no copy, so the bounded waits of every role of that CTA for its
+ * first stage give up after 1 s (CBQ_DEVERR_PIPE_TIMEOUT in the handle's
+ * error word); the CTA issues no MMA after giving up, waits (bounded) for
+ * those it issued and frees its tensor memory before it exits.  A call in
+ * this mode returns after about a second with undefined outputs, sets only
+ * that bit, and leaves the handle usable: the next call is correct.
+ * Errors: EINVAL (null handle, mode outside 0..1). */
+int cbq_debug_mmq_stall(cbq_weights *W, int mode);
 
 /* Copy the intermediate of the last cbq_moe_matvec on this handle, for
  * slots p < nslots (at most CBQ_MAX_TOKENS * (CBQ_MAX_TOPK + 1)): routed

@@ -390,3 +390,29 @@ void oracle_quantize_weights(const float *w, int64_t M, int64_t K, uint8_t *bloc
         for (int64_t b = 0; b < nb; ++b)
             oracle_quantize_weights_block(w + r * K + b * ORACLE_QK, blocks + (r * nb + b) * ORACLE_BLOCK_BYTES);
 }
+
+/* One matrix at a time: P = exp(c - max c), then `iters` rounds of row
+ * normalisation followed by column normalisation. */
+void oracle_hc_sinkhorn(const float *logits, int64_t n, int nhc, int iters, double *out) {
+    const int nn = nhc * nhc;
+    for (int64_t m = 0; m < n; ++m) {
+        const float *c = logits + m * nn;
+        double *P = out + m * nn;
+        double cmax = (double)c[0];
+        for (int i = 1; i < nn; ++i)
+            if ((double)c[i] > cmax) cmax = (double)c[i];
+        for (int i = 0; i < nn; ++i) P[i] = exp((double)c[i] - cmax);
+        for (int t = 0; t < iters; ++t) {
+            for (int r = 0; r < nhc; ++r) {
+                double sum = 0.0;
+                for (int j = 0; j < nhc; ++j) sum += P[r * nhc + j];
+                for (int j = 0; j < nhc; ++j) P[r * nhc + j] /= sum;
+            }
+            for (int j = 0; j < nhc; ++j) {
+                double sum = 0.0;
+                for (int r = 0; r < nhc; ++r) sum += P[r * nhc + j];
+                for (int r = 0; r < nhc; ++r) P[r * nhc + j] /= sum;
+            }
+        }
+    }
+}

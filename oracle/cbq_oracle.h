@@ -48,7 +48,11 @@
  * against its k=1 reduction, the silu odd-part identity and token independence;
  * the weight converter against numpy's binary16 rounding, hand-worked blocks
  * (ties, a negative maximum, a zero block), an exact round trip of weights on
- * the codebook grid and an exact-rational nearest-level search.
+ * the codebook grid and an exact-rational nearest-level search; the sinkhorn
+ * normalisation against the closed forms of a rank-one matrix (uniform after
+ * one step) and of the 2 x 2 limit, the fixed point of a doubly stochastic
+ * input, invariance to a constant added to a row, permutation equivariance
+ * and the column sums.
  */
 #ifndef CBQ_ORACLE_H
 #define CBQ_ORACLE_H
@@ -177,6 +181,21 @@ void oracle_quantize_weights_block(const float *w, uint8_t *blk);
 
 /* A row-major M x K fp32 matrix (K % 32 == 0) to M x (K/32) blocks. */
 void oracle_quantize_weights(const float *w, int64_t M, int64_t K, uint8_t *blocks);
+
+/* Sinkhorn normalisation of the hyper-connection mixing matrices (the
+ * "register-resident sinkhorn kernel" of the fused DS4 hyper-connection op,
+ * GGML_OP_DS4_HC, in "feat(ds4): add DSpark speculative runtime +
+ * optimizations" #496; its NHC = 4 specialisation in "fix(ds4): keep ROCmFPX
+ * generation byte-safe" #494; the pages give neither the iteration count nor
+ * the update, the plain reading of a Sinkhorn normalisation is used).  For
+ * each of the n row-major nhc x nhc matrices c of logits:
+ *   P = exp(c - max(c)), in fp64 (the shift multiplies P by a positive
+ *       constant, which the first normalisation removes);
+ *   `iters` times: divide every row of P by its sum, then every column by
+ *       its sum (sums in index order);
+ * out = P after the last column step (its columns sum to 1).
+ * nhc >= 1, iters >= 0 (0 gives exp(c - max c) itself). */
+void oracle_hc_sinkhorn(const float *logits, int64_t n, int nhc, int iters, double *out);
 
 #ifdef __cplusplus
 }

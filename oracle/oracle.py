@@ -77,6 +77,8 @@ def _bind(lib):
     lib.oracle_float_to_half.restype = ctypes.c_uint16
     lib.oracle_quantize_weights_block.argtypes = [P, P]
     lib.oracle_quantize_weights.argtypes = [P, I64, I64, P]
+    lib.oracle_hc_sinkhorn.argtypes = [P, I64, I, I, P]
+    lib.oracle_hc_sinkhorn.restype = None
     return lib
 
 
@@ -274,4 +276,16 @@ def quantize_weights(w: np.ndarray, M: int, K: int) -> np.ndarray:
     w = np.ascontiguousarray(w, dtype=np.float32).reshape(M, K)
     out = np.empty((M, K // QK, BLOCK_BYTES), dtype=np.uint8)
     _load().oracle_quantize_weights(_p(w), M, K, _p(out))
+    return out
+
+
+def hc_sinkhorn(logits, iters: int) -> np.ndarray:
+    """Sinkhorn normalisation of fp32 logits (..., nhc, nhc): exp(c - max c),
+    then `iters` rounds of row then column normalisation, fp64 out."""
+    c = np.ascontiguousarray(logits, dtype=np.float32)
+    nhc = c.shape[-1]
+    assert c.shape[-2] == nhc
+    n = c.size // (nhc * nhc)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_hc_sinkhorn(_p(c), n, nhc, int(iters), _p(out))
     return out

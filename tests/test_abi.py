@@ -73,6 +73,16 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.cbq_quantize_weights(aligned, 4, 0, aligned, None) == EINVAL                    # K < 32
     assert lib.cbq_quantize_weights(ctypes.c_void_p(0x1004), 4, 64, aligned, None) == EINVAL  # w not 16-aligned
     assert lib.cbq_quantize_weights(aligned, 4, 64, ctypes.c_void_p(0x1001), None) == EINVAL  # odd output
+    assert lib.cbq_debug_mmq_stall(None, 1) == EINVAL
+    far = ctypes.c_void_p(0x100000)
+    assert lib.cbq_hc_sinkhorn(None, 4, 20, far, None) == EINVAL                               # no logits
+    assert lib.cbq_hc_sinkhorn(aligned, 4, 20, None, None) == EINVAL                           # no output
+    assert lib.cbq_hc_sinkhorn(aligned, 0, 20, far, None) == EINVAL                            # n < 1
+    assert lib.cbq_hc_sinkhorn(aligned, cbq.CBQ_HC_MAX_N + 1, 20, far, None) == EINVAL         # n too large
+    assert lib.cbq_hc_sinkhorn(aligned, 4, -1, far, None) == EINVAL                            # iters < 0
+    assert lib.cbq_hc_sinkhorn(aligned, 4, cbq.CBQ_HC_MAX_ITERS + 1, far, None) == EINVAL      # too many rounds
+    assert lib.cbq_hc_sinkhorn(ctypes.c_void_p(0x1008), 4, 20, far, None) == EINVAL            # not 16-aligned
+    assert lib.cbq_hc_sinkhorn(aligned, 4, 20, ctypes.c_void_p(0x1040), None) == EINVAL        # overlaps, not in place
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -1,6 +1,7 @@
-"""The bounded waits of the layer kernel, run out on purpose through its
-give-up test mode (cbq_moe_debug_stall): a wait for a dependency count that is
-never reached, or for a weight stage that never arrives.  Every wait in the
+"""The bounded waits of the layer kernel and of the tensor-core path, run out
+on purpose through their give-up test modes (cbq_moe_debug_stall,
+cbq_debug_mmq_stall): a wait for a dependency count that is never reached, or
+for a weight stage that never arrives.  Every wait in the
 kernels has a 1 s limit; when it runs out the kernel records a timeout bit in
 the handle's error word and the CTA winds down without leaving a copy in
 flight.  The tests check the bits the host reads, and that the handle keeps
@@ -52,3 +53,28 @@ def test_wait_gives_up_and_handle_recovers(torch, layer, mode, must, n_tok, k):
         y = cbq.cbq_moe_matvec(L, hd, idd, wd).cpu().numpy()
         np.testing.assert_array_equal(y, y_ok)
         assert cbq.cbq_moe_get_error(L) == 0
+
+
+@pytest.mark.parametrize("n", [8, 16])
+def test_tensor_core_wait_gives_up_and_handle_recovers(torch, n):
+    """The first CTA of the tensor-core kernel fills no stage: every role's
+    wait for it runs out, the CTA frees its tensor memory and exits, the
+    error word holds the pipe timeout bit only, and the next calls give the
+    bits of a call before the stall."""
+    M, K = 384, 512  # three 128-row tiles: CTA 0 gives up, the others finish
+    W = cbq.Weights(synth.weight_blocks(M, K, stream=820), M, K)
+    x = torch.from_numpy(synth.activations(n, K, stream=821)).cuda()
+    y_ok = cbq.cbq_matmat(W, x).cpu().numpy()
+    assert cbq.cbq_weights_get_error(W) == 0
+    cbq.cbq_debug_mmq_stall(W, 1)
+    try:
+        cbq.cbq_matmat(W, x)
+        torch.cuda.synchronize()
+        err = cbq.cbq_weights_get_error(W)
+    finally:
+        cbq.cbq_debug_mmq_stall(W, 0)
+    assert err == cbq.CBQ_DEVERR_PIPE_TIMEOUT, f"error word {err:#x}"
+    for _ in range(2):
+        y = cbq.cbq_matmat(W, x).cpu().numpy()
+        np.testing.assert_array_equal(y, y_ok)
+        assert cbq.cbq_weights_get_error(W) == 0

@@ -652,3 +652,78 @@ def test_convert_error_bound_and_zero_blocks():
             x = w[r, 32 * b:32 * b + 32].astype(np.float64)
             dw = abs(O.half_to_float(int(blocks[r, b, 0]) | (int(blocks[r, b, 1]) << 8)))
             assert np.all(np.abs(dq - x) <= 14 * dw + 127 * dw * 2.0 ** -10)
+
+
+# ---- sinkhorn normalisation of the hyper-connection matrices ----------------
+
+def _logits(rng, n, nhc, scale=1.0, step=1.0 / 64):
+    """Logits on a grid of 1/64 in [-4*scale, 4*scale]: exact in fp32, so a
+    shifted copy stays exact too."""
+    return (np.round(rng.uniform(-4 * scale, 4 * scale, (n, nhc, nhc)) / step) * step).astype(np.float32)
+
+
+def test_sinkhorn_zero_rounds_is_the_shifted_exponential():
+    """With no round the output is exp(c - max c): numpy's exp, 1 at the
+    largest logit."""
+    rng = np.random.default_rng(40)
+    c = _logits(rng, 7, 4)
+    got = O.hc_sinkhorn(c, 0)
+    want = np.exp(c.astype(np.float64) - c.reshape(7, -1).max(axis=1)[:, None, None])
+    np.testing.assert_allclose(got, want, rtol=1e-15, atol=0)
+    assert np.all(got.reshape(7, -1).max(axis=1) == 1.0)
+
+
+@pytest.mark.parametrize("nhc", [2, 3, 4])
+def test_sinkhorn_rank_one_is_uniform_after_one_round(nhc):
+    """c_ij = a_i + b_j makes exp(c) rank one: one row step gives identical
+    rows, the column step then gives every entry 1/nhc."""
+    rng = np.random.default_rng(41 + nhc)
+    a = np.round(rng.uniform(-3, 3, (5, nhc, 1)) * 16) / 16
+    b = np.round(rng.uniform(-3, 3, (5, 1, nhc)) * 16) / 16
+    c = (a + b).astype(np.float32)
+    np.testing.assert_allclose(O.hc_sinkhorn(c, 1), np.full((5, nhc, nhc), 1.0 / nhc), rtol=0, atol=1e-14)
+
+
+def test_sinkhorn_two_by_two_limit_closed_form():
+    """A positive 2 x 2 matrix [[a, b], [c, d]] converges to [[p, 1-p], [1-p,
+    p]] with p = sqrt(ad) / (sqrt(ad) + sqrt(bc)) (the only doubly stochastic
+    matrix of the form diag(x) P diag(y))."""
+    rng = np.random.default_rng(44)
+    c = _logits(rng, 9, 2, scale=0.5)
+    e = np.exp(c.astype(np.float64))
+    ad = np.sqrt(e[:, 0, 0] * e[:, 1, 1])
+    bc = np.sqrt(e[:, 0, 1] * e[:, 1, 0])
+    p = ad / (ad + bc)
+    want = np.stack([np.stack([p, 1 - p], -1), np.stack([1 - p, p], -1)], -2)
+    np.testing.assert_allclose(O.hc_sinkhorn(c, 400), want, rtol=0, atol=1e-12)
+
+
+def test_sinkhorn_doubly_stochastic_input_is_a_fixed_point():
+    """A Latin square of 1/2, 1/4, 1/8, 1/8 is doubly stochastic: given its
+    logarithms (rounded to fp32) the rounds leave it where it is, within the
+    rounding of the logits."""
+    vals = np.array([0.5, 0.25, 0.125, 0.125])
+    P = np.array([[vals[(i + j) % 4] for j in range(4)] for i in range(4)])
+    c = np.log(P).astype(np.float32)[None]
+    for iters in (1, 5, 50):
+        np.testing.assert_allclose(O.hc_sinkhorn(c, iters)[0], P, rtol=0, atol=1e-6)
+
+
+def test_sinkhorn_sums_row_shift_and_permutations():
+    """After every round the columns sum to 1; with many rounds the rows do
+    too; a constant added to one row of logits changes nothing (the row step
+    removes it); permuting rows and columns of the logits permutes the
+    result."""
+    rng = np.random.default_rng(45)
+    c = _logits(rng, 6, 4)
+    for iters in (1, 2, 7):
+        out = O.hc_sinkhorn(c, iters)
+        np.testing.assert_allclose(out.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+    out = O.hc_sinkhorn(c, 300)
+    np.testing.assert_allclose(out.sum(axis=2), 1.0, rtol=0, atol=1e-12)
+    shifted = c.copy()
+    shifted[:, 2, :] += np.float32(1.25)
+    np.testing.assert_allclose(O.hc_sinkhorn(shifted, 3), O.hc_sinkhorn(c, 3), rtol=0, atol=1e-14)
+    pr, pc = np.array([2, 0, 3, 1]), np.array([1, 3, 0, 2])
+    got = O.hc_sinkhorn(c[:, pr][:, :, pc], 4)
+    np.testing.assert_allclose(got, O.hc_sinkhorn(c, 4)[:, pr][:, :, pc], rtol=0, atol=1e-14)

@@ -46,6 +46,13 @@ MUTANTS = {
                                         "if (i < 16) blk[2 + i] |= (uint8_t)(best << 4);\n        else blk[2 + i - 16] |= (uint8_t)best;"),
     "half rounding truncates": ("double q = nearbyint(ldexp(a, 11 - e));", "double q = floor(ldexp(a, 11 - e));"),
     "half subnormals flushed": ("const double q = nearbyint(ldexp(a, 24));", "const double q = 0.0;"),
+    "sinkhorn without the exponential": ("P[i] = exp((double)c[i] - cmax);", "P[i] = (double)c[i] - cmax;"),
+    "sinkhorn row step dropped": ("for (int j = 0; j < nhc; ++j) P[r * nhc + j] /= sum;", ""),
+    "sinkhorn column step dropped": ("for (int r = 0; r < nhc; ++r) P[r * nhc + j] /= sum;", ""),
+    "sinkhorn one round short": ("for (int t = 0; t < iters; ++t)", "for (int t = 1; t < iters; ++t)"),
+    "sinkhorn transposed": ("const float *c = logits + m * nn;\n        double *P = out + m * nn;",
+                            "const float *c = logits + m * nn;\n        double *P = out + m * nn;\n        float ct[64];\n"
+                            "        for (int i = 0; i < nn; ++i) ct[(i % nhc) * nhc + i / nhc] = c[i];\n        c = ct;"),
 }
 
 
@@ -85,6 +92,11 @@ def _pins():
         lambda: T.test_convert_grid_round_trip(),
         lambda: T.test_convert_brute_force_exact(),
         lambda: T.test_convert_error_bound_and_zero_blocks(),
+        lambda: T.test_sinkhorn_zero_rounds_is_the_shifted_exponential(),
+        lambda: T.test_sinkhorn_rank_one_is_uniform_after_one_round(4),
+        lambda: T.test_sinkhorn_two_by_two_limit_closed_form(),
+        lambda: T.test_sinkhorn_doubly_stochastic_input_is_a_fixed_point(),
+        lambda: T.test_sinkhorn_sums_row_shift_and_permutations(),
     ]
 
 

@@ -1,6 +1,6 @@
 """Build libcbq.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-Two translation units compiled in parallel, linked with the static CUDA
+The translation units compiled in parallel, linked with the static CUDA
 runtime.  `python -m verify_matvec_gb300.build` or `build()`; the result sits
 next to this file and is what the binding loads.
 """
@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "libcbq.so")
 OBJDIR = os.path.join(HERE, "_build")
-SOURCES = ["cbq_kernels.cu", "cbq_mmq.cu", "cbq_api.cu"]
+SOURCES = ["cbq_kernels.cu", "cbq_mmq.cu", "cbq_hc.cu", "cbq_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "-Xptxas", "-v", "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -29,6 +29,9 @@ CBQ_DEVERR_DEPENDENCY_TIMEOUT = 0x200
 CBQ_STATIC_SCRATCH_MAX_K = 16384
 CBQ_ROUTER_MAX_E = 16384
 CBQ_MAX_MMQ_COLS = 16
+CBQ_HC_NHC = 4
+CBQ_HC_MAX_ITERS = 1024
+CBQ_HC_MAX_N = 1 << 28
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -52,12 +55,14 @@ _SIGS = {
     "cbq_moe_matvec_host": ([_P, _P, _I, _P, _P, _I, _I, _P, _P], _I),
     "cbq_router_topk": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "cbq_quantize_weights": ([_P, _I64, _I64, _P, _P], _I),
+    "cbq_hc_sinkhorn": ([_P, _I64, _I, _P, _P], _I),
     "cbq_matmat": ([_P, _P, _I, _P, _P], _I),
     "cbq_debug_mmq_block_dots": ([_P, _P, _I, _P, _P], _I),
     "cbq_moe_matvec_logits": ([_P, _P, _I, _P, _I, _I, _P, _P], _I),
     "cbq_weights_get_error": ([_P, _P, ctypes.POINTER(ctypes.c_uint)], _I),
     "cbq_moe_get_error": ([_P, _P, ctypes.POINTER(ctypes.c_uint)], _I),
     "cbq_moe_debug_stall": ([_P, _I], _I),
+    "cbq_debug_mmq_stall": ([_P, _I], _I),
     "cbq_debug_block_dots": ([_P, _P, _I, _P, _P], _I),
     "cbq_moe_debug_block_dots": ([_P, _I, _I, _P, _I, _P, _P], _I),
     "cbq_moe_set_debug": ([_P, _I], _I),
@@ -393,6 +398,12 @@ def cbq_moe_debug_stall(L: Moe, mode: int):
     _check(load().cbq_moe_debug_stall(L.handle, int(mode)), "cbq_moe_debug_stall")
 
 
+def cbq_debug_mmq_stall(W: Weights, mode: int):
+    """Give-up test mode of the tensor-core path (0 off; 1 the first CTA
+    copies nothing, so its waits run out)."""
+    _check(load().cbq_debug_mmq_stall(W.handle, int(mode)), "cbq_debug_mmq_stall")
+
+
 def cbq_debug_block_dots(W: Weights, qx, s=None, stream=None):
     torch = _torch()
     n = qx.reshape(-1, W.K).shape[0]
@@ -447,6 +458,23 @@ def cbq_quantize_weights(w, out=None, stream=None):
         raise ValueError("out must be a contiguous uint8 tensor of M x K/32 x 18 bytes")
     _check(load().cbq_quantize_weights(_dev_ptr(w, torch.float32, "w"), M, K, ctypes.c_void_p(out.data_ptr()),
                                        _stream(stream)), "cbq_quantize_weights")
+    return out
+
+
+def cbq_hc_sinkhorn(logits, iters, out=None, stream=None):
+    """Sinkhorn normalisation of the fp32 hyper-connection logits (..., 4, 4)
+    on the device: exp(c - max c), then `iters` rounds of row and column
+    normalisation; out (same shape) may be logits itself."""
+    torch = _torch()
+    if logits.dim() < 2 or tuple(logits.shape[-2:]) != (CBQ_HC_NHC, CBQ_HC_NHC):
+        raise ValueError(f"logits must end in ({CBQ_HC_NHC}, {CBQ_HC_NHC})")
+    if out is None:
+        out = torch.empty_like(logits)
+    if out.shape != logits.shape:
+        raise ValueError("out must have the shape of logits")
+    n = logits.numel() // (CBQ_HC_NHC * CBQ_HC_NHC)
+    _check(load().cbq_hc_sinkhorn(_dev_ptr(logits, torch.float32, "logits"), n, int(iters),
+                                  _dev_ptr(out, torch.float32, "out"), _stream(stream)), "cbq_hc_sinkhorn")
     return out
 
 

@@ -32,6 +32,7 @@ struct cbq_weights {
     float *mq_dx;    // CBQ_MAX_MMQ_COLS x K/32
     uint8_t *mq_b;   // its B tiles (1 KB per block)
     float *mq_meta;  // its block metadata
+    int mq_stall;    // give-up test mode of the tensor-core path (cbq_debug_mmq_stall)
     int64_t K;
     int64_t bytes;
 };
@@ -350,7 +351,7 @@ int cbq_matmat(const cbq_weights *W, const float *x_dev, int n, float *y_dev, vo
     cudaStream_t s = as_stream(stream);
     CBQ_CUDA(cbq::launch_quantize(x_dev, W->K, n, W->mq_qx, W->mq_dx, s));
     CBQ_CUDA(cbq::launch_mmq_prep(W->mq_qx, W->mq_dx, n, W->K, W->mq_b, W->mq_meta, s));
-    CBQ_CUDA(cbq::launch_mmq(W->mat, W->mq_b, W->mq_meta, n, y_dev, nullptr, s));
+    CBQ_CUDA(cbq::launch_mmq(W->mat, W->mq_b, W->mq_meta, n, y_dev, nullptr, W->mq_stall, s));
     return CBQ_OK;
 }
 
@@ -360,7 +361,7 @@ int cbq_debug_mmq_block_dots(const cbq_weights *W, const int8_t *qx_dev, int n, 
     CBQ_CUDA(scope.status());
     cudaStream_t s = as_stream(stream);
     CBQ_CUDA(cbq::launch_mmq_prep(qx_dev, nullptr, n, W->K, W->mq_b, W->mq_meta, s));
-    CBQ_CUDA(cbq::launch_mmq(W->mat, W->mq_b, W->mq_meta, n, nullptr, s_dev, s));
+    CBQ_CUDA(cbq::launch_mmq(W->mat, W->mq_b, W->mq_meta, n, nullptr, s_dev, W->mq_stall, s));
     return CBQ_OK;
 }
 
@@ -569,6 +570,21 @@ int cbq_quantize_weights(const float *w_dev, int64_t M, int64_t K, void *blocks_
     return CBQ_OK;
 }
 
+int cbq_hc_sinkhorn(const float *logits_dev, int64_t n, int iters, float *out_dev, void *stream) {
+    static_assert(CBQ_HC_NHC == cbq::kHcNhc, "one matrix size on both sides of the ABI");
+    if (!logits_dev || !out_dev || n < 1 || n > CBQ_HC_MAX_N || iters < 0 || iters > CBQ_HC_MAX_ITERS ||
+        !aligned16(logits_dev) || !aligned16(out_dev))
+        return CBQ_EINVAL;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(logits_dev), b = reinterpret_cast<uintptr_t>(out_dev);
+    const uintptr_t bytes = (uintptr_t)n * CBQ_HC_NHC * CBQ_HC_NHC * sizeof(float);
+    if (a != b && a < b + bytes && b < a + bytes) return CBQ_EINVAL;  // overlapping, not in place
+    int dev = 0;
+    const int rc = check_device(&dev);
+    if (rc != CBQ_OK) return rc;
+    CBQ_CUDA(cbq::launch_hc_sinkhorn(logits_dev, n, iters, out_dev, as_stream(stream)));
+    return CBQ_OK;
+}
+
 int cbq_moe_matvec_logits(const cbq_moe *L, const float *h_dev, int n_tok, const float *logits_dev, int topk,
                           int swiglu, float *y_dev, void *stream) {
     if (!L || !h_dev || !logits_dev || !y_dev || n_tok < 1 || n_tok > CBQ_MAX_TOKENS || topk < 1 ||
@@ -690,6 +706,12 @@ int cbq_moe_get_error(const cbq_moe *L, void *stream, unsigned int *code) {
 int cbq_moe_debug_stall(cbq_moe *L, int mode) {
     if (!L || mode < 0 || mode > 2) return CBQ_EINVAL;
     L->ws.stall = mode;
+    return CBQ_OK;
+}
+
+int cbq_debug_mmq_stall(cbq_weights *W, int mode) {
+    if (!W || mode < 0 || mode > 1) return CBQ_EINVAL;
+    W->mq_stall = mode;
     return CBQ_OK;
 }
 

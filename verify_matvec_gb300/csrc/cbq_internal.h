@@ -133,16 +133,21 @@ cudaError_t launch_quantize_weights(const float *w, int64_t nblocks, uint8_t *ou
 // The tensor-core (tcgen05) path for up to kMaxMmqCols columns: the B tiles
 // and block metadata from quantized columns (qx[c][K], dx[c][K/32]; dx null
 // gives zero scales), then the tiles of W; dbg, when not null, receives the
-// exact block dots s[c][row][b].
+// exact block dots s[c][row][b].  stall = 1 (give-up test mode): CTA 0
+// copies nothing, so its bounded waits run out.
 constexpr int kMaxMmqCols = 16;
 size_t mmq_bimg_bytes(int nb);
 size_t mmq_meta_bytes(int nb);
 cudaError_t launch_mmq_prep(const int8_t *qx, const float *dx, int n, int64_t K, uint8_t *bimg, float *meta,
                             cudaStream_t s);
 cudaError_t launch_mmq(const DevMat &W, const uint8_t *bimg, const float *meta, int n, float *y, int32_t *dbg,
-                       cudaStream_t s);
+                       int stall, cudaStream_t s);
 // Top-k expert ids and softmax weights per token from router logits (n_tok x E).
 cudaError_t launch_router_topk(const float *logits, int n_tok, int E, int k, int32_t *ids, float *wts,
                                cudaStream_t s);
+// Sinkhorn normalisation of n row-major kHcNhc x kHcNhc matrices of logits
+// (16-byte aligned; out may equal logits).
+constexpr int kHcNhc = 4;
+cudaError_t launch_hc_sinkhorn(const float *logits, int64_t n, int iters, float *out, cudaStream_t s);
 
 }  // namespace cbq

@@ -150,6 +150,7 @@ struct MmqArgs {
     int n;                // columns (1..16)
     float *y;             // n x M (null: no outputs, block-dot checking)
     int32_t *dbg;         // optional: the block dots s[c][row][b] (checking)
+    int stall;            // give-up test mode: CTA 0's producer issues no copy
 };
 
 constexpr unsigned kErrMmqTimeout = 0x100u;  // the pipeline's timeout bit: an MMA batch never completed
@@ -274,7 +275,9 @@ __global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ M
     if (warp == kM2ProducerWarp) {
         if (lane == 0) {
             uint32_t k = 0;
-            bool ok = true;
+            // give-up test mode: CTA 0 fills no stage, so every role's
+            // bounded wait for its first stage runs out
+            bool ok = !(A.stall == 1 && blockIdx.x == 0);
             for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
                 const int p0 = 2 * t, p1 = 2 * t + 1;
                 for (int c = 0; c < nch && ok; ++c, ++k) {
@@ -511,7 +514,7 @@ cudaError_t launch_mmq_prep(const int8_t *qx, const float *dx, int n, int64_t K,
 }
 
 cudaError_t launch_mmq(const DevMat &W, const uint8_t *bimg, const float *meta, int n, float *y, int32_t *dbg,
-                       cudaStream_t s) {
+                       int stall, cudaStream_t s) {
     static bool raised = false;  // the dynamic shared memory above the default 48 KB
     if (!raised) {
         cudaError_t e = cudaFuncSetAttribute(k_mmq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kM2Smem);
@@ -524,7 +527,7 @@ cudaError_t launch_mmq(const DevMat &W, const uint8_t *bimg, const float *meta, 
     if (e != cudaSuccess) return e;
     const int T = (int)((W.P + 1) / 2);
     const int grid = std::max(1, std::min(T, sms));  // one CTA per SM
-    MmqArgs A{W, bimg, meta, n, y, dbg};
+    MmqArgs A{W, bimg, meta, n, y, dbg, stall};
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -27,7 +27,7 @@ QK = 32
 BLOCK_BYTES = 18
 
 # stream ids, one per tensor role
-S_W, S_X, S_GATE_UP, S_DOWN, S_H, S_IDS, S_HEAD, S_HEAD_X, S_MISC = range(1, 10)
+S_W, S_X, S_GATE_UP, S_DOWN, S_H, S_IDS, S_HEAD, S_HEAD_X, S_MISC, S_HC = range(1, 11)
 
 
 def rng(seed: int, stream: int) -> np.random.Generator:
@@ -83,6 +83,11 @@ def router(n_tok: int, k: int, E: int, seed: int = SEED, stream: int = S_IDS):
         ex = np.exp(logits - logits.max())
         wts[t] = (ex / ex.sum()).astype(np.float32)
     return ids, wts
+
+
+def hc_logits(n: int, nhc: int = 4, scale: float = 1.0, seed: int = SEED, stream: int = S_HC) -> np.ndarray:
+    """Hyper-connection mixing logits (n, nhc, nhc) fp32 ~ N(0, scale^2)."""
+    return (rng(seed, stream).standard_normal((n, nhc, nhc)) * scale).astype(np.float32)
 
 
 def distinct_experts(ids: np.ndarray, E: int) -> np.ndarray:
