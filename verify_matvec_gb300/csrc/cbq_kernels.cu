@@ -180,6 +180,8 @@ struct MatvecArgs {
     int64_t K;
     float *y;
     int S;             // pipeline stages
+    int singles;       // first single-group item: items below are whole pairs
+    int items;         // singles + 2 * (pairs - singles)
 };
 
 // Work counters of a persistent kernel (sched[0] items taken, sched[1] CTAs
@@ -219,29 +221,70 @@ __device__ __forceinline__ void quad(const Codebook &cb, const uint4 *qs, uint2 
     }
 }
 
-// One item pass of the dense kernel over a pair for NC columns staged
-// block-major (act, dx: stride NC), one row per lane: warp w takes row set
-// w / 4 (the pair's first or second group) and quad w % 4 of each 16-block
-// stage, so its sums (acc) are those of one group.  False on a give-up.
+// Two consecutive blocks (a quad's first or second half) of one row for NC
+// columns: index words at qs[0] and qs[32], their fp16 scales in s, the
+// activations block-major at act, the scale pairs at dxp[c].
+template <int NC>
+__device__ __forceinline__ void duo(const Codebook &cb, const uint4 *qs, uint32_t s, const uint4 *act,
+                                    const float2 *dxp, float2 acc[NC]) {
+    const float2 dw = __half22float2(*reinterpret_cast<const __half2 *>(&s));
+    const uint4 w0 = qs[0], w1 = qs[32];
+    int sa[NC], sb[NC];
+    block_dots<NC>(cb, w0, act, sa);
+    block_dots<NC>(cb, w1, act + NC * 2, sb);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) acc[c] = scale_acc2(acc[c], dw, dxp[c], sa[c], sb[c]);
+}
+
+// One item pass of the dense kernel for NC columns staged block-major (act,
+// dx: stride NC), one row per lane, over the 16-block stages of the item.
+// A pair item: warp w takes row set w / 4 (the pair's first or second group)
+// and quad w % 4 of each stage, so its sums (acc) are those of one group.  A
+// single-group item (single): the stage holds one group, and warp w takes
+// blocks 2w and 2w + 1 of it, so all eight warps' sums belong to that group.
+// False on a give-up.
 template <int NC>
 __device__ __forceinline__ bool dense_pass(Consumer &co, const Pipe &P, int nbp, const uint4 *act, const float *dx,
-                                           float2 acc[NC], int warp, int lane) {
+                                           float2 acc[NC], int warp, int lane, bool single) {
     const int h = warp >> 2, q = warp & 3;
     bool ok = true;
     for (int b = 0; b < nbp; b += kChunk) {
         if (b > 0) ok = ok && co.wait(P);
         const int nblk = min(kChunk, nbp - b);
-        if (ok && 4 * q < nblk) {
-            const unsigned char *half = co.st + (size_t)h * nblk * kBlockBytes;
-            const uint4 *qs = reinterpret_cast<const uint4 *>(half) + q * 128 + lane;
-            const uint2 s = reinterpret_cast<const uint2 *>(half + (size_t)nblk * 512)[q * 32 + lane];
-            const int bq = b + 4 * q;
-            quad<NC>(co.cb, qs, s, act + (size_t)bq * NC * 2, reinterpret_cast<const float2 *>(dx) + (bq >> 1) * NC,
-                     acc);
+        if (!single) {
+            if (ok && 4 * q < nblk) {
+                const unsigned char *half = co.st + (size_t)h * nblk * kBlockBytes;
+                const uint4 *qs = reinterpret_cast<const uint4 *>(half) + q * 128 + lane;
+                const uint2 s = reinterpret_cast<const uint2 *>(half + (size_t)nblk * 512)[q * 32 + lane];
+                const int bq = b + 4 * q;
+                quad<NC>(co.cb, qs, s, act + (size_t)bq * NC * 2,
+                         reinterpret_cast<const float2 *>(dx) + (bq >> 1) * NC, acc);
+            }
+        } else if (ok && 2 * warp < nblk) {
+            const uint4 *qs = reinterpret_cast<const uint4 *>(co.st) + warp * 64 + lane;
+            const uint2 s = reinterpret_cast<const uint2 *>(co.st + (size_t)nblk * 512)[(warp >> 1) * 32 + lane];
+            const int bq = b + 2 * warp;
+            duo<NC>(co.cb, qs, (warp & 1) ? s.y : s.x, act + (size_t)bq * NC * 2,
+                    reinterpret_cast<const float2 *>(dx) + (bq >> 1) * NC, acc);
         }
         co.release(P);
     }
     return ok;
+}
+
+// The work items of a dense launch: items below A.singles are pairs (item i =
+// pair i); the rest are single 32-row groups of the last pairs (item T + j =
+// group j & 1 of pair T + j / 2, T = A.singles).  A single-group item takes half
+// the time of a pair item, so the last items of a launch with more pairs than
+// CTAs end closer together, and a launch with fewer pairs than CTAs puts more
+// of them to work.
+struct DenseItem {
+    int pair, half;  // half -1: the whole pair
+};
+__device__ __forceinline__ DenseItem dense_item(int it, int singles) {
+    if (it < singles) return DenseItem{it, -1};
+    const int j = it - singles;
+    return DenseItem{singles + (j >> 1), j & 1};
 }
 
 // Dense MMVQ: pairs of 32-row groups fetched per CTA, all NC columns per
@@ -259,25 +302,30 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
     pipe_init(S.pipe);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const unsigned total = (unsigned)W.P;
+    const unsigned total = (unsigned)A.items;
     const size_t pb = pair_bytes(W.nbp);
     const int nch = (W.nbp + kChunk - 1) / kChunk;
     if (warp == kProducerWarp) {
         if (lane == 0) {
             Producer pr;
+            auto pass = [&](unsigned item) {
+                const DenseItem d = dense_item((int)item, A.singles);
+                pr.half = d.half;
+                pr.pass(S.pipe, W.w + d.pair * pb, W.nbp, 0, nch, (int)item);
+            };
             // The first item is the CTA index (the launcher sizes the grid to
             // at most the item count): its weights stream before the wait for
             // the work ahead of this kernel, which the work counter needs (a
             // call still running on the handle owns it).  The index of the
             // next item is fetched when an item starts and used once its
             // stages are issued, so the atomic's latency overlaps them.
-            if (blockIdx.x < total) pr.pass(S.pipe, W.w + blockIdx.x * pb, W.nbp, 0, nch, (int)blockIdx.x);
+            if (blockIdx.x < total) pass(blockIdx.x);
             pdl_wait();
             unsigned next = gridDim.x + atomicAdd(W.sched, 1u);
             while (next < total && !pr.stopped) {
                 const unsigned item = next;
                 next = gridDim.x + atomicAdd(W.sched, 1u);
-                pr.pass(S.pipe, W.w + item * pb, W.nbp, 0, nch, (int)item);
+                pass(item);
             }
             const bool last = done_taking(W.sched);
             pr.finish(S.pipe);
@@ -292,22 +340,39 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
             if (!rd.wait(S.pipe, tag, part)) break;
             const int it = *(volatile const int *)tag;
             if (it < 0) break;
-            float v[2][NC];
+            const DenseItem d = dense_item(it, A.singles);
+            if (d.half < 0) {
+                float v[2][NC];
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        v[r][c] = 0.0f;
+#pragma unroll
+                        for (int w = 4 * r; w < 4 * r + 4; ++w) v[r][c] += part[(w * NC + c) * 32 + lane];
+                    }
+                rd.release(S.pipe);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int64_t row = (int64_t)(2 * d.pair + r) * 32 + lane;
+                    if (row < W.M) {
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) A.y[(size_t)c * W.M + row] = v[r][c];
+                    }
+                }
+            } else {  // one group: the sums of all eight warps, in warp order
+                float v[NC];
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
-                    v[r][c] = 0.0f;
+                    v[c] = 0.0f;
 #pragma unroll
-                    for (int w = 4 * r; w < 4 * r + 4; ++w) v[r][c] += part[(w * NC + c) * 32 + lane];
+                    for (int w = 0; w < kConsumerWarps; ++w) v[c] += part[(w * NC + c) * 32 + lane];
                 }
-            rd.release(S.pipe);
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int64_t row = (int64_t)(2 * it + r) * 32 + lane;
+                rd.release(S.pipe);
+                const int64_t row = (int64_t)(2 * d.pair + d.half) * 32 + lane;
                 if (row < W.M) {
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) A.y[(size_t)c * W.M + row] = v[r][c];
+                    for (int c = 0; c < NC; ++c) A.y[(size_t)c * W.M + row] = v[c];
                 }
             }
         }
@@ -335,7 +400,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
             float2 acc[NC];
 #pragma unroll
             for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
-            const bool ok = dense_pass<NC>(co, S.pipe, W.nbp, S.act, S.dx, acc, warp, lane);
+            const bool ok = dense_pass<NC>(co, S.pipe, W.nbp, S.act, S.dx, acc, warp, lane, it >= A.singles);
             // the set is taken only now: the epilogue had the whole pass to free it
             if (!wr.acquire(S.pipe, tag, part)) break;
 #pragma unroll
@@ -511,10 +576,24 @@ static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const floa
         }
     }
     const size_t smem = dense_smem_bytes(S, W.nbp, NC);
-    int grid = 0;
-    e = dynamic_grid(k_matvec<NC, kF32>, smem, W.P, &grid);
+    // Every pair split into two single-group items when that lightens the
+    // busiest SM by at least 8% (a single-group item costs a little more per
+    // byte: its stages are half as large): the SMs take pairs in whole units,
+    // so ceil(P / SMs) pairs land on the busiest one, against ceil(2P / SMs)
+    // halves.  Measured on 4096 x 4096 at n = 1 (64 pairs: twice as many CTAs
+    // at work) 8.9 -> 7.5 us and on 32768 x 4096 at n = 5 31.5 -> 28.7 us;
+    // no split where the ratio says none (16384 x 4096 and the 129280-row
+    // head were slower split, in full or only in their last wave).
+    int cap = 0;
+    e = dynamic_grid(k_matvec<NC, kF32>, smem, INT32_MAX, &cap);
     if (e != cudaSuccess) return e;
+    const int64_t pair_load = (W.P + sms - 1) / sms, half_load = (2 * (int64_t)W.P + sms - 1) / sms;
+    const int split_pairs = half_load * 25 <= pair_load * 46 ? W.P : 0;
+    const int items = W.P + split_pairs;
+    const int grid = std::min(items, cap);
     MatvecArgs A;
+    A.singles = W.P - split_pairs;
+    A.items = items;
     A.W = W;
     A.qx = qx;
     A.dx = dx;

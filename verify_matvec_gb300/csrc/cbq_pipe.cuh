@@ -147,10 +147,14 @@ struct ActSlice {
     int cols;
 };
 
-// Producer side: a running count of issued stages.
+// Producer side: a running count of issued stages.  half >= 0 streams only
+// that group of each pair chunk (its index fields and scales, contiguous:
+// nblk * kBlockBytes bytes from h * nblk * kBlockBytes in the chunk), to the
+// start of the stage.
 struct Producer {
     uint32_t it = 0;
     bool stopped = false;
+    int half = -1;
 
     // Claim the next slot (waiting until the consumers released it).
     __device__ __forceinline__ bool claim(const Pipe &P, uint32_t &slot) {
@@ -172,10 +176,12 @@ struct Producer {
         if (!claim(P, slot)) return false;
         dst = smem_addr(P.ring) + slot * P.stage_bytes;
         bar = P.full0 + 8u * slot;
-        const uint32_t bw = (uint32_t)nblk * (2 * kBlockBytes), ba = (uint32_t)(nblk * act.cols) * 36u;
+        const uint32_t bw = (uint32_t)nblk * (half < 0 ? 2 * kBlockBytes : kBlockBytes);
+        const uint32_t ba = (uint32_t)(nblk * act.cols) * 36u;
+        const size_t src = (size_t)c * kChunkBytes + (half > 0 ? (size_t)nblk * kBlockBytes : 0u);
         P.tag[slot] = tag;
         mbar_expect_tx(bar, bw + ba);
-        bulk_g2s(dst, w + (size_t)c * kChunkBytes, bw, bar);
+        bulk_g2s(dst, w + src, bw, bar);
         ++it;
         return true;
     }
