@@ -3,13 +3,15 @@
 //
 //   k_repack          canonical 18-byte blocks -> device layout (handle creation)
 //   k_quantize        activation quantization, one warp per 32-value block
-//   k_matvec<NC,F32>  dense MMVQ over NC <= 5 columns, one pass over the weights
-//                     (F32: one fp32 column, quantized inside the kernel)
+//   k_matvec<NC,F32,S> dense MMVQ over NC <= 5 columns, one pass over the weights
+//                     (F32: one fp32 column, quantized inside the kernel; S:
+//                     single 32-row groups as work items instead of pairs)
 //   k_block_dots<NC>  the same integer path, exporting every per-block dot
 //   k_moe             routed experts (and an optional shared expert), one
 //                     kernel per layer call: gate+up rows, SwiGLU split,
 //                     requantization, then down rows per slot
 //   k_moe_combine     router-weighted combine of the per-slot down outputs
+//   k_quantize_weights fp32 weights -> canonical blocks (the weight converter)
 //   k_router_topk     top-k expert ids and softmax weights from router logits
 //
 // The matvec-type kernels are persistent: a grid of at most (SMs x resident
@@ -180,8 +182,6 @@ struct MatvecArgs {
     int64_t K;
     float *y;
     int S;             // pipeline stages
-    int singles;       // first single-group item: items below are whole pairs
-    int items;         // singles + 2 * (pairs - singles)
 };
 
 // Work counters of a persistent kernel (sched[0] items taken, sched[1] CTAs
@@ -221,37 +221,24 @@ __device__ __forceinline__ void quad(const Codebook &cb, const uint4 *qs, uint2 
     }
 }
 
-// Two consecutive blocks (a quad's first or second half) of one row for NC
-// columns: index words at qs[0] and qs[32], their fp16 scales in s, the
-// activations block-major at act, the scale pairs at dxp[c].
-template <int NC>
-__device__ __forceinline__ void duo(const Codebook &cb, const uint4 *qs, uint32_t s, const uint4 *act,
-                                    const float2 *dxp, float2 acc[NC]) {
-    const float2 dw = __half22float2(*reinterpret_cast<const __half2 *>(&s));
-    const uint4 w0 = qs[0], w1 = qs[32];
-    int sa[NC], sb[NC];
-    block_dots<NC>(cb, w0, act, sa);
-    block_dots<NC>(cb, w1, act + NC * 2, sb);
-#pragma unroll
-    for (int c = 0; c < NC; ++c) acc[c] = scale_acc2(acc[c], dw, dxp[c], sa[c], sb[c]);
-}
-
 // One item pass of the dense kernel for NC columns staged block-major (act,
-// dx: stride NC), one row per lane, over the 16-block stages of the item.
-// A pair item: warp w takes row set w / 4 (the pair's first or second group)
-// and quad w % 4 of each stage, so its sums (acc) are those of one group.  A
-// single-group item (single): the stage holds one group, and warp w takes
-// blocks 2w and 2w + 1 of it, so all eight warps' sums belong to that group.
-// False on a give-up.
-template <int NC>
+// dx: stride NC), one row per lane.  Warp w takes quad w % 4 of sub-stage
+// w / 4 of every stage, so its sums (acc) are those of one 32-row group.  A
+// pair item's stage holds the pair's two groups of one 16-block chunk
+// (sub-stage h = group h, at h * nblk * kBlockBytes).  With kSingle the item
+// is one group and a stage holds its part of two consecutive chunks
+// (sub-stage k = chunk 2s + k, at k * nblk0 * kBlockBytes, nblk0 the blocks of
+// the first), so all eight warps work on that group.  Each sub-stage holds its
+// index fields and then its scales.  False on a give-up.
+template <int NC, bool kSingle>
 __device__ __forceinline__ bool dense_pass(Consumer &co, const Pipe &P, int nbp, const uint4 *act, const float *dx,
-                                           float2 acc[NC], int warp, int lane, bool single) {
+                                           float2 acc[NC], int warp, int lane) {
     const int h = warp >> 2, q = warp & 3;
     bool ok = true;
-    for (int b = 0; b < nbp; b += kChunk) {
-        if (b > 0) ok = ok && co.wait(P);
-        const int nblk = min(kChunk, nbp - b);
-        if (!single) {
+    if constexpr (!kSingle) {
+        for (int b = 0; b < nbp; b += kChunk) {
+            if (b > 0) ok = ok && co.wait(P);
+            const int nblk = min(kChunk, nbp - b);
             if (ok && 4 * q < nblk) {
                 const unsigned char *half = co.st + (size_t)h * nblk * kBlockBytes;
                 const uint4 *qs = reinterpret_cast<const uint4 *>(half) + q * 128 + lane;
@@ -260,40 +247,37 @@ __device__ __forceinline__ bool dense_pass(Consumer &co, const Pipe &P, int nbp,
                 quad<NC>(co.cb, qs, s, act + (size_t)bq * NC * 2,
                          reinterpret_cast<const float2 *>(dx) + (bq >> 1) * NC, acc);
             }
-        } else if (ok && 2 * warp < nblk) {
-            const uint4 *qs = reinterpret_cast<const uint4 *>(co.st) + warp * 64 + lane;
-            const uint2 s = reinterpret_cast<const uint2 *>(co.st + (size_t)nblk * 512)[(warp >> 1) * 32 + lane];
-            const int bq = b + 2 * warp;
-            duo<NC>(co.cb, qs, (warp & 1) ? s.y : s.x, act + (size_t)bq * NC * 2,
-                    reinterpret_cast<const float2 *>(dx) + (bq >> 1) * NC, acc);
+            co.release(P);
         }
-        co.release(P);
+    } else {
+        for (int b = 0; b < nbp; b += 2 * kChunk) {
+            if (b > 0) ok = ok && co.wait(P);
+            const int nblk0 = min(kChunk, nbp - b);
+            const int bh = b + h * kChunk;  // first block of this warp's sub-stage
+            const int nblk = min(kChunk, nbp - bh);
+            if (ok && 4 * q < nblk) {
+                const unsigned char *sub = co.st + (size_t)h * nblk0 * kBlockBytes;
+                const uint4 *qs = reinterpret_cast<const uint4 *>(sub) + q * 128 + lane;
+                const uint2 s = reinterpret_cast<const uint2 *>(sub + (size_t)nblk * 512)[q * 32 + lane];
+                const int bq = bh + 4 * q;
+                quad<NC>(co.cb, qs, s, act + (size_t)bq * NC * 2,
+                         reinterpret_cast<const float2 *>(dx) + (bq >> 1) * NC, acc);
+            }
+            co.release(P);
+        }
     }
     return ok;
 }
 
-// The work items of a dense launch: items below A.singles are pairs (item i =
-// pair i); the rest are single 32-row groups of the last pairs (item T + j =
-// group j & 1 of pair T + j / 2, T = A.singles).  A single-group item takes half
-// the time of a pair item, so the last items of a launch with more pairs than
-// CTAs end closer together, and a launch with fewer pairs than CTAs puts more
-// of them to work.
-struct DenseItem {
-    int pair, half;  // half -1: the whole pair
-};
-__device__ __forceinline__ DenseItem dense_item(int it, int singles) {
-    if (it < singles) return DenseItem{it, -1};
-    const int j = it - singles;
-    return DenseItem{singles + (j >> 1), j & 1};
-}
-
 // Dense MMVQ: pairs of 32-row groups fetched per CTA, all NC columns per
 // pass; the epilogue warp adds the consumer warps' sums of a pair (four per
-// group) and stores its 64 rows of y.  kF32: the consumers quantize the fp32
+// group) and stores its 64 rows of y.  kSingle: the work items are single
+// 32-row groups (item i = group i & 1 of pair i / 2) and the epilogue adds
+// all eight warps' sums of the group.  kF32: the consumers quantize the fp32
 // column xf themselves while the producer starts the weight stream (no
 // quantization kernel before it); otherwise they stage qx/dx written by the
 // quantization kernel launched just before (a programmatic dependency).
-template <int NC, bool kF32>
+template <int NC, bool kF32, bool kSingle>
 __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constant__ MatvecArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_trigger();  // the next kernel may launch; it waits for this grid before touching what it writes
@@ -302,16 +286,17 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
     pipe_init(S.pipe);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const unsigned total = (unsigned)A.items;
+    const unsigned total = (unsigned)(kSingle ? 2 * W.P : W.P);
     const size_t pb = pair_bytes(W.nbp);
     const int nch = (W.nbp + kChunk - 1) / kChunk;
     if (warp == kProducerWarp) {
         if (lane == 0) {
             Producer pr;
             auto pass = [&](unsigned item) {
-                const DenseItem d = dense_item((int)item, A.singles);
-                pr.half = d.half;
-                pr.pass(S.pipe, W.w + d.pair * pb, W.nbp, 0, nch, (int)item);
+                if constexpr (kSingle)
+                    pr.pass_single(S.pipe, W.w + (item >> 1) * pb, W.nbp, nch, (int)(item & 1u), (int)item);
+                else
+                    pr.pass(S.pipe, W.w + item * pb, W.nbp, 0, nch, (int)item);
             };
             // The first item is the CTA index (the launcher sizes the grid to
             // at most the item count): its weights stream before the wait for
@@ -340,8 +325,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
             if (!rd.wait(S.pipe, tag, part)) break;
             const int it = *(volatile const int *)tag;
             if (it < 0) break;
-            const DenseItem d = dense_item(it, A.singles);
-            if (d.half < 0) {
+            if constexpr (!kSingle) {
                 float v[2][NC];
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
@@ -354,13 +338,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
                 rd.release(S.pipe);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const int64_t row = (int64_t)(2 * d.pair + r) * 32 + lane;
+                    const int64_t row = (int64_t)(2 * it + r) * 32 + lane;
                     if (row < W.M) {
 #pragma unroll
                         for (int c = 0; c < NC; ++c) A.y[(size_t)c * W.M + row] = v[r][c];
                     }
                 }
-            } else {  // one group: the sums of all eight warps, in warp order
+            } else {  // one group (item it = group it of the matrix): all eight warps' sums, in warp order
                 float v[NC];
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
@@ -369,7 +353,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
                     for (int w = 0; w < kConsumerWarps; ++w) v[c] += part[(w * NC + c) * 32 + lane];
                 }
                 rd.release(S.pipe);
-                const int64_t row = (int64_t)(2 * d.pair + d.half) * 32 + lane;
+                const int64_t row = (int64_t)it * 32 + lane;
                 if (row < W.M) {
 #pragma unroll
                     for (int c = 0; c < NC; ++c) A.y[(size_t)c * W.M + row] = v[c];
@@ -400,7 +384,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_matvec(const __grid_constan
             float2 acc[NC];
 #pragma unroll
             for (int c = 0; c < NC; ++c) acc[c] = make_float2(0.0f, 0.0f);
-            const bool ok = dense_pass<NC>(co, S.pipe, W.nbp, S.act, S.dx, acc, warp, lane, it >= A.singles);
+            const bool ok = dense_pass<NC, kSingle>(co, S.pipe, W.nbp, S.act, S.dx, acc, warp, lane);
             // the set is taken only now: the epilogue had the whole pass to free it
             if (!wr.acquire(S.pipe, tag, part)) break;
 #pragma unroll
@@ -513,8 +497,12 @@ static cudaError_t resident(Kernel kern, int threads, size_t smem, int *sms, int
 cudaError_t matvec_smem_limit(size_t *bytes) {
     size_t optin = 0, st = 0;
     cudaError_t e = device_smem_limit(&optin);
-    void (*kerns[])(const MatvecArgs) = {k_matvec<1, true>,  k_matvec<1, false>, k_matvec<2, false>,
-                                         k_matvec<3, false>, k_matvec<4, false>, k_matvec<5, false>};
+    void (*kerns[])(const MatvecArgs) = {k_matvec<1, true, false>,  k_matvec<1, false, false>,
+                                         k_matvec<2, false, false>, k_matvec<3, false, false>,
+                                         k_matvec<4, false, false>, k_matvec<5, false, false>,
+                                         k_matvec<1, true, true>,   k_matvec<1, false, true>,
+                                         k_matvec<2, false, true>,  k_matvec<3, false, true>,
+                                         k_matvec<4, false, true>,  k_matvec<5, false, true>};
     for (auto k : kerns) {
         cudaFuncAttributes fa;
         if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k);
@@ -558,42 +546,37 @@ static cudaError_t dynamic_grid(Kernel kern, size_t smem, int64_t items, int *gr
     return cudaSuccess;
 }
 
-template <int NC, bool kF32>
-static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const float *dx, const float *xf, float *y,
-                                   cudaStream_t s, bool pdl) {
-    // the deepest ring that keeps the residency of the kMinStages ring (two
-    // CTAs per SM where that fits), so the next call's weights stream sooner
-    int S = kMinStages, sms = 0, base = 0;
-    cudaError_t e = resident(k_matvec<NC, kF32>, kPipeThreads, dense_smem_bytes(S, W.nbp, NC), &sms, &base);
+// Stages of the dense kernel's ring: the deepest that keeps the residency of
+// the kMinStages ring (two CTAs per SM where that fits), so the next call's
+// weights stream sooner.
+template <typename Kernel>
+static cudaError_t dense_stages(Kernel kern, const DevMat &W, int NC, int *S_out, int *sms) {
+    int S = kMinStages, base = 0;
+    cudaError_t e = resident(kern, kPipeThreads, dense_smem_bytes(S, W.nbp, NC), sms, &base);
     if (e != cudaSuccess) return e;
     for (int t = kMaxStages; t > kMinStages; --t) {
         int per_sm = 0;
-        e = resident(k_matvec<NC, kF32>, kPipeThreads, dense_smem_bytes(t, W.nbp, NC), &sms, &per_sm);
+        e = resident(kern, kPipeThreads, dense_smem_bytes(t, W.nbp, NC), sms, &per_sm);
         if (e != cudaSuccess) return e;
         if (per_sm >= std::min(base, 2)) {
             S = t;
             break;
         }
     }
-    const size_t smem = dense_smem_bytes(S, W.nbp, NC);
-    // Every pair split into two single-group items when that lightens the
-    // busiest SM by at least 8% (a single-group item costs a little more per
-    // byte: its stages are half as large): the SMs take pairs in whole units,
-    // so ceil(P / SMs) pairs land on the busiest one, against ceil(2P / SMs)
-    // halves.  Measured on 4096 x 4096 at n = 1 (64 pairs: twice as many CTAs
-    // at work) 8.9 -> 7.5 us and on 32768 x 4096 at n = 5 31.5 -> 28.7 us;
-    // no split where the ratio says none (16384 x 4096 and the 129280-row
-    // head were slower split, in full or only in their last wave).
-    int cap = 0;
-    e = dynamic_grid(k_matvec<NC, kF32>, smem, INT32_MAX, &cap);
+    *S_out = S;
+    return cudaSuccess;
+}
+
+template <int NC, bool kF32, bool kSingle>
+static cudaError_t launch_matvec_k(const DevMat &W, const int8_t *qx, const float *dx, const float *xf, float *y,
+                                   cudaStream_t s, bool pdl) {
+    int S = 0, sms = 0, grid = 0;
+    cudaError_t e = dense_stages(k_matvec<NC, kF32, kSingle>, W, NC, &S, &sms);
     if (e != cudaSuccess) return e;
-    const int64_t pair_load = (W.P + sms - 1) / sms, half_load = (2 * (int64_t)W.P + sms - 1) / sms;
-    const int split_pairs = half_load * 25 <= pair_load * 46 ? W.P : 0;
-    const int items = W.P + split_pairs;
-    const int grid = std::min(items, cap);
+    const size_t smem = dense_smem_bytes(S, W.nbp, NC);
+    e = dynamic_grid(k_matvec<NC, kF32, kSingle>, smem, kSingle ? 2 * (int64_t)W.P : W.P, &grid);
+    if (e != cudaSuccess) return e;
     MatvecArgs A;
-    A.singles = W.P - split_pairs;
-    A.items = items;
     A.W = W;
     A.qx = qx;
     A.dx = dx;
@@ -601,7 +584,26 @@ static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const floa
     A.K = (int64_t)W.nb * kQK;
     A.y = y;
     A.S = S;
-    return launch_k(k_matvec<NC, kF32>, grid, kPipeThreads, smem, s, pdl, A);
+    return launch_k(k_matvec<NC, kF32, kSingle>, grid, kPipeThreads, smem, s, pdl, A);
+}
+
+// Work items of whole pairs, or every pair as two single-group items when
+// that lightens the busiest SM by at least 8%: the SMs take work in whole
+// items, so ceil(P / SMs) pairs land on the busiest one against ceil(2P / SMs)
+// halves.  Measured by graph replay: 4096 x 4096 at n = 1 (64 pairs) 8.7 ->
+// 6.7 us, 32768 x 4096 at n = 1 / 5 18.3 -> 16.1 / 29.8 -> 27.7 us; 16384 x
+// 4096 (ratio 1) was 3-14% slower split, the 129280-row head (ratio 0.96)
+// no faster.
+template <int NC, bool kF32>
+static cudaError_t launch_matvec_n(const DevMat &W, const int8_t *qx, const float *dx, const float *xf, float *y,
+                                   cudaStream_t s, bool pdl) {
+    int sms = 0, per_sm = 0;
+    cudaError_t e = resident(k_matvec<NC, kF32, false>, kPipeThreads, dense_smem_bytes(kMinStages, W.nbp, NC), &sms,
+                             &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t pair_load = (W.P + sms - 1) / sms, half_load = (2 * (int64_t)W.P + sms - 1) / sms;
+    if (half_load * 25 <= pair_load * 46) return launch_matvec_k<NC, kF32, true>(W, qx, dx, xf, y, s, pdl);
+    return launch_matvec_k<NC, kF32, false>(W, qx, dx, xf, y, s, pdl);
 }
 
 cudaError_t launch_matvec(const DevMat &W, const int8_t *qx, const float *dx, int n, float *y, cudaStream_t s,

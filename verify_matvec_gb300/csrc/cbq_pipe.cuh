@@ -147,14 +147,10 @@ struct ActSlice {
     int cols;
 };
 
-// Producer side: a running count of issued stages.  half >= 0 streams only
-// that group of each pair chunk (its index fields and scales, contiguous:
-// nblk * kBlockBytes bytes from h * nblk * kBlockBytes in the chunk), to the
-// start of the stage.
+// Producer side: a running count of issued stages.
 struct Producer {
     uint32_t it = 0;
     bool stopped = false;
-    int half = -1;
 
     // Claim the next slot (waiting until the consumers released it).
     __device__ __forceinline__ bool claim(const Pipe &P, uint32_t &slot) {
@@ -176,12 +172,10 @@ struct Producer {
         if (!claim(P, slot)) return false;
         dst = smem_addr(P.ring) + slot * P.stage_bytes;
         bar = P.full0 + 8u * slot;
-        const uint32_t bw = (uint32_t)nblk * (half < 0 ? 2 * kBlockBytes : kBlockBytes);
-        const uint32_t ba = (uint32_t)(nblk * act.cols) * 36u;
-        const size_t src = (size_t)c * kChunkBytes + (half > 0 ? (size_t)nblk * kBlockBytes : 0u);
+        const uint32_t bw = (uint32_t)nblk * (2 * kBlockBytes), ba = (uint32_t)(nblk * act.cols) * 36u;
         P.tag[slot] = tag;
         mbar_expect_tx(bar, bw + ba);
-        bulk_g2s(dst, w + src, bw, bar);
+        bulk_g2s(dst, w + (size_t)c * kChunkBytes, bw, bar);
         ++it;
         return true;
     }
@@ -255,6 +249,26 @@ struct Producer {
     __device__ __forceinline__ void pass(const Pipe &P, const uint8_t *w, int nbp, int c0, int c1, int tag) {
         NoDep nd;
         pass(P, w, nbp, c0, c1, tag, ActSlice{nullptr, 0}, nd);
+    }
+
+    // A pass over one group (half h) of a pair (its bytes at w, nch chunks):
+    // each stage holds that group's part of two consecutive chunks (its index
+    // fields and scales, nblk * kBlockBytes contiguous bytes from h * nblk *
+    // kBlockBytes in each chunk), one after the other, so a stage carries as
+    // many blocks of work as a stage of a whole pair.
+    __device__ __forceinline__ void pass_single(const Pipe &P, const uint8_t *w, int nbp, int nch, int h, int tag) {
+        for (int c = 0; c < nch && !stopped; c += 2) {
+            uint32_t slot;
+            if (!claim(P, slot)) break;
+            const uint32_t dst = smem_addr(P.ring) + slot * P.stage_bytes, bar = P.full0 + 8u * slot;
+            const int n0 = chunk_blocks(nbp, c), n1 = c + 1 < nch ? chunk_blocks(nbp, c + 1) : 0;
+            const uint32_t b0 = (uint32_t)n0 * kBlockBytes, b1 = (uint32_t)n1 * kBlockBytes;
+            P.tag[slot] = tag;
+            mbar_expect_tx(bar, b0 + b1);
+            bulk_g2s(dst, w + (size_t)c * kChunkBytes + (size_t)h * b0, b0, bar);
+            if (n1) bulk_g2s(dst + b0, w + (size_t)(c + 1) * kChunkBytes + (size_t)h * b1, b1, bar);
+            ++it;
+        }
     }
 
     // Give-up test mode only: claim a slot and tag it, but never fill it (the
