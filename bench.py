@@ -53,10 +53,10 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure
 # one ncu capture of each kernel (summaries in profiles/), valid only for the
 # kernel sources they were taken on (digest below); otherwise reported as null.
 PROFILED = {
-    "source_digest": "d7cc04691493f254",
-    "k_matvec<5> (head)": 297_937_920 + 5_145_856,          # one launch, 129280 x 4096, n=5
+    "source_digest": "168f2b2edcd757e1",
+    "k_matvec<5> (head)": 297_930_496 + 5_312_256,          # one launch, 129280 x 4096, n=5
     # one layer call (k_quantize_chunked + k_moe + k_moe_combine) with 28 distinct experts
-    "moe call per expert": (90_880 + 396_650_496 + 3_427_584 + 673_536) / 28,
+    "moe call per expert": (89_600 + 396_644_096 + 3_252_736 + 673_536) / 28,
 }
 
 
