@@ -119,6 +119,18 @@ def test_matvec_16384_all_rows(torch, n):
     _check_matvec(torch, W, M, K, synth.activations(n, K, stream=synth.S_X + 50, outliers=True))
 
 
+@pytest.mark.parametrize("n", [1, 5])
+def test_matvec_single_group_items_all_rows(torch, n):
+    """32,800 x 2080: 513 pairs of row groups, more than the resident CTAs, so
+    the launcher takes single-group work items (1,026 of them, several per
+    CTA), with a ragged last pair (one real group) and an odd chunk count
+    (65 blocks, padded to 68: the last stage holds one chunk of four blocks,
+    three of them padding).  Every row against the oracle."""
+    M, K = 32800, 2080
+    W = synth.weight_blocks(M, K, stream=synth.S_W + 60)
+    _check_matvec(torch, W, M, K, synth.activations(n, K, stream=synth.S_X + 60, outliers=True))
+
+
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("K", [1024, 1056])
 def test_matvec_q_equals_matvec_and_host_entry(torch, n, K):
