@@ -180,6 +180,41 @@ def oracle_sample(sets, n_steps, threads=1):
     return step_bytes, times, sample
 
 
+def oracle_next_rows():
+    """The single-threaded CPU oracle timed beside the next rows of the path,
+    each on a bounded sample (a second or two of CPU work): the weight
+    converter on 256 x 4096 fp32 weights (bytes in + out per second), the
+    quantized matmat at n = 16 on 512 rows of a 4096-wide matrix (weight bytes
+    per second), and the sinkhorn normalisation of 2^14 4x4 matrices at 20
+    rounds (matrices per second)."""
+    from oracle import oracle as O
+    out = {}
+    Mw, Kw = 256, 4096
+    w = (np.random.default_rng(5).standard_normal((Mw, Kw)) * 0.02).astype(np.float32)
+    t0 = time.perf_counter()
+    O.quantize_weights(w, Mw, Kw)
+    dt = time.perf_counter() - t0
+    nbytes = Mw * Kw * 4 + Mw * (Kw // QK) * BB
+    out["weight_converter"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                               "sample": f"{Mw} x {Kw} fp32 weights"}
+    Mm, n = 512, 16
+    Wm = synth.weight_blocks(Mm, Kw, stream=synth.S_W * 1000 + 3)
+    qx, dx = O.quantize_act(synth.activations(n, Kw, stream=synth.S_X))
+    t0 = time.perf_counter()
+    O.matvec_q(Wm, Mm, Kw, qx, dx)
+    dt = time.perf_counter() - t0
+    out["tensor_core_path"] = {"value": Mm * (Kw // QK) * BB / dt / 1e9, "unit": "GB/s", "cores": 1,
+                               "kind": "oracle", "sample": f"{Mm} rows x {Kw} at n={n}"}
+    nh = 1 << 14
+    c = synth.hc_logits(nh, stream=synth.S_HC * 1000 + 7)
+    t0 = time.perf_counter()
+    O.hc_sinkhorn(c, 20)
+    dt = time.perf_counter() - t0
+    out["hc_sinkhorn"] = {"value": nh / dt, "unit": "matrices/s", "cores": 1, "kind": "oracle",
+                          "sample": f"{nh} 4x4 matrices, 20 rounds"}
+    return out
+
+
 REFERENCE_BUDGET_S = 120.0  # whole --impl reference run (warm-up + timed steps), about
 
 
@@ -730,6 +765,10 @@ def run_gpu(args):
 
     cpu = cpu_mt = None
     if rank == 0 and world == 1:
+        nxt = oracle_next_rows()
+        converter["cpu_oracle"] = nxt["weight_converter"]
+        mmq["cpu_oracle"] = nxt["tensor_core_path"]
+        hc["cpu_oracle"] = nxt["hc_sinkhorn"]
         n_cpu = 1
         _, t1s = oracle_sample(sets, 1)[0:2]
         n_cpu = max(1, min(20, int(10.0 / max(t1s[0], 1e-3))))
