@@ -70,8 +70,11 @@ def test_matmat_vs_oracle(torch, M, K, n):
     _check(torch, W, M, K, x)
 
 
-def test_matmat_16384_all_rows_and_repeatable(torch):
-    M, K, n = 16384, 4096, 16
+@pytest.mark.parametrize("n", [8, 16])
+def test_matmat_16384_all_rows_and_repeatable(torch, n):
+    """Every row of a 16384 x 4096 call at n = 8 (the N = 8 MMAs) and 16,
+    and the same bits on a second call."""
+    M, K = 16384, 4096
     W = synth.weight_blocks(M, K, stream=730)
     x = synth.activations(n, K, stream=731)
     Wh, y = _check(torch, W, M, K, x)

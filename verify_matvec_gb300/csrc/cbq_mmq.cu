@@ -28,6 +28,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include <cuda_fp16.h>
 
@@ -60,7 +61,8 @@ __device__ __forceinline__ uint64_t mmq_desc(uint32_t saddr, uint32_t lbo, uint3
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), fp16
 // A and B (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at
 // bit 17, M >> 4 at bit 24.
-constexpr uint32_t kMmqIdesc = (1u << 4) | ((uint32_t)(kMmqN >> 3) << 17) | ((uint32_t)(kMmqM >> 4) << 24);
+template <int N>
+constexpr uint32_t mmq_idesc() { return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kMmqM >> 4) << 24); }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_saddr, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_saddr), "r"(ncols)
@@ -75,11 +77,12 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+template <int N>
 __device__ __forceinline__ void mmq_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, int accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kMmqIdesc), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(mmq_idesc<N>()), "r"(accumulate)
         : "memory");
 }
 
@@ -99,21 +102,20 @@ __device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16
         : "r"(taddr)
         : "memory");
 }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// 16 consecutive fp32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+// 8 consecutive fp32 columns of this thread's tensor-memory lane, as raw
+// words; complete once tmem_wait_ld() returns.
+__device__ __forceinline__ void tmem_ld8_issue(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
 }
+template <int N>
+__device__ __forceinline__ void tmem_ld_issue(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 16) tmem_ld16_issue(taddr, r);
+    else tmem_ld8_issue(taddr, r);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // -------------------------------------------------------- activations ---
 
@@ -198,15 +200,20 @@ constexpr int kM2MetaOff = kM2BOff + kChunk * kMmqBTile; // their metadata
 constexpr int kM2StageBytes = kM2MetaOff + kChunk * kMmqMetaFloats * 4;  // 55,296
 constexpr int kM2EpWarps = 8, kM2ExWarps = 4;  // multiples of 4 (one warp per tensor-memory lane quadrant)
 constexpr int kM2EpGroups = kM2EpWarps / 4;     // epilogue groups: group g reads the units u with u % groups == g
-constexpr int kM2ExGroups = kM2ExWarps / 4;     // expander groups: group g expands blocks i == g (mod groups) of a unit
+constexpr int kM2ExGroups = kM2ExWarps / 4;     // expander groups (one: a thread per row takes every block)
 constexpr int kM2EpBatch = 2;  // blocks whose sums the epilogue loads before one wait
 constexpr int kM2ProducerWarp = kM2EpWarps + kM2ExWarps, kM2MmaWarp = kM2ProducerWarp + 1;
 constexpr int kM2Threads = (kM2MmaWarp + 1) * 32;      // 448
 constexpr int kM2StageArrivals = kM2ExWarps * 32 + kM2EpWarps * 32 + 1;
-constexpr uint32_t kM2TmemCols = kM2DUnits * kM2Unit * kMmqN;  // 256
+template <int N>
+constexpr uint32_t m2_tmem_cols() { return kM2DUnits * kM2Unit * N; }  // 256 at N = 16, 128 at N = 8
 constexpr size_t kM2AUnitBytes = (size_t)kM2Unit * kMmqATile;  // 32 KB
-constexpr size_t kM2PartBytes = (size_t)(kM2EpGroups - 1) * kMmqM * kMmqN * 4;  // partial sums of groups 1..
-constexpr size_t kM2Smem = (size_t)kM2Stages * kM2StageBytes + (size_t)kM2AUnits * kM2AUnitBytes + kM2PartBytes;
+template <int N>
+constexpr size_t m2_part_bytes() { return (size_t)(kM2EpGroups - 1) * kMmqM * N * 4; }  // partial sums of groups 1..
+template <int N>
+constexpr size_t m2_smem() {
+    return (size_t)kM2Stages * kM2StageBytes + (size_t)kM2AUnits * kM2AUnitBytes + m2_part_bytes<N>();
+}
 
 struct M2Shared {
     uint64_t sfull[kM2Stages], sempty[kM2Stages];
@@ -232,6 +239,7 @@ __device__ __forceinline__ bool m2_wait(M2Shared &S, uint64_t &bar, uint32_t par
     return false;
 }
 
+template <int N>
 __global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ MmqArgs A) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ M2Shared S;
@@ -240,7 +248,7 @@ __global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ M
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const DevMat &W = A.W;
     unsigned *err = W.err;
-    if (warp == 0) tmem_alloc(smem_addr(&S.tmem_slot), kM2TmemCols);
+    if (warp == 0) tmem_alloc(smem_addr(&S.tmem_slot), m2_tmem_cols<N>());
     if (tid == 32) {
         for (int i = 0; i < kM2Stages; ++i) {
             mbar_init(smem_addr(&S.sfull[i]), 1);
@@ -329,11 +337,11 @@ __global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ M
                         tc_fence_after();
                         const int nu = min(kM2Unit, nv - j0);
                         for (int i = 0; i < nu; ++i) {
-                            const uint32_t d = tmem + (ds * kM2Unit + (uint32_t)i) * kMmqN;
+                            const uint32_t d = tmem + (ds * kM2Unit + (uint32_t)i) * N;
                             const uint32_t at = smem_addr(aunits) + (uint32_t)(as * kM2AUnitBytes) + (uint32_t)i * kMmqATile;
                             const uint32_t bt = bt0 + (uint32_t)(j0 + i) * kMmqBTile;
-                            mmq_mma(d, mmq_desc(at, 128, 512), mmq_desc(bt, 128, 512), 0);
-                            mmq_mma(d, mmq_desc(at + 256, 128, 512), mmq_desc(bt + 256, 128, 512), 1);
+                            mmq_mma<N>(d, mmq_desc(at, 128, 512), mmq_desc(bt, 128, 512), 0);
+                            mmq_mma<N>(d, mmq_desc(at + 256, 128, 512), mmq_desc(bt + 256, 128, 512), 1);
                         }
                         mmq_commit(smem_addr(&S.aempty[as]));
                         mmq_commit(smem_addr(&S.dfull[ds]));
@@ -347,8 +355,8 @@ __global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ M
             while (!mbar_try_wait(smem_addr(&S.done), 0u) && global_ns() - t0 < kWaitLimitNs) {}
         }
     } else if (warp >= kM2EpWarps) {
-        // expanders: thread (row, group) -- blocks i == group (mod groups) of a unit
-        const int e = tid - kM2EpWarps * 32, row = e & (kMmqM - 1), par = e >> 7;
+        // expanders: thread = row, every block of a unit
+        const int e = tid - kM2EpWarps * 32, row = e & (kMmqM - 1);
         const int pl = row >> 6, h = (row >> 5) & 1, rl = row & 31;
         const Codebook cb{S.cbw[0], S.cbw[1], S.cbw[2], S.cbw[3], 0u, 0u, 0};
         uint32_t k = 0, u = 0;
@@ -371,10 +379,18 @@ __global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ M
                         break;
                     }
                     const int nu = min(kM2Unit, nv - j0);
-                    for (int i = par; i < nu; i += kM2ExGroups) {
-                        const int j = j0 + i;
-                        const uint4 q = live ? *reinterpret_cast<const uint4 *>(wst + ((size_t)j * 32 + rl) * 16)
-                                             : make_uint4(0u, 0u, 0u, 0u);
+                    // the unit's index words are loaded together, ahead of their
+                    // expansion (one expander group: this thread takes every block)
+                    static_assert(kM2ExGroups == 1, "one expander group");
+                    uint4 qq[kM2Unit];
+#pragma unroll
+                    for (int i = 0; i < kM2Unit; ++i)
+                        qq[i] = live && i < nu ? *reinterpret_cast<const uint4 *>(wst + ((size_t)(j0 + i) * 32 + rl) * 16)
+                                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int i = 0; i < kM2Unit; ++i) {
+                        if (i >= nu) break;
+                        const uint4 q = qq[i];
                         const uint32_t ws[4] = {q.x, q.y, q.z, q.w};
                         uint32_t lo[4][2], hi[4][2];
 #pragma unroll
@@ -408,9 +424,9 @@ __global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ M
             const int pair = 2 * t + pl;
             const bool live = pair < W.P;
             const int64_t grow = (int64_t)pair * 64 + h * 32 + rl;
-            float acc[kMmqN];
+            float acc[N];
 #pragma unroll
-            for (int c = 0; c < kMmqN; ++c) acc[c] = 0.0f;
+            for (int c = 0; c < N; ++c) acc[c] = 0.0f;
             for (int c = 0; c < nch && ok; ++c, ++k) {
                 const uint32_t slot = k % kM2Stages;
                 if (!m2_wait(S, S.sfull[slot], (k / kM2Stages) & 1u, err)) {
@@ -433,11 +449,11 @@ __global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ M
                     const int nu = min(kM2Unit, nv - j0);
                     const uint2 sq = live ? scp[(j0 >> 2) * 32] : make_uint2(0u, 0u);  // the unit's four scales
                     for (int i0 = 0; i0 < nu; i0 += kM2EpBatch) {
-                        uint32_t d[kM2EpBatch][kMmqN];
+                        uint32_t d[kM2EpBatch][N];
 #pragma unroll
                         for (int i = 0; i < kM2EpBatch; ++i)
                             if (i0 + i < nu)
-                                tmem_ld16_issue(tmem + lane_base + (ds * kM2Unit + (uint32_t)(i0 + i)) * kMmqN, d[i]);
+                                tmem_ld_issue<N>(tmem + lane_base + (ds * kM2Unit + (uint32_t)(i0 + i)) * N, d[i]);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < kM2EpBatch; ++i) {
@@ -446,16 +462,17 @@ __global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ M
                             const uint32_t sw = (jj & 2) ? sq.y : sq.x;
                             const float dw = (jj & 1) ? half_hi(sw) : half_lo(sw);
                             const float *md = mt + j * kMmqMetaFloats;
+                            // every one of the N columns: a padded column has a zero sum, correction
+                            // and scale, so its running sum stays zero (no per-column test)
 #pragma unroll
-                            for (int cc = 0; cc < kMmqN; ++cc) {
-                                if (cc >= n) break;
+                            for (int cc = 0; cc < N; ++cc) {
                                 const float sdot = __fsub_rn(__uint_as_float(d[i][cc]), md[kMmqN + cc]);
                                 acc[cc] = __fmaf_rn(__fmul_rn(dw, md[cc]), sdot, acc[cc]);
                             }
                             if (A.dbg && live && grow < W.M) {
                                 const int b = c * kChunk + j;
 #pragma unroll
-                                for (int cc = 0; cc < kMmqN; ++cc)
+                                for (int cc = 0; cc < N; ++cc)
                                     if (cc < n)
                                         A.dbg[((size_t)cc * W.M + grow) * nb + b] =
                                             (int32_t)__fsub_rn(__uint_as_float(d[i][cc]), md[kMmqN + cc]);
@@ -472,26 +489,26 @@ __global__ void __launch_bounds__(kM2Threads, 1) k_mmq(const __grid_constant__ M
                 // to group 0 through shared memory (epilogue threads only)
                 if (eg > 0) {
 #pragma unroll
-                    for (int cc = 0; cc < kMmqN; ++cc) part[((eg - 1) * kMmqN + cc) * kMmqM + row] = acc[cc];
+                    for (int cc = 0; cc < N; ++cc) part[((eg - 1) * N + cc) * kMmqM + row] = acc[cc];
                 }
                 asm volatile("bar.sync 2, %0;" ::"n"(kM2EpWarps * 32) : "memory");
                 if (eg == 0) {
                     for (int g2 = 1; g2 < kM2EpGroups; ++g2)
 #pragma unroll
-                        for (int cc = 0; cc < kMmqN; ++cc) acc[cc] += part[((g2 - 1) * kMmqN + cc) * kMmqM + row];
+                        for (int cc = 0; cc < N; ++cc) acc[cc] += part[((g2 - 1) * N + cc) * kMmqM + row];
                 }
                 asm volatile("bar.sync 2, %0;" ::"n"(kM2EpWarps * 32) : "memory");
             }
             if (eg == 0 && ok && A.y && live && grow < W.M) {
 #pragma unroll
-                for (int cc = 0; cc < kMmqN; ++cc)
+                for (int cc = 0; cc < N; ++cc)
                     if (cc < n) A.y[(size_t)cc * W.M + grow] = acc[cc];
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kM2TmemCols);
+    if (warp == 0) tmem_dealloc(tmem, m2_tmem_cols<N>());
 }
 
 size_t mmq_bimg_bytes(int nb) { return (size_t)nb * kMmqBTile; }
@@ -513,16 +530,28 @@ cudaError_t launch_mmq_prep(const int8_t *qx, const float *dx, int n, int64_t K,
     return cudaLaunchKernelEx(&cfg, k_mmq_prep, qx, dx, n, K, nb, bimg, meta);
 }
 
-cudaError_t launch_mmq(const DevMat &W, const uint8_t *bimg, const float *meta, int n, float *y, int32_t *dbg,
-                       int stall, cudaStream_t s) {
-    static bool raised = false;  // the dynamic shared memory above the default 48 KB
-    if (!raised) {
-        cudaError_t e = cudaFuncSetAttribute(k_mmq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kM2Smem);
+// Raise the kernel's dynamic shared memory limit above the default 48 KB,
+// once per device (a function attribute belongs to the device's context).
+template <int N>
+static cudaError_t mmq_raise_smem(int dev) {
+    static std::mutex mu;
+    static bool raised[64] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!raised[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(k_mmq<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m2_smem<N>());
         if (e != cudaSuccess) return e;
-        raised = true;
+        raised[dev] = true;
     }
+    return cudaSuccess;
+}
+
+template <int N>
+static cudaError_t launch_mmq_n(const DevMat &W, const uint8_t *bimg, const float *meta, int n, float *y,
+                                int32_t *dbg, int stall, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = mmq_raise_smem<N>(dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int T = (int)((W.P + 1) / 2);
@@ -534,11 +563,19 @@ cudaError_t launch_mmq(const DevMat &W, const uint8_t *bimg, const float *meta, 
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kM2Threads);
-    cfg.dynamicSmemBytes = kM2Smem;
+    cfg.dynamicSmemBytes = m2_smem<N>();
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_mmq, A);
+    return cudaLaunchKernelEx(&cfg, k_mmq<N>, A);
+}
+
+// Up to eight columns: MMAs of N = 8 (half the tensor memory, half the
+// read-out and scaling per block); otherwise N = 16.
+cudaError_t launch_mmq(const DevMat &W, const uint8_t *bimg, const float *meta, int n, float *y, int32_t *dbg,
+                       int stall, cudaStream_t s) {
+    if (n <= 8) return launch_mmq_n<8>(W, bimg, meta, n, y, dbg, stall, s);
+    return launch_mmq_n<16>(W, bimg, meta, n, y, dbg, stall, s);
 }
 
 }  // namespace cbq
