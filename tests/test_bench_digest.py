@@ -44,3 +44,14 @@ def test_string_literals_are_code(tmp_path):
     one = bench.source_digest(str(d))
     (d / "extra.h").write_text('const char *a = "x // z";\n')
     assert bench.source_digest(str(d)) != one
+
+
+def test_other_translation_units_do_not_change_it(tmp_path):
+    """The digest follows the profiled kernels' translation unit and the
+    headers only: a code change in another translation unit keeps it."""
+    d = _copy(tmp_path)
+    base = bench.source_digest(str(d))
+    _edit(d, "cbq_mmq.cu", "constexpr int kM2Stages = 2;", "constexpr int kM2Stages = 3;")
+    assert bench.source_digest(str(d)) == base
+    _edit(d, "cbq_pipe.cuh", "struct Producer {", "struct Producer { int unused_ = 0;")
+    assert bench.source_digest(str(d)) != base
